@@ -1,0 +1,396 @@
+"""Pins for the fp64 CPU oracle, independent of the oracle's own code.
+
+Each test checks the oracle against something other than itself: hand-computed
+K=V=2 steps (tests/golden/hand_cases.json), an algebraically different closed
+form of the recurrence, a library routine (numpy matmul, torch softplus /
+sigmoid / normalize), or an invariant that the pages state (slot placement does
+not change a sequence's result, untouched slots stay bit-identical, negative
+write slots skip the writeback, strided pools are written in place).
+
+Recurrence (ROCm/aiter PR #4584, advisory review): per token
+    S <- exp(g_t) S;  S <- S + beta_t k_t (x) (v_t - S^T k_t);  o_t = S^T q_t.
+Pool semantics: flashinfer "fp32 sibling of #3268" (read/write slots, -1 skip,
+in-place strided 4D pool, intermediate-state cache) and cuLA PR #75 (LA state at
+row h0_indices[n] * H + h).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_cases.json")
+
+
+def _t(x, dtype=torch.float64):
+    return torch.tensor(x, dtype=dtype)
+
+
+# --------------------------------------------------------------------------- hand cases
+
+def _run_hand_case(case):
+    form = case["form"]
+    S0 = np.array(case["S0"], dtype=np.float64)          # K x V
+    K, V = S0.shape
+    toks = case["tokens"]
+    T = len(toks)
+    pool = torch.zeros(3, 1, V, K, dtype=torch.float32)
+    pool[1, 0] = torch.from_numpy(S0.T.copy()).float()   # storage is S^T
+    pool[2] = 7.0                                        # a slot nobody touches
+    before = pool.clone()
+    q = _t([[t["q"]] for t in toks])[None]               # [1,T,1,K]
+    k = _t([[t["k"]] for t in toks])[None]
+    v = _t([[t["v"]] for t in toks])[None]
+    ri, wi = torch.tensor([1]), torch.tensor([0])
+    if form == "la":
+        lam = _t([toks[0]["decay"]])
+        res = oracle.la_decode(q, k, v, lam, pool.view(3, V, K), ri, wi,
+                               cache_intermediate=True)
+    else:
+        raw = case.get("raw")
+        if raw:
+            g = _t([[t["g_raw"]] for t in toks])[None]
+            beta = _t([[t["beta_raw"]] for t in toks])[None]
+            A_log = _t([raw["A_log"]])
+            dtb = raw["dt_bias"]
+            dt_bias = _t(dtb if isinstance(dtb, list) else [dtb])
+            kw = dict(A_log=A_log, dt_bias=dt_bias, gate_raw=True, beta_raw=True)
+        else:
+            g = torch.log(_t([[t["decay"]] for t in toks]))[None]
+            beta = _t([[t["beta"]] for t in toks])[None]
+            kw = {}
+        fn = oracle.kda_decode if form == "kda" else oracle.gdn_decode
+        res = fn(q, k, v, g, beta, pool, ri, wi, cache_intermediate=True, **kw)
+    return res, pool, before, toks
+
+
+@pytest.mark.parametrize("name", [c["name"] for c in json.load(open(GOLDEN))["cases"]])
+def test_hand_cases(name):
+    case = next(c for c in json.load(open(GOLDEN))["cases"] if c["name"] == name)
+    # exact where only +,*,- on dyadic values occur; exp(log(d)) may cost 1-2 ulp
+    tol = case.get("tol", 0.0 if case["form"] == "la" else 1e-15)
+    res, pool, before, toks = _run_hand_case(case)
+    for t, tok in enumerate(toks):
+        np.testing.assert_allclose(res["out"][0, t, 0], tok["o"], rtol=0, atol=tol)
+        np.testing.assert_allclose(res["inter"][0, t, 0], np.array(tok["S"]).T, rtol=0, atol=tol)
+    S_T = np.array(toks[-1]["S"]).T
+    np.testing.assert_allclose(res["final_state"][0, 0], S_T, rtol=0, atol=tol)
+    np.testing.assert_allclose(pool[0, 0].double().numpy(), S_T, rtol=0, atol=max(tol, 1e-7))
+    assert torch.equal(pool[1:], before[1:])             # read slot and bystander untouched
+    assert res["n_bad"] == 0
+
+
+# --------------------------------------------------------------------------- closed forms
+
+def _rand_delta_case(per_channel, B=3, T=3, H=2, HV=4, K=8, V=6, P=7, seed=0):
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, T, H, K, generator=gen, dtype=torch.float64)
+    k = F.normalize(torch.randn(B, T, H, K, generator=gen, dtype=torch.float64), dim=-1)
+    v = torch.randn(B, T, HV, V, generator=gen, dtype=torch.float64)
+    gshape = (B, T, HV, K) if per_channel else (B, T, HV)
+    g = -torch.rand(gshape, generator=gen, dtype=torch.float64)
+    beta = torch.rand(B, T, HV, generator=gen, dtype=torch.float64)
+    pool = torch.randn(P, HV, V, K, generator=gen) * 0.5
+    ri = torch.tensor([4, -1, 2][:B])
+    wi = torch.tensor([4, 6, -1][:B])
+    return q, k, v, g, beta, pool, ri, wi
+
+
+@pytest.mark.parametrize("per_channel", [False, True])
+def test_delta_rule_matches_householder_product_form(per_channel):
+    """Each token is S <- (I - beta k k^T) D S + beta k v^T, D = diag(exp(g)):
+    the same update written as one matrix product (K x V orientation)."""
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(per_channel)
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    pool0 = pool.clone()
+    fn = oracle.kda_decode if per_channel else oracle.gdn_decode
+    res = fn(q, k, v, g, beta, pool, ri, wi, cache_intermediate=True, scale=0.75)
+    for b in range(B):
+        for hv in range(HV):
+            h = hv // (HV // H)
+            r = int(ri[b])
+            S = pool0[r, hv].double().numpy().T.copy() if r >= 0 else np.zeros((K, V))
+            for t in range(T):
+                d = g[b, t, hv].numpy() if per_channel else np.full(K, float(g[b, t, hv]))
+                kk = k[b, t, h].numpy()
+                bt = float(beta[b, t, hv])
+                S = (np.eye(K) - bt * np.outer(kk, kk)) @ np.diag(np.exp(d)) @ S \
+                    + bt * np.outer(kk, v[b, t, hv].numpy())
+                np.testing.assert_allclose(res["out"][b, t, hv], 0.75 * S.T @ q[b, t, h].numpy(),
+                                           rtol=0, atol=1e-12)
+                np.testing.assert_allclose(res["inter"][b, t, hv], S.T, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(res["final_state"][b, hv], S.T, rtol=0, atol=1e-12)
+    # writeback: slot 4 (b=0, in place) and 6 (b=1) written; b=2 skipped (-1)
+    for b, w in ((0, 4), (1, 6)):
+        np.testing.assert_allclose(pool[w].double().numpy(), res["final_state"][b],
+                                   rtol=1e-7, atol=1e-7)
+    untouched = [p for p in range(pool.shape[0]) if p not in (4, 6)]
+    assert torch.equal(pool[untouched], pool0[untouched])
+
+
+def test_la_matches_unrolled_closed_form():
+    """S_t = lambda^(t+1) S_0 + sum_{s<=t} lambda^(t-s) k_s v_s^T, o_t = S_t^T q_t."""
+    gen = torch.Generator().manual_seed(1)
+    B, T, H, K, V, P = 2, 4, 3, 8, 5, 5
+    q = torch.randn(B, T, H, K, generator=gen, dtype=torch.float64)
+    k = torch.randn(B, T, H, K, generator=gen, dtype=torch.float64)
+    v = torch.randn(B, T, H, V, generator=gen, dtype=torch.float64)
+    lam = torch.tensor([0.5, 0.9, 1.0], dtype=torch.float64)
+    pool = torch.randn(P * H, V, K, generator=gen)
+    pool0 = pool.clone()
+    ri = torch.tensor([3, 1])
+    res = oracle.la_decode(q, k, v, lam, pool, ri, cache_intermediate=True)
+    for b in range(B):
+        for h in range(H):
+            S0 = pool0[int(ri[b]) * H + h].double().numpy().T
+            L = float(lam[h])
+            for t in range(T):
+                St = L ** (t + 1) * S0 + sum(
+                    L ** (t - s) * np.outer(k[b, s, h].numpy(), v[b, s, h].numpy())
+                    for s in range(t + 1))
+                np.testing.assert_allclose(res["inter"][b, t, h], St.T, rtol=0, atol=1e-12)
+                np.testing.assert_allclose(res["out"][b, t, h], St.T @ q[b, t, h].numpy(),
+                                           rtol=0, atol=1e-12)
+    # rows r*H + h of the flat pool were rewritten in place, nothing else
+    written = [int(r) * H + h for r in ri for h in range(H)]
+    other = [i for i in range(P * H) if i not in written]
+    assert torch.equal(pool[other], pool0[other])
+    for b in range(B):
+        for h in range(H):
+            np.testing.assert_allclose(pool[int(ri[b]) * H + h].double().numpy(),
+                                       res["final_state"][b, h], rtol=1e-7, atol=1e-7)
+
+
+def test_delta_rule_projection_property():
+    """With beta = 1 and a unit key, the updated state maps k exactly to v."""
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(False, B=2, T=1)
+    beta = torch.ones_like(beta)
+    res = oracle.gdn_decode(q, k, v, g, beta, pool, ri, wi)
+    HV, H = v.shape[2], q.shape[2]
+    for b in range(2):
+        for hv in range(HV):
+            S = res["final_state"][b, hv].T                     # K x V
+            np.testing.assert_allclose(S.T @ k[b, 0, hv // (HV // H)].numpy(),
+                                       v[b, 0, hv].numpy(), rtol=0, atol=1e-12)
+
+
+def test_no_gate_no_beta_is_plain_readout():
+    """g = 0, beta = 0: the state is bit-unchanged and o = S0^T q (numpy matmul)."""
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(False, B=1, T=1)
+    g.zero_()
+    beta.zero_()
+    pool0 = pool.clone()
+    res = oracle.gdn_decode(q, k, v, g, beta, pool, ri, wi)
+    for hv in range(v.shape[2]):
+        S0 = pool0[4, hv].double().numpy()                     # [V,K]
+        assert np.array_equal(res["final_state"][0, hv], S0)
+        np.testing.assert_allclose(res["out"][0, 0, hv], S0 @ q[0, 0, hv // 2].numpy(),
+                                   rtol=0, atol=1e-12)
+    assert torch.equal(pool, pool0)                            # rewrote the same bits
+
+
+def test_zero_initial_state_for_negative_read():
+    """read -1: S0 = 0, so S = beta k v^T and o = beta (k.q) v."""
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(False, B=2, T=1)
+    res = oracle.gdn_decode(q, k, v, g, beta, pool, ri, wi)
+    b = 1                                                      # ri[1] == -1
+    for hv in range(v.shape[2]):
+        h = hv // 2
+        kq = float(k[b, 0, h] @ q[b, 0, h])
+        np.testing.assert_allclose(res["out"][b, 0, hv], float(beta[b, 0, hv]) * kq * v[b, 0, hv].numpy(),
+                                   rtol=0, atol=1e-12)
+
+
+def test_kda_with_uniform_gate_equals_gdn():
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(False)
+    pool_a, pool_b = pool.clone(), pool.clone()
+    a = oracle.gdn_decode(q, k, v, g, beta, pool_a, ri, wi, cache_intermediate=True)
+    gk = g[..., None].expand(*g.shape, q.shape[-1]).contiguous()
+    b = oracle.kda_decode(q, k, v, gk, beta, pool_b, ri, wi, cache_intermediate=True)
+    for key in ("out", "final_state", "inter"):
+        assert np.array_equal(a[key], b[key])
+    assert torch.equal(pool_a, pool_b)
+
+
+@pytest.mark.parametrize("per_channel", [False, True])
+def test_gate_chain_matches_torch(per_channel):
+    """In-kernel gate: g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b),
+    against torch's softplus (threshold 20) and sigmoid in fp64."""
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(per_channel, seed=3)
+    B, T, H, K = q.shape
+    HV = v.shape[2]
+    gen = torch.Generator().manual_seed(9)
+    a = torch.randn(g.shape, generator=gen, dtype=torch.float64) * 4
+    a.view(-1)[:3] = torch.tensor([25.0, 19.5, -30.0], dtype=torch.float64)  # both softplus branches
+    b_raw = torch.randn(beta.shape, generator=gen, dtype=torch.float64) * 3
+    A_log = torch.rand(HV, generator=gen, dtype=torch.float64) * math.log(16)
+    dt_bias = torch.randn(HV * K if per_channel else HV, generator=gen, dtype=torch.float64) * 0.1
+    fn = oracle.kda_decode if per_channel else oracle.gdn_decode
+    p1, p2 = pool.clone(), pool.clone()
+    raw = fn(q, k, v, a, b_raw, p1, ri, wi, A_log=A_log, dt_bias=dt_bias, gate_raw=True,
+             beta_raw=True, cache_intermediate=True)
+    if per_channel:
+        x = a + dt_bias.view(HV, K)
+        g_ref = -torch.exp(A_log)[:, None] * F.softplus(x)
+    else:
+        g_ref = -torch.exp(A_log) * F.softplus(a + dt_bias)
+    act = fn(q, k, v, g_ref, torch.sigmoid(b_raw), p2, ri, wi, cache_intermediate=True)
+    for key in ("out", "final_state", "inter"):
+        np.testing.assert_allclose(raw[key], act[key], rtol=1e-12, atol=1e-13)
+
+
+def test_l2norm_matches_normalize():
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(False, seed=5)
+    q, k = q * 1000, k * 1000      # eps effect 1e-6 / (2 |x|^2) ~ 5e-13
+    p1, p2 = pool.clone(), pool.clone()
+    a = oracle.gdn_decode(q, k, v, g, beta, p1, ri, wi, qk_l2norm=True)
+    b = oracle.gdn_decode(F.normalize(q, dim=-1), F.normalize(k, dim=-1), v, g, beta, p2, ri, wi)
+    np.testing.assert_allclose(a["out"], b["out"], rtol=0, atol=1e-10)
+    np.testing.assert_allclose(a["final_state"], b["final_state"], rtol=0, atol=1e-10)
+
+
+def test_l2norm_epsilon_inside_sqrt():
+    """q = [3, 4]: q_hat = q / sqrt(25 + 1e-6); with S0 = I and g = beta = 0, o = q_hat."""
+    q = _t([[[[3.0, 4.0]]]])
+    k = _t([[[[1.0, 0.0]]]])
+    v = _t([[[[0.0, 0.0]]]])
+    pool = torch.eye(2).view(1, 1, 2, 2).clone()
+    res = oracle.gdn_decode(q, k, v, _t([[[0.0]]]), _t([[[0.0]]]), pool, torch.tensor([0]),
+                            torch.tensor([-1]), qk_l2norm=True)
+    np.testing.assert_allclose(res["out"][0, 0, 0], np.array([3.0, 4.0]) / math.sqrt(25 + 1e-6),
+                               rtol=0, atol=1e-16)
+
+
+# --------------------------------------------------------------------------- indexing invariants
+
+def _pool_with_states(states, slots, P):
+    """Place per-sequence states [n,HV,V,K] at the given slots of a fresh pool."""
+    HV, V, K = states.shape[1:]
+    pool = torch.full((P, HV, V, K), -3.0)
+    for i, s in enumerate(slots):
+        pool[s] = states[i]
+    return pool
+
+
+@pytest.mark.parametrize("slots,P", [([0, 1, 2, 3], 4), ([2, 0, 5, 1], 6), ([3, 2, 1, 0], 4)])
+def test_slot_placement_does_not_change_results(slots, P):
+    """cuLA PR #75 pool tests: identity, non-identity (pool 6, [2,0,5,1]) and
+    reversed offsets give the same per-sequence output and state."""
+    gen = torch.Generator().manual_seed(11)
+    B, T, H, HV, K, V = 4, 2, 1, 2, 4, 3
+    states = torch.randn(B, HV, V, K, generator=gen)
+    q = torch.randn(B, T, H, K, generator=gen, dtype=torch.float64)
+    k = F.normalize(torch.randn(B, T, H, K, generator=gen, dtype=torch.float64), dim=-1)
+    v = torch.randn(B, T, HV, V, generator=gen, dtype=torch.float64)
+    g = -torch.rand(B, T, HV, generator=gen, dtype=torch.float64)
+    beta = torch.rand(B, T, HV, generator=gen, dtype=torch.float64)
+    ref_pool = _pool_with_states(states, [0, 1, 2, 3], 4)
+    ref = oracle.gdn_decode(q, k, v, g, beta, ref_pool, torch.arange(4))
+    pool = _pool_with_states(states, slots, P)
+    before = pool.clone()
+    res = oracle.gdn_decode(q, k, v, g, beta, pool, torch.tensor(slots))
+    assert np.array_equal(res["out"], ref["out"])
+    assert np.array_equal(res["final_state"], ref["final_state"])
+    for i, s in enumerate(slots):
+        assert torch.equal(pool[s], ref_pool[i])
+    inactive = [p for p in range(P) if p not in slots]
+    assert torch.equal(pool[inactive], before[inactive])
+
+
+def test_gqa_map_equals_repeated_heads():
+    """v-head hv uses q/k head hv // (HV / H): equal to HV independent heads
+    with q/k repeated consecutively."""
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(False)
+    rep = v.shape[2] // q.shape[2]
+    p1, p2 = pool.clone(), pool.clone()
+    a = oracle.gdn_decode(q, k, v, g, beta, p1, ri, wi, cache_intermediate=True)
+    b = oracle.gdn_decode(q.repeat_interleave(rep, dim=2), k.repeat_interleave(rep, dim=2),
+                          v, g, beta, p2, ri, wi, cache_intermediate=True)
+    for key in ("out", "final_state", "inter"):
+        assert np.array_equal(a[key], b[key])
+    assert torch.equal(p1, p2)
+
+
+@pytest.mark.parametrize("mult", [2, 3])
+def test_strided_pool_written_in_place(mult):
+    """flashinfer 4D pool fix: a strided view of a bigger backing buffer is
+    updated in place; the gap slots stay bit-identical."""
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(True)
+    P = pool.shape[0]
+    backing = torch.randn(P * mult, *pool.shape[1:], generator=torch.Generator().manual_seed(2))
+    backing[::mult] = pool
+    view = backing[::mult]
+    assert not view.is_contiguous()
+    before = backing.clone()
+    flat = pool.clone()
+    a = oracle.kda_decode(q, k, v, g, beta, view, ri, wi)
+    b = oracle.kda_decode(q, k, v, g, beta, flat, ri, wi)
+    assert np.array_equal(a["out"], b["out"])
+    assert torch.equal(backing[::mult], flat)
+    gaps = [i for i in range(P * mult) if i % mult]
+    assert torch.equal(backing[gaps], before[gaps])
+
+
+def test_flat_pool_equals_4d():
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(False)
+    P, HV, V, K = pool.shape
+    p4, p3 = pool.clone(), pool.clone().view(P * HV, V, K)
+    a = oracle.gdn_decode(q, k, v, g, beta, p4, ri, wi)
+    b = oracle.gdn_decode(q, k, v, g, beta, p3, ri, wi)
+    assert np.array_equal(a["out"], b["out"])
+    assert torch.equal(p4.view(P * HV, V, K), p3)
+
+
+def test_la_reads_row_slot_times_h_plus_h():
+    """lambda = 1, k = 0: o = S^T q for S at flat row read_idx * H + h."""
+    gen = torch.Generator().manual_seed(4)
+    B, H, K, V, P = 3, 2, 4, 3, 5
+    pool = torch.randn(P * H, V, K, generator=gen)
+    q = torch.randn(B, H, K, generator=gen, dtype=torch.float64)
+    k = torch.zeros(B, H, K, dtype=torch.float64)
+    v = torch.randn(B, H, V, generator=gen, dtype=torch.float64)
+    ri = torch.tensor([4, 0, 2])
+    res = oracle.la_decode(q, k, v, torch.ones(H, dtype=torch.float64), pool.clone(), ri)
+    for b in range(B):
+        for h in range(H):
+            S = pool[int(ri[b]) * H + h].double().numpy()       # [V,K]
+            np.testing.assert_allclose(res["out"][b, 0, h], S @ q[b, h].numpy(), rtol=0, atol=1e-12)
+
+
+def test_multi_token_equals_chained_single_tokens():
+    """A T-token call equals T one-token calls chained through the pool (the
+    chained form rounds the state to fp32 between tokens, so 1e-6 relative)."""
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(True, T=4)
+    ri = torch.tensor([4, 0, 2])          # every entry carries its state through the pool
+    wi = ri.clone()
+    p_multi, p_chain = pool.clone(), pool.clone()
+    multi = oracle.kda_decode(q, k, v, g, beta, p_multi, ri, wi, cache_intermediate=True)
+    for t in range(4):
+        one = oracle.kda_decode(q[:, t:t + 1], k[:, t:t + 1], v[:, t:t + 1], g[:, t:t + 1],
+                                beta[:, t:t + 1], p_chain, ri, wi)
+        np.testing.assert_allclose(one["out"][:, 0], multi["out"][:, t], rtol=1e-6, atol=1e-6)
+    np.testing.assert_allclose(p_chain.numpy(), p_multi.numpy(), rtol=1e-6, atol=1e-6)
+    # inter[:, T-1] is the final state
+    assert np.array_equal(multi["inter"][:, -1], multi["final_state"])
+
+
+def test_out_of_range_slots_are_counted_and_skipped():
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(False, B=2, T=1)
+    P = pool.shape[0]
+    before = pool.clone()
+    ri = torch.tensor([P, 3])
+    wi = torch.tensor([2, P + 5])
+    res = oracle.gdn_decode(q, k, v, g, beta, pool, ri, wi)
+    assert res["n_bad"] == 2
+    # entry 0 read out of range -> zero state, its write to slot 2 still happens
+    zero = oracle.gdn_decode(q[:1], k[:1], v[:1], g[:1], beta[:1], before.clone(),
+                             torch.tensor([-1]), torch.tensor([-1]))
+    assert np.array_equal(res["out"][0], zero["out"][0])
+    others = [p for p in range(P) if p != 2]
+    assert torch.equal(pool[others], before[others])

@@ -1,0 +1,306 @@
+"""Seeded synthetic inputs for the recurrent decode step.
+
+This module is the one piece shared by the oracle side (tests) and the CUDA
+side (tests, ``bench.py``, ``smoke()``).  It draws inputs and nothing else: it
+performs none of the decode arithmetic, and imports neither the oracle nor the
+library.  Where a workload recipe defines an input as a transformed draw
+(``q, k`` l2-normalised in fp32 before the bf16 cast, ``g = -softplus(N(0,1))``,
+``beta = sigmoid(N(0,1))``, ``lambda_h = exp(-2^(-8(h+1)/H))``), torch's own
+functions shape the distribution; the decode kernels receive the result as
+plain data with their in-kernel gate / l2norm switches off.
+
+Recipes (seed s; CPU ``torch.Generator``; draw order q, k, v, g or a, beta,
+A_log, dt_bias, read_idx, write_idx, then the pool):
+
+=================  ===========================================================
+gdn_tiny           B=2 T=1 H=HV=2 K=V=16, fp32 everywhere, pool [4,2,16,16],
+                   read = write = [3, 1], seed 0
+gdn_b64            B=64 T=1 H=16 HV=32 K=V=128, bf16 q/k/v/out, fp32 g/beta,
+                   pool [256,32,128,128]; read = write = randperm(256)[:64]; seed 2
+gdn_mtp_strided    B=16 T=4 H=16 HV=32, pool = backing[::2] of [256,32,128,128];
+                   read = randperm(128)[:16]; write = 16 distinct unread slots,
+                   4 of them set to -1; all T states cached; seed 3
+kda_b256           B=256 T=1 H=HV=24, raw bf16 q/k (l2norm in kernel), raw bf16
+                   gate a [B,T,HV,K], A_log ~ U(log 1, log 16) [HV], dt_bias ~
+                   N(0, 0.1) [HV*K], raw beta logits; pool [320,24,128,128];
+                   read = write = randperm(320)[:256]; seed 4
+la_b512_packed     B=512 T=1 H=64, q/k/v head-dim slices of one fused bf16
+                   [B,H,384] buffer (q, k ~ N(0,1)/sqrt(128), v ~ N(0,1)),
+                   lambda_h = exp(-2^(-8(h+1)/64)), flat pool [640*64,128,128];
+                   read = write = randperm(640)[:512]; seed 5
+=================  ===========================================================
+
+Pool entries are N(0, 0.1^2) (standard deviation 0.1).  Full-size pools are
+large (up to 2.7 GB), so ``pool_device="cuda"`` draws them on the device with
+a CUDA ``torch.Generator`` seeded with s; the oracle then reads a host copy of
+those drawn values.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+import torch.nn.functional as F
+
+BF16 = torch.bfloat16
+F32 = torch.float32
+
+CONFIGS = ("gdn_tiny", "gdn_b64", "gdn_mtp_strided", "kda_b256", "la_b512_packed")
+SEEDS = {"gdn_tiny": 0, "gdn_b64": 2, "gdn_mtp_strided": 3, "kda_b256": 4,
+         "la_b512_packed": 5}
+
+
+@dataclass
+class Workload:
+    name: str
+    form: str                      # "gdn" | "kda" | "la"
+    B: int
+    T: int
+    H: int
+    HV: int
+    K: int
+    V: int
+    P: int                         # pool slots
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    pool: torch.Tensor             # the view the decode step reads and writes
+    read_idx: torch.Tensor
+    write_idx: torch.Tensor | None
+    out_dtype: torch.dtype
+    g: torch.Tensor | None = None
+    beta: torch.Tensor | None = None
+    A_log: torch.Tensor | None = None
+    dt_bias: torch.Tensor | None = None
+    decay: torch.Tensor | None = None
+    backing: torch.Tensor | None = None    # set when `pool` is a strided view
+    fused: torch.Tensor | None = None      # set when q/k/v are slices of one buffer
+    qk_l2norm: bool = False
+    gate_raw: bool = False
+    beta_raw: bool = False
+    scale: float = 1.0
+    cache_intermediate: bool = False
+    meta: dict = field(default_factory=dict)
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes a perfect implementation moves per call (each input read once,
+        each output written once): state read for entries with a valid read
+        slot, state write for entries with a valid write slot, every cached
+        intermediate state, plus q/k/v/gate/out/index bytes."""
+        unit = self.K * self.V * 4
+        heads = self.HV
+        r = self.read_idx.to("cpu")
+        w = (self.write_idx if self.write_idx is not None else self.read_idx).to("cpu")
+        n_read = int(((r >= 0) & (r < self.P)).sum())
+        n_write = int(((w >= 0) & (w < self.P)).sum())
+        total = (n_read + n_write) * heads * unit
+        if self.cache_intermediate:
+            total += self.B * self.T * heads * unit
+        small = [self.q, self.k, self.v, self.g, self.beta, self.A_log, self.dt_bias,
+                 self.decay, self.read_idx, self.write_idx]
+        total += sum(t.numel() * t.element_size() for t in small if t is not None)
+        total += self.B * self.T * heads * self.V * torch.finfo(self.out_dtype).bits // 8
+        return int(total)
+
+    def tokens(self) -> int:
+        return self.B * self.T
+
+
+def _normal(gen, shape, std=1.0):
+    return torch.randn(shape, generator=gen, dtype=F32) * std
+
+
+def _l2n(x):
+    return F.normalize(x, p=2.0, dim=-1)
+
+
+def _draw_pool(gen, shape, seed, device):
+    if torch.device(device).type == "cpu":
+        return _normal(gen, shape, 0.1)
+    dg = torch.Generator(device=device)
+    dg.manual_seed(seed)
+    pool = torch.empty(shape, dtype=F32, device=device)
+    pool.normal_(0.0, 0.1, generator=dg)
+    return pool
+
+
+def make(name: str, *, seed: int | None = None, pool_device="cpu",
+         index_dtype=torch.int32) -> Workload:
+    """Draw the named workload (see the module docstring for the recipes)."""
+    s = SEEDS[name] if seed is None else seed
+    gen = torch.Generator().manual_seed(s)
+    if name == "gdn_tiny":
+        B, T, H, HV, K, V, P = 2, 1, 2, 2, 16, 16, 4
+        q = _l2n(_normal(gen, (B, T, H, K)))
+        k = _l2n(_normal(gen, (B, T, H, K)))
+        v = _normal(gen, (B, T, HV, V))
+        g = -F.softplus(_normal(gen, (B, T, HV)))
+        beta = torch.sigmoid(_normal(gen, (B, T, HV)))
+        ri = torch.tensor([3, 1], dtype=index_dtype)
+        pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
+        return Workload(name, "gdn", B, T, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
+                        F32, g=g, beta=beta)
+    if name == "gdn_b64":
+        B, T, H, HV, K, V, P = 64, 1, 16, 32, 128, 128, 256
+        q = _l2n(_normal(gen, (B, T, H, K))).to(BF16)
+        k = _l2n(_normal(gen, (B, T, H, K))).to(BF16)
+        v = _normal(gen, (B, T, HV, V)).to(BF16)
+        g = -F.softplus(_normal(gen, (B, T, HV)))
+        beta = torch.sigmoid(_normal(gen, (B, T, HV)))
+        ri = torch.randperm(P, generator=gen)[:B].to(index_dtype)
+        pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
+        return Workload(name, "gdn", B, T, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
+                        BF16, g=g, beta=beta)
+    if name == "gdn_mtp_strided":
+        B, T, H, HV, K, V, M = 16, 4, 16, 32, 128, 128, 2
+        P = 128
+        q = _l2n(_normal(gen, (B, T, H, K))).to(BF16)
+        k = _l2n(_normal(gen, (B, T, H, K))).to(BF16)
+        v = _normal(gen, (B, T, HV, V)).to(BF16)
+        g = -F.softplus(_normal(gen, (B, T, HV)))
+        beta = torch.sigmoid(_normal(gen, (B, T, HV)))
+        ri, wi = _read_write_disjoint(gen, P, B, skip_frac=0.25)
+        backing = _draw_pool(gen, (P * M, HV, V, K), s, pool_device)
+        pool = backing[::M]
+        return Workload(name, "gdn", B, T, H, HV, K, V, P, q, k, v, pool,
+                        ri.to(index_dtype), wi.to(index_dtype), BF16, g=g, beta=beta,
+                        backing=backing, cache_intermediate=True, meta={"stride_mult": M})
+    if name == "kda_b256":
+        B, T, H, HV, K, V, P = 256, 1, 24, 24, 128, 128, 320
+        q = _normal(gen, (B, T, H, K)).to(BF16)
+        k = _normal(gen, (B, T, H, K)).to(BF16)
+        v = _normal(gen, (B, T, HV, V)).to(BF16)
+        a = _normal(gen, (B, T, HV, K)).to(BF16)
+        b_raw = _normal(gen, (B, T, HV))
+        A_log = torch.empty(HV).uniform_(math.log(1.0), math.log(16.0), generator=gen)
+        dt_bias = _normal(gen, (HV * K,), 0.1)
+        ri = torch.randperm(P, generator=gen)[:B].to(index_dtype)
+        pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
+        return Workload(name, "kda", B, T, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
+                        BF16, g=a, beta=b_raw, A_log=A_log, dt_bias=dt_bias,
+                        qk_l2norm=True, gate_raw=True, beta_raw=True)
+    if name == "la_b512_packed":
+        B, H, K, V, P = 512, 64, 128, 128, 640
+        fused = torch.cat([_normal(gen, (B, H, K), 1.0 / math.sqrt(K)),
+                           _normal(gen, (B, H, K), 1.0 / math.sqrt(K)),
+                           _normal(gen, (B, H, V))], dim=-1).to(BF16)
+        q, k, v = fused[..., :K], fused[..., K:2 * K], fused[..., 2 * K:]
+        decay = la_decay_rates(H)
+        ri = torch.randperm(P, generator=gen)[:B].to(index_dtype)
+        pool = _draw_pool(gen, (P * H, V, K), s, pool_device)
+        return Workload(name, "la", B, 1, H, H, K, V, P, q, k, v, pool, ri, ri.clone(),
+                        BF16, decay=decay, fused=fused)
+    raise KeyError(name)
+
+
+def la_decay_rates(H: int) -> torch.Tensor:
+    """lambda_h = exp(-2^(-8(h+1)/H)), h = 0..H-1, as fp32 (the LA workload's rates)."""
+    h = torch.arange(H, dtype=torch.float64)
+    return torch.exp(-torch.pow(2.0, -8.0 * (h + 1) / H)).to(F32)
+
+
+def _read_write_disjoint(gen, P, B, skip_frac=0.0):
+    """Distinct read slots, and distinct write slots drawn from the slots no entry
+    reads; round(skip_frac * B) write entries are then set to -1."""
+    perm = torch.randperm(P, generator=gen)
+    ri = perm[:B].clone()
+    unread = perm[B:]
+    wi = unread[torch.randperm(unread.numel(), generator=gen)[:B]].clone()
+    n_skip = int(round(skip_frac * B))
+    if n_skip:
+        wi[torch.randperm(B, generator=gen)[:n_skip]] = -1
+    return ri, wi
+
+
+def make_custom(form: str, *, B: int, T: int, H: int, HV: int | None = None, K: int = 128,
+                V: int = 128, P: int | None = None, seed: int = 0, in_dtype=BF16,
+                out_dtype=BF16, separate_write: bool = False, skip_frac: float = 0.0,
+                stride_mult: int = 1, cache_intermediate: bool = False,
+                raw_gates: bool = False, packed: bool = False, flat_pool: bool = False,
+                index_dtype=torch.int32, pool_device="cpu") -> Workload:
+    """A workload of any size in the same distributions as the named recipes.
+
+    ``raw_gates``: q/k raw N(0,1) with in-kernel l2norm, raw gate input and beta
+    logits with A_log/dt_bias (the KDA recipe); otherwise activated g/beta and
+    pre-normalised q/k (the GDN recipe).  LA always uses the LA recipe.
+    ``separate_write``: write slots distinct from every read slot.
+    ``stride_mult`` > 1: the pool is backing[::stride_mult].
+    ``packed``: q/k/v are slices of one fused [B,T,H,2K+V] buffer (needs H == HV).
+    """
+    HV = H if HV is None else HV
+    P = max(2 * B, 4) if P is None else P
+    gen = torch.Generator().manual_seed(seed)
+    fused = None
+    if form == "la":
+        HV = H
+        if packed:
+            fused = torch.cat([_normal(gen, (B, T, H, K), 1.0 / math.sqrt(K)),
+                               _normal(gen, (B, T, H, K), 1.0 / math.sqrt(K)),
+                               _normal(gen, (B, T, H, V))], dim=-1).to(in_dtype)
+            q, k, v = fused[..., :K], fused[..., K:2 * K], fused[..., 2 * K:]
+        else:
+            q = _normal(gen, (B, T, H, K), 1.0 / math.sqrt(K)).to(in_dtype)
+            k = _normal(gen, (B, T, H, K), 1.0 / math.sqrt(K)).to(in_dtype)
+            v = _normal(gen, (B, T, H, V)).to(in_dtype)
+        g = beta = A_log = dt_bias = None
+        decay = la_decay_rates(H)
+    else:
+        if packed:
+            if H != HV:
+                raise ValueError("packed q/k/v needs H == HV")
+            raw = torch.cat([_normal(gen, (B, T, H, K)), _normal(gen, (B, T, H, K)),
+                             _normal(gen, (B, T, H, V))], dim=-1)
+            if not raw_gates:
+                raw = torch.cat([_l2n(raw[..., :K]), _l2n(raw[..., K:2 * K]),
+                                 raw[..., 2 * K:]], dim=-1)
+            fused = raw.to(in_dtype)
+            q, k, v = fused[..., :K], fused[..., K:2 * K], fused[..., 2 * K:]
+        else:
+            qf, kf = _normal(gen, (B, T, H, K)), _normal(gen, (B, T, H, K))
+            if not raw_gates:
+                qf, kf = _l2n(qf), _l2n(kf)
+            q, k = qf.to(in_dtype), kf.to(in_dtype)
+            v = _normal(gen, (B, T, HV, V)).to(in_dtype)
+        gshape = (B, T, HV, K) if form == "kda" else (B, T, HV)
+        if raw_gates:
+            g = _normal(gen, gshape).to(in_dtype)
+            beta = _normal(gen, (B, T, HV))
+            A_log = torch.empty(HV).uniform_(math.log(1.0), math.log(16.0), generator=gen)
+            dt_bias = _normal(gen, (HV * K,) if form == "kda" else (HV,), 0.1)
+        else:
+            g = -F.softplus(_normal(gen, gshape))
+            beta = torch.sigmoid(_normal(gen, (B, T, HV)))
+            A_log = dt_bias = None
+        decay = None
+    if separate_write:
+        ri, wi = _read_write_disjoint(gen, P, B, skip_frac)
+    else:
+        ri = torch.randperm(P, generator=gen)[:B]
+        wi = ri.clone()
+        n_skip = int(round(skip_frac * B))
+        if n_skip:
+            wi[torch.randperm(B, generator=gen)[:n_skip]] = -1
+    backing = None
+    if form == "la" and flat_pool:
+        pool = _draw_pool(gen, (P * H, V, K), seed, pool_device)
+    elif stride_mult > 1:
+        backing = _draw_pool(gen, (P * stride_mult, HV, V, K), seed, pool_device)
+        pool = backing[::stride_mult]
+    else:
+        pool = _draw_pool(gen, (P, HV, V, K), seed, pool_device)
+    return Workload(f"custom_{form}", form, B, T, H, HV, K, V, P, q, k, v, pool,
+                    ri.to(index_dtype), wi.to(index_dtype), out_dtype, g=g, beta=beta,
+                    A_log=A_log, dt_bias=dt_bias, decay=decay, backing=backing,
+                    fused=fused, qk_l2norm=raw_gates and form != "la",
+                    gate_raw=raw_gates and form != "la",
+                    beta_raw=raw_gates and form != "la",
+                    cache_intermediate=cache_intermediate)
+
+
+def disjoint_index_sets(P: int, B: int, n: int, seed: int, index_dtype=torch.int32):
+    """n index sets of B distinct slots each, pairwise disjoint (n * B <= P)."""
+    if n * B > P:
+        raise ValueError("not enough slots for disjoint sets")
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(seed))
+    return [perm[i * B:(i + 1) * B].to(index_dtype) for i in range(n)]
