@@ -1,0 +1,167 @@
+/*
+ * lar.h -- C ABI of the recurrent linear-attention decode library (GB300, sm_103a).
+ *
+ * One decode step of linear attention with a fixed-size recurrent state per
+ * (sequence, value head), kept in a paged fp32 state pool.  Three forms:
+ *
+ *   gdn_decode  gated delta rule, scalar decay per (token, v-head)
+ *   kda_decode  gated delta rule, decay per key channel
+ *   la_decode   Lightning Attention: decay per head, no delta term
+ *
+ * The delta-rule recurrence is the one the ROCm/aiter PR #4584 "Fused Gluon KDA
+ * decode path" advisory review states: per token
+ *     S <- exp(g_t) S;   S <- S + beta_t k_t (x) (v_t - S^T k_t);   o_t = S^T q_t
+ * with S a K x V matrix (for KDA exp(g_t) scales key channel k by exp(g_t[k])).
+ * Lightning Attention: S <- lambda_h S + k_t (x) v_t;  o_t = S^T q_t.
+ * Every output is multiplied by `scale`.
+ *
+ * Pool addressing (flashinfer "fp32 sibling of #3268" 4D-pool page; cuLA PR #75):
+ *   the state of batch entry b and v-head hv is read from slot read_idx[b] and
+ *   written to slot write_idx[b] (NULL write_idx: the read slot).  A negative
+ *   read index means a zero initial state; a negative write index skips the
+ *   writeback.  Every pool byte outside the written (slot, head) states is left
+ *   bit-identical.  The pool is read and written in place through its strides.
+ *
+ * Layouts (all strides in ELEMENTS and non-negative; shape[] is logical):
+ *   S is stored transposed: pool[slot][hv][v][k] = S[k][v], k fastest.
+ *   pool   fp32, rank 4 [P, HV, V, K] (any slot/head/row strides), or rank 3
+ *          [P*HV, V, K] (slot p, head hv at row p*HV + hv).  k stride must be 1;
+ *          the data pointer 16-byte aligned; slot, head and row strides
+ *          multiples of 4 (rows move as 16-byte vectors).
+ *   q, k   [B, T, H, K]  (rank 3 [B, H, K] means T = 1); fp32 or bf16, any strides
+ *          (so q/k/v may be head-dim slices of one fused buffer).
+ *   v      [B, T, HV, V] (rank 3 [B, HV, V]); fp32 or bf16, any strides.
+ *   out    [B, T, HV, V] (rank 3 [B, HV, V]); fp32 or bf16 (round to nearest even).
+ *   inter  NULL, or fp32 [B, T, HV, V, K] (rank 4 [B, HV, V, K] when T = 1):
+ *          the state after each token; same alignment rules as the pool.
+ *   read_idx, write_idx  rank 1 [B], int32 or int64, any stride.
+ *   H divides HV; v-head hv reads q/k head hv / (HV / H).
+ *   K must be 16, 32, 64 or 128; V from 1 to 2^24; T from 1 to 16;
+ *   B and HV at most 65535.
+ *
+ * Ownership and execution: the caller owns every buffer (device memory).  The
+ * library allocates nothing, keeps no state between calls and never
+ * synchronises: each call validates on the host and then enqueues one kernel
+ * on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *
+ * Errors: a host-detectable problem returns a status other than LAR_OK BEFORE
+ * anything is launched (nothing is written).  Slot indices >= P are caught on
+ * the device: that entry's state is not read (zero state) / not written, and
+ * the bits LAR_DEVERR_* are OR-ed into *dev_err when dev_err is not NULL (a
+ * caller-owned device int32, never cleared by the library).  No kernel traps
+ * or asserts.
+ *
+ * Aliasing: pool, out and inter must not overlap one another or any input
+ * (checked on the host by address range).  Entries must not read a slot that
+ * another entry writes, and write slots must be distinct; such calls are
+ * undefined (the kernels run entries concurrently).  In-place update (write
+ * slot == read slot of the same entry) is allowed.
+ */
+#ifndef LAR_H_
+#define LAR_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LAR_F32 = 0,
+    LAR_BF16 = 1,
+    LAR_I32 = 2,
+    LAR_I64 = 3
+} lar_dtype;
+
+/* A strided view of device memory.  data points at element [0, ..., 0]. */
+typedef struct {
+    void* data;
+    int32_t dtype;      /* lar_dtype */
+    int32_t ndim;       /* 1..5 */
+    int64_t shape[5];
+    int64_t stride[5];  /* in elements */
+} lar_tensor;
+
+typedef enum {
+    LAR_OK = 0,
+    LAR_ERR_NULL = 1,        /* a required tensor or pointer is NULL */
+    LAR_ERR_DTYPE = 2,       /* unsupported dtype for that argument */
+    LAR_ERR_RANK = 3,        /* wrong ndim */
+    LAR_ERR_SHAPE = 4,       /* shapes disagree, or a size outside the supported range */
+    LAR_ERR_STRIDE = 5,      /* k stride of pool/inter not 1, or negative strides */
+    LAR_ERR_ALIGN = 6,       /* pool/inter pointer or strides not 16-byte aligned */
+    LAR_ERR_ARG = 7,         /* inconsistent flags/arguments (e.g. A_log without LAR_GATE_RAW) */
+    LAR_ERR_ALIAS = 8,       /* an output overlaps another output or an input */
+    LAR_ERR_LAUNCH = 9       /* the CUDA launch itself failed */
+} lar_status;
+
+/* flags for gdn_decode / kda_decode */
+enum {
+    LAR_QK_L2NORM = 1u << 0, /* q, k <- x / sqrt(sum x^2 + 1e-6) over K, in kernel */
+    LAR_GATE_RAW = 1u << 1,  /* g <- -exp(A_log[hv]) * softplus(g + dt_bias), in kernel */
+    LAR_BETA_RAW = 1u << 2   /* beta <- 1 / (1 + exp(-beta)), in kernel */
+};
+
+/* bits OR-ed into *dev_err */
+enum {
+    LAR_DEVERR_READ_SLOT = 1,  /* some read_idx[b] >= P (that entry started from zero) */
+    LAR_DEVERR_WRITE_SLOT = 2  /* some write_idx[b] >= P (that writeback was skipped) */
+};
+
+/*
+ * Gated delta rule, scalar decay (GDN).  Interface of flashinfer's
+ * `gated_delta_rule_mtp` (initial_state = pool, initial_state_indices =
+ * read_idx, output_state_indices = write_idx, cache_intermediate_states =
+ * inter), recurrence from the aiter review.
+ *   g       [B, T, HV] (rank 2 [B, HV] when T = 1): log-decay, or the raw gate
+ *           input when LAR_GATE_RAW; fp32 or bf16, any strides.
+ *   beta    [B, T, HV] (rank 2 when T = 1): fp32 or bf16; a logit when LAR_BETA_RAW.
+ *   A_log   fp32 [HV]; required with LAR_GATE_RAW, must be NULL without it.
+ *   dt_bias fp32 [HV]; optional with LAR_GATE_RAW (zero), must be NULL without it.
+ */
+lar_status gdn_decode(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                      const lar_tensor* g, const lar_tensor* beta,
+                      const lar_tensor* A_log, const lar_tensor* dt_bias,
+                      const lar_tensor* pool,
+                      const lar_tensor* read_idx, const lar_tensor* write_idx,
+                      const lar_tensor* out, const lar_tensor* inter,
+                      float scale, uint32_t flags, int32_t* dev_err, void* stream);
+
+/*
+ * Gated delta rule, per-key-channel decay (KDA, "Kimi Delta Attention" in the
+ * aiter review; its wrapper consumes A_log, dt_bias and use_gate_in_kernel).
+ * Same as gdn_decode except:
+ *   g       [B, T, HV, K] (rank 3 [B, HV, K] when T = 1)
+ *   dt_bias fp32 [HV * K], channel k of head hv at hv * K + k
+ */
+lar_status kda_decode(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                      const lar_tensor* g, const lar_tensor* beta,
+                      const lar_tensor* A_log, const lar_tensor* dt_bias,
+                      const lar_tensor* pool,
+                      const lar_tensor* read_idx, const lar_tensor* write_idx,
+                      const lar_tensor* out, const lar_tensor* inter,
+                      float scale, uint32_t flags, int32_t* dev_err, void* stream);
+
+/*
+ * Lightning-Attention decode (cuLA PR #75): S <- lambda_h S + k (x) v, o = S^T q.
+ * HV == H here: q, k [B, T, H, K], v and out [B, T, H, V] (rank 3 for T = 1).
+ *   decay  fp32 [H]: lambda_h.
+ *   pool   rank 3 [P*H, V, K] (the page's layout; the state of entry b, head h
+ *          is row read_idx[b] * H + h), or rank 4 [P, H, V, K] whose slot
+ *          stride equals H times its head stride.  The first dimension of a
+ *          rank-3 pool must be a multiple of H.
+ */
+lar_status la_decode(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                     const lar_tensor* decay, const lar_tensor* pool,
+                     const lar_tensor* read_idx, const lar_tensor* write_idx,
+                     const lar_tensor* out, const lar_tensor* inter,
+                     float scale, int32_t* dev_err, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* lar_status_string(lar_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAR_H_ */

@@ -1,0 +1,178 @@
+"""ctypes binding over liblar.so: the same three calls as include/lar.h, taking
+torch tensors.  Marshalling only -- every step of the decode runs in the CUDA
+kernels behind the C ABI; there is no Python or CPU fallback.  A missing
+library, a CPU tensor or a non-OK status raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+_LIB_PATH = _build.LIB
+
+LAR_F32, LAR_BF16, LAR_I32, LAR_I64 = 0, 1, 2, 3
+LAR_QK_L2NORM, LAR_GATE_RAW, LAR_BETA_RAW = 1, 2, 4
+LAR_DEVERR_READ_SLOT, LAR_DEVERR_WRITE_SLOT = 1, 2
+
+STATUS = {0: "LAR_OK", 1: "LAR_ERR_NULL", 2: "LAR_ERR_DTYPE", 3: "LAR_ERR_RANK",
+          4: "LAR_ERR_SHAPE", 5: "LAR_ERR_STRIDE", 6: "LAR_ERR_ALIGN", 7: "LAR_ERR_ARG",
+          8: "LAR_ERR_ALIAS", 9: "LAR_ERR_LAUNCH"}
+
+_DT = {torch.float32: LAR_F32, torch.bfloat16: LAR_BF16, torch.int32: LAR_I32,
+       torch.int64: LAR_I64}
+
+
+class LarTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 5), ("stride", ctypes.c_int64 * 5)]
+
+
+class LarError(RuntimeError):
+    def __init__(self, fn, status, msg):
+        super().__init__(f"{fn}: {STATUS.get(status, status)} ({msg})")
+        self.status = status
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load liblar.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.POINTER(LarTensor)
+        tail = [ctypes.c_float, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p]
+        for name in ("gdn_decode", "kda_decode"):
+            fn = getattr(lib, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = [P] * 12 + tail
+        lib.la_decode.restype = ctypes.c_int
+        lib.la_decode.argtypes = [P] * 9 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+        lib.lar_status_string.restype = ctypes.c_char_p
+        lib.lar_status_string.argtypes = [ctypes.c_int]
+        _lib = lib
+    return _lib
+
+
+def describe(t: torch.Tensor | None):
+    """lar_tensor descriptor of a CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("liblar works on CUDA tensors only")
+    if t.dtype not in _DT:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    if t.dim() < 1 or t.dim() > 5:
+        raise ValueError(f"unsupported rank {t.dim()}")
+    d = LarTensor()
+    d.data = t.data_ptr()
+    d.dtype = _DT[t.dtype]
+    d.ndim = t.dim()
+    for i, (s, st) in enumerate(zip(t.shape, t.stride())):
+        d.shape[i] = s
+        d.stride[i] = st
+    return d
+
+
+def _ref(d):
+    return ctypes.byref(d) if d is not None else None
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(fn, status):
+    if status != 0:
+        raise LarError(fn, status, load().lar_status_string(status).decode())
+
+
+def _flags(qk_l2norm, gate_raw, beta_raw):
+    return (LAR_QK_L2NORM if qk_l2norm else 0) | (LAR_GATE_RAW if gate_raw else 0) | \
+        (LAR_BETA_RAW if beta_raw else 0)
+
+
+def gdn_decode(q, k, v, g, beta, pool, read_idx, write_idx=None, *, out=None, inter=None,
+               A_log=None, dt_bias=None, scale=1.0, qk_l2norm=False, gate_raw=False,
+               beta_raw=False, dev_err=None, out_dtype=None, stream=None):
+    """Gated delta rule decode (scalar decay).  Updates `pool` in place; returns `out`."""
+    return _delta("gdn_decode", q, k, v, g, beta, pool, read_idx, write_idx, out, inter, A_log,
+                  dt_bias, scale, _flags(qk_l2norm, gate_raw, beta_raw), dev_err, out_dtype, stream)
+
+
+def kda_decode(q, k, v, g, beta, pool, read_idx, write_idx=None, *, out=None, inter=None,
+               A_log=None, dt_bias=None, scale=1.0, qk_l2norm=False, gate_raw=False,
+               beta_raw=False, dev_err=None, out_dtype=None, stream=None):
+    """Gated delta rule decode (per-key-channel decay).  Updates `pool` in place."""
+    return _delta("kda_decode", q, k, v, g, beta, pool, read_idx, write_idx, out, inter, A_log,
+                  dt_bias, scale, _flags(qk_l2norm, gate_raw, beta_raw), dev_err, out_dtype, stream)
+
+
+def _delta(name, q, k, v, g, beta, pool, read_idx, write_idx, out, inter, A_log, dt_bias, scale,
+           flags, dev_err, out_dtype, stream):
+    lib = load()
+    if out is None:
+        out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
+    ds = [describe(t) for t in (q, k, v, g, beta, A_log, dt_bias, pool, read_idx, write_idx, out,
+                                inter)]
+    err = dev_err.data_ptr() if dev_err is not None else None
+    st = getattr(lib, name)(*[_ref(d) for d in ds], float(scale), flags, err, _stream(stream))
+    _check(name, st)
+    return out
+
+
+def la_decode(q, k, v, decay, pool, read_idx, write_idx=None, *, out=None, inter=None, scale=1.0,
+              dev_err=None, out_dtype=None, stream=None):
+    """Lightning-Attention decode.  Updates `pool` in place; returns `out`."""
+    lib = load()
+    if out is None:
+        out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
+    ds = [describe(t) for t in (q, k, v, decay, pool, read_idx, write_idx, out, inter)]
+    err = dev_err.data_ptr() if dev_err is not None else None
+    st = lib.la_decode(*[_ref(d) for d in ds], float(scale), err, _stream(stream))
+    _check("la_decode", st)
+    return out
+
+
+class PreparedCall:
+    """A decode call whose descriptors are built once, for tight launch loops.
+    The tensors it was built from must stay alive and keep their storage."""
+
+    def __init__(self, form, *, scale=1.0, qk_l2norm=False, gate_raw=False, beta_raw=False,
+                 dev_err=None, stream=None, **tensors):
+        lib = load()
+        self._name = f"{form}_decode"
+        self._fn = getattr(lib, self._name)
+        self._keep = (tensors, dev_err)
+        err = dev_err.data_ptr() if dev_err is not None else None
+        st = _stream(stream)
+        if form == "la":
+            names = ("q", "k", "v", "decay", "pool", "read_idx", "write_idx", "out", "inter")
+            self._descs = [describe(tensors.get(n)) for n in names]
+            self._args = [_ref(d) for d in self._descs] + [float(scale), err, st]
+        else:
+            names = ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "pool", "read_idx",
+                     "write_idx", "out", "inter")
+            self._descs = [describe(tensors.get(n)) for n in names]
+            self._args = [_ref(d) for d in self._descs] + [
+                float(scale), _flags(qk_l2norm, gate_raw, beta_raw), err, st]
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != 0:
+            _check(self._name, st)

@@ -1,0 +1,46 @@
+// decode_params.h -- the validated, flattened argument block handed from the
+// C ABI layer (lar_abi.cpp) to the kernel launchers (decode_*.cu).
+#pragma once
+
+#include <stdint.h>
+
+#include "lar.h"
+
+namespace lar {
+
+enum Form : int { FORM_GDN = 0, FORM_KDA = 1, FORM_LA = 2 };
+
+// Every stride is in elements.  Per-token tensors are indexed (b, t, head, x);
+// a rank-3 input (T = 1) has its t stride set to 0 by the ABI layer.
+struct DecodeParams {
+    int form;
+    int B, T, H, HV, K, V;
+    int group;             // HV / H
+    int64_t P;             // pool slots
+
+    const void* q;    int64_t qs[4];  int q_dt;
+    const void* k;    int64_t ks[4];  int k_dt;
+    const void* v;    int64_t vs[4];  int v_dt;
+    const void* g;    int64_t gs[4];  int g_dt;    // GDN uses gs[0..2]
+    const void* beta; int64_t bs[3];  int beta_dt;
+    const float* A_log;   int64_t A_s;            // [HV]
+    const float* dt_bias; int64_t dtb_s;          // GDN [HV]; KDA [HV*K]
+    const float* decay;   int64_t dec_s;          // LA [H]
+
+    float* pool; int64_t ps[3];                   // slot, head, row strides (k stride 1)
+    const void* ridx; int64_t ri_s; int ri_dt;
+    const void* widx; int64_t wi_s; int wi_dt;    // NULL: write to the read slot
+
+    void* out;    int64_t os[4]; int out_dt;
+    float* inter; int64_t is[4];                  // b, t, head, row (k stride 1); may be NULL
+
+    float scale;
+    uint32_t flags;
+    int32_t* dev_err;
+};
+
+lar_status launch_gdn(const DecodeParams& p, void* stream);
+lar_status launch_kda(const DecodeParams& p, void* stream);
+lar_status launch_la(const DecodeParams& p, void* stream);
+
+}  // namespace lar

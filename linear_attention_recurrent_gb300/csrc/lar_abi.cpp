@@ -1,0 +1,341 @@
+// lar_abi.cpp -- the exported C entry points: validate every descriptor on the
+// host, flatten it into a DecodeParams block and enqueue one kernel.  Nothing
+// is launched (and nothing written) unless every check passes.
+#include <stdint.h>
+
+#include "decode_params.h"
+#include "lar.h"
+
+namespace {
+
+using lar::DecodeParams;
+
+bool is_float(const lar_tensor* t) { return t->dtype == LAR_F32 || t->dtype == LAR_BF16; }
+bool is_index(const lar_tensor* t) { return t->dtype == LAR_I32 || t->dtype == LAR_I64; }
+
+int64_t elem_size(int32_t dt) {
+    switch (dt) {
+        case LAR_F32: return 4;
+        case LAR_BF16: return 2;
+        case LAR_I32: return 4;
+        case LAR_I64: return 8;
+        default: return 0;
+    }
+}
+
+// Rank in 1..5, non-negative sizes and strides.
+lar_status check_header(const lar_tensor* t) {
+    if (t->ndim < 1 || t->ndim > 5) return LAR_ERR_RANK;
+    for (int i = 0; i < t->ndim; ++i) {
+        if (t->shape[i] < 0) return LAR_ERR_SHAPE;
+        if (t->stride[i] < 0) return LAR_ERR_STRIDE;
+    }
+    return LAR_OK;
+}
+
+// Half-open byte range [lo, hi) that a view can touch (empty views touch nothing).
+struct Span {
+    uintptr_t lo = 0, hi = 0;
+};
+
+Span span_of(const lar_tensor* t) {
+    Span s;
+    if (!t || !t->data) return s;
+    int64_t last = 0;
+    for (int i = 0; i < t->ndim; ++i) {
+        if (t->shape[i] == 0) return s;
+        last += (t->shape[i] - 1) * t->stride[i];
+    }
+    const uintptr_t base = reinterpret_cast<uintptr_t>(t->data);
+    s.lo = base;
+    s.hi = base + static_cast<uintptr_t>((last + 1) * elem_size(t->dtype));
+    return s;
+}
+
+bool overlap(const Span& a, const Span& b) {
+    return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+
+// A per-token tensor of logical shape [B, T, heads, X] given at rank `full`
+// or rank `full - 1` (T = 1).  Writes strides (b, t, head, x), with t stride 0
+// for the short form.  X < 0 means the tensor has no trailing x dimension.
+bool per_token_view(const lar_tensor* t, int full, int64_t B, int64_t T, int64_t heads, int64_t X,
+                    int64_t st[4]) {
+    const bool has_x = X >= 0;
+    int64_t shp[4] = {0, 0, 0, 0};
+    int64_t str[4] = {0, 0, 0, 0};
+    if (t->ndim == full) {
+        for (int i = 0; i < full; ++i) { shp[i] = t->shape[i]; str[i] = t->stride[i]; }
+    } else if (t->ndim == full - 1 && T == 1) {
+        shp[0] = t->shape[0]; str[0] = t->stride[0];
+        shp[1] = 1; str[1] = 0;
+        for (int i = 1; i < full - 1; ++i) { shp[i + 1] = t->shape[i]; str[i + 1] = t->stride[i]; }
+    } else {
+        return false;
+    }
+    if (shp[0] != B || shp[1] != T || shp[2] != heads) return false;
+    if (has_x && shp[3] != X) return false;
+    for (int i = 0; i < 4; ++i) st[i] = str[i];
+    if (!has_x) st[3] = 0;
+    return true;
+}
+
+struct Common {
+    const lar_tensor *q, *k, *v, *pool, *read_idx, *write_idx, *out, *inter;
+};
+
+// Checks shared by every form; fills sizes, q/k/v/out/pool/index/inter fields.
+lar_status check_common(const Common& c, int form, DecodeParams& p) {
+    if (!c.q || !c.k || !c.v || !c.pool || !c.read_idx || !c.out) return LAR_ERR_NULL;
+    if (!c.q->data || !c.k->data || !c.v->data || !c.pool->data || !c.read_idx->data || !c.out->data)
+        return LAR_ERR_NULL;
+    const lar_tensor* all[] = {c.q, c.k, c.v, c.pool, c.read_idx, c.write_idx, c.out, c.inter};
+    for (const lar_tensor* t : all) {
+        if (!t) continue;
+        const lar_status st = check_header(t);
+        if (st != LAR_OK) return st;
+    }
+
+    if (c.q->ndim != 3 && c.q->ndim != 4) return LAR_ERR_RANK;
+    if (c.k->ndim != c.q->ndim || c.v->ndim != c.q->ndim || c.out->ndim != c.q->ndim) return LAR_ERR_RANK;
+    if (!is_float(c.q) || !is_float(c.k) || !is_float(c.v) || !is_float(c.out)) return LAR_ERR_DTYPE;
+    if (c.pool->dtype != LAR_F32) return LAR_ERR_DTYPE;
+
+    const bool short_form = c.q->ndim == 3;
+    const int64_t B = c.q->shape[0];
+    const int64_t T = short_form ? 1 : c.q->shape[1];
+    const int64_t H = c.q->shape[short_form ? 1 : 2];
+    const int64_t K = c.q->shape[short_form ? 2 : 3];
+    const int64_t HV = c.v->shape[short_form ? 1 : 2];
+    const int64_t V = c.v->shape[short_form ? 2 : 3];
+    if (K != 16 && K != 32 && K != 64 && K != 128) return LAR_ERR_SHAPE;
+    if (T < 1 || T > 16 || H < 1 || HV < 1 || V < 1 || B > 65535 || HV > 65535 || V > (1 << 24))
+        return LAR_ERR_SHAPE;
+    if (HV % H != 0) return LAR_ERR_SHAPE;
+    if (form == lar::FORM_LA && HV != H) return LAR_ERR_SHAPE;
+
+    p.form = form;
+    p.B = static_cast<int>(B);
+    p.T = static_cast<int>(T);
+    p.H = static_cast<int>(H);
+    p.HV = static_cast<int>(HV);
+    p.K = static_cast<int>(K);
+    p.V = static_cast<int>(V);
+    p.group = static_cast<int>(HV / H);
+
+    if (!per_token_view(c.q, 4, B, T, H, K, p.qs)) return LAR_ERR_SHAPE;
+    if (!per_token_view(c.k, 4, B, T, H, K, p.ks)) return LAR_ERR_SHAPE;
+    if (!per_token_view(c.v, 4, B, T, HV, V, p.vs)) return LAR_ERR_SHAPE;
+    if (!per_token_view(c.out, 4, B, T, HV, V, p.os)) return LAR_ERR_SHAPE;
+    p.q = c.q->data; p.q_dt = c.q->dtype;
+    p.k = c.k->data; p.k_dt = c.k->dtype;
+    p.v = c.v->data; p.v_dt = c.v->dtype;
+    p.out = c.out->data; p.out_dt = c.out->dtype;
+
+    // pool: [P, HV, V, K] or flat [P*HV, V, K]; k contiguous, 16-byte rows
+    const lar_tensor* pl = c.pool;
+    int64_t P;
+    if (pl->ndim == 4) {
+        if (pl->shape[1] != HV || pl->shape[2] != V || pl->shape[3] != K) return LAR_ERR_SHAPE;
+        if (pl->stride[3] != 1) return LAR_ERR_STRIDE;
+        P = pl->shape[0];
+        p.ps[0] = pl->stride[0];
+        p.ps[1] = pl->stride[1];
+        p.ps[2] = pl->stride[2];
+        if (form == lar::FORM_LA && P > 1 && pl->stride[0] != HV * pl->stride[1]) return LAR_ERR_STRIDE;
+    } else if (pl->ndim == 3) {
+        if (pl->shape[1] != V || pl->shape[2] != K) return LAR_ERR_SHAPE;
+        if (pl->shape[0] % HV != 0) return LAR_ERR_SHAPE;
+        if (pl->stride[2] != 1) return LAR_ERR_STRIDE;
+        P = pl->shape[0] / HV;
+        p.ps[0] = pl->stride[0] * HV;
+        p.ps[1] = pl->stride[0];
+        p.ps[2] = pl->stride[1];
+    } else {
+        return LAR_ERR_RANK;
+    }
+    if (reinterpret_cast<uintptr_t>(pl->data) % 16 != 0) return LAR_ERR_ALIGN;
+    if (p.ps[0] % 4 || p.ps[1] % 4 || p.ps[2] % 4) return LAR_ERR_ALIGN;
+    p.P = P;
+    p.pool = static_cast<float*>(pl->data);
+
+    // slot indices
+    if (c.read_idx->ndim != 1) return LAR_ERR_RANK;
+    if (c.read_idx->shape[0] != B) return LAR_ERR_SHAPE;
+    if (!is_index(c.read_idx)) return LAR_ERR_DTYPE;
+    p.ridx = c.read_idx->data; p.ri_s = c.read_idx->stride[0]; p.ri_dt = c.read_idx->dtype;
+    if (c.write_idx) {
+        if (!c.write_idx->data) return LAR_ERR_NULL;
+        if (c.write_idx->ndim != 1) return LAR_ERR_RANK;
+        if (c.write_idx->shape[0] != B) return LAR_ERR_SHAPE;
+        if (!is_index(c.write_idx)) return LAR_ERR_DTYPE;
+        p.widx = c.write_idx->data; p.wi_s = c.write_idx->stride[0]; p.wi_dt = c.write_idx->dtype;
+    } else {
+        p.widx = nullptr; p.wi_s = 0; p.wi_dt = LAR_I32;
+    }
+
+    // intermediate-state cache: [B, T, HV, V, K] (rank 4 [B, HV, V, K] for T = 1)
+    p.inter = nullptr;
+    for (int i = 0; i < 4; ++i) p.is[i] = 0;
+    if (c.inter) {
+        const lar_tensor* it = c.inter;
+        if (!it->data) return LAR_ERR_NULL;
+        if (it->dtype != LAR_F32) return LAR_ERR_DTYPE;
+        int64_t shp[5], str[5];
+        if (it->ndim == 5) {
+            for (int i = 0; i < 5; ++i) { shp[i] = it->shape[i]; str[i] = it->stride[i]; }
+        } else if (it->ndim == 4 && T == 1) {
+            shp[0] = it->shape[0]; str[0] = it->stride[0];
+            shp[1] = 1; str[1] = 0;
+            for (int i = 1; i < 4; ++i) { shp[i + 1] = it->shape[i]; str[i + 1] = it->stride[i]; }
+        } else {
+            return LAR_ERR_RANK;
+        }
+        if (shp[0] != B || shp[1] != T || shp[2] != HV || shp[3] != V || shp[4] != K) return LAR_ERR_SHAPE;
+        if (str[4] != 1) return LAR_ERR_STRIDE;
+        if (reinterpret_cast<uintptr_t>(it->data) % 16 != 0) return LAR_ERR_ALIGN;
+        if (str[0] % 4 || str[1] % 4 || str[2] % 4 || str[3] % 4) return LAR_ERR_ALIGN;
+        p.inter = static_cast<float*>(it->data);
+        for (int i = 0; i < 4; ++i) p.is[i] = str[i];
+    }
+    return LAR_OK;
+}
+
+lar_status check_aliasing(const lar_tensor* const* outs, int n_out, const lar_tensor* const* ins, int n_in) {
+    for (int i = 0; i < n_out; ++i) {
+        if (!outs[i]) continue;
+        const Span a = span_of(outs[i]);
+        for (int j = i + 1; j < n_out; ++j)
+            if (outs[j] && overlap(a, span_of(outs[j]))) return LAR_ERR_ALIAS;
+        for (int j = 0; j < n_in; ++j)
+            if (ins[j] && overlap(a, span_of(ins[j]))) return LAR_ERR_ALIAS;
+    }
+    return LAR_OK;
+}
+
+// A 1-D fp32 parameter vector of length n (A_log, dt_bias, decay).
+lar_status check_vec(const lar_tensor* t, int64_t n, const float** ptr, int64_t* stride) {
+    const lar_status st = check_header(t);
+    if (st != LAR_OK) return st;
+    if (!t->data) return LAR_ERR_NULL;
+    if (t->ndim != 1) return LAR_ERR_RANK;
+    if (t->shape[0] != n) return LAR_ERR_SHAPE;
+    if (t->dtype != LAR_F32) return LAR_ERR_DTYPE;
+    *ptr = static_cast<const float*>(t->data);
+    *stride = t->stride[0];
+    return LAR_OK;
+}
+
+lar_status delta_rule(int form, const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                      const lar_tensor* g, const lar_tensor* beta, const lar_tensor* A_log,
+                      const lar_tensor* dt_bias, const lar_tensor* pool, const lar_tensor* read_idx,
+                      const lar_tensor* write_idx, const lar_tensor* out, const lar_tensor* inter,
+                      float scale, uint32_t flags, int32_t* dev_err, void* stream) {
+    DecodeParams p{};
+    if (flags & ~static_cast<uint32_t>(LAR_QK_L2NORM | LAR_GATE_RAW | LAR_BETA_RAW)) return LAR_ERR_ARG;
+    lar_status st = check_common(Common{q, k, v, pool, read_idx, write_idx, out, inter}, form, p);
+    if (st != LAR_OK) return st;
+    if (!g || !beta) return LAR_ERR_NULL;
+    if (!g->data || !beta->data) return LAR_ERR_NULL;
+    if ((st = check_header(g)) != LAR_OK) return st;
+    if ((st = check_header(beta)) != LAR_OK) return st;
+    if (!is_float(g) || !is_float(beta)) return LAR_ERR_DTYPE;
+    const bool kda = form == lar::FORM_KDA;
+    if (!per_token_view(g, kda ? 4 : 3, p.B, p.T, p.HV, kda ? p.K : -1, p.gs)) return LAR_ERR_SHAPE;
+    int64_t bst[4];
+    if (!per_token_view(beta, 3, p.B, p.T, p.HV, -1, bst)) return LAR_ERR_SHAPE;
+    for (int i = 0; i < 3; ++i) p.bs[i] = bst[i];
+    p.g = g->data; p.g_dt = g->dtype;
+    p.beta = beta->data; p.beta_dt = beta->dtype;
+
+    // Gate parameters only make sense with the in-kernel gate: the aiter review
+    // found a wrapper that accepted them without the flag and silently ran
+    // ungated decay.
+    const bool raw = (flags & LAR_GATE_RAW) != 0;
+    if (!raw && (A_log || dt_bias)) return LAR_ERR_ARG;
+    if (raw && !A_log) return LAR_ERR_NULL;
+    p.A_log = nullptr; p.A_s = 0; p.dt_bias = nullptr; p.dtb_s = 0;
+    if (raw) {
+        st = check_vec(A_log, p.HV, &p.A_log, &p.A_s);
+        if (st != LAR_OK) return st;
+        if (dt_bias) {
+            st = check_vec(dt_bias, kda ? static_cast<int64_t>(p.HV) * p.K : p.HV, &p.dt_bias, &p.dtb_s);
+            if (st != LAR_OK) return st;
+        }
+    }
+    p.decay = nullptr; p.dec_s = 0;
+    p.scale = scale;
+    p.flags = flags;
+    p.dev_err = dev_err;
+
+    const lar_tensor* outs[] = {pool, out, inter};
+    const lar_tensor* ins[] = {q, k, v, g, beta, A_log, dt_bias, read_idx, write_idx};
+    st = check_aliasing(outs, 3, ins, 9);
+    if (st != LAR_OK) return st;
+    if (p.B == 0) return LAR_OK;
+    return kda ? lar::launch_kda(p, stream) : lar::launch_gdn(p, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+lar_status gdn_decode(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                      const lar_tensor* g, const lar_tensor* beta, const lar_tensor* A_log,
+                      const lar_tensor* dt_bias, const lar_tensor* pool,
+                      const lar_tensor* read_idx, const lar_tensor* write_idx,
+                      const lar_tensor* out, const lar_tensor* inter, float scale, uint32_t flags,
+                      int32_t* dev_err, void* stream) {
+    return delta_rule(lar::FORM_GDN, q, k, v, g, beta, A_log, dt_bias, pool, read_idx, write_idx,
+                      out, inter, scale, flags, dev_err, stream);
+}
+
+lar_status kda_decode(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                      const lar_tensor* g, const lar_tensor* beta, const lar_tensor* A_log,
+                      const lar_tensor* dt_bias, const lar_tensor* pool,
+                      const lar_tensor* read_idx, const lar_tensor* write_idx,
+                      const lar_tensor* out, const lar_tensor* inter, float scale, uint32_t flags,
+                      int32_t* dev_err, void* stream) {
+    return delta_rule(lar::FORM_KDA, q, k, v, g, beta, A_log, dt_bias, pool, read_idx, write_idx,
+                      out, inter, scale, flags, dev_err, stream);
+}
+
+lar_status la_decode(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                     const lar_tensor* decay, const lar_tensor* pool, const lar_tensor* read_idx,
+                     const lar_tensor* write_idx, const lar_tensor* out, const lar_tensor* inter,
+                     float scale, int32_t* dev_err, void* stream) {
+    DecodeParams p{};
+    lar_status st = check_common(Common{q, k, v, pool, read_idx, write_idx, out, inter}, lar::FORM_LA, p);
+    if (st != LAR_OK) return st;
+    if (!decay) return LAR_ERR_NULL;
+    st = check_vec(decay, p.H, &p.decay, &p.dec_s);
+    if (st != LAR_OK) return st;
+    p.g = nullptr; p.beta = nullptr; p.A_log = nullptr; p.dt_bias = nullptr;
+    p.scale = scale;
+    p.flags = 0;
+    p.dev_err = dev_err;
+    const lar_tensor* outs[] = {pool, out, inter};
+    const lar_tensor* ins[] = {q, k, v, decay, read_idx, write_idx};
+    st = check_aliasing(outs, 3, ins, 6);
+    if (st != LAR_OK) return st;
+    if (p.B == 0) return LAR_OK;
+    return lar::launch_la(p, stream);
+}
+
+const char* lar_status_string(lar_status status) {
+    switch (status) {
+        case LAR_OK: return "ok";
+        case LAR_ERR_NULL: return "a required tensor or pointer is NULL";
+        case LAR_ERR_DTYPE: return "unsupported dtype";
+        case LAR_ERR_RANK: return "wrong tensor rank";
+        case LAR_ERR_SHAPE: return "shapes disagree or a size is outside the supported range";
+        case LAR_ERR_STRIDE: return "unsupported strides (k stride of pool/inter must be 1; no negative strides)";
+        case LAR_ERR_ALIGN: return "pool/inter must be 16-byte aligned with strides that are multiples of 4 elements";
+        case LAR_ERR_ARG: return "inconsistent arguments or flags";
+        case LAR_ERR_ALIAS: return "an output overlaps another output or an input";
+        case LAR_ERR_LAUNCH: return "kernel launch failed";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,153 @@
+"""The C ABI without a GPU: liblar.so loads, exports every function include/lar.h
+declares, and rejects invalid arguments on the host with the documented status
+before anything is launched.  Descriptors here carry fake (never dereferenced)
+addresses; every call below fails validation, so no CUDA call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_recurrent_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lar.h")
+
+OK, NULL, DTYPE, RANK, SHAPE, STRIDE, ALIGN, ARG, ALIAS = range(9)
+F32, BF16, I32, I64 = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("gdn_decode", "kda_decode", "la_decode", "lar_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for s in range(10):
+        assert lib.lar_status_string(s)
+    assert lib.lar_status_string(0) == b"ok"
+
+
+_next_addr = [0x10000000]
+
+
+def fake(shape, dtype=F32, strides=None, addr=None):
+    d = binding.LarTensor()
+    es = {F32: 4, BF16: 2, I32: 4, I64: 8}[dtype]
+    if strides is None:
+        strides, acc = [], 1
+        for s in reversed(shape):
+            strides.insert(0, acc)
+            acc *= s
+    n = 1 + sum((s - 1) * st for s, st in zip(shape, strides))
+    if addr is None:
+        addr = _next_addr[0]
+        _next_addr[0] += ((n * es + 4095) // 4096 + 1) * 4096
+    d.data = addr
+    d.dtype = dtype
+    d.ndim = len(shape)
+    for i, (s, st) in enumerate(zip(shape, strides)):
+        d.shape[i] = s
+        d.stride[i] = st
+    return d
+
+
+def gdn_args(B=2, T=1, H=2, HV=4, K=128, V=64, P=8, kda=False):
+    a = dict(q=fake([B, T, H, K], BF16), k=fake([B, T, H, K], BF16), v=fake([B, T, HV, V], BF16),
+             g=fake([B, T, HV, K] if kda else [B, T, HV]), beta=fake([B, T, HV]),
+             A_log=None, dt_bias=None, pool=fake([P, HV, V, K]), read_idx=fake([B], I32),
+             write_idx=fake([B], I32), out=fake([B, T, HV, V], BF16), inter=None)
+    return a
+
+
+ORDER = ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "pool", "read_idx", "write_idx", "out",
+         "inter")
+
+
+def call(lib, a, flags=0, kda=False):
+    fn = lib.kda_decode if kda else lib.gdn_decode
+    refs = [ctypes.byref(a[n]) if a[n] is not None else None for n in ORDER]
+    return fn(*refs, 1.0, flags, None, None)
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert call(lib, gdn_args(B=0)) == OK
+
+
+@pytest.mark.parametrize("mutate,flags,expect", [
+    (lambda a: a.update(q=None), 0, NULL),
+    (lambda a: a.update(pool=None), 0, NULL),
+    (lambda a: a.update(g=None), 0, NULL),
+    (lambda a: setattr(a["q"], "ndim", 6), 0, RANK),
+    (lambda a: a.update(q=fake([2, 1, 2, 100], BF16), k=fake([2, 1, 2, 100], BF16)), 0, SHAPE),
+    (lambda a: a.update(v=fake([2, 1, 3, 64], BF16), out=fake([2, 1, 3, 64], BF16)), 0, SHAPE),
+    (lambda a: a.update(pool=fake([8, 4, 64, 128], BF16)), 0, DTYPE),
+    (lambda a: a.update(q=fake([2, 1, 2, 128], I32)), 0, DTYPE),
+    (lambda a: a.update(pool=fake([8, 4, 64, 128], strides=[64 * 256 * 4, 64 * 256, 256, 2])), 0, STRIDE),
+    (lambda a: a.update(pool=fake([8, 4, 64, 128], addr=0x7000004)), 0, ALIGN),
+    (lambda a: a.update(pool=fake([8, 4, 64, 128], strides=[4 * 64 * 130, 64 * 130, 130, 1])), 0, ALIGN),
+    (lambda a: a.update(A_log=fake([4])), 0, ARG),                  # gate params without the flag
+    (lambda a: a.update(dt_bias=fake([4])), 0, ARG),
+    (lambda a: None, 2, NULL),                                        # LAR_GATE_RAW without A_log
+    (lambda a: a.update(A_log=fake([3])), 2, SHAPE),
+    (lambda a: None, 8, ARG),                                         # unknown flag bit
+    (lambda a: a.update(read_idx=fake([3], I32)), 0, SHAPE),
+    (lambda a: a.update(read_idx=fake([2], F32)), 0, DTYPE),
+    (lambda a: a.update(write_idx=fake([2, 1], I32)), 0, RANK),
+    (lambda a: a.update(inter=fake([2, 1, 4, 64, 64])), 0, SHAPE),
+    (lambda a: a.update(inter=fake([2, 1, 4, 64, 128], strides=[1, 1, 1, 1, 2])), 0, STRIDE),
+    (lambda a: a.update(out=fake([2, 1, 4, 64], F32, addr=a["pool"].data)), 0, ALIAS),
+    (lambda a: a.update(out=fake([2, 1, 4, 64], BF16, addr=a["v"].data)), 0, ALIAS),
+])
+def test_gdn_rejects_on_host(lib, mutate, flags, expect):
+    a = gdn_args()
+    mutate(a)
+    assert call(lib, a, flags) == expect
+
+
+def test_multi_token_limit(lib):
+    assert call(lib, gdn_args(T=17)) == SHAPE
+
+
+def test_kda_gate_shape(lib):
+    a = gdn_args(kda=True)
+    a["g"] = fake([2, 1, 4])                                          # GDN-shaped gate
+    assert call(lib, a, kda=True) == SHAPE
+    a = gdn_args(kda=True)
+    a["A_log"], a["dt_bias"] = fake([4]), fake([4])                   # dt_bias must be [HV*K]
+    assert call(lib, a, flags=2, kda=True) == SHAPE
+
+
+def la_call(lib, B=2, H=4, K=128, V=128, P=5, pool=None, decay=None):
+    q, k, v = fake([B, H, K], BF16), fake([B, H, K], BF16), fake([B, H, V], BF16)
+    pool = pool or fake([P * H, V, K])
+    decay = decay or fake([H])
+    ri, out = fake([B], I64), fake([B, H, V], BF16)
+    refs = [ctypes.byref(x) for x in (q, k, v, decay, pool, ri)] + [None, ctypes.byref(out), None]
+    return lib.la_decode(*refs, 1.0, None, None)
+
+
+def test_la_rejects_on_host(lib):
+    assert la_call(lib, pool=fake([4 * 5 + 1, 128, 128])) == SHAPE   # rows not a multiple of H
+    assert la_call(lib, decay=fake([3])) == SHAPE
+    assert la_call(lib, decay=fake([4], BF16)) == DTYPE
+    # 4D pool whose slot stride is not H * head stride cannot be the flat layout
+    assert la_call(lib, pool=fake([5, 4, 128, 128], strides=[8 * 128 * 128, 128 * 128, 128, 1])) == STRIDE
+    assert la_call(lib, B=0) == OK
