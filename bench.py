@@ -1,0 +1,472 @@
+"""Benchmark of the recurrent decode step on GB300.
+
+Default workload: gdn_b64 (GDN decode, B=64, T=1, H=16, HV=32, K=V=128, bf16
+q/k/v/out, fp32 pool [256,32,128,128]).  A step is one decode call over the
+batch.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl lar|reference]
+
+Timing: W untimed steps, then K steps bracketed by barrier + synchronize, with
+a CUDA event pair around every launch on the launching stream.  When the pool
+holds several disjoint batches (gdn_b64: 4 x 64 slots, 512 MiB of state) the
+steps rotate over them so no launch finds its state in L2; the other
+workloads touch more state than L2 holds.  value = algorithmic bytes of all
+ranks' steps / max-over-ranks device time (GB/s).
+
+--impl reference times the fp64 CPU oracle instead (the slow reference arm) on
+bounded samples of the same workload; rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "decode state-pool HBM GB/s (% of GB300 peak) and tokens/s at K=V=128"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DESCRIPTIONS = {
+    "gdn_tiny": "GDN decode B=2 T=1 H=HV=2 K=V=16 fp32",
+    "gdn_b64": "GDN decode B=64 T=1 H=16 HV=32 K=V=128, bf16 q/k/v/out, fp32 pool [256,32,128,128]",
+    "gdn_mtp_strided": "GDN MTP B=16 T=4 H=16 HV=32 K=V=128, pool = backing[::2] of [256,32,128,128], "
+                       "separate write slots (25% -1), all T states cached",
+    "kda_b256": "KDA decode B=256 T=1 H=HV=24 K=V=128, in-kernel gate/l2norm/sigmoid, pool [320,24,128,128]",
+    "la_b512_packed": "Lightning-Attention decode B=512 T=1 H=64 K=V=128, packed bf16 QKV, "
+                      "flat pool [640*64,128,128]",
+}
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources; ncu traffic figures are valid only for this hash."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_attention_recurrent_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:12]
+
+
+def measured_traffic(config: str):
+    """dram bytes per launch from profiles/dram_traffic.txt, if captured on the current kernel."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == config and parts[1] == want:
+            return int(parts[2])
+    return None
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        sel = []
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if ids and device_index < len(ids):
+            sel = ["-i", ids[device_index]]
+        else:
+            try:
+                u = str(torch.cuda.get_device_properties(device_index).uuid)
+                sel = ["-i", u if u.startswith("GPU-") else "GPU-" + u]
+            except Exception:
+                sel = ["-i", str(device_index)]
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "50"] + sel
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons, n = [], [], set(), 0
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ts, line in self.lines:
+            if not (t0 - 0.06 <= ts <= t1 + 0.06):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            n += 1
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ workload on device
+
+def device_inputs(w, dev):
+    cu = lambda t: None if t is None else t.to(dev)
+    d = {"q": cu(w.q), "k": cu(w.k), "v": cu(w.v), "pool": w.pool if w.pool.is_cuda else w.pool.to(dev)}
+    if w.form == "la":
+        d["decay"] = cu(w.decay)
+    else:
+        d.update(g=cu(w.g), beta=cu(w.beta), A_log=cu(w.A_log), dt_bias=cu(w.dt_bias))
+    return d
+
+
+def index_sets(w):
+    """Disjoint (read, write) index sets to rotate over, when the pool holds
+    several batches (in-place workloads only); else the workload's own set."""
+    same = w.write_idx is not None and torch.equal(w.read_idx, w.write_idx)
+    n = w.P // w.B if same else 1
+    if n >= 2:
+        n = min(n, 4)
+        sets = W.disjoint_index_sets(w.P, w.B, n, seed=1234, index_dtype=w.read_idx.dtype)
+        return [(s, s.clone()) for s in sets], n
+    return [(w.read_idx, w.write_idx)], 1
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_lar(args, world, rank, local):
+    import linear_attention_recurrent_gb300 as lar
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lar.load()
+    w = W.make(args.config, pool_device=dev)
+    d = device_inputs(w, dev)
+    sets, n_sets = index_sets(w)
+    stream = torch.cuda.Stream(device=dev)
+    outs, inters, calls = [], [], []
+    with torch.cuda.stream(stream):
+        for ri, wi in sets:
+            out = torch.empty(w.v.shape, dtype=w.out_dtype, device=dev)
+            inter = (torch.empty(w.B, w.T, w.HV, w.V, w.K, device=dev)
+                     if w.cache_intermediate else None)
+            kw = dict(d, read_idx=ri.to(dev), write_idx=None if wi is None else wi.to(dev),
+                      out=out, inter=inter)
+            if w.form != "la":
+                kw.update(qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw)
+            calls.append(lar.PreparedCall(w.form, scale=w.scale, stream=stream, **kw))
+            outs.append(out)
+            inters.append(inter)
+    bytes_per_step = w.algorithmic_bytes()
+    torch.cuda.synchronize(dev)
+
+    for i in range(args.warmup):
+        calls[i % n_sets]()
+    torch.cuda.synchronize(dev)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    # keep the GPU busy while the sampler spins up, then time exactly K steps
+    for i in range(min(args.warmup, 50)):
+        calls[i % n_sets]()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        first = torch.cuda.Event(enable_timing=True)
+        last = torch.cuda.Event(enable_timing=True)
+        first.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            calls[i % n_sets]()
+            ev[i][1].record(stream)
+        last.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(world)
+    clocks = sampler.stop(t_wall0, t_wall1)
+
+    total_ms = first.elapsed_time(last)
+    per_launch = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms_per_step = total_ms / args.steps
+    gbs = bytes_per_step * args.steps * world / (total_ms * 1e-3) / 1e9
+    tokens = w.tokens() * args.steps * world / (total_ms * 1e-3)
+    mean_launch_ms = sum(per_launch) / len(per_launch)
+    achieved = bytes_per_step / (mean_launch_ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    e2e = run_e2e(w, d, sets, dev, stream, args) if rank == 0 else None
+    cpu = cpu_baseline(w, args) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; see workloads.py)",
+        "config": {"workload": f"{args.config}: {DESCRIPTIONS.get(args.config, args.config)}",
+                   "bytes_per_step": bytes_per_step, "tokens_per_step": w.tokens(),
+                   "l2": (f"rotating {n_sets} disjoint slot sets "
+                          f"({n_sets * w.B * w.HV * w.K * w.V * 4 / 2**20:.0f} MiB of state), "
+                          "inputs larger than L2" if n_sets > 1 else "inputs larger than L2"),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tokens_per_s": round(tokens, 1),
+        "pct_of_8tbs": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_peak": round(100 * gbs / world / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": measured_traffic(args.config),
+                     "peak_source": f"{peak_kind} copy bandwidth",
+                     "kernel": f"decode_kernel<{w.form}> ({kernel_source_hash()})",
+                     "mean_launch_us": round(mean_launch_ms * 1e3, 3),
+                     "median_launch_us": round(statistics.median(per_launch) * 1e3, 3)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    return line
+
+
+def run_e2e(w, d, sets, dev, stream, args):
+    """The same metric through the public call with host buffers: per step,
+    pinned host -> device copies of the step's inputs, one gdn/kda/la_decode
+    call, device -> host copy of the output, synchronize."""
+    import linear_attention_recurrent_gb300 as lar
+
+    names = ["q", "k", "v"] + (["decay"] if w.form == "la" else ["g", "beta"])
+    ri, wi = sets[0]
+    host = {n: getattr(w, n).contiguous().pin_memory() for n in names if getattr(w, n) is not None}
+    host["read_idx"] = ri.pin_memory()
+    host["write_idx"] = wi.pin_memory()
+    devbuf = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    out_dev = torch.empty(w.v.shape, dtype=w.out_dtype, device=dev)
+    out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
+    inter = torch.empty(w.B, w.T, w.HV, w.V, w.K, device=dev) if w.cache_intermediate else None
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    steps = max(10, min(args.steps, 2000))
+
+    def step():
+        with torch.cuda.stream(stream):
+            for n, t in host.items():
+                devbuf[n].copy_(t, non_blocking=True)
+            if w.form == "la":
+                lar.la_decode(devbuf["q"], devbuf["k"], devbuf["v"], devbuf["decay"], d["pool"],
+                              devbuf["read_idx"], devbuf["write_idx"], out=out_dev, inter=inter,
+                              scale=w.scale, stream=stream)
+            else:
+                fn = lar.gdn_decode if w.form == "gdn" else lar.kda_decode
+                fn(devbuf["q"], devbuf["k"], devbuf["v"], devbuf["g"], devbuf["beta"], d["pool"],
+                   devbuf["read_idx"], devbuf["write_idx"], out=out_dev, inter=inter,
+                   A_log=d.get("A_log"), dt_bias=d.get("dt_bias"), scale=w.scale,
+                   qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw, stream=stream)
+            out_host.copy_(out_dev, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(5):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": round(w.algorithmic_bytes() / dt / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(dt * 1e3, 4), "steps": steps,
+            "tokens_per_s": round(w.tokens() / dt, 1),
+            "note": "wall clock per step incl. H2D inputs, the decode call, D2H output and a stream sync; "
+                    "the pool stays resident on the device"}
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def _oracle_step(w, host_pool, batch):
+    import oracle
+    sel = lambda t: None if t is None else t[batch]
+    if w.form == "la":
+        oracle.la_decode(sel(w.q), sel(w.k), sel(w.v), w.decay, host_pool, sel(w.read_idx),
+                         sel(w.write_idx), scale=w.scale, cache_intermediate=w.cache_intermediate)
+    else:
+        fn = oracle.gdn_decode if w.form == "gdn" else oracle.kda_decode
+        fn(sel(w.q), sel(w.k), sel(w.v), sel(w.g), sel(w.beta), host_pool, sel(w.read_idx),
+           sel(w.write_idx), A_log=w.A_log, dt_bias=w.dt_bias, qk_l2norm=w.qk_l2norm,
+           gate_raw=w.gate_raw, beta_raw=w.beta_raw, scale=w.scale,
+           cache_intermediate=w.cache_intermediate)
+
+
+def _host_workload(config):
+    """The workload with its pool on the host (the oracle reads it in place)."""
+    w = W.make(config, pool_device="cuda" if torch.cuda.is_available() else "cpu")
+    if w.backing is not None:
+        mult = w.pool.stride(0) // w.backing.stride(0)
+        w.backing = w.backing.cpu()
+        w.pool = w.backing[::mult]
+    else:
+        w.pool = w.pool.cpu()
+    return w
+
+
+def cpu_baseline(w_dev, args, budget_s=10.0):
+    """The oracle as it stands, single-threaded C, on whole steps of the same
+    workload repeated for about `budget_s` seconds."""
+    import oracle
+    oracle.build()
+    w = _host_workload(args.config)
+    batch = torch.arange(w.B)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_step(w, w.pool, batch)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 1000:
+            break
+    return {"value": round(w.algorithmic_bytes() * reps / el / 1e9, 4), "unit": "GB/s",
+            "cores": 1, "kind": "oracle",
+            "sample": f"{reps} whole {args.config} steps ({w.B} entries x {w.HV} heads each), "
+                      f"{el:.1f} s, fp64 C loops, one thread",
+            "tokens_per_s": round(w.tokens() * reps / el, 2)}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the fp64 CPU oracle, rank 0 only, on bounded samples."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    w = _host_workload(args.config)
+    # size each step's sample so warmup + steps stay around a minute
+    probe_t0 = time.perf_counter()
+    _oracle_step(w, w.pool, torch.arange(1))
+    per_entry = max(time.perf_counter() - probe_t0, 1e-6)
+    n = max(1, min(w.B, int(60.0 / ((args.steps + args.warmup) * per_entry))))
+    batch = torch.arange(n)
+    for _ in range(args.warmup):
+        _oracle_step(w, w.pool, batch)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(w, w.pool, batch)
+    el = time.perf_counter() - t0
+    bytes_step = w.algorithmic_bytes() * n / w.B
+    gbs = bytes_step * args.steps / el / 1e9
+    sample = (f"{n} of {w.B} entries ({n * w.HV} (entry, head) states) per step; "
+              f"bytes scaled by {n}/{w.B}")
+    return {"impl": "reference", "metric": METRIC, "value": round(gbs, 5), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.config}: {DESCRIPTIONS.get(args.config, args.config)}",
+                       "parallelism": "single host thread"},
+            "cpu_baseline": {"value": round(gbs, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--config", default="gdn_b64", choices=W.CONFIGS)
+    ap.add_argument("--impl", default="lar", choices=["lar", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback exists)")
+        line = run_lar(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

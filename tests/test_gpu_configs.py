@@ -1,0 +1,58 @@
+"""The named workloads at full size, in the launch configuration bench.py
+times: sampled batch entries (first, last and six seeded others) against the
+fp64 oracle, every untouched pool byte bit-identical, written states finite."""
+import pytest
+import torch
+
+import _parity as P
+import workloads as W
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def _sample(B, seed=0, n=6):
+    rest = torch.randperm(B - 2, generator=torch.Generator().manual_seed(seed))[:n] + 1
+    return sorted({0, B - 1, *rest.tolist()})
+
+
+@pytest.mark.parametrize("name", ["gdn_b64", "gdn_mtp_strided", "kda_b256", "la_b512_packed"])
+def test_full_size(name, cuda_device):
+    dev = cuda_device
+    w = W.make(name, pool_device=dev)
+    storage = P.storage(w)
+    before = storage.clone()
+    mult = w.pool.stride(0) // w.backing.stride(0) if w.backing is not None else 1
+    before_view = before[::mult] if w.backing is not None else before
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out, inter = P.run_gpu(w, dev, pool=w.pool, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+
+    mask = P.written_mask(w).to(dev)
+    assert torch.equal(storage[~mask], before[~mask]), "untouched pool bytes changed"
+    assert torch.isfinite(storage[mask]).all()
+
+    sample = _sample(w.B)
+    n = len(sample)
+    ri = w.read_idx.long()
+    shape = (n * w.HV,) + tuple(w.pool.shape[1:]) if w.pool.dim() == 3 else (n,) + tuple(w.pool.shape[1:])
+    sub = torch.zeros(shape)
+    for i, b in enumerate(sample):
+        r = int(ri[b])
+        if 0 <= r < w.P:
+            if w.pool.dim() == 3:
+                sub[i * w.HV:(i + 1) * w.HV] = P.slot_state(before_view, w, r).cpu()
+            else:
+                sub[i] = before_view[r].cpu()
+    ri_sub = torch.full((w.B,), -1, dtype=torch.int64)
+    ri_sub[sample] = torch.arange(n)
+    wi_sub = torch.full((w.B,), -1, dtype=torch.int64)
+    ref = P.run_oracle(w, sub, read_idx=ri_sub, write_idx=wi_sub, batch=sample)
+    P.assert_out_close(out[sample], ref["out"].reshape(out[sample].shape))
+    if inter is not None:
+        P.assert_state_close(inter[sample], ref["inter"], "inter")
+    wi = (w.write_idx if w.write_idx is not None else w.read_idx).tolist()
+    for i, b in enumerate(sample):
+        if 0 <= wi[b] < w.P:
+            P.assert_state_close(P.slot_state(w.pool, w, wi[b]), ref["final_state"][i],
+                                 f"slot {wi[b]} (entry {b})")
