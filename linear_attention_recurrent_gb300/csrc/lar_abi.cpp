@@ -33,6 +33,16 @@ lar_status check_header(const lar_tensor* t) {
     return LAR_OK;
 }
 
+// A view with a zero-sized dimension holds no elements and may carry a NULL
+// data pointer (torch gives empty tensors one).
+bool empty(const lar_tensor* t) {
+    for (int i = 0; i < t->ndim && i < 5; ++i)
+        if (t->shape[i] == 0) return true;
+    return false;
+}
+
+bool missing(const lar_tensor* t) { return !t || (!t->data && !empty(t)); }
+
 // Half-open byte range [lo, hi) that a view can touch (empty views touch nothing).
 struct Span {
     uintptr_t lo = 0, hi = 0;
@@ -86,8 +96,8 @@ struct Common {
 
 // Checks shared by every form; fills sizes, q/k/v/out/pool/index/inter fields.
 lar_status check_common(const Common& c, int form, DecodeParams& p) {
-    if (!c.q || !c.k || !c.v || !c.pool || !c.read_idx || !c.out) return LAR_ERR_NULL;
-    if (!c.q->data || !c.k->data || !c.v->data || !c.pool->data || !c.read_idx->data || !c.out->data)
+    if (missing(c.q) || missing(c.k) || missing(c.v) || missing(c.pool) || missing(c.read_idx) ||
+        missing(c.out))
         return LAR_ERR_NULL;
     const lar_tensor* all[] = {c.q, c.k, c.v, c.pool, c.read_idx, c.write_idx, c.out, c.inter};
     for (const lar_tensor* t : all) {
@@ -165,7 +175,7 @@ lar_status check_common(const Common& c, int form, DecodeParams& p) {
     if (!is_index(c.read_idx)) return LAR_ERR_DTYPE;
     p.ridx = c.read_idx->data; p.ri_s = c.read_idx->stride[0]; p.ri_dt = c.read_idx->dtype;
     if (c.write_idx) {
-        if (!c.write_idx->data) return LAR_ERR_NULL;
+        if (missing(c.write_idx)) return LAR_ERR_NULL;
         if (c.write_idx->ndim != 1) return LAR_ERR_RANK;
         if (c.write_idx->shape[0] != B) return LAR_ERR_SHAPE;
         if (!is_index(c.write_idx)) return LAR_ERR_DTYPE;
@@ -179,7 +189,7 @@ lar_status check_common(const Common& c, int form, DecodeParams& p) {
     for (int i = 0; i < 4; ++i) p.is[i] = 0;
     if (c.inter) {
         const lar_tensor* it = c.inter;
-        if (!it->data) return LAR_ERR_NULL;
+        if (missing(it)) return LAR_ERR_NULL;
         if (it->dtype != LAR_F32) return LAR_ERR_DTYPE;
         int64_t shp[5], str[5];
         if (it->ndim == 5) {
@@ -217,7 +227,7 @@ lar_status check_aliasing(const lar_tensor* const* outs, int n_out, const lar_te
 lar_status check_vec(const lar_tensor* t, int64_t n, const float** ptr, int64_t* stride) {
     const lar_status st = check_header(t);
     if (st != LAR_OK) return st;
-    if (!t->data) return LAR_ERR_NULL;
+    if (missing(t)) return LAR_ERR_NULL;
     if (t->ndim != 1) return LAR_ERR_RANK;
     if (t->shape[0] != n) return LAR_ERR_SHAPE;
     if (t->dtype != LAR_F32) return LAR_ERR_DTYPE;
@@ -235,8 +245,7 @@ lar_status delta_rule(int form, const lar_tensor* q, const lar_tensor* k, const 
     if (flags & ~static_cast<uint32_t>(LAR_QK_L2NORM | LAR_GATE_RAW | LAR_BETA_RAW)) return LAR_ERR_ARG;
     lar_status st = check_common(Common{q, k, v, pool, read_idx, write_idx, out, inter}, form, p);
     if (st != LAR_OK) return st;
-    if (!g || !beta) return LAR_ERR_NULL;
-    if (!g->data || !beta->data) return LAR_ERR_NULL;
+    if (missing(g) || missing(beta)) return LAR_ERR_NULL;
     if ((st = check_header(g)) != LAR_OK) return st;
     if ((st = check_header(beta)) != LAR_OK) return st;
     if (!is_float(g) || !is_float(beta)) return LAR_ERR_DTYPE;
