@@ -1,12 +1,19 @@
 // decode_kernel.cuh -- the sm_103a decode kernel shared by GDN, KDA and LA.
 //
-// Work decomposition: one CTA per (V-tile, v-head hv, batch entry b); grid
-// (ceil(V / TV), HV, B), sized from the active batch, never from the pool.
-// Inside a CTA a state row (one value channel v, all K key channels = K fp32,
-// contiguous in the pool) is owned by a group of LPR consecutive lanes; lane j
-// of the group holds the 16-byte chunks j, j + LPR, j + 2 LPR, ... of the row,
-// so one warp instruction moves RPW = 32 / LPR whole rows in full 128-byte
-// lines.  Each thread keeps NR rows in registers for the whole step.
+// Work decomposition.  A tile is TV consecutive state rows of one
+// (batch entry b, v-head hv) pair; a state row is one value channel v with its
+// K key channels (K fp32, contiguous in the pool).  Tiles are numbered with
+// the V-tile fastest, then hv, then b, and a persistent grid of
+// (SM count x resident CTAs per SM) CTAs takes contiguous, equal ranges of
+// them.  The grid is sized from the active batch B*HV, never from the pool.
+//
+// State streaming.  Every thread owns the same 16-byte chunks of every tile
+// (lane group of LPR lanes per row, lane j holding chunks j, j+LPR, ...), and
+// moves them HBM -> shared memory with cp.async through an S-stage ring: the
+// copies for tile i+S-1 are in flight while tile i is computed.  Because each
+// thread only ever reads back the chunks it copied itself, the ring needs no
+// barrier between threads (cp.async.wait_group orders a thread's own copies).
+// Updated rows go from registers straight back to HBM with streaming stores.
 //
 // Per token (aiter KDA review recurrence, S^T stored row-wise):
 //     s      <- s * exp(g)              (per element for KDA, scalar for GDN)
@@ -16,15 +23,33 @@
 //     o_row  =  scale * (p + delta * (k_hat . q_hat))      [= scale * s_new . q_hat]
 // LA:  s <- lambda s;  p = s . q;  s <- s + v_row k;  o_row = scale (p + v_row (k . q)).
 //
-// The per-token vectors (q, k, the KDA decay row) and scalars are built once
-// per CTA in shared memory (gate chain and l2 norms included) while the state
-// loads issued at kernel entry are in flight.
+// The per-token vectors (q, k, the KDA decay row) and scalars of the current
+// (b, hv) pair are built by the whole CTA in shared memory (gate chain and l2
+// norms included) when the pair changes, into one of two buffers so that
+// building the next pair's vectors never races with readers of the last.
 #pragma once
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "decode_params.h"
+
+// K = 128 tile shape: rows per thread, warps per CTA, ring stages.
+#ifndef LAR_K128_NR
+#define LAR_K128_NR 2
+#endif
+#ifndef LAR_K128_NW
+#define LAR_K128_NW 4
+#endif
+#ifndef LAR_MIN_BLOCKS
+#define LAR_MIN_BLOCKS 1
+#endif
+#ifndef LAR_PDL
+#define LAR_PDL 1
+#endif
+#ifndef LAR_K128_S
+#define LAR_K128_S 2
+#endif
 
 namespace lar {
 
@@ -63,235 +88,414 @@ __device__ __forceinline__ void axpy4(float4& s, const float a, const float4 x) 
     s.w = fmaf(a, x.w, s.w);
 }
 
-template <int LPR>
-__device__ __forceinline__ float group_sum(float x) {
-#pragma unroll
-    for (int off = LPR / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-    return x;
+// 16-byte global -> shared copy that bypasses L1 (the state is touched once).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    const unsigned dst = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(gmem_src) : "memory");
 }
 
-// Shared-memory bytes the kernel needs for T tokens.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Tile geometry shared by the kernel and its launcher.
+template <int K, int LPR, int NR, int NW>
+struct Tile {
+    static constexpr int KPL = K / LPR;       // floats of a row held by one lane
+    static constexpr int NCH = KPL / 4;       // 16-byte chunks of a row held by one lane
+    static constexpr int RPW = 32 / LPR;      // rows covered by one warp instruction
+    static constexpr int TV = NW * NR * RPW;  // rows per tile
+    static_assert(KPL % 4 == 0 && NCH >= 1, "a lane holds whole 16-byte chunks");
+    static_assert(32 % LPR == 0, "row groups tile the warp");
+};
+
+// v values of a (b, hv) pair are staged in shared memory with the other
+// per-pair vectors when T * V is at most this many floats; otherwise the
+// token loop reads them from global memory.
+constexpr int kStageVMax = 4096;
+
+__host__ __device__ constexpr bool stage_v(int T, int V) { return T * V <= kStageVMax; }
+
+// Floats of one per-pair vector buffer: q, k (and the KDA decay rows) for T
+// tokens, the staged v values, and 5 scalars per token; a multiple of 4 so
+// the second buffer stays 16-byte aligned.
 template <int FORM, int K>
-__host__ __device__ constexpr size_t decode_smem_bytes(int T) {
-    return (static_cast<size_t>(FORM == FORM_KDA ? 3 : 2) * T * K + 5 * static_cast<size_t>(T)) *
+__host__ __device__ constexpr int vec_floats(int T, int V) {
+    return ((FORM == FORM_KDA ? 3 : 2) * T * K + (stage_v(T, V) ? T * V : 0) + 5 * T + 3) & ~3;
+}
+
+template <int FORM, int K, int LPR, int NR, int NW, int S>
+__host__ __device__ constexpr size_t decode_smem_bytes(int T, int V) {
+    using G = Tile<K, LPR, NR, NW>;
+    return (static_cast<size_t>(S) * G::TV * K + 2 * static_cast<size_t>(vec_floats<FORM, K>(T, V))) *
            sizeof(float);
 }
 
-template <int FORM, int K, int LPR, int NR, int NW>
-__global__ void __launch_bounds__(NW * 32)
+template <int FORM, int K, int LPR, int NR, int NW, int S>
+__global__ void __launch_bounds__(NW * 32, LAR_MIN_BLOCKS)
 decode_kernel(const DecodeParams p) {
-    constexpr int KPL = K / LPR;       // floats of a row held by one lane
-    constexpr int NCH = KPL / 4;       // 16-byte chunks of a row held by one lane
-    constexpr int RPW = 32 / LPR;      // rows covered by one warp instruction
-    constexpr int TV = NW * NR * RPW;  // rows per CTA
-    static_assert(KPL % 4 == 0 && NCH >= 1, "a lane holds whole 16-byte chunks");
-    static_assert(32 % LPR == 0, "row groups tile the warp");
+    using G = Tile<K, LPR, NR, NW>;
+    constexpr int NCH = G::NCH, RPW = G::RPW, TV = G::TV;
 
     extern __shared__ __align__(16) float smem[];
     const int T = p.T;
-    float* sq = smem;                                   // [T][K] q (raw)
-    float* sk = sq + T * K;                             // [T][K] k (raw)
-    float* sd = sk + T * K;                             // [T][K] KDA exp(g)
-    float* sc = sd + (FORM == FORM_KDA ? T * K : 0);    // [5][T] beta, decay, 1/|q|, 1/|k|, k.q
+    const int V = p.V;
+    const bool sv_on = stage_v(T, V);
+    float* ring = smem;                                        // [S][TV][K]
+    float* vecs = smem + static_cast<size_t>(S) * TV * K;      // 2 x vec_floats
+    const int vstride = vec_floats<FORM, K>(T, V);
+    // offsets inside a vector buffer
+    const int o_k = T * K;
+    const int o_d = 2 * T * K;
+    const int o_v = (FORM == FORM_KDA ? 3 : 2) * T * K;
+    const int o_s = o_v + (sv_on ? T * V : 0);                  // beta, decay, 1/|q|, 1/|k|, q.k/(|q||k|)
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int j = lane % LPR;
     const int gi = lane / LPR;
-    const int b = blockIdx.z;
-    const int hv = blockIdx.y;
-    const int h = hv / p.group;
-    const int v0 = blockIdx.x * TV;
 
-    const int64_t r = ld_idx(p.ridx, b * p.ri_s, p.ri_dt);
-    const int64_t w = p.widx ? ld_idx(p.widx, b * p.wi_s, p.wi_dt) : r;
-    const bool rd = r >= 0 && r < p.P;
-    const bool wr = w >= 0 && w < p.P;
-    if (threadIdx.x == 0 && blockIdx.x == 0 && hv == 0 && p.dev_err) {
-        const int e = (r >= p.P ? LAR_DEVERR_READ_SLOT : 0) | (w >= p.P ? LAR_DEVERR_WRITE_SLOT : 0);
-        if (e) atomicOr(p.dev_err, e);
-    }
+    const int nvt = (V + TV - 1) / TV;
+    const int64_t total = static_cast<int64_t>(p.B) * p.HV * nvt;
+    const int64_t t_begin = blockIdx.x * total / gridDim.x;
+    const int64_t t_end = (blockIdx.x + 1) * total / gridDim.x;
 
-    // ---- state load: issued first so the preamble overlaps its latency
-    float4 s[NR][NCH];
+#if LAR_PDL
+    // programmatic dependent launch: everything below may read what the
+    // previous kernel on the stream wrote, so wait for it first; then let the
+    // next kernel's CTAs be scheduled as soon as ours retire.
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+#endif
+
+    // local row (within a tile) of this thread's i-th row
+    auto lrow = [&](int i) { return (warp * NR + i) * RPW + gi; };
+
+    // tile coordinates, advanced incrementally (no per-tile 64-bit division)
+    struct Pos {
+        int64_t tile;
+        int vt, hv, b;
+    };
+    auto advance = [&](Pos& q) {
+        ++q.tile;
+        if (++q.vt == nvt) {
+            q.vt = 0;
+            if (++q.hv == p.HV) {
+                q.hv = 0;
+                ++q.b;
+            }
+        }
+    };
+    Pos cur;
     {
-        const float* src = p.pool + (rd ? r : 0) * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1];
-#pragma unroll
-        for (int i = 0; i < NR; ++i) {
-            const int row = v0 + (warp * NR + i) * RPW + gi;
-            const bool ok = rd && row < p.V;
-            const float4* rp = reinterpret_cast<const float4*>(src + row * p.ps[2]) + j;
-#pragma unroll
-            for (int c = 0; c < NCH; ++c)
-                s[i][c] = ok ? __ldcs(rp + c * LPR) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        const int64_t u = t_begin / nvt;
+        cur.tile = t_begin;
+        cur.vt = static_cast<int>(t_begin - u * nvt);
+        cur.b = static_cast<int>(u / p.HV);
+        cur.hv = static_cast<int>(u - static_cast<int64_t>(cur.b) * p.HV);
     }
 
-    // ---- preamble: per-token vectors and scalars into shared memory
-    const bool gate_raw = (p.flags & LAR_GATE_RAW) != 0;
-    for (int i = threadIdx.x; i < T * K; i += NW * 32) {
-        const int t = i / K;
-        const int c = i - t * K;
-        sq[i] = ld_in(p.q, b * p.qs[0] + t * p.qs[1] + h * p.qs[2] + c * p.qs[3], p.q_dt);
-        sk[i] = ld_in(p.k, b * p.ks[0] + t * p.ks[1] + h * p.ks[2] + c * p.ks[3], p.k_dt);
-        if constexpr (FORM == FORM_KDA) {
-            float x = ld_in(p.g, b * p.gs[0] + t * p.gs[1] + hv * p.gs[2] + c * p.gs[3], p.g_dt);
-            if (gate_raw) {
-                const float bias =
-                    p.dt_bias ? p.dt_bias[(static_cast<int64_t>(hv) * K + c) * p.dtb_s] : 0.f;
-                x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
-            }
-            sd[i] = expf(x);
+    // read slot of a prefetch position, reloaded only when its batch entry changes
+    int ahead_b = -1;
+    int64_t ahead_r = -1;
+    auto slot_of = [&](const Pos& q) -> int64_t {
+        if (q.tile >= t_end) return -1;
+        if (q.b != ahead_b) {
+            ahead_b = q.b;
+            ahead_r = ld_idx(p.ridx, q.b * p.ri_s, p.ri_dt);
         }
-    }
-    for (int t = threadIdx.x; t < T; t += NW * 32) {
-        float bt = 0.f, dec = 1.f;
-        if constexpr (FORM != FORM_LA) {
-            bt = ld_in(p.beta, b * p.bs[0] + t * p.bs[1] + hv * p.bs[2], p.beta_dt);
-            if (p.flags & LAR_BETA_RAW) bt = 1.f / (1.f + expf(-bt));
-        }
-        if constexpr (FORM == FORM_GDN) {
-            float x = ld_in(p.g, b * p.gs[0] + t * p.gs[1] + hv * p.gs[2], p.g_dt);
-            if (gate_raw) {
-                const float bias = p.dt_bias ? p.dt_bias[hv * p.dtb_s] : 0.f;
-                x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
-            }
-            dec = expf(x);
-        } else if constexpr (FORM == FORM_LA) {
-            dec = p.decay[h * p.dec_s];
-        }
-        sc[t] = bt;
-        sc[T + t] = dec;
-    }
-    __syncthreads();
-    const bool l2 = FORM != FORM_LA && (p.flags & LAR_QK_L2NORM) != 0;
-    for (int t = warp; t < T; t += NW) {
-        float qq = 0.f, kk = 0.f, kq = 0.f;
-        for (int c = lane; c < K; c += 32) {
-            const float a = sq[t * K + c], bb = sk[t * K + c];
-            qq = fmaf(a, a, qq);
-            kk = fmaf(bb, bb, kk);
-            kq = fmaf(a, bb, kq);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            qq += __shfl_xor_sync(0xffffffffu, qq, off);
-            kk += __shfl_xor_sync(0xffffffffu, kk, off);
-            kq += __shfl_xor_sync(0xffffffffu, kq, off);
-        }
-        if (lane == 0) {
-            const float iq = l2 ? 1.f / sqrtf(qq + 1e-6f) : 1.f;
-            const float ik = l2 ? 1.f / sqrtf(kk + 1e-6f) : 1.f;
-            sc[2 * T + t] = iq;
-            sc[3 * T + t] = ik;
-            sc[4 * T + t] = kq * iq * ik;
-        }
-    }
-    __syncthreads();
+        return ahead_r;
+    };
 
-    // ---- token loop: the state never leaves registers between tokens
+    // issue this thread's copies of the tile at `q` (read slot r) into ring stage `st`
+    auto issue = [&](const Pos& q, int64_t r, int st) {
+        if (q.tile < t_end && r >= 0 && r < p.P) {
+            const float* src = p.pool + r * p.ps[0] + static_cast<int64_t>(q.hv) * p.ps[1];
+            float* dst = ring + static_cast<size_t>(st) * TV * K;
+#pragma unroll
+            for (int i = 0; i < NR; ++i) {
+                const int row = q.vt * TV + lrow(i);
+                if (row < V) {
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        const int k0 = (c * LPR + j) * 4;
+                        cp_async16(dst + lrow(i) * K + k0, src + row * p.ps[2] + k0);
+                    }
+                }
+            }
+        }
+        cp_async_commit();   // always commit, so group counting stays uniform
+    };
+
+    // ---- prologue: S-1 tiles in flight before the first is consumed
+    Pos ahead = cur;
+#pragma unroll
+    for (int s = 0; s < S - 1; ++s) {
+        issue(ahead, slot_of(ahead), s);
+        advance(ahead);
+    }
+
+    int buf = 1;
+    bool rd = false, wr = false;
+    float* dst_state = p.pool;              // state rows of the current pair (write slot)
+    int64_t v_off = 0, o_off = 0;           // per-pair offsets into v and out
+    float* inter_base = p.inter;
     const float scale = p.scale;
+    const bool gate_raw = (p.flags & LAR_GATE_RAW) != 0;
+    const bool l2 = FORM != FORM_LA && (p.flags & LAR_QK_L2NORM) != 0;
+
+    int stage = 0;                 // ring stage of the tile being consumed
+    int stage_next = S - 1;        // ring stage the next issue goes to
 #pragma unroll 1
-    for (int t = 0; t < T; ++t) {
-        const float bt = sc[t], dec = sc[T + t];
-        const float iq = sc[2 * T + t], ik = sc[3 * T + t], kq = sc[4 * T + t];
-        float4 kv[NCH], qv[NCH], dv[NCH];
+    for (; cur.tile < t_end; advance(cur)) {
+        // read slot of the tile issued at the end of this iteration
+        const int64_t r_ahead = slot_of(ahead);
+        const int b = cur.b, hv = cur.hv, vt = cur.vt;
+        if (vt == 0 || cur.tile == t_begin) {
+            // ---- new (b, hv) pair: slots, bases and per-token vectors
+            const int h = hv / p.group;
+            buf ^= 1;
+            const int64_t r = ld_idx(p.ridx, b * p.ri_s, p.ri_dt);
+            const int64_t w = p.widx ? ld_idx(p.widx, b * p.wi_s, p.wi_dt) : r;
+            rd = r >= 0 && r < p.P;
+            wr = w >= 0 && w < p.P;
+            if (threadIdx.x == 0 && hv == 0 && p.dev_err) {
+                const int e = (r >= p.P ? LAR_DEVERR_READ_SLOT : 0) | (w >= p.P ? LAR_DEVERR_WRITE_SLOT : 0);
+                if (e) atomicOr(p.dev_err, e);
+            }
+            dst_state = p.pool + (wr ? w : 0) * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1];
+            v_off = b * p.vs[0] + hv * p.vs[2];
+            o_off = b * p.os[0] + hv * p.os[2];
+            if (p.inter) inter_base = p.inter + b * p.is[0] + hv * p.is[2];
+
+            float* vb = vecs + buf * vstride;
+            const int64_t q_off = b * p.qs[0] + h * p.qs[2];
+            const int64_t k_off = b * p.ks[0] + h * p.ks[2];
+            for (int i = threadIdx.x; i < T * K; i += NW * 32) {
+                const int t = i / K;
+                const int c = i - t * K;
+                vb[i] = ld_in(p.q, q_off + t * p.qs[1] + c * p.qs[3], p.q_dt);
+                vb[o_k + i] = ld_in(p.k, k_off + t * p.ks[1] + c * p.ks[3], p.k_dt);
+                if constexpr (FORM == FORM_KDA) {
+                    float x = ld_in(p.g, b * p.gs[0] + t * p.gs[1] + hv * p.gs[2] + c * p.gs[3], p.g_dt);
+                    if (gate_raw) {
+                        const float bias =
+                            p.dt_bias ? p.dt_bias[(static_cast<int64_t>(hv) * K + c) * p.dtb_s] : 0.f;
+                        x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
+                    }
+                    vb[o_d + i] = expf(x);
+                }
+            }
+            if (sv_on) {
+                for (int i = threadIdx.x; i < T * V; i += NW * 32) {
+                    const int t = i / V;
+                    const int row = i - t * V;
+                    vb[o_v + i] = ld_in(p.v, v_off + t * p.vs[1] + row * p.vs[3], p.v_dt);
+                }
+            }
+            float* sc = vb + o_s;
+            for (int t = threadIdx.x; t < T; t += NW * 32) {
+                float bt = 0.f, dec = 1.f;
+                if constexpr (FORM != FORM_LA) {
+                    bt = ld_in(p.beta, b * p.bs[0] + t * p.bs[1] + hv * p.bs[2], p.beta_dt);
+                    if (p.flags & LAR_BETA_RAW) bt = 1.f / (1.f + expf(-bt));
+                }
+                if constexpr (FORM == FORM_GDN) {
+                    float x = ld_in(p.g, b * p.gs[0] + t * p.gs[1] + hv * p.gs[2], p.g_dt);
+                    if (gate_raw) {
+                        const float bias = p.dt_bias ? p.dt_bias[hv * p.dtb_s] : 0.f;
+                        x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
+                    }
+                    dec = expf(x);
+                } else if constexpr (FORM == FORM_LA) {
+                    dec = p.decay[h * p.dec_s];
+                }
+                sc[t] = bt;
+                sc[T + t] = dec;
+            }
+            __syncthreads();
+            for (int t = warp; t < T; t += NW) {
+                float qq = 0.f, kk = 0.f, kq = 0.f;
+                for (int c = lane; c < K; c += 32) {
+                    const float a = vb[t * K + c], bb = vb[o_k + t * K + c];
+                    qq = fmaf(a, a, qq);
+                    kk = fmaf(bb, bb, kk);
+                    kq = fmaf(a, bb, kq);
+                }
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-            const int kidx = (c * LPR + j) * 4;
-            const float4 a = *reinterpret_cast<const float4*>(sk + t * K + kidx);
-            const float4 bq = *reinterpret_cast<const float4*>(sq + t * K + kidx);
-            kv[c] = make_float4(a.x * ik, a.y * ik, a.z * ik, a.w * ik);
-            qv[c] = make_float4(bq.x * iq, bq.y * iq, bq.z * iq, bq.w * iq);
-            if constexpr (FORM == FORM_KDA) dv[c] = *reinterpret_cast<const float4*>(sd + t * K + kidx);
+                for (int off = 16; off > 0; off >>= 1) {
+                    qq += __shfl_xor_sync(0xffffffffu, qq, off);
+                    kk += __shfl_xor_sync(0xffffffffu, kk, off);
+                    kq += __shfl_xor_sync(0xffffffffu, kq, off);
+                }
+                if (lane == 0) {
+                    const float iq = l2 ? 1.f / sqrtf(qq + 1e-6f) : 1.f;
+                    const float ik = l2 ? 1.f / sqrtf(kk + 1e-6f) : 1.f;
+                    sc[2 * T + t] = iq;
+                    sc[3 * T + t] = ik;
+                    sc[4 * T + t] = kq * iq * ik;
+                }
+            }
+            __syncthreads();
         }
+
+        // ---- this thread's copies of the tile have landed: pull its rows into registers
+        cp_async_wait<S - 2>();
+        float4 s[NR][NCH];
+        {
+            const float* src = ring + static_cast<size_t>(stage) * TV * K;
 #pragma unroll
-        for (int i = 0; i < NR; ++i) {
-            const int row = v0 + (warp * NR + i) * RPW + gi;
-            const bool rv = row < p.V;
-            const float vval =
-                rv ? ld_in(p.v, b * p.vs[0] + t * p.vs[1] + hv * p.vs[2] + row * p.vs[3], p.v_dt) : 0.f;
+            for (int i = 0; i < NR; ++i) {
+                const bool ok = rd && vt * TV + lrow(i) < V;
+#pragma unroll
+                for (int c = 0; c < NCH; ++c)
+                    s[i][c] = ok ? *reinterpret_cast<const float4*>(src + lrow(i) * K + (c * LPR + j) * 4)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        // refill the stage consumed in the previous iteration (its rows were used long ago)
+        issue(ahead, r_ahead, stage_next);
+        advance(ahead);
+        stage = stage + 1 == S ? 0 : stage + 1;
+        stage_next = stage_next + 1 == S ? 0 : stage_next + 1;
+
+        // ---- token loop: the state never leaves registers between tokens
+        const float* vb = vecs + buf * vstride;
+        const float* sc = vb + o_s;
+#pragma unroll 1
+        for (int t = 0; t < T; ++t) {
+            const float bt = sc[t], dec = sc[T + t];
+            const float iq = sc[2 * T + t], ik = sc[3 * T + t], kq = sc[4 * T + t];
+            float4 kv[NCH], qv[NCH], dv[NCH];
 #pragma unroll
             for (int c = 0; c < NCH; ++c) {
-                if constexpr (FORM == FORM_KDA) {
-                    s[i][c].x *= dv[c].x; s[i][c].y *= dv[c].y;
-                    s[i][c].z *= dv[c].z; s[i][c].w *= dv[c].w;
-                } else {
-                    s[i][c].x *= dec; s[i][c].y *= dec; s[i][c].z *= dec; s[i][c].w *= dec;
-                }
+                const int kidx = t * K + (c * LPR + j) * 4;
+                qv[c] = *reinterpret_cast<const float4*>(vb + kidx);
+                kv[c] = *reinterpret_cast<const float4*>(vb + o_k + kidx);
+                if constexpr (FORM == FORM_KDA) dv[c] = *reinterpret_cast<const float4*>(vb + o_d + kidx);
             }
-            float o;
-            if constexpr (FORM == FORM_LA) {
-                float pp = 0.f;
 #pragma unroll
-                for (int c = 0; c < NCH; ++c) pp = dot4(s[i][c], qv[c], pp);
-                pp = group_sum<LPR>(pp);
-#pragma unroll
-                for (int c = 0; c < NCH; ++c) axpy4(s[i][c], vval, kv[c]);
-                o = fmaf(vval, kq, pp);
-            } else {
-                float u = 0.f, pp = 0.f;
+            for (int i = 0; i < NR; ++i) {
+                const int row = vt * TV + lrow(i);
+                const bool rv = row < V;
+                float vval = 0.f;
+                if (rv) vval = sv_on ? vb[o_v + t * V + row] : ld_in(p.v, v_off + t * p.vs[1] + row * p.vs[3], p.v_dt);
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
-                    u = dot4(s[i][c], kv[c], u);
-                    pp = dot4(s[i][c], qv[c], pp);
+                    if constexpr (FORM == FORM_KDA) {
+                        s[i][c].x *= dv[c].x; s[i][c].y *= dv[c].y;
+                        s[i][c].z *= dv[c].z; s[i][c].w *= dv[c].w;
+                    } else {
+                        s[i][c].x *= dec; s[i][c].y *= dec; s[i][c].z *= dec; s[i][c].w *= dec;
+                    }
                 }
+                // q_hat = iq q and k_hat = ik k: the norms scale the reduced sums
+                float o;
+                if constexpr (FORM == FORM_LA) {
+                    float pp = 0.f;
 #pragma unroll
-                for (int off = LPR / 2; off > 0; off >>= 1) {
-                    u += __shfl_xor_sync(0xffffffffu, u, off);
-                    pp += __shfl_xor_sync(0xffffffffu, pp, off);
+                    for (int c = 0; c < NCH; ++c) pp = dot4(s[i][c], qv[c], pp);
+#pragma unroll
+                    for (int off = LPR / 2; off > 0; off >>= 1) pp += __shfl_xor_sync(0xffffffffu, pp, off);
+                    const float a = vval * ik;
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) axpy4(s[i][c], a, kv[c]);
+                    o = fmaf(vval, kq, pp * iq);
+                } else {
+                    float uu = 0.f, pp = 0.f;
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        uu = dot4(s[i][c], kv[c], uu);
+                        pp = dot4(s[i][c], qv[c], pp);
+                    }
+#pragma unroll
+                    for (int off = LPR / 2; off > 0; off >>= 1) {
+                        uu += __shfl_xor_sync(0xffffffffu, uu, off);
+                        pp += __shfl_xor_sync(0xffffffffu, pp, off);
+                    }
+                    const float delta = bt * (vval - uu * ik);
+                    const float a = delta * ik;
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) axpy4(s[i][c], a, kv[c]);
+                    o = fmaf(delta, kq, pp * iq);
                 }
-                const float delta = bt * (vval - u);
+                if (j == 0 && rv)
+                    st_out(p.out, o_off + t * p.os[1] + row * p.os[3], p.out_dt, o * scale);
+                if (p.inter != nullptr && rv) {
+                    float4* ip = reinterpret_cast<float4*>(inter_base + t * p.is[1] + row * p.is[3]) + j;
 #pragma unroll
-                for (int c = 0; c < NCH; ++c) axpy4(s[i][c], delta, kv[c]);
-                o = fmaf(delta, kq, pp);
-            }
-            if (j == 0 && rv)
-                st_out(p.out, b * p.os[0] + t * p.os[1] + hv * p.os[2] + row * p.os[3], p.out_dt, o * scale);
-            if (p.inter != nullptr && rv) {
-                float4* ip = reinterpret_cast<float4*>(p.inter + b * p.is[0] + t * p.is[1] +
-                                                       hv * p.is[2] + row * p.is[3]) + j;
-#pragma unroll
-                for (int c = 0; c < NCH; ++c) __stcs(ip + c * LPR, s[i][c]);
+                    for (int c = 0; c < NCH; ++c) __stcs(ip + c * LPR, s[i][c]);
+                }
             }
         }
-    }
 
-    // ---- writeback to the write slot (skipped for negative / out-of-range slots)
-    if (wr) {
-        float* dst = p.pool + w * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1];
+        // ---- writeback to the write slot (skipped for negative / out-of-range slots)
+        if (wr) {
 #pragma unroll
-        for (int i = 0; i < NR; ++i) {
-            const int row = v0 + (warp * NR + i) * RPW + gi;
-            if (row < p.V) {
-                float4* wp = reinterpret_cast<float4*>(dst + row * p.ps[2]) + j;
+            for (int i = 0; i < NR; ++i) {
+                const int row = vt * TV + lrow(i);
+                if (row < V) {
+                    float4* wp = reinterpret_cast<float4*>(dst_state + row * p.ps[2]) + j;
 #pragma unroll
-                for (int c = 0; c < NCH; ++c) __stcs(wp + c * LPR, s[i][c]);
+                    for (int c = 0; c < NCH; ++c) __stcs(wp + c * LPR, s[i][c]);
+                }
             }
         }
     }
+    cp_async_wait<0>();   // nothing may be left in flight into shared memory at exit
 }
 
-template <int FORM, int K, int LPR, int NR, int NW>
+// Resident CTAs per SM for a kernel instance and shared-memory size, looked up
+// once per (device, size) and cached.
+int cached_occupancy(const void* kern, int threads, size_t smem, size_t smem_max, int* sms_out);
+
+template <int FORM, int K, int LPR, int NR, int NW, int S>
 lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
-    constexpr int TV = NW * NR * (32 / LPR);
-    const dim3 grid(static_cast<unsigned>((p.V + TV - 1) / TV), static_cast<unsigned>(p.HV),
-                    static_cast<unsigned>(p.B));
-    const size_t smem = decode_smem_bytes<FORM, K>(p.T);
-    decode_kernel<FORM, K, LPR, NR, NW><<<grid, NW * 32, smem, stream>>>(p);
+    using G = Tile<K, LPR, NR, NW>;
+    auto kern = decode_kernel<FORM, K, LPR, NR, NW, S>;
+    const size_t smem = decode_smem_bytes<FORM, K, LPR, NR, NW, S>(p.T, p.V);
+    // the largest footprint any call can ask for (T = 16 with staged v)
+    constexpr size_t smem_max = decode_smem_bytes<FORM, K, LPR, NR, NW, S>(16, kStageVMax / 16);
+    int sms = 0;
+    const int occ = cached_occupancy(reinterpret_cast<const void*>(kern), NW * 32, smem, smem_max, &sms);
+    if (occ < 1) return LAR_ERR_LAUNCH;
+    const int nvt = (p.V + G::TV - 1) / G::TV;
+    const int64_t tiles = static_cast<int64_t>(p.B) * p.HV * nvt;
+    const int64_t cap = static_cast<int64_t>(sms) * occ;
+    const int64_t grid = tiles < cap ? tiles : cap;
+#if LAR_PDL
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(NW * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? LAR_OK : LAR_ERR_LAUNCH;
+#else
+    kern<<<static_cast<unsigned>(grid), NW * 32, smem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? LAR_OK : LAR_ERR_LAUNCH;
+#endif
 }
 
 // Tile shapes per key size: 8 lanes per 512-byte row at K = 128 (one full line
-// per lane group per instruction), 32 rows per CTA of 4 warps.
+// per lane group per instruction), 32-row tiles (16 KB), a 2-stage ring (one
+// tile in flight while one is computed; four CTAs per SM keep ~64 KB of state
+// loads in flight per SM).
 template <int FORM>
 lar_status launch_form(const DecodeParams& p, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (p.K) {
-        case 16: return launch_tile<FORM, 16, 4, 2, 2>(p, st);
-        case 32: return launch_tile<FORM, 32, 8, 2, 4>(p, st);
-        case 64: return launch_tile<FORM, 64, 8, 2, 4>(p, st);
-        case 128: return launch_tile<FORM, 128, 8, 2, 4>(p, st);
+        case 16: return launch_tile<FORM, 16, 4, 2, 2, 3>(p, st);
+        case 32: return launch_tile<FORM, 32, 8, 2, 4, 3>(p, st);
+        case 64: return launch_tile<FORM, 64, 8, 2, 4, 3>(p, st);
+        case 128: return launch_tile<FORM, 128, 8, LAR_K128_NR, LAR_K128_NW, LAR_K128_S>(p, st);
         default: return LAR_ERR_SHAPE;
     }
 }
