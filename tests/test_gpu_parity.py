@@ -43,6 +43,12 @@ SWEEP = {
                                    separate_write=True, skip_frac=0.34)),
     "la_f32_k16": ("la", dict(B=2, T=2, H=2, K=16, V=24, in_dtype=F32, out_dtype=F32,
                               flat_pool=True)),
+    # T * V > 4096: v is read from global memory in the token loop instead of staged
+    "gdn_unstaged_v": ("gdn", dict(B=2, T=16, H=1, HV=2, K=64, V=300, cache_intermediate=True)),
+    "kda_unstaged_v": ("kda", dict(B=2, T=9, H=1, HV=1, K=128, V=520, raw_gates=True)),
+    "la_unstaged_v": ("la", dict(B=2, T=11, H=2, K=32, V=400, separate_write=True)),
+    "kda_t16_gqa": ("kda", dict(B=3, T=16, H=2, HV=4, K=128, V=64, raw_gates=True,
+                                cache_intermediate=True)),
 }
 
 
