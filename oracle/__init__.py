@@ -8,8 +8,9 @@ use and calls through ctypes.
 
 Every input other than the pool is widened exactly to a contiguous fp64 array
 (bf16 -> fp32 -> fp64 loses nothing).  The pool is a float32 CPU tensor (or
-numpy array), possibly a strided view of a larger backing buffer, and is
-updated IN PLACE through its own strides, exactly as the writeback rule of
+numpy array) or a bfloat16 CPU tensor, possibly a strided view of a larger
+backing buffer, and is updated IN PLACE through its own strides (bf16 written
+back rounded to nearest even straight from fp64), exactly as the writeback rule of
 the flashinfer "fp32 sibling of #3268" page asks.
 
 Functions return a dict with
@@ -52,17 +53,19 @@ def _load():
             build()
             lib = ctypes.CDLL(_LIB)
             dp = ctypes.POINTER(ctypes.c_double)
-            fp = ctypes.POINTER(ctypes.c_float)
             ip = ctypes.POINTER(ctypes.c_int64)
             i64 = ctypes.c_int64
+            vp = ctypes.c_void_p
             for name in ("oracle_gdn_decode", "oracle_kda_decode"):
                 fn = getattr(lib, name)
                 fn.restype = ctypes.c_long
                 fn.argtypes = [i64] * 6 + [dp] * 7 + [ctypes.c_int] * 3 + [
-                    ctypes.c_double, fp, i64, ip, ip, ip, dp, dp, dp]
+                    ctypes.c_double, vp, ctypes.c_int, i64, ip, ip, ip, dp, dp, dp]
             lib.oracle_la_decode.restype = ctypes.c_long
             lib.oracle_la_decode.argtypes = [i64] * 5 + [dp] * 4 + [
-                ctypes.c_double, fp, i64, ip, ip, ip, dp, dp, dp]
+                ctypes.c_double, vp, ctypes.c_int, i64, ip, ip, ip, dp, dp, dp]
+            lib.oracle_round_bf16.restype = ctypes.c_uint16
+            lib.oracle_round_bf16.argtypes = [ctypes.c_double]
             _lib = lib
     return _lib
 
@@ -91,21 +94,36 @@ def _ptr(a, ctype):
 
 
 def _pool_view(pool):
-    """float32 numpy view that shares memory with `pool` (writes land in it)."""
+    """numpy view sharing memory with `pool` (writes land in it): float32, or
+    the raw 16-bit patterns of a bfloat16 pool.  Returns (array, address,
+    element strides, is_bf16)."""
+    bf16 = False
     if hasattr(pool, "detach"):
-        if pool.device.type != "cpu" or str(pool.dtype) != "torch.float32":
-            raise TypeError("oracle pool must be a float32 CPU tensor")
-        arr = pool.detach().numpy()
+        if pool.device.type != "cpu":
+            raise TypeError("oracle pool must be a CPU tensor")
+        if str(pool.dtype) == "torch.bfloat16":
+            bf16 = True
+            import torch
+            arr = pool.detach().view(torch.int16).numpy()
+        elif str(pool.dtype) == "torch.float32":
+            arr = pool.detach().numpy()
+        else:
+            raise TypeError("oracle pool must be float32 or bfloat16")
     else:
         arr = pool
-    if arr.dtype != np.float32:
-        raise TypeError("oracle pool must be float32")
-    if any(s % 4 for s in arr.strides):
+        if arr.dtype != np.float32:
+            raise TypeError("oracle pool arrays must be float32")
+    es = arr.dtype.itemsize
+    if any(s % es for s in arr.strides):
         raise ValueError("pool strides must be whole elements")
-    strides = np.array([s // 4 for s in arr.strides], dtype=np.int64)
-    # ctypes pointer at the view's first element (numpy handles the offset)
-    base = arr.__array_interface__["data"][0]
-    return arr, ctypes.cast(base, ctypes.POINTER(ctypes.c_float)), strides
+    strides = np.array([s // es for s in arr.strides], dtype=np.int64)
+    # address of the view's first element (numpy handles the offset)
+    return arr, arr.__array_interface__["data"][0], strides, bf16
+
+
+def round_bf16(x: float) -> int:
+    """Bit pattern of the bfloat16 nearest to x (ties to even), as the oracle stores it."""
+    return int(_load().oracle_round_bf16(float(x)))
 
 
 def _as_btxk(x, name):
@@ -138,7 +156,7 @@ def _delta(per_channel, q, k, v, g, beta, pool, read_idx, write_idx, A_log, dt_b
     HV, V = v.shape[2], v.shape[3]
     if k.shape != q.shape or v.shape[:2] != (B, T):
         raise ValueError("q/k/v shapes disagree")
-    arr, pptr, st = _pool_view(pool)
+    arr, pptr, st, pbf = _pool_view(pool)
     if arr.ndim == 3:  # flat [P*HV, V, K]: one slot spans HV consecutive rows
         if arr.shape[0] % HV:
             raise ValueError("flat pool rows must be a multiple of HV")
@@ -159,7 +177,7 @@ def _delta(per_channel, q, k, v, g, beta, pool, read_idx, write_idx, A_log, dt_b
     dp = ctypes.c_double
     bad = fn(B, T, H, HV, K, V, _ptr(q, dp), _ptr(k, dp), _ptr(v, dp), _ptr(g, dp),
              _ptr(beta, dp), _ptr(A, dp), _ptr(D, dp), int(qk_l2norm), int(gate_raw),
-             int(beta_raw), float(scale), pptr, P, _ptr(st, ctypes.c_int64),
+             int(beta_raw), float(scale), pptr, int(pbf), P, _ptr(st, ctypes.c_int64),
              _ptr(ri, ctypes.c_int64), _ptr(wi, ctypes.c_int64), _ptr(out, dp),
              _ptr(fin, dp), _ptr(inter, dp))
     if bad < 0:
@@ -195,7 +213,7 @@ def la_decode(q, k, v, decay, pool, read_idx, write_idx=None, *, scale=1.0,
     V = v.shape[3]
     if k.shape != q.shape or v.shape[:3] != (B, T, H) or lam.shape != (H,):
         raise ValueError("q/k/v/decay shapes disagree")
-    arr, pptr, st = _pool_view(pool)
+    arr, pptr, st, pbf = _pool_view(pool)
     if arr.ndim == 4:  # [P,H,V,K] is only valid as a flat [P*H,V,K] view
         if st[0] != st[1] * H:
             raise ValueError("4D LA pool must have slot stride == H * head stride")
@@ -212,7 +230,7 @@ def la_decode(q, k, v, decay, pool, read_idx, write_idx=None, *, scale=1.0,
     inter = np.zeros((B, T, H, V, K)) if cache_intermediate else None
     dp = ctypes.c_double
     bad = lib.oracle_la_decode(B, T, H, K, V, _ptr(q, dp), _ptr(k, dp), _ptr(v, dp),
-                               _ptr(lam, dp), float(scale), pptr, rows,
+                               _ptr(lam, dp), float(scale), pptr, int(pbf), rows,
                                _ptr(st, ctypes.c_int64), _ptr(ri, ctypes.c_int64),
                                _ptr(wi, ctypes.c_int64), _ptr(out, dp), _ptr(fin, dp),
                                _ptr(inter, dp))

@@ -41,8 +41,10 @@
  *  - o is multiplied by `scale` (1.0 unless a caller asks otherwise).
  *
  * Every input except the pool arrives as a contiguous fp64 array (the Python
- * wrapper widens bf16/fp32 exactly).  The pool is fp32, read and written in
- * place through four element strides (slot, hv, v, k), so strided views of a
+ * wrapper widens bf16/fp32 exactly).  The pool is fp32 or bfloat16 (flag
+ * pool_bf16; values are widened exactly on read and rounded to nearest even
+ * on write), read and written in place through four element strides (slot,
+ * hv, v, k), so strided views of a
  * larger backing buffer are handled the way the pages require.  All reads of
  * the pool happen before any write (phase 1 / phase 2), so every entry sees
  * the pool as it was when the call started.
@@ -56,16 +58,60 @@ static double softplus(double x) { return x > 20.0 ? x : log1p(exp(x)); }
 
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 
-/* Widened pool element S[k][v] of slot p, head hv. */
-static double pool_get(const float* pool, const int64_t* st, int64_t p, int64_t hv,
-                       int64_t vv, int64_t kk) {
-    return (double)pool[p * st[0] + hv * st[1] + vv * st[2] + kk * st[3]];
+/*
+ * bfloat16: the upper 16 bits of an IEEE fp32 (sign, 8 exponent bits, 7 stored
+ * fraction bits, i.e. 8 significant bits).  oracle_round_bf16 rounds an fp64
+ * value straight to the nearest bfloat16, ties to even (one rounding, not via
+ * fp32), and returns its bit pattern.
+ */
+uint16_t oracle_round_bf16(double x) {
+    if (isnan(x)) return 0x7FC0;
+    const uint16_t sign = signbit(x) ? 0x8000 : 0;
+    const double ax = fabs(x);
+    double q;                               /* spacing of bfloat16 values around ax */
+    if (ax >= 0x1p-126) {
+        int e;
+        frexp(ax, &e);                      /* ax = m 2^e, m in [0.5, 1) */
+        q = ldexp(1.0, e - 8);
+    } else {
+        q = 0x1p-133;                       /* subnormal spacing: 2^-126 / 2^7 */
+    }
+    const double r = nearbyint(ax / q) * q; /* ax / q is exact; ties to even */
+    if (r >= 0x1p128) return sign | 0x7F80; /* overflow to infinity */
+    const float f = (float)r;               /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return sign | (uint16_t)(u >> 16);
 }
 
-static void pool_put(float* pool, const int64_t* st, int64_t p, int64_t hv, int64_t vv,
-                     int64_t kk, double x) {
-    /* fp64 -> fp32 conversion rounds to nearest even under the default mode. */
-    pool[p * st[0] + hv * st[1] + vv * st[2] + kk * st[3]] = (float)x;
+static double bf16_value(uint16_t b) {
+    const uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Pool element at element offset `off`, widened; pool_bf16 selects the storage type. */
+static double elem_get(const void* pool, int pool_bf16, int64_t off) {
+    if (pool_bf16) return bf16_value(((const uint16_t*)pool)[off]);
+    return (double)((const float*)pool)[off];
+}
+
+/* Store x rounded to the pool's type (nearest, ties to even). */
+static void elem_put(void* pool, int pool_bf16, int64_t off, double x) {
+    if (pool_bf16) ((uint16_t*)pool)[off] = oracle_round_bf16(x);
+    else ((float*)pool)[off] = (float)x;    /* fp64 -> fp32 rounds to nearest even */
+}
+
+/* Widened pool element S[k][v] of slot p, head hv. */
+static double pool_get(const void* pool, int pool_bf16, const int64_t* st, int64_t p, int64_t hv,
+                       int64_t vv, int64_t kk) {
+    return elem_get(pool, pool_bf16, p * st[0] + hv * st[1] + vv * st[2] + kk * st[3]);
+}
+
+static void pool_put(void* pool, int pool_bf16, const int64_t* st, int64_t p, int64_t hv,
+                     int64_t vv, int64_t kk, double x) {
+    elem_put(pool, pool_bf16, p * st[0] + hv * st[1] + vv * st[2] + kk * st[3], x);
 }
 
 /*
@@ -77,7 +123,7 @@ static void pool_put(float* pool, const int64_t* st, int64_t p, int64_t hv, int6
  *   beta    [B,T,HV]                       (or raw logit if beta_raw)
  *   A_log   [HV]            required when gate_raw
  *   dt_bias GDN [HV]; KDA [HV*K]; may be NULL (zero) when gate_raw
- *   pool    fp32, strides st[4] in elements over (slot, hv, v, k), P slots
+ *   pool    fp32 or bf16 (pool_bf16), strides st[4] in elements over (slot, hv, v, k), P slots
  *   read_idx, write_idx [B] (write_idx NULL: write to the read slot)
  *   out     [B,T,HV,V]
  *   final_state [B,HV,V,K] or NULL: the state after the last token (storage order)
@@ -89,7 +135,7 @@ static long delta_rule(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, i
                        int per_channel, const double* q, const double* k, const double* v,
                        const double* g, const double* beta, const double* A_log,
                        const double* dt_bias, int qk_l2norm, int gate_raw, int beta_raw,
-                       double scale, float* pool, int64_t P, const int64_t* st,
+                       double scale, void* pool, int pool_bf16, int64_t P, const int64_t* st,
                        const int64_t* read_idx, const int64_t* write_idx, double* out,
                        double* final_state, double* inter) {
     if (B < 0 || T < 1 || H < 1 || HV < 1 || K < 1 || V < 1 || HV % H != 0) return -1;
@@ -117,7 +163,7 @@ static long delta_rule(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, i
 
             for (int64_t kk = 0; kk < K; ++kk)
                 for (int64_t vv = 0; vv < V; ++vv)
-                    S[kk * V + vv] = (r >= 0 && r < P) ? pool_get(pool, st, r, hv, vv, kk) : 0.0;
+                    S[kk * V + vv] = (r >= 0 && r < P) ? pool_get(pool, pool_bf16, st, r, hv, vv, kk) : 0.0;
 
             for (int64_t t = 0; t < T; ++t) {
                 const double* qt = q + ((b * T + t) * H + h) * K;
@@ -188,7 +234,7 @@ static long delta_rule(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, i
         for (int64_t hv = 0; hv < HV; ++hv) {
             const double* f = fin + ((b * HV + hv) * V) * K;
             for (int64_t vv = 0; vv < V; ++vv)
-                for (int64_t kk = 0; kk < K; ++kk) pool_put(pool, st, w, hv, vv, kk, f[vv * K + kk]);
+                for (int64_t kk = 0; kk < K; ++kk) pool_put(pool, pool_bf16, st, w, hv, vv, kk, f[vv * K + kk]);
         }
     }
 
@@ -200,24 +246,24 @@ static long delta_rule(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, i
 long oracle_gdn_decode(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V,
                        const double* q, const double* k, const double* v, const double* g,
                        const double* beta, const double* A_log, const double* dt_bias,
-                       int qk_l2norm, int gate_raw, int beta_raw, double scale, float* pool,
-                       int64_t P, const int64_t* pool_strides, const int64_t* read_idx,
+                       int qk_l2norm, int gate_raw, int beta_raw, double scale, void* pool,
+                       int pool_bf16, int64_t P, const int64_t* pool_strides, const int64_t* read_idx,
                        const int64_t* write_idx, double* out, double* final_state,
                        double* inter) {
     return delta_rule(B, T, H, HV, K, V, 0, q, k, v, g, beta, A_log, dt_bias, qk_l2norm,
-                      gate_raw, beta_raw, scale, pool, P, pool_strides, read_idx, write_idx,
+                      gate_raw, beta_raw, scale, pool, pool_bf16, P, pool_strides, read_idx, write_idx,
                       out, final_state, inter);
 }
 
 long oracle_kda_decode(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V,
                        const double* q, const double* k, const double* v, const double* g,
                        const double* beta, const double* A_log, const double* dt_bias,
-                       int qk_l2norm, int gate_raw, int beta_raw, double scale, float* pool,
-                       int64_t P, const int64_t* pool_strides, const int64_t* read_idx,
+                       int qk_l2norm, int gate_raw, int beta_raw, double scale, void* pool,
+                       int pool_bf16, int64_t P, const int64_t* pool_strides, const int64_t* read_idx,
                        const int64_t* write_idx, double* out, double* final_state,
                        double* inter) {
     return delta_rule(B, T, H, HV, K, V, 1, q, k, v, g, beta, A_log, dt_bias, qk_l2norm,
-                      gate_raw, beta_raw, scale, pool, P, pool_strides, read_idx, write_idx,
+                      gate_raw, beta_raw, scale, pool, pool_bf16, P, pool_strides, read_idx, write_idx,
                       out, final_state, inter);
 }
 
@@ -225,7 +271,7 @@ long oracle_kda_decode(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, i
  * Lightning-Attention decode (no delta term), cuLA PR #75 layout.
  *
  *   q, k   [B,T,H,K];  v [B,T,H,V];  decay [H] = lambda_h
- *   pool   fp32 [P*H, V, K] with element strides st[3] over (row, v, k);
+ *   pool   fp32 or bf16 (pool_bf16) [P*H, V, K], element strides st[3] over (row, v, k);
  *          the state of (entry b, head h) is row read_idx[b] * H + h.
  *   out    [B,T,H,V];  final_state [B,H,V,K] or NULL;  inter [B,T,H,V,K] or NULL
  *
@@ -234,7 +280,7 @@ long oracle_kda_decode(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, i
  */
 long oracle_la_decode(int64_t B, int64_t T, int64_t H, int64_t K, int64_t V, const double* q,
                       const double* k, const double* v, const double* decay, double scale,
-                      float* pool, int64_t pool_rows, const int64_t* st,
+                      void* pool, int pool_bf16, int64_t pool_rows, const int64_t* st,
                       const int64_t* read_idx, const int64_t* write_idx, double* out,
                       double* final_state, double* inter) {
     if (B < 0 || T < 1 || H < 1 || K < 1 || V < 1 || pool_rows % H != 0) return -1;
@@ -255,7 +301,7 @@ long oracle_la_decode(int64_t B, int64_t T, int64_t H, int64_t K, int64_t V, con
             for (int64_t kk = 0; kk < K; ++kk)
                 for (int64_t vv = 0; vv < V; ++vv)
                     S[kk * V + vv] = (r >= 0 && r < P)
-                        ? (double)pool[row * st[0] + vv * st[1] + kk * st[2]] : 0.0;
+                        ? elem_get(pool, pool_bf16, row * st[0] + vv * st[1] + kk * st[2]) : 0.0;
 
             const double lam = decay[h];
             for (int64_t t = 0; t < T; ++t) {
@@ -291,7 +337,7 @@ long oracle_la_decode(int64_t B, int64_t T, int64_t H, int64_t K, int64_t V, con
             const double* f = fin + ((b * H + h) * V) * K;
             for (int64_t vv = 0; vv < V; ++vv)
                 for (int64_t kk = 0; kk < K; ++kk)
-                    pool[row * st[0] + vv * st[1] + kk * st[2]] = (float)f[vv * K + kk];
+                    elem_put(pool, pool_bf16, row * st[0] + vv * st[1] + kk * st[2], f[vv * K + kk]);
         }
     }
     free(S);

@@ -394,3 +394,66 @@ def test_out_of_range_slots_are_counted_and_skipped():
     assert np.array_equal(res["out"][0], zero["out"][0])
     others = [p for p in range(P) if p != 2]
     assert torch.equal(pool[others], before[others])
+
+
+# --------------------------------------------------------------------------- bfloat16 pool
+
+def _bf16_bits(x32: torch.Tensor) -> list:
+    return (x32.to(torch.bfloat16).view(torch.int16).to(torch.int32) & 0xFFFF).tolist()
+
+
+def test_round_bf16_matches_torch():
+    """The oracle's fp64 -> bf16 rounding against torch's fp32 -> bf16 (round to
+    nearest even) on values exactly representable in fp32, so both see one rounding."""
+    gen = torch.Generator().manual_seed(21)
+    vals = torch.randn(4000, generator=gen) * torch.exp2(torch.randint(-40, 40, (4000,), generator=gen).float())
+    special = torch.tensor([0.0, -0.0, 1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 1 - 2 ** -9,
+                            2 ** -130, 3 * 2 ** -134, 1e-40, -1e-42, 3.0e38, 3.4028234e38, -3.4028234e38,
+                            65504.0, 0.1, -0.3], dtype=torch.float32)
+    x = torch.cat([vals, special])
+    got = [oracle.round_bf16(float(v)) for v in x.tolist()]
+    assert got == _bf16_bits(x)
+
+
+def test_bf16_pool_reads_exactly_and_writes_nearest():
+    """A bf16 pool gives the same fp64 results as an fp32 pool holding the
+    widened values; the written slots hold the bf16 nearest to the fp64 state."""
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(True, seed=13)
+    pb = pool.to(torch.bfloat16)
+    pf = pb.float()
+    a = oracle.kda_decode(q, k, v, g, beta, pb, ri, wi, cache_intermediate=True)
+    b = oracle.kda_decode(q, k, v, g, beta, pf, ri, wi, cache_intermediate=True)
+    for key in ("out", "final_state", "inter"):
+        assert np.array_equal(a[key], b[key])
+    for bidx, w in ((0, 4), (1, 6)):
+        x = a["final_state"][bidx]
+        got = pb[w].double().numpy()
+        # nearest: no other bf16 value is closer (the two neighbours of `got`)
+        bits = pb[w].view(torch.int16).to(torch.int32) & 0xFFFF
+        up = (bits + 1).to(torch.int16).view(torch.bfloat16).double().numpy()
+        dn = (bits - 1).to(torch.int16).view(torch.bfloat16).double().numpy()
+        err = np.abs(got - x)
+        assert (err <= np.abs(up - x)).all() and (err <= np.abs(dn - x)).all()
+    untouched = [p for p in range(pb.shape[0]) if p not in (4, 6)]
+    assert torch.equal(pb[untouched], pool.to(torch.bfloat16)[untouched])
+
+
+def test_bf16_la_flat_pool():
+    gen = torch.Generator().manual_seed(3)
+    B, H, K, V, P = 2, 2, 8, 4, 3
+    q = torch.randn(B, H, K, generator=gen, dtype=torch.float64)
+    k = torch.randn(B, H, K, generator=gen, dtype=torch.float64)
+    v = torch.randn(B, H, V, generator=gen, dtype=torch.float64)
+    lam = torch.tensor([0.5, 0.75], dtype=torch.float64)
+    pb = torch.randn(P * H, V, K, generator=gen).to(torch.bfloat16)
+    pf = pb.float()
+    ri = torch.tensor([2, 0])
+    a = oracle.la_decode(q, k, v, lam, pb, ri)
+    b = oracle.la_decode(q, k, v, lam, pf, ri)
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["final_state"], b["final_state"])
+    for bi in range(B):
+        for h in range(H):
+            row = int(ri[bi]) * H + h
+            exp = [oracle.round_bf16(x) for x in a["final_state"][bi, h].ravel().tolist()]
+            got = (pb[row].view(torch.int16).to(torch.int32) & 0xFFFF).ravel().tolist()
+            assert got == exp
