@@ -43,6 +43,7 @@ FALLBACK_HBM_GBS = 6800.0
 DESCRIPTIONS = {
     "gdn_tiny": "GDN decode B=2 T=1 H=HV=2 K=V=16 fp32",
     "gdn_b64": "GDN decode B=64 T=1 H=16 HV=32 K=V=128, bf16 q/k/v/out, fp32 pool [256,32,128,128]",
+    "gdn_b64_bf16": "GDN decode B=64 T=1 H=16 HV=32 K=V=128, bf16 q/k/v/out, bf16 pool [256,32,128,128]",
     "gdn_mtp_strided": "GDN MTP B=16 T=4 H=16 HV=32 K=V=128, pool = backing[::2] of [256,32,128,128], "
                        "separate write slots (25% -1), all T states cached",
     "kda_b256": "KDA decode B=256 T=1 H=HV=24 K=V=128, in-kernel gate/l2norm/sigmoid, pool [320,24,128,128]",
@@ -226,7 +227,7 @@ def run_lar(args, world, rank, local):
     with torch.cuda.stream(stream):
         for ri, wi in sets:
             out = torch.empty(w.v.shape, dtype=w.out_dtype, device=dev)
-            inter = (torch.empty(w.B, w.T, w.HV, w.V, w.K, device=dev)
+            inter = (torch.empty(w.B, w.T, w.HV, w.V, w.K, device=dev, dtype=w.inter_dtype)
                      if w.cache_intermediate else None)
             kw = dict(d, read_idx=ri.to(dev), write_idx=None if wi is None else wi.to(dev),
                       out=out, inter=inter)
@@ -287,7 +288,7 @@ def run_lar(args, world, rank, local):
         "config": {"workload": f"{args.config}: {DESCRIPTIONS.get(args.config, args.config)}",
                    "bytes_per_step": bytes_per_step, "tokens_per_step": w.tokens(),
                    "l2": (f"rotating {n_sets} disjoint slot sets "
-                          f"({n_sets * w.B * w.HV * w.K * w.V * 4 / 2**20:.0f} MiB of state), "
+                          f"({n_sets * w.B * w.HV * w.K * w.V * w.pool.element_size() / 2**20:.0f} MiB of state), "
                           "inputs larger than L2" if n_sets > 1 else "inputs larger than L2"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tokens_per_s": round(tokens, 1),
@@ -332,7 +333,8 @@ def run_e2e(w, d, sets, dev, stream, args):
         views[n] = dbuf[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
     out_dev = torch.empty(w.v.shape, dtype=w.out_dtype, device=dev)
     out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
-    inter = torch.empty(w.B, w.T, w.HV, w.V, w.K, device=dev) if w.cache_intermediate else None
+    inter = (torch.empty(w.B, w.T, w.HV, w.V, w.K, device=dev, dtype=w.inter_dtype)
+             if w.cache_intermediate else None)
     kw = dict(views, pool=d["pool"], out=out_dev, inter=inter)
     if w.form != "la":
         kw.update(A_log=d.get("A_log"), dt_bias=d.get("dt_bias"), qk_l2norm=w.qk_l2norm,

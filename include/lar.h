@@ -24,16 +24,19 @@
  *
  * Layouts (all strides in ELEMENTS and non-negative; shape[] is logical):
  *   S is stored transposed: pool[slot][hv][v][k] = S[k][v], k fastest.
- *   pool   fp32, rank 4 [P, HV, V, K] (any slot/head/row strides), or rank 3
- *          [P*HV, V, K] (slot p, head hv at row p*HV + hv).  k stride must be 1;
- *          the data pointer 16-byte aligned; slot, head and row strides
- *          multiples of 4 (rows move as 16-byte vectors).
+ *   pool   fp32 or bf16, rank 4 [P, HV, V, K] (any slot/head/row strides), or
+ *          rank 3 [P*HV, V, K] (slot p, head hv at row p*HV + hv).  k stride
+ *          must be 1; the data pointer 16-byte aligned; slot, head and row
+ *          strides multiples of 16 bytes (rows move as 16-byte chunks).  The
+ *          arithmetic is fp32 either way: a bf16 state is widened on load and
+ *          rounded to nearest even once per store.
  *   q, k   [B, T, H, K]  (rank 3 [B, H, K] means T = 1); fp32 or bf16, any strides
  *          (so q/k/v may be head-dim slices of one fused buffer).
  *   v      [B, T, HV, V] (rank 3 [B, HV, V]); fp32 or bf16, any strides.
  *   out    [B, T, HV, V] (rank 3 [B, HV, V]); fp32 or bf16 (round to nearest even).
- *   inter  NULL, or fp32 [B, T, HV, V, K] (rank 4 [B, HV, V, K] when T = 1):
- *          the state after each token; same alignment rules as the pool.
+ *   inter  NULL, or fp32 or bf16 [B, T, HV, V, K] (rank 4 [B, HV, V, K] when
+ *          T = 1): the state after each token; same alignment rules as the
+ *          pool; its type is independent of the pool's.
  *   read_idx, write_idx  rank 1 [B], int32 or int64, any stride.
  *   H divides HV; v-head hv reads q/k head hv / (HV / H).
  *   K must be 16, 32, 64 or 128; V from 1 to 2^24; T from 1 to 16;
@@ -89,7 +92,7 @@ typedef enum {
     LAR_ERR_RANK = 3,        /* wrong ndim */
     LAR_ERR_SHAPE = 4,       /* shapes disagree, or a size outside the supported range */
     LAR_ERR_STRIDE = 5,      /* k stride of pool/inter not 1, or negative strides */
-    LAR_ERR_ALIGN = 6,       /* pool/inter pointer or strides not 16-byte aligned */
+    LAR_ERR_ALIGN = 6,       /* pool/inter pointer or strides not multiples of 16 bytes */
     LAR_ERR_ARG = 7,         /* inconsistent flags/arguments (e.g. A_log without LAR_GATE_RAW) */
     LAR_ERR_ALIAS = 8,       /* an output overlaps another output or an input */
     LAR_ERR_LAUNCH = 9       /* the CUDA launch itself failed */

@@ -42,10 +42,13 @@
 #define LAR_K128_NW 4
 #endif
 #ifndef LAR_MIN_BLOCKS
-#define LAR_MIN_BLOCKS 1
+#define LAR_MIN_BLOCKS 3
 #endif
 #ifndef LAR_PDL
 #define LAR_PDL 1
+#endif
+#ifndef LAR_K128_BF16_S
+#define LAR_K128_BF16_S 3
 #endif
 #ifndef LAR_K128_S
 #define LAR_K128_S 2
@@ -74,20 +77,6 @@ __device__ __forceinline__ void st_out(void* base, int64_t off, int dt, float x)
 
 __device__ __forceinline__ float softplus_f(float x) { return x > 20.f ? x : log1pf(expf(x)); }
 
-__device__ __forceinline__ float dot4(const float4 a, const float4 b, float acc) {
-    acc = fmaf(a.x, b.x, acc);
-    acc = fmaf(a.y, b.y, acc);
-    acc = fmaf(a.z, b.z, acc);
-    return fmaf(a.w, b.w, acc);
-}
-
-__device__ __forceinline__ void axpy4(float4& s, const float a, const float4 x) {
-    s.x = fmaf(a, x.x, s.x);
-    s.y = fmaf(a, x.y, s.y);
-    s.z = fmaf(a, x.z, s.z);
-    s.w = fmaf(a, x.w, s.w);
-}
-
 // 16-byte global -> shared copy that bypasses L1 (the state is touched once).
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
     const unsigned dst = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
@@ -101,16 +90,57 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Tile geometry shared by the kernel and its launcher.
-template <int K, int LPR, int NR, int NW>
+// Tile geometry shared by the kernel and its launcher.  SB is the byte size
+// of a pool element (4: fp32, 2: bf16); rows move in 16-byte chunks.
+template <int K, int LPR, int NR, int NW, int SB>
 struct Tile {
-    static constexpr int KPL = K / LPR;       // floats of a row held by one lane
-    static constexpr int NCH = KPL / 4;       // 16-byte chunks of a row held by one lane
+    static constexpr int EPC = 16 / SB;       // state elements per 16-byte chunk
+    static constexpr int KPL = K / LPR;       // state elements of a row held by one lane
+    static constexpr int NCH = KPL / EPC;     // 16-byte chunks of a row held by one lane
     static constexpr int RPW = 32 / LPR;      // rows covered by one warp instruction
     static constexpr int TV = NW * NR * RPW;  // rows per tile
-    static_assert(KPL % 4 == 0 && NCH >= 1, "a lane holds whole 16-byte chunks");
+    static_assert(KPL % EPC == 0 && NCH >= 1, "a lane holds whole 16-byte chunks");
     static_assert(32 % LPR == 0, "row groups tile the warp");
 };
+
+// 16-byte shared-memory chunk of EPC pool elements -> EPC floats (bf16 widens exactly).
+template <int SB>
+__device__ __forceinline__ void chunk_to_f32(const unsigned char* p, float* d) {
+    if constexpr (SB == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(p);
+        d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+    } else {
+        const uint4 v = *reinterpret_cast<const uint4*>(p);
+        const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            d[2 * q] = __uint_as_float(w[q] << 16);            // element 2q: low half
+            d[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u); // element 2q+1: high half
+        }
+    }
+}
+
+__device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // .x = lo (low 16 bits)
+    return *reinterpret_cast<const unsigned*>(&h);
+}
+
+// Streaming store of N floats (N = 4 or 8, contiguous) as fp32 or as bf16 (RNE).
+template <int N>
+__device__ __forceinline__ void store_run(void* g, const float* d, bool bf16) {
+    if (bf16) {
+        if constexpr (N == 8) {
+            __stcs(reinterpret_cast<uint4*>(g), make_uint4(pack_bf16x2(d[0], d[1]), pack_bf16x2(d[2], d[3]),
+                                                          pack_bf16x2(d[4], d[5]), pack_bf16x2(d[6], d[7])));
+        } else {
+            __stcs(reinterpret_cast<uint2*>(g), make_uint2(pack_bf16x2(d[0], d[1]), pack_bf16x2(d[2], d[3])));
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < N / 4; ++q)
+            __stcs(reinterpret_cast<float4*>(g) + q, make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]));
+    }
+}
 
 // v values of a (b, hv) pair are staged in shared memory with the other
 // per-pair vectors when T * V is at most this many floats; otherwise the
@@ -127,25 +157,27 @@ __host__ __device__ constexpr int vec_floats(int T, int V) {
     return ((FORM == FORM_KDA ? 3 : 2) * T * K + (stage_v(T, V) ? T * V : 0) + 5 * T + 3) & ~3;
 }
 
-template <int FORM, int K, int LPR, int NR, int NW, int S>
+template <int FORM, int K, int LPR, int NR, int NW, int S, int SB>
 __host__ __device__ constexpr size_t decode_smem_bytes(int T, int V) {
-    using G = Tile<K, LPR, NR, NW>;
-    return (static_cast<size_t>(S) * G::TV * K + 2 * static_cast<size_t>(vec_floats<FORM, K>(T, V))) *
-           sizeof(float);
+    using G = Tile<K, LPR, NR, NW, SB>;
+    return static_cast<size_t>(S) * G::TV * K * SB + 2 * static_cast<size_t>(vec_floats<FORM, K>(T, V)) * sizeof(float);
 }
 
-template <int FORM, int K, int LPR, int NR, int NW, int S>
+template <int FORM, int K, int LPR, int NR, int NW, int S, int SB>
 __global__ void __launch_bounds__(NW * 32, LAR_MIN_BLOCKS)
 decode_kernel(const DecodeParams p) {
-    using G = Tile<K, LPR, NR, NW>;
-    constexpr int NCH = G::NCH, RPW = G::RPW, TV = G::TV;
+    using G = Tile<K, LPR, NR, NW, SB>;
+    constexpr int NCH = G::NCH, RPW = G::RPW, TV = G::TV, EPC = G::EPC, KPL = G::KPL;
 
-    extern __shared__ __align__(16) float smem[];
+    extern __shared__ __align__(16) unsigned char smem[];
     const int T = p.T;
     const int V = p.V;
     const bool sv_on = stage_v(T, V);
-    float* ring = smem;                                        // [S][TV][K]
-    float* vecs = smem + static_cast<size_t>(S) * TV * K;      // 2 x vec_floats
+    unsigned char* ring = smem;                                               // [S][TV][K] pool elements
+    float* vecs = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * TV * K * SB);  // 2 x vec_floats
+    const unsigned char* pool_b = static_cast<const unsigned char*>(p.pool);
+    const bool inter_bf16 = p.inter_dt == LAR_BF16;
+    const int inter_es = inter_bf16 ? 2 : 4;
     const int vstride = vec_floats<FORM, K>(T, V);
     // offsets inside a vector buffer
     const int o_k = T * K;
@@ -213,16 +245,16 @@ decode_kernel(const DecodeParams p) {
     // issue this thread's copies of the tile at `q` (read slot r) into ring stage `st`
     auto issue = [&](const Pos& q, int64_t r, int st) {
         if (q.tile < t_end && r >= 0 && r < p.P) {
-            const float* src = p.pool + r * p.ps[0] + static_cast<int64_t>(q.hv) * p.ps[1];
-            float* dst = ring + static_cast<size_t>(st) * TV * K;
+            const unsigned char* src = pool_b + (r * p.ps[0] + static_cast<int64_t>(q.hv) * p.ps[1]) * SB;
+            unsigned char* dst = ring + static_cast<size_t>(st) * TV * K * SB;
 #pragma unroll
             for (int i = 0; i < NR; ++i) {
                 const int row = q.vt * TV + lrow(i);
                 if (row < V) {
 #pragma unroll
                     for (int c = 0; c < NCH; ++c) {
-                        const int k0 = (c * LPR + j) * 4;
-                        cp_async16(dst + lrow(i) * K + k0, src + row * p.ps[2] + k0);
+                        const int k0 = (c * LPR + j) * EPC;
+                        cp_async16(dst + (lrow(i) * K + k0) * SB, src + (row * p.ps[2] + k0) * SB);
                     }
                 }
             }
@@ -240,9 +272,9 @@ decode_kernel(const DecodeParams p) {
 
     int buf = 1;
     bool rd = false, wr = false;
-    float* dst_state = p.pool;              // state rows of the current pair (write slot)
+    unsigned char* dst_state = nullptr;     // state rows of the current pair (write slot)
     int64_t v_off = 0, o_off = 0;           // per-pair offsets into v and out
-    float* inter_base = p.inter;
+    unsigned char* inter_base = nullptr;
     const float scale = p.scale;
     const bool gate_raw = (p.flags & LAR_GATE_RAW) != 0;
     const bool l2 = FORM != FORM_LA && (p.flags & LAR_QK_L2NORM) != 0;
@@ -266,10 +298,11 @@ decode_kernel(const DecodeParams p) {
                 const int e = (r >= p.P ? LAR_DEVERR_READ_SLOT : 0) | (w >= p.P ? LAR_DEVERR_WRITE_SLOT : 0);
                 if (e) atomicOr(p.dev_err, e);
             }
-            dst_state = p.pool + (wr ? w : 0) * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1];
+            dst_state = static_cast<unsigned char*>(p.pool) +
+                        ((wr ? w : 0) * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1]) * SB;
             v_off = b * p.vs[0] + hv * p.vs[2];
             o_off = b * p.os[0] + hv * p.os[2];
-            if (p.inter) inter_base = p.inter + b * p.is[0] + hv * p.is[2];
+            if (p.inter) inter_base = static_cast<unsigned char*>(p.inter) + (b * p.is[0] + hv * p.is[2]) * inter_es;
 
             float* vb = vecs + buf * vstride;
             const int64_t q_off = b * p.qs[0] + h * p.qs[2];
@@ -344,16 +377,21 @@ decode_kernel(const DecodeParams p) {
 
         // ---- this thread's copies of the tile have landed: pull its rows into registers
         cp_async_wait<S - 2>();
-        float4 s[NR][NCH];
+        float s[NR][KPL];
         {
-            const float* src = ring + static_cast<size_t>(stage) * TV * K;
+            const unsigned char* src = ring + static_cast<size_t>(stage) * TV * K * SB;
 #pragma unroll
             for (int i = 0; i < NR; ++i) {
                 const bool ok = rd && vt * TV + lrow(i) < V;
 #pragma unroll
-                for (int c = 0; c < NCH; ++c)
-                    s[i][c] = ok ? *reinterpret_cast<const float4*>(src + lrow(i) * K + (c * LPR + j) * 4)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int c = 0; c < NCH; ++c) {
+                    if (ok) {
+                        chunk_to_f32<SB>(src + (lrow(i) * K + (c * LPR + j) * EPC) * SB, &s[i][c * EPC]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < EPC; ++e) s[i][c * EPC + e] = 0.f;
+                    }
+                }
             }
         }
         // refill the stage consumed in the previous iteration (its rows were used long ago)
@@ -369,13 +407,24 @@ decode_kernel(const DecodeParams p) {
         for (int t = 0; t < T; ++t) {
             const float bt = sc[t], dec = sc[T + t];
             const float iq = sc[2 * T + t], ik = sc[3 * T + t], kq = sc[4 * T + t];
-            float4 kv[NCH], qv[NCH], dv[NCH];
+            float kv[KPL], qv[KPL], dv[KPL];
 #pragma unroll
             for (int c = 0; c < NCH; ++c) {
-                const int kidx = t * K + (c * LPR + j) * 4;
-                qv[c] = *reinterpret_cast<const float4*>(vb + kidx);
-                kv[c] = *reinterpret_cast<const float4*>(vb + o_k + kidx);
-                if constexpr (FORM == FORM_KDA) dv[c] = *reinterpret_cast<const float4*>(vb + o_d + kidx);
+#pragma unroll
+                for (int e4 = 0; e4 < EPC / 4; ++e4) {
+                    const int kidx = t * K + (c * LPR + j) * EPC + 4 * e4;
+                    const float4 a4 = *reinterpret_cast<const float4*>(vb + kidx);
+                    const float4 b4 = *reinterpret_cast<const float4*>(vb + o_k + kidx);
+                    float* qd = &qv[c * EPC + 4 * e4];
+                    float* kd = &kv[c * EPC + 4 * e4];
+                    qd[0] = a4.x; qd[1] = a4.y; qd[2] = a4.z; qd[3] = a4.w;
+                    kd[0] = b4.x; kd[1] = b4.y; kd[2] = b4.z; kd[3] = b4.w;
+                    if constexpr (FORM == FORM_KDA) {
+                        const float4 d4 = *reinterpret_cast<const float4*>(vb + o_d + kidx);
+                        float* dd = &dv[c * EPC + 4 * e4];
+                        dd[0] = d4.x; dd[1] = d4.y; dd[2] = d4.z; dd[3] = d4.w;
+                    }
+                }
             }
 #pragma unroll
             for (int i = 0; i < NR; ++i) {
@@ -384,32 +433,25 @@ decode_kernel(const DecodeParams p) {
                 float vval = 0.f;
                 if (rv) vval = sv_on ? vb[o_v + t * V + row] : ld_in(p.v, v_off + t * p.vs[1] + row * p.vs[3], p.v_dt);
 #pragma unroll
-                for (int c = 0; c < NCH; ++c) {
-                    if constexpr (FORM == FORM_KDA) {
-                        s[i][c].x *= dv[c].x; s[i][c].y *= dv[c].y;
-                        s[i][c].z *= dv[c].z; s[i][c].w *= dv[c].w;
-                    } else {
-                        s[i][c].x *= dec; s[i][c].y *= dec; s[i][c].z *= dec; s[i][c].w *= dec;
-                    }
-                }
+                for (int e = 0; e < KPL; ++e) s[i][e] *= (FORM == FORM_KDA ? dv[e] : dec);
                 // q_hat = iq q and k_hat = ik k: the norms scale the reduced sums
                 float o;
                 if constexpr (FORM == FORM_LA) {
                     float pp = 0.f;
 #pragma unroll
-                    for (int c = 0; c < NCH; ++c) pp = dot4(s[i][c], qv[c], pp);
+                    for (int e = 0; e < KPL; ++e) pp = fmaf(s[i][e], qv[e], pp);
 #pragma unroll
                     for (int off = LPR / 2; off > 0; off >>= 1) pp += __shfl_xor_sync(0xffffffffu, pp, off);
                     const float a = vval * ik;
 #pragma unroll
-                    for (int c = 0; c < NCH; ++c) axpy4(s[i][c], a, kv[c]);
+                    for (int e = 0; e < KPL; ++e) s[i][e] = fmaf(a, kv[e], s[i][e]);
                     o = fmaf(vval, kq, pp * iq);
                 } else {
                     float uu = 0.f, pp = 0.f;
 #pragma unroll
-                    for (int c = 0; c < NCH; ++c) {
-                        uu = dot4(s[i][c], kv[c], uu);
-                        pp = dot4(s[i][c], qv[c], pp);
+                    for (int e = 0; e < KPL; ++e) {
+                        uu = fmaf(s[i][e], kv[e], uu);
+                        pp = fmaf(s[i][e], qv[e], pp);
                     }
 #pragma unroll
                     for (int off = LPR / 2; off > 0; off >>= 1) {
@@ -419,15 +461,16 @@ decode_kernel(const DecodeParams p) {
                     const float delta = bt * (vval - uu * ik);
                     const float a = delta * ik;
 #pragma unroll
-                    for (int c = 0; c < NCH; ++c) axpy4(s[i][c], a, kv[c]);
+                    for (int e = 0; e < KPL; ++e) s[i][e] = fmaf(a, kv[e], s[i][e]);
                     o = fmaf(delta, kq, pp * iq);
                 }
                 if (j == 0 && rv)
                     st_out(p.out, o_off + t * p.os[1] + row * p.os[3], p.out_dt, o * scale);
                 if (p.inter != nullptr && rv) {
-                    float4* ip = reinterpret_cast<float4*>(inter_base + t * p.is[1] + row * p.is[3]) + j;
+                    unsigned char* ip = inter_base + (t * p.is[1] + row * p.is[3]) * inter_es;
 #pragma unroll
-                    for (int c = 0; c < NCH; ++c) __stcs(ip + c * LPR, s[i][c]);
+                    for (int c = 0; c < NCH; ++c)
+                        store_run<EPC>(ip + (c * LPR + j) * EPC * inter_es, &s[i][c * EPC], inter_bf16);
                 }
             }
         }
@@ -438,9 +481,10 @@ decode_kernel(const DecodeParams p) {
             for (int i = 0; i < NR; ++i) {
                 const int row = vt * TV + lrow(i);
                 if (row < V) {
-                    float4* wp = reinterpret_cast<float4*>(dst_state + row * p.ps[2]) + j;
+                    unsigned char* wp = dst_state + row * p.ps[2] * SB;
 #pragma unroll
-                    for (int c = 0; c < NCH; ++c) __stcs(wp + c * LPR, s[i][c]);
+                    for (int c = 0; c < NCH; ++c)
+                        store_run<EPC>(wp + (c * LPR + j) * EPC * SB, &s[i][c * EPC], SB == 2);
                 }
             }
         }
@@ -452,13 +496,13 @@ decode_kernel(const DecodeParams p) {
 // once per (device, size) and cached.
 int cached_occupancy(const void* kern, int threads, size_t smem, size_t smem_max, int* sms_out);
 
-template <int FORM, int K, int LPR, int NR, int NW, int S>
+template <int FORM, int K, int LPR, int NR, int NW, int S, int SB>
 lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
-    using G = Tile<K, LPR, NR, NW>;
-    auto kern = decode_kernel<FORM, K, LPR, NR, NW, S>;
-    const size_t smem = decode_smem_bytes<FORM, K, LPR, NR, NW, S>(p.T, p.V);
+    using G = Tile<K, LPR, NR, NW, SB>;
+    auto kern = decode_kernel<FORM, K, LPR, NR, NW, S, SB>;
+    const size_t smem = decode_smem_bytes<FORM, K, LPR, NR, NW, S, SB>(p.T, p.V);
     // the largest footprint any call can ask for (T = 16 with staged v)
-    constexpr size_t smem_max = decode_smem_bytes<FORM, K, LPR, NR, NW, S>(16, kStageVMax / 16);
+    constexpr size_t smem_max = decode_smem_bytes<FORM, K, LPR, NR, NW, S, SB>(16, kStageVMax / 16);
     int sms = 0;
     const int occ = cached_occupancy(reinterpret_cast<const void*>(kern), NW * 32, smem, smem_max, &sms);
     if (occ < 1) return LAR_ERR_LAUNCH;
@@ -484,18 +528,28 @@ lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
 #endif
 }
 
-// Tile shapes per key size: 8 lanes per 512-byte row at K = 128 (one full line
-// per lane group per instruction), 32-row tiles (16 KB), a 2-stage ring (one
-// tile in flight while one is computed; four CTAs per SM keep ~64 KB of state
-// loads in flight per SM).
+// Tile shapes per key size and pool type: a row is split over LPR lanes so each
+// lane holds whole 16-byte chunks (fp32 K = 128: 8 lanes x 4 chunks of 4; bf16
+// K = 128: 8 lanes x 2 chunks of 8); 32-row tiles at K = 128, a 2-stage ring
+// (one tile in flight while one is computed) for fp32 and a 3-stage ring for
+// bf16, whose tiles are half the bytes.
 template <int FORM>
 lar_status launch_form(const DecodeParams& p, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (p.pool_dt == LAR_F32) {
+        switch (p.K) {
+            case 16: return launch_tile<FORM, 16, 4, 2, 2, 3, 4>(p, st);
+            case 32: return launch_tile<FORM, 32, 8, 2, 4, 3, 4>(p, st);
+            case 64: return launch_tile<FORM, 64, 8, 2, 4, 3, 4>(p, st);
+            case 128: return launch_tile<FORM, 128, 8, LAR_K128_NR, LAR_K128_NW, LAR_K128_S, 4>(p, st);
+            default: return LAR_ERR_SHAPE;
+        }
+    }
     switch (p.K) {
-        case 16: return launch_tile<FORM, 16, 4, 2, 2, 3>(p, st);
-        case 32: return launch_tile<FORM, 32, 8, 2, 4, 3>(p, st);
-        case 64: return launch_tile<FORM, 64, 8, 2, 4, 3>(p, st);
-        case 128: return launch_tile<FORM, 128, 8, LAR_K128_NR, LAR_K128_NW, LAR_K128_S>(p, st);
+        case 16: return launch_tile<FORM, 16, 2, 2, 2, 3, 2>(p, st);
+        case 32: return launch_tile<FORM, 32, 4, 2, 4, 3, 2>(p, st);
+        case 64: return launch_tile<FORM, 64, 8, 2, 4, 3, 2>(p, st);
+        case 128: return launch_tile<FORM, 128, 8, LAR_K128_NR, LAR_K128_NW, LAR_K128_BF16_S, 2>(p, st);
         default: return LAR_ERR_SHAPE;
     }
 }

@@ -109,7 +109,7 @@ lar_status check_common(const Common& c, int form, DecodeParams& p) {
     if (c.q->ndim != 3 && c.q->ndim != 4) return LAR_ERR_RANK;
     if (c.k->ndim != c.q->ndim || c.v->ndim != c.q->ndim || c.out->ndim != c.q->ndim) return LAR_ERR_RANK;
     if (!is_float(c.q) || !is_float(c.k) || !is_float(c.v) || !is_float(c.out)) return LAR_ERR_DTYPE;
-    if (c.pool->dtype != LAR_F32) return LAR_ERR_DTYPE;
+    if (!is_float(c.pool)) return LAR_ERR_DTYPE;
 
     const bool short_form = c.q->ndim == 3;
     const int64_t B = c.q->shape[0];
@@ -164,10 +164,13 @@ lar_status check_common(const Common& c, int form, DecodeParams& p) {
     } else {
         return LAR_ERR_RANK;
     }
+    // state rows move as 16-byte chunks: aligned base, strides in whole chunks
+    const int64_t pes = elem_size(pl->dtype);
     if (reinterpret_cast<uintptr_t>(pl->data) % 16 != 0) return LAR_ERR_ALIGN;
-    if (p.ps[0] % 4 || p.ps[1] % 4 || p.ps[2] % 4) return LAR_ERR_ALIGN;
+    if ((p.ps[0] * pes) % 16 || (p.ps[1] * pes) % 16 || (p.ps[2] * pes) % 16) return LAR_ERR_ALIGN;
     p.P = P;
-    p.pool = static_cast<float*>(pl->data);
+    p.pool = pl->data;
+    p.pool_dt = pl->dtype;
 
     // slot indices
     if (c.read_idx->ndim != 1) return LAR_ERR_RANK;
@@ -186,11 +189,12 @@ lar_status check_common(const Common& c, int form, DecodeParams& p) {
 
     // intermediate-state cache: [B, T, HV, V, K] (rank 4 [B, HV, V, K] for T = 1)
     p.inter = nullptr;
+    p.inter_dt = LAR_F32;
     for (int i = 0; i < 4; ++i) p.is[i] = 0;
     if (c.inter) {
         const lar_tensor* it = c.inter;
         if (missing(it)) return LAR_ERR_NULL;
-        if (it->dtype != LAR_F32) return LAR_ERR_DTYPE;
+        if (!is_float(it)) return LAR_ERR_DTYPE;
         int64_t shp[5], str[5];
         if (it->ndim == 5) {
             for (int i = 0; i < 5; ++i) { shp[i] = it->shape[i]; str[i] = it->stride[i]; }
@@ -203,9 +207,13 @@ lar_status check_common(const Common& c, int form, DecodeParams& p) {
         }
         if (shp[0] != B || shp[1] != T || shp[2] != HV || shp[3] != V || shp[4] != K) return LAR_ERR_SHAPE;
         if (str[4] != 1) return LAR_ERR_STRIDE;
+        // cached rows are written in aligned runs of 8 or 16 bytes: aligned base, 16-byte strides
+        const int64_t ies = elem_size(it->dtype);
         if (reinterpret_cast<uintptr_t>(it->data) % 16 != 0) return LAR_ERR_ALIGN;
-        if (str[0] % 4 || str[1] % 4 || str[2] % 4 || str[3] % 4) return LAR_ERR_ALIGN;
-        p.inter = static_cast<float*>(it->data);
+        if ((str[0] * ies) % 16 || (str[1] * ies) % 16 || (str[2] * ies) % 16 || (str[3] * ies) % 16)
+            return LAR_ERR_ALIGN;
+        p.inter = it->data;
+        p.inter_dt = it->dtype;
         for (int i = 0; i < 4; ++i) p.is[i] = str[i];
     }
     return LAR_OK;
@@ -339,7 +347,7 @@ const char* lar_status_string(lar_status status) {
         case LAR_ERR_RANK: return "wrong tensor rank";
         case LAR_ERR_SHAPE: return "shapes disagree or a size is outside the supported range";
         case LAR_ERR_STRIDE: return "unsupported strides (k stride of pool/inter must be 1; no negative strides)";
-        case LAR_ERR_ALIGN: return "pool/inter must be 16-byte aligned with strides that are multiples of 4 elements";
+        case LAR_ERR_ALIGN: return "pool/inter must be 16-byte aligned with strides that are multiples of 16 bytes";
         case LAR_ERR_ARG: return "inconsistent arguments or flags";
         case LAR_ERR_ALIAS: return "an output overlaps another output or an input";
         case LAR_ERR_LAUNCH: return "kernel launch failed";

@@ -98,7 +98,10 @@ def test_empty_batch_is_a_no_op(lib):
     (lambda a: setattr(a["q"], "ndim", 6), 0, RANK),
     (lambda a: a.update(q=fake([2, 1, 2, 100], BF16), k=fake([2, 1, 2, 100], BF16)), 0, SHAPE),
     (lambda a: a.update(v=fake([2, 1, 3, 64], BF16), out=fake([2, 1, 3, 64], BF16)), 0, SHAPE),
-    (lambda a: a.update(pool=fake([8, 4, 64, 128], BF16)), 0, DTYPE),
+    (lambda a: a.update(pool=fake([8, 4, 64, 128], I32)), 0, DTYPE),
+    # a bf16 pool whose rows start 8 bytes apart cannot move in 16-byte chunks
+    (lambda a: a.update(pool=fake([8, 4, 64, 128], BF16, strides=[4 * 64 * 132, 64 * 132, 132, 1])), 0, ALIGN),
+    (lambda a: a.update(inter=fake([2, 1, 4, 64, 128], I32)), 0, DTYPE),
     (lambda a: a.update(q=fake([2, 1, 2, 128], I32)), 0, DTYPE),
     (lambda a: a.update(pool=fake([8, 4, 64, 128], strides=[64 * 256 * 4, 64 * 256, 256, 2])), 0, STRIDE),
     (lambda a: a.update(pool=fake([8, 4, 64, 128], addr=0x7000004)), 0, ALIGN),

@@ -15,7 +15,8 @@ def _sample(B, seed=0, n=6):
     return sorted({0, B - 1, *rest.tolist()})
 
 
-@pytest.mark.parametrize("name", ["gdn_b64", "gdn_mtp_strided", "kda_b256", "la_b512_packed"])
+@pytest.mark.parametrize("name", ["gdn_b64", "gdn_mtp_strided", "kda_b256", "la_b512_packed",
+                                  "gdn_b64_bf16"])
 def test_full_size(name, cuda_device):
     dev = cuda_device
     w = W.make(name, pool_device=dev)
@@ -36,7 +37,7 @@ def test_full_size(name, cuda_device):
     n = len(sample)
     ri = w.read_idx.long()
     shape = (n * w.HV,) + tuple(w.pool.shape[1:]) if w.pool.dim() == 3 else (n,) + tuple(w.pool.shape[1:])
-    sub = torch.zeros(shape)
+    sub = torch.zeros(shape, dtype=w.pool.dtype)
     for i, b in enumerate(sample):
         r = int(ri[b])
         if 0 <= r < w.P:

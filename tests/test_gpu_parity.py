@@ -49,6 +49,22 @@ SWEEP = {
     "la_unstaged_v": ("la", dict(B=2, T=11, H=2, K=32, V=400, separate_write=True)),
     "kda_t16_gqa": ("kda", dict(B=3, T=16, H=2, HV=4, K=128, V=64, raw_gates=True,
                                 cache_intermediate=True)),
+    # bfloat16 state pool (fp32 arithmetic, state rounded once per store)
+    "gdn_bf16_t1": ("gdn", dict(B=5, T=1, H=2, HV=4, K=128, V=128, state_dtype=torch.bfloat16)),
+    "gdn_bf16_mtp_strided": ("gdn", dict(B=4, T=4, H=2, HV=4, K=128, V=96, state_dtype=torch.bfloat16,
+                                         stride_mult=2, separate_write=True, skip_frac=0.25,
+                                         cache_intermediate=True)),
+    "gdn_bf16_pool_f32_cache": ("gdn", dict(B=3, T=3, H=1, HV=2, K=64, V=70, state_dtype=torch.bfloat16,
+                                            cache_intermediate=True, inter_dtype=torch.float32)),
+    "gdn_f32_pool_bf16_cache": ("gdn", dict(B=3, T=3, H=1, HV=2, K=64, V=70, cache_intermediate=True,
+                                            inter_dtype=torch.bfloat16)),
+    "kda_bf16_raw": ("kda", dict(B=4, T=2, H=2, HV=2, K=128, V=128, raw_gates=True,
+                                 state_dtype=torch.bfloat16, cache_intermediate=True)),
+    "kda_bf16_k32": ("kda", dict(B=3, T=1, H=2, HV=2, K=32, V=33, state_dtype=torch.bfloat16)),
+    "la_bf16_packed": ("la", dict(B=4, T=1, H=3, K=128, V=128, packed=True, flat_pool=True,
+                                  state_dtype=torch.bfloat16)),
+    "la_bf16_k16": ("la", dict(B=2, T=2, H=2, K=16, V=24, flat_pool=True, state_dtype=torch.bfloat16)),
+    "gdn_bf16_unstaged_v": ("gdn", dict(B=2, T=16, H=1, HV=1, K=64, V=300, state_dtype=torch.bfloat16)),
 }
 
 

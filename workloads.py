@@ -24,6 +24,7 @@ kda_b256           B=256 T=1 H=HV=24, raw bf16 q/k (l2norm in kernel), raw bf16
                    gate a [B,T,HV,K], A_log ~ U(log 1, log 16) [HV], dt_bias ~
                    N(0, 0.1) [HV*K], raw beta logits; pool [320,24,128,128];
                    read = write = randperm(320)[:256]; seed 4
+gdn_b64_bf16       gdn_b64 with a bfloat16 state pool (drawn in fp32, rounded once)
 la_b512_packed     B=512 T=1 H=64, q/k/v head-dim slices of one fused bf16
                    [B,H,384] buffer (q, k ~ N(0,1)/sqrt(128), v ~ N(0,1)),
                    lambda_h = exp(-2^(-8(h+1)/64)), flat pool [640*64,128,128];
@@ -46,9 +47,10 @@ import torch.nn.functional as F
 BF16 = torch.bfloat16
 F32 = torch.float32
 
-CONFIGS = ("gdn_tiny", "gdn_b64", "gdn_mtp_strided", "kda_b256", "la_b512_packed")
+CONFIGS = ("gdn_tiny", "gdn_b64", "gdn_mtp_strided", "kda_b256", "la_b512_packed",
+           "gdn_b64_bf16")
 SEEDS = {"gdn_tiny": 0, "gdn_b64": 2, "gdn_mtp_strided": 3, "kda_b256": 4,
-         "la_b512_packed": 5}
+         "la_b512_packed": 5, "gdn_b64_bf16": 2}
 
 
 @dataclass
@@ -81,6 +83,7 @@ class Workload:
     beta_raw: bool = False
     scale: float = 1.0
     cache_intermediate: bool = False
+    inter_dtype: torch.dtype = F32
     meta: dict = field(default_factory=dict)
 
     def algorithmic_bytes(self) -> int:
@@ -88,7 +91,7 @@ class Workload:
         each output written once): state read for entries with a valid read
         slot, state write for entries with a valid write slot, every cached
         intermediate state, plus q/k/v/gate/out/index bytes."""
-        unit = self.K * self.V * 4
+        unit = self.K * self.V * self.pool.element_size()
         heads = self.HV
         r = self.read_idx.to("cpu")
         w = (self.write_idx if self.write_idx is not None else self.read_idx).to("cpu")
@@ -96,7 +99,7 @@ class Workload:
         n_write = int(((w >= 0) & (w < self.P)).sum())
         total = (n_read + n_write) * heads * unit
         if self.cache_intermediate:
-            total += self.B * self.T * heads * unit
+            total += self.B * self.T * heads * self.K * self.V * torch.finfo(self.inter_dtype).bits // 8
         small = [self.q, self.k, self.v, self.g, self.beta, self.A_log, self.dt_bias,
                  self.decay, self.read_idx, self.write_idx]
         total += sum(t.numel() * t.element_size() for t in small if t is not None)
@@ -115,14 +118,15 @@ def _l2n(x):
     return F.normalize(x, p=2.0, dim=-1)
 
 
-def _draw_pool(gen, shape, seed, device):
+def _draw_pool(gen, shape, seed, device, dtype=F32):
+    """N(0, 0.1^2) state, drawn in fp32 and (for a bf16 pool) rounded once."""
     if torch.device(device).type == "cpu":
-        return _normal(gen, shape, 0.1)
+        return _normal(gen, shape, 0.1).to(dtype)
     dg = torch.Generator(device=device)
     dg.manual_seed(seed)
     pool = torch.empty(shape, dtype=F32, device=device)
     pool.normal_(0.0, 0.1, generator=dg)
-    return pool
+    return pool.to(dtype)
 
 
 def make(name: str, *, seed: int | None = None, pool_device="cpu",
@@ -141,7 +145,7 @@ def make(name: str, *, seed: int | None = None, pool_device="cpu",
         pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
         return Workload(name, "gdn", B, T, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
                         F32, g=g, beta=beta)
-    if name == "gdn_b64":
+    if name in ("gdn_b64", "gdn_b64_bf16"):
         B, T, H, HV, K, V, P = 64, 1, 16, 32, 128, 128, 256
         q = _l2n(_normal(gen, (B, T, H, K))).to(BF16)
         k = _l2n(_normal(gen, (B, T, H, K))).to(BF16)
@@ -149,7 +153,8 @@ def make(name: str, *, seed: int | None = None, pool_device="cpu",
         g = -F.softplus(_normal(gen, (B, T, HV)))
         beta = torch.sigmoid(_normal(gen, (B, T, HV)))
         ri = torch.randperm(P, generator=gen)[:B].to(index_dtype)
-        pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
+        pool = _draw_pool(gen, (P, HV, V, K), s, pool_device,
+                          BF16 if name == "gdn_b64_bf16" else F32)
         return Workload(name, "gdn", B, T, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
                         BF16, g=g, beta=beta)
     if name == "gdn_mtp_strided":
@@ -218,7 +223,8 @@ def make_custom(form: str, *, B: int, T: int, H: int, HV: int | None = None, K: 
                 out_dtype=BF16, separate_write: bool = False, skip_frac: float = 0.0,
                 stride_mult: int = 1, cache_intermediate: bool = False,
                 raw_gates: bool = False, packed: bool = False, flat_pool: bool = False,
-                index_dtype=torch.int32, pool_device="cpu") -> Workload:
+                index_dtype=torch.int32, pool_device="cpu", state_dtype=F32,
+                inter_dtype=None) -> Workload:
     """A workload of any size in the same distributions as the named recipes.
 
     ``raw_gates``: q/k raw N(0,1) with in-kernel l2norm, raw gate input and beta
@@ -227,6 +233,8 @@ def make_custom(form: str, *, B: int, T: int, H: int, HV: int | None = None, K: 
     ``separate_write``: write slots distinct from every read slot.
     ``stride_mult`` > 1: the pool is backing[::stride_mult].
     ``packed``: q/k/v are slices of one fused [B,T,H,2K+V] buffer (needs H == HV).
+    ``state_dtype``: fp32 or bf16 pool; ``inter_dtype``: the state cache's type
+    (default: the pool's).
     """
     HV = H if HV is None else HV
     P = max(2 * B, 4) if P is None else P
@@ -283,19 +291,20 @@ def make_custom(form: str, *, B: int, T: int, H: int, HV: int | None = None, K: 
             wi[torch.randperm(B, generator=gen)[:n_skip]] = -1
     backing = None
     if form == "la" and flat_pool:
-        pool = _draw_pool(gen, (P * H, V, K), seed, pool_device)
+        pool = _draw_pool(gen, (P * H, V, K), seed, pool_device, state_dtype)
     elif stride_mult > 1:
-        backing = _draw_pool(gen, (P * stride_mult, HV, V, K), seed, pool_device)
+        backing = _draw_pool(gen, (P * stride_mult, HV, V, K), seed, pool_device, state_dtype)
         pool = backing[::stride_mult]
     else:
-        pool = _draw_pool(gen, (P, HV, V, K), seed, pool_device)
+        pool = _draw_pool(gen, (P, HV, V, K), seed, pool_device, state_dtype)
     return Workload(f"custom_{form}", form, B, T, H, HV, K, V, P, q, k, v, pool,
                     ri.to(index_dtype), wi.to(index_dtype), out_dtype, g=g, beta=beta,
                     A_log=A_log, dt_bias=dt_bias, decay=decay, backing=backing,
                     fused=fused, qk_l2norm=raw_gates and form != "la",
                     gate_raw=raw_gates and form != "la",
                     beta_raw=raw_gates and form != "la",
-                    cache_intermediate=cache_intermediate)
+                    cache_intermediate=cache_intermediate,
+                    inter_dtype=state_dtype if inter_dtype is None else inter_dtype)
 
 
 def disjoint_index_sets(P: int, B: int, n: int, seed: int, index_dtype=torch.int32):
