@@ -41,8 +41,11 @@
 #ifndef LAR_K128_NW
 #define LAR_K128_NW 4
 #endif
-#ifndef LAR_MIN_BLOCKS
-#define LAR_MIN_BLOCKS 3
+#ifndef LAR_KDA_MIN_BLOCKS
+#define LAR_KDA_MIN_BLOCKS 3
+#endif
+#ifndef LAR_K128_LPR
+#define LAR_K128_LPR 8
 #endif
 #ifndef LAR_PDL
 #define LAR_PDL 1
@@ -163,8 +166,8 @@ __host__ __device__ constexpr size_t decode_smem_bytes(int T, int V) {
     return static_cast<size_t>(S) * G::TV * K * SB + 2 * static_cast<size_t>(vec_floats<FORM, K>(T, V)) * sizeof(float);
 }
 
-template <int FORM, int K, int LPR, int NR, int NW, int S, int SB>
-__global__ void __launch_bounds__(NW * 32, LAR_MIN_BLOCKS)
+template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB>
+__global__ void __launch_bounds__(NW * 32, MB)
 decode_kernel(const DecodeParams p) {
     using G = Tile<K, LPR, NR, NW, SB>;
     constexpr int NCH = G::NCH, RPW = G::RPW, TV = G::TV, EPC = G::EPC, KPL = G::KPL;
@@ -206,6 +209,18 @@ decode_kernel(const DecodeParams p) {
     // local row (within a tile) of this thread's i-th row
     auto lrow = [&](int i) { return (warp * NR + i) * RPW + gi; };
 
+    // Byte offsets fixed for the whole kernel.  A thread's rows in a tile are
+    // row0, row0 + RPW, ... and its chunks in a row are CSTEP bytes apart, so
+    // every chunk address is a per-tile base plus compile-time steps.
+    const int row0 = lrow(0);
+    constexpr int CSTEP = LPR * 16;                 // between a lane's chunks of one row
+    constexpr int STAGE = TV * K * SB;              // one ring stage
+    constexpr int S_RSTEP = RPW * K * SB;           // between a thread's rows in a stage
+    const int s_row0 = row0 * K * SB + j * 16;
+    const int64_t g_row0 = static_cast<int64_t>(row0) * p.ps[2] * SB + j * 16;
+    const int64_t g_rstep = static_cast<int64_t>(RPW) * p.ps[2] * SB;
+    const int64_t g_tile = static_cast<int64_t>(TV) * p.ps[2] * SB;
+
     // tile coordinates, advanced incrementally (no per-tile 64-bit division)
     struct Pos {
         int64_t tile;
@@ -245,17 +260,15 @@ decode_kernel(const DecodeParams p) {
     // issue this thread's copies of the tile at `q` (read slot r) into ring stage `st`
     auto issue = [&](const Pos& q, int64_t r, int st) {
         if (q.tile < t_end && r >= 0 && r < p.P) {
-            const unsigned char* src = pool_b + (r * p.ps[0] + static_cast<int64_t>(q.hv) * p.ps[1]) * SB;
-            unsigned char* dst = ring + static_cast<size_t>(st) * TV * K * SB;
+            const unsigned char* src = pool_b + (r * p.ps[0] + static_cast<int64_t>(q.hv) * p.ps[1]) * SB +
+                                       q.vt * g_tile + g_row0;
+            unsigned char* dst = ring + st * STAGE + s_row0;
 #pragma unroll
             for (int i = 0; i < NR; ++i) {
-                const int row = q.vt * TV + lrow(i);
-                if (row < V) {
+                if (q.vt * TV + row0 + i * RPW < V) {
 #pragma unroll
-                    for (int c = 0; c < NCH; ++c) {
-                        const int k0 = (c * LPR + j) * EPC;
-                        cp_async16(dst + (lrow(i) * K + k0) * SB, src + (row * p.ps[2] + k0) * SB);
-                    }
+                    for (int c = 0; c < NCH; ++c)
+                        cp_async16(dst + i * S_RSTEP + c * CSTEP, src + i * g_rstep + c * CSTEP);
                 }
             }
         }
@@ -379,14 +392,14 @@ decode_kernel(const DecodeParams p) {
         cp_async_wait<S - 2>();
         float s[NR][KPL];
         {
-            const unsigned char* src = ring + static_cast<size_t>(stage) * TV * K * SB;
+            const unsigned char* src = ring + stage * STAGE + s_row0;
 #pragma unroll
             for (int i = 0; i < NR; ++i) {
-                const bool ok = rd && vt * TV + lrow(i) < V;
+                const bool ok = rd && vt * TV + row0 + i * RPW < V;
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
                     if (ok) {
-                        chunk_to_f32<SB>(src + (lrow(i) * K + (c * LPR + j) * EPC) * SB, &s[i][c * EPC]);
+                        chunk_to_f32<SB>(src + i * S_RSTEP + c * CSTEP, &s[i][c * EPC]);
                     } else {
 #pragma unroll
                         for (int e = 0; e < EPC; ++e) s[i][c * EPC + e] = 0.f;
@@ -467,24 +480,23 @@ decode_kernel(const DecodeParams p) {
                 if (j == 0 && rv)
                     st_out(p.out, o_off + t * p.os[1] + row * p.os[3], p.out_dt, o * scale);
                 if (p.inter != nullptr && rv) {
-                    unsigned char* ip = inter_base + (t * p.is[1] + row * p.is[3]) * inter_es;
+                    unsigned char* ip = inter_base + (t * p.is[1] + row * p.is[3]) * inter_es + j * EPC * inter_es;
+                    const int cstep = LPR * EPC * inter_es;
 #pragma unroll
-                    for (int c = 0; c < NCH; ++c)
-                        store_run<EPC>(ip + (c * LPR + j) * EPC * inter_es, &s[i][c * EPC], inter_bf16);
+                    for (int c = 0; c < NCH; ++c) store_run<EPC>(ip + c * cstep, &s[i][c * EPC], inter_bf16);
                 }
             }
         }
 
         // ---- writeback to the write slot (skipped for negative / out-of-range slots)
         if (wr) {
+            unsigned char* wb = dst_state + vt * g_tile + g_row0;
 #pragma unroll
             for (int i = 0; i < NR; ++i) {
-                const int row = vt * TV + lrow(i);
-                if (row < V) {
-                    unsigned char* wp = dst_state + row * p.ps[2] * SB;
+                if (vt * TV + row0 + i * RPW < V) {
 #pragma unroll
                     for (int c = 0; c < NCH; ++c)
-                        store_run<EPC>(wp + (c * LPR + j) * EPC * SB, &s[i][c * EPC], SB == 2);
+                        store_run<EPC>(wb + i * g_rstep + c * CSTEP, &s[i][c * EPC], SB == 2);
                 }
             }
         }
@@ -496,10 +508,10 @@ decode_kernel(const DecodeParams p) {
 // once per (device, size) and cached.
 int cached_occupancy(const void* kern, int threads, size_t smem, size_t smem_max, int* sms_out);
 
-template <int FORM, int K, int LPR, int NR, int NW, int S, int SB>
+template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB = 1>
 lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
     using G = Tile<K, LPR, NR, NW, SB>;
-    auto kern = decode_kernel<FORM, K, LPR, NR, NW, S, SB>;
+    auto kern = decode_kernel<FORM, K, LPR, NR, NW, S, SB, MB>;
     const size_t smem = decode_smem_bytes<FORM, K, LPR, NR, NW, S, SB>(p.T, p.V);
     // the largest footprint any call can ask for (T = 16 with staged v)
     constexpr size_t smem_max = decode_smem_bytes<FORM, K, LPR, NR, NW, S, SB>(16, kStageVMax / 16);
@@ -529,10 +541,10 @@ lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
 }
 
 // Tile shapes per key size and pool type: a row is split over LPR lanes so each
-// lane holds whole 16-byte chunks (fp32 K = 128: 8 lanes x 4 chunks of 4; bf16
-// K = 128: 8 lanes x 2 chunks of 8); 32-row tiles at K = 128, a 2-stage ring
-// (one tile in flight while one is computed) for fp32 and a 3-stage ring for
-// bf16, whose tiles are half the bytes.
+// lane holds whole 16-byte chunks (fp32 K = 128: 8 lanes x 4 chunks of 4
+// elements); 32-row tiles at K = 128, a 2-stage ring (one tile in flight while
+// one is computed) for fp32 and a 3-stage ring for bf16, whose tiles are half
+// the bytes.  KDA caps registers so that 3 CTAs fit on an SM.
 template <int FORM>
 lar_status launch_form(const DecodeParams& p, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -541,7 +553,9 @@ lar_status launch_form(const DecodeParams& p, void* stream) {
             case 16: return launch_tile<FORM, 16, 4, 2, 2, 3, 4>(p, st);
             case 32: return launch_tile<FORM, 32, 8, 2, 4, 3, 4>(p, st);
             case 64: return launch_tile<FORM, 64, 8, 2, 4, 3, 4>(p, st);
-            case 128: return launch_tile<FORM, 128, 8, LAR_K128_NR, LAR_K128_NW, LAR_K128_S, 4>(p, st);
+            case 128:
+                return launch_tile<FORM, 128, LAR_K128_LPR, LAR_K128_NR, LAR_K128_NW, LAR_K128_S, 4,
+                                   FORM == FORM_KDA ? LAR_KDA_MIN_BLOCKS : 1>(p, st);
             default: return LAR_ERR_SHAPE;
         }
     }
@@ -549,7 +563,14 @@ lar_status launch_form(const DecodeParams& p, void* stream) {
         case 16: return launch_tile<FORM, 16, 2, 2, 2, 3, 2>(p, st);
         case 32: return launch_tile<FORM, 32, 4, 2, 4, 3, 2>(p, st);
         case 64: return launch_tile<FORM, 64, 8, 2, 4, 3, 2>(p, st);
-        case 128: return launch_tile<FORM, 128, 8, LAR_K128_NR, LAR_K128_NW, LAR_K128_BF16_S, 2>(p, st);
+        case 128:
+            // bf16 rows are half the bytes: GDN/LA give each lane 32 elements (4 lanes
+            // per row, one row per thread), which halves the per-row bookkeeping;
+            // KDA keeps 8 lanes per row to stay within its register budget.
+            if constexpr (FORM == FORM_KDA)
+                return launch_tile<FORM, 128, 8, 2, LAR_K128_NW, LAR_K128_BF16_S, 2, LAR_KDA_MIN_BLOCKS>(p, st);
+            else
+                return launch_tile<FORM, 128, 4, 1, LAR_K128_NW, LAR_K128_BF16_S, 2, 1>(p, st);
         default: return LAR_ERR_SHAPE;
     }
 }
