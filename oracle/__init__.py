@@ -31,6 +31,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
+# tests that plant mistakes in a copy of oracle.c point this at the mutated build
+_OVERRIDE = os.environ.get("LAR_ORACLE_LIB")
 _lock = threading.Lock()
 _lib = None
 
@@ -50,8 +52,11 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB)
+            if _OVERRIDE:
+                lib = ctypes.CDLL(_OVERRIDE)
+            else:
+                build()
+                lib = ctypes.CDLL(_LIB)
             dp = ctypes.POINTER(ctypes.c_double)
             ip = ctypes.POINTER(ctypes.c_int64)
             i64 = ctypes.c_int64
