@@ -66,6 +66,11 @@ def _load():
                 fn.restype = ctypes.c_long
                 fn.argtypes = [i64] * 6 + [dp] * 7 + [ctypes.c_int] * 3 + [
                     ctypes.c_double, vp, ctypes.c_int, i64, ip, ip, ip, dp, dp, dp]
+            for name in ("oracle_gdn_decode_tokens", "oracle_kda_decode_tokens"):
+                fn = getattr(lib, name)
+                fn.restype = ctypes.c_long
+                fn.argtypes = [i64] * 6 + [dp] * 7 + [ctypes.c_int] * 3 + [
+                    ctypes.c_double, vp, ctypes.c_int, i64, ip, ip, ip, ip, dp, dp, dp]
             lib.oracle_la_decode.restype = ctypes.c_long
             lib.oracle_la_decode.argtypes = [i64] * 5 + [dp] * 4 + [
                 ctypes.c_double, vp, ctypes.c_int, i64, ip, ip, ip, dp, dp, dp]
@@ -149,7 +154,7 @@ def _as_btx(x, name, ndim_full):
 
 
 def _delta(per_channel, q, k, v, g, beta, pool, read_idx, write_idx, A_log, dt_bias,
-           qk_l2norm, gate_raw, beta_raw, scale, cache_intermediate):
+           qk_l2norm, gate_raw, beta_raw, scale, cache_intermediate, tokens=None):
     lib = _load()
     q = _as_btxk(_f64(q), "q")
     k = _as_btxk(_f64(k), "k")
@@ -178,13 +183,25 @@ def _delta(per_channel, q, k, v, g, beta, pool, read_idx, write_idx, A_log, dt_b
     out = np.zeros((B, T, HV, V))
     fin = np.zeros((B, HV, V, K))
     inter = np.zeros((B, T, HV, V, K)) if cache_intermediate else None
-    fn = lib.oracle_kda_decode if per_channel else lib.oracle_gdn_decode
     dp = ctypes.c_double
-    bad = fn(B, T, H, HV, K, V, _ptr(q, dp), _ptr(k, dp), _ptr(v, dp), _ptr(g, dp),
-             _ptr(beta, dp), _ptr(A, dp), _ptr(D, dp), int(qk_l2norm), int(gate_raw),
-             int(beta_raw), float(scale), pptr, int(pbf), P, _ptr(st, ctypes.c_int64),
-             _ptr(ri, ctypes.c_int64), _ptr(wi, ctypes.c_int64), _ptr(out, dp),
-             _ptr(fin, dp), _ptr(inter, dp))
+    if tokens is None:
+        fn = lib.oracle_kda_decode if per_channel else lib.oracle_gdn_decode
+        bad = fn(B, T, H, HV, K, V, _ptr(q, dp), _ptr(k, dp), _ptr(v, dp), _ptr(g, dp),
+                 _ptr(beta, dp), _ptr(A, dp), _ptr(D, dp), int(qk_l2norm), int(gate_raw),
+                 int(beta_raw), float(scale), pptr, int(pbf), P, _ptr(st, ctypes.c_int64),
+                 _ptr(ri, ctypes.c_int64), _ptr(wi, ctypes.c_int64), _ptr(out, dp),
+                 _ptr(fin, dp), _ptr(inter, dp))
+    else:
+        na, sidx = _i64(tokens[0]), _i64(tokens[1])
+        if sidx.shape != (B, T):
+            raise ValueError("state_idx must be [B, T]")
+        fn = lib.oracle_kda_decode_tokens if per_channel else lib.oracle_gdn_decode_tokens
+        bad = fn(B, T, H, HV, K, V, _ptr(q, dp), _ptr(k, dp), _ptr(v, dp), _ptr(g, dp),
+                 _ptr(beta, dp), _ptr(A, dp), _ptr(D, dp), int(qk_l2norm), int(gate_raw),
+                 int(beta_raw), float(scale), pptr, int(pbf), P, _ptr(st, ctypes.c_int64),
+                 _ptr(ri, ctypes.c_int64), _ptr(na, ctypes.c_int64),
+                 _ptr(np.ascontiguousarray(sidx), ctypes.c_int64), _ptr(out, dp), _ptr(fin, dp),
+                 _ptr(inter, dp))
     if bad < 0:
         raise ValueError("oracle rejected its arguments")
     return {"out": out, "final_state": fin, "inter": inter, "n_bad": int(bad)}
@@ -204,6 +221,24 @@ def kda_decode(q, k, v, g, beta, pool, read_idx, write_idx=None, *, A_log=None,
     """KDA: per-key-channel log-decay g[b,t,hv,k]; see oracle.c."""
     return _delta(True, q, k, v, g, beta, pool, read_idx, write_idx, A_log, dt_bias,
                   qk_l2norm, gate_raw, beta_raw, scale, cache_intermediate)
+
+
+def gdn_decode_tokens(q, k, v, g, beta, pool, state_idx, *, read_idx=None, num_accepted=None,
+                      A_log=None, dt_bias=None, qk_l2norm=False, gate_raw=False, beta_raw=False,
+                      scale=1.0, cache_intermediate=False):
+    """GDN with per-token pool slots: the state after token t is written to slot
+    state_idx[b, t]; the seed comes from state_idx[b, num_accepted[b] - 1] when
+    num_accepted is given, else from read_idx[b]."""
+    return _delta(False, q, k, v, g, beta, pool, read_idx, None, A_log, dt_bias, qk_l2norm,
+                  gate_raw, beta_raw, scale, cache_intermediate, tokens=(num_accepted, state_idx))
+
+
+def kda_decode_tokens(q, k, v, g, beta, pool, state_idx, *, read_idx=None, num_accepted=None,
+                      A_log=None, dt_bias=None, qk_l2norm=False, gate_raw=False, beta_raw=False,
+                      scale=1.0, cache_intermediate=False):
+    """KDA with per-token pool slots (see gdn_decode_tokens)."""
+    return _delta(True, q, k, v, g, beta, pool, read_idx, None, A_log, dt_bias, qk_l2norm,
+                  gate_raw, beta_raw, scale, cache_intermediate, tokens=(num_accepted, state_idx))
 
 
 def la_decode(q, k, v, decay, pool, read_idx, write_idx=None, *, scale=1.0,

@@ -136,10 +136,19 @@ static long delta_rule(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, i
                        const double* g, const double* beta, const double* A_log,
                        const double* dt_bias, int qk_l2norm, int gate_raw, int beta_raw,
                        double scale, void* pool, int pool_bf16, int64_t P, const int64_t* st,
-                       const int64_t* read_idx, const int64_t* write_idx, double* out,
+                       const int64_t* read_idx, const int64_t* write_idx,
+                       const int64_t* num_accepted, const int64_t* state_idx, double* out,
                        double* final_state, double* inter) {
     if (B < 0 || T < 1 || H < 1 || HV < 1 || K < 1 || V < 1 || HV % H != 0) return -1;
     if (gate_raw && !A_log) return -1;
+    if (num_accepted && !state_idx) return -1;
+    if (!num_accepted && !read_idx) return -1;
+    /* per-token slots need every token's state: keep them even if the caller did not ask */
+    double* tok = inter;
+    if (state_idx && !tok) {
+        tok = (double*)malloc(sizeof(double) * (size_t)(B * T * HV * V * K));
+        if (!tok && B > 0) return -1;
+    }
     const int64_t group = HV / H;
     long bad = 0;
 
@@ -156,7 +165,21 @@ static long delta_rule(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, i
 
     /* phase 1: every state is read and advanced before anything is written */
     for (int64_t b = 0; b < B; ++b) {
-        const int64_t r = read_idx[b];
+        int64_t r;
+        if (num_accepted) {
+            /* the seed is the state stored after the last accepted token: slot
+               state_idx[b][num_accepted[b] - 1]; a count outside [1, T] has no
+               such slot and is counted, with a zero seed */
+            const int64_t a = num_accepted[b];
+            if (a >= 1 && a <= T) {
+                r = state_idx[b * T + a - 1];
+            } else {
+                r = -1;
+                ++bad;
+            }
+        } else {
+            r = read_idx[b];
+        }
         if (r >= P) ++bad;
         for (int64_t hv = 0; hv < HV; ++hv) {
             const int64_t h = hv / group;
@@ -213,8 +236,8 @@ static long delta_rule(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, i
                     for (int64_t kk = 0; kk < K; ++kk) acc += S[kk * V + vv] * qh[kk];
                     out[((b * T + t) * HV + hv) * V + vv] = scale * acc;
                 }
-                if (inter) {
-                    double* it = inter + (((b * T + t) * HV + hv) * V) * K;
+                if (tok) {
+                    double* it = tok + (((b * T + t) * HV + hv) * V) * K;
                     for (int64_t vv = 0; vv < V; ++vv)
                         for (int64_t kk = 0; kk < K; ++kk) it[vv * K + kk] = S[kk * V + vv];
                 }
@@ -224,6 +247,27 @@ static long delta_rule(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, i
             for (int64_t vv = 0; vv < V; ++vv)
                 for (int64_t kk = 0; kk < K; ++kk) f[vv * K + kk] = S[kk * V + vv];
         }
+    }
+
+    /* phase 2, per-token slots: the state after token t goes to slot state_idx[b][t]
+       (in token order); negative skips, >= P is counted and skipped */
+    if (state_idx) {
+        for (int64_t b = 0; b < B; ++b)
+            for (int64_t t = 0; t < T; ++t) {
+                const int64_t w = state_idx[b * T + t];
+                if (w < 0) continue;
+                if (w >= P) { ++bad; continue; }
+                for (int64_t hv = 0; hv < HV; ++hv) {
+                    const double* f = tok + (((b * T + t) * HV + hv) * V) * K;
+                    for (int64_t vv = 0; vv < V; ++vv)
+                        for (int64_t kk = 0; kk < K; ++kk)
+                            pool_put(pool, pool_bf16, st, w, hv, vv, kk, f[vv * K + kk]);
+                }
+            }
+        if (tok != inter) free(tok);
+        free(S); free(qh); free(kh); free(gk); free(u);
+        if (fin != final_state) free(fin);
+        return bad;
     }
 
     /* phase 2: writeback to the write slot; negative skips, >= P is counted and skipped */
@@ -252,7 +296,7 @@ long oracle_gdn_decode(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, i
                        double* inter) {
     return delta_rule(B, T, H, HV, K, V, 0, q, k, v, g, beta, A_log, dt_bias, qk_l2norm,
                       gate_raw, beta_raw, scale, pool, pool_bf16, P, pool_strides, read_idx, write_idx,
-                      out, final_state, inter);
+                      NULL, NULL, out, final_state, inter);
 }
 
 long oracle_kda_decode(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V,
@@ -264,7 +308,44 @@ long oracle_kda_decode(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, i
                        double* inter) {
     return delta_rule(B, T, H, HV, K, V, 1, q, k, v, g, beta, A_log, dt_bias, qk_l2norm,
                       gate_raw, beta_raw, scale, pool, pool_bf16, P, pool_strides, read_idx, write_idx,
-                      out, final_state, inter);
+                      NULL, NULL, out, final_state, inter);
+}
+
+/*
+ * Multi-token decode with per-token pool slots (the aiter review's paged
+ * per-token state slots and speculative seed):
+ *   state_idx    [B, T]: slot that receives the state after token t of entry b
+ *   num_accepted [B] or NULL: when given, the seed state is read from slot
+ *                state_idx[b][num_accepted[b] - 1] (the state after the last
+ *                accepted token of the previous step); otherwise from read_idx[b].
+ * Everything else as oracle_gdn_decode / oracle_kda_decode (no write_idx).
+ */
+long oracle_gdn_decode_tokens(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V,
+                              const double* q, const double* k, const double* v, const double* g,
+                              const double* beta, const double* A_log, const double* dt_bias,
+                              int qk_l2norm, int gate_raw, int beta_raw, double scale, void* pool,
+                              int pool_bf16, int64_t P, const int64_t* pool_strides,
+                              const int64_t* read_idx, const int64_t* num_accepted,
+                              const int64_t* state_idx, double* out, double* final_state,
+                              double* inter) {
+    if (!state_idx) return -1;
+    return delta_rule(B, T, H, HV, K, V, 0, q, k, v, g, beta, A_log, dt_bias, qk_l2norm,
+                      gate_raw, beta_raw, scale, pool, pool_bf16, P, pool_strides, read_idx, NULL,
+                      num_accepted, state_idx, out, final_state, inter);
+}
+
+long oracle_kda_decode_tokens(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V,
+                              const double* q, const double* k, const double* v, const double* g,
+                              const double* beta, const double* A_log, const double* dt_bias,
+                              int qk_l2norm, int gate_raw, int beta_raw, double scale, void* pool,
+                              int pool_bf16, int64_t P, const int64_t* pool_strides,
+                              const int64_t* read_idx, const int64_t* num_accepted,
+                              const int64_t* state_idx, double* out, double* final_state,
+                              double* inter) {
+    if (!state_idx) return -1;
+    return delta_rule(B, T, H, HV, K, V, 1, q, k, v, g, beta, A_log, dt_bias, qk_l2norm,
+                      gate_raw, beta_raw, scale, pool, pool_bf16, P, pool_strides, read_idx, NULL,
+                      num_accepted, state_idx, out, final_state, inter);
 }
 
 /*

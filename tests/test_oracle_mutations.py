@@ -43,6 +43,9 @@ MUTATIONS = {
                                    "        if (w < 0) w = 0;\n        if (w >= P) { ++bad; continue; }\n"
                                    "        for (int64_t hv"),
     "bf16_truncates": ("const double r = nearbyint(ax / q) * q;", "const double r = floor(ax / q) * q;"),
+    "seed_off_by_one": ("r = state_idx[b * T + a - 1];", "r = state_idx[b * T + (a < T ? a : a - 1)];"),
+    "token_state_shifted": ("const double* f = tok + (((b * T + t) * HV + hv) * V) * K;",
+                            "const double* f = tok + (((b * T + (t > 0 ? t - 1 : t)) * HV + hv) * V) * K;"),
 }
 
 

@@ -457,3 +457,68 @@ def test_bf16_la_flat_pool():
             exp = [oracle.round_bf16(x) for x in a["final_state"][bi, h].ravel().tolist()]
             got = (pb[row].view(torch.int16).to(torch.int32) & 0xFFFF).ravel().tolist()
             assert got == exp
+
+
+# --------------------------------------------------------------------------- per-token pool slots
+
+def _tok_case(per_channel, seed=17, B=3, T=4, P=16):
+    q, k, v, g, beta, pool, _, _ = _rand_delta_case(per_channel, B=B, T=T, P=P, seed=seed)
+    slots = torch.randperm(P, generator=torch.Generator().manual_seed(seed))[:B * T].view(B, T)
+    return q, k, v, g, beta, pool, slots
+
+
+@pytest.mark.parametrize("per_channel", [False, True])
+def test_token_slots_hold_the_cached_states(per_channel):
+    """Per-token slots receive exactly the states the intermediate cache holds
+    (the state after token t), rounded to the pool type; nothing else changes."""
+    q, k, v, g, beta, pool, slots = _tok_case(per_channel)
+    ri = torch.tensor([3, -1, 9])
+    p_plain, p_tok = pool.clone(), pool.clone()
+    fn = oracle.kda_decode if per_channel else oracle.gdn_decode
+    tfn = oracle.kda_decode_tokens if per_channel else oracle.gdn_decode_tokens
+    ref = fn(q, k, v, g, beta, p_plain, ri, torch.full((3,), -1), cache_intermediate=True)
+    res = tfn(q, k, v, g, beta, p_tok, slots, read_idx=ri)
+    assert np.array_equal(res["out"], ref["out"])
+    for b in range(3):
+        for t in range(4):
+            s = int(slots[b, t])
+            assert torch.equal(p_tok[s], torch.from_numpy(ref["inter"][b, t]).float())
+    others = [p for p in range(pool.shape[0]) if p not in slots.view(-1).tolist()]
+    assert torch.equal(p_tok[others], pool[others])
+
+
+def test_seed_is_the_state_after_the_last_accepted_token():
+    """Speculative flow with one slot row per sequence, reused every step.
+    Step 1 (seeded from a plain slot) stores the state after each token in the
+    row; with a tokens accepted, (1) slot row[a-1] holds the state of running
+    only those a tokens, and (2) step 2 seeded by num_accepted = a equals step
+    2 seeded explicitly from slot row[a-1]."""
+    q, k, v, g, beta, pool0, _ = _tok_case(False, B=2, T=4, P=24)
+    table = torch.tensor([[3, 7, 1, 12], [5, 0, 9, 2]])
+    seeds = torch.tensor([20, 21])
+    pool = pool0.clone()
+    oracle.gdn_decode_tokens(q, k, v, g, beta, pool, table, read_idx=seeds)          # step 1
+    accepted = torch.tensor([2, 4])
+    for b in range(2):
+        a = int(accepted[b])
+        chained = oracle.gdn_decode(q[b:b + 1, :a], k[b:b + 1, :a], v[b:b + 1, :a], g[b:b + 1, :a],
+                                    beta[b:b + 1, :a], pool0.clone(), seeds[b:b + 1],
+                                    torch.full((1,), -1))
+        np.testing.assert_allclose(pool[int(table[b, a - 1])].double().numpy(),
+                                   chained["final_state"][0], rtol=1e-6, atol=1e-7)
+    q2, k2, v2, g2, beta2, _, _ = _tok_case(False, seed=99, B=2, T=4, P=24)
+    pa, pb = pool.clone(), pool.clone()
+    tok = oracle.gdn_decode_tokens(q2, k2, v2, g2, beta2, pa, table, num_accepted=accepted)  # step 2
+    explicit = oracle.gdn_decode_tokens(q2, k2, v2, g2, beta2, pb, table,
+                                        read_idx=torch.tensor([int(table[0, 1]), int(table[1, 3])]))
+    assert np.array_equal(tok["out"], explicit["out"])
+    assert torch.equal(pa, pb)
+
+
+def test_accepted_count_outside_range_is_counted_with_zero_seed():
+    q, k, v, g, beta, pool, slots = _tok_case(True, B=3, T=4)
+    p1, p2 = pool.clone(), pool.clone()
+    res = oracle.kda_decode_tokens(q, k, v, g, beta, p1, slots, num_accepted=torch.tensor([0, 5, 4]))
+    assert res["n_bad"] == 2
+    zero = oracle.kda_decode_tokens(q, k, v, g, beta, p2, slots, read_idx=torch.tensor([-1, -1, int(slots[2, 3])]))
+    assert np.array_equal(res["out"], zero["out"])
