@@ -33,8 +33,8 @@ MUTATIONS = {
     "la_row_index": ("const int64_t row = r * H + h;", "const int64_t row = r + h * P;"),
     "scale_dropped": ("out[((b * T + t) * HV + hv) * V + vv] = scale * acc;",
                       "out[((b * T + t) * HV + hv) * V + vv] = acc;"),
-    "cache_shifted": ("if (inter) {\n                    double* it = inter + (((b * T + t) * HV + hv) * V) * K;",
-                      "if (inter && t > 0) {\n                    double* it = inter + (((b * T + t - 1) * HV + hv) * V) * K;"),
+    "cache_shifted": ("if (tok) {\n                    double* it = tok + (((b * T + t) * HV + hv) * V) * K;",
+                      "if (tok && t > 0) {\n                    double* it = tok + (((b * T + t - 1) * HV + hv) * V) * K;"),
     "kda_channel_reversed": ("dt_bias[hv * K + kk]", "dt_bias[hv * K + (K - 1 - kk)]"),
     "negative_write_not_skipped": ("        const int64_t w = write_idx ? write_idx[b] : read_idx[b];\n"
                                    "        if (w < 0) continue;\n        if (w >= P) { ++bad; continue; }\n"
