@@ -108,7 +108,8 @@ enum {
 /* bits OR-ed into *dev_err */
 enum {
     LAR_DEVERR_READ_SLOT = 1,  /* some read_idx[b] >= P (that entry started from zero) */
-    LAR_DEVERR_WRITE_SLOT = 2  /* some write_idx[b] >= P (that writeback was skipped) */
+    LAR_DEVERR_WRITE_SLOT = 2, /* some write slot >= P (that writeback was skipped) */
+    LAR_DEVERR_ACCEPTED = 4    /* some num_accepted[b] outside [1, T] (that entry started from zero) */
 };
 
 /*
@@ -159,6 +160,45 @@ lar_status la_decode(const lar_tensor* q, const lar_tensor* k, const lar_tensor*
                      const lar_tensor* read_idx, const lar_tensor* write_idx,
                      const lar_tensor* out, const lar_tensor* inter,
                      float scale, int32_t* dev_err, void* stream);
+
+/*
+ * Multi-token decode with per-token pool slots (speculative / MTP verify).
+ * The aiter KDA review describes these paged per-token state slots and the
+ * seed chosen by the number of accepted draft tokens, and lists the two ways
+ * such a wrapper went wrong (a flat index table read with the wrong row
+ * stride; an accepted count of 0 reading before its row); both are closed here.
+ *
+ *   state_idx     int32/int64 [B, T] (rank 2 only): the state after token t of
+ *                 entry b is written to pool slot state_idx[b][t]; a negative
+ *                 slot skips that store.  There is no other writeback.
+ *   num_accepted  int32/int64 [B] or NULL: the seed state of entry b is read
+ *                 from slot state_idx[b][num_accepted[b] - 1] (the state after
+ *                 the last accepted token of the previous step, which stored
+ *                 its token states in the same row).  A count outside [1, T]
+ *                 starts that entry from a zero state and sets
+ *                 LAR_DEVERR_ACCEPTED.
+ *   read_idx      [B] or NULL: the seed slot when num_accepted is NULL.
+ *                 Exactly one of read_idx and num_accepted must be given.
+ * All other arguments as gdn_decode / kda_decode (no write_idx, no inter).
+ * The seed of an entry may be one of its own per-token slots (each state row
+ * is read before it is overwritten); across entries the aliasing rules of
+ * gdn_decode apply.
+ */
+lar_status gdn_decode_tokens(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                             const lar_tensor* g, const lar_tensor* beta,
+                             const lar_tensor* A_log, const lar_tensor* dt_bias,
+                             const lar_tensor* pool, const lar_tensor* read_idx,
+                             const lar_tensor* num_accepted, const lar_tensor* state_idx,
+                             const lar_tensor* out, float scale, uint32_t flags,
+                             int32_t* dev_err, void* stream);
+
+lar_status kda_decode_tokens(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                             const lar_tensor* g, const lar_tensor* beta,
+                             const lar_tensor* A_log, const lar_tensor* dt_bias,
+                             const lar_tensor* pool, const lar_tensor* read_idx,
+                             const lar_tensor* num_accepted, const lar_tensor* state_idx,
+                             const lar_tensor* out, float scale, uint32_t flags,
+                             int32_t* dev_err, void* stream);
 
 /* Static, human-readable name of a status code. */
 const char* lar_status_string(lar_status status);

@@ -16,7 +16,7 @@ _LIB_PATH = _build.LIB
 
 LAR_F32, LAR_BF16, LAR_I32, LAR_I64 = 0, 1, 2, 3
 LAR_QK_L2NORM, LAR_GATE_RAW, LAR_BETA_RAW = 1, 2, 4
-LAR_DEVERR_READ_SLOT, LAR_DEVERR_WRITE_SLOT = 1, 2
+LAR_DEVERR_READ_SLOT, LAR_DEVERR_WRITE_SLOT, LAR_DEVERR_ACCEPTED = 1, 2, 4
 
 STATUS = {0: "LAR_OK", 1: "LAR_ERR_NULL", 2: "LAR_ERR_DTYPE", 3: "LAR_ERR_RANK",
           4: "LAR_ERR_SHAPE", 5: "LAR_ERR_STRIDE", 6: "LAR_ERR_ALIGN", 7: "LAR_ERR_ARG",
@@ -56,6 +56,10 @@ def load() -> ctypes.CDLL:
         P = ctypes.POINTER(LarTensor)
         tail = [ctypes.c_float, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p]
         for name in ("gdn_decode", "kda_decode"):
+            fn = getattr(lib, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = [P] * 12 + tail
+        for name in ("gdn_decode_tokens", "kda_decode_tokens"):
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [P] * 12 + tail
@@ -130,6 +134,39 @@ def _delta(name, q, k, v, g, beta, pool, read_idx, write_idx, out, inter, A_log,
         out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
     ds = [describe(t) for t in (q, k, v, g, beta, A_log, dt_bias, pool, read_idx, write_idx, out,
                                 inter)]
+    err = dev_err.data_ptr() if dev_err is not None else None
+    st = getattr(lib, name)(*[_ref(d) for d in ds], float(scale), flags, err, _stream(stream))
+    _check(name, st)
+    return out
+
+
+def gdn_decode_tokens(q, k, v, g, beta, pool, state_idx, *, read_idx=None, num_accepted=None,
+                      out=None, A_log=None, dt_bias=None, scale=1.0, qk_l2norm=False,
+                      gate_raw=False, beta_raw=False, dev_err=None, out_dtype=None, stream=None):
+    """GDN with per-token pool slots: the state after token t goes to slot
+    state_idx[b, t]; the seed is slot state_idx[b, num_accepted[b] - 1] (or
+    read_idx[b] when num_accepted is None)."""
+    return _tokens("gdn_decode_tokens", q, k, v, g, beta, pool, state_idx, read_idx, num_accepted,
+                   out, A_log, dt_bias, scale, _flags(qk_l2norm, gate_raw, beta_raw), dev_err,
+                   out_dtype, stream)
+
+
+def kda_decode_tokens(q, k, v, g, beta, pool, state_idx, *, read_idx=None, num_accepted=None,
+                      out=None, A_log=None, dt_bias=None, scale=1.0, qk_l2norm=False,
+                      gate_raw=False, beta_raw=False, dev_err=None, out_dtype=None, stream=None):
+    """KDA with per-token pool slots (see gdn_decode_tokens)."""
+    return _tokens("kda_decode_tokens", q, k, v, g, beta, pool, state_idx, read_idx, num_accepted,
+                   out, A_log, dt_bias, scale, _flags(qk_l2norm, gate_raw, beta_raw), dev_err,
+                   out_dtype, stream)
+
+
+def _tokens(name, q, k, v, g, beta, pool, state_idx, read_idx, num_accepted, out, A_log, dt_bias,
+            scale, flags, dev_err, out_dtype, stream):
+    lib = load()
+    if out is None:
+        out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
+    ds = [describe(t) for t in (q, k, v, g, beta, A_log, dt_bias, pool, read_idx, num_accepted,
+                                state_idx, out)]
     err = dev_err.data_ptr() if dev_err is not None else None
     st = getattr(lib, name)(*[_ref(d) for d in ds], float(scale), flags, err, _stream(stream))
     _check(name, st)

@@ -163,7 +163,8 @@ __host__ __device__ constexpr int vec_floats(int T, int V) {
 template <int FORM, int K, int LPR, int NR, int NW, int S, int SB>
 __host__ __device__ constexpr size_t decode_smem_bytes(int T, int V) {
     using G = Tile<K, LPR, NR, NW, SB>;
-    return static_cast<size_t>(S) * G::TV * K * SB + 2 * static_cast<size_t>(vec_floats<FORM, K>(T, V)) * sizeof(float);
+    return static_cast<size_t>(S) * G::TV * K * SB + 2 * static_cast<size_t>(vec_floats<FORM, K>(T, V)) * sizeof(float) +
+           2 * kMaxTokens * sizeof(long long);   // per-pair tables of per-token write slots
 }
 
 template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB>
@@ -178,6 +179,7 @@ decode_kernel(const DecodeParams p) {
     const bool sv_on = stage_v(T, V);
     unsigned char* ring = smem;                                               // [S][TV][K] pool elements
     float* vecs = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * TV * K * SB);  // 2 x vec_floats
+    long long* slot_tab = reinterpret_cast<long long*>(vecs + 2 * vec_floats<FORM, K>(T, V));  // 2 x kMaxTokens
     const unsigned char* pool_b = static_cast<const unsigned char*>(p.pool);
     const bool inter_bf16 = p.inter_dt == LAR_BF16;
     const int inter_es = inter_bf16 ? 2 : 4;
@@ -248,11 +250,22 @@ decode_kernel(const DecodeParams p) {
     // read slot of a prefetch position, reloaded only when its batch entry changes
     int ahead_b = -1;
     int64_t ahead_r = -1;
+    // Read slot of entry b: read_idx[b], or, with accepted-token counts, the
+    // slot that holds the state after the last accepted token,
+    // state_idx[b][num_accepted[b] - 1]; a count outside [1, T] has no such
+    // slot and yields kBadCount (zero seed, flagged).
+    constexpr int64_t kBadCount = INT64_MIN;
+    auto seed_of = [&](int b) -> int64_t {
+        if (p.nacc == nullptr) return ld_idx(p.ridx, b * p.ri_s, p.ri_dt);
+        const int64_t a = ld_idx(p.nacc, b * p.na_s, p.na_dt);
+        if (a < 1 || a > T) return kBadCount;
+        return ld_idx(p.tslot, b * p.tsl_s[0] + (a - 1) * p.tsl_s[1], p.tsl_dt);
+    };
     auto slot_of = [&](const Pos& q) -> int64_t {
         if (q.tile >= t_end) return -1;
         if (q.b != ahead_b) {
             ahead_b = q.b;
-            ahead_r = ld_idx(p.ridx, q.b * p.ri_s, p.ri_dt);
+            ahead_r = seed_of(q.b);
         }
         return ahead_r;
     };
@@ -303,12 +316,21 @@ decode_kernel(const DecodeParams p) {
             // ---- new (b, hv) pair: slots, bases and per-token vectors
             const int h = hv / p.group;
             buf ^= 1;
-            const int64_t r = ld_idx(p.ridx, b * p.ri_s, p.ri_dt);
-            const int64_t w = p.widx ? ld_idx(p.widx, b * p.wi_s, p.wi_dt) : r;
+            const int64_t r = seed_of(b);
+            // with per-token slots every token's state is stored; there is no final writeback
+            const int64_t w = p.tslot ? -1 : (p.widx ? ld_idx(p.widx, b * p.wi_s, p.wi_dt) : r);
             rd = r >= 0 && r < p.P;
             wr = w >= 0 && w < p.P;
+            long long* tab = slot_tab + buf * kMaxTokens;
+            if (p.tslot)
+                for (int t = threadIdx.x; t < T; t += NW * 32)
+                    tab[t] = ld_idx(p.tslot, b * p.tsl_s[0] + t * p.tsl_s[1], p.tsl_dt);
             if (threadIdx.x == 0 && hv == 0 && p.dev_err) {
-                const int e = (r >= p.P ? LAR_DEVERR_READ_SLOT : 0) | (w >= p.P ? LAR_DEVERR_WRITE_SLOT : 0);
+                int e = (r >= p.P ? LAR_DEVERR_READ_SLOT : 0) | (w >= p.P ? LAR_DEVERR_WRITE_SLOT : 0) |
+                        (r == kBadCount ? LAR_DEVERR_ACCEPTED : 0);
+                if (p.tslot)
+                    for (int t = 0; t < T; ++t)
+                        if (ld_idx(p.tslot, b * p.tsl_s[0] + t * p.tsl_s[1], p.tsl_dt) >= p.P) e |= LAR_DEVERR_WRITE_SLOT;
                 if (e) atomicOr(p.dev_err, e);
             }
             dst_state = static_cast<unsigned char*>(p.pool) +
@@ -484,6 +506,16 @@ decode_kernel(const DecodeParams p) {
                     const int cstep = LPR * EPC * inter_es;
 #pragma unroll
                     for (int c = 0; c < NCH; ++c) store_run<EPC>(ip + c * cstep, &s[i][c * EPC], inter_bf16);
+                }
+                if (p.tslot != nullptr && rv) {
+                    const long long ts = slot_tab[buf * kMaxTokens + t];
+                    if (ts >= 0 && ts < p.P) {
+                        unsigned char* tp = static_cast<unsigned char*>(p.pool) +
+                                            (ts * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1]) * SB +
+                                            vt * g_tile + g_row0 + i * g_rstep;
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) store_run<EPC>(tp + c * CSTEP, &s[i][c * EPC], SB == 2);
+                    }
                 }
             }
         }

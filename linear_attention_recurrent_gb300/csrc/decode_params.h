@@ -31,6 +31,9 @@ struct DecodeParams {
     const void* ridx; int64_t ri_s; int ri_dt;
     const void* widx; int64_t wi_s; int wi_dt;    // NULL: write to the read slot
 
+    const void* nacc;  int64_t na_s; int na_dt;     // accepted-token counts [B] or NULL (seed selection)
+    const void* tslot; int64_t tsl_s[2]; int tsl_dt; // per-token write slots [B, T] or NULL
+
     void* out;    int64_t os[4]; int out_dt;
     void* inter; int64_t is[4]; int inter_dt;     // fp32 or bf16; b, t, head, row (k stride 1); may be NULL
 
@@ -42,5 +45,8 @@ struct DecodeParams {
 lar_status launch_gdn(const DecodeParams& p, void* stream);
 lar_status launch_kda(const DecodeParams& p, void* stream);
 lar_status launch_la(const DecodeParams& p, void* stream);
+
+// Largest T a call may use (per-pair token tables are sized for it).
+constexpr int kMaxTokens = 16;
 
 }  // namespace lar

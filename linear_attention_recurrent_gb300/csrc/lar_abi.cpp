@@ -244,15 +244,41 @@ lar_status check_vec(const lar_tensor* t, int64_t n, const float** ptr, int64_t*
     return LAR_OK;
 }
 
+// num_accepted / state_idx select the per-token-slot mode (state_idx != NULL).
 lar_status delta_rule(int form, const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
                       const lar_tensor* g, const lar_tensor* beta, const lar_tensor* A_log,
                       const lar_tensor* dt_bias, const lar_tensor* pool, const lar_tensor* read_idx,
-                      const lar_tensor* write_idx, const lar_tensor* out, const lar_tensor* inter,
+                      const lar_tensor* write_idx, const lar_tensor* num_accepted,
+                      const lar_tensor* state_idx, const lar_tensor* out, const lar_tensor* inter,
                       float scale, uint32_t flags, int32_t* dev_err, void* stream) {
     DecodeParams p{};
     if (flags & ~static_cast<uint32_t>(LAR_QK_L2NORM | LAR_GATE_RAW | LAR_BETA_RAW)) return LAR_ERR_ARG;
-    lar_status st = check_common(Common{q, k, v, pool, read_idx, write_idx, out, inter}, form, p);
+    const bool tok = state_idx != nullptr;
+    if (tok && (read_idx == nullptr) == (num_accepted == nullptr)) return LAR_ERR_ARG;
+    // the seed source ([B] index vector) goes through the common checks as the read index
+    const lar_tensor* seed = read_idx ? read_idx : num_accepted;
+    lar_status st = check_common(Common{q, k, v, pool, seed, write_idx, out, inter}, form, p);
     if (st != LAR_OK) return st;
+    p.nacc = nullptr; p.na_s = 0; p.na_dt = LAR_I32;
+    p.tslot = nullptr; p.tsl_s[0] = p.tsl_s[1] = 0; p.tsl_dt = LAR_I32;
+    if (tok) {
+        if (missing(state_idx)) return LAR_ERR_NULL;
+        if ((st = check_header(state_idx)) != LAR_OK) return st;
+        // rank 2 only: a flat table read with a guessed row stride is the bug the aiter review found
+        if (state_idx->ndim != 2) return LAR_ERR_RANK;
+        if (state_idx->shape[0] != p.B || state_idx->shape[1] != p.T) return LAR_ERR_SHAPE;
+        if (!is_index(state_idx)) return LAR_ERR_DTYPE;
+        p.tslot = state_idx->data;
+        p.tsl_s[0] = state_idx->stride[0];
+        p.tsl_s[1] = state_idx->stride[1];
+        p.tsl_dt = state_idx->dtype;
+        if (num_accepted) {
+            p.nacc = num_accepted->data;
+            p.na_s = num_accepted->stride[0];
+            p.na_dt = num_accepted->dtype;
+            p.ridx = nullptr;
+        }
+    }
     if (missing(g) || missing(beta)) return LAR_ERR_NULL;
     if ((st = check_header(g)) != LAR_OK) return st;
     if ((st = check_header(beta)) != LAR_OK) return st;
@@ -286,8 +312,8 @@ lar_status delta_rule(int form, const lar_tensor* q, const lar_tensor* k, const 
     p.dev_err = dev_err;
 
     const lar_tensor* outs[] = {pool, out, inter};
-    const lar_tensor* ins[] = {q, k, v, g, beta, A_log, dt_bias, read_idx, write_idx};
-    st = check_aliasing(outs, 3, ins, 9);
+    const lar_tensor* ins[] = {q, k, v, g, beta, A_log, dt_bias, read_idx, write_idx, num_accepted, state_idx};
+    st = check_aliasing(outs, 3, ins, 11);
     if (st != LAR_OK) return st;
     if (p.B == 0) return LAR_OK;
     return kda ? lar::launch_kda(p, stream) : lar::launch_gdn(p, stream);
@@ -304,7 +330,7 @@ lar_status gdn_decode(const lar_tensor* q, const lar_tensor* k, const lar_tensor
                       const lar_tensor* out, const lar_tensor* inter, float scale, uint32_t flags,
                       int32_t* dev_err, void* stream) {
     return delta_rule(lar::FORM_GDN, q, k, v, g, beta, A_log, dt_bias, pool, read_idx, write_idx,
-                      out, inter, scale, flags, dev_err, stream);
+                      nullptr, nullptr, out, inter, scale, flags, dev_err, stream);
 }
 
 lar_status kda_decode(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
@@ -314,7 +340,29 @@ lar_status kda_decode(const lar_tensor* q, const lar_tensor* k, const lar_tensor
                       const lar_tensor* out, const lar_tensor* inter, float scale, uint32_t flags,
                       int32_t* dev_err, void* stream) {
     return delta_rule(lar::FORM_KDA, q, k, v, g, beta, A_log, dt_bias, pool, read_idx, write_idx,
-                      out, inter, scale, flags, dev_err, stream);
+                      nullptr, nullptr, out, inter, scale, flags, dev_err, stream);
+}
+
+lar_status gdn_decode_tokens(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                             const lar_tensor* g, const lar_tensor* beta, const lar_tensor* A_log,
+                             const lar_tensor* dt_bias, const lar_tensor* pool,
+                             const lar_tensor* read_idx, const lar_tensor* num_accepted,
+                             const lar_tensor* state_idx, const lar_tensor* out, float scale,
+                             uint32_t flags, int32_t* dev_err, void* stream) {
+    if (!state_idx) return LAR_ERR_NULL;
+    return delta_rule(lar::FORM_GDN, q, k, v, g, beta, A_log, dt_bias, pool, read_idx, nullptr,
+                      num_accepted, state_idx, out, nullptr, scale, flags, dev_err, stream);
+}
+
+lar_status kda_decode_tokens(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                             const lar_tensor* g, const lar_tensor* beta, const lar_tensor* A_log,
+                             const lar_tensor* dt_bias, const lar_tensor* pool,
+                             const lar_tensor* read_idx, const lar_tensor* num_accepted,
+                             const lar_tensor* state_idx, const lar_tensor* out, float scale,
+                             uint32_t flags, int32_t* dev_err, void* stream) {
+    if (!state_idx) return LAR_ERR_NULL;
+    return delta_rule(lar::FORM_KDA, q, k, v, g, beta, A_log, dt_bias, pool, read_idx, nullptr,
+                      num_accepted, state_idx, out, nullptr, scale, flags, dev_err, stream);
 }
 
 lar_status la_decode(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
@@ -328,6 +376,7 @@ lar_status la_decode(const lar_tensor* q, const lar_tensor* k, const lar_tensor*
     st = check_vec(decay, p.H, &p.decay, &p.dec_s);
     if (st != LAR_OK) return st;
     p.g = nullptr; p.beta = nullptr; p.A_log = nullptr; p.dt_bias = nullptr;
+    p.nacc = nullptr; p.tslot = nullptr;
     p.scale = scale;
     p.flags = 0;
     p.dev_err = dev_err;

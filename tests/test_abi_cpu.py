@@ -154,3 +154,24 @@ def test_la_rejects_on_host(lib):
     # 4D pool whose slot stride is not H * head stride cannot be the flat layout
     assert la_call(lib, pool=fake([5, 4, 128, 128], strides=[8 * 128 * 128, 128 * 128, 128, 1])) == STRIDE
     assert la_call(lib, B=0) == OK
+
+
+def tok_call(lib, a, state_idx, read_idx="default", num_accepted=None):
+    ri = a["read_idx"] if read_idx == "default" else read_idx
+    args = [a[n] for n in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "pool")] + [ri, num_accepted,
+                                                                                         state_idx, a["out"]]
+    refs = [ctypes.byref(x) if x is not None else None for x in args]
+    return lib.gdn_decode_tokens(*refs, 1.0, 0, None, None)
+
+
+def test_token_slots_rejects_on_host(lib):
+    a = gdn_args(B=2, T=3)
+    good = fake([2, 3], I32)
+    assert tok_call(lib, a, None) == NULL
+    assert tok_call(lib, a, fake([6], I32)) == RANK                   # flat table: rejected, not guessed
+    assert tok_call(lib, a, fake([2, 4], I32)) == SHAPE
+    assert tok_call(lib, a, fake([2, 3], F32)) == DTYPE
+    assert tok_call(lib, a, good, read_idx=None) == ARG               # no seed source
+    assert tok_call(lib, a, good, num_accepted=fake([2], I32)) == ARG  # two seed sources
+    assert tok_call(lib, a, good, read_idx=None, num_accepted=fake([3], I32)) == SHAPE
+    assert tok_call(lib, gdn_args(B=0, T=3), fake([0, 3], I32)) == OK

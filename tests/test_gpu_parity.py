@@ -274,3 +274,102 @@ def test_empty_batch_changes_nothing(cuda_device):
     out = P.run_gpu(w, dev, pool=pool)[0]
     torch.cuda.synchronize()
     assert out.shape[0] == 0 and torch.equal(pool, before)
+
+
+# ---------------------------------------------------------------- per-token pool slots
+
+def _token_case(form, B, T, seed, state_dtype=F32, HV=4, H=2):
+    w = W.make_custom(form, B=B, T=T, H=H, HV=HV, K=128, V=96, P=B * T + B + 3, seed=seed,
+                      raw_gates=form == "kda", state_dtype=state_dtype)
+    g = torch.Generator().manual_seed(seed + 1)
+    perm = torch.randperm(w.P, generator=g)
+    table = perm[:B * T].view(B, T).clone()
+    seeds = perm[B * T:B * T + B].clone()
+    table[0, -1] = -1                                    # a skipped token store
+    return w, table, seeds
+
+
+@pytest.mark.parametrize("form", ["gdn", "kda"])
+@pytest.mark.parametrize("state_dtype", [F32, torch.bfloat16])
+@pytest.mark.parametrize("use_accepted", [False, True])
+def test_token_slots_against_oracle(form, state_dtype, use_accepted, cuda_device):
+    import linear_attention_recurrent_gb300 as lar
+    import oracle
+    dev = cuda_device
+    B, T = 5, 4
+    w, table, seeds = _token_case(form, B, T, seed=30 + T, state_dtype=state_dtype)
+    host = w.pool.clone()
+    pool = w.pool.to(dev)
+    before = pool.clone()
+    kw = dict(A_log=w.A_log, dt_bias=w.dt_bias, qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw,
+              beta_raw=w.beta_raw)
+    if use_accepted:
+        acc = torch.tensor([1, 4, 2, 3, 4])
+        acc_seed = {"num_accepted": acc}
+        # the seeds live in the table row: make them valid states first (they are: pool slots)
+    else:
+        acc_seed = {"read_idx": seeds}
+    ofn = oracle.kda_decode_tokens if form == "kda" else oracle.gdn_decode_tokens
+    gfn = lar.kda_decode_tokens if form == "kda" else lar.gdn_decode_tokens
+    ref = ofn(w.q, w.k, w.v, w.g, w.beta, host, table, cache_intermediate=True, **acc_seed, **kw)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    cu = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in kw.items()}
+    cu_seed = {n: t.to(dev) for n, t in acc_seed.items()}
+    out = gfn(w.q.to(dev), w.k.to(dev), w.v.to(dev), w.g.to(dev), w.beta.to(dev), pool, table.to(dev),
+              out_dtype=w.out_dtype, dev_err=err, **cu_seed, **cu)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and ref["n_bad"] == 0
+    P.assert_out_close(out, ref["out"])
+    # each written slot holds the state after its token (fp64 reference, before any rounding)
+    written = {}
+    for b in range(B):
+        for t in range(T):
+            if int(table[b, t]) >= 0:
+                written[int(table[b, t])] = (b, t)
+    for s in range(w.P):
+        if s in written:
+            b, t = written[s]
+            P.assert_state_close(pool[s], ref["inter"][b, t], f"slot {s} (entry {b}, token {t})")
+        else:
+            assert torch.equal(pool[s], before[s]), f"slot {s} changed"
+
+
+def test_token_slots_bad_accepted_count(cuda_device):
+    import linear_attention_recurrent_gb300 as lar
+    import oracle
+    dev = cuda_device
+    w, table, _ = _token_case("gdn", 3, 4, seed=50)
+    host = w.pool.clone()
+    pool = w.pool.to(dev)
+    acc = torch.tensor([0, 5, 2])
+    ref = oracle.gdn_decode_tokens(w.q, w.k, w.v, w.g, w.beta, host, table, num_accepted=acc)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = lar.gdn_decode_tokens(w.q.to(dev), w.k.to(dev), w.v.to(dev), w.g.to(dev), w.beta.to(dev), pool,
+                                table.to(dev), num_accepted=acc.to(dev), out_dtype=w.out_dtype, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 4 and ref["n_bad"] == 2   # LAR_DEVERR_ACCEPTED
+    P.assert_out_close(out, ref["out"])
+    P.assert_state_close(pool.cpu(), host.double().numpy(), "pool")
+
+
+def test_token_slots_two_step_speculative_flow(cuda_device):
+    """Step 1 stores every token's state in the row; step 2 seeds from the
+    accepted count; both on the GPU and in the oracle, pools compared at the end."""
+    import linear_attention_recurrent_gb300 as lar
+    import oracle
+    dev = cuda_device
+    w1, table, seeds = _token_case("gdn", 4, 4, seed=60)
+    w2, _, _ = _token_case("gdn", 4, 4, seed=61)
+    host = w1.pool.clone()
+    pool = w1.pool.to(dev)
+    oracle.gdn_decode_tokens(w1.q, w1.k, w1.v, w1.g, w1.beta, host, table, read_idx=seeds)
+    lar.gdn_decode_tokens(w1.q.to(dev), w1.k.to(dev), w1.v.to(dev), w1.g.to(dev), w1.beta.to(dev), pool,
+                          table.to(dev), read_idx=seeds.to(dev), out_dtype=w1.out_dtype)
+    acc = torch.tensor([3, 1, 4, 2])
+    table2 = table.clone()                               # the same slot row serves every step
+    ref = oracle.gdn_decode_tokens(w2.q, w2.k, w2.v, w2.g, w2.beta, host, table2, num_accepted=acc)
+    out = lar.gdn_decode_tokens(w2.q.to(dev), w2.k.to(dev), w2.v.to(dev), w2.g.to(dev), w2.beta.to(dev), pool,
+                                table2.to(dev), num_accepted=acc.to(dev), out_dtype=w2.out_dtype)
+    torch.cuda.synchronize()
+    P.assert_out_close(out, ref["out"])
+    P.assert_state_close(pool.cpu(), host.double().numpy(), "pool")
