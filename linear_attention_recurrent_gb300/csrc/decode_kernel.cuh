@@ -167,7 +167,10 @@ __host__ __device__ constexpr size_t decode_smem_bytes(int T, int V) {
            2 * kMaxTokens * sizeof(long long);   // per-pair tables of per-token write slots
 }
 
-template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB>
+// TOK: per-token pool slots (seed from the accepted count or read_idx, the state
+// after every token stored to its slot, no final writeback); compiled
+// separately so the plain decode carries none of it.
+template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB, bool TOK>
 __global__ void __launch_bounds__(NW * 32, MB)
 decode_kernel(const DecodeParams p) {
     using G = Tile<K, LPR, NR, NW, SB>;
@@ -256,7 +259,7 @@ decode_kernel(const DecodeParams p) {
     // slot and yields kBadCount (zero seed, flagged).
     constexpr int64_t kBadCount = INT64_MIN;
     auto seed_of = [&](int b) -> int64_t {
-        if (p.nacc == nullptr) return ld_idx(p.ridx, b * p.ri_s, p.ri_dt);
+        if (!TOK || p.nacc == nullptr) return ld_idx(p.ridx, b * p.ri_s, p.ri_dt);
         const int64_t a = ld_idx(p.nacc, b * p.na_s, p.na_dt);
         if (a < 1 || a > T) return kBadCount;
         return ld_idx(p.tslot, b * p.tsl_s[0] + (a - 1) * p.tsl_s[1], p.tsl_dt);
@@ -318,17 +321,18 @@ decode_kernel(const DecodeParams p) {
             buf ^= 1;
             const int64_t r = seed_of(b);
             // with per-token slots every token's state is stored; there is no final writeback
-            const int64_t w = p.tslot ? -1 : (p.widx ? ld_idx(p.widx, b * p.wi_s, p.wi_dt) : r);
+            const int64_t w = TOK ? -1 : (p.widx ? ld_idx(p.widx, b * p.wi_s, p.wi_dt) : r);
             rd = r >= 0 && r < p.P;
             wr = w >= 0 && w < p.P;
-            long long* tab = slot_tab + buf * kMaxTokens;
-            if (p.tslot)
+            if constexpr (TOK) {
+                long long* tab = slot_tab + buf * kMaxTokens;
                 for (int t = threadIdx.x; t < T; t += NW * 32)
                     tab[t] = ld_idx(p.tslot, b * p.tsl_s[0] + t * p.tsl_s[1], p.tsl_dt);
+            }
             if (threadIdx.x == 0 && hv == 0 && p.dev_err) {
                 int e = (r >= p.P ? LAR_DEVERR_READ_SLOT : 0) | (w >= p.P ? LAR_DEVERR_WRITE_SLOT : 0) |
                         (r == kBadCount ? LAR_DEVERR_ACCEPTED : 0);
-                if (p.tslot)
+                if (TOK)
                     for (int t = 0; t < T; ++t)
                         if (ld_idx(p.tslot, b * p.tsl_s[0] + t * p.tsl_s[1], p.tsl_dt) >= p.P) e |= LAR_DEVERR_WRITE_SLOT;
                 if (e) atomicOr(p.dev_err, e);
@@ -507,7 +511,7 @@ decode_kernel(const DecodeParams p) {
 #pragma unroll
                     for (int c = 0; c < NCH; ++c) store_run<EPC>(ip + c * cstep, &s[i][c * EPC], inter_bf16);
                 }
-                if (p.tslot != nullptr && rv) {
+                if (TOK && rv) {
                     const long long ts = slot_tab[buf * kMaxTokens + t];
                     if (ts >= 0 && ts < p.P) {
                         unsigned char* tp = static_cast<unsigned char*>(p.pool) +
@@ -540,10 +544,10 @@ decode_kernel(const DecodeParams p) {
 // once per (device, size) and cached.
 int cached_occupancy(const void* kern, int threads, size_t smem, size_t smem_max, int* sms_out);
 
-template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB = 1>
-lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
+template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB, bool TOK>
+lar_status launch_tile_mode(const DecodeParams& p, cudaStream_t stream) {
     using G = Tile<K, LPR, NR, NW, SB>;
-    auto kern = decode_kernel<FORM, K, LPR, NR, NW, S, SB, MB>;
+    auto kern = decode_kernel<FORM, K, LPR, NR, NW, S, SB, MB, TOK>;
     const size_t smem = decode_smem_bytes<FORM, K, LPR, NR, NW, S, SB>(p.T, p.V);
     // the largest footprint any call can ask for (T = 16 with staged v)
     constexpr size_t smem_max = decode_smem_bytes<FORM, K, LPR, NR, NW, S, SB>(16, kStageVMax / 16);
@@ -570,6 +574,15 @@ lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
     kern<<<static_cast<unsigned>(grid), NW * 32, smem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? LAR_OK : LAR_ERR_LAUNCH;
 #endif
+}
+
+
+template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB = 1>
+lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
+    if constexpr (FORM != FORM_LA) {
+        if (p.tslot != nullptr) return launch_tile_mode<FORM, K, LPR, NR, NW, S, SB, MB, true>(p, stream);
+    }
+    return launch_tile_mode<FORM, K, LPR, NR, NW, S, SB, MB, false>(p, stream);
 }
 
 // Tile shapes per key size and pool type: a row is split over LPR lanes so each
