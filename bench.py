@@ -44,6 +44,8 @@ DESCRIPTIONS = {
     "gdn_tiny": "GDN decode B=2 T=1 H=HV=2 K=V=16 fp32",
     "gdn_b64": "GDN decode B=64 T=1 H=16 HV=32 K=V=128, bf16 q/k/v/out, fp32 pool [256,32,128,128]",
     "gdn_b64_bf16": "GDN decode B=64 T=1 H=16 HV=32 K=V=128, bf16 q/k/v/out, bf16 pool [256,32,128,128]",
+    "gdn_spec_b64": "GDN speculative verify B=64 T=4 H=16 HV=32 K=V=128, per-token pool slots "
+                    "(4 per sequence, 320-slot pool), seed = slot of the last accepted token",
     "gdn_mtp_strided": "GDN MTP B=16 T=4 H=16 HV=32 K=V=128, pool = backing[::2] of [256,32,128,128], "
                        "separate write slots (25% -1), all T states cached",
     "kda_b256": "KDA decode B=256 T=1 H=HV=24 K=V=128, in-kernel gate/l2norm/sigmoid, pool [320,24,128,128]",
@@ -202,6 +204,8 @@ def device_inputs(w, dev):
 def index_sets(w):
     """Disjoint (read, write) index sets to rotate over, when the pool holds
     several batches (in-place workloads only); else the workload's own set."""
+    if w.state_idx is not None:
+        return [(w.read_idx, w.write_idx)], 1
     same = w.write_idx is not None and torch.equal(w.read_idx, w.write_idx)
     n = w.P // w.B if same else 1
     if n >= 2:
@@ -231,6 +235,10 @@ def run_lar(args, world, rank, local):
                      if w.cache_intermediate else None)
             kw = dict(d, read_idx=ri.to(dev), write_idx=None if wi is None else wi.to(dev),
                       out=out, inter=inter)
+            if w.state_idx is not None:
+                kw.update(state_idx=w.state_idx.to(dev), write_idx=None, inter=None)
+                if w.num_accepted is not None:
+                    kw.update(num_accepted=w.num_accepted.to(dev), read_idx=None)
             if w.form != "la":
                 kw.update(qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw)
             calls.append(lar.PreparedCall(w.form, scale=w.scale, stream=stream, **kw))
@@ -318,8 +326,15 @@ def run_e2e(w, d, sets, dev, stream, args):
     names = ["q", "k", "v"] + (["decay"] if w.form == "la" else ["g", "beta"])
     ri, wi = sets[0]
     host_parts = {n: getattr(w, n).contiguous() for n in names if getattr(w, n) is not None}
-    host_parts["read_idx"] = ri.contiguous()
-    host_parts["write_idx"] = wi.contiguous()
+    if w.state_idx is not None:
+        host_parts["state_idx"] = w.state_idx.contiguous()
+        if w.num_accepted is not None:
+            host_parts["num_accepted"] = w.num_accepted.contiguous()
+        else:
+            host_parts["read_idx"] = ri.contiguous()
+    else:
+        host_parts["read_idx"] = ri.contiguous()
+        host_parts["write_idx"] = wi.contiguous()
     offs, total = {}, 0
     for n, t in host_parts.items():
         offs[n] = total
@@ -373,6 +388,12 @@ def _oracle_step(w, host_pool, batch):
     if w.form == "la":
         oracle.la_decode(sel(w.q), sel(w.k), sel(w.v), w.decay, host_pool, sel(w.read_idx),
                          sel(w.write_idx), scale=w.scale, cache_intermediate=w.cache_intermediate)
+    elif w.state_idx is not None:
+        fn = oracle.gdn_decode_tokens if w.form == "gdn" else oracle.kda_decode_tokens
+        fn(sel(w.q), sel(w.k), sel(w.v), sel(w.g), sel(w.beta), host_pool, sel(w.state_idx),
+           read_idx=None if w.num_accepted is not None else sel(w.read_idx),
+           num_accepted=sel(w.num_accepted), A_log=w.A_log, dt_bias=w.dt_bias,
+           qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw, scale=w.scale)
     else:
         fn = oracle.gdn_decode if w.form == "gdn" else oracle.kda_decode
         fn(sel(w.q), sel(w.k), sel(w.v), sel(w.g), sel(w.beta), host_pool, sel(w.read_idx),

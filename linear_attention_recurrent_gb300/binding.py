@@ -188,12 +188,15 @@ def la_decode(q, k, v, decay, pool, read_idx, write_idx=None, *, out=None, inter
 
 class PreparedCall:
     """A decode call whose descriptors are built once, for tight launch loops.
-    The tensors it was built from must stay alive and keep their storage."""
+    The tensors it was built from must stay alive and keep their storage.
+    Passing ``state_idx`` (and ``num_accepted`` or ``read_idx``) selects the
+    per-token-slot call (gdn_decode_tokens / kda_decode_tokens)."""
 
     def __init__(self, form, *, scale=1.0, qk_l2norm=False, gate_raw=False, beta_raw=False,
                  dev_err=None, stream=None, **tensors):
         lib = load()
-        self._name = f"{form}_decode"
+        tokens = tensors.get("state_idx") is not None
+        self._name = f"{form}_decode_tokens" if tokens else f"{form}_decode"
         self._fn = getattr(lib, self._name)
         self._keep = (tensors, dev_err)
         err = dev_err.data_ptr() if dev_err is not None else None
@@ -203,8 +206,12 @@ class PreparedCall:
             self._descs = [describe(tensors.get(n)) for n in names]
             self._args = [_ref(d) for d in self._descs] + [float(scale), err, st]
         else:
-            names = ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "pool", "read_idx",
-                     "write_idx", "out", "inter")
+            if tokens:
+                names = ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "pool", "read_idx",
+                         "num_accepted", "state_idx", "out")
+            else:
+                names = ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "pool", "read_idx",
+                         "write_idx", "out", "inter")
             self._descs = [describe(tensors.get(n)) for n in names]
             self._args = [_ref(d) for d in self._descs] + [
                 float(scale), _flags(qk_l2norm, gate_raw, beta_raw), err, st]

@@ -57,3 +57,39 @@ def test_full_size(name, cuda_device):
         if 0 <= wi[b] < w.P:
             P.assert_state_close(P.slot_state(w.pool, w, wi[b]), ref["final_state"][i],
                                  f"slot {wi[b]} (entry {b})")
+
+
+def test_full_size_speculative_token_slots(cuda_device):
+    """gdn_spec_b64 at full size: outputs of sampled entries and the state in
+    every written slot of those entries against the oracle; every other pool
+    byte bit-identical."""
+    import linear_attention_recurrent_gb300 as lar
+    import oracle
+    dev = cuda_device
+    w = W.make("gdn_spec_b64", pool_device=dev)
+    before = w.pool.clone()
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = lar.gdn_decode_tokens(w.q.to(dev), w.k.to(dev), w.v.to(dev), w.g.to(dev), w.beta.to(dev), w.pool,
+                                w.state_idx.to(dev), num_accepted=w.num_accepted.to(dev),
+                                out_dtype=w.out_dtype, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    written = w.state_idx.view(-1).long()
+    mask = torch.zeros(w.P, dtype=torch.bool)
+    mask[written] = True
+    assert torch.equal(w.pool[~mask.to(dev)], before[~mask.to(dev)])
+    sample = _sample(w.B)
+    n = len(sample)
+    # sub-problem: the sampled rows of the slot table, renumbered into a small host pool
+    sub_tab = torch.arange(n * w.T).view(n, w.T)
+    sub = torch.zeros((n * w.T,) + tuple(w.pool.shape[1:]))
+    for i, b in enumerate(sample):
+        for t in range(w.T):
+            sub[i * w.T + t] = before[int(w.state_idx[b, t])].cpu()
+    idx = torch.tensor(sample)
+    ref = oracle.gdn_decode_tokens(w.q[idx], w.k[idx], w.v[idx], w.g[idx], w.beta[idx], sub, sub_tab,
+                                   num_accepted=w.num_accepted[idx], cache_intermediate=True)
+    P.assert_out_close(out[idx], ref["out"])
+    for i, b in enumerate(sample):
+        for t in range(w.T):
+            P.assert_state_close(w.pool[int(w.state_idx[b, t])], ref["inter"][i, t], f"entry {b} token {t}")

@@ -25,6 +25,9 @@ kda_b256           B=256 T=1 H=HV=24, raw bf16 q/k (l2norm in kernel), raw bf16
                    N(0, 0.1) [HV*K], raw beta logits; pool [320,24,128,128];
                    read = write = randperm(320)[:256]; seed 4
 gdn_b64_bf16       gdn_b64 with a bfloat16 state pool (drawn in fp32, rounded once)
+gdn_spec_b64       B=64 T=4 H=16 HV=32, per-token pool slots: one row of 4 distinct
+                   slots per sequence (of 320), seed = slot of the last accepted
+                   token, accepted counts uniform in 1..4; seed 6
 la_b512_packed     B=512 T=1 H=64, q/k/v head-dim slices of one fused bf16
                    [B,H,384] buffer (q, k ~ N(0,1)/sqrt(128), v ~ N(0,1)),
                    lambda_h = exp(-2^(-8(h+1)/64)), flat pool [640*64,128,128];
@@ -48,9 +51,9 @@ BF16 = torch.bfloat16
 F32 = torch.float32
 
 CONFIGS = ("gdn_tiny", "gdn_b64", "gdn_mtp_strided", "kda_b256", "la_b512_packed",
-           "gdn_b64_bf16")
+           "gdn_b64_bf16", "gdn_spec_b64")
 SEEDS = {"gdn_tiny": 0, "gdn_b64": 2, "gdn_mtp_strided": 3, "kda_b256": 4,
-         "la_b512_packed": 5, "gdn_b64_bf16": 2}
+         "la_b512_packed": 5, "gdn_b64_bf16": 2, "gdn_spec_b64": 6}
 
 
 @dataclass
@@ -84,6 +87,8 @@ class Workload:
     scale: float = 1.0
     cache_intermediate: bool = False
     inter_dtype: torch.dtype = F32
+    state_idx: torch.Tensor | None = None      # per-token write slots [B, T] (token-slot mode)
+    num_accepted: torch.Tensor | None = None   # seed selection [B] (token-slot mode)
     meta: dict = field(default_factory=dict)
 
     def algorithmic_bytes(self) -> int:
@@ -93,15 +98,31 @@ class Workload:
         intermediate state, plus q/k/v/gate/out/index bytes."""
         unit = self.K * self.V * self.pool.element_size()
         heads = self.HV
-        r = self.read_idx.to("cpu")
-        w = (self.write_idx if self.write_idx is not None else self.read_idx).to("cpu")
-        n_read = int(((r >= 0) & (r < self.P)).sum())
-        n_write = int(((w >= 0) & (w < self.P)).sum())
+        if self.state_idx is not None:
+            tab = self.state_idx.to("cpu")
+            if self.num_accepted is not None:
+                a = self.num_accepted.to("cpu").long()
+                ok = (a >= 1) & (a <= self.T)
+                seed = torch.where(ok, tab.gather(1, (a.clamp(1, self.T) - 1)[:, None])[:, 0],
+                                   torch.full_like(a, -1))
+            else:
+                seed = self.read_idx.to("cpu")
+            n_read = int(((seed >= 0) & (seed < self.P)).sum())
+            n_write = int(((tab >= 0) & (tab < self.P)).sum())
+        else:
+            r = self.read_idx.to("cpu")
+            w = (self.write_idx if self.write_idx is not None else self.read_idx).to("cpu")
+            n_read = int(((r >= 0) & (r < self.P)).sum())
+            n_write = int(((w >= 0) & (w < self.P)).sum())
         total = (n_read + n_write) * heads * unit
         if self.cache_intermediate:
             total += self.B * self.T * heads * self.K * self.V * torch.finfo(self.inter_dtype).bits // 8
         small = [self.q, self.k, self.v, self.g, self.beta, self.A_log, self.dt_bias,
-                 self.decay, self.read_idx, self.write_idx]
+                 self.decay, self.state_idx, self.num_accepted]
+        if self.state_idx is None:
+            small += [self.read_idx, self.write_idx]
+        elif self.num_accepted is None:
+            small += [self.read_idx]
         total += sum(t.numel() * t.element_size() for t in small if t is not None)
         total += self.B * self.T * heads * self.V * torch.finfo(self.out_dtype).bits // 8
         return int(total)
@@ -171,6 +192,20 @@ def make(name: str, *, seed: int | None = None, pool_device="cpu",
         return Workload(name, "gdn", B, T, H, HV, K, V, P, q, k, v, pool,
                         ri.to(index_dtype), wi.to(index_dtype), BF16, g=g, beta=beta,
                         backing=backing, cache_intermediate=True, meta={"stride_mult": M})
+    if name == "gdn_spec_b64":
+        # speculative verify: one row of T slots per sequence, reused every step;
+        # the seed is the state after the last accepted draft token
+        B, T, H, HV, K, V, P = 64, 4, 16, 32, 128, 128, 320
+        q = _l2n(_normal(gen, (B, T, H, K))).to(BF16)
+        k = _l2n(_normal(gen, (B, T, H, K))).to(BF16)
+        v = _normal(gen, (B, T, HV, V)).to(BF16)
+        g = -F.softplus(_normal(gen, (B, T, HV)))
+        beta = torch.sigmoid(_normal(gen, (B, T, HV)))
+        table = torch.randperm(P, generator=gen)[:B * T].view(B, T).to(index_dtype)
+        accepted = torch.randint(1, T + 1, (B,), generator=gen).to(index_dtype)
+        pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
+        return Workload(name, "gdn", B, T, H, HV, K, V, P, q, k, v, pool, table[:, 0].clone(), None,
+                        BF16, g=g, beta=beta, state_idx=table, num_accepted=accepted)
     if name == "kda_b256":
         B, T, H, HV, K, V, P = 256, 1, 24, 24, 128, 128, 320
         q = _normal(gen, (B, T, H, K)).to(BF16)
