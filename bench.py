@@ -44,6 +44,8 @@ DESCRIPTIONS = {
     "gdn_tiny": "GDN decode B=2 T=1 H=HV=2 K=V=16 fp32",
     "gdn_b64": "GDN decode B=64 T=1 H=16 HV=32 K=V=128, bf16 q/k/v/out, fp32 pool [256,32,128,128]",
     "gdn_b64_bf16": "GDN decode B=64 T=1 H=16 HV=32 K=V=128, bf16 q/k/v/out, bf16 pool [256,32,128,128]",
+    "gdn_b64_kv": "GDN decode B=64 T=1 H=16 HV=32 K=V=128, bf16 q/k/v/out, fp32 pool [256,32,128(k),128(v)] "
+                  "(state stored untransposed)",
     "gdn_spec_b64": "GDN speculative verify B=64 T=4 H=16 HV=32 K=V=128, per-token pool slots "
                     "(4 per sequence, 320-slot pool), seed = slot of the last accepted token",
     "gdn_mtp_strided": "GDN MTP B=16 T=4 H=16 HV=32 K=V=128, pool = backing[::2] of [256,32,128,128], "
@@ -240,7 +242,8 @@ def run_lar(args, world, rank, local):
                 if w.num_accepted is not None:
                     kw.update(num_accepted=w.num_accepted.to(dev), read_idx=None)
             if w.form != "la":
-                kw.update(qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw)
+                kw.update(qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw,
+                          state_kv=w.state_kv)
             calls.append(lar.PreparedCall(w.form, scale=w.scale, stream=stream, **kw))
             outs.append(out)
             inters.append(inter)
@@ -353,7 +356,7 @@ def run_e2e(w, d, sets, dev, stream, args):
     kw = dict(views, pool=d["pool"], out=out_dev, inter=inter)
     if w.form != "la":
         kw.update(A_log=d.get("A_log"), dt_bias=d.get("dt_bias"), qk_l2norm=w.qk_l2norm,
-                  gate_raw=w.gate_raw, beta_raw=w.beta_raw)
+                  gate_raw=w.gate_raw, beta_raw=w.beta_raw, state_kv=w.state_kv)
     call = lar.PreparedCall(w.form, scale=w.scale, stream=stream, **kw)
     h2d = sum(t.numel() * t.element_size() for t in host_parts.values())
     d2h = out_host.numel() * out_host.element_size()
@@ -399,7 +402,7 @@ def _oracle_step(w, host_pool, batch):
         fn(sel(w.q), sel(w.k), sel(w.v), sel(w.g), sel(w.beta), host_pool, sel(w.read_idx),
            sel(w.write_idx), A_log=w.A_log, dt_bias=w.dt_bias, qk_l2norm=w.qk_l2norm,
            gate_raw=w.gate_raw, beta_raw=w.beta_raw, scale=w.scale,
-           cache_intermediate=w.cache_intermediate)
+           cache_intermediate=w.cache_intermediate, layout="kv" if w.state_kv else "vk")
 
 
 def _host_workload(config):

@@ -34,6 +34,11 @@
  *          (so q/k/v may be head-dim slices of one fused buffer).
  *   v      [B, T, HV, V] (rank 3 [B, HV, V]); fp32 or bf16, any strides.
  *   out    [B, T, HV, V] (rank 3 [B, HV, V]); fp32 or bf16 (round to nearest even).
+ *          With LAR_STATE_KV (gdn_decode / kda_decode only) the state is held
+ *          untransposed, pool[slot][hv][k][v] = S[k][v] with v fastest (the
+ *          "nontranspose" layout of the flashinfer GDN decode kernels): rank 4
+ *          [P, HV, K, V] or rank 3 [P*HV, K, V], v stride 1, V a multiple of
+ *          16 bytes of elements (4 fp32 or 8 bf16); inter is [B, T, HV, K, V].
  *   inter  NULL, or fp32 or bf16 [B, T, HV, V, K] (rank 4 [B, HV, V, K] when
  *          T = 1): the state after each token; same alignment rules as the
  *          pool; its type is independent of the pool's.
@@ -102,7 +107,8 @@ typedef enum {
 enum {
     LAR_QK_L2NORM = 1u << 0, /* q, k <- x / sqrt(sum x^2 + 1e-6) over K, in kernel */
     LAR_GATE_RAW = 1u << 1,  /* g <- -exp(A_log[hv]) * softplus(g + dt_bias), in kernel */
-    LAR_BETA_RAW = 1u << 2   /* beta <- 1 / (1 + exp(-beta)), in kernel */
+    LAR_BETA_RAW = 1u << 2,  /* beta <- 1 / (1 + exp(-beta)), in kernel */
+    LAR_STATE_KV = 1u << 3   /* pool and inter hold S as [k][v] (v fastest), see below */
 };
 
 /* bits OR-ed into *dev_err */

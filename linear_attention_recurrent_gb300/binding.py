@@ -15,7 +15,7 @@ from . import _build
 _LIB_PATH = _build.LIB
 
 LAR_F32, LAR_BF16, LAR_I32, LAR_I64 = 0, 1, 2, 3
-LAR_QK_L2NORM, LAR_GATE_RAW, LAR_BETA_RAW = 1, 2, 4
+LAR_QK_L2NORM, LAR_GATE_RAW, LAR_BETA_RAW, LAR_STATE_KV = 1, 2, 4, 8
 LAR_DEVERR_READ_SLOT, LAR_DEVERR_WRITE_SLOT, LAR_DEVERR_ACCEPTED = 1, 2, 4
 
 STATUS = {0: "LAR_OK", 1: "LAR_ERR_NULL", 2: "LAR_ERR_DTYPE", 3: "LAR_ERR_RANK",
@@ -106,25 +106,28 @@ def _check(fn, status):
         raise LarError(fn, status, load().lar_status_string(status).decode())
 
 
-def _flags(qk_l2norm, gate_raw, beta_raw):
+def _flags(qk_l2norm, gate_raw, beta_raw, state_kv=False):
     return (LAR_QK_L2NORM if qk_l2norm else 0) | (LAR_GATE_RAW if gate_raw else 0) | \
-        (LAR_BETA_RAW if beta_raw else 0)
+        (LAR_BETA_RAW if beta_raw else 0) | (LAR_STATE_KV if state_kv else 0)
 
 
 def gdn_decode(q, k, v, g, beta, pool, read_idx, write_idx=None, *, out=None, inter=None,
                A_log=None, dt_bias=None, scale=1.0, qk_l2norm=False, gate_raw=False,
-               beta_raw=False, dev_err=None, out_dtype=None, stream=None):
-    """Gated delta rule decode (scalar decay).  Updates `pool` in place; returns `out`."""
+               beta_raw=False, state_kv=False, dev_err=None, out_dtype=None, stream=None):
+    """Gated delta rule decode (scalar decay).  Updates `pool` in place; returns `out`.
+    state_kv: the pool (and inter) hold S as [k][v], v fastest."""
     return _delta("gdn_decode", q, k, v, g, beta, pool, read_idx, write_idx, out, inter, A_log,
-                  dt_bias, scale, _flags(qk_l2norm, gate_raw, beta_raw), dev_err, out_dtype, stream)
+                  dt_bias, scale, _flags(qk_l2norm, gate_raw, beta_raw, state_kv), dev_err,
+                  out_dtype, stream)
 
 
 def kda_decode(q, k, v, g, beta, pool, read_idx, write_idx=None, *, out=None, inter=None,
                A_log=None, dt_bias=None, scale=1.0, qk_l2norm=False, gate_raw=False,
-               beta_raw=False, dev_err=None, out_dtype=None, stream=None):
+               beta_raw=False, state_kv=False, dev_err=None, out_dtype=None, stream=None):
     """Gated delta rule decode (per-key-channel decay).  Updates `pool` in place."""
     return _delta("kda_decode", q, k, v, g, beta, pool, read_idx, write_idx, out, inter, A_log,
-                  dt_bias, scale, _flags(qk_l2norm, gate_raw, beta_raw), dev_err, out_dtype, stream)
+                  dt_bias, scale, _flags(qk_l2norm, gate_raw, beta_raw, state_kv), dev_err,
+                  out_dtype, stream)
 
 
 def _delta(name, q, k, v, g, beta, pool, read_idx, write_idx, out, inter, A_log, dt_bias, scale,
@@ -193,7 +196,7 @@ class PreparedCall:
     per-token-slot call (gdn_decode_tokens / kda_decode_tokens)."""
 
     def __init__(self, form, *, scale=1.0, qk_l2norm=False, gate_raw=False, beta_raw=False,
-                 dev_err=None, stream=None, **tensors):
+                 state_kv=False, dev_err=None, stream=None, **tensors):
         lib = load()
         tokens = tensors.get("state_idx") is not None
         self._name = f"{form}_decode_tokens" if tokens else f"{form}_decode"
@@ -214,7 +217,7 @@ class PreparedCall:
                          "write_idx", "out", "inter")
             self._descs = [describe(tensors.get(n)) for n in names]
             self._args = [_ref(d) for d in self._descs] + [
-                float(scale), _flags(qk_l2norm, gate_raw, beta_raw), err, st]
+                float(scale), _flags(qk_l2norm, gate_raw, beta_raw, state_kv), err, st]
 
     def __call__(self):
         st = self._fn(*self._args)

@@ -41,8 +41,11 @@
 #ifndef LAR_K128_NW
 #define LAR_K128_NW 4
 #endif
-#ifndef LAR_KDA_MIN_BLOCKS
-#define LAR_KDA_MIN_BLOCKS 3
+// Resident CTAs per SM that register-heavy K = 128 kernels are compiled for
+// (caps registers at 65536 / (3 x 128) -> 168 per thread, so three 4-warp
+// CTAs fit).
+#ifndef LAR_K128_MIN_BLOCKS
+#define LAR_K128_MIN_BLOCKS 3
 #endif
 #ifndef LAR_K128_LPR
 #define LAR_K128_LPR 8
@@ -166,6 +169,89 @@ __host__ __device__ constexpr size_t decode_smem_bytes(int T, int V) {
     return static_cast<size_t>(S) * G::TV * K * SB + 2 * static_cast<size_t>(vec_floats<FORM, K>(T, V)) * sizeof(float) +
            2 * kMaxTokens * sizeof(long long);   // per-pair tables of per-token write slots
 }
+
+// Per-(b, hv) vectors into the buffer vb: the raw q and k rows of all T tokens,
+// the KDA decay rows exp(g) (gate chain included), the pair's v values when
+// staged, and per token beta, the scalar decay, 1/|q|, 1/|k| and
+// q.k / (|q| |k|).  All threads of the CTA take part; ends with a barrier.
+template <int FORM, int K, int NW>
+__device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float* vb, int b, int hv, int h,
+                                                   int64_t v_off, bool sv_on, int o_k, int o_d, int o_v,
+                                                   int o_s) {
+    const int T = p.T;
+    const int V = p.V;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const bool gate_raw = (p.flags & LAR_GATE_RAW) != 0;
+    const bool l2 = FORM != FORM_LA && (p.flags & LAR_QK_L2NORM) != 0;
+    const int64_t q_off = b * p.qs[0] + h * p.qs[2];
+    const int64_t k_off = b * p.ks[0] + h * p.ks[2];
+    for (int i = threadIdx.x; i < T * K; i += NW * 32) {
+        const int t = i / K;
+        const int c = i - t * K;
+        vb[i] = ld_in(p.q, q_off + t * p.qs[1] + c * p.qs[3], p.q_dt);
+        vb[o_k + i] = ld_in(p.k, k_off + t * p.ks[1] + c * p.ks[3], p.k_dt);
+        if constexpr (FORM == FORM_KDA) {
+            float x = ld_in(p.g, b * p.gs[0] + t * p.gs[1] + hv * p.gs[2] + c * p.gs[3], p.g_dt);
+            if (gate_raw) {
+                const float bias =
+                    p.dt_bias ? p.dt_bias[(static_cast<int64_t>(hv) * K + c) * p.dtb_s] : 0.f;
+                x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
+            }
+            vb[o_d + i] = expf(x);
+        }
+    }
+    if (sv_on) {
+        for (int i = threadIdx.x; i < T * V; i += NW * 32) {
+            const int t = i / V;
+            const int row = i - t * V;
+            vb[o_v + i] = ld_in(p.v, v_off + t * p.vs[1] + row * p.vs[3], p.v_dt);
+        }
+    }
+    float* sc = vb + o_s;
+    for (int t = threadIdx.x; t < T; t += NW * 32) {
+        float bt = 0.f, dec = 1.f;
+        if constexpr (FORM != FORM_LA) {
+            bt = ld_in(p.beta, b * p.bs[0] + t * p.bs[1] + hv * p.bs[2], p.beta_dt);
+            if (p.flags & LAR_BETA_RAW) bt = 1.f / (1.f + expf(-bt));
+        }
+        if constexpr (FORM == FORM_GDN) {
+            float x = ld_in(p.g, b * p.gs[0] + t * p.gs[1] + hv * p.gs[2], p.g_dt);
+            if (gate_raw) {
+                const float bias = p.dt_bias ? p.dt_bias[hv * p.dtb_s] : 0.f;
+                x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
+            }
+            dec = expf(x);
+        } else if constexpr (FORM == FORM_LA) {
+            dec = p.decay[h * p.dec_s];
+        }
+        sc[t] = bt;
+        sc[T + t] = dec;
+    }
+    __syncthreads();
+    for (int t = warp; t < T; t += NW) {
+        float qq = 0.f, kk = 0.f, kq = 0.f;
+        for (int c = lane; c < K; c += 32) {
+            const float a = vb[t * K + c], bb = vb[o_k + t * K + c];
+            qq = fmaf(a, a, qq);
+            kk = fmaf(bb, bb, kk);
+            kq = fmaf(a, bb, kq);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            qq += __shfl_xor_sync(0xffffffffu, qq, off);
+            kk += __shfl_xor_sync(0xffffffffu, kk, off);
+            kq += __shfl_xor_sync(0xffffffffu, kq, off);
+        }
+        if (lane == 0) {
+            const float iq = l2 ? 1.f / sqrtf(qq + 1e-6f) : 1.f;
+            const float ik = l2 ? 1.f / sqrtf(kk + 1e-6f) : 1.f;
+            sc[2 * T + t] = iq;
+            sc[3 * T + t] = ik;
+            sc[4 * T + t] = kq * iq * ik;
+        }
+    }
+    __syncthreads();}
 
 // TOK: per-token pool slots (seed from the accepted count or read_idx, the state
 // after every token stored to its slot, no final writeback); compiled
@@ -305,8 +391,6 @@ decode_kernel(const DecodeParams p) {
     int64_t v_off = 0, o_off = 0;           // per-pair offsets into v and out
     unsigned char* inter_base = nullptr;
     const float scale = p.scale;
-    const bool gate_raw = (p.flags & LAR_GATE_RAW) != 0;
-    const bool l2 = FORM != FORM_LA && (p.flags & LAR_QK_L2NORM) != 0;
 
     int stage = 0;                 // ring stage of the tile being consumed
     int stage_next = S - 1;        // ring stage the next issue goes to
@@ -343,75 +427,7 @@ decode_kernel(const DecodeParams p) {
             o_off = b * p.os[0] + hv * p.os[2];
             if (p.inter) inter_base = static_cast<unsigned char*>(p.inter) + (b * p.is[0] + hv * p.is[2]) * inter_es;
 
-            float* vb = vecs + buf * vstride;
-            const int64_t q_off = b * p.qs[0] + h * p.qs[2];
-            const int64_t k_off = b * p.ks[0] + h * p.ks[2];
-            for (int i = threadIdx.x; i < T * K; i += NW * 32) {
-                const int t = i / K;
-                const int c = i - t * K;
-                vb[i] = ld_in(p.q, q_off + t * p.qs[1] + c * p.qs[3], p.q_dt);
-                vb[o_k + i] = ld_in(p.k, k_off + t * p.ks[1] + c * p.ks[3], p.k_dt);
-                if constexpr (FORM == FORM_KDA) {
-                    float x = ld_in(p.g, b * p.gs[0] + t * p.gs[1] + hv * p.gs[2] + c * p.gs[3], p.g_dt);
-                    if (gate_raw) {
-                        const float bias =
-                            p.dt_bias ? p.dt_bias[(static_cast<int64_t>(hv) * K + c) * p.dtb_s] : 0.f;
-                        x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
-                    }
-                    vb[o_d + i] = expf(x);
-                }
-            }
-            if (sv_on) {
-                for (int i = threadIdx.x; i < T * V; i += NW * 32) {
-                    const int t = i / V;
-                    const int row = i - t * V;
-                    vb[o_v + i] = ld_in(p.v, v_off + t * p.vs[1] + row * p.vs[3], p.v_dt);
-                }
-            }
-            float* sc = vb + o_s;
-            for (int t = threadIdx.x; t < T; t += NW * 32) {
-                float bt = 0.f, dec = 1.f;
-                if constexpr (FORM != FORM_LA) {
-                    bt = ld_in(p.beta, b * p.bs[0] + t * p.bs[1] + hv * p.bs[2], p.beta_dt);
-                    if (p.flags & LAR_BETA_RAW) bt = 1.f / (1.f + expf(-bt));
-                }
-                if constexpr (FORM == FORM_GDN) {
-                    float x = ld_in(p.g, b * p.gs[0] + t * p.gs[1] + hv * p.gs[2], p.g_dt);
-                    if (gate_raw) {
-                        const float bias = p.dt_bias ? p.dt_bias[hv * p.dtb_s] : 0.f;
-                        x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
-                    }
-                    dec = expf(x);
-                } else if constexpr (FORM == FORM_LA) {
-                    dec = p.decay[h * p.dec_s];
-                }
-                sc[t] = bt;
-                sc[T + t] = dec;
-            }
-            __syncthreads();
-            for (int t = warp; t < T; t += NW) {
-                float qq = 0.f, kk = 0.f, kq = 0.f;
-                for (int c = lane; c < K; c += 32) {
-                    const float a = vb[t * K + c], bb = vb[o_k + t * K + c];
-                    qq = fmaf(a, a, qq);
-                    kk = fmaf(bb, bb, kk);
-                    kq = fmaf(a, bb, kq);
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    qq += __shfl_xor_sync(0xffffffffu, qq, off);
-                    kk += __shfl_xor_sync(0xffffffffu, kk, off);
-                    kq += __shfl_xor_sync(0xffffffffu, kq, off);
-                }
-                if (lane == 0) {
-                    const float iq = l2 ? 1.f / sqrtf(qq + 1e-6f) : 1.f;
-                    const float ik = l2 ? 1.f / sqrtf(kk + 1e-6f) : 1.f;
-                    sc[2 * T + t] = iq;
-                    sc[3 * T + t] = ik;
-                    sc[4 * T + t] = kq * iq * ik;
-                }
-            }
-            __syncthreads();
+            build_pair_vectors<FORM, K, NW>(p, vecs + buf * vstride, b, hv, h, v_off, sv_on, o_k, o_d, o_v, o_s);
         }
 
         // ---- this thread's copies of the tile have landed: pull its rows into registers
@@ -589,7 +605,8 @@ lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
 // lane holds whole 16-byte chunks (fp32 K = 128: 8 lanes x 4 chunks of 4
 // elements); 32-row tiles at K = 128, a 2-stage ring (one tile in flight while
 // one is computed) for fp32 and a 3-stage ring for bf16, whose tiles are half
-// the bytes.  KDA caps registers so that 3 CTAs fit on an SM.
+// the bytes.  Instances whose unconstrained register count would exceed 168
+// (fp32 KDA and LA) are compiled for 3 resident CTAs per SM.
 template <int FORM>
 lar_status launch_form(const DecodeParams& p, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -600,7 +617,7 @@ lar_status launch_form(const DecodeParams& p, void* stream) {
             case 64: return launch_tile<FORM, 64, 8, 2, 4, 3, 4>(p, st);
             case 128:
                 return launch_tile<FORM, 128, LAR_K128_LPR, LAR_K128_NR, LAR_K128_NW, LAR_K128_S, 4,
-                                   FORM == FORM_KDA ? LAR_KDA_MIN_BLOCKS : 1>(p, st);
+                                   FORM == FORM_GDN ? 1 : LAR_K128_MIN_BLOCKS>(p, st);
             default: return LAR_ERR_SHAPE;
         }
     }
@@ -613,7 +630,7 @@ lar_status launch_form(const DecodeParams& p, void* stream) {
             // per row, one row per thread), which halves the per-row bookkeeping;
             // KDA keeps 8 lanes per row to stay within its register budget.
             if constexpr (FORM == FORM_KDA)
-                return launch_tile<FORM, 128, 8, 2, LAR_K128_NW, LAR_K128_BF16_S, 2, LAR_KDA_MIN_BLOCKS>(p, st);
+                return launch_tile<FORM, 128, 8, 2, LAR_K128_NW, LAR_K128_BF16_S, 2, LAR_K128_MIN_BLOCKS>(p, st);
             else
                 return launch_tile<FORM, 128, 4, 1, LAR_K128_NW, LAR_K128_BF16_S, 2, 1>(p, st);
         default: return LAR_ERR_SHAPE;

@@ -27,7 +27,8 @@ struct DecodeParams {
     const float* dt_bias; int64_t dtb_s;          // GDN [HV]; KDA [HV*K]
     const float* decay;   int64_t dec_s;          // LA [H]
 
-    void* pool; int64_t ps[3]; int pool_dt;       // fp32 or bf16; slot, head, row strides (k stride 1)
+    void* pool; int64_t ps[3]; int pool_dt;       // fp32 or bf16; slot, head, row strides (innermost stride 1)
+    int state_kv;                                 // 0: rows are v (S^T, k fastest); 1: rows are k (v fastest)
     const void* ridx; int64_t ri_s; int ri_dt;
     const void* widx; int64_t wi_s; int wi_dt;    // NULL: write to the read slot
 
@@ -35,7 +36,7 @@ struct DecodeParams {
     const void* tslot; int64_t tsl_s[2]; int tsl_dt; // per-token write slots [B, T] or NULL
 
     void* out;    int64_t os[4]; int out_dt;
-    void* inter; int64_t is[4]; int inter_dt;     // fp32 or bf16; b, t, head, row (k stride 1); may be NULL
+    void* inter; int64_t is[4]; int inter_dt;     // fp32 or bf16; b, t, head, row (same layout as the pool); may be NULL
 
     float scale;
     uint32_t flags;

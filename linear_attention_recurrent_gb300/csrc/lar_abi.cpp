@@ -95,7 +95,8 @@ struct Common {
 };
 
 // Checks shared by every form; fills sizes, q/k/v/out/pool/index/inter fields.
-lar_status check_common(const Common& c, int form, DecodeParams& p) {
+// kv: the state is stored [k][v] (LAR_STATE_KV) instead of [v][k].
+lar_status check_common(const Common& c, int form, DecodeParams& p, bool kv = false) {
     if (missing(c.q) || missing(c.k) || missing(c.v) || missing(c.pool) || missing(c.read_idx) ||
         missing(c.out))
         return LAR_ERR_NULL;
@@ -142,11 +143,16 @@ lar_status check_common(const Common& c, int form, DecodeParams& p) {
     p.v = c.v->data; p.v_dt = c.v->dtype;
     p.out = c.out->data; p.out_dt = c.out->dtype;
 
-    // pool: [P, HV, V, K] or flat [P*HV, V, K]; k contiguous, 16-byte rows
+    // pool: [P, HV, V, K] or flat [P*HV, V, K] (kv: [P, HV, K, V] / [P*HV, K, V]);
+    // innermost dimension contiguous, 16-byte chunks
     const lar_tensor* pl = c.pool;
+    const int64_t R1 = kv ? K : V;   // rows of one state
+    const int64_t R2 = kv ? V : K;   // elements of one row
+    p.state_kv = kv ? 1 : 0;
+    if (kv && (R2 * elem_size(pl->dtype)) % 16 != 0) return LAR_ERR_SHAPE;
     int64_t P;
     if (pl->ndim == 4) {
-        if (pl->shape[1] != HV || pl->shape[2] != V || pl->shape[3] != K) return LAR_ERR_SHAPE;
+        if (pl->shape[1] != HV || pl->shape[2] != R1 || pl->shape[3] != R2) return LAR_ERR_SHAPE;
         if (pl->stride[3] != 1) return LAR_ERR_STRIDE;
         P = pl->shape[0];
         p.ps[0] = pl->stride[0];
@@ -154,7 +160,7 @@ lar_status check_common(const Common& c, int form, DecodeParams& p) {
         p.ps[2] = pl->stride[2];
         if (form == lar::FORM_LA && P > 1 && pl->stride[0] != HV * pl->stride[1]) return LAR_ERR_STRIDE;
     } else if (pl->ndim == 3) {
-        if (pl->shape[1] != V || pl->shape[2] != K) return LAR_ERR_SHAPE;
+        if (pl->shape[1] != R1 || pl->shape[2] != R2) return LAR_ERR_SHAPE;
         if (pl->shape[0] % HV != 0) return LAR_ERR_SHAPE;
         if (pl->stride[2] != 1) return LAR_ERR_STRIDE;
         P = pl->shape[0] / HV;
@@ -205,7 +211,7 @@ lar_status check_common(const Common& c, int form, DecodeParams& p) {
         } else {
             return LAR_ERR_RANK;
         }
-        if (shp[0] != B || shp[1] != T || shp[2] != HV || shp[3] != V || shp[4] != K) return LAR_ERR_SHAPE;
+        if (shp[0] != B || shp[1] != T || shp[2] != HV || shp[3] != R1 || shp[4] != R2) return LAR_ERR_SHAPE;
         if (str[4] != 1) return LAR_ERR_STRIDE;
         // cached rows are written in aligned runs of 8 or 16 bytes: aligned base, 16-byte strides
         const int64_t ies = elem_size(it->dtype);
@@ -252,12 +258,15 @@ lar_status delta_rule(int form, const lar_tensor* q, const lar_tensor* k, const 
                       const lar_tensor* state_idx, const lar_tensor* out, const lar_tensor* inter,
                       float scale, uint32_t flags, int32_t* dev_err, void* stream) {
     DecodeParams p{};
-    if (flags & ~static_cast<uint32_t>(LAR_QK_L2NORM | LAR_GATE_RAW | LAR_BETA_RAW)) return LAR_ERR_ARG;
+    if (flags & ~static_cast<uint32_t>(LAR_QK_L2NORM | LAR_GATE_RAW | LAR_BETA_RAW | LAR_STATE_KV))
+        return LAR_ERR_ARG;
     const bool tok = state_idx != nullptr;
+    const bool kv = (flags & LAR_STATE_KV) != 0;
+    if (tok && kv) return LAR_ERR_ARG;   // per-token slots are served for the [v][k] layout only
     if (tok && (read_idx == nullptr) == (num_accepted == nullptr)) return LAR_ERR_ARG;
     // the seed source ([B] index vector) goes through the common checks as the read index
     const lar_tensor* seed = read_idx ? read_idx : num_accepted;
-    lar_status st = check_common(Common{q, k, v, pool, seed, write_idx, out, inter}, form, p);
+    lar_status st = check_common(Common{q, k, v, pool, seed, write_idx, out, inter}, form, p, kv);
     if (st != LAR_OK) return st;
     p.nacc = nullptr; p.na_s = 0; p.na_dt = LAR_I32;
     p.tslot = nullptr; p.tsl_s[0] = p.tsl_s[1] = 0; p.tsl_dt = LAR_I32;

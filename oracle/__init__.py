@@ -154,7 +154,7 @@ def _as_btx(x, name, ndim_full):
 
 
 def _delta(per_channel, q, k, v, g, beta, pool, read_idx, write_idx, A_log, dt_bias,
-           qk_l2norm, gate_raw, beta_raw, scale, cache_intermediate, tokens=None):
+           qk_l2norm, gate_raw, beta_raw, scale, cache_intermediate, tokens=None, layout="vk"):
     lib = _load()
     q = _as_btxk(_f64(q), "q")
     k = _as_btxk(_f64(k), "k")
@@ -176,6 +176,12 @@ def _delta(per_channel, q, k, v, g, beta, pool, read_idx, write_idx, A_log, dt_b
         P = arr.shape[0]
     else:
         raise ValueError("pool must be [P,HV,V,K] or [P*HV,V,K]")
+    if layout == "kv":
+        # the pool holds S itself ([.., k, v]): the element of S[k][v] is reached
+        # with the row stride on k and the inner stride on v
+        st = np.array([st[0], st[1], st[3], st[2]], dtype=np.int64)
+    elif layout != "vk":
+        raise ValueError("layout must be 'vk' or 'kv'")
     ri = _i64(read_idx)
     wi = _i64(write_idx)
     A = _f64(A_log)
@@ -209,18 +215,20 @@ def _delta(per_channel, q, k, v, g, beta, pool, read_idx, write_idx, A_log, dt_b
 
 def gdn_decode(q, k, v, g, beta, pool, read_idx, write_idx=None, *, A_log=None,
                dt_bias=None, qk_l2norm=False, gate_raw=False, beta_raw=False, scale=1.0,
-               cache_intermediate=False):
-    """GDN: scalar log-decay g[b,t,hv]; see oracle.c for the recurrence."""
+               cache_intermediate=False, layout="vk"):
+    """GDN: scalar log-decay g[b,t,hv]; see oracle.c for the recurrence.
+    layout "vk": pool[p, hv, v, k] = S[k][v] (default); "kv": pool[p, hv, k, v] = S[k][v].
+    Returned states are in the [v][k] order either way."""
     return _delta(False, q, k, v, g, beta, pool, read_idx, write_idx, A_log, dt_bias,
-                  qk_l2norm, gate_raw, beta_raw, scale, cache_intermediate)
+                  qk_l2norm, gate_raw, beta_raw, scale, cache_intermediate, layout=layout)
 
 
 def kda_decode(q, k, v, g, beta, pool, read_idx, write_idx=None, *, A_log=None,
                dt_bias=None, qk_l2norm=False, gate_raw=False, beta_raw=False, scale=1.0,
-               cache_intermediate=False):
-    """KDA: per-key-channel log-decay g[b,t,hv,k]; see oracle.c."""
+               cache_intermediate=False, layout="vk"):
+    """KDA: per-key-channel log-decay g[b,t,hv,k]; see oracle.c (layout as gdn_decode)."""
     return _delta(True, q, k, v, g, beta, pool, read_idx, write_idx, A_log, dt_bias,
-                  qk_l2norm, gate_raw, beta_raw, scale, cache_intermediate)
+                  qk_l2norm, gate_raw, beta_raw, scale, cache_intermediate, layout=layout)
 
 
 def gdn_decode_tokens(q, k, v, g, beta, pool, state_idx, *, read_idx=None, num_accepted=None,

@@ -99,7 +99,8 @@ def run_gpu(w, dev, *, pool=None, read_idx=None, write_idx="same", inter=True, d
     v = v if v is not None else to_dev(w.v, dev)
     it = None
     if inter and w.cache_intermediate:
-        it = torch.full((w.B, w.T, w.HV, w.V, w.K), float("nan"), device=dev, dtype=w.inter_dtype)
+        shape = (w.B, w.T, w.HV, w.K, w.V) if w.state_kv else (w.B, w.T, w.HV, w.V, w.K)
+        it = torch.full(shape, float("nan"), device=dev, dtype=w.inter_dtype)
     if w.form == "la":
         out = lar.la_decode(q, k, v, to_dev(w.decay, dev), pool, ri, wi, inter=it,
                             scale=w.scale, dev_err=dev_err, out_dtype=w.out_dtype)
@@ -108,7 +109,7 @@ def run_gpu(w, dev, *, pool=None, read_idx=None, write_idx="same", inter=True, d
         out = fn(q, k, v, to_dev(w.g, dev), to_dev(w.beta, dev), pool, ri, wi, inter=it,
                  A_log=to_dev(w.A_log, dev), dt_bias=to_dev(w.dt_bias, dev), scale=w.scale,
                  qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw,
-                 dev_err=dev_err, out_dtype=w.out_dtype)
+                 state_kv=w.state_kv, dev_err=dev_err, out_dtype=w.out_dtype)
     return out, it
 
 
@@ -124,7 +125,8 @@ def run_oracle(w, host_pool, *, read_idx=None, write_idx="same", batch=None):
     fn = oracle.gdn_decode if w.form == "gdn" else oracle.kda_decode
     return fn(sel(w.q), sel(w.k), sel(w.v), sel(w.g), sel(w.beta), host_pool, sel(ri), sel(wi),
               A_log=w.A_log, dt_bias=w.dt_bias, qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw,
-              beta_raw=w.beta_raw, scale=w.scale, cache_intermediate=w.cache_intermediate)
+              beta_raw=w.beta_raw, scale=w.scale, cache_intermediate=w.cache_intermediate,
+              layout="kv" if w.state_kv else "vk")
 
 
 def full_check(w, dev):
@@ -145,15 +147,17 @@ def full_check(w, dev):
     torch.cuda.synchronize()
     ref = run_oracle(w, host_view)
     errs = {"out": assert_out_close(out, ref["out"])}
+    # the oracle reports states as [v][k]; a [k][v] pool is compared through its transpose
+    tr = (lambda x: x.transpose(-1, -2)) if w.state_kv else (lambda x: x)
     if inter is not None:
-        errs["inter"] = assert_state_close(inter, ref["inter"], "inter")
+        errs["inter"] = assert_state_close(tr(inter), ref["inter"], "inter")
     mask = written_mask(w)
     assert torch.equal(dev_storage[~mask.to(dev)], before[~mask.to(dev)]), "untouched pool bytes changed"
     wi = (w.write_idx if w.write_idx is not None else w.read_idx).tolist()
     for b, s in enumerate(wi):
         if 0 <= s < w.P:
             errs["state"] = max(errs.get("state", 0.0),
-                                assert_state_close(slot_state(pool_dev, w, s), ref["final_state"][b],
+                                assert_state_close(tr(slot_state(pool_dev, w, s)), ref["final_state"][b],
                                                    f"slot {s} (entry {b})"))
     assert int(dev_err.item()) == 0
     return errs

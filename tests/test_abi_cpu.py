@@ -110,7 +110,7 @@ def test_empty_batch_is_a_no_op(lib):
     (lambda a: a.update(dt_bias=fake([4])), 0, ARG),
     (lambda a: None, 2, NULL),                                        # LAR_GATE_RAW without A_log
     (lambda a: a.update(A_log=fake([3])), 2, SHAPE),
-    (lambda a: None, 8, ARG),                                         # unknown flag bit
+    (lambda a: None, 16, ARG),                                        # unknown flag bit
     (lambda a: a.update(read_idx=fake([3], I32)), 0, SHAPE),
     (lambda a: a.update(read_idx=fake([2], F32)), 0, DTYPE),
     (lambda a: a.update(write_idx=fake([2, 1], I32)), 0, RANK),
@@ -175,3 +175,23 @@ def test_token_slots_rejects_on_host(lib):
     assert tok_call(lib, a, good, num_accepted=fake([2], I32)) == ARG  # two seed sources
     assert tok_call(lib, a, good, read_idx=None, num_accepted=fake([3], I32)) == SHAPE
     assert tok_call(lib, gdn_args(B=0, T=3), fake([0, 3], I32)) == OK
+
+
+def test_kv_layout_validation(lib):
+    KV = 8
+    a = gdn_args(B=2, T=1, H=2, HV=4, K=128, V=64)
+    a["pool"] = fake([8, 4, 64, 128])                                 # [P,HV,V,K] is not [P,HV,K,V]
+    assert call(lib, a, KV) == SHAPE
+    a = gdn_args(B=2, T=1, H=2, HV=4, K=128, V=66)
+    a["pool"] = fake([8, 4, 128, 66])                                 # 66 fp32 rows: not 16-byte chunks
+    assert call(lib, a, KV) == SHAPE
+    a = gdn_args(B=2, T=1, H=2, HV=4, K=128, V=64)
+    a["pool"] = fake([8, 4, 128, 64], strides=[4 * 128 * 64, 128 * 64, 1, 128])   # v not contiguous
+    assert call(lib, a, KV) == STRIDE
+    # per-token slots are served for the [v][k] layout only
+    a = gdn_args(B=2, T=3)
+    a["pool"] = fake([8, 4, 128, 64])
+    refs = [ctypes.byref(x) if x is not None else None for x in
+            [a[n] for n in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "pool")] + [a["read_idx"], None,
+                                                                                       fake([2, 3], I32), a["out"]]]
+    assert lib.gdn_decode_tokens(*refs, 1.0, KV, None, None) == ARG

@@ -16,7 +16,7 @@ def _sample(B, seed=0, n=6):
 
 
 @pytest.mark.parametrize("name", ["gdn_b64", "gdn_mtp_strided", "kda_b256", "la_b512_packed",
-                                  "gdn_b64_bf16"])
+                                  "gdn_b64_bf16", "gdn_b64_kv"])
 def test_full_size(name, cuda_device):
     dev = cuda_device
     w = W.make(name, pool_device=dev)
@@ -50,12 +50,13 @@ def test_full_size(name, cuda_device):
     wi_sub = torch.full((w.B,), -1, dtype=torch.int64)
     ref = P.run_oracle(w, sub, read_idx=ri_sub, write_idx=wi_sub, batch=sample)
     P.assert_out_close(out[sample], ref["out"].reshape(out[sample].shape))
+    tr = (lambda x: x.transpose(-1, -2)) if w.state_kv else (lambda x: x)
     if inter is not None:
-        P.assert_state_close(inter[sample], ref["inter"], "inter")
+        P.assert_state_close(tr(inter[sample]), ref["inter"], "inter")
     wi = (w.write_idx if w.write_idx is not None else w.read_idx).tolist()
     for i, b in enumerate(sample):
         if 0 <= wi[b] < w.P:
-            P.assert_state_close(P.slot_state(w.pool, w, wi[b]), ref["final_state"][i],
+            P.assert_state_close(tr(P.slot_state(w.pool, w, wi[b])), ref["final_state"][i],
                                  f"slot {wi[b]} (entry {b})")
 
 

@@ -65,6 +65,22 @@ SWEEP = {
                                   state_dtype=torch.bfloat16)),
     "la_bf16_k16": ("la", dict(B=2, T=2, H=2, K=16, V=24, flat_pool=True, state_dtype=torch.bfloat16)),
     "gdn_bf16_unstaged_v": ("gdn", dict(B=2, T=16, H=1, HV=1, K=64, V=300, state_dtype=torch.bfloat16)),
+    # [k][v] ("nontranspose") state layout
+    "gdn_kv_t1": ("gdn", dict(B=5, T=1, H=2, HV=4, K=128, V=128, state_kv=True)),
+    "gdn_kv_mtp_strided": ("gdn", dict(B=4, T=4, H=2, HV=4, K=128, V=96, state_kv=True, stride_mult=2,
+                                       separate_write=True, skip_frac=0.25, cache_intermediate=True)),
+    "gdn_kv_ragged_k64": ("gdn", dict(B=3, T=3, H=1, HV=2, K=64, V=72, state_kv=True,
+                                      cache_intermediate=True)),
+    "gdn_kv_k16": ("gdn", dict(B=2, T=2, H=2, HV=2, K=16, V=16, state_kv=True)),
+    "gdn_kv_k32_f32": ("gdn", dict(B=3, T=1, H=1, HV=3, K=32, V=40, state_kv=True, in_dtype=F32,
+                                   out_dtype=F32)),
+    "kda_kv_raw": ("kda", dict(B=4, T=2, H=2, HV=2, K=128, V=128, raw_gates=True, state_kv=True,
+                               cache_intermediate=True)),
+    "gdn_kv_bf16": ("gdn", dict(B=4, T=2, H=2, HV=4, K=128, V=128, state_kv=True,
+                                state_dtype=torch.bfloat16, cache_intermediate=True)),
+    "kda_kv_bf16_k16": ("kda", dict(B=3, T=1, H=1, HV=2, K=16, V=24, state_kv=True,
+                                    state_dtype=torch.bfloat16)),
+    "gdn_kv_unstaged_v": ("gdn", dict(B=2, T=16, H=1, HV=1, K=64, V=320, state_kv=True)),
 }
 
 

@@ -522,3 +522,17 @@ def test_accepted_count_outside_range_is_counted_with_zero_seed():
     assert res["n_bad"] == 2
     zero = oracle.kda_decode_tokens(q, k, v, g, beta, p2, slots, read_idx=torch.tensor([-1, -1, int(slots[2, 3])]))
     assert np.array_equal(res["out"], zero["out"])
+
+
+def test_kv_layout_equals_transposed_pool():
+    """Holding S untransposed ([.., k, v]) is only a different storage order: the
+    results equal those of the [.., v, k] pool holding the transposed states,
+    and the written slots are the transposes of each other."""
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(True, seed=23)
+    p_vk = pool.clone()
+    p_kv = pool.transpose(2, 3).contiguous()
+    a = oracle.kda_decode(q, k, v, g, beta, p_vk, ri, wi, cache_intermediate=True)
+    b = oracle.kda_decode(q, k, v, g, beta, p_kv, ri, wi, cache_intermediate=True, layout="kv")
+    for key in ("out", "final_state", "inter"):
+        assert np.array_equal(a[key], b[key])
+    assert torch.equal(p_kv, p_vk.transpose(2, 3))

@@ -25,6 +25,7 @@ kda_b256           B=256 T=1 H=HV=24, raw bf16 q/k (l2norm in kernel), raw bf16
                    N(0, 0.1) [HV*K], raw beta logits; pool [320,24,128,128];
                    read = write = randperm(320)[:256]; seed 4
 gdn_b64_bf16       gdn_b64 with a bfloat16 state pool (drawn in fp32, rounded once)
+gdn_b64_kv         gdn_b64 with the state held untransposed, pool [256,32,128(k),128(v)]
 gdn_spec_b64       B=64 T=4 H=16 HV=32, per-token pool slots: one row of 4 distinct
                    slots per sequence (of 320), seed = slot of the last accepted
                    token, accepted counts uniform in 1..4; seed 6
@@ -51,9 +52,9 @@ BF16 = torch.bfloat16
 F32 = torch.float32
 
 CONFIGS = ("gdn_tiny", "gdn_b64", "gdn_mtp_strided", "kda_b256", "la_b512_packed",
-           "gdn_b64_bf16", "gdn_spec_b64")
+           "gdn_b64_bf16", "gdn_spec_b64", "gdn_b64_kv")
 SEEDS = {"gdn_tiny": 0, "gdn_b64": 2, "gdn_mtp_strided": 3, "kda_b256": 4,
-         "la_b512_packed": 5, "gdn_b64_bf16": 2, "gdn_spec_b64": 6}
+         "la_b512_packed": 5, "gdn_b64_bf16": 2, "gdn_spec_b64": 6, "gdn_b64_kv": 2}
 
 
 @dataclass
@@ -87,6 +88,7 @@ class Workload:
     scale: float = 1.0
     cache_intermediate: bool = False
     inter_dtype: torch.dtype = F32
+    state_kv: bool = False                     # pool / cache hold S as [k][v] (v fastest)
     state_idx: torch.Tensor | None = None      # per-token write slots [B, T] (token-slot mode)
     num_accepted: torch.Tensor | None = None   # seed selection [B] (token-slot mode)
     meta: dict = field(default_factory=dict)
@@ -166,7 +168,7 @@ def make(name: str, *, seed: int | None = None, pool_device="cpu",
         pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
         return Workload(name, "gdn", B, T, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
                         F32, g=g, beta=beta)
-    if name in ("gdn_b64", "gdn_b64_bf16"):
+    if name in ("gdn_b64", "gdn_b64_bf16", "gdn_b64_kv"):
         B, T, H, HV, K, V, P = 64, 1, 16, 32, 128, 128, 256
         q = _l2n(_normal(gen, (B, T, H, K))).to(BF16)
         k = _l2n(_normal(gen, (B, T, H, K))).to(BF16)
@@ -174,10 +176,11 @@ def make(name: str, *, seed: int | None = None, pool_device="cpu",
         g = -F.softplus(_normal(gen, (B, T, HV)))
         beta = torch.sigmoid(_normal(gen, (B, T, HV)))
         ri = torch.randperm(P, generator=gen)[:B].to(index_dtype)
-        pool = _draw_pool(gen, (P, HV, V, K), s, pool_device,
+        kv = name == "gdn_b64_kv"
+        pool = _draw_pool(gen, (P, HV, K, V) if kv else (P, HV, V, K), s, pool_device,
                           BF16 if name == "gdn_b64_bf16" else F32)
         return Workload(name, "gdn", B, T, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
-                        BF16, g=g, beta=beta)
+                        BF16, g=g, beta=beta, state_kv=kv)
     if name == "gdn_mtp_strided":
         B, T, H, HV, K, V, M = 16, 4, 16, 32, 128, 128, 2
         P = 128
@@ -259,7 +262,7 @@ def make_custom(form: str, *, B: int, T: int, H: int, HV: int | None = None, K: 
                 stride_mult: int = 1, cache_intermediate: bool = False,
                 raw_gates: bool = False, packed: bool = False, flat_pool: bool = False,
                 index_dtype=torch.int32, pool_device="cpu", state_dtype=F32,
-                inter_dtype=None) -> Workload:
+                inter_dtype=None, state_kv: bool = False) -> Workload:
     """A workload of any size in the same distributions as the named recipes.
 
     ``raw_gates``: q/k raw N(0,1) with in-kernel l2norm, raw gate input and beta
@@ -269,7 +272,7 @@ def make_custom(form: str, *, B: int, T: int, H: int, HV: int | None = None, K: 
     ``stride_mult`` > 1: the pool is backing[::stride_mult].
     ``packed``: q/k/v are slices of one fused [B,T,H,2K+V] buffer (needs H == HV).
     ``state_dtype``: fp32 or bf16 pool; ``inter_dtype``: the state cache's type
-    (default: the pool's).
+    (default: the pool's).  ``state_kv``: the pool holds S as [P, HV, K, V].
     """
     HV = H if HV is None else HV
     P = max(2 * B, 4) if P is None else P
@@ -328,8 +331,11 @@ def make_custom(form: str, *, B: int, T: int, H: int, HV: int | None = None, K: 
     if form == "la" and flat_pool:
         pool = _draw_pool(gen, (P * H, V, K), seed, pool_device, state_dtype)
     elif stride_mult > 1:
-        backing = _draw_pool(gen, (P * stride_mult, HV, V, K), seed, pool_device, state_dtype)
+        rows = (K, V) if state_kv else (V, K)
+        backing = _draw_pool(gen, (P * stride_mult, HV) + rows, seed, pool_device, state_dtype)
         pool = backing[::stride_mult]
+    elif state_kv:
+        pool = _draw_pool(gen, (P, HV, K, V), seed, pool_device, state_dtype)
     else:
         pool = _draw_pool(gen, (P, HV, V, K), seed, pool_device, state_dtype)
     return Workload(f"custom_{form}", form, B, T, H, HV, K, V, P, q, k, v, pool,
@@ -339,7 +345,8 @@ def make_custom(form: str, *, B: int, T: int, H: int, HV: int | None = None, K: 
                     gate_raw=raw_gates and form != "la",
                     beta_raw=raw_gates and form != "la",
                     cache_intermediate=cache_intermediate,
-                    inter_dtype=state_dtype if inter_dtype is None else inter_dtype)
+                    inter_dtype=state_dtype if inter_dtype is None else inter_dtype,
+                    state_kv=state_kv)
 
 
 def disjoint_index_sets(P: int, B: int, n: int, seed: int, index_dtype=torch.int32):
