@@ -47,6 +47,14 @@
 #ifndef LAR_K128_MIN_BLOCKS
 #define LAR_K128_MIN_BLOCKS 3
 #endif
+// Resident CTAs per SM the fp32 GDN and the bf16 GDN / LA K = 128 kernels are
+// compiled for (1: no register cap).
+#ifndef LAR_K128_GDN_MB
+#define LAR_K128_GDN_MB 1
+#endif
+#ifndef LAR_K128_BF16_MB
+#define LAR_K128_BF16_MB 1
+#endif
 #ifndef LAR_K128_LPR
 #define LAR_K128_LPR 8
 #endif
@@ -58,6 +66,14 @@
 #endif
 #ifndef LAR_K128_S
 #define LAR_K128_S 2
+#endif
+// ring stages of the fp32 K = 128 multi-token instances (a tile's compute
+// grows with T, so one more tile stays in flight)
+#ifndef LAR_K128_S_MTP
+#define LAR_K128_S_MTP 3
+#endif
+#ifndef LAR_K128_BF16_NR
+#define LAR_K128_BF16_NR 1
 #endif
 
 namespace lar {
@@ -126,9 +142,48 @@ __device__ __forceinline__ void chunk_to_f32(const unsigned char* p, float* d) {
     }
 }
 
+// 16-byte shared-memory chunk of EPC pool elements -> EPC/2 float pairs
+// (element 2i in .x, 2i+1 in .y; bf16 widens exactly).
+template <int SB>
+__device__ __forceinline__ void chunk_to_f2(const unsigned char* p, float2* d) {
+    if constexpr (SB == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(p);
+        d[0] = make_float2(v.x, v.y);
+        d[1] = make_float2(v.z, v.w);
+    } else {
+        const uint4 v = *reinterpret_cast<const uint4*>(p);
+        const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)   // low half: element 2q, high half: element 2q+1
+            d[q] = make_float2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u));
+    }
+}
+
+__device__ __forceinline__ void st_shared_zero16(void* smem_dst) {
+    *reinterpret_cast<float4*>(smem_dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 __device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // .x = lo (low 16 bits)
     return *reinterpret_cast<const unsigned*>(&h);
+}
+
+// Streaming store of N floats held as N/2 pairs (N = 4 or 8, contiguous), as
+// fp32 or as bf16 (RNE).
+template <int N>
+__device__ __forceinline__ void store_pairs(void* g, const float2* d, bool bf16) {
+    if (bf16) {
+        if constexpr (N == 8) {
+            __stcs(reinterpret_cast<uint4*>(g), make_uint4(pack_bf16x2(d[0].x, d[0].y), pack_bf16x2(d[1].x, d[1].y),
+                                                          pack_bf16x2(d[2].x, d[2].y), pack_bf16x2(d[3].x, d[3].y)));
+        } else {
+            __stcs(reinterpret_cast<uint2*>(g), make_uint2(pack_bf16x2(d[0].x, d[0].y), pack_bf16x2(d[1].x, d[1].y)));
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < N / 4; ++q)
+            __stcs(reinterpret_cast<float4*>(g) + q, make_float4(d[2 * q].x, d[2 * q].y, d[2 * q + 1].x, d[2 * q + 1].y));
+    }
 }
 
 // Streaming store of N floats (N = 4 or 8, contiguous) as fp32 or as bf16 (RNE).
@@ -202,11 +257,9 @@ __device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float*
         }
     }
     if (sv_on) {
-        for (int i = threadIdx.x; i < T * V; i += NW * 32) {
-            const int t = i / V;
-            const int row = i - t * V;
-            vb[o_v + i] = ld_in(p.v, v_off + t * p.vs[1] + row * p.vs[3], p.v_dt);
-        }
+        for (int t = 0; t < T; ++t)
+            for (int row = threadIdx.x; row < V; row += NW * 32)
+                vb[o_v + t * V + row] = ld_in(p.v, v_off + t * p.vs[1] + row * p.vs[3], p.v_dt);
     }
     float* sc = vb + o_s;
     for (int t = threadIdx.x; t < T; t += NW * 32) {
@@ -255,15 +308,16 @@ __device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float*
 
 // TOK: per-token pool slots (seed from the accepted count or read_idx, the state
 // after every token stored to its slot, no final writeback); compiled
-// separately so the plain decode carries none of it.
-template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB, bool TOK>
+// separately so the plain decode carries none of it.  TT: the token count when
+// fixed at compile time (single-token decode), 0 when taken from the call.
+template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB, bool TOK, int TT>
 __global__ void __launch_bounds__(NW * 32, MB)
 decode_kernel(const DecodeParams p) {
     using G = Tile<K, LPR, NR, NW, SB>;
     constexpr int NCH = G::NCH, RPW = G::RPW, TV = G::TV, EPC = G::EPC, KPL = G::KPL;
 
     extern __shared__ __align__(16) unsigned char smem[];
-    const int T = p.T;
+    const int T = TT > 0 ? TT : p.T;
     const int V = p.V;
     const bool sv_on = stage_v(T, V);
     unsigned char* ring = smem;                                               // [S][TV][K] pool elements
@@ -272,6 +326,8 @@ decode_kernel(const DecodeParams p) {
     const unsigned char* pool_b = static_cast<const unsigned char*>(p.pool);
     const bool inter_bf16 = p.inter_dt == LAR_BF16;
     const int inter_es = inter_bf16 ? 2 : 4;
+    const bool out_bf16 = p.out_dt == LAR_BF16;
+    const int out_es = out_bf16 ? 2 : 4;
     const int vstride = vec_floats<FORM, K>(T, V);
     // offsets inside a vector buffer
     const int o_k = T * K;
@@ -296,14 +352,12 @@ decode_kernel(const DecodeParams p) {
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 #endif
+    if (t_begin >= t_end) return;
 
-    // local row (within a tile) of this thread's i-th row
-    auto lrow = [&](int i) { return (warp * NR + i) * RPW + gi; };
-
-    // Byte offsets fixed for the whole kernel.  A thread's rows in a tile are
-    // row0, row0 + RPW, ... and its chunks in a row are CSTEP bytes apart, so
-    // every chunk address is a per-tile base plus compile-time steps.
-    const int row0 = lrow(0);
+    // A thread's rows in a tile are row0, row0 + RPW, ... and its chunks in a
+    // row are CSTEP bytes apart, so every address below is a per-pair base,
+    // advanced by a fixed step per tile, plus compile-time offsets.
+    const int row0 = (warp * NR) * RPW + gi;
     constexpr int CSTEP = LPR * 16;                 // between a lane's chunks of one row
     constexpr int STAGE = TV * K * SB;              // one ring stage
     constexpr int S_RSTEP = RPW * K * SB;           // between a thread's rows in a stage
@@ -311,34 +365,13 @@ decode_kernel(const DecodeParams p) {
     const int64_t g_row0 = static_cast<int64_t>(row0) * p.ps[2] * SB + j * 16;
     const int64_t g_rstep = static_cast<int64_t>(RPW) * p.ps[2] * SB;
     const int64_t g_tile = static_cast<int64_t>(TV) * p.ps[2] * SB;
+    const int64_t o_rstep = static_cast<int64_t>(RPW) * p.os[3] * out_es;
+    const int64_t o_tstep = p.os[1] * out_es;
+    const int64_t o_tile = static_cast<int64_t>(TV) * p.os[3] * out_es;
+    const int64_t i_rstep = static_cast<int64_t>(RPW) * p.is[3] * inter_es;
+    const int64_t i_tstep = p.is[1] * inter_es;
+    const int64_t i_tile = static_cast<int64_t>(TV) * p.is[3] * inter_es;
 
-    // tile coordinates, advanced incrementally (no per-tile 64-bit division)
-    struct Pos {
-        int64_t tile;
-        int vt, hv, b;
-    };
-    auto advance = [&](Pos& q) {
-        ++q.tile;
-        if (++q.vt == nvt) {
-            q.vt = 0;
-            if (++q.hv == p.HV) {
-                q.hv = 0;
-                ++q.b;
-            }
-        }
-    };
-    Pos cur;
-    {
-        const int64_t u = t_begin / nvt;
-        cur.tile = t_begin;
-        cur.vt = static_cast<int>(t_begin - u * nvt);
-        cur.b = static_cast<int>(u / p.HV);
-        cur.hv = static_cast<int>(u - static_cast<int64_t>(cur.b) * p.HV);
-    }
-
-    // read slot of a prefetch position, reloaded only when its batch entry changes
-    int ahead_b = -1;
-    int64_t ahead_r = -1;
     // Read slot of entry b: read_idx[b], or, with accepted-token counts, the
     // slot that holds the state after the last accepted token,
     // state_idx[b][num_accepted[b] - 1]; a count outside [1, T] has no such
@@ -350,27 +383,61 @@ decode_kernel(const DecodeParams p) {
         if (a < 1 || a > T) return kBadCount;
         return ld_idx(p.tslot, b * p.tsl_s[0] + (a - 1) * p.tsl_s[1], p.tsl_dt);
     };
-    auto slot_of = [&](const Pos& q) -> int64_t {
-        if (q.tile >= t_end) return -1;
-        if (q.b != ahead_b) {
-            ahead_b = q.b;
-            ahead_r = seed_of(q.b);
-        }
-        return ahead_r;
-    };
 
-    // issue this thread's copies of the tile at `q` (read slot r) into ring stage `st`
-    auto issue = [&](const Pos& q, int64_t r, int st) {
-        if (q.tile < t_end && r >= 0 && r < p.P) {
-            const unsigned char* src = pool_b + (r * p.ps[0] + static_cast<int64_t>(q.hv) * p.ps[1]) * SB +
-                                       q.vt * g_tile + g_row0;
+    // ---- issue cursor: the next tile whose copies go out.  Its read slot is
+    // loaded one tile before the copies need it (a_r), and its source address
+    // is a running pointer rebuilt only when the cursor enters a new pair.
+    int64_t a_left = t_end - t_begin;
+    int a_vt, a_hv, a_b;
+    {
+        const int64_t u = t_begin / nvt;
+        a_vt = static_cast<int>(t_begin - u * nvt);
+        a_b = static_cast<int>(u / p.HV);
+        a_hv = static_cast<int>(u - static_cast<int64_t>(a_b) * p.HV);
+    }
+    const int c_vt0 = a_vt, c_hv0 = a_hv, c_b0 = a_b;   // the consumer starts where the issuer does
+    int a_rb = a_b;                  // batch entry whose read slot a_r holds
+    int64_t a_r = seed_of(a_b);
+    bool a_new = true;               // a_src must be rebuilt from a_r before the next issue
+    bool a_ok = false;
+    const unsigned char* a_src = pool_b;
+
+    // issue this thread's copies of the next tile into ring stage `st`; chunks
+    // with no state behind them (no valid read slot, rows past V) are zeroed in
+    // place, so the consumer reads every chunk unconditionally
+    auto issue = [&](int st) {
+        if (a_left > 0) {
+            if (a_new) {
+                a_ok = a_r >= 0 && a_r < p.P;
+                a_src = pool_b + ((a_ok ? a_r : 0) * p.ps[0] + static_cast<int64_t>(a_hv) * p.ps[1]) * SB +
+                        a_vt * g_tile + g_row0;
+                a_new = false;
+            }
             unsigned char* dst = ring + st * STAGE + s_row0;
+            const int rl = V - a_vt * TV - row0;     // rows of the tile from this thread's first row on
 #pragma unroll
             for (int i = 0; i < NR; ++i) {
-                if (q.vt * TV + row0 + i * RPW < V) {
+                const bool ok = a_ok && i * RPW < rl;
 #pragma unroll
-                    for (int c = 0; c < NCH; ++c)
-                        cp_async16(dst + i * S_RSTEP + c * CSTEP, src + i * g_rstep + c * CSTEP);
+                for (int c = 0; c < NCH; ++c) {
+                    if (ok) cp_async16(dst + i * S_RSTEP + c * CSTEP, a_src + i * g_rstep + c * CSTEP);
+                    else st_shared_zero16(dst + i * S_RSTEP + c * CSTEP);
+                }
+            }
+            if (--a_left > 0) {
+                if (++a_vt == nvt) {
+                    a_vt = 0;
+                    if (++a_hv == p.HV) {
+                        a_hv = 0;
+                        ++a_b;
+                    }
+                    if (a_b != a_rb) {       // the slot load's latency hides behind one tile of work
+                        a_rb = a_b;
+                        a_r = seed_of(a_b);
+                    }
+                    a_new = true;
+                } else {
+                    a_src += g_tile;
                 }
             }
         }
@@ -378,35 +445,34 @@ decode_kernel(const DecodeParams p) {
     };
 
     // ---- prologue: S-1 tiles in flight before the first is consumed
-    Pos ahead = cur;
 #pragma unroll
-    for (int s = 0; s < S - 1; ++s) {
-        issue(ahead, slot_of(ahead), s);
-        advance(ahead);
-    }
+    for (int s = 0; s < S - 1; ++s) issue(s);
 
+    // ---- consumer cursor and the current pair's running pointers
+    int c_vt = c_vt0, c_hv = c_hv0, c_b = c_b0;
     int buf = 1;
-    bool rd = false, wr = false;
-    unsigned char* dst_state = nullptr;     // state rows of the current pair (write slot)
-    int64_t v_off = 0, o_off = 0;           // per-pair offsets into v and out
-    unsigned char* inter_base = nullptr;
+    bool wr = false;
+    unsigned char* wb = nullptr;         // this thread's first row of the tile in the write slot
+    unsigned char* op = nullptr;         // its output element for token 0
+    unsigned char* ip = nullptr;         // its first cached chunk for token 0
+    unsigned char* tk = nullptr;         // per-token slots: head + tile + row offset inside a slot
+    int64_t v_off = 0;
     const float scale = p.scale;
+    bool pair_start = true;
 
     int stage = 0;                 // ring stage of the tile being consumed
     int stage_next = S - 1;        // ring stage the next issue goes to
 #pragma unroll 1
-    for (; cur.tile < t_end; advance(cur)) {
-        // read slot of the tile issued at the end of this iteration
-        const int64_t r_ahead = slot_of(ahead);
-        const int b = cur.b, hv = cur.hv, vt = cur.vt;
-        if (vt == 0 || cur.tile == t_begin) {
+    for (int64_t n = t_end - t_begin; n > 0; --n) {
+        const int b = c_b, hv = c_hv, vt = c_vt;
+        if (pair_start) {
             // ---- new (b, hv) pair: slots, bases and per-token vectors
+            pair_start = false;
             const int h = hv / p.group;
             buf ^= 1;
             const int64_t r = seed_of(b);
             // with per-token slots every token's state is stored; there is no final writeback
             const int64_t w = TOK ? -1 : (p.widx ? ld_idx(p.widx, b * p.wi_s, p.wi_dt) : r);
-            rd = r >= 0 && r < p.P;
             wr = w >= 0 && w < p.P;
             if constexpr (TOK) {
                 long long* tab = slot_tab + buf * kMaxTokens;
@@ -421,93 +487,110 @@ decode_kernel(const DecodeParams p) {
                         if (ld_idx(p.tslot, b * p.tsl_s[0] + t * p.tsl_s[1], p.tsl_dt) >= p.P) e |= LAR_DEVERR_WRITE_SLOT;
                 if (e) atomicOr(p.dev_err, e);
             }
-            dst_state = static_cast<unsigned char*>(p.pool) +
-                        ((wr ? w : 0) * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1]) * SB;
+            const int64_t head_tile = static_cast<int64_t>(hv) * p.ps[1] * SB + vt * g_tile + g_row0;
+            wb = static_cast<unsigned char*>(p.pool) + (wr ? w : 0) * p.ps[0] * SB + head_tile;
+            tk = static_cast<unsigned char*>(p.pool) + head_tile;
+            const int64_t first_row = static_cast<int64_t>(vt) * TV + row0;
             v_off = b * p.vs[0] + hv * p.vs[2];
-            o_off = b * p.os[0] + hv * p.os[2];
-            if (p.inter) inter_base = static_cast<unsigned char*>(p.inter) + (b * p.is[0] + hv * p.is[2]) * inter_es;
+            op = static_cast<unsigned char*>(p.out) + (b * p.os[0] + hv * p.os[2] + first_row * p.os[3]) * out_es;
+            if (p.inter)
+                ip = static_cast<unsigned char*>(p.inter) +
+                     (b * p.is[0] + hv * p.is[2] + first_row * p.is[3] + j * EPC) * inter_es;
 
             build_pair_vectors<FORM, K, NW>(p, vecs + buf * vstride, b, hv, h, v_off, sv_on, o_k, o_d, o_v, o_s);
         }
 
         // ---- this thread's copies of the tile have landed: pull its rows into registers
         cp_async_wait<S - 2>();
-        float s[NR][KPL];
+        float2 s[NR][KPL / 2];   // element 2e in .x, 2e+1 in .y
         {
             const unsigned char* src = ring + stage * STAGE + s_row0;
 #pragma unroll
-            for (int i = 0; i < NR; ++i) {
-                const bool ok = rd && vt * TV + row0 + i * RPW < V;
+            for (int i = 0; i < NR; ++i)
 #pragma unroll
-                for (int c = 0; c < NCH; ++c) {
-                    if (ok) {
-                        chunk_to_f32<SB>(src + i * S_RSTEP + c * CSTEP, &s[i][c * EPC]);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < EPC; ++e) s[i][c * EPC + e] = 0.f;
-                    }
-                }
-            }
+                for (int c = 0; c < NCH; ++c) chunk_to_f2<SB>(src + i * S_RSTEP + c * CSTEP, &s[i][c * EPC / 2]);
         }
         // refill the stage consumed in the previous iteration (its rows were used long ago)
-        issue(ahead, r_ahead, stage_next);
-        advance(ahead);
+        issue(stage_next);
         stage = stage + 1 == S ? 0 : stage + 1;
         stage_next = stage_next + 1 == S ? 0 : stage_next + 1;
 
-        // ---- token loop: the state never leaves registers between tokens
+        const int rl = V - vt * TV - row0;   // rows of the tile from this thread's first row on
+
+        // ---- token loop: the state never leaves registers between tokens.  The
+        // arithmetic runs on element pairs (packed fp32x2 multiply / fma); each
+        // reduction keeps two pair accumulators, summed before the shuffles.
         const float* vb = vecs + buf * vstride;
         const float* sc = vb + o_s;
+        constexpr int KP = KPL / 2;   // element pairs per lane and row
+        unsigned char* opt = op;
+        unsigned char* ipt = ip;
 #pragma unroll 1
-        for (int t = 0; t < T; ++t) {
+        for (int t = 0; t < T; ++t, opt += o_tstep, ipt += i_tstep) {
             const float bt = sc[t], dec = sc[T + t];
             const float iq = sc[2 * T + t], ik = sc[3 * T + t], kq = sc[4 * T + t];
-            float kv[KPL], qv[KPL], dv[KPL];
+            float2 kv[KP], qv[KP], dv[KP];
+            const float* qrow = vb + t * K + j * EPC;
 #pragma unroll
             for (int c = 0; c < NCH; ++c) {
 #pragma unroll
                 for (int e4 = 0; e4 < EPC / 4; ++e4) {
-                    const int kidx = t * K + (c * LPR + j) * EPC + 4 * e4;
-                    const float4 a4 = *reinterpret_cast<const float4*>(vb + kidx);
-                    const float4 b4 = *reinterpret_cast<const float4*>(vb + o_k + kidx);
-                    float* qd = &qv[c * EPC + 4 * e4];
-                    float* kd = &kv[c * EPC + 4 * e4];
-                    qd[0] = a4.x; qd[1] = a4.y; qd[2] = a4.z; qd[3] = a4.w;
-                    kd[0] = b4.x; kd[1] = b4.y; kd[2] = b4.z; kd[3] = b4.w;
+                    const int kidx = c * LPR * EPC + 4 * e4;
+                    const int e = (c * EPC + 4 * e4) / 2;
+                    const float4 a4 = *reinterpret_cast<const float4*>(qrow + kidx);
+                    const float4 b4 = *reinterpret_cast<const float4*>(qrow + o_k + kidx);
+                    qv[e] = make_float2(a4.x, a4.y);
+                    qv[e + 1] = make_float2(a4.z, a4.w);
+                    kv[e] = make_float2(b4.x, b4.y);
+                    kv[e + 1] = make_float2(b4.z, b4.w);
                     if constexpr (FORM == FORM_KDA) {
-                        const float4 d4 = *reinterpret_cast<const float4*>(vb + o_d + kidx);
-                        float* dd = &dv[c * EPC + 4 * e4];
-                        dd[0] = d4.x; dd[1] = d4.y; dd[2] = d4.z; dd[3] = d4.w;
+                        const float4 d4 = *reinterpret_cast<const float4*>(qrow + o_d + kidx);
+                        dv[e] = make_float2(d4.x, d4.y);
+                        dv[e + 1] = make_float2(d4.z, d4.w);
                     }
                 }
             }
+            const float2 dec2 = make_float2(dec, dec);
+            long long ts = -1;
+            if constexpr (TOK) ts = slot_tab[buf * kMaxTokens + t];
 #pragma unroll
             for (int i = 0; i < NR; ++i) {
-                const int row = vt * TV + lrow(i);
-                const bool rv = row < V;
+                const bool rv = i * RPW < rl;
+                const int row = vt * TV + row0 + i * RPW;
                 float vval = 0.f;
                 if (rv) vval = sv_on ? vb[o_v + t * V + row] : ld_in(p.v, v_off + t * p.vs[1] + row * p.vs[3], p.v_dt);
 #pragma unroll
-                for (int e = 0; e < KPL; ++e) s[i][e] *= (FORM == FORM_KDA ? dv[e] : dec);
+                for (int e = 0; e < KP; ++e) s[i][e] = __fmul2_rn(s[i][e], FORM == FORM_KDA ? dv[e] : dec2);
                 // q_hat = iq q and k_hat = ik k: the norms scale the reduced sums
                 float o;
                 if constexpr (FORM == FORM_LA) {
-                    float pp = 0.f;
+                    float2 p0 = make_float2(0.f, 0.f), p1 = p0;
 #pragma unroll
-                    for (int e = 0; e < KPL; ++e) pp = fmaf(s[i][e], qv[e], pp);
+                    for (int e = 0; e < KP; e += 2) {
+                        p0 = __ffma2_rn(s[i][e], qv[e], p0);
+                        if (e + 1 < KP) p1 = __ffma2_rn(s[i][e + 1], qv[e + 1], p1);
+                    }
+                    float pp = (p0.x + p1.x) + (p0.y + p1.y);
 #pragma unroll
                     for (int off = LPR / 2; off > 0; off >>= 1) pp += __shfl_xor_sync(0xffffffffu, pp, off);
                     const float a = vval * ik;
+                    const float2 a2 = make_float2(a, a);
 #pragma unroll
-                    for (int e = 0; e < KPL; ++e) s[i][e] = fmaf(a, kv[e], s[i][e]);
+                    for (int e = 0; e < KP; ++e) s[i][e] = __ffma2_rn(a2, kv[e], s[i][e]);
                     o = fmaf(vval, kq, pp * iq);
                 } else {
-                    float uu = 0.f, pp = 0.f;
+                    float2 u0 = make_float2(0.f, 0.f), u1 = u0, p0 = u0, p1 = u0;
 #pragma unroll
-                    for (int e = 0; e < KPL; ++e) {
-                        uu = fmaf(s[i][e], kv[e], uu);
-                        pp = fmaf(s[i][e], qv[e], pp);
+                    for (int e = 0; e < KP; e += 2) {
+                        u0 = __ffma2_rn(s[i][e], kv[e], u0);
+                        p0 = __ffma2_rn(s[i][e], qv[e], p0);
+                        if (e + 1 < KP) {
+                            u1 = __ffma2_rn(s[i][e + 1], kv[e + 1], u1);
+                            p1 = __ffma2_rn(s[i][e + 1], qv[e + 1], p1);
+                        }
                     }
+                    float uu = (u0.x + u1.x) + (u0.y + u1.y);
+                    float pp = (p0.x + p1.x) + (p0.y + p1.y);
 #pragma unroll
                     for (int off = LPR / 2; off > 0; off >>= 1) {
                         uu += __shfl_xor_sync(0xffffffffu, uu, off);
@@ -515,42 +598,55 @@ decode_kernel(const DecodeParams p) {
                     }
                     const float delta = bt * (vval - uu * ik);
                     const float a = delta * ik;
+                    const float2 a2 = make_float2(a, a);
 #pragma unroll
-                    for (int e = 0; e < KPL; ++e) s[i][e] = fmaf(a, kv[e], s[i][e]);
+                    for (int e = 0; e < KP; ++e) s[i][e] = __ffma2_rn(a2, kv[e], s[i][e]);
                     o = fmaf(delta, kq, pp * iq);
                 }
-                if (j == 0 && rv)
-                    st_out(p.out, o_off + t * p.os[1] + row * p.os[3], p.out_dt, o * scale);
+                if (j == 0 && rv) {
+                    unsigned char* dst = opt + i * o_rstep;
+                    if (out_bf16) *reinterpret_cast<__nv_bfloat16*>(dst) = __float2bfloat16_rn(o * scale);
+                    else *reinterpret_cast<float*>(dst) = o * scale;
+                }
                 if (p.inter != nullptr && rv) {
-                    unsigned char* ip = inter_base + (t * p.is[1] + row * p.is[3]) * inter_es + j * EPC * inter_es;
+                    unsigned char* dst = ipt + i * i_rstep;
                     const int cstep = LPR * EPC * inter_es;
 #pragma unroll
-                    for (int c = 0; c < NCH; ++c) store_run<EPC>(ip + c * cstep, &s[i][c * EPC], inter_bf16);
+                    for (int c = 0; c < NCH; ++c) store_pairs<EPC>(dst + c * cstep, &s[i][c * EPC / 2], inter_bf16);
                 }
-                if (TOK && rv) {
-                    const long long ts = slot_tab[buf * kMaxTokens + t];
-                    if (ts >= 0 && ts < p.P) {
-                        unsigned char* tp = static_cast<unsigned char*>(p.pool) +
-                                            (ts * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1]) * SB +
-                                            vt * g_tile + g_row0 + i * g_rstep;
+                if (TOK && rv && ts >= 0 && ts < p.P) {
+                    unsigned char* dst = tk + ts * p.ps[0] * SB + i * g_rstep;
 #pragma unroll
-                        for (int c = 0; c < NCH; ++c) store_run<EPC>(tp + c * CSTEP, &s[i][c * EPC], SB == 2);
-                    }
+                    for (int c = 0; c < NCH; ++c) store_pairs<EPC>(dst + c * CSTEP, &s[i][c * EPC / 2], SB == 2);
                 }
             }
         }
 
         // ---- writeback to the write slot (skipped for negative / out-of-range slots)
         if (wr) {
-            unsigned char* wb = dst_state + vt * g_tile + g_row0;
 #pragma unroll
             for (int i = 0; i < NR; ++i) {
-                if (vt * TV + row0 + i * RPW < V) {
+                if (i * RPW < rl) {
 #pragma unroll
                     for (int c = 0; c < NCH; ++c)
-                        store_run<EPC>(wb + i * g_rstep + c * CSTEP, &s[i][c * EPC], SB == 2);
+                        store_pairs<EPC>(wb + i * g_rstep + c * CSTEP, &s[i][c * EPC / 2], SB == 2);
                 }
             }
+        }
+
+        // ---- advance the consumer: next tile of this pair, or the next pair
+        if (++c_vt == nvt) {
+            c_vt = 0;
+            if (++c_hv == p.HV) {
+                c_hv = 0;
+                ++c_b;
+            }
+            pair_start = true;
+        } else {
+            wb += g_tile;
+            tk += g_tile;
+            op += o_tile;
+            ip += i_tile;
         }
     }
     cp_async_wait<0>();   // nothing may be left in flight into shared memory at exit
@@ -560,10 +656,10 @@ decode_kernel(const DecodeParams p) {
 // once per (device, size) and cached.
 int cached_occupancy(const void* kern, int threads, size_t smem, size_t smem_max, int* sms_out);
 
-template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB, bool TOK>
+template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB, bool TOK, int TT>
 lar_status launch_tile_mode(const DecodeParams& p, cudaStream_t stream) {
     using G = Tile<K, LPR, NR, NW, SB>;
-    auto kern = decode_kernel<FORM, K, LPR, NR, NW, S, SB, MB, TOK>;
+    auto kern = decode_kernel<FORM, K, LPR, NR, NW, S, SB, MB, TOK, TT>;
     const size_t smem = decode_smem_bytes<FORM, K, LPR, NR, NW, S, SB>(p.T, p.V);
     // the largest footprint any call can ask for (T = 16 with staged v)
     constexpr size_t smem_max = decode_smem_bytes<FORM, K, LPR, NR, NW, S, SB>(16, kStageVMax / 16);
@@ -593,20 +689,31 @@ lar_status launch_tile_mode(const DecodeParams& p, cudaStream_t stream) {
 }
 
 
-template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB = 1>
+// S1: ring stages of the single-token instance (K = 128 only; 0: no such
+// instance, single tokens take the general one).  The per-token-slot instance
+// stores every token's state, so it streams like a single-token call and
+// takes S1 stages too.
+template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB = 1, int S1 = 0>
 lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
     if constexpr (FORM != FORM_LA) {
-        if (p.tslot != nullptr) return launch_tile_mode<FORM, K, LPR, NR, NW, S, SB, MB, true>(p, stream);
+        if (p.tslot != nullptr)
+            return launch_tile_mode<FORM, K, LPR, NR, NW, (S1 > 0 ? S1 : S), SB, MB, true, 0>(p, stream);
     }
-    return launch_tile_mode<FORM, K, LPR, NR, NW, S, SB, MB, false>(p, stream);
+    if constexpr (S1 > 0) {
+        if (p.T == 1) return launch_tile_mode<FORM, K, LPR, NR, NW, S1, SB, MB, false, 1>(p, stream);
+    }
+    return launch_tile_mode<FORM, K, LPR, NR, NW, S, SB, MB, false, 0>(p, stream);
 }
 
 // Tile shapes per key size and pool type: a row is split over LPR lanes so each
 // lane holds whole 16-byte chunks (fp32 K = 128: 8 lanes x 4 chunks of 4
 // elements); 32-row tiles at K = 128, a 2-stage ring (one tile in flight while
-// one is computed) for fp32 and a 3-stage ring for bf16, whose tiles are half
-// the bytes.  Instances whose unconstrained register count would exceed 168
-// (fp32 KDA and LA) are compiled for 3 resident CTAs per SM.
+// one is computed) for single-token fp32, 3 stages for multi-token fp32 and
+// for bf16, whose tiles are half the bytes.  Instances whose unconstrained
+// register count would exceed 168 (fp32 KDA and LA) are compiled for 3
+// resident CTAs per SM.  At K = 128 single-token GDN / KDA calls (and bf16 LA)
+// take an instance with T fixed at 1; fp32 LA keeps one 2-stage instance for
+// every T (both the T = 1 instance and 3 stages measured slower for it).
 template <int FORM>
 lar_status launch_form(const DecodeParams& p, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -616,8 +723,12 @@ lar_status launch_form(const DecodeParams& p, void* stream) {
             case 32: return launch_tile<FORM, 32, 8, 2, 4, 3, 4>(p, st);
             case 64: return launch_tile<FORM, 64, 8, 2, 4, 3, 4>(p, st);
             case 128:
-                return launch_tile<FORM, 128, LAR_K128_LPR, LAR_K128_NR, LAR_K128_NW, LAR_K128_S, 4,
-                                   FORM == FORM_GDN ? 1 : LAR_K128_MIN_BLOCKS>(p, st);
+                if constexpr (FORM == FORM_LA)
+                    return launch_tile<FORM, 128, LAR_K128_LPR, LAR_K128_NR, LAR_K128_NW, LAR_K128_S, 4,
+                                       LAR_K128_MIN_BLOCKS>(p, st);
+                else
+                    return launch_tile<FORM, 128, LAR_K128_LPR, LAR_K128_NR, LAR_K128_NW, LAR_K128_S_MTP, 4,
+                                       FORM == FORM_GDN ? LAR_K128_GDN_MB : LAR_K128_MIN_BLOCKS, LAR_K128_S>(p, st);
             default: return LAR_ERR_SHAPE;
         }
     }
@@ -630,9 +741,11 @@ lar_status launch_form(const DecodeParams& p, void* stream) {
             // per row, one row per thread), which halves the per-row bookkeeping;
             // KDA keeps 8 lanes per row to stay within its register budget.
             if constexpr (FORM == FORM_KDA)
-                return launch_tile<FORM, 128, 8, 2, LAR_K128_NW, LAR_K128_BF16_S, 2, LAR_K128_MIN_BLOCKS>(p, st);
+                return launch_tile<FORM, 128, 8, 2, LAR_K128_NW, LAR_K128_BF16_S, 2, LAR_K128_MIN_BLOCKS,
+                                   LAR_K128_BF16_S>(p, st);
             else
-                return launch_tile<FORM, 128, 4, 1, LAR_K128_NW, LAR_K128_BF16_S, 2, 1>(p, st);
+                return launch_tile<FORM, 128, 4, LAR_K128_BF16_NR, LAR_K128_NW, LAR_K128_BF16_S, 2, LAR_K128_BF16_MB,
+                                   LAR_K128_BF16_S>(p, st);
         default: return LAR_ERR_SHAPE;
     }
 }

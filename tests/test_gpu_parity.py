@@ -61,6 +61,15 @@ SWEEP = {
     "kda_bf16_raw": ("kda", dict(B=4, T=2, H=2, HV=2, K=128, V=128, raw_gates=True,
                                  state_dtype=torch.bfloat16, cache_intermediate=True)),
     "kda_bf16_k32": ("kda", dict(B=3, T=1, H=2, HV=2, K=32, V=33, state_dtype=torch.bfloat16)),
+    # single-token K = 128 instances with ragged V, skipped and separate writes
+    "gdn_t1_ragged_skip": ("gdn", dict(B=5, T=1, H=2, HV=4, K=128, V=100, separate_write=True,
+                                       skip_frac=0.3)),
+    "kda_bf16_t1_ragged": ("kda", dict(B=4, T=1, H=2, HV=2, K=128, V=72, raw_gates=True,
+                                       state_dtype=torch.bfloat16, separate_write=True, skip_frac=0.3)),
+    "gdn_bf16_t1_ragged": ("gdn", dict(B=4, T=1, H=1, HV=3, K=128, V=100, state_dtype=torch.bfloat16,
+                                       stride_mult=2)),
+    "la_k128_t2_cache": ("la", dict(B=3, T=2, H=2, K=128, V=96, cache_intermediate=True,
+                                    separate_write=True, skip_frac=0.34)),
     "la_bf16_packed": ("la", dict(B=4, T=1, H=3, K=128, V=128, packed=True, flat_pool=True,
                                   state_dtype=torch.bfloat16)),
     "la_bf16_k16": ("la", dict(B=2, T=2, H=2, K=16, V=24, flat_pool=True, state_dtype=torch.bfloat16)),
@@ -255,10 +264,13 @@ def test_index_dtypes_agree(cuda_device):
     assert torch.equal(oa, ob) and torch.equal(pa, pb)
 
 
-def test_negative_and_out_of_range_slots(cuda_device):
+@pytest.mark.parametrize("form,T,state_dtype", [("gdn", 2, F32), ("gdn", 1, F32), ("gdn", 1, torch.bfloat16),
+                                                ("kda", 1, F32), ("kda", 1, torch.bfloat16)])
+def test_negative_and_out_of_range_slots(form, T, state_dtype, cuda_device):
     """read -1: zero initial state; write -1: no writeback; slots >= P: the
     same, plus the device error bits; every other byte untouched."""
-    w = W.make_custom("gdn", B=4, T=2, H=1, HV=2, K=128, V=64, P=6, seed=9)
+    w = W.make_custom(form, B=4, T=T, H=1, HV=2, K=128, V=64, P=6, seed=9, raw_gates=form == "kda",
+                      state_dtype=state_dtype)
     dev = cuda_device
     ri = torch.tensor([-1, 2, 6, 4], dtype=torch.int32)
     wi = torch.tensor([0, -1, 1, 9], dtype=torch.int32)
