@@ -38,14 +38,15 @@ __host__ __device__ constexpr size_t decode_kv_smem_bytes(int T, int V) {
            (2 * static_cast<size_t>(vec_floats<FORM, K>(T, V)) + kv_red_floats<FORM, K, NW, S>()) * sizeof(float);
 }
 
-template <int FORM, int K, int NW, int S, int SB, int MB>
+template <int FORM, int K, int NW, int S, int SB, int MB, int TT>
 __global__ void __launch_bounds__(NW * 32, MB)
 decode_kv_kernel(const DecodeParams p) {
     using G = KvTile<K, NW, SB>;
     constexpr int EPC = G::EPC, TVC = G::TVC, CL = G::CL, RL = G::RL, RG = G::RG, NRK = G::NRK;
+    constexpr int EP = EPC / 2;            // column pairs per chunk
 
     extern __shared__ __align__(16) unsigned char smem[];
-    const int T = p.T;
+    const int T = TT > 0 ? TT : p.T;
     const int V = p.V;
     const bool sv_on = stage_v(T, V);
     constexpr int STAGE = K * TVC * SB;                                   // one ring stage: [K][TVC]
@@ -60,6 +61,8 @@ decode_kv_kernel(const DecodeParams p) {
     const unsigned char* pool_b = static_cast<const unsigned char*>(p.pool);
     const bool inter_bf16 = p.inter_dt == LAR_BF16;
     const int inter_es = inter_bf16 ? 2 : 4;
+    const bool out_bf16 = p.out_dt == LAR_BF16;
+    const int out_es = out_bf16 ? 2 : 4;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -77,207 +80,244 @@ decode_kv_kernel(const DecodeParams p) {
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 #endif
+    if (t_begin >= t_end) return;
 
-    // byte offsets fixed for the kernel: rows are RG apart, chunks never move
+    // byte offsets fixed for the kernel: rows are RG apart, chunks never move;
+    // every address below is a per-pair base advanced by a fixed step per tile
     const int s_row0 = (rg * TVC + col0) * SB;
     constexpr int S_RSTEP = RG * TVC * SB;
     const int64_t g_row0 = (static_cast<int64_t>(rg) * p.ps[2] + col0) * SB;
     const int64_t g_rstep = static_cast<int64_t>(RG) * p.ps[2] * SB;
     constexpr int G_TILE = TVC * SB;
+    const int64_t o_cstep = p.os[3] * out_es;                 // between output columns
+    const int64_t o_tstep = p.os[1] * out_es;
+    const int64_t o_tile = static_cast<int64_t>(TVC) * p.os[3] * out_es;
+    const int64_t i_rstep = static_cast<int64_t>(RG) * p.is[3] * inter_es;
+    const int64_t i_tstep = p.is[1] * inter_es;
+    const int i_tile = TVC * inter_es;
 
-    struct Pos {
-        int64_t tile;
-        int vt, hv, b;
-    };
-    auto advance = [&](Pos& q) {
-        ++q.tile;
-        if (++q.vt == nvt) {
-            q.vt = 0;
-            if (++q.hv == p.HV) {
-                q.hv = 0;
-                ++q.b;
-            }
-        }
-    };
-    Pos cur;
+    // ---- issue cursor (see decode_kernel): running source pointer, read slot
+    // loaded one tile before the copies need it
+    const int64_t n_tiles = t_end - t_begin;
+    int64_t a_left = n_tiles;
+    int a_vt, a_hv, a_b;
     {
         const int64_t u = t_begin / nvt;
-        cur.tile = t_begin;
-        cur.vt = static_cast<int>(t_begin - u * nvt);
-        cur.b = static_cast<int>(u / p.HV);
-        cur.hv = static_cast<int>(u - static_cast<int64_t>(cur.b) * p.HV);
+        a_vt = static_cast<int>(t_begin - u * nvt);
+        a_b = static_cast<int>(u / p.HV);
+        a_hv = static_cast<int>(u - static_cast<int64_t>(a_b) * p.HV);
     }
-    int ahead_b = -1;
-    int64_t ahead_r = -1;
-    auto slot_of = [&](const Pos& q) -> int64_t {
-        if (q.tile >= t_end) return -1;
-        if (q.b != ahead_b) {
-            ahead_b = q.b;
-            ahead_r = ld_idx(p.ridx, q.b * p.ri_s, p.ri_dt);
-        }
-        return ahead_r;
-    };
-    auto issue = [&](const Pos& q, int64_t r, int st) {
-        if (q.tile < t_end && r >= 0 && r < p.P && q.vt * TVC + col0 < V) {
-            const unsigned char* src = pool_b + (r * p.ps[0] + static_cast<int64_t>(q.hv) * p.ps[1]) * SB +
-                                       q.vt * G_TILE + g_row0;
+    const int c_vt0 = a_vt, c_hv0 = a_hv, c_b0 = a_b;
+    int a_rb = a_b;
+    int64_t a_r = ld_idx(p.ridx, a_b * p.ri_s, p.ri_dt);
+    bool a_new = true, a_ok = false;
+    const unsigned char* a_src = pool_b;
+    // copies of the next tile into ring stage `st`; chunks with no state behind
+    // them (no valid read slot, columns past V) are zeroed in place
+    auto issue = [&](int st) {
+        if (a_left > 0) {
+            if (a_new) {
+                a_ok = a_r >= 0 && a_r < p.P;
+                a_src = pool_b + ((a_ok ? a_r : 0) * p.ps[0] + static_cast<int64_t>(a_hv) * p.ps[1]) * SB +
+                        a_vt * G_TILE + g_row0;
+                a_new = false;
+            }
             unsigned char* dst = ring + st * STAGE + s_row0;
+            const bool ok = a_ok && a_vt * TVC + col0 < V;
 #pragma unroll
-            for (int i = 0; i < NRK; ++i) cp_async16(dst + i * S_RSTEP, src + i * g_rstep);
+            for (int i = 0; i < NRK; ++i) {
+                if (ok) cp_async16(dst + i * S_RSTEP, a_src + i * g_rstep);
+                else st_shared_zero16(dst + i * S_RSTEP);
+            }
+            if (--a_left > 0) {
+                if (++a_vt == nvt) {
+                    a_vt = 0;
+                    if (++a_hv == p.HV) {
+                        a_hv = 0;
+                        ++a_b;
+                    }
+                    if (a_b != a_rb) {
+                        a_rb = a_b;
+                        a_r = ld_idx(p.ridx, a_b * p.ri_s, p.ri_dt);
+                    }
+                    a_new = true;
+                } else {
+                    a_src += G_TILE;
+                }
+            }
         }
         cp_async_commit();
     };
 
-    Pos ahead = cur;
 #pragma unroll
-    for (int s = 0; s < S - 1; ++s) {
-        issue(ahead, slot_of(ahead), s);
-        advance(ahead);
-    }
+    for (int s = 0; s < S - 1; ++s) issue(s);
 
+    int c_vt = c_vt0, c_hv = c_hv0, c_b = c_b0;
     int buf = 1;
     int rp = 0;                       // reduction buffer parity, alternates every token
-    bool rd = false, wr = false;
-    unsigned char* dst_state = nullptr;
-    int64_t v_off = 0, o_off = 0;
-    unsigned char* inter_base = nullptr;
+    bool wr = false;
+    unsigned char* wb = nullptr;      // this thread's first row chunk of the tile in the write slot
+    unsigned char* op = nullptr;      // output of the tile's first column of this thread, token 0
+    unsigned char* ip = nullptr;      // its first cached chunk, token 0
+    int64_t v_off = 0;
     const float scale = p.scale;
+    bool pair_start = true;
     int stage = 0;
     int stage_next = S - 1;
 #pragma unroll 1
-    for (; cur.tile < t_end; advance(cur)) {
-        const int64_t r_ahead = slot_of(ahead);
-        const int b = cur.b, hv = cur.hv, vt = cur.vt;
+    for (int64_t n = n_tiles; n > 0; --n) {
+        const int b = c_b, hv = c_hv, vt = c_vt;
         const bool cv = vt * TVC + col0 < V;   // this thread's column chunk exists
-        if (vt == 0 || cur.tile == t_begin) {
+        if (pair_start) {
+            pair_start = false;
             const int h = hv / p.group;
             buf ^= 1;
             const int64_t r = ld_idx(p.ridx, b * p.ri_s, p.ri_dt);
             const int64_t w = p.widx ? ld_idx(p.widx, b * p.wi_s, p.wi_dt) : r;
-            rd = r >= 0 && r < p.P;
             wr = w >= 0 && w < p.P;
             if (threadIdx.x == 0 && hv == 0 && p.dev_err) {
                 const int e = (r >= p.P ? LAR_DEVERR_READ_SLOT : 0) | (w >= p.P ? LAR_DEVERR_WRITE_SLOT : 0);
                 if (e) atomicOr(p.dev_err, e);
             }
-            dst_state = static_cast<unsigned char*>(p.pool) +
-                        ((wr ? w : 0) * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1]) * SB;
+            wb = static_cast<unsigned char*>(p.pool) +
+                 ((wr ? w : 0) * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1]) * SB + vt * G_TILE + g_row0;
+            const int64_t first_col = static_cast<int64_t>(vt) * TVC + col0;
             v_off = b * p.vs[0] + hv * p.vs[2];
-            o_off = b * p.os[0] + hv * p.os[2];
-            if (p.inter) inter_base = static_cast<unsigned char*>(p.inter) + (b * p.is[0] + hv * p.is[2]) * inter_es;
+            op = static_cast<unsigned char*>(p.out) + (b * p.os[0] + hv * p.os[2] + first_col * p.os[3]) * out_es;
+            if (p.inter)
+                ip = static_cast<unsigned char*>(p.inter) +
+                     (b * p.is[0] + hv * p.is[2] + static_cast<int64_t>(rg) * p.is[3] + first_col) * inter_es;
             build_pair_vectors<FORM, K, NW>(p, vecs + buf * vstride, b, hv, h, v_off, sv_on, o_k, o_d, o_v, o_s);
         }
 
         cp_async_wait<S - 2>();
-        float s[NRK][EPC];
+        float2 s[NRK][EP];          // columns 2e (.x) and 2e+1 (.y) of each own row
         {
             const unsigned char* src = ring + stage * STAGE + s_row0;
 #pragma unroll
-            for (int i = 0; i < NRK; ++i) {
-                if (rd && cv) {
-                    chunk_to_f32<SB>(src + i * S_RSTEP, s[i]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < EPC; ++e) s[i][e] = 0.f;
-                }
-            }
+            for (int i = 0; i < NRK; ++i) chunk_to_f2<SB>(src + i * S_RSTEP, s[i]);
         }
-        issue(ahead, r_ahead, stage_next);
-        advance(ahead);
+        issue(stage_next);
         stage = stage + 1 == S ? 0 : stage + 1;
         stage_next = stage_next + 1 == S ? 0 : stage_next + 1;
 
         const float* vb = vecs + buf * vstride;
         const float* sc = vb + o_s;
+        unsigned char* opt = op;
+        unsigned char* ipt = ip;
 #pragma unroll 1
-        for (int t = 0; t < T; ++t) {
+        for (int t = 0; t < T; ++t, opt += o_tstep, ipt += i_tstep) {
             const float bt = sc[t], dec = sc[T + t];
             const float iq = sc[2 * T + t], ik = sc[3 * T + t], kq = sc[4 * T + t];
-            float kr[NRK], qr[NRK];
+            float2 kr[NRK];   // k of each own row, in both halves
+            float2 u[EP], pq[EP];
+#pragma unroll
+            for (int e = 0; e < EP; ++e) u[e] = pq[e] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < NRK; ++i) {
-                const int kk = rg + i * RG;
-                kr[i] = vb[o_k + t * K + kk];
-                qr[i] = vb[t * K + kk];
-                const float d = FORM == FORM_KDA ? vb[o_d + t * K + kk] : dec;
+                const int kk = t * K + rg + i * RG;
+                const float ki = vb[o_k + kk], qi = vb[kk];
+                const float d = FORM == FORM_KDA ? vb[o_d + kk] : dec;
+                kr[i] = make_float2(ki, ki);
+                const float2 q2 = make_float2(qi, qi), d2 = make_float2(d, d);
 #pragma unroll
-                for (int e = 0; e < EPC; ++e) s[i][e] *= d;
+                for (int e = 0; e < EP; ++e) {
+                    s[i][e] = __fmul2_rn(s[i][e], d2);
+                    u[e] = __ffma2_rn(s[i][e], kr[i], u[e]);
+                    pq[e] = __ffma2_rn(s[i][e], q2, pq[e]);
+                }
             }
-            // sums over this thread's rows, then over the warp's row lanes
-            float u[EPC], pq[EPC];
+            // sums over this thread's rows are done; now over the warp's row lanes
 #pragma unroll
-            for (int e = 0; e < EPC; ++e) {
-                float a = 0.f, c = 0.f;
+            for (int off = CL; off < 32; off <<= 1) {
 #pragma unroll
-                for (int i = 0; i < NRK; ++i) {
-                    a = fmaf(s[i][e], kr[i], a);
-                    c = fmaf(s[i][e], qr[i], c);
+                for (int e = 0; e < EP; ++e) {
+                    u[e].x += __shfl_xor_sync(0xffffffffu, u[e].x, off);
+                    u[e].y += __shfl_xor_sync(0xffffffffu, u[e].y, off);
+                    pq[e].x += __shfl_xor_sync(0xffffffffu, pq[e].x, off);
+                    pq[e].y += __shfl_xor_sync(0xffffffffu, pq[e].y, off);
                 }
-#pragma unroll
-                for (int off = CL; off < 32; off <<= 1) {
-                    a += __shfl_xor_sync(0xffffffffu, a, off);
-                    c += __shfl_xor_sync(0xffffffffu, c, off);
-                }
-                u[e] = a;
-                pq[e] = c;
             }
             // then over the warps, through shared memory
             float* rb = red + rp * (NW * 2 * TVC);
             if (rl == 0) {
 #pragma unroll
-                for (int e = 0; e < EPC; ++e) {
-                    rb[(warp * 2 + 0) * TVC + col0 + e] = u[e];
-                    rb[(warp * 2 + 1) * TVC + col0 + e] = pq[e];
+                for (int e = 0; e < EP; ++e) {
+                    *reinterpret_cast<float2*>(rb + (warp * 2 + 0) * TVC + col0 + 2 * e) = u[e];
+                    *reinterpret_cast<float2*>(rb + (warp * 2 + 1) * TVC + col0 + 2 * e) = pq[e];
                 }
             }
             __syncthreads();
             rp ^= 1;
+            float2 coef[EP];
 #pragma unroll
-            for (int e = 0; e < EPC; ++e) {
-                float a = 0.f, c = 0.f;
+            for (int e = 0; e < EP; ++e) {
+                float2 a = make_float2(0.f, 0.f), c = a;
 #pragma unroll
                 for (int w2 = 0; w2 < NW; ++w2) {
-                    a += rb[(w2 * 2 + 0) * TVC + col0 + e];
-                    c += rb[(w2 * 2 + 1) * TVC + col0 + e];
+                    a = __fadd2_rn(a, *reinterpret_cast<const float2*>(rb + (w2 * 2 + 0) * TVC + col0 + 2 * e));
+                    c = __fadd2_rn(c, *reinterpret_cast<const float2*>(rb + (w2 * 2 + 1) * TVC + col0 + 2 * e));
                 }
-                const int col = vt * TVC + col0 + e;
-                float vval = 0.f;
-                if (cv) vval = sv_on ? vb[o_v + t * V + col] : ld_in(p.v, v_off + t * p.vs[1] + col * p.vs[3], p.v_dt);
-                float o, coef;
-                if constexpr (FORM == FORM_LA) {
-                    coef = vval * ik;
-                    o = fmaf(vval, kq, c * iq);
-                } else {
-                    const float delta = bt * (vval - a * ik);
-                    coef = delta * ik;
-                    o = fmaf(delta, kq, c * iq);
-                }
-                if (warp == 0 && rl == 0 && cv)
-                    st_out(p.out, o_off + t * p.os[1] + col * p.os[3], p.out_dt, o * scale);
+                float o[2], cf[2];
 #pragma unroll
-                for (int i = 0; i < NRK; ++i) s[i][e] = fmaf(coef, kr[i], s[i][e]);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const float ah = h2 ? a.y : a.x, ch = h2 ? c.y : c.x;
+                    const int col = vt * TVC + col0 + 2 * e + h2;
+                    float vval = 0.f;
+                    if (cv) vval = sv_on ? vb[o_v + t * V + col] : ld_in(p.v, v_off + t * p.vs[1] + col * p.vs[3], p.v_dt);
+                    if constexpr (FORM == FORM_LA) {
+                        cf[h2] = vval * ik;
+                        o[h2] = fmaf(vval, kq, ch * iq);
+                    } else {
+                        const float delta = bt * (vval - ah * ik);
+                        cf[h2] = delta * ik;
+                        o[h2] = fmaf(delta, kq, ch * iq);
+                    }
+                }
+                coef[e] = make_float2(cf[0], cf[1]);
+                if (warp == 0 && rl == 0 && cv) {
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        unsigned char* dst = opt + (2 * e + h2) * o_cstep;
+                        if (out_bf16) *reinterpret_cast<__nv_bfloat16*>(dst) = __float2bfloat16_rn(o[h2] * scale);
+                        else *reinterpret_cast<float*>(dst) = o[h2] * scale;
+                    }
+                }
             }
-            if (p.inter != nullptr && cv) {
-                unsigned char* ip = inter_base + (t * p.is[1] + static_cast<int64_t>(rg) * p.is[3] +
-                                                  vt * TVC + col0) * inter_es;
 #pragma unroll
-                for (int i = 0; i < NRK; ++i)
-                    store_run<EPC>(ip + static_cast<int64_t>(i) * RG * p.is[3] * inter_es, s[i], inter_bf16);
+            for (int i = 0; i < NRK; ++i)
+#pragma unroll
+                for (int e = 0; e < EP; ++e) s[i][e] = __ffma2_rn(kr[i], coef[e], s[i][e]);
+            if (p.inter != nullptr && cv) {
+#pragma unroll
+                for (int i = 0; i < NRK; ++i) store_pairs<EPC>(ipt + i * i_rstep, s[i], inter_bf16);
             }
         }
 
         if (wr && cv) {
-            unsigned char* wb = dst_state + vt * G_TILE + g_row0;
 #pragma unroll
-            for (int i = 0; i < NRK; ++i) store_run<EPC>(wb + i * g_rstep, s[i], SB == 2);
+            for (int i = 0; i < NRK; ++i) store_pairs<EPC>(wb + i * g_rstep, s[i], SB == 2);
+        }
+
+        if (++c_vt == nvt) {
+            c_vt = 0;
+            if (++c_hv == p.HV) {
+                c_hv = 0;
+                ++c_b;
+            }
+            pair_start = true;
+        } else {
+            wb += G_TILE;
+            op += o_tile;
+            ip += i_tile;
         }
     }
     cp_async_wait<0>();
 }
 
-template <int FORM, int K, int NW, int S, int SB, int MB = 1>
-lar_status launch_kv_tile(const DecodeParams& p, cudaStream_t stream) {
-    auto kern = decode_kv_kernel<FORM, K, NW, S, SB, MB>;
+template <int FORM, int K, int NW, int S, int SB, int MB, int TT>
+lar_status launch_kv_tile_mode(const DecodeParams& p, cudaStream_t stream) {
+    auto kern = decode_kv_kernel<FORM, K, NW, S, SB, MB, TT>;
     const size_t smem = decode_kv_smem_bytes<FORM, K, NW, S, SB>(p.T, p.V);
     constexpr size_t smem_max = decode_kv_smem_bytes<FORM, K, NW, S, SB>(16, kStageVMax / 16);
     int sms = 0;
@@ -305,6 +345,15 @@ lar_status launch_kv_tile(const DecodeParams& p, cudaStream_t stream) {
 #endif
 }
 
+// T1: compile a separate single-token instance (K = 128).
+template <int FORM, int K, int NW, int S, int SB, int MB = 1, bool T1 = false>
+lar_status launch_kv_tile(const DecodeParams& p, cudaStream_t stream) {
+    if constexpr (T1) {
+        if (p.T == 1) return launch_kv_tile_mode<FORM, K, NW, S, SB, MB, 1>(p, stream);
+    }
+    return launch_kv_tile_mode<FORM, K, NW, S, SB, MB, 0>(p, stream);
+}
+
 // K x V layout: 4 warps (2 for bf16 at K = 16, whose 32 row lanes would
 // otherwise exceed the 16 rows), 2-stage ring.
 template <int FORM>
@@ -316,7 +365,7 @@ lar_status launch_form_kv(const DecodeParams& p, void* stream) {
             case 16: return launch_kv_tile<FORM, 16, 4, 2, 4>(p, st);
             case 32: return launch_kv_tile<FORM, 32, 4, 2, 4>(p, st);
             case 64: return launch_kv_tile<FORM, 64, 4, 2, 4>(p, st);
-            case 128: return launch_kv_tile<FORM, 128, 4, 2, 4, MB>(p, st);
+            case 128: return launch_kv_tile<FORM, 128, 4, 2, 4, MB, true>(p, st);
             default: return LAR_ERR_SHAPE;
         }
     }
@@ -324,7 +373,7 @@ lar_status launch_form_kv(const DecodeParams& p, void* stream) {
         case 16: return launch_kv_tile<FORM, 16, 2, 2, 2>(p, st);
         case 32: return launch_kv_tile<FORM, 32, 4, 2, 2>(p, st);
         case 64: return launch_kv_tile<FORM, 64, 4, 2, 2>(p, st);
-        case 128: return launch_kv_tile<FORM, 128, 4, 2, 2, MB>(p, st);
+        case 128: return launch_kv_tile<FORM, 128, 4, 2, 2, MB, true>(p, st);
         default: return LAR_ERR_SHAPE;
     }
 }

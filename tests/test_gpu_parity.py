@@ -70,6 +70,15 @@ SWEEP = {
                                        stride_mult=2)),
     "la_k128_t2_cache": ("la", dict(B=3, T=2, H=2, K=128, V=96, cache_intermediate=True,
                                     separate_write=True, skip_frac=0.34)),
+    # more tiles than resident CTAs: every CTA streams several tiles across pair boundaries
+    "gdn_split_tiles": ("gdn", dict(B=48, T=1, H=2, HV=4, K=128, V=100, separate_write=True,
+                                    skip_frac=0.25)),
+    "gdn_bf16_split_tiles": ("gdn", dict(B=48, T=1, H=2, HV=4, K=128, V=128, P=60,
+                                         state_dtype=torch.bfloat16)),
+    "gdn_split_mtp_cache": ("gdn", dict(B=40, T=4, H=2, HV=4, K=128, V=112, cache_intermediate=True,
+                                        separate_write=True, skip_frac=0.25, stride_mult=2)),
+    "kda_split_tiles": ("kda", dict(B=40, T=2, H=4, HV=4, K=128, V=128, raw_gates=True)),
+    "la_split_tiles": ("la", dict(B=64, T=1, H=4, K=128, V=128, flat_pool=True)),
     "la_bf16_packed": ("la", dict(B=4, T=1, H=3, K=128, V=128, packed=True, flat_pool=True,
                                   state_dtype=torch.bfloat16)),
     "la_bf16_k16": ("la", dict(B=2, T=2, H=2, K=16, V=24, flat_pool=True, state_dtype=torch.bfloat16)),
