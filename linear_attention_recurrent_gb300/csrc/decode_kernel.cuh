@@ -67,10 +67,9 @@
 #ifndef LAR_K128_S
 #define LAR_K128_S 2
 #endif
-// ring stages of the fp32 K = 128 multi-token instances (a tile's compute
-// grows with T, so one more tile stays in flight)
+// ring stages of the fp32 K = 128 multi-token instances
 #ifndef LAR_K128_S_MTP
-#define LAR_K128_S_MTP 3
+#define LAR_K128_S_MTP LAR_K128_S
 #endif
 #ifndef LAR_K128_BF16_NR
 #define LAR_K128_BF16_NR 1
@@ -229,11 +228,11 @@ __host__ __device__ constexpr size_t decode_smem_bytes(int T, int V) {
 // the KDA decay rows exp(g) (gate chain included), the pair's v values when
 // staged, and per token beta, the scalar decay, 1/|q|, 1/|k| and
 // q.k / (|q| |k|).  All threads of the CTA take part; ends with a barrier.
-template <int FORM, int K, int NW>
+template <int FORM, int K, int NW, int TT>
 __device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float* vb, int b, int hv, int h,
                                                    int64_t v_off, bool sv_on, int o_k, int o_d, int o_v,
                                                    int o_s) {
-    const int T = p.T;
+    const int T = TT > 0 ? TT : p.T;
     const int V = p.V;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -241,6 +240,7 @@ __device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float*
     const bool l2 = FORM != FORM_LA && (p.flags & LAR_QK_L2NORM) != 0;
     const int64_t q_off = b * p.qs[0] + h * p.qs[2];
     const int64_t k_off = b * p.ks[0] + h * p.ks[2];
+#pragma unroll 4
     for (int i = threadIdx.x; i < T * K; i += NW * 32) {
         const int t = i / K;
         const int c = i - t * K;
@@ -257,9 +257,11 @@ __device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float*
         }
     }
     if (sv_on) {
-        for (int t = 0; t < T; ++t)
-            for (int row = threadIdx.x; row < V; row += NW * 32)
-                vb[o_v + t * V + row] = ld_in(p.v, v_off + t * p.vs[1] + row * p.vs[3], p.v_dt);
+        // tokens innermost and unrolled, so one thread's loads are in flight together
+        for (int row = threadIdx.x; row < V; row += NW * 32) {
+#pragma unroll 4
+            for (int t = 0; t < T; ++t) vb[o_v + t * V + row] = ld_in(p.v, v_off + t * p.vs[1] + row * p.vs[3], p.v_dt);
+        }
     }
     float* sc = vb + o_s;
     for (int t = threadIdx.x; t < T; t += NW * 32) {
@@ -497,7 +499,7 @@ decode_kernel(const DecodeParams p) {
                 ip = static_cast<unsigned char*>(p.inter) +
                      (b * p.is[0] + hv * p.is[2] + first_row * p.is[3] + j * EPC) * inter_es;
 
-            build_pair_vectors<FORM, K, NW>(p, vecs + buf * vstride, b, hv, h, v_off, sv_on, o_k, o_d, o_v, o_s);
+            build_pair_vectors<FORM, K, NW, TT>(p, vecs + buf * vstride, b, hv, h, v_off, sv_on, o_k, o_d, o_v, o_s);
         }
 
         // ---- this thread's copies of the tile have landed: pull its rows into registers
@@ -708,8 +710,8 @@ lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
 // Tile shapes per key size and pool type: a row is split over LPR lanes so each
 // lane holds whole 16-byte chunks (fp32 K = 128: 8 lanes x 4 chunks of 4
 // elements); 32-row tiles at K = 128, a 2-stage ring (one tile in flight while
-// one is computed) for single-token fp32, 3 stages for multi-token fp32 and
-// for bf16, whose tiles are half the bytes.  Instances whose unconstrained
+// one is computed) for fp32 and 3 stages for bf16, whose tiles are half the
+// bytes.  Instances whose unconstrained
 // register count would exceed 168 (fp32 KDA and LA) are compiled for 3
 // resident CTAs per SM.  At K = 128 single-token GDN / KDA calls (and bf16 LA)
 // take an instance with T fixed at 1; fp32 LA keeps one 2-stage instance for

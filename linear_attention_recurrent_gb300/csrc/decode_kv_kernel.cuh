@@ -187,7 +187,7 @@ decode_kv_kernel(const DecodeParams p) {
             if (p.inter)
                 ip = static_cast<unsigned char*>(p.inter) +
                      (b * p.is[0] + hv * p.is[2] + static_cast<int64_t>(rg) * p.is[3] + first_col) * inter_es;
-            build_pair_vectors<FORM, K, NW>(p, vecs + buf * vstride, b, hv, h, v_off, sv_on, o_k, o_d, o_v, o_s);
+            build_pair_vectors<FORM, K, NW, TT>(p, vecs + buf * vstride, b, hv, h, v_off, sv_on, o_k, o_d, o_v, o_s);
         }
 
         cp_async_wait<S - 2>();
