@@ -70,6 +70,12 @@ SWEEP = {
                                        stride_mult=2)),
     "la_k128_t2_cache": ("la", dict(B=3, T=2, H=2, K=128, V=96, cache_intermediate=True,
                                     separate_write=True, skip_frac=0.34)),
+    # multi-token GDN without a cache, raw gates, odd token counts
+    "gdn_t6_nocache": ("gdn", dict(B=3, T=6, H=2, HV=4, K=128, V=96, separate_write=True, skip_frac=0.34)),
+    "gdn_t16_nocache_raw": ("gdn", dict(B=2, T=16, H=1, HV=2, K=64, V=64, raw_gates=True)),
+    "gdn_bf16_t5_nocache": ("gdn", dict(B=3, T=5, H=1, HV=3, K=128, V=128, state_dtype=torch.bfloat16)),
+    "gdn_t7_cache_k32": ("gdn", dict(B=2, T=7, H=2, HV=2, K=32, V=40, cache_intermediate=True,
+                                     in_dtype=F32, out_dtype=F32)),
     # more tiles than resident CTAs: every CTA streams several tiles across pair boundaries
     "gdn_split_tiles": ("gdn", dict(B=48, T=1, H=2, HV=4, K=128, V=100, separate_write=True,
                                     skip_frac=0.25)),
