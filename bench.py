@@ -5,6 +5,7 @@ q/k/v/out, fp32 pool [256,32,128,128]).  A step is one decode call over the
 batch.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl lar|reference]
+  python bench.py --sweep      # batch / token curve, one JSON line per point
 
 Timing: W untimed steps, then K steps bracketed by barrier + synchronize and
 by one CUDA event pair on the launching stream (the decode kernel is the only
@@ -473,6 +474,62 @@ def run_reference(args, world, rank):
                     "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------------------------ sweep
+
+SWEEP_POINTS = (
+    [("gdn", B, 1) for B in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024)]
+    + [("gdn", 64, T) for T in (2, 4, 8)]
+    + [("kda", B, 1) for B in (16, 64, 256, 1024)]
+    + [("la", B, 1) for B in (16, 64, 512)]
+)
+SWEEP_HEADS = {"gdn": (16, 32), "kda": (24, 24), "la": (64, 64)}
+
+
+def run_sweep(args):
+    """GB/s and tokens/s over batch size and token count at K = V = 128 (the
+    gdn_b64 / kda_b256 / la_b512 head shapes, no state cache), one JSON line per
+    point.  Each point rotates over disjoint slot sets (4 when the pool holds
+    them) and times back-to-back launches with one CUDA event pair."""
+    import linear_attention_recurrent_gb300 as lar
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lar.load()
+    peak, _ = hbm_peak()
+    for form, B, T in SWEEP_POINTS:
+        H, HV = SWEEP_HEADS[form]
+        w = W.make_custom(form, B=B, T=T, H=H, HV=HV, K=128, V=128, P=4 * B, seed=1, pool_device=dev,
+                          raw_gates=form == "kda", flat_pool=form == "la")
+        d = device_inputs(w, dev)
+        sets, n_sets = index_sets(w)
+        stream = torch.cuda.Stream(device=dev)
+        calls = []
+        for ri, wi in sets:
+            out = torch.empty(w.v.shape, dtype=w.out_dtype, device=dev)
+            kw = dict(d, read_idx=ri.to(dev), write_idx=wi.to(dev), out=out)
+            if form != "la":
+                kw.update(qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw)
+            calls.append(lar.PreparedCall(form, scale=w.scale, stream=stream, **kw))
+        for i in range(max(args.warmup, 20)):
+            calls[i % n_sets]()
+        torch.cuda.synchronize(dev)
+        launches = max(20, min(5000, int(60e9 / w.algorithmic_bytes())))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(launches):
+                calls[i % n_sets]()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) / launches * 1e3
+        gbs = w.algorithmic_bytes() / us / 1e3
+        print(json.dumps({"sweep": form, "B": B, "T": T, "H": H, "HV": HV, "us": round(us, 2),
+                          "GBs": round(gbs, 1), "pct_of_measured_peak": round(100 * gbs / peak, 1),
+                          "tokens_per_s": round(B * T / us * 1e6), "launches": launches}), flush=True)
+        del w, d, calls
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -481,9 +538,16 @@ def main(argv=None):
     ap.add_argument("--config", default="gdn_b64", choices=W.CONFIGS)
     ap.add_argument("--impl", default="lar", choices=["lar", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="print one line per (form, B, T) point of the batch / token sweep instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.sweep:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback exists)")
+        run_sweep(args)
+        return
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         line = run_reference(args, world, rank)
