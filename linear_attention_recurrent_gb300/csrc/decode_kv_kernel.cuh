@@ -13,6 +13,17 @@
 
 #include "decode_kernel.cuh"
 
+// K = 128 tile: warps per CTA (row groups of the reduction), ring stages
+#ifndef LAR_KV_NW
+#define LAR_KV_NW 4
+#endif
+#ifndef LAR_KV_S
+#define LAR_KV_S 2
+#endif
+#ifndef LAR_KV_MB
+#define LAR_KV_MB LAR_K128_MIN_BLOCKS
+#endif
+
 namespace lar {
 
 template <int K, int NW, int SB>
@@ -355,17 +366,17 @@ lar_status launch_kv_tile(const DecodeParams& p, cudaStream_t stream) {
 }
 
 // K x V layout: 4 warps (2 for bf16 at K = 16, whose 32 row lanes would
-// otherwise exceed the 16 rows), 2-stage ring.
+// otherwise exceed the 16 rows), 2-stage ring.  At K = 128, 2 or 8 warps and a
+// 3-stage ring measured slower (gdn_b64_kv: 5745 / 4657 / 5516 against 5753 GB/s).
 template <int FORM>
 lar_status launch_form_kv(const DecodeParams& p, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    constexpr int MB = LAR_K128_MIN_BLOCKS;
     if (p.pool_dt == LAR_F32) {
         switch (p.K) {
             case 16: return launch_kv_tile<FORM, 16, 4, 2, 4>(p, st);
             case 32: return launch_kv_tile<FORM, 32, 4, 2, 4>(p, st);
             case 64: return launch_kv_tile<FORM, 64, 4, 2, 4>(p, st);
-            case 128: return launch_kv_tile<FORM, 128, 4, 2, 4, MB, true>(p, st);
+            case 128: return launch_kv_tile<FORM, 128, LAR_KV_NW, LAR_KV_S, 4, LAR_KV_MB, true>(p, st);
             default: return LAR_ERR_SHAPE;
         }
     }
@@ -373,7 +384,7 @@ lar_status launch_form_kv(const DecodeParams& p, void* stream) {
         case 16: return launch_kv_tile<FORM, 16, 2, 2, 2>(p, st);
         case 32: return launch_kv_tile<FORM, 32, 4, 2, 2>(p, st);
         case 64: return launch_kv_tile<FORM, 64, 4, 2, 2>(p, st);
-        case 128: return launch_kv_tile<FORM, 128, 4, 2, 2, MB, true>(p, st);
+        case 128: return launch_kv_tile<FORM, 128, LAR_KV_NW, LAR_KV_S, 2, LAR_KV_MB, true>(p, st);
         default: return LAR_ERR_SHAPE;
     }
 }
