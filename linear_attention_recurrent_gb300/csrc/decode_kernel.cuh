@@ -530,7 +530,8 @@ decode_kernel(const DecodeParams p) {
 
         // ---- token loop: the state never leaves registers between tokens.  The
         // arithmetic runs on element pairs (packed fp32x2 multiply / fma); each
-        // reduction keeps two pair accumulators, summed before the shuffles.
+        // reduction keeps one pair accumulator (even and odd elements), summed
+        // before the shuffles.
         const float* vb = vecs + buf * vstride;
         const float* sc = vb + o_s;
         constexpr int KP = KPL / 2;   // element pairs per lane and row
@@ -568,20 +569,20 @@ decode_kernel(const DecodeParams p) {
             for (int i = 0; i < NR; ++i) {
                 const bool rv = i * RPW < rl;
                 const int row = vt * TV + row0 + i * RPW;
+                // rows past V compute on zeros and store nothing; their staged-v read is
+                // clamped into the row range instead of branched around
                 float vval = 0.f;
-                if (rv) vval = sv_on ? vb[o_v + t * V + row] : ld_in(p.v, v_off + t * p.vs[1] + row * p.vs[3], p.v_dt);
+                if (sv_on) vval = vb[o_v + t * V + min(row, V - 1)];
+                else if (rv) vval = ld_in(p.v, v_off + t * p.vs[1] + row * p.vs[3], p.v_dt);
 #pragma unroll
                 for (int e = 0; e < KP; ++e) s[i][e] = __fmul2_rn(s[i][e], FORM == FORM_KDA ? dv[e] : dec2);
                 // q_hat = iq q and k_hat = ik k: the norms scale the reduced sums
                 float o;
                 if constexpr (FORM == FORM_LA) {
-                    float2 p0 = make_float2(0.f, 0.f), p1 = p0;
+                    float2 p2 = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int e = 0; e < KP; e += 2) {
-                        p0 = __ffma2_rn(s[i][e], qv[e], p0);
-                        if (e + 1 < KP) p1 = __ffma2_rn(s[i][e + 1], qv[e + 1], p1);
-                    }
-                    float pp = (p0.x + p1.x) + (p0.y + p1.y);
+                    for (int e = 0; e < KP; ++e) p2 = __ffma2_rn(s[i][e], qv[e], p2);
+                    float pp = p2.x + p2.y;
 #pragma unroll
                     for (int off = LPR / 2; off > 0; off >>= 1) pp += __shfl_xor_sync(0xffffffffu, pp, off);
                     const float a = vval * ik;
@@ -590,18 +591,14 @@ decode_kernel(const DecodeParams p) {
                     for (int e = 0; e < KP; ++e) s[i][e] = __ffma2_rn(a2, kv[e], s[i][e]);
                     o = fmaf(vval, kq, pp * iq);
                 } else {
-                    float2 u0 = make_float2(0.f, 0.f), u1 = u0, p0 = u0, p1 = u0;
+                    float2 u2 = make_float2(0.f, 0.f), p2 = u2;
 #pragma unroll
-                    for (int e = 0; e < KP; e += 2) {
-                        u0 = __ffma2_rn(s[i][e], kv[e], u0);
-                        p0 = __ffma2_rn(s[i][e], qv[e], p0);
-                        if (e + 1 < KP) {
-                            u1 = __ffma2_rn(s[i][e + 1], kv[e + 1], u1);
-                            p1 = __ffma2_rn(s[i][e + 1], qv[e + 1], p1);
-                        }
+                    for (int e = 0; e < KP; ++e) {
+                        u2 = __ffma2_rn(s[i][e], kv[e], u2);
+                        p2 = __ffma2_rn(s[i][e], qv[e], p2);
                     }
-                    float uu = (u0.x + u1.x) + (u0.y + u1.y);
-                    float pp = (p0.x + p1.x) + (p0.y + p1.y);
+                    float uu = u2.x + u2.y;
+                    float pp = p2.x + p2.y;
 #pragma unroll
                     for (int off = LPR / 2; off > 0; off >>= 1) {
                         uu += __shfl_xor_sync(0xffffffffu, uu, off);
