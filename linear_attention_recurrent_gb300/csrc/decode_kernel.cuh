@@ -218,12 +218,21 @@ constexpr int kStageVMax = 4096;
 
 __host__ __device__ constexpr bool stage_v(int T, int V) { return T * V <= kStageVMax; }
 
-// Floats of one per-pair vector buffer: q, k (and the KDA decay rows) for T
-// tokens, the staged v values, and 5 scalars per token; a multiple of 4 so
-// the second buffer stays 16-byte aligned.
+// Per-token scalars of a pair, kScal floats per token (16-byte aligned):
+// beta, decay, 1/|q|, 1/|k|, q.k / (|q| |k|), 3 unused.
+constexpr int kScal = 8;
+
+// Offset of the scalars in a vector buffer: after q, k (and the KDA decay
+// rows) and the staged v values, rounded up to 16 bytes.
+__host__ __device__ constexpr int scal_offset(int form, int K, int T, int V) {
+    return ((form == FORM_KDA ? 3 : 2) * T * K + (stage_v(T, V) ? T * V : 0) + 3) & ~3;
+}
+
+// Floats of one per-pair vector buffer; a multiple of 4 so the second buffer
+// stays 16-byte aligned.
 template <int FORM, int K>
 __host__ __device__ constexpr int vec_floats(int T, int V) {
-    return ((FORM == FORM_KDA ? 3 : 2) * T * K + (stage_v(T, V) ? T * V : 0) + 5 * T + 3) & ~3;
+    return scal_offset(FORM, K, T, V) + kScal * T;
 }
 
 template <int FORM, int K, int LPR, int NR, int NW, int S, int SB>
@@ -235,8 +244,8 @@ __host__ __device__ constexpr size_t decode_smem_bytes(int T, int V) {
 
 // Per-(b, hv) vectors into the buffer vb: the raw q and k rows of all T tokens,
 // the KDA decay rows exp(g) (gate chain included), the pair's v values when
-// staged, and per token beta, the scalar decay, 1/|q|, 1/|k| and
-// q.k / (|q| |k|).  All threads of the CTA take part; ends with a barrier.
+// staged, and per token (kScal floats each) beta, the scalar decay, 1/|q|,
+// 1/|k| and q.k / (|q| |k|).  All threads of the CTA take part; ends with a barrier.
 template <int FORM, int K, int NW, int TT>
 __device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float* vb, int b, int hv, int h,
                                                    int64_t v_off, bool sv_on, int o_k, int o_d, int o_v,
@@ -289,8 +298,8 @@ __device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float*
         } else if constexpr (FORM == FORM_LA) {
             dec = p.decay[h * p.dec_s];
         }
-        sc[t] = bt;
-        sc[T + t] = dec;
+        sc[kScal * t] = bt;
+        sc[kScal * t + 1] = dec;
     }
     __syncthreads();
     for (int t = warp; t < T; t += NW) {
@@ -310,9 +319,9 @@ __device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float*
         if (lane == 0) {
             const float iq = l2 ? 1.f / sqrtf(qq + 1e-6f) : 1.f;
             const float ik = l2 ? 1.f / sqrtf(kk + 1e-6f) : 1.f;
-            sc[2 * T + t] = iq;
-            sc[3 * T + t] = ik;
-            sc[4 * T + t] = kq * iq * ik;
+            sc[kScal * t + 2] = iq;
+            sc[kScal * t + 3] = ik;
+            sc[kScal * t + 4] = kq * iq * ik;
         }
     }
     __syncthreads();}
@@ -344,7 +353,7 @@ decode_kernel(const DecodeParams p) {
     const int o_k = T * K;
     const int o_d = 2 * T * K;
     const int o_v = (FORM == FORM_KDA ? 3 : 2) * T * K;
-    const int o_s = o_v + (sv_on ? T * V : 0);                  // beta, decay, 1/|q|, 1/|k|, q.k/(|q||k|)
+    const int o_s = scal_offset(FORM, K, T, V);        // per-token scalars
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -539,8 +548,8 @@ decode_kernel(const DecodeParams p) {
         unsigned char* ipt = ip;
 #pragma unroll 1
         for (int t = 0; t < T; ++t, opt += o_tstep, ipt += i_tstep) {
-            const float bt = sc[t], dec = sc[T + t];
-            const float iq = sc[2 * T + t], ik = sc[3 * T + t], kq = sc[4 * T + t];
+            const float4 s4 = *reinterpret_cast<const float4*>(sc + kScal * t);
+            const float bt = s4.x, dec = s4.y, iq = s4.z, ik = s4.w, kq = sc[kScal * t + 4];
             float2 kv[KP], qv[KP], dv[KP];
             const float* qrow = vb + t * K + j * EPC;
 #pragma unroll

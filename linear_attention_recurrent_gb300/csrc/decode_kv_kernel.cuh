@@ -68,7 +68,7 @@ decode_kv_kernel(const DecodeParams p) {
     const int o_k = T * K;
     const int o_d = 2 * T * K;
     const int o_v = (FORM == FORM_KDA ? 3 : 2) * T * K;
-    const int o_s = o_v + (sv_on ? T * V : 0);
+    const int o_s = scal_offset(FORM, K, T, V);
     const unsigned char* pool_b = static_cast<const unsigned char*>(p.pool);
     const bool inter_bf16 = p.inter_dt == LAR_BF16;
     const int inter_es = inter_bf16 ? 2 : 4;
@@ -218,8 +218,8 @@ decode_kv_kernel(const DecodeParams p) {
         unsigned char* ipt = ip;
 #pragma unroll 1
         for (int t = 0; t < T; ++t, opt += o_tstep, ipt += i_tstep) {
-            const float bt = sc[t], dec = sc[T + t];
-            const float iq = sc[2 * T + t], ik = sc[3 * T + t], kq = sc[4 * T + t];
+            const float4 s4 = *reinterpret_cast<const float4*>(sc + kScal * t);
+            const float bt = s4.x, dec = s4.y, iq = s4.z, ik = s4.w, kq = sc[kScal * t + 4];
             float2 kr[NRK];   // k of each own row, in both halves
             float2 u[EP], pq[EP];
 #pragma unroll
