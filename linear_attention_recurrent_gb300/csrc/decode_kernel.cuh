@@ -2,7 +2,7 @@
 //
 // Work decomposition.  A tile is TV consecutive state rows of one
 // (batch entry b, v-head hv) pair; a state row is one value channel v with its
-// K key channels (K fp32, contiguous in the pool).  Tiles are numbered with
+// K key channels (K fp32 or bf16 values, contiguous in the pool).  Tiles are numbered with
 // the V-tile fastest, then hv, then b, and a persistent grid of
 // (SM count x resident CTAs per SM) CTAs takes contiguous, equal ranges of
 // them.  The grid is sized from the active batch B*HV, never from the pool.
@@ -365,13 +365,6 @@ decode_kernel(const DecodeParams p) {
     const int64_t t_begin = blockIdx.x * total / gridDim.x;
     const int64_t t_end = (blockIdx.x + 1) * total / gridDim.x;
 
-#if LAR_PDL
-    // programmatic dependent launch: everything below may read what the
-    // previous kernel on the stream wrote, so wait for it first; then let the
-    // next kernel's CTAs be scheduled as soon as ours retire.
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-#endif
     if (t_begin >= t_end) return;
 
     // A thread's rows in a tile are row0, row0 + RPW, ... and its chunks in a
@@ -416,6 +409,16 @@ decode_kernel(const DecodeParams p) {
         a_hv = static_cast<int>(u - static_cast<int64_t>(a_b) * p.HV);
     }
     const int c_vt0 = a_vt, c_hv0 = a_hv, c_b0 = a_b;   // the consumer starts where the issuer does
+
+#if LAR_PDL
+    // Programmatic dependent launch.  Everything above is arithmetic on the
+    // launch parameters and overlaps the previous kernel's tail; everything
+    // below may read what the previous kernel on the stream wrote, so wait for
+    // it here.  Then let the next kernel's CTAs be scheduled as soon as ours
+    // retire.
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+#endif
     int a_rb = a_b;                  // batch entry whose read slot a_r holds
     int64_t a_r = seed_of(a_b);
     bool a_new = true;               // a_src must be rebuilt from a_r before the next issue

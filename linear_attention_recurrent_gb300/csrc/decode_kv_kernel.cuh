@@ -87,10 +87,6 @@ decode_kv_kernel(const DecodeParams p) {
     const int64_t t_begin = blockIdx.x * total / gridDim.x;
     const int64_t t_end = (blockIdx.x + 1) * total / gridDim.x;
 
-#if LAR_PDL
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-#endif
     if (t_begin >= t_end) return;
 
     // byte offsets fixed for the kernel: rows are RG apart, chunks never move;
@@ -119,6 +115,11 @@ decode_kv_kernel(const DecodeParams p) {
         a_hv = static_cast<int>(u - static_cast<int64_t>(a_b) * p.HV);
     }
     const int c_vt0 = a_vt, c_hv0 = a_hv, c_b0 = a_b;
+#if LAR_PDL
+    // as in decode_kernel: arithmetic above, the first global read below
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+#endif
     int a_rb = a_b;
     int64_t a_r = ld_idx(p.ridx, a_b * p.ri_s, p.ri_dt);
     bool a_new = true, a_ok = false;
