@@ -102,6 +102,10 @@ SWEEP = {
                                cache_intermediate=True)),
     "gdn_kv_bf16": ("gdn", dict(B=4, T=2, H=2, HV=4, K=128, V=128, state_kv=True,
                                 state_dtype=torch.bfloat16, cache_intermediate=True)),
+    "gdn_kv_bf16_t1_ragged": ("gdn", dict(B=5, T=1, H=2, HV=4, K=128, V=96, state_kv=True,
+                                          state_dtype=torch.bfloat16, separate_write=True, skip_frac=0.2)),
+    "kda_kv_bf16_t1": ("kda", dict(B=3, T=1, H=2, HV=2, K=128, V=128, state_kv=True, raw_gates=True,
+                                   state_dtype=torch.bfloat16)),
     "kda_kv_bf16_k16": ("kda", dict(B=3, T=1, H=1, HV=2, K=16, V=24, state_kv=True,
                                     state_dtype=torch.bfloat16)),
     "gdn_kv_unstaged_v": ("gdn", dict(B=2, T=16, H=1, HV=1, K=64, V=320, state_kv=True)),
