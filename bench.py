@@ -52,6 +52,11 @@ DESCRIPTIONS = {
     "gdn_mtp_strided": "GDN MTP B=16 T=4 H=16 HV=32 K=V=128, pool = backing[::2] of [256,32,128,128], "
                        "separate write slots (25% -1), all T states cached",
     "kda_b256": "KDA decode B=256 T=1 H=HV=24 K=V=128, in-kernel gate/l2norm/sigmoid, pool [320,24,128,128]",
+    "kda_b256_bf16": "KDA decode B=256 T=1 H=HV=24 K=V=128, in-kernel gate/l2norm/sigmoid, bf16 pool [320,24,128,128]",
+    "la_b512_bf16": "Lightning-Attention decode B=512 T=1 H=64 K=V=128, packed bf16 QKV, "
+                    "bf16 flat pool [640*64,128,128]",
+    "gdn_b64_kv_bf16": "GDN decode B=64 T=1 H=16 HV=32 K=V=128, bf16 q/k/v/out, bf16 pool "
+                       "[256,32,128(k),128(v)] (state stored untransposed)",
     "la_b512_packed": "Lightning-Attention decode B=512 T=1 H=64 K=V=128, packed bf16 QKV, "
                       "flat pool [640*64,128,128]",
 }

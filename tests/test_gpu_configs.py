@@ -16,7 +16,8 @@ def _sample(B, seed=0, n=6):
 
 
 @pytest.mark.parametrize("name", ["gdn_b64", "gdn_mtp_strided", "kda_b256", "la_b512_packed",
-                                  "gdn_b64_bf16", "gdn_b64_kv"])
+                                  "gdn_b64_bf16", "gdn_b64_kv", "gdn_b64_kv_bf16", "kda_b256_bf16",
+                                  "la_b512_bf16"])
 def test_full_size(name, cuda_device):
     dev = cuda_device
     w = W.make(name, pool_device=dev)

@@ -33,6 +33,9 @@ la_b512_packed     B=512 T=1 H=64, q/k/v head-dim slices of one fused bf16
                    [B,H,384] buffer (q, k ~ N(0,1)/sqrt(128), v ~ N(0,1)),
                    lambda_h = exp(-2^(-8(h+1)/64)), flat pool [640*64,128,128];
                    read = write = randperm(640)[:512]; seed 5
+gdn_b64_kv_bf16    gdn_b64_kv with a bfloat16 state pool
+kda_b256_bf16      kda_b256 with a bfloat16 state pool
+la_b512_bf16       la_b512_packed with a bfloat16 state pool
 =================  ===========================================================
 
 Pool entries are N(0, 0.1^2) (standard deviation 0.1).  Full-size pools are
@@ -52,9 +55,11 @@ BF16 = torch.bfloat16
 F32 = torch.float32
 
 CONFIGS = ("gdn_tiny", "gdn_b64", "gdn_mtp_strided", "kda_b256", "la_b512_packed",
-           "gdn_b64_bf16", "gdn_spec_b64", "gdn_b64_kv")
+           "gdn_b64_bf16", "gdn_spec_b64", "gdn_b64_kv", "gdn_b64_kv_bf16", "kda_b256_bf16",
+           "la_b512_bf16")
 SEEDS = {"gdn_tiny": 0, "gdn_b64": 2, "gdn_mtp_strided": 3, "kda_b256": 4,
-         "la_b512_packed": 5, "gdn_b64_bf16": 2, "gdn_spec_b64": 6, "gdn_b64_kv": 2}
+         "la_b512_packed": 5, "gdn_b64_bf16": 2, "gdn_spec_b64": 6, "gdn_b64_kv": 2,
+         "gdn_b64_kv_bf16": 2, "kda_b256_bf16": 4, "la_b512_bf16": 5}
 
 
 @dataclass
@@ -168,7 +173,7 @@ def make(name: str, *, seed: int | None = None, pool_device="cpu",
         pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
         return Workload(name, "gdn", B, T, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
                         F32, g=g, beta=beta)
-    if name in ("gdn_b64", "gdn_b64_bf16", "gdn_b64_kv"):
+    if name in ("gdn_b64", "gdn_b64_bf16", "gdn_b64_kv", "gdn_b64_kv_bf16"):
         B, T, H, HV, K, V, P = 64, 1, 16, 32, 128, 128, 256
         q = _l2n(_normal(gen, (B, T, H, K))).to(BF16)
         k = _l2n(_normal(gen, (B, T, H, K))).to(BF16)
@@ -176,9 +181,9 @@ def make(name: str, *, seed: int | None = None, pool_device="cpu",
         g = -F.softplus(_normal(gen, (B, T, HV)))
         beta = torch.sigmoid(_normal(gen, (B, T, HV)))
         ri = torch.randperm(P, generator=gen)[:B].to(index_dtype)
-        kv = name == "gdn_b64_kv"
+        kv = name.startswith("gdn_b64_kv")
         pool = _draw_pool(gen, (P, HV, K, V) if kv else (P, HV, V, K), s, pool_device,
-                          BF16 if name == "gdn_b64_bf16" else F32)
+                          BF16 if name.endswith("_bf16") else F32)
         return Workload(name, "gdn", B, T, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
                         BF16, g=g, beta=beta, state_kv=kv)
     if name == "gdn_mtp_strided":
@@ -209,7 +214,7 @@ def make(name: str, *, seed: int | None = None, pool_device="cpu",
         pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
         return Workload(name, "gdn", B, T, H, HV, K, V, P, q, k, v, pool, table[:, 0].clone(), None,
                         BF16, g=g, beta=beta, state_idx=table, num_accepted=accepted)
-    if name == "kda_b256":
+    if name in ("kda_b256", "kda_b256_bf16"):
         B, T, H, HV, K, V, P = 256, 1, 24, 24, 128, 128, 320
         q = _normal(gen, (B, T, H, K)).to(BF16)
         k = _normal(gen, (B, T, H, K)).to(BF16)
@@ -219,11 +224,11 @@ def make(name: str, *, seed: int | None = None, pool_device="cpu",
         A_log = torch.empty(HV).uniform_(math.log(1.0), math.log(16.0), generator=gen)
         dt_bias = _normal(gen, (HV * K,), 0.1)
         ri = torch.randperm(P, generator=gen)[:B].to(index_dtype)
-        pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
+        pool = _draw_pool(gen, (P, HV, V, K), s, pool_device, BF16 if name.endswith("_bf16") else F32)
         return Workload(name, "kda", B, T, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
                         BF16, g=a, beta=b_raw, A_log=A_log, dt_bias=dt_bias,
                         qk_l2norm=True, gate_raw=True, beta_raw=True)
-    if name == "la_b512_packed":
+    if name in ("la_b512_packed", "la_b512_bf16"):
         B, H, K, V, P = 512, 64, 128, 128, 640
         fused = torch.cat([_normal(gen, (B, H, K), 1.0 / math.sqrt(K)),
                            _normal(gen, (B, H, K), 1.0 / math.sqrt(K)),
@@ -231,7 +236,7 @@ def make(name: str, *, seed: int | None = None, pool_device="cpu",
         q, k, v = fused[..., :K], fused[..., K:2 * K], fused[..., 2 * K:]
         decay = la_decay_rates(H)
         ri = torch.randperm(P, generator=gen)[:B].to(index_dtype)
-        pool = _draw_pool(gen, (P * H, V, K), s, pool_device)
+        pool = _draw_pool(gen, (P * H, V, K), s, pool_device, BF16 if name.endswith("_bf16") else F32)
         return Workload(name, "la", B, 1, H, H, K, V, P, q, k, v, pool, ri, ri.clone(),
                         BF16, decay=decay, fused=fused)
     raise KeyError(name)
