@@ -84,7 +84,7 @@
 #define LAR_K128_BF16_NW 2
 #endif
 #ifndef LAR_K128_BF16_KDA_NW
-#define LAR_K128_BF16_KDA_NW 2
+#define LAR_K128_BF16_KDA_NW 1
 #endif
 
 namespace lar {
@@ -764,7 +764,8 @@ lar_status launch_form(const DecodeParams& p, void* stream) {
             // per row, one row per thread), which halves the per-row bookkeeping, in
             // 2-warp CTAs (16-row tiles; up to 8 CTAs per SM progress independently,
             // 6 % faster than 4-warp CTAs); KDA keeps 8 lanes per row to stay within
-            // its register budget, also in 2-warp CTAs (12 % faster than 4 warps).
+            // its register budget, in 1-warp CTAs (8-row tiles; 15 % faster than 4
+            // warps, 3 % faster than 2).
             if constexpr (FORM == FORM_KDA)
                 return launch_tile<FORM, 128, 8, 2, LAR_K128_BF16_KDA_NW, LAR_K128_BF16_S, 2, LAR_K128_MIN_BLOCKS,
                                    LAR_K128_BF16_S>(p, st);

@@ -30,6 +30,9 @@
 #ifndef LAR_KV_BF16_NW
 #define LAR_KV_BF16_NW 2
 #endif
+#ifndef LAR_KV_BF16_S
+#define LAR_KV_BF16_S LAR_KV_S
+#endif
 #ifndef LAR_KV_BF16_MB
 #define LAR_KV_BF16_MB LAR_KV_MB
 #endif
@@ -397,7 +400,7 @@ lar_status launch_form_kv(const DecodeParams& p, void* stream) {
         case 16: return launch_kv_tile<FORM, 16, 2, 2, 2>(p, st);
         case 32: return launch_kv_tile<FORM, 32, 4, 2, 2>(p, st);
         case 64: return launch_kv_tile<FORM, 64, 4, 2, 2>(p, st);
-        case 128: return launch_kv_tile<FORM, 128, LAR_KV_BF16_NW, LAR_KV_S, 2, LAR_KV_BF16_MB, true>(p, st);
+        case 128: return launch_kv_tile<FORM, 128, LAR_KV_BF16_NW, LAR_KV_BF16_S, 2, LAR_KV_BF16_MB, true>(p, st);
         default: return LAR_ERR_SHAPE;
     }
 }
