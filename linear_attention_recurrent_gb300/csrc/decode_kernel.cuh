@@ -47,10 +47,11 @@
 #ifndef LAR_K128_MIN_BLOCKS
 #define LAR_K128_MIN_BLOCKS 3
 #endif
-// Resident CTAs per SM the fp32 GDN and the bf16 GDN / LA K = 128 kernels are
-// compiled for (1: no register cap).  fp32 GDN: 3 (its single-token instance
-// then takes 130 registers and runs 3 CTAs per SM, which measured faster from
-// B = 64 up than the 4 CTAs per SM of its uncapped 128-register build).
+// Resident CTAs per SM the fp32 GDN and the bf16 K = 128 kernels are
+// compiled for (1: no register cap; the bf16 CTAs have 64 threads, so any
+// value up to 3 leaves the compiler all 255 registers).  fp32 GDN: 3, which
+// keeps every instance within 168 registers (the single-token one takes 128
+// and runs 4 CTAs per SM).
 #ifndef LAR_K128_GDN_MB
 #define LAR_K128_GDN_MB 3
 #endif
@@ -73,7 +74,7 @@
 #ifndef LAR_K128_S_MTP
 #define LAR_K128_S_MTP LAR_K128_S
 #endif
-// bf16 GDN / LA K = 128 tile: lanes per row, rows per thread, warps per CTA
+// bf16 K = 128 tile: lanes per row, rows per thread, warps per CTA
 #ifndef LAR_K128_BF16_LPR
 #define LAR_K128_BF16_LPR 4
 #endif
@@ -82,9 +83,6 @@
 #endif
 #ifndef LAR_K128_BF16_NW
 #define LAR_K128_BF16_NW 2
-#endif
-#ifndef LAR_K128_BF16_KDA_NW
-#define LAR_K128_BF16_KDA_NW 1
 #endif
 
 namespace lar {
@@ -760,18 +758,13 @@ lar_status launch_form(const DecodeParams& p, void* stream) {
         case 32: return launch_tile<FORM, 32, 4, 2, 4, 3, 2>(p, st);
         case 64: return launch_tile<FORM, 64, 8, 2, 4, 3, 2>(p, st);
         case 128:
-            // bf16 rows are half the bytes: GDN/LA give each lane 32 elements (4 lanes
-            // per row, one row per thread), which halves the per-row bookkeeping, in
-            // 2-warp CTAs (16-row tiles; up to 8 CTAs per SM progress independently,
-            // 6 % faster than 4-warp CTAs); KDA keeps 8 lanes per row to stay within
-            // its register budget, in 1-warp CTAs (8-row tiles; 15 % faster than 4
-            // warps, 3 % faster than 2).
-            if constexpr (FORM == FORM_KDA)
-                return launch_tile<FORM, 128, 8, 2, LAR_K128_BF16_KDA_NW, LAR_K128_BF16_S, 2, LAR_K128_MIN_BLOCKS,
-                                   LAR_K128_BF16_S>(p, st);
-            else
-                return launch_tile<FORM, 128, LAR_K128_BF16_LPR, LAR_K128_BF16_NR, LAR_K128_BF16_NW, LAR_K128_BF16_S, 2,
-                                   LAR_K128_BF16_MB, LAR_K128_BF16_S>(p, st);
+            // bf16 rows are half the bytes: each lane holds 32 elements (4 lanes per
+            // row, one row per thread), which halves the per-row bookkeeping, in
+            // 2-warp CTAs (16-row tiles; up to 8 CTAs per SM progress independently).
+            // Against 4-warp CTAs: GDN 6 % faster, KDA 19 % (its former 8-lane,
+            // 2-row shape in 1-warp CTAs: 5 % slower).
+            return launch_tile<FORM, 128, LAR_K128_BF16_LPR, LAR_K128_BF16_NR, LAR_K128_BF16_NW, LAR_K128_BF16_S, 2,
+                               LAR_K128_BF16_MB, LAR_K128_BF16_S>(p, st);
         default: return LAR_ERR_SHAPE;
     }
 }
