@@ -50,7 +50,14 @@
  * Ownership and execution: the caller owns every buffer (device memory).  The
  * library allocates nothing, keeps no state between calls and never
  * synchronises: each call validates on the host and then enqueues one kernel
- * on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ * on `stream` (a cudaStream_t; NULL is the legacy default stream).  The kernel
+ * is launched with programmatic dependent launch: it may be scheduled while
+ * the previous kernel on the stream drains, but it reads no memory before that
+ * kernel has completed, so stream order is kept.  Calls may be made from
+ * several host threads at once (the only host-side state is a per-device cache
+ * of occupancy figures, filled under a lock on a kernel's first call) and may
+ * be captured into CUDA graphs; make one uncaptured call of a configuration
+ * first so that the one-time setup does not fall inside the capture.
  *
  * Errors: a host-detectable problem returns a status other than LAR_OK BEFORE
  * anything is launched (nothing is written).  Slot indices >= P are caught on
