@@ -114,3 +114,46 @@ def test_back_to_back_dependent_launches(cuda_device):
         torch.cuda.synchronize()
     assert torch.equal(out_a, out_b)
     assert torch.equal(pool_a, pool_b)
+
+
+def test_calls_from_several_host_threads(cuda_device):
+    """Four host threads, each with its own stream and its own disjoint slots,
+    issue ten in-place steps at once (the first call of a configuration from
+    any thread sets up the launch cache under its lock); the pool ends up as
+    forty serial steps leave it."""
+    import threading
+    dev = cuda_device
+    w = W.make_custom("gdn", B=8, T=1, H=2, HV=4, K=64, V=96, P=40, seed=44)
+    sets = W.disjoint_index_sets(w.P, w.B, 4, seed=9)
+    pool_t, pool_s = w.pool.to(dev), w.pool.to(dev)
+
+    def steps(pool, idx, stream, n=10):
+        w2 = W.make_custom("gdn", B=8, T=1, H=2, HV=4, K=64, V=96, P=40, seed=44)
+        w2.read_idx, w2.write_idx = idx, idx.clone()
+        out = torch.empty(w2.v.shape, dtype=w2.out_dtype, device=dev)
+        call, _ = _call(w2, dev, pool, out, stream)
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                call()
+        stream.synchronize()
+
+    errors = []
+
+    def guarded(*args):
+        try:
+            steps(*args)
+        except Exception as e:   # surfaced below: a thread's exception does not fail the test by itself
+            errors.append(e)
+
+    threads = [threading.Thread(target=guarded, args=(pool_t, idx, torch.cuda.Stream(device=dev)))
+               for idx in sets]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    st = torch.cuda.Stream(device=dev)
+    for idx in sets:
+        steps(pool_s, idx, st)
+    torch.cuda.synchronize()
+    assert torch.equal(pool_t, pool_s)
