@@ -330,7 +330,8 @@ __device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float*
 // TOK: per-token pool slots (seed from the accepted count or read_idx, the state
 // after every token stored to its slot, no final writeback); compiled
 // separately so the plain decode carries none of it.  TT: the token count when
-// fixed at compile time (single-token decode), 0 when taken from the call.
+// fixed at compile time (single-token decode without a state cache), 0 when
+// taken from the call.
 template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB, bool TOK, int TT>
 __global__ void __launch_bounds__(NW * 32, MB)
 decode_kernel(const DecodeParams p) {
@@ -347,6 +348,8 @@ decode_kernel(const DecodeParams p) {
     const unsigned char* pool_b = static_cast<const unsigned char*>(p.pool);
     const bool inter_bf16 = p.inter_dt == LAR_BF16;
     const int inter_es = inter_bf16 ? 2 : 4;
+    // the single-token instance is only launched without a state cache
+    const bool has_inter = TT != 1 && p.inter != nullptr;
     const bool out_bf16 = p.out_dt == LAR_BF16;
     const int out_es = out_bf16 ? 2 : 4;
     const int vstride = vec_floats<FORM, K>(T, V);
@@ -517,7 +520,7 @@ decode_kernel(const DecodeParams p) {
             const int64_t first_row = static_cast<int64_t>(vt) * TV + row0;
             v_off = b * p.vs[0] + hv * p.vs[2];
             op = static_cast<unsigned char*>(p.out) + (b * p.os[0] + hv * p.os[2] + first_row * p.os[3]) * out_es;
-            if (p.inter)
+            if (has_inter)
                 ip = static_cast<unsigned char*>(p.inter) +
                      (b * p.is[0] + hv * p.is[2] + first_row * p.is[3] + j * EPC) * inter_es;
 
@@ -629,7 +632,7 @@ decode_kernel(const DecodeParams p) {
                     if (out_bf16) *reinterpret_cast<__nv_bfloat16*>(dst) = __float2bfloat16_rn(o * scale);
                     else *reinterpret_cast<float*>(dst) = o * scale;
                 }
-                if (p.inter != nullptr && rv) {
+                if (has_inter && rv) {
                     unsigned char* dst = ipt + i * i_rstep;
                     const int cstep = LPR * EPC * inter_es;
 #pragma unroll
@@ -721,7 +724,8 @@ lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
             return launch_tile_mode<FORM, K, LPR, NR, NW, (S1 > 0 ? S1 : S), SB, MB, true, 0>(p, stream);
     }
     if constexpr (S1 > 0) {
-        if (p.T == 1) return launch_tile_mode<FORM, K, LPR, NR, NW, S1, SB, MB, false, 1>(p, stream);
+        if (p.T == 1 && p.inter == nullptr)
+            return launch_tile_mode<FORM, K, LPR, NR, NW, S1, SB, MB, false, 1>(p, stream);
     }
     return launch_tile_mode<FORM, K, LPR, NR, NW, S, SB, MB, false, 0>(p, stream);
 }

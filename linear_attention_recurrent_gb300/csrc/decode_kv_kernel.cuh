@@ -85,6 +85,7 @@ decode_kv_kernel(const DecodeParams p) {
     const unsigned char* pool_b = static_cast<const unsigned char*>(p.pool);
     const bool inter_bf16 = p.inter_dt == LAR_BF16;
     const int inter_es = inter_bf16 ? 2 : 4;
+    const bool has_inter = TT != 1 && p.inter != nullptr;   // single-token instances run without a cache
     const bool out_bf16 = p.out_dt == LAR_BF16;
     const int out_es = out_bf16 ? 2 : 4;
 
@@ -209,7 +210,7 @@ decode_kv_kernel(const DecodeParams p) {
             const int64_t first_col = static_cast<int64_t>(vt) * TVC + col0;
             v_off = b * p.vs[0] + hv * p.vs[2];
             op = static_cast<unsigned char*>(p.out) + (b * p.os[0] + hv * p.os[2] + first_col * p.os[3]) * out_es;
-            if (p.inter)
+            if (has_inter)
                 ip = static_cast<unsigned char*>(p.inter) +
                      (b * p.is[0] + hv * p.is[2] + static_cast<int64_t>(rg) * p.is[3] + first_col) * inter_es;
             build_pair_vectors<FORM, K, NW, TT>(p, vecs + buf * vstride, b, hv, h, v_off, sv_on, o_k, o_d, o_v, o_s);
@@ -313,7 +314,7 @@ decode_kv_kernel(const DecodeParams p) {
             for (int i = 0; i < NRK; ++i)
 #pragma unroll
                 for (int e = 0; e < EP; ++e) s[i][e] = __ffma2_rn(kr[i], coef[e], s[i][e]);
-            if (p.inter != nullptr && cv) {
+            if (has_inter && cv) {
 #pragma unroll
                 for (int i = 0; i < NRK; ++i) store_pairs<EPC>(ipt + i * i_rstep, s[i], inter_bf16);
             }
@@ -374,7 +375,7 @@ lar_status launch_kv_tile_mode(const DecodeParams& p, cudaStream_t stream) {
 template <int FORM, int K, int NW, int S, int SB, int MB = 1, bool T1 = false>
 lar_status launch_kv_tile(const DecodeParams& p, cudaStream_t stream) {
     if constexpr (T1) {
-        if (p.T == 1) return launch_kv_tile_mode<FORM, K, NW, S, SB, MB, 1>(p, stream);
+        if (p.T == 1 && p.inter == nullptr) return launch_kv_tile_mode<FORM, K, NW, S, SB, MB, 1>(p, stream);
     }
     return launch_kv_tile_mode<FORM, K, NW, S, SB, MB, 0>(p, stream);
 }

@@ -76,6 +76,13 @@ SWEEP = {
     "gdn_bf16_t5_nocache": ("gdn", dict(B=3, T=5, H=1, HV=3, K=128, V=128, state_dtype=torch.bfloat16)),
     "gdn_t7_cache_k32": ("gdn", dict(B=2, T=7, H=2, HV=2, K=32, V=40, cache_intermediate=True,
                                      in_dtype=F32, out_dtype=F32)),
+    # single-token calls with a state cache (served by the general instances)
+    "gdn_t1_cache": ("gdn", dict(B=4, T=1, H=2, HV=4, K=128, V=128, cache_intermediate=True)),
+    "gdn_kv_t1_cache_bf16": ("gdn", dict(B=3, T=1, H=1, HV=2, K=128, V=96, state_kv=True,
+                                         state_dtype=torch.bfloat16, cache_intermediate=True)),
+    "kda_t1_cache_bf16_pool": ("kda", dict(B=3, T=1, H=2, HV=2, K=128, V=64, raw_gates=True,
+                                           state_dtype=torch.bfloat16, cache_intermediate=True,
+                                           inter_dtype=F32)),
     # more tiles than resident CTAs: every CTA streams several tiles across pair boundaries
     "gdn_split_tiles": ("gdn", dict(B=48, T=1, H=2, HV=4, K=128, V=100, separate_write=True,
                                     skip_frac=0.25)),
