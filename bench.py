@@ -57,6 +57,8 @@ DESCRIPTIONS = {
                     "bf16 flat pool [640*64,128,128]",
     "gdn_b64_kv_bf16": "GDN decode B=64 T=1 H=16 HV=32 K=V=128, bf16 q/k/v/out, bf16 pool "
                        "[256,32,128(k),128(v)] (state stored untransposed)",
+    "gdn_varlen_b64": "GDN variable-length spans N=64 (48 of 1-4 tokens, 16 prefill chunks of 16-128; "
+                      "1159 tokens) H=16 HV=32 K=V=128, bf16 q/k/v/out, fp32 pool [256,32,128,128]",
     "la_b512_packed": "Lightning-Attention decode B=512 T=1 H=64 K=V=128, packed bf16 QKV, "
                       "flat pool [640*64,128,128]",
 }
@@ -209,6 +211,12 @@ def device_inputs(w, dev):
     return d
 
 
+def inter_shape(w):
+    if w.cu_seqlens is not None:
+        return (w.v.shape[0], w.HV, w.V, w.K)
+    return (w.B, w.T, w.HV, w.V, w.K)
+
+
 def index_sets(w):
     """Disjoint (read, write) index sets to rotate over, when the pool holds
     several batches (in-place workloads only); else the workload's own set."""
@@ -239,10 +247,12 @@ def run_lar(args, world, rank, local):
     with torch.cuda.stream(stream):
         for ri, wi in sets:
             out = torch.empty(w.v.shape, dtype=w.out_dtype, device=dev)
-            inter = (torch.empty(w.B, w.T, w.HV, w.V, w.K, device=dev, dtype=w.inter_dtype)
+            inter = (torch.empty(inter_shape(w), device=dev, dtype=w.inter_dtype)
                      if w.cache_intermediate else None)
             kw = dict(d, read_idx=ri.to(dev), write_idx=None if wi is None else wi.to(dev),
                       out=out, inter=inter)
+            if w.cu_seqlens is not None:
+                kw.update(cu_seqlens=w.cu_seqlens.to(dev))
             if w.state_idx is not None:
                 kw.update(state_idx=w.state_idx.to(dev), write_idx=None, inter=None)
                 if w.num_accepted is not None:
@@ -344,6 +354,8 @@ def run_e2e(w, d, sets, dev, stream, args):
     else:
         host_parts["read_idx"] = ri.contiguous()
         host_parts["write_idx"] = wi.contiguous()
+    if w.cu_seqlens is not None:
+        host_parts["cu_seqlens"] = w.cu_seqlens.contiguous()
     offs, total = {}, 0
     for n, t in host_parts.items():
         offs[n] = total
@@ -357,7 +369,7 @@ def run_e2e(w, d, sets, dev, stream, args):
         views[n] = dbuf[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
     out_dev = torch.empty(w.v.shape, dtype=w.out_dtype, device=dev)
     out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
-    inter = (torch.empty(w.B, w.T, w.HV, w.V, w.K, device=dev, dtype=w.inter_dtype)
+    inter = (torch.empty(inter_shape(w), device=dev, dtype=w.inter_dtype)
              if w.cache_intermediate else None)
     kw = dict(views, pool=d["pool"], out=out_dev, inter=inter)
     if w.form != "la":
@@ -394,6 +406,18 @@ def run_e2e(w, d, sets, dev, stream, args):
 def _oracle_step(w, host_pool, batch):
     import oracle
     sel = lambda t: None if t is None else t[batch]
+    if w.cu_seqlens is not None:
+        # one call per sequence on its own token rows
+        fn = {"gdn": oracle.gdn_decode_varlen, "kda": oracle.kda_decode_varlen}[w.form]
+        cu = w.cu_seqlens.long()
+        for n in torch.as_tensor(batch).view(-1).tolist():
+            lo, hi = int(cu[n]), int(cu[n + 1])
+            tok = lambda t: None if t is None else t[lo:hi]
+            fn(tok(w.q), tok(w.k), tok(w.v), tok(w.g), tok(w.beta), host_pool, torch.tensor([0, hi - lo]),
+               w.read_idx[n:n + 1], w.write_idx[n:n + 1], A_log=w.A_log, dt_bias=w.dt_bias,
+               qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw, scale=w.scale,
+               cache_intermediate=w.cache_intermediate)
+        return
     if w.form == "la":
         oracle.la_decode(sel(w.q), sel(w.k), sel(w.v), w.decay, host_pool, sel(w.read_idx),
                          sel(w.write_idx), scale=w.scale, cache_intermediate=w.cache_intermediate)
@@ -463,6 +487,22 @@ def cpu_baseline(w_dev, args, budget_s=10.0):
                               "sample": f"{reps1} whole steps in {el1:.1f} s"}}
 
 
+def sample_bytes(w, n):
+    """Algorithmic bytes of the first n entries of a step: their share of the
+    state traffic and, with variable-length spans, their share of the per-token
+    traffic (their tokens over all tokens)."""
+    total = w.algorithmic_bytes()
+    if w.cu_seqlens is None:
+        return total * n / w.B
+    cu = w.cu_seqlens.long()
+    unit = w.HV * w.K * w.V * w.pool.element_size()
+    ok = lambda t: ((t >= 0) & (t < w.P)).long()
+    state = int((ok(w.read_idx.long()) + ok(w.write_idx.long())).sum()) * unit
+    state_n = int((ok(w.read_idx[:n].long()) + ok(w.write_idx[:n].long())).sum()) * unit
+    tok_frac = int(cu[n] - cu[0]) / max(int(cu[-1] - cu[0]), 1)
+    return state_n + (total - state) * tok_frac
+
+
 def run_reference(args, world, rank):
     """Reference arm: the fp64 CPU oracle, rank 0 only, on bounded samples, the
     sample of each step split over all host cores as in cpu_baseline."""
@@ -474,9 +514,10 @@ def run_reference(args, world, rank):
     w = _host_workload(args.config)
     ncores = max(1, min(os.cpu_count() or 1, w.B))
     # size each step's sample so warmup + steps stay around a minute
+    n_probe = min(8, w.B)
     probe_t0 = time.perf_counter()
-    _oracle_step(w, w.pool, torch.arange(1))
-    per_entry = max(time.perf_counter() - probe_t0, 1e-6)
+    _oracle_step(w, w.pool, torch.arange(n_probe))
+    per_entry = max((time.perf_counter() - probe_t0) / n_probe, 1e-6)
     n = max(1, min(w.B, int(60.0 * ncores / ((args.steps + args.warmup) * per_entry))))
     ncores = min(ncores, n)
     slices = [torch.arange(n)[i::ncores] for i in range(ncores)]
@@ -488,10 +529,10 @@ def run_reference(args, world, rank):
         for _ in range(args.steps):
             step()
         el = time.perf_counter() - t0
-    bytes_step = w.algorithmic_bytes() * n / w.B
+    bytes_step = sample_bytes(w, n)
     gbs = bytes_step * args.steps / el / 1e9
     sample = (f"{n} of {w.B} entries ({n * w.HV} (entry, head) states) per step, split over "
-              f"{ncores} threads; bytes scaled by {n}/{w.B}")
+              f"{ncores} threads; bytes: those of the {n} entries")
     return {"impl": "reference", "metric": METRIC, "value": round(gbs, 5), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,

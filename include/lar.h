@@ -122,7 +122,9 @@ enum {
 enum {
     LAR_DEVERR_READ_SLOT = 1,  /* some read_idx[b] >= P (that entry started from zero) */
     LAR_DEVERR_WRITE_SLOT = 2, /* some write slot >= P (that writeback was skipped) */
-    LAR_DEVERR_ACCEPTED = 4    /* some num_accepted[b] outside [1, T] (that entry started from zero) */
+    LAR_DEVERR_ACCEPTED = 4,   /* some num_accepted[b] outside [1, T] (that entry started from zero) */
+    LAR_DEVERR_SEQLEN = 8      /* varlen: some span cu_seqlens[n]..[n+1] reversed or past the token
+                                  arrays (treated as empty: the read state goes to the write slot) */
 };
 
 /*
@@ -212,6 +214,50 @@ lar_status kda_decode_tokens(const lar_tensor* q, const lar_tensor* k, const lar
                              const lar_tensor* num_accepted, const lar_tensor* state_idx,
                              const lar_tensor* out, float scale, uint32_t flags,
                              int32_t* dev_err, void* stream);
+
+/*
+ * Variable-length spans (the "varlen" mode of the aiter KDA decode path): N
+ * sequences whose tokens are packed token-major, sequence n owning tokens
+ * cu_seqlens[n] .. cu_seqlens[n+1] - 1 (any length, 0 included; long spans are
+ * a fused-recurrent prefill that leaves its final state in the pool).  Each
+ * sequence starts from slot read_idx[n] (negative: zero state), runs the same
+ * recurrence token by token, writes o for each of its tokens and its final
+ * state to write_idx[n] (negative: skipped; an empty span copies the read
+ * state there).  Tokens outside every span are not written.
+ *   q, k        [Ntok, H, K];  v, out  [Ntok, HV, V];  any strides, fp32 or bf16
+ *   g, beta     [Ntok, HV] (KDA g: [Ntok, HV, K])
+ *   cu_seqlens  [N + 1], int32 or int64, non-decreasing from 0 to at most Ntok
+ *               (a span that is reversed or runs past Ntok is treated as empty
+ *               and sets LAR_DEVERR_SEQLEN in *dev_err; spans that overlap,
+ *               which non-decreasing offsets rule out, write the shared output
+ *               rows in an unspecified order)
+ *   read_idx, write_idx  [N] (write_idx NULL: the read slot)
+ *   inter       NULL, or [Ntok, HV, V, K] fp32 or bf16: the state after each token
+ *   pool        as for gdn_decode, [v][k] layout only (LAR_STATE_KV is rejected)
+ * Flags, A_log, dt_bias and decay as for the fixed-T calls.  N <= 65535,
+ * Ntok < 2^31.
+ */
+lar_status gdn_decode_varlen(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                             const lar_tensor* g, const lar_tensor* beta,
+                             const lar_tensor* A_log, const lar_tensor* dt_bias,
+                             const lar_tensor* pool, const lar_tensor* cu_seqlens,
+                             const lar_tensor* read_idx, const lar_tensor* write_idx,
+                             const lar_tensor* out, const lar_tensor* inter,
+                             float scale, uint32_t flags, int32_t* dev_err, void* stream);
+
+lar_status kda_decode_varlen(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                             const lar_tensor* g, const lar_tensor* beta,
+                             const lar_tensor* A_log, const lar_tensor* dt_bias,
+                             const lar_tensor* pool, const lar_tensor* cu_seqlens,
+                             const lar_tensor* read_idx, const lar_tensor* write_idx,
+                             const lar_tensor* out, const lar_tensor* inter,
+                             float scale, uint32_t flags, int32_t* dev_err, void* stream);
+
+lar_status la_decode_varlen(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                            const lar_tensor* decay, const lar_tensor* pool,
+                            const lar_tensor* cu_seqlens, const lar_tensor* read_idx,
+                            const lar_tensor* write_idx, const lar_tensor* out,
+                            const lar_tensor* inter, float scale, int32_t* dev_err, void* stream);
 
 /* Static, human-readable name of a status code. */
 const char* lar_status_string(lar_status status);

@@ -16,7 +16,7 @@ _LIB_PATH = _build.LIB
 
 LAR_F32, LAR_BF16, LAR_I32, LAR_I64 = 0, 1, 2, 3
 LAR_QK_L2NORM, LAR_GATE_RAW, LAR_BETA_RAW, LAR_STATE_KV = 1, 2, 4, 8
-LAR_DEVERR_READ_SLOT, LAR_DEVERR_WRITE_SLOT, LAR_DEVERR_ACCEPTED = 1, 2, 4
+LAR_DEVERR_READ_SLOT, LAR_DEVERR_WRITE_SLOT, LAR_DEVERR_ACCEPTED, LAR_DEVERR_SEQLEN = 1, 2, 4, 8
 
 STATUS = {0: "LAR_OK", 1: "LAR_ERR_NULL", 2: "LAR_ERR_DTYPE", 3: "LAR_ERR_RANK",
           4: "LAR_ERR_SHAPE", 5: "LAR_ERR_STRIDE", 6: "LAR_ERR_ALIGN", 7: "LAR_ERR_ARG",
@@ -65,6 +65,12 @@ def load() -> ctypes.CDLL:
             fn.argtypes = [P] * 12 + tail
         lib.la_decode.restype = ctypes.c_int
         lib.la_decode.argtypes = [P] * 9 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+        for name in ("gdn_decode_varlen", "kda_decode_varlen"):
+            fn = getattr(lib, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = [P] * 13 + tail
+        lib.la_decode_varlen.restype = ctypes.c_int
+        lib.la_decode_varlen.argtypes = [P] * 10 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
         lib.lar_status_string.restype = ctypes.c_char_p
         lib.lar_status_string.argtypes = [ctypes.c_int]
         _lib = lib
@@ -189,25 +195,75 @@ def la_decode(q, k, v, decay, pool, read_idx, write_idx=None, *, out=None, inter
     return out
 
 
+def gdn_decode_varlen(q, k, v, g, beta, pool, cu_seqlens, read_idx, write_idx=None, *, out=None,
+                      inter=None, A_log=None, dt_bias=None, scale=1.0, qk_l2norm=False, gate_raw=False,
+                      beta_raw=False, dev_err=None, out_dtype=None, stream=None):
+    """GDN over variable-length spans: q, k [Ntok, H, K], v [Ntok, HV, V], g and
+    beta [Ntok, HV]; sequence n owns tokens cu_seqlens[n] .. cu_seqlens[n+1]-1.
+    Returns out [Ntok, HV, V] (tokens outside every span are left as allocated)."""
+    return _varlen("gdn_decode_varlen", q, k, v, (g, beta, A_log, dt_bias), pool, cu_seqlens, read_idx,
+                   write_idx, out, inter, scale, _flags(qk_l2norm, gate_raw, beta_raw), dev_err, out_dtype,
+                   stream)
+
+
+def kda_decode_varlen(q, k, v, g, beta, pool, cu_seqlens, read_idx, write_idx=None, *, out=None,
+                      inter=None, A_log=None, dt_bias=None, scale=1.0, qk_l2norm=False, gate_raw=False,
+                      beta_raw=False, dev_err=None, out_dtype=None, stream=None):
+    """KDA over variable-length spans (g [Ntok, HV, K]); see gdn_decode_varlen."""
+    return _varlen("kda_decode_varlen", q, k, v, (g, beta, A_log, dt_bias), pool, cu_seqlens, read_idx,
+                   write_idx, out, inter, scale, _flags(qk_l2norm, gate_raw, beta_raw), dev_err, out_dtype,
+                   stream)
+
+
+def la_decode_varlen(q, k, v, decay, pool, cu_seqlens, read_idx, write_idx=None, *, out=None, inter=None,
+                     scale=1.0, dev_err=None, out_dtype=None, stream=None):
+    """Lightning Attention over variable-length spans; see gdn_decode_varlen."""
+    return _varlen("la_decode_varlen", q, k, v, (decay,), pool, cu_seqlens, read_idx, write_idx, out, inter,
+                   scale, None, dev_err, out_dtype, stream)
+
+
+def _varlen(name, q, k, v, gates, pool, cu_seqlens, read_idx, write_idx, out, inter, scale, flags, dev_err,
+            out_dtype, stream):
+    lib = load()
+    if out is None:
+        out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
+    ds = [describe(t) for t in (q, k, v) + tuple(gates) + (pool, cu_seqlens, read_idx, write_idx, out, inter)]
+    err = dev_err.data_ptr() if dev_err is not None else None
+    tail = [float(scale)] + ([] if flags is None else [flags]) + [err, _stream(stream)]
+    st = getattr(lib, name)(*[_ref(d) for d in ds], *tail)
+    _check(name, st)
+    return out
+
+
 class PreparedCall:
     """A decode call whose descriptors are built once, for tight launch loops.
     The tensors it was built from must stay alive and keep their storage.
     Passing ``state_idx`` (and ``num_accepted`` or ``read_idx``) selects the
-    per-token-slot call (gdn_decode_tokens / kda_decode_tokens)."""
+    per-token-slot call (gdn_decode_tokens / kda_decode_tokens); passing
+    ``cu_seqlens`` selects the variable-length call (*_decode_varlen)."""
 
     def __init__(self, form, *, scale=1.0, qk_l2norm=False, gate_raw=False, beta_raw=False,
                  state_kv=False, dev_err=None, stream=None, **tensors):
         lib = load()
         tokens = tensors.get("state_idx") is not None
-        self._name = f"{form}_decode_tokens" if tokens else f"{form}_decode"
+        varlen = tensors.get("cu_seqlens") is not None
+        self._name = f"{form}_decode_varlen" if varlen else (f"{form}_decode_tokens" if tokens else f"{form}_decode")
         self._fn = getattr(lib, self._name)
         self._keep = (tensors, dev_err)
         err = dev_err.data_ptr() if dev_err is not None else None
         st = _stream(stream)
         if form == "la":
-            names = ("q", "k", "v", "decay", "pool", "read_idx", "write_idx", "out", "inter")
+            names = ("q", "k", "v", "decay", "pool") + (("cu_seqlens",) if varlen else ()) + \
+                ("read_idx", "write_idx", "out", "inter")
             self._descs = [describe(tensors.get(n)) for n in names]
             self._args = [_ref(d) for d in self._descs] + [float(scale), err, st]
+        elif varlen:
+            names = ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "pool", "cu_seqlens", "read_idx",
+                     "write_idx", "out", "inter")
+            self._descs = [describe(tensors.get(n)) for n in names]
+            # a state_kv flag is passed on, for the library to reject
+            self._args = [_ref(d) for d in self._descs] + [
+                float(scale), _flags(qk_l2norm, gate_raw, beta_raw, state_kv), err, st]
         else:
             if tokens:
                 names = ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "pool", "read_idx",

@@ -224,8 +224,10 @@ __host__ __device__ constexpr size_t decode_smem_bytes(int T, int V) {
 template <int FORM, int K, int NW, int TT>
 __device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float* vb, int b, int hv, int h,
                                                    int64_t v_off, bool sv_on, int o_k, int o_d, int o_v,
-                                                   int o_s) {
-    const int T = TT > 0 ? TT : p.T;
+                                                   int o_s, int64_t t0 = 0, int nt = -1) {
+    // T: the tokens built, t0 onward (all of the call's tokens by default); the
+    // buffer layout offsets come from the caller
+    const int T = nt >= 0 ? nt : (TT > 0 ? TT : p.T);
     const int V = p.V;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -237,10 +239,10 @@ __device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float*
     for (int i = threadIdx.x; i < T * K; i += NW * 32) {
         const int t = i / K;
         const int c = i - t * K;
-        vb[i] = ld_in(p.q, q_off + t * p.qs[1] + c * p.qs[3], p.q_dt);
-        vb[o_k + i] = ld_in(p.k, k_off + t * p.ks[1] + c * p.ks[3], p.k_dt);
+        vb[i] = ld_in(p.q, q_off + (t0 + t) * p.qs[1] + c * p.qs[3], p.q_dt);
+        vb[o_k + i] = ld_in(p.k, k_off + (t0 + t) * p.ks[1] + c * p.ks[3], p.k_dt);
         if constexpr (FORM == FORM_KDA) {
-            float x = ld_in(p.g, b * p.gs[0] + t * p.gs[1] + hv * p.gs[2] + c * p.gs[3], p.g_dt);
+            float x = ld_in(p.g, b * p.gs[0] + (t0 + t) * p.gs[1] + hv * p.gs[2] + c * p.gs[3], p.g_dt);
             if (gate_raw) {
                 const float bias =
                     p.dt_bias ? p.dt_bias[(static_cast<int64_t>(hv) * K + c) * p.dtb_s] : 0.f;
@@ -253,18 +255,19 @@ __device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float*
         // tokens innermost and unrolled, so one thread's loads are in flight together
         for (int row = threadIdx.x; row < V; row += NW * 32) {
 #pragma unroll 4
-            for (int t = 0; t < T; ++t) vb[o_v + t * V + row] = ld_in(p.v, v_off + t * p.vs[1] + row * p.vs[3], p.v_dt);
+            for (int t = 0; t < T; ++t)
+                vb[o_v + t * V + row] = ld_in(p.v, v_off + (t0 + t) * p.vs[1] + row * p.vs[3], p.v_dt);
         }
     }
     float* sc = vb + o_s;
     for (int t = threadIdx.x; t < T; t += NW * 32) {
         float bt = 0.f, dec = 1.f;
         if constexpr (FORM != FORM_LA) {
-            bt = ld_in(p.beta, b * p.bs[0] + t * p.bs[1] + hv * p.bs[2], p.beta_dt);
+            bt = ld_in(p.beta, b * p.bs[0] + (t0 + t) * p.bs[1] + hv * p.bs[2], p.beta_dt);
             if (p.flags & LAR_BETA_RAW) bt = 1.f / (1.f + expf(-bt));
         }
         if constexpr (FORM == FORM_GDN) {
-            float x = ld_in(p.g, b * p.gs[0] + t * p.gs[1] + hv * p.gs[2], p.g_dt);
+            float x = ld_in(p.g, b * p.gs[0] + (t0 + t) * p.gs[1] + hv * p.gs[2], p.g_dt);
             if (gate_raw) {
                 const float bias = p.dt_bias ? p.dt_bias[hv * p.dtb_s] : 0.f;
                 x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
@@ -305,8 +308,10 @@ __device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float*
 // after every token stored to its slot, no final writeback); compiled
 // separately so the plain decode carries none of it.  TT: the token count when
 // fixed at compile time (single-token decode without a state cache), 0 when
-// taken from the call.
-template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB, bool TOK, int TT>
+// taken from the call.  VL: variable-length sequences (token spans from
+// cu_seqlens, any length; the per-token vectors are staged kMaxTokens at a
+// time, T being the staging capacity).
+template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB, bool TOK, int TT, bool VL>
 __global__ void __launch_bounds__(NW * 32, MB)
 decode_kernel(const DecodeParams p) {
     using G = Tile<K, LPR, NR, NW, SB>;
@@ -458,6 +463,9 @@ decode_kernel(const DecodeParams p) {
     unsigned char* ip = nullptr;         // its first cached chunk for token 0
     unsigned char* tk = nullptr;         // per-token slots: head + tile + row offset inside a slot
     int64_t v_off = 0;
+    int64_t tb = 0;                      // varlen: the pair's first token
+    int L = 0;                           // varlen: the pair's token count
+    bool fresh = false;                  // varlen: this tile built the pair's first chunk
     const float scale = p.scale;
     bool pair_start = true;
 
@@ -480,9 +488,20 @@ decode_kernel(const DecodeParams p) {
                 for (int t = threadIdx.x; t < T; t += NW * 32)
                     tab[t] = ld_idx(p.tslot, b * p.tsl_s[0] + t * p.tsl_s[1], p.tsl_dt);
             }
+            bool span_ok = true;
+            if constexpr (VL) {
+                // token span [cu[b], cu[b+1]); a span that is reversed or runs
+                // past the token arrays is treated as empty and flagged
+                const int64_t lo = ld_idx(p.cu, b * p.cu_s, p.cu_dt);
+                const int64_t hi = ld_idx(p.cu, (b + 1) * p.cu_s, p.cu_dt);
+                span_ok = lo >= 0 && hi >= lo && hi <= p.ntok;
+                tb = span_ok ? lo : 0;
+                L = span_ok ? static_cast<int>(hi - lo) : 0;
+                fresh = true;
+            }
             if (threadIdx.x == 0 && hv == 0 && p.dev_err) {
                 int e = (r >= p.P ? LAR_DEVERR_READ_SLOT : 0) | (w >= p.P ? LAR_DEVERR_WRITE_SLOT : 0) |
-                        (r == kBadCount ? LAR_DEVERR_ACCEPTED : 0);
+                        (r == kBadCount ? LAR_DEVERR_ACCEPTED : 0) | (span_ok ? 0 : LAR_DEVERR_SEQLEN);
                 if (TOK)
                     for (int t = 0; t < T; ++t)
                         if (ld_idx(p.tslot, b * p.tsl_s[0] + t * p.tsl_s[1], p.tsl_dt) >= p.P) e |= LAR_DEVERR_WRITE_SLOT;
@@ -493,12 +512,18 @@ decode_kernel(const DecodeParams p) {
             tk = static_cast<unsigned char*>(p.pool) + head_tile;
             const int64_t first_row = static_cast<int64_t>(vt) * TV + row0;
             v_off = b * p.vs[0] + hv * p.vs[2];
-            op = static_cast<unsigned char*>(p.out) + (b * p.os[0] + hv * p.os[2] + first_row * p.os[3]) * out_es;
+            op = static_cast<unsigned char*>(p.out) +
+                 (b * p.os[0] + tb * p.os[1] + hv * p.os[2] + first_row * p.os[3]) * out_es;
             if (has_inter)
                 ip = static_cast<unsigned char*>(p.inter) +
-                     (b * p.is[0] + hv * p.is[2] + first_row * p.is[3] + j * EPC) * inter_es;
+                     (b * p.is[0] + tb * p.is[1] + hv * p.is[2] + first_row * p.is[3] + j * EPC) * inter_es;
 
-            build_pair_vectors<FORM, K, NW, TT>(p, vecs + buf * vstride, b, hv, h, v_off, sv_on, o_k, o_d, o_v, o_s);
+            if constexpr (VL)
+                build_pair_vectors<FORM, K, NW, TT>(p, vecs + buf * vstride, b, hv, h, v_off, sv_on, o_k, o_d, o_v,
+                                                    o_s, tb, L < T ? L : T);
+            else
+                build_pair_vectors<FORM, K, NW, TT>(p, vecs + buf * vstride, b, hv, h, v_off, sv_on, o_k, o_d, o_v,
+                                                    o_s);
         }
 
         // ---- this thread's copies of the tile have landed: pull its rows into registers
@@ -522,13 +547,29 @@ decode_kernel(const DecodeParams p) {
         // arithmetic runs on element pairs (packed fp32x2 multiply / fma); each
         // reduction keeps one pair accumulator (even and odd elements), summed
         // before the shuffles.
-        const float* vb = vecs + buf * vstride;
-        const float* sc = vb + o_s;
         constexpr int KP = KPL / 2;   // element pairs per lane and row
         unsigned char* opt = op;
         unsigned char* ipt = ip;
+        // varlen spans run in chunks of up to T tokens; each chunk's vectors are
+        // built when it is not the one already in the buffer (the pair's first
+        // chunk, built at the pair start, serves every tile of a short span)
+        int c0 = 0;
+        do {
+        int nt = T;
+        int64_t tg0 = 0;              // first token of the chunk in the token arrays
+        if constexpr (VL) {
+            nt = L - c0 < T ? L - c0 : T;
+            tg0 = tb + c0;
+            if (c0 > 0 || (!fresh && L > T)) {
+                buf ^= 1;
+                build_pair_vectors<FORM, K, NW, TT>(p, vecs + buf * vstride, b, hv, hv / p.group, v_off, sv_on,
+                                                    o_k, o_d, o_v, o_s, tg0, nt);
+            }
+        }
+        const float* vb = vecs + buf * vstride;
+        const float* sc = vb + o_s;
 #pragma unroll 1
-        for (int t = 0; t < T; ++t, opt += o_tstep, ipt += i_tstep) {
+        for (int t = 0; t < nt; ++t, opt += o_tstep, ipt += i_tstep) {
             const float4 s4 = *reinterpret_cast<const float4*>(sc + kScal * t);
             const float bt = s4.x, dec = s4.y, iq = s4.z, ik = s4.w, kq = sc[kScal * t + 4];
             float2 kv[KP], qv[KP], dv[KP];
@@ -563,7 +604,7 @@ decode_kernel(const DecodeParams p) {
                 // clamped into the row range instead of branched around
                 float vval = 0.f;
                 if (sv_on) vval = vb[o_v + t * V + min(row, V - 1)];
-                else if (rv) vval = ld_in(p.v, v_off + t * p.vs[1] + row * p.vs[3], p.v_dt);
+                else if (rv) vval = ld_in(p.v, v_off + (tg0 + t) * p.vs[1] + row * p.vs[3], p.v_dt);
 #pragma unroll
                 for (int e = 0; e < KP; ++e) s[i][e] = __fmul2_rn(s[i][e], FORM == FORM_KDA ? dv[e] : dec2);
                 // q_hat = iq q and k_hat = ik k: the norms scale the reduced sums
@@ -619,6 +660,9 @@ decode_kernel(const DecodeParams p) {
                 }
             }
         }
+        c0 += T;
+        } while (VL && c0 < L);
+        if constexpr (VL) fresh = false;
 
         // ---- writeback to the write slot (skipped for negative / out-of-range slots)
         if (wr) {
@@ -654,10 +698,10 @@ decode_kernel(const DecodeParams p) {
 // once per (device, size) and cached.
 int cached_occupancy(const void* kern, int threads, size_t smem, size_t smem_max, int* sms_out);
 
-template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB, bool TOK, int TT>
+template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB, bool TOK, int TT, bool VL = false>
 lar_status launch_tile_mode(const DecodeParams& p, cudaStream_t stream) {
     using G = Tile<K, LPR, NR, NW, SB>;
-    auto kern = decode_kernel<FORM, K, LPR, NR, NW, S, SB, MB, TOK, TT>;
+    auto kern = decode_kernel<FORM, K, LPR, NR, NW, S, SB, MB, TOK, TT, VL>;
     const size_t smem = decode_smem_bytes<FORM, K, LPR, NR, NW, S, SB>(p.T, p.V);
     // the largest footprint any call can ask for (T = 16 with staged v)
     constexpr size_t smem_max = decode_smem_bytes<FORM, K, LPR, NR, NW, S, SB>(16, kStageVMax / 16);
@@ -693,6 +737,7 @@ lar_status launch_tile_mode(const DecodeParams& p, cudaStream_t stream) {
 // takes S1 stages too.
 template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB = 1, int S1 = 0>
 lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
+    if (p.cu != nullptr) return launch_tile_mode<FORM, K, LPR, NR, NW, S, SB, MB, false, 0, true>(p, stream);
     if constexpr (FORM != FORM_LA) {
         if (p.tslot != nullptr)
             return launch_tile_mode<FORM, K, LPR, NR, NW, (S1 > 0 ? S1 : S), SB, MB, true, 0>(p, stream);

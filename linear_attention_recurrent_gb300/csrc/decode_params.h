@@ -35,6 +35,9 @@ struct DecodeParams {
     const void* nacc;  int64_t na_s; int na_dt;     // accepted-token counts [B] or NULL (seed selection)
     const void* tslot; int64_t tsl_s[2]; int tsl_dt; // per-token write slots [B, T] or NULL
 
+    const void* cu;    int64_t cu_s; int cu_dt;    // varlen: token spans [N+1] or NULL (fixed T)
+    int64_t ntok;                                   // varlen: tokens in the q/k/v arrays
+
     void* out;    int64_t os[4]; int out_dt;
     void* inter; int64_t is[4]; int inter_dt;     // fp32 or bf16; b, t, head, row (same layout as the pool); may be NULL
 

@@ -90,6 +90,61 @@ bool per_token_view(const lar_tensor* t, int full, int64_t B, int64_t T, int64_t
     return true;
 }
 
+// pool: [P, HV, V, K] or flat [P*HV, V, K] (kv: [P, HV, K, V] / [P*HV, K, V]);
+// innermost dimension contiguous, 16-byte chunks.  Fills the pool fields of p.
+lar_status check_pool(const lar_tensor* pl, int form, int64_t HV, int64_t K, int64_t V, bool kv, DecodeParams& p) {
+    const int64_t R1 = kv ? K : V;   // rows of one state
+    const int64_t R2 = kv ? V : K;   // elements of one row
+    p.state_kv = kv ? 1 : 0;
+    if (kv && (R2 * elem_size(pl->dtype)) % 16 != 0) return LAR_ERR_SHAPE;
+    int64_t P;
+    if (pl->ndim == 4) {
+        if (pl->shape[1] != HV || pl->shape[2] != R1 || pl->shape[3] != R2) return LAR_ERR_SHAPE;
+        if (pl->stride[3] != 1) return LAR_ERR_STRIDE;
+        P = pl->shape[0];
+        p.ps[0] = pl->stride[0];
+        p.ps[1] = pl->stride[1];
+        p.ps[2] = pl->stride[2];
+        if (form == lar::FORM_LA && P > 1 && pl->stride[0] != HV * pl->stride[1]) return LAR_ERR_STRIDE;
+    } else if (pl->ndim == 3) {
+        if (pl->shape[1] != R1 || pl->shape[2] != R2) return LAR_ERR_SHAPE;
+        if (pl->shape[0] % HV != 0) return LAR_ERR_SHAPE;
+        if (pl->stride[2] != 1) return LAR_ERR_STRIDE;
+        P = pl->shape[0] / HV;
+        p.ps[0] = pl->stride[0] * HV;
+        p.ps[1] = pl->stride[0];
+        p.ps[2] = pl->stride[1];
+    } else {
+        return LAR_ERR_RANK;
+    }
+    // state rows move as 16-byte chunks: aligned base, strides in whole chunks
+    const int64_t pes = elem_size(pl->dtype);
+    if (reinterpret_cast<uintptr_t>(pl->data) % 16 != 0) return LAR_ERR_ALIGN;
+    if ((p.ps[0] * pes) % 16 || (p.ps[1] * pes) % 16 || (p.ps[2] * pes) % 16) return LAR_ERR_ALIGN;
+    p.P = P;
+    p.pool = pl->data;
+    p.pool_dt = pl->dtype;
+    return LAR_OK;
+}
+
+// read / write slot vectors [B] (write may be NULL: the read slot).
+lar_status check_slots(const lar_tensor* read_idx, const lar_tensor* write_idx, int64_t B, DecodeParams& p) {
+    if (read_idx->ndim != 1) return LAR_ERR_RANK;
+    if (read_idx->shape[0] != B) return LAR_ERR_SHAPE;
+    if (!is_index(read_idx)) return LAR_ERR_DTYPE;
+    p.ridx = read_idx->data; p.ri_s = read_idx->stride[0]; p.ri_dt = read_idx->dtype;
+    if (write_idx) {
+        if (missing(write_idx)) return LAR_ERR_NULL;
+        if (write_idx->ndim != 1) return LAR_ERR_RANK;
+        if (write_idx->shape[0] != B) return LAR_ERR_SHAPE;
+        if (!is_index(write_idx)) return LAR_ERR_DTYPE;
+        p.widx = write_idx->data; p.wi_s = write_idx->stride[0]; p.wi_dt = write_idx->dtype;
+    } else {
+        p.widx = nullptr; p.wi_s = 0; p.wi_dt = LAR_I32;
+    }
+    return LAR_OK;
+}
+
 struct Common {
     const lar_tensor *q, *k, *v, *pool, *read_idx, *write_idx, *out, *inter;
 };
@@ -143,55 +198,12 @@ lar_status check_common(const Common& c, int form, DecodeParams& p, bool kv = fa
     p.v = c.v->data; p.v_dt = c.v->dtype;
     p.out = c.out->data; p.out_dt = c.out->dtype;
 
-    // pool: [P, HV, V, K] or flat [P*HV, V, K] (kv: [P, HV, K, V] / [P*HV, K, V]);
-    // innermost dimension contiguous, 16-byte chunks
-    const lar_tensor* pl = c.pool;
+    lar_status st = check_pool(c.pool, form, HV, K, V, kv, p);
+    if (st != LAR_OK) return st;
+    st = check_slots(c.read_idx, c.write_idx, B, p);
+    if (st != LAR_OK) return st;
     const int64_t R1 = kv ? K : V;   // rows of one state
     const int64_t R2 = kv ? V : K;   // elements of one row
-    p.state_kv = kv ? 1 : 0;
-    if (kv && (R2 * elem_size(pl->dtype)) % 16 != 0) return LAR_ERR_SHAPE;
-    int64_t P;
-    if (pl->ndim == 4) {
-        if (pl->shape[1] != HV || pl->shape[2] != R1 || pl->shape[3] != R2) return LAR_ERR_SHAPE;
-        if (pl->stride[3] != 1) return LAR_ERR_STRIDE;
-        P = pl->shape[0];
-        p.ps[0] = pl->stride[0];
-        p.ps[1] = pl->stride[1];
-        p.ps[2] = pl->stride[2];
-        if (form == lar::FORM_LA && P > 1 && pl->stride[0] != HV * pl->stride[1]) return LAR_ERR_STRIDE;
-    } else if (pl->ndim == 3) {
-        if (pl->shape[1] != R1 || pl->shape[2] != R2) return LAR_ERR_SHAPE;
-        if (pl->shape[0] % HV != 0) return LAR_ERR_SHAPE;
-        if (pl->stride[2] != 1) return LAR_ERR_STRIDE;
-        P = pl->shape[0] / HV;
-        p.ps[0] = pl->stride[0] * HV;
-        p.ps[1] = pl->stride[0];
-        p.ps[2] = pl->stride[1];
-    } else {
-        return LAR_ERR_RANK;
-    }
-    // state rows move as 16-byte chunks: aligned base, strides in whole chunks
-    const int64_t pes = elem_size(pl->dtype);
-    if (reinterpret_cast<uintptr_t>(pl->data) % 16 != 0) return LAR_ERR_ALIGN;
-    if ((p.ps[0] * pes) % 16 || (p.ps[1] * pes) % 16 || (p.ps[2] * pes) % 16) return LAR_ERR_ALIGN;
-    p.P = P;
-    p.pool = pl->data;
-    p.pool_dt = pl->dtype;
-
-    // slot indices
-    if (c.read_idx->ndim != 1) return LAR_ERR_RANK;
-    if (c.read_idx->shape[0] != B) return LAR_ERR_SHAPE;
-    if (!is_index(c.read_idx)) return LAR_ERR_DTYPE;
-    p.ridx = c.read_idx->data; p.ri_s = c.read_idx->stride[0]; p.ri_dt = c.read_idx->dtype;
-    if (c.write_idx) {
-        if (missing(c.write_idx)) return LAR_ERR_NULL;
-        if (c.write_idx->ndim != 1) return LAR_ERR_RANK;
-        if (c.write_idx->shape[0] != B) return LAR_ERR_SHAPE;
-        if (!is_index(c.write_idx)) return LAR_ERR_DTYPE;
-        p.widx = c.write_idx->data; p.wi_s = c.write_idx->stride[0]; p.wi_dt = c.write_idx->dtype;
-    } else {
-        p.widx = nullptr; p.wi_s = 0; p.wi_dt = LAR_I32;
-    }
 
     // intermediate-state cache: [B, T, HV, V, K] (rank 4 [B, HV, V, K] for T = 1)
     p.inter = nullptr;
@@ -328,6 +340,131 @@ lar_status delta_rule(int form, const lar_tensor* q, const lar_tensor* k, const 
     return kda ? lar::launch_kda(p, stream) : lar::launch_gdn(p, stream);
 }
 
+// Variable-length spans: token-major q/k [Ntok, H, K], v / out [Ntok, HV, V],
+// g [Ntok, HV] (KDA [Ntok, HV, K]), beta [Ntok, HV], cu_seqlens [N+1], slots
+// [N], cache [Ntok, HV, V, K] or NULL.  Sequence n owns tokens
+// cu_seqlens[n] .. cu_seqlens[n+1] - 1.  g / beta / A_log / dt_bias are NULL
+// for LA, decay NULL for GDN / KDA.
+lar_status varlen(int form, const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                  const lar_tensor* g, const lar_tensor* beta, const lar_tensor* A_log,
+                  const lar_tensor* dt_bias, const lar_tensor* decay, const lar_tensor* pool,
+                  const lar_tensor* cu_seqlens, const lar_tensor* read_idx, const lar_tensor* write_idx,
+                  const lar_tensor* out, const lar_tensor* inter, float scale, uint32_t flags,
+                  int32_t* dev_err, void* stream) {
+    DecodeParams p{};
+    const bool delta = form != lar::FORM_LA;
+    if (flags & ~static_cast<uint32_t>(LAR_QK_L2NORM | LAR_GATE_RAW | LAR_BETA_RAW)) return LAR_ERR_ARG;
+    if (missing(q) || missing(k) || missing(v) || missing(pool) || missing(cu_seqlens) || missing(read_idx) ||
+        missing(out))
+        return LAR_ERR_NULL;
+    if (delta && (missing(g) || missing(beta))) return LAR_ERR_NULL;
+    const lar_tensor* all[] = {q, k, v, g, beta, pool, cu_seqlens, read_idx, write_idx, out, inter};
+    for (const lar_tensor* t : all) {
+        if (!t) continue;
+        const lar_status st = check_header(t);
+        if (st != LAR_OK) return st;
+    }
+    if (q->ndim != 3 || k->ndim != 3 || v->ndim != 3 || out->ndim != 3) return LAR_ERR_RANK;
+    if (!is_float(q) || !is_float(k) || !is_float(v) || !is_float(out) || !is_float(pool)) return LAR_ERR_DTYPE;
+    const int64_t NT = q->shape[0], H = q->shape[1], K = q->shape[2];
+    const int64_t HV = v->shape[1], V = v->shape[2];
+    if (k->shape[0] != NT || k->shape[1] != H || k->shape[2] != K) return LAR_ERR_SHAPE;
+    if (v->shape[0] != NT || out->shape[0] != NT || out->shape[1] != HV || out->shape[2] != V) return LAR_ERR_SHAPE;
+    if (K != 16 && K != 32 && K != 64 && K != 128) return LAR_ERR_SHAPE;
+    if (H < 1 || HV < 1 || V < 1 || HV > 65535 || V > (1 << 24) || NT > INT32_MAX) return LAR_ERR_SHAPE;
+    if (HV % H != 0) return LAR_ERR_SHAPE;
+    if (!delta && HV != H) return LAR_ERR_SHAPE;
+    if (cu_seqlens->ndim != 1) return LAR_ERR_RANK;
+    if (!is_index(cu_seqlens)) return LAR_ERR_DTYPE;
+    const int64_t N = cu_seqlens->shape[0] - 1;
+    if (N < 0 || N > 65535) return LAR_ERR_SHAPE;
+
+    p.form = form;
+    p.B = static_cast<int>(N);
+    p.T = lar::kMaxTokens;   // tokens staged per chunk
+    p.H = static_cast<int>(H);
+    p.HV = static_cast<int>(HV);
+    p.K = static_cast<int>(K);
+    p.V = static_cast<int>(V);
+    p.group = static_cast<int>(HV / H);
+    // (sequence, token, head, x) strides: the sequence term is 0, tokens are
+    // addressed through cu_seqlens
+    const lar_tensor* tv[] = {q, k, v, out};
+    int64_t* dst[] = {p.qs, p.ks, p.vs, p.os};
+    for (int i = 0; i < 4; ++i) {
+        dst[i][0] = 0;
+        for (int d = 0; d < 3; ++d) dst[i][d + 1] = tv[i]->stride[d];
+    }
+    p.q = q->data; p.q_dt = q->dtype;
+    p.k = k->data; p.k_dt = k->dtype;
+    p.v = v->data; p.v_dt = v->dtype;
+    p.out = out->data; p.out_dt = out->dtype;
+    lar_status st = check_pool(pool, form, HV, K, V, false, p);
+    if (st != LAR_OK) return st;
+    if ((st = check_slots(read_idx, write_idx, N, p)) != LAR_OK) return st;
+    p.cu = cu_seqlens->data; p.cu_s = cu_seqlens->stride[0]; p.cu_dt = cu_seqlens->dtype;
+    p.ntok = NT;
+
+    // per-token state cache [Ntok, HV, V, K]
+    p.inter = nullptr; p.inter_dt = LAR_F32;
+    for (int i = 0; i < 4; ++i) p.is[i] = 0;
+    if (inter) {
+        if (missing(inter)) return LAR_ERR_NULL;
+        if (!is_float(inter)) return LAR_ERR_DTYPE;
+        if (inter->ndim != 4) return LAR_ERR_RANK;
+        if (inter->shape[0] != NT || inter->shape[1] != HV || inter->shape[2] != V || inter->shape[3] != K)
+            return LAR_ERR_SHAPE;
+        if (inter->stride[3] != 1) return LAR_ERR_STRIDE;
+        const int64_t ies = elem_size(inter->dtype);
+        if (reinterpret_cast<uintptr_t>(inter->data) % 16 != 0) return LAR_ERR_ALIGN;
+        for (int d = 0; d < 3; ++d)
+            if ((inter->stride[d] * ies) % 16) return LAR_ERR_ALIGN;
+        p.inter = inter->data;
+        p.inter_dt = inter->dtype;
+        p.is[1] = inter->stride[0]; p.is[2] = inter->stride[1]; p.is[3] = inter->stride[2];
+    }
+
+    p.nacc = nullptr; p.tslot = nullptr;
+    p.A_log = nullptr; p.A_s = 0; p.dt_bias = nullptr; p.dtb_s = 0;
+    p.decay = nullptr; p.dec_s = 0;
+    if (delta) {
+        const bool kda = form == lar::FORM_KDA;
+        if (!is_float(g) || !is_float(beta)) return LAR_ERR_DTYPE;
+        if (g->ndim != (kda ? 3 : 2) || beta->ndim != 2) return LAR_ERR_RANK;
+        if (g->shape[0] != NT || g->shape[1] != HV || (kda && g->shape[2] != K)) return LAR_ERR_SHAPE;
+        if (beta->shape[0] != NT || beta->shape[1] != HV) return LAR_ERR_SHAPE;
+        p.gs[0] = 0; p.gs[1] = g->stride[0]; p.gs[2] = g->stride[1]; p.gs[3] = kda ? g->stride[2] : 0;
+        p.bs[0] = 0; p.bs[1] = beta->stride[0]; p.bs[2] = beta->stride[1];
+        p.g = g->data; p.g_dt = g->dtype;
+        p.beta = beta->data; p.beta_dt = beta->dtype;
+        const bool raw = (flags & LAR_GATE_RAW) != 0;
+        if (!raw && (A_log || dt_bias)) return LAR_ERR_ARG;
+        if (raw && !A_log) return LAR_ERR_NULL;
+        if (raw) {
+            if ((st = check_vec(A_log, HV, &p.A_log, &p.A_s)) != LAR_OK) return st;
+            if (dt_bias && (st = check_vec(dt_bias, kda ? HV * K : HV, &p.dt_bias, &p.dtb_s)) != LAR_OK) return st;
+        }
+    } else {
+        if (g || beta || A_log || dt_bias || flags) return LAR_ERR_ARG;
+        if (!decay) return LAR_ERR_NULL;
+        if ((st = check_vec(decay, H, &p.decay, &p.dec_s)) != LAR_OK) return st;
+        p.g = nullptr; p.beta = nullptr;
+    }
+    p.scale = scale;
+    p.flags = flags;
+    p.dev_err = dev_err;
+
+    const lar_tensor* outs[] = {pool, out, inter};
+    const lar_tensor* ins[] = {q, k, v, g, beta, A_log, dt_bias, decay, cu_seqlens, read_idx, write_idx};
+    if ((st = check_aliasing(outs, 3, ins, 11)) != LAR_OK) return st;
+    if (N == 0) return LAR_OK;
+    switch (form) {
+        case lar::FORM_GDN: return lar::launch_gdn(p, stream);
+        case lar::FORM_KDA: return lar::launch_kda(p, stream);
+        default: return lar::launch_la(p, stream);
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -395,6 +532,34 @@ lar_status la_decode(const lar_tensor* q, const lar_tensor* k, const lar_tensor*
     if (st != LAR_OK) return st;
     if (p.B == 0) return LAR_OK;
     return lar::launch_la(p, stream);
+}
+
+lar_status gdn_decode_varlen(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                             const lar_tensor* g, const lar_tensor* beta, const lar_tensor* A_log,
+                             const lar_tensor* dt_bias, const lar_tensor* pool, const lar_tensor* cu_seqlens,
+                             const lar_tensor* read_idx, const lar_tensor* write_idx, const lar_tensor* out,
+                             const lar_tensor* inter, float scale, uint32_t flags, int32_t* dev_err,
+                             void* stream) {
+    return varlen(lar::FORM_GDN, q, k, v, g, beta, A_log, dt_bias, nullptr, pool, cu_seqlens, read_idx,
+                  write_idx, out, inter, scale, flags, dev_err, stream);
+}
+
+lar_status kda_decode_varlen(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                             const lar_tensor* g, const lar_tensor* beta, const lar_tensor* A_log,
+                             const lar_tensor* dt_bias, const lar_tensor* pool, const lar_tensor* cu_seqlens,
+                             const lar_tensor* read_idx, const lar_tensor* write_idx, const lar_tensor* out,
+                             const lar_tensor* inter, float scale, uint32_t flags, int32_t* dev_err,
+                             void* stream) {
+    return varlen(lar::FORM_KDA, q, k, v, g, beta, A_log, dt_bias, nullptr, pool, cu_seqlens, read_idx,
+                  write_idx, out, inter, scale, flags, dev_err, stream);
+}
+
+lar_status la_decode_varlen(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                            const lar_tensor* decay, const lar_tensor* pool, const lar_tensor* cu_seqlens,
+                            const lar_tensor* read_idx, const lar_tensor* write_idx, const lar_tensor* out,
+                            const lar_tensor* inter, float scale, int32_t* dev_err, void* stream) {
+    return varlen(lar::FORM_LA, q, k, v, nullptr, nullptr, nullptr, nullptr, decay, pool, cu_seqlens, read_idx,
+                  write_idx, out, inter, scale, 0, dev_err, stream);
 }
 
 const char* lar_status_string(lar_status status) {

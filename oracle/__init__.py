@@ -249,6 +249,68 @@ def kda_decode_tokens(q, k, v, g, beta, pool, state_idx, *, read_idx=None, num_a
                   gate_raw, beta_raw, scale, cache_intermediate, tokens=(num_accepted, state_idx))
 
 
+def _varlen(run, per_token, cu_seqlens, pool, read_idx, write_idx, cache_intermediate, HV, V, K, ntok):
+    """Variable-length spans: sequence n owns tokens cu_seqlens[n] .. cu_seqlens[n+1]-1
+    and is run as a batch of one with T = its length (T = 0 copies the read
+    state to the write slot).  `per_token` are the token-major inputs, sliced
+    per sequence and given a batch axis.  A span that is reversed or runs past
+    the token arrays is run as empty and counted in n_bad.  Outputs of tokens
+    outside every span stay NaN."""
+    cu = _i64(cu_seqlens)
+    ri = _i64(read_idx)
+    wi = None if write_idx is None else _i64(write_idx)
+    N = cu.shape[0] - 1
+    out = np.full((ntok, HV, V), np.nan)
+    fin = np.zeros((N, HV, V, K))
+    inter = np.full((ntok, HV, V, K), np.nan) if cache_intermediate else None
+    bad = 0
+    for n in range(N):
+        lo, hi = int(cu[n]), int(cu[n + 1])
+        if not 0 <= lo <= hi <= ntok:
+            lo = hi = 0
+            bad += 1
+        part = [None if x is None else x[lo:hi][None] for x in per_token]
+        res = run(*part, pool, ri[n:n + 1], None if wi is None else wi[n:n + 1])
+        out[lo:hi] = res["out"][0]
+        fin[n] = res["final_state"][0]
+        if inter is not None:
+            inter[lo:hi] = res["inter"][0]
+        bad += res["n_bad"]
+    return {"out": out, "final_state": fin, "inter": inter, "n_bad": bad}
+
+
+def gdn_decode_varlen(q, k, v, g, beta, pool, cu_seqlens, read_idx, write_idx=None, *, A_log=None,
+                      dt_bias=None, qk_l2norm=False, gate_raw=False, beta_raw=False, scale=1.0,
+                      cache_intermediate=False):
+    """GDN over token-major variable-length spans: q, k [Ntok,H,K], v [Ntok,HV,V],
+    g, beta [Ntok,HV]; out [Ntok,HV,V], final_state [N,HV,V,K], inter [Ntok,HV,V,K]."""
+    run = lambda q_, k_, v_, g_, b_, pool_, r_, w_: gdn_decode(
+        q_, k_, v_, g_, b_, pool_, r_, w_, A_log=A_log, dt_bias=dt_bias, qk_l2norm=qk_l2norm,
+        gate_raw=gate_raw, beta_raw=beta_raw, scale=scale, cache_intermediate=cache_intermediate)
+    return _varlen(run, (_f64(q), _f64(k), _f64(v), _f64(g), _f64(beta)), cu_seqlens, pool, read_idx,
+                   write_idx, cache_intermediate, v.shape[1], v.shape[2], q.shape[2], q.shape[0])
+
+
+def kda_decode_varlen(q, k, v, g, beta, pool, cu_seqlens, read_idx, write_idx=None, *, A_log=None,
+                      dt_bias=None, qk_l2norm=False, gate_raw=False, beta_raw=False, scale=1.0,
+                      cache_intermediate=False):
+    """KDA over token-major variable-length spans (g [Ntok,HV,K]); see gdn_decode_varlen."""
+    run = lambda q_, k_, v_, g_, b_, pool_, r_, w_: kda_decode(
+        q_, k_, v_, g_, b_, pool_, r_, w_, A_log=A_log, dt_bias=dt_bias, qk_l2norm=qk_l2norm,
+        gate_raw=gate_raw, beta_raw=beta_raw, scale=scale, cache_intermediate=cache_intermediate)
+    return _varlen(run, (_f64(q), _f64(k), _f64(v), _f64(g), _f64(beta)), cu_seqlens, pool, read_idx,
+                   write_idx, cache_intermediate, v.shape[1], v.shape[2], q.shape[2], q.shape[0])
+
+
+def la_decode_varlen(q, k, v, decay, pool, cu_seqlens, read_idx, write_idx=None, *, scale=1.0,
+                     cache_intermediate=False):
+    """Lightning Attention over token-major variable-length spans; see gdn_decode_varlen."""
+    run = lambda q_, k_, v_, pool_, r_, w_: la_decode(q_, k_, v_, decay, pool_, r_, w_, scale=scale,
+                                                      cache_intermediate=cache_intermediate)
+    return _varlen(run, (_f64(q), _f64(k), _f64(v)), cu_seqlens, pool, read_idx, write_idx,
+                   cache_intermediate, v.shape[1], v.shape[2], q.shape[2], q.shape[0])
+
+
 def la_decode(q, k, v, decay, pool, read_idx, write_idx=None, *, scale=1.0,
               cache_intermediate=False):
     """Lightning Attention: S <- lambda_h S + k (x) v, o = S^T q; pool [P*H,V,K] or [P,H,V,K]."""

@@ -38,6 +38,9 @@
  *    treated the same way on the read side, skipped on the write side, and
  *    counted in the return value.
  *  - The intermediate cache holds the state after token t, t = 0..T-1.
+ *  - T = 0 is a step of no tokens: the recurrence is applied zero times, so
+ *    the state as read is what goes to the write slot (the empty spans of the
+ *    variable-length mode).
  *  - o is multiplied by `scale` (1.0 unless a caller asks otherwise).
  *
  * Every input except the pool arrives as a contiguous fp64 array (the Python
@@ -139,7 +142,7 @@ static long delta_rule(int64_t B, int64_t T, int64_t H, int64_t HV, int64_t K, i
                        const int64_t* read_idx, const int64_t* write_idx,
                        const int64_t* num_accepted, const int64_t* state_idx, double* out,
                        double* final_state, double* inter) {
-    if (B < 0 || T < 1 || H < 1 || HV < 1 || K < 1 || V < 1 || HV % H != 0) return -1;
+    if (B < 0 || T < 0 || H < 1 || HV < 1 || K < 1 || V < 1 || HV % H != 0) return -1;
     if (gate_raw && !A_log) return -1;
     if (num_accepted && !state_idx) return -1;
     if (!num_accepted && !read_idx) return -1;
@@ -364,7 +367,7 @@ long oracle_la_decode(int64_t B, int64_t T, int64_t H, int64_t K, int64_t V, con
                       void* pool, int pool_bf16, int64_t pool_rows, const int64_t* st,
                       const int64_t* read_idx, const int64_t* write_idx, double* out,
                       double* final_state, double* inter) {
-    if (B < 0 || T < 1 || H < 1 || K < 1 || V < 1 || pool_rows % H != 0) return -1;
+    if (B < 0 || T < 0 || H < 1 || K < 1 || V < 1 || pool_rows % H != 0) return -1;
     const int64_t P = pool_rows / H;
     long bad = 0;
     double* fin = final_state;

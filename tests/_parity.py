@@ -161,3 +161,76 @@ def full_check(w, dev):
                                                    f"slot {s} (entry {b})"))
     assert int(dev_err.item()) == 0
     return errs
+
+
+# --------------------------------------------------------------------------- variable-length spans
+
+def run_gpu_varlen(w, dev, *, pool, cu_seqlens=None, dev_err=None, out_fill=float("nan")):
+    """Run a make_varlen workload through *_decode_varlen.  out (and the state
+    cache) start filled with `out_fill`, so untouched rows can be checked."""
+    cu = to_dev(w.cu_seqlens if cu_seqlens is None else cu_seqlens, dev)
+    ri, wi = to_dev(w.read_idx, dev), to_dev(w.write_idx, dev)
+    out = torch.full(tuple(w.v.shape), out_fill, dtype=w.out_dtype, device=dev)
+    it = None
+    if w.cache_intermediate:
+        it = torch.full((w.v.shape[0], w.HV, w.V, w.K), out_fill, device=dev, dtype=w.inter_dtype)
+    q, k, v = to_dev(w.q, dev), to_dev(w.k, dev), to_dev(w.v, dev)
+    if w.form == "la":
+        lar.la_decode_varlen(q, k, v, to_dev(w.decay, dev), pool, cu, ri, wi, out=out, inter=it,
+                             scale=w.scale, dev_err=dev_err)
+    else:
+        fn = lar.gdn_decode_varlen if w.form == "gdn" else lar.kda_decode_varlen
+        fn(q, k, v, to_dev(w.g, dev), to_dev(w.beta, dev), pool, cu, ri, wi, out=out, inter=it,
+           A_log=to_dev(w.A_log, dev), dt_bias=to_dev(w.dt_bias, dev), scale=w.scale,
+           qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw, dev_err=dev_err)
+    return out, it
+
+
+def run_oracle_varlen(w, host_pool, cu_seqlens=None):
+    cu = w.cu_seqlens if cu_seqlens is None else cu_seqlens
+    if w.form == "la":
+        return oracle.la_decode_varlen(w.q, w.k, w.v, w.decay, host_pool, cu, w.read_idx, w.write_idx,
+                                       scale=w.scale, cache_intermediate=w.cache_intermediate)
+    fn = oracle.gdn_decode_varlen if w.form == "gdn" else oracle.kda_decode_varlen
+    return fn(w.q, w.k, w.v, w.g, w.beta, host_pool, cu, w.read_idx, w.write_idx, A_log=w.A_log,
+              dt_bias=w.dt_bias, qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw,
+              scale=w.scale, cache_intermediate=w.cache_intermediate)
+
+
+def varlen_check(w, dev, *, cu_seqlens=None, expect_err=0):
+    """Variable-length parity: the outputs and cached states of every token in
+    a valid span against the oracle, rows of tokens outside every span left as
+    allocated (NaN), written slots against the oracle's final states, every
+    other pool byte bit-identical, and the device error word as expected."""
+    st_host = storage(w)
+    dev_storage = st_host.to(dev)
+    before = dev_storage.clone()
+    if w.backing is not None:
+        mult = w.pool.stride(0) // w.backing.stride(0)
+        pool_dev, host_view = dev_storage[::mult], st_host.clone()[::mult]
+    else:
+        pool_dev, host_view = dev_storage, st_host.clone()
+    dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out, inter = run_gpu_varlen(w, dev, pool=pool_dev, cu_seqlens=cu_seqlens, dev_err=dev_err)
+    torch.cuda.synchronize()
+    ref = run_oracle_varlen(w, host_view, cu_seqlens)
+    covered = ~np.isnan(ref["out"]).all(axis=(1, 2))
+    cov_t = torch.from_numpy(covered)
+    errs = {}
+    if covered.any():
+        errs["out"] = assert_out_close(out[cov_t.to(dev)], ref["out"][covered])
+        if inter is not None:
+            errs["inter"] = assert_state_close(inter[cov_t.to(dev)], ref["inter"][covered], "inter")
+    if (~covered).any():
+        assert torch.isnan(out[(~cov_t).to(dev)].float()).all(), "output rows outside every span written"
+        if inter is not None:
+            assert torch.isnan(inter[(~cov_t).to(dev)].float()).all(), "cache rows outside every span written"
+    mask = written_mask(w)
+    assert torch.equal(dev_storage[~mask.to(dev)], before[~mask.to(dev)]), "untouched pool bytes changed"
+    for n, s in enumerate(w.write_idx.tolist()):
+        if 0 <= s < w.P:
+            errs["state"] = max(errs.get("state", 0.0),
+                                assert_state_close(slot_state(pool_dev, w, s), ref["final_state"][n],
+                                                   f"slot {s} (sequence {n})"))
+    assert int(dev_err.item()) == expect_err, int(dev_err.item())
+    return errs

@@ -195,3 +195,60 @@ def test_kv_layout_validation(lib):
             [a[n] for n in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "pool")] + [a["read_idx"], None,
                                                                                        fake([2, 3], I32), a["out"]]]
     assert lib.gdn_decode_tokens(*refs, 1.0, KV, None, None) == ARG
+
+
+def varlen_args(NT=10, N=3, H=2, HV=4, K=128, V=64, P=8, kda=False):
+    return dict(q=fake([NT, H, K], BF16), k=fake([NT, H, K], BF16), v=fake([NT, HV, V], BF16),
+                g=fake([NT, HV, K] if kda else [NT, HV]), beta=fake([NT, HV]), A_log=None, dt_bias=None,
+                pool=fake([P, HV, V, K]), cu_seqlens=fake([N + 1], I32), read_idx=fake([N], I32),
+                write_idx=fake([N], I32), out=fake([NT, HV, V], BF16), inter=None)
+
+
+VARLEN_ORDER = ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "pool", "cu_seqlens", "read_idx",
+                "write_idx", "out", "inter")
+
+
+def varlen_call(lib, a, flags=0, kda=False):
+    fn = lib.kda_decode_varlen if kda else lib.gdn_decode_varlen
+    refs = [ctypes.byref(a[n]) if a[n] is not None else None for n in VARLEN_ORDER]
+    return fn(*refs, 1.0, flags, None, None)
+
+
+def test_varlen_no_sequences_is_a_no_op(lib):
+    assert varlen_call(lib, varlen_args(N=0)) == OK
+
+
+@pytest.mark.parametrize("mutate,flags,expect", [
+    (lambda a: a.update(cu_seqlens=None), 0, NULL),
+    (lambda a: a.update(q=fake([2, 10, 2, 128], BF16)), 0, RANK),          # batched shapes are not varlen
+    (lambda a: a.update(cu_seqlens=fake([4], F32)), 0, DTYPE),
+    (lambda a: a.update(cu_seqlens=fake([4, 1], I32)), 0, RANK),
+    (lambda a: a.update(read_idx=fake([4], I32)), 0, SHAPE),              # N + 1 offsets, N slots
+    (lambda a: a.update(out=fake([9, 4, 64], BF16)), 0, SHAPE),
+    (lambda a: a.update(g=fake([10, 4, 128])), 0, RANK),                  # KDA-shaped gate on GDN
+    (lambda a: a.update(beta=fake([10, 3])), 0, SHAPE),
+    (lambda a: a.update(inter=fake([10, 4, 64, 128, 1])), 0, RANK),
+    (lambda a: a.update(inter=fake([3, 4, 64, 128])), 0, SHAPE),          # per token, not per sequence
+    (lambda a: a.update(out=fake([10, 4, 64], F32, addr=a["pool"].data)), 0, ALIAS),
+    (lambda a: None, 8, ARG),                                             # no K x V layout here
+    (lambda a: None, 2, NULL),                                            # raw gates without A_log
+])
+def test_varlen_rejects_on_host(lib, mutate, flags, expect):
+    a = varlen_args()
+    mutate(a)
+    assert varlen_call(lib, a, flags) == expect
+
+
+def test_varlen_kda_and_la_shapes(lib):
+    a = varlen_args(kda=True)
+    a["g"] = fake([10, 4])
+    assert varlen_call(lib, a, kda=True) == RANK
+    q, k, v = fake([10, 4, 128], BF16), fake([10, 4, 128], BF16), fake([10, 4, 128], BF16)
+    pool, decay, cu, ri, out = fake([5 * 4, 128, 128]), fake([4]), fake([3], I64), fake([2], I64), fake([10, 4, 128], BF16)
+    la = lambda decay: lib.la_decode_varlen(*[ctypes.byref(x) for x in (q, k, v, decay, pool, cu, ri)], None,
+                                            ctypes.byref(out), None, 1.0, None, None)
+    assert la(fake([3])) == SHAPE
+    assert la(fake([4], BF16)) == DTYPE
+    cu0, ri0 = fake([1], I64), fake([0], I64)
+    assert lib.la_decode_varlen(*[ctypes.byref(x) for x in (q, k, v, decay, pool, cu0, ri0)], None,
+                                ctypes.byref(out), None, 1.0, None, None) == OK

@@ -536,3 +536,75 @@ def test_kv_layout_equals_transposed_pool():
     for key in ("out", "final_state", "inter"):
         assert np.array_equal(a[key], b[key])
     assert torch.equal(p_kv, p_vk.transpose(2, 3))
+
+
+# --------------------------------------------------------------------------- variable-length spans
+# (the aiter KDA review names a "varlen" mode: packed sequences of mixed length,
+# token-major, delimited by cumulative offsets)
+
+def _flat(x):
+    return x.reshape((-1,) + tuple(x.shape[2:]))
+
+
+@pytest.mark.parametrize("per_channel", [False, True])
+def test_varlen_equal_lengths_equals_batched(per_channel):
+    """Spans of equal length T over the token-major flattening of a [B, T, ..]
+    batch give the batched results exactly: out row b*T + t is out[b, t] and
+    the written slots match."""
+    q, k, v, g, beta, pool, ri, wi = _rand_delta_case(per_channel, T=3, seed=31)
+    pa, pb = pool.clone(), pool.clone()
+    fn = oracle.kda_decode if per_channel else oracle.gdn_decode
+    vfn = oracle.kda_decode_varlen if per_channel else oracle.gdn_decode_varlen
+    ref = fn(q, k, v, g, beta, pa, ri, wi, cache_intermediate=True)
+    cu = torch.tensor([0, 3, 6, 9])
+    res = vfn(_flat(q), _flat(k), _flat(v), _flat(g), _flat(beta), pb, cu, ri, wi, cache_intermediate=True)
+    assert np.array_equal(res["out"], _flat(torch.from_numpy(ref["out"])).numpy())
+    assert np.array_equal(res["inter"], _flat(torch.from_numpy(ref["inter"])).numpy())
+    assert np.array_equal(res["final_state"], ref["final_state"])
+    assert torch.equal(pa, pb)
+
+
+def test_varlen_split_span_equals_one_span():
+    """A sequence decoded as one span of 7 tokens, or as a span of 3 whose state
+    goes through a pool slot into a span of the next 4 (the chunk boundary of a
+    prefill), ends in the same state with the same outputs (fp32 rounding of
+    the state at the boundary: 1e-6 relative)."""
+    q, k, v, g, beta, pool, _, _ = _rand_delta_case(True, B=1, T=7, P=6, seed=32)
+    q, k, v, g, beta = _flat(q), _flat(k), _flat(v), _flat(g), _flat(beta)
+    whole = oracle.kda_decode_varlen(q, k, v, g, beta, pool.clone(), torch.tensor([0, 7]),
+                                     torch.tensor([2]), torch.tensor([5]))
+    p = pool.clone()
+    first = oracle.kda_decode_varlen(q[:3], k[:3], v[:3], g[:3], beta[:3], p, torch.tensor([0, 3]),
+                                     torch.tensor([2]), torch.tensor([4]))
+    second = oracle.kda_decode_varlen(q[3:], k[3:], v[3:], g[3:], beta[3:], p, torch.tensor([0, 4]),
+                                      torch.tensor([4]), torch.tensor([5]))
+    np.testing.assert_allclose(np.concatenate([first["out"], second["out"]]), whole["out"],
+                               rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(second["final_state"], whole["final_state"], rtol=1e-6, atol=1e-7)
+
+
+def test_varlen_empty_and_bad_spans():
+    """An empty span applies no token: its write slot receives the state as
+    read (bit-exact for an fp32 pool) and no output row belongs to it.  A span
+    that is reversed or runs past the token arrays is counted and run as
+    empty; tokens outside every span keep no output (NaN here)."""
+    gen = torch.Generator().manual_seed(33)
+    q = torch.randn(6, 1, 4, generator=gen, dtype=torch.float64)
+    k = F.normalize(torch.randn(6, 1, 4, generator=gen, dtype=torch.float64), dim=-1)
+    v = torch.randn(6, 1, 3, generator=gen, dtype=torch.float64)
+    g = -torch.rand(6, 1, generator=gen, dtype=torch.float64)
+    beta = torch.rand(6, 1, generator=gen, dtype=torch.float64)
+    pool = torch.randn(8, 1, 3, 4, generator=gen)
+    before = pool.clone()
+    cu = torch.tensor([0, 2, 2, 5, 3, 9])          # spans [0,2) [2,2) [2,5) [5,3) [3,9)
+    ri = torch.tensor([0, 1, 2, 3, 4])
+    wi = torch.tensor([5, 6, 7, -1, 4])
+    res = oracle.gdn_decode_varlen(q, k, v, g, beta, pool, cu, ri, wi)
+    assert res["n_bad"] == 2
+    assert torch.equal(pool[6], before[1])                       # empty span: copy
+    assert torch.equal(pool[4], before[4])                       # bad span: run as empty, in place
+    assert np.isnan(res["out"][5]).all()                         # token 5 lies in no valid span
+    assert not np.isnan(res["out"][:5]).any()
+    one = oracle.gdn_decode(q[None, 2:5], k[None, 2:5], v[None, 2:5], g[None, 2:5], beta[None, 2:5],
+                            before.clone(), torch.tensor([2]), torch.tensor([-1]))
+    assert np.array_equal(res["out"][2:5], one["out"][0])

@@ -55,3 +55,23 @@ def test_disjoint_sets():
     sets = W.disjoint_index_sets(256, 64, 4, seed=7)
     flat = torch.cat(sets).tolist()
     assert len(flat) == 256 and len(set(flat)) == 256
+
+
+def test_varlen_recipe():
+    w = W.make("gdn_varlen_b64")
+    cu = w.cu_seqlens.long()
+    lengths = (cu[1:] - cu[:-1]).tolist()
+    assert cu[0] == 0 and len(lengths) == 64 and int(cu[-1]) == w.q.shape[0] == w.v.shape[0]
+    assert sum(1 for x in lengths if 1 <= x <= 4) == 48 and sum(1 for x in lengths if 16 <= x <= 128) == 16
+    assert w.q.shape[1:] == (16, 128) and w.v.shape[1:] == (32, 128) and w.g.shape == (w.q.shape[0], 32)
+    assert w.tokens() == int(cu[-1])
+    # 2 x 64 x 32 states of 64 KiB, plus q/k/v/g/beta/out of every token and the index arrays
+    per_tok = 2 * (2 * 16 * 128 + 32 * 128) + 2 * 4 * 32 + 2 * 32 * 128
+    assert w.algorithmic_bytes() == 2 * 64 * 32 * 65536 + w.tokens() * per_tok + 2 * 64 * 4 + 65 * 4
+
+
+def test_make_varlen_layout():
+    w = W.make_varlen("kda", [3, 0, 5], H=2, HV=4, K=16, V=8, seed=1, raw_gates=True, separate_write=True)
+    assert w.q.shape == (8, 2, 16) and w.g.shape == (8, 4, 16) and w.beta.shape == (8, 4)
+    assert w.cu_seqlens.tolist() == [0, 3, 3, 8] and w.B == 3
+    assert not set(w.read_idx.tolist()) & set(w.write_idx.tolist())

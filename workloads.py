@@ -36,6 +36,11 @@ la_b512_packed     B=512 T=1 H=64, q/k/v head-dim slices of one fused bf16
 gdn_b64_kv_bf16    gdn_b64_kv with a bfloat16 state pool
 kda_b256_bf16      kda_b256 with a bfloat16 state pool
 la_b512_bf16       la_b512_packed with a bfloat16 state pool
+gdn_varlen_b64     N=64 variable-length spans (draw order: 48 lengths U{1..4}, 16
+                   lengths U{16..128}, a permutation of the 64), token-major bf16
+                   q/k/v [Ntok,..] drawn as gdn_b64 draws them, fp32 g/beta
+                   [Ntok,HV], H=16 HV=32 K=V=128, pool [256,32,128,128];
+                   read = write = randperm(256)[:64]; seed 7
 =================  ===========================================================
 
 Pool entries are N(0, 0.1^2) (standard deviation 0.1).  Full-size pools are
@@ -56,10 +61,10 @@ F32 = torch.float32
 
 CONFIGS = ("gdn_tiny", "gdn_b64", "gdn_mtp_strided", "kda_b256", "la_b512_packed",
            "gdn_b64_bf16", "gdn_spec_b64", "gdn_b64_kv", "gdn_b64_kv_bf16", "kda_b256_bf16",
-           "la_b512_bf16")
+           "la_b512_bf16", "gdn_varlen_b64")
 SEEDS = {"gdn_tiny": 0, "gdn_b64": 2, "gdn_mtp_strided": 3, "kda_b256": 4,
          "la_b512_packed": 5, "gdn_b64_bf16": 2, "gdn_spec_b64": 6, "gdn_b64_kv": 2,
-         "gdn_b64_kv_bf16": 2, "kda_b256_bf16": 4, "la_b512_bf16": 5}
+         "gdn_b64_kv_bf16": 2, "kda_b256_bf16": 4, "la_b512_bf16": 5, "gdn_varlen_b64": 7}
 
 
 @dataclass
@@ -94,6 +99,7 @@ class Workload:
     cache_intermediate: bool = False
     inter_dtype: torch.dtype = F32
     state_kv: bool = False                     # pool / cache hold S as [k][v] (v fastest)
+    cu_seqlens: torch.Tensor | None = None     # [N+1] token offsets (variable-length mode)
     state_idx: torch.Tensor | None = None      # per-token write slots [B, T] (token-slot mode)
     num_accepted: torch.Tensor | None = None   # seed selection [B] (token-slot mode)
     meta: dict = field(default_factory=dict)
@@ -123,18 +129,25 @@ class Workload:
             n_write = int(((w >= 0) & (w < self.P)).sum())
         total = (n_read + n_write) * heads * unit
         if self.cache_intermediate:
-            total += self.B * self.T * heads * self.K * self.V * torch.finfo(self.inter_dtype).bits // 8
+            total += self.tokens() * heads * self.K * self.V * torch.finfo(self.inter_dtype).bits // 8
         small = [self.q, self.k, self.v, self.g, self.beta, self.A_log, self.dt_bias,
                  self.decay, self.state_idx, self.num_accepted]
         if self.state_idx is None:
             small += [self.read_idx, self.write_idx]
         elif self.num_accepted is None:
             small += [self.read_idx]
+        if self.cu_seqlens is not None:
+            small += [self.cu_seqlens]
         total += sum(t.numel() * t.element_size() for t in small if t is not None)
-        total += self.B * self.T * heads * self.V * torch.finfo(self.out_dtype).bits // 8
+        total += self.tokens() * heads * self.V * torch.finfo(self.out_dtype).bits // 8
         return int(total)
 
     def tokens(self) -> int:
+        """Tokens the call decodes (in variable-length mode: the tokens inside
+        the spans, the only ones that produce an output)."""
+        if self.cu_seqlens is not None:
+            cu = self.cu_seqlens.to("cpu").long()
+            return int((cu[1:] - cu[:-1]).clamp(min=0).sum())
         return self.B * self.T
 
 
@@ -239,6 +252,25 @@ def make(name: str, *, seed: int | None = None, pool_device="cpu",
         pool = _draw_pool(gen, (P * H, V, K), s, pool_device, BF16 if name.endswith("_bf16") else F32)
         return Workload(name, "la", B, 1, H, H, K, V, P, q, k, v, pool, ri, ri.clone(),
                         BF16, decay=decay, fused=fused)
+    if name == "gdn_varlen_b64":
+        # variable-length spans: 48 short decode / verify spans and 16 prefill
+        # chunks, in random order, token-major
+        N, H, HV, K, V, P = 64, 16, 32, 128, 128, 256
+        short = torch.randint(1, 5, (48,), generator=gen)
+        long_ = torch.randint(16, 129, (16,), generator=gen)
+        lengths = torch.cat([short, long_])[torch.randperm(N, generator=gen)]
+        cu = torch.zeros(N + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(lengths, 0).to(torch.int32)
+        NT = int(cu[-1])
+        q = _l2n(_normal(gen, (NT, H, K))).to(BF16)
+        k = _l2n(_normal(gen, (NT, H, K))).to(BF16)
+        v = _normal(gen, (NT, HV, V)).to(BF16)
+        g = -F.softplus(_normal(gen, (NT, HV)))
+        beta = torch.sigmoid(_normal(gen, (NT, HV)))
+        ri = torch.randperm(P, generator=gen)[:N].to(index_dtype)
+        pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
+        return Workload(name, "gdn", N, 0, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
+                        BF16, g=g, beta=beta, cu_seqlens=cu)
     raise KeyError(name)
 
 
@@ -352,6 +384,44 @@ def make_custom(form: str, *, B: int, T: int, H: int, HV: int | None = None, K: 
                     cache_intermediate=cache_intermediate,
                     inter_dtype=state_dtype if inter_dtype is None else inter_dtype,
                     state_kv=state_kv)
+
+
+def make_varlen(form: str, lengths, *, H: int, HV: int | None = None, K: int = 128, V: int = 128,
+                P: int | None = None, seed: int = 0, pool_device="cpu", **kw) -> Workload:
+    """Variable-length spans: sequence n owns ``lengths[n]`` consecutive tokens
+    of token-major inputs (q, k [Ntok,H,K], v [Ntok,HV,V], g and beta
+    [Ntok,HV] or [Ntok,HV,K]), ``cu_seqlens`` = [0, cumsum(lengths)].  The
+    tokens are drawn as ``make_custom`` draws one sequence of Ntok tokens; the
+    N read / write slots are then drawn from a second generator seeded with
+    seed + 1 (``separate_write`` and ``skip_frac`` as in ``make_custom``).
+    Other keywords go to ``make_custom`` (dtypes, gates, pool layout, cache)."""
+    lengths = [int(x) for x in lengths]
+    N, ntok = len(lengths), sum(lengths)
+    HV = H if HV is None else HV
+    P = max(2 * N, 4) if P is None else P
+    separate_write = kw.pop("separate_write", False)
+    skip_frac = kw.pop("skip_frac", 0.0)
+    index_dtype = kw.pop("index_dtype", torch.int32)
+    w = make_custom(form, B=1, T=ntok, H=H, HV=HV, K=K, V=V, P=P, seed=seed,
+                    pool_device=pool_device, **kw)
+    gen = torch.Generator().manual_seed(seed + 1)
+    if separate_write:
+        ri, wi = _read_write_disjoint(gen, P, N, skip_frac)
+    else:
+        ri = torch.randperm(P, generator=gen)[:N]
+        wi = ri.clone()
+        n_skip = int(round(skip_frac * N))
+        if n_skip:
+            wi[torch.randperm(N, generator=gen)[:n_skip]] = -1
+    tok = lambda x: None if x is None else x[0]
+    cu = torch.zeros(N + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    w.name, w.B, w.T = f"varlen_{form}", N, 0
+    w.q, w.k, w.v, w.g, w.beta = tok(w.q), tok(w.k), tok(w.v), tok(w.g), tok(w.beta)
+    w.fused = tok(w.fused)
+    w.read_idx, w.write_idx = ri.to(index_dtype), wi.to(index_dtype)
+    w.cu_seqlens = cu
+    return w
 
 
 def disjoint_index_sets(P: int, B: int, n: int, seed: int, index_dtype=torch.int32):
