@@ -304,6 +304,74 @@ __device__ __forceinline__ void build_pair_vectors(const DecodeParams& p, float*
     }
     __syncthreads();}
 
+// Variable-length spans: the tile range [t_begin, t_end) of this CTA, ranges of
+// nearly equal weight.  A tile of sequence n weighs L_n + kVlTileCost: its
+// tokens, plus a fixed cost in token units for loading and storing its state
+// (one token: of 1, 2, 4, 8 and 16, the smallest balanced a mix of 1-4 token
+// spans and 16-128 token spans best); a reversed or overlong span counts as
+// empty.  The
+// weighted start of the j-th tile of sequence n is U (sum over n' < n of the
+// weights) + j (L_n + kVlTileCost), U = HV * (tiles per head); CTA i takes the
+// tiles whose weighted start lies in [i W / G, (i+1) W / G), W the total and G
+// the grid size.  Every CTA scans all of cu_seqlens (each thread a contiguous
+// run of sequences, then a block-wide scan) and derives the same boundaries,
+// so the ranges tile [0, total) exactly.  `red`: shared scratch of NTH / 32 + 2
+// entries.  Weighted positions reach about 2^82 at the largest accepted sizes,
+// hence 128-bit arithmetic.
+#ifndef LAR_VL_TILE_COST
+#define LAR_VL_TILE_COST 1
+#endif
+constexpr int kVlTileCost = LAR_VL_TILE_COST;
+
+template <int NTH>
+__device__ __forceinline__ void vl_partition(const DecodeParams& p, int64_t U, int64_t total, long long* red,
+                                             int64_t& t_begin, int64_t& t_end) {
+    constexpr int NWARP = NTH / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t N = p.B;
+    const int64_t seg = (N + NTH - 1) / NTH;
+    const int64_t lo = min(N, tid * seg), hi = min(N, lo + seg);
+    auto weight = [&](int64_t b) -> long long {
+        const int64_t a = ld_idx(p.cu, b * p.cu_s, p.cu_dt);
+        const int64_t e = ld_idx(p.cu, (b + 1) * p.cu_s, p.cu_dt);
+        return (a >= 0 && e >= a && e <= p.ntok ? e - a : 0) + kVlTileCost;
+    };
+    long long own = 0;
+    for (int64_t b = lo; b < hi; ++b) own += weight(b);
+    long long incl = own;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) red[warp] = incl;
+    if (tid == 0) red[NWARP] = red[NWARP + 1] = 0;   // boundaries at weight 0 match no tile start below
+    __syncthreads();
+    long long w = incl - own, sum = 0;
+#pragma unroll
+    for (int i = 0; i < NWARP; ++i) {
+        if (i < warp) w += red[i];
+        sum += red[i];
+    }
+    using u128 = unsigned __int128;
+    const u128 tot = static_cast<u128>(U) * static_cast<u128>(sum);
+    const u128 x0 = tot * blockIdx.x / gridDim.x;
+    const u128 x1 = tot * (blockIdx.x + 1) / gridDim.x;
+    // the tiles that start below x: all of the sequences before the one whose
+    // weight interval (W_n, W_n+1] holds x, and ceil((x - W_n) / weight) of its own
+    for (int64_t b = lo; b < hi; ++b) {
+        const long long c = weight(b);
+        const u128 wb = static_cast<u128>(U) * static_cast<u128>(w);
+        const u128 wn = static_cast<u128>(U) * static_cast<u128>(w + c);
+        if (wb < x0 && x0 <= wn) red[NWARP] = b * U + static_cast<long long>((x0 - wb + c - 1) / c);
+        if (wb < x1 && x1 <= wn) red[NWARP + 1] = b * U + static_cast<long long>((x1 - wb + c - 1) / c);
+        w += c;
+    }
+    __syncthreads();
+    t_begin = min(max(static_cast<int64_t>(red[NWARP]), int64_t{0}), total);
+    t_end = min(max(static_cast<int64_t>(red[NWARP + 1]), t_begin), total);
+}
+
 // TOK: per-token pool slots (seed from the accepted count or read_idx, the state
 // after every token stored to its slot, no final writeback); compiled
 // separately so the plain decode carries none of it.  TT: the token count when
@@ -345,8 +413,18 @@ decode_kernel(const DecodeParams p) {
 
     const int nvt = (V + TV - 1) / TV;
     const int64_t total = static_cast<int64_t>(p.B) * p.HV * nvt;
-    const int64_t t_begin = blockIdx.x * total / gridDim.x;
-    const int64_t t_end = (blockIdx.x + 1) * total / gridDim.x;
+    int64_t t_begin, t_end;
+    if constexpr (VL) {
+#if LAR_PDL
+        // the span offsets may come from the previous kernel on the stream
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+#endif
+        vl_partition<NW * 32>(p, static_cast<int64_t>(p.HV) * nvt, total, slot_tab, t_begin, t_end);
+    } else {
+        t_begin = blockIdx.x * total / gridDim.x;
+        t_end = (blockIdx.x + 1) * total / gridDim.x;
+    }
 
     if (t_begin >= t_end) return;
 
@@ -397,10 +475,12 @@ decode_kernel(const DecodeParams p) {
     // Programmatic dependent launch.  Everything above is arithmetic on the
     // launch parameters and overlaps the previous kernel's tail; everything
     // below may read what the previous kernel on the stream wrote, so wait for
-    // it here.  Then let the next kernel's CTAs be scheduled as soon as ours
-    // retire.
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    // it here (variable-length calls waited before reading the span offsets).
+    // Then let the next kernel's CTAs be scheduled as soon as ours retire.
+    if constexpr (!VL) {
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    }
 #endif
     int a_rb = a_b;                  // batch entry whose read slot a_r holds
     int64_t a_r = seed_of(a_b);
