@@ -41,6 +41,9 @@ import workloads as W  # noqa: E402
 METRIC = "decode state-pool HBM GB/s (% of GB300 peak) and tokens/s at K=V=128"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+# fp32 FMA-pipe peak: 152 SMs x 128 fp32 lanes x 2.07 GHz (maximum SM clock), in
+# lane operations (one multiply or fused multiply-add on one fp32 value) per second
+ALU_PEAK_OPS = 152 * 128 * 2.07e9
 DESCRIPTIONS = {
     "gdn_tiny": "GDN decode B=2 T=1 H=HV=2 K=V=16 fp32",
     "gdn_b64": "GDN decode B=64 T=1 H=16 HV=32 K=V=128, bf16 q/k/v/out, fp32 pool [256,32,128,128]",
@@ -321,17 +324,35 @@ def run_lar(args, world, rank, local):
         "tokens_per_s": round(tokens, 1),
         "pct_of_8tbs": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_peak": round(100 * gbs / world / peak, 2),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": measured_traffic(args.config),
-                     "peak_source": f"{peak_kind} copy bandwidth",
-                     "kernel": f"decode_kernel<{w.form}> ({kernel_source_hash()})",
-                     "mean_launch_us": round(mean_launch_ms * 1e3, 3)},
+        "roofline": roofline(w, args.config, mean_launch_ms, achieved, peak, peak_kind),
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
     return line
+
+
+def roofline(w, config, mean_launch_ms, achieved_gbs, peak_gbs, peak_kind):
+    """The bound of the launch: HBM (algorithmic bytes / copy bandwidth) unless
+    the fp32 arithmetic of the state update takes longer at the FMA-pipe peak
+    (long variable-length spans), in which case the line reports against that."""
+    base = {"traffic": measured_traffic(config),
+            "kernel": f"decode_kernel<{w.form}> ({kernel_source_hash()})",
+            "mean_launch_us": round(mean_launch_ms * 1e3, 3)}
+    ops = w.alu_ops()
+    t_hbm = w.algorithmic_bytes() / (peak_gbs * 1e9)
+    t_alu = ops / ALU_PEAK_OPS
+    if t_alu > t_hbm:
+        achieved = ops / (mean_launch_ms * 1e-3) / 1e12
+        peak = ALU_PEAK_OPS / 1e12
+        return dict({"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 2),
+                     "unit": "T lane-op/s", "frac": round(achieved / peak, 4),
+                     "peak_source": "152 SMs x 128 fp32 lanes x 2.07 GHz",
+                     "ops_per_launch": ops, "hbm_frac": round(achieved_gbs / peak_gbs, 4)}, **base)
+    return dict({"bound": "hbm", "achieved": round(achieved_gbs, 2), "peak": peak_gbs, "unit": "GB/s",
+                 "frac": round(achieved_gbs / peak_gbs, 4), "peak_source": f"{peak_kind} copy bandwidth"},
+                **base)
 
 
 def run_e2e(w, d, sets, dev, stream, args):

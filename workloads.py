@@ -142,6 +142,13 @@ class Workload:
         total += self.tokens() * heads * self.V * torch.finfo(self.out_dtype).bits // 8
         return int(total)
 
+    def alu_ops(self) -> int:
+        """fp32 lane operations of the state update per call: per token and state
+        element a decay multiply, the S^T k and S^T q multiply-adds and the
+        rank-1 update (GDN, KDA: 4); LA has no S^T k (3)."""
+        per = 3 if self.form == "la" else 4
+        return self.tokens() * self.HV * self.K * self.V * per
+
     def tokens(self) -> int:
         """Tokens the call decodes (in variable-length mode: the tokens inside
         the spans, the only ones that produce an output)."""
