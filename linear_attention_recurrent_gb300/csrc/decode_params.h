@@ -52,5 +52,21 @@ lar_status launch_la(const DecodeParams& p, void* stream);
 
 // Largest T a call may use (per-pair token tables are sized for it).
 constexpr int kMaxTokens = 16;
+// Tokens of a variable-length span staged per chunk (at most kMaxTokens): the
+// per-token vectors of one chunk live in shared memory, so the chunk size sets
+// the CTA's footprint and with it the CTAs per SM.  At K = V = 128, 16-token
+// chunks leave room for 2 fp32-pool CTAs per SM, 12 for 3 (18 % faster on a
+// mix of short and long spans), and 8 for 4 of the bf16 pool's (16 %).
+#ifndef LAR_VL_CHUNK
+#define LAR_VL_CHUNK 12
+#endif
+#ifndef LAR_VL_CHUNK_BF16
+#define LAR_VL_CHUNK_BF16 8
+#endif
+constexpr int kVarlenChunk = LAR_VL_CHUNK;
+constexpr int kVarlenChunkBf16 = LAR_VL_CHUNK_BF16;
+static_assert(kVarlenChunk >= 1 && kVarlenChunk <= kMaxTokens && kVarlenChunkBf16 >= 1 &&
+                  kVarlenChunkBf16 <= kMaxTokens,
+              "chunks within the staging capacity");
 
 }  // namespace lar

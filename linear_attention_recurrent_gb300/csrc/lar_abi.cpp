@@ -381,7 +381,7 @@ lar_status varlen(int form, const lar_tensor* q, const lar_tensor* k, const lar_
 
     p.form = form;
     p.B = static_cast<int>(N);
-    p.T = lar::kMaxTokens;   // tokens staged per chunk
+    // tokens staged per chunk (set below, once the pool type is known)
     p.H = static_cast<int>(H);
     p.HV = static_cast<int>(HV);
     p.K = static_cast<int>(K);
@@ -401,6 +401,7 @@ lar_status varlen(int form, const lar_tensor* q, const lar_tensor* k, const lar_
     p.out = out->data; p.out_dt = out->dtype;
     lar_status st = check_pool(pool, form, HV, K, V, false, p);
     if (st != LAR_OK) return st;
+    p.T = p.pool_dt == LAR_BF16 ? lar::kVarlenChunkBf16 : lar::kVarlenChunk;
     if ((st = check_slots(read_idx, write_idx, N, p)) != LAR_OK) return st;
     p.cu = cu_seqlens->data; p.cu_s = cu_seqlens->stride[0]; p.cu_dt = cu_seqlens->dtype;
     p.ntok = NT;

@@ -2,9 +2,10 @@
 
 N sequences packed token-major, sequence n owning tokens cu_seqlens[n] ..
 cu_seqlens[n+1]-1 (the "varlen" mode the aiter KDA decode review names).  A
-span of more than 16 tokens is staged in chunks of 16, so long spans (a
-fused-recurrent prefill that leaves its final state in the pool) exercise the
-chunk loop; short and empty spans, spans over several V tiles, GQA, bf16 pools
+span longer than the kernel's chunk (12 tokens with an fp32 pool, 8 with a bf16
+pool) is staged chunk by chunk, so long spans (a fused-recurrent prefill that
+leaves its final state in the pool) exercise the chunk loop, and spans of
+exactly one or two chunks its boundaries; short and empty spans, spans over several V tiles, GQA, bf16 pools
 and caches, in-kernel gates, Lightning Attention, skipped and separate write
 slots, reversed and overlong spans are all compared with the oracle.
 """
@@ -39,6 +40,11 @@ CASES = {
     "la_flat_bf16": dict(form="la", lengths=[4, 0, 21, 1], H=2, K=128, V=96, flat_pool=True,
                          state_dtype=BF16, cache_intermediate=True),
     "la_packed": dict(form="la", lengths=[7, 17, 3], H=2, K=128, V=128, packed=True),
+    "gdn_chunk_edges": dict(form="gdn", lengths=[12, 24, 13, 25, 11, 1], H=1, HV=2, K=128, V=128),
+    "gdn_chunk_edges_bf16": dict(form="gdn", lengths=[8, 16, 9, 17, 7, 1], H=1, HV=2, K=128, V=128,
+                                 state_dtype=BF16, cache_intermediate=True),
+    "kda_chunk_edges_k64": dict(form="kda", lengths=[12, 8, 24, 16], H=1, HV=2, K=64, V=64, raw_gates=True,
+                                cache_intermediate=True),
 }
 
 
