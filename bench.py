@@ -573,8 +573,11 @@ SWEEP_POINTS = (
     + [("gdn", 64, T) for T in (2, 4, 8)]
     + [("kda", B, 1) for B in (16, 64, 256, 1024)]
     + [("la", B, 1) for B in (16, 64, 512)]
+    # variable-length spans (T = tokens per span, every span the same length)
+    + [("gdn_varlen", 64, L) for L in (1, 4, 16, 64, 256)]
+    + [("gdn_varlen", 8, 1024)]
 )
-SWEEP_HEADS = {"gdn": (16, 32), "kda": (24, 24), "la": (64, 64)}
+SWEEP_HEADS = {"gdn": (16, 32), "kda": (24, 24), "la": (64, 64), "gdn_varlen": (16, 32)}
 
 
 def run_sweep(args):
@@ -590,8 +593,11 @@ def run_sweep(args):
     peak, _ = hbm_peak()
     for form, B, T in SWEEP_POINTS:
         H, HV = SWEEP_HEADS[form]
-        w = W.make_custom(form, B=B, T=T, H=H, HV=HV, K=128, V=128, P=4 * B, seed=1, pool_device=dev,
-                          raw_gates=form == "kda", flat_pool=form == "la")
+        if form == "gdn_varlen":
+            w = W.make_varlen("gdn", [T] * B, H=H, HV=HV, K=128, V=128, P=4 * B, seed=1, pool_device=dev)
+        else:
+            w = W.make_custom(form, B=B, T=T, H=H, HV=HV, K=128, V=128, P=4 * B, seed=1, pool_device=dev,
+                              raw_gates=form == "kda", flat_pool=form == "la")
         d = device_inputs(w, dev)
         sets, n_sets = index_sets(w)
         stream = torch.cuda.Stream(device=dev)
@@ -599,9 +605,11 @@ def run_sweep(args):
         for ri, wi in sets:
             out = torch.empty(w.v.shape, dtype=w.out_dtype, device=dev)
             kw = dict(d, read_idx=ri.to(dev), write_idx=wi.to(dev), out=out)
-            if form != "la":
+            if w.cu_seqlens is not None:
+                kw.update(cu_seqlens=w.cu_seqlens.to(dev))
+            if w.form != "la":
                 kw.update(qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw)
-            calls.append(lar.PreparedCall(form, scale=w.scale, stream=stream, **kw))
+            calls.append(lar.PreparedCall(w.form, scale=w.scale, stream=stream, **kw))
         for i in range(max(args.warmup, 20)):
             calls[i % n_sets]()
         torch.cuda.synchronize(dev)
@@ -617,6 +625,7 @@ def run_sweep(args):
         gbs = w.algorithmic_bytes() / us / 1e3
         print(json.dumps({"sweep": form, "B": B, "T": T, "H": H, "HV": HV, "us": round(us, 2),
                           "GBs": round(gbs, 1), "pct_of_measured_peak": round(100 * gbs / peak, 1),
+                          "alu_frac": round(w.alu_ops() / (us * 1e-6) / ALU_PEAK_OPS, 3),
                           "tokens_per_s": round(B * T / us * 1e6), "launches": launches}), flush=True)
         del w, d, calls
         torch.cuda.empty_cache()

@@ -1,7 +1,8 @@
 /* A plain C client of the decode library: no Python, no torch.  It builds a
  * small gated-delta-rule decode case on the host, runs it through the C ABI
- * (gdn_decode on device buffers it allocates itself), runs the same inputs
- * through the fp64 oracle, and compares.  It also checks that a host-side
+ * (gdn_decode on device buffers it allocates itself, then gdn_decode_varlen on
+ * the same tokens packed as spans), runs the same inputs through the fp64
+ * oracle, and compares.  It also checks that a host-side
  * argument error comes back as a status before any launch.
  *
  * Exit status 0 on success; prints the first mismatch otherwise.
@@ -63,6 +64,7 @@ int main(void) {
     float *q = malloc(nq * 4), *k = malloc(nq * 4), *v = malloc(nv * 4), *g = malloc(ng * 4);
     float *beta = malloc(ng * 4), *pool = malloc(npool * 4), *pool_ref = malloc(npool * 4);
     float* out = malloc(nv * 4);
+    float* pool0 = malloc(npool * 4);
     for (size_t i = 0; i < nq; ++i) q[i] = uniform_pm1() * 0.3f;
     for (size_t i = 0; i < nq; ++i) k[i] = uniform_pm1() * 0.3f;
     for (size_t i = 0; i < nv; ++i) v[i] = uniform_pm1();
@@ -70,6 +72,7 @@ int main(void) {
     for (size_t i = 0; i < ng; ++i) beta[i] = 0.5f * (uniform_pm1() + 1.0f);
     for (size_t i = 0; i < npool; ++i) pool[i] = 0.1f * uniform_pm1();
     memcpy(pool_ref, pool, npool * 4);
+    memcpy(pool0, pool, npool * 4);
     const int32_t ridx[B] = {4, 0, 2}, widx[B] = {1, -1, 3};
 
     /* ---- device side through the C ABI */
@@ -154,6 +157,46 @@ int main(void) {
             return 1;
         }
     }
-    printf("C ABI client: gdn_decode matches the oracle (%zu outputs, %zu pool elements)\n", nv, npool);
+
+    /* ---- the same tokens as variable-length spans: B sequences of T tokens, token-major */
+    int32_t* dcu;
+    const int32_t cu[B + 1] = {0, T, 2 * T, 3 * T};
+    CHECK_CUDA(cudaMalloc((void**)&dcu, sizeof cu));
+    CHECK_CUDA(cudaMemcpy(dcu, cu, sizeof cu, cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemcpy(dpool, pool0, npool * 4, cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemset(dout, 0, nv * 4));
+    const int64_t vq[3] = {B * T, H, K}, vv[3] = {B * T, HV, V}, vg[2] = {B * T, HV}, vc[1] = {B + 1};
+    lar_tensor uq = desc(dq, LAR_F32, 3, vq), uk = desc(dk, LAR_F32, 3, vq), uv = desc(dv, LAR_F32, 3, vv);
+    lar_tensor ug = desc(dg, LAR_F32, 2, vg), ub = desc(dbeta, LAR_F32, 2, vg), uo = desc(dout, LAR_F32, 3, vv);
+    lar_tensor uc = desc(dcu, LAR_I32, 1, vc);
+    st = gdn_decode_varlen(&uq, &uk, &uv, &ug, &ub, NULL, NULL, &tp, &uc, &tr, &tw, &uo, NULL, scale, 0, derr, NULL);
+    if (st != LAR_OK) {
+        fprintf(stderr, "gdn_decode_varlen: %s\n", lar_status_string(st));
+        return 1;
+    }
+    CHECK_CUDA(cudaDeviceSynchronize());
+    CHECK_CUDA(cudaMemcpy(out, dout, nv * 4, cudaMemcpyDeviceToHost));
+    CHECK_CUDA(cudaMemcpy(pool, dpool, npool * 4, cudaMemcpyDeviceToHost));
+    CHECK_CUDA(cudaMemcpy(&err, derr, 4, cudaMemcpyDeviceToHost));
+    if (err != 0) {
+        fprintf(stderr, "varlen dev_err = %d\n", err);
+        return 1;
+    }
+    for (size_t i = 0; i < nv; ++i) {
+        const double d = fabs((double)out[i] - out64[i]);
+        if (d > 1e-4 * fabs(out64[i]) + 1e-5) {
+            fprintf(stderr, "varlen out[%zu]: lib %.9g oracle %.9g\n", i, (double)out[i], out64[i]);
+            return 1;
+        }
+    }
+    for (size_t i = 0; i < npool; ++i) {
+        const double d = fabs((double)pool[i] - (double)pool_ref[i]);
+        if (d > 1e-4 * fabs((double)pool_ref[i]) + 1e-6) {
+            fprintf(stderr, "varlen pool[%zu]: lib %.9g oracle %.9g\n", i, (double)pool[i], (double)pool_ref[i]);
+            return 1;
+        }
+    }
+    printf("C ABI client: gdn_decode and gdn_decode_varlen match the oracle (%zu outputs, %zu pool elements)\n",
+           nv, npool);
     return 0;
 }

@@ -43,4 +43,4 @@ def test_c_client_matches_oracle(tmp_path, cuda_device):
     exe = _build_client(str(tmp_path))
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
-    assert "matches the oracle" in r.stdout
+    assert "gdn_decode_varlen match the oracle" in r.stdout

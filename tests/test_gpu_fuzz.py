@@ -1,4 +1,4 @@
-"""Seeded random parity sweep: small decode problems with every option drawn at
+"""Seeded random parity sweeps: small decode problems with every option drawn at
 random (form, K, V, T, B, GQA group, input / output / state / cache dtypes,
 state layout, gate flags, separate and skipped writes, strided, flat and packed
 pools), each checked in full against the oracle (outputs, cached states,
@@ -58,3 +58,34 @@ def test_random_case(seed, cuda_device):
     form, kw = draw_case(seed)
     w = W.make_custom(form, **kw)
     P.full_check(w, cuda_device)
+
+
+def draw_varlen_case(seed):
+    """Random variable-length spans: 1-12 sequences of 0-40 tokens, the same
+    option space as the fixed-T draw (bar the [k][v] layout and packed views)."""
+    rnd = random.Random(10_000 + seed)
+    form = rnd.choice(["gdn", "gdn", "kda", "la"])
+    K = rnd.choice([16, 32, 64, 128])
+    H = rnd.randint(1, 3)
+    HV = H * rnd.choice([1, 1, 2, 3]) if form != "la" else H
+    lengths = [rnd.choice([0, 1, 1, 2, 3, 5, 8, 9, 12, 13, 17, 25, 40]) for _ in range(rnd.randint(1, 12))]
+    kw = dict(H=H, HV=HV, K=K, V=rnd.randint(1, 200), seed=2000 + seed,
+              state_dtype=rnd.choice([F32, F32, BF16]), in_dtype=rnd.choice([F32, BF16]),
+              out_dtype=rnd.choice([F32, BF16]), cache_intermediate=rnd.random() < 0.4,
+              inter_dtype=rnd.choice([None, F32, BF16]), index_dtype=rnd.choice([torch.int32, torch.int64]))
+    if form != "la":
+        kw.update(raw_gates=rnd.random() < 0.5)
+    if rnd.random() < 0.4:
+        kw.update(separate_write=True, skip_frac=rnd.choice([0.0, 0.25, 0.5]))
+    if form == "la":
+        kw.update(flat_pool=rnd.random() < 0.5)
+    elif rnd.random() < 0.25:
+        kw.update(stride_mult=rnd.choice([2, 3]))
+    return form, lengths, kw
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_varlen_case(seed, cuda_device):
+    form, lengths, kw = draw_varlen_case(seed)
+    w = W.make_varlen(form, lengths, **kw)
+    P.varlen_check(w, cuda_device)

@@ -124,3 +124,41 @@ def test_guards_token_slots(cuda_device):
                                    num_accepted=accepted.to(torch.int64), scale=w.scale)
     P.assert_out_close(out, ref["out"])
     P.assert_state_close(pool.cpu(), host.double().numpy(), "pool")
+
+
+def test_guards_varlen(cuda_device):
+    """Variable-length spans with an empty span and three trailing tokens that
+    belong to no span: sequence 0 updates the pool's last slot in place; the
+    guards around the pool, the output and the cache stay intact, and the
+    output and cache rows of the trailing tokens keep their sentinel bits."""
+    dev = cuda_device
+    w = W.make_varlen("gdn", [5, 0, 14, 1, 3], H=1, HV=2, K=128, V=100, P=12, seed=53, cache_intermediate=True)
+    N = 4
+    w.cu_seqlens = w.cu_seqlens[:N + 1].clone()
+    ri = torch.tensor([w.P - 1, 3, 7, 0], dtype=torch.int32)
+    w.read_idx, w.write_idx = ri, torch.tensor([w.P - 1, 5, 7, -1], dtype=torch.int32)
+    big_pool, pool = _guarded(tuple(w.pool.shape), w.pool.dtype, dev)
+    pool.copy_(w.pool.to(dev))
+    ntok = w.v.shape[0]
+    big_out, out = _guarded((ntok, w.HV, w.V), w.out_dtype, dev)
+    big_inter, inter = _guarded((ntok, w.HV, w.V, w.K), w.inter_dtype, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lar.gdn_decode_varlen(w.q.to(dev), w.k.to(dev), w.v.to(dev), w.g.to(dev), w.beta.to(dev), pool,
+                          w.cu_seqlens.to(dev), w.read_idx.to(dev), w.write_idx.to(dev), out=out, inter=inter,
+                          scale=w.scale, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert _guards_intact(big_pool, w.pool.dtype), "pool guard overwritten"
+    assert _guards_intact(big_out, w.out_dtype), "output guard overwritten"
+    assert _guards_intact(big_inter, w.inter_dtype), "cache guard overwritten"
+    idt, pat = _PATTERN[w.out_dtype]
+    assert bool((out[20:].contiguous().view(idt) == pat).all()), "output rows outside every span written"
+    idt, pat = _PATTERN[w.inter_dtype]
+    assert bool((inter[20:].contiguous().view(idt) == pat).all()), "cache rows outside every span written"
+    import oracle
+    host = w.pool.clone()
+    ref = oracle.gdn_decode_varlen(w.q, w.k, w.v, w.g, w.beta, host, w.cu_seqlens, w.read_idx, w.write_idx,
+                                   scale=w.scale, cache_intermediate=True)
+    P.assert_out_close(out[:20], ref["out"][:20])
+    P.assert_state_close(inter[:20], ref["inter"][:20], "inter")
+    P.assert_state_close(pool.cpu(), host.double().numpy(), "pool")
