@@ -42,6 +42,10 @@ MUTATIONS = {
                                    "        int64_t w = write_idx ? write_idx[b] : read_idx[b];\n"
                                    "        if (w < 0) w = 0;\n        if (w >= P) { ++bad; continue; }\n"
                                    "        for (int64_t hv"),
+    "empty_span_not_written": ("        if (w < 0) continue;\n        if (w >= P) { ++bad; continue; }\n"
+                               "        for (int64_t hv",
+                               "        if (w < 0 || T == 0) continue;\n        if (w >= P) { ++bad; continue; }\n"
+                               "        for (int64_t hv"),
     "bf16_truncates": ("const double r = nearbyint(ax / q) * q;", "const double r = floor(ax / q) * q;"),
     "seed_off_by_one": ("r = state_idx[b * T + a - 1];", "r = state_idx[b * T + (a < T ? a : a - 1)];"),
     "token_state_shifted": ("const double* f = tok + (((b * T + t) * HV + hv) * V) * K;",
