@@ -76,3 +76,38 @@ def test_max_over_ranks_gloo():
         assert p.exitcode == 0
     got = sorted(q.get(timeout=10) for _ in range(2))
     assert got == [(0, 2.5), (1, 2.5)]
+
+
+def test_roofline_bound_and_sample_bytes():
+    """The roofline names the larger ideal time (HBM for fixed-T decode, the
+    FMA pipe for long variable-length spans), and the reference arm's sample
+    bytes of all entries equal the whole step's algorithmic bytes."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    dec = W.make_custom("gdn", B=64, T=1, H=16, HV=32, K=128, V=128, P=128, seed=1)
+    r = bench.roofline(dec, "x", 0.045, 6000.0, 6791.4, "measured")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and abs(r["frac"] - 6000.0 / 6791.4) < 1e-4
+    vl = W.make_varlen("gdn", [256] * 16, H=16, HV=32, K=128, V=128, P=64, seed=1)
+    assert vl.alu_ops() == 16 * 256 * 32 * 128 * 128 * 4
+    r = bench.roofline(vl, "x", 1.0, 100.0, 6791.4, "measured")
+    assert r["bound"] == "alu" and r["unit"] == "T lane-op/s"
+    assert abs(r["achieved"] - vl.alu_ops() / 1e-3 / 1e12) < 1e-3
+    assert bench.sample_bytes(vl, vl.B) == vl.algorithmic_bytes()
+    mixed = W.make("gdn_varlen_b64")
+    assert abs(bench.sample_bytes(mixed, mixed.B) - mixed.algorithmic_bytes()) < 1
+    assert bench.sample_bytes(mixed, 8) < mixed.algorithmic_bytes()
+
+
+def test_oracle_step_on_variable_length_spans():
+    """The CPU baseline's per-entry oracle step on variable-length spans writes
+    what one whole-workload oracle call writes."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    import workloads as W
+    w = W.make_varlen("gdn", [3, 0, 5, 1], H=1, HV=2, K=16, V=8, seed=4, separate_write=True)
+    ref_pool, step_pool = w.pool.clone(), w.pool.clone()
+    oracle.gdn_decode_varlen(w.q, w.k, w.v, w.g, w.beta, ref_pool, w.cu_seqlens, w.read_idx, w.write_idx)
+    bench._oracle_step(w, step_pool, torch.arange(w.B))
+    assert torch.equal(ref_pool, step_pool)
