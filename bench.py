@@ -62,6 +62,8 @@ DESCRIPTIONS = {
                        "[256,32,128(k),128(v)] (state stored untransposed)",
     "gdn_varlen_b64": "GDN variable-length spans N=64 (48 of 1-4 tokens, 16 prefill chunks of 16-128; "
                       "1159 tokens) H=16 HV=32 K=V=128, bf16 q/k/v/out, fp32 pool [256,32,128,128]",
+    "gdn_prefill_n16": "GDN chunked prefill, N=16 spans of 256-1024 tokens (11094 tokens) H=16 HV=32 K=V=128, "
+                       "bf16 q/k/v/out, fp32 pool [64,32,128,128]",
     "la_b512_packed": "Lightning-Attention decode B=512 T=1 H=64 K=V=128, packed bf16 QKV, "
                       "flat pool [640*64,128,128]",
 }
@@ -263,6 +265,8 @@ def run_lar(args, world, rank, local):
             if w.form != "la":
                 kw.update(qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw,
                           state_kv=w.state_kv)
+            if w.meta.get("prefill"):
+                kw.update(prefill=True)
             calls.append(lar.PreparedCall(w.form, scale=w.scale, stream=stream, **kw))
             outs.append(out)
             inters.append(inter)
@@ -337,8 +341,9 @@ def roofline(w, config, mean_launch_ms, achieved_gbs, peak_gbs, peak_kind):
     """The bound of the launch: HBM (algorithmic bytes / copy bandwidth) unless
     the fp32 arithmetic of the state update takes longer at the FMA-pipe peak
     (long variable-length spans), in which case the line reports against that."""
+    kname = "prefill_kernel" if w.meta.get("prefill") else "decode_kernel"
     base = {"traffic": measured_traffic(config),
-            "kernel": f"decode_kernel<{w.form}> ({kernel_source_hash()})",
+            "kernel": f"{kname}<{w.form}> ({kernel_source_hash()})",
             "mean_launch_us": round(mean_launch_ms * 1e3, 3)}
     ops = w.alu_ops()
     t_hbm = w.algorithmic_bytes() / (peak_gbs * 1e9)
@@ -396,6 +401,8 @@ def run_e2e(w, d, sets, dev, stream, args):
     if w.form != "la":
         kw.update(A_log=d.get("A_log"), dt_bias=d.get("dt_bias"), qk_l2norm=w.qk_l2norm,
                   gate_raw=w.gate_raw, beta_raw=w.beta_raw, state_kv=w.state_kv)
+    if w.meta.get("prefill"):
+        kw.update(prefill=True)
     call = lar.PreparedCall(w.form, scale=w.scale, stream=stream, **kw)
     h2d = sum(t.numel() * t.element_size() for t in host_parts.values())
     d2h = out_host.numel() * out_host.element_size()

@@ -259,6 +259,35 @@ lar_status la_decode_varlen(const lar_tensor* q, const lar_tensor* k, const lar_
                             const lar_tensor* write_idx, const lar_tensor* out,
                             const lar_tensor* inter, float scale, int32_t* dev_err, void* stream);
 
+/*
+ * Chunked prefill over variable-length spans (the form of the recurrence for
+ * long spans): the same operation and arguments as gdn_decode_varlen /
+ * la_decode_varlen, computed 32 tokens at a time with the recurrence unrolled
+ * over each chunk into matrix products and a unit lower-triangular solve (the
+ * per-token recurrence of the aiter KDA review, rearranged; equal up to
+ * rounding).  Every output row of a token inside a span and every written state
+ * is produced; there is no per-token state cache (the chunked form never forms
+ * the intermediate states).
+ *   K = V = 128 only (other shapes: LAR_ERR_SHAPE; use *_decode_varlen);
+ *   GDN and LA only (KDA's per-channel decay has no entry point here).
+ * One CTA per (sequence, v-head) pair holds the state in shared memory for the
+ * whole span, so the work of a sequence is spread over its heads; short spans
+ * are served better by the *_decode_varlen calls.
+ */
+lar_status gdn_prefill(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                       const lar_tensor* g, const lar_tensor* beta,
+                       const lar_tensor* A_log, const lar_tensor* dt_bias,
+                       const lar_tensor* pool, const lar_tensor* cu_seqlens,
+                       const lar_tensor* read_idx, const lar_tensor* write_idx,
+                       const lar_tensor* out, float scale, uint32_t flags, int32_t* dev_err,
+                       void* stream);
+
+lar_status la_prefill(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                      const lar_tensor* decay, const lar_tensor* pool,
+                      const lar_tensor* cu_seqlens, const lar_tensor* read_idx,
+                      const lar_tensor* write_idx, const lar_tensor* out, float scale,
+                      int32_t* dev_err, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* lar_status_string(lar_status status);
 

@@ -71,6 +71,10 @@ def load() -> ctypes.CDLL:
             fn.argtypes = [P] * 13 + tail
         lib.la_decode_varlen.restype = ctypes.c_int
         lib.la_decode_varlen.argtypes = [P] * 10 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+        lib.gdn_prefill.restype = ctypes.c_int
+        lib.gdn_prefill.argtypes = [P] * 12 + tail
+        lib.la_prefill.restype = ctypes.c_int
+        lib.la_prefill.argtypes = [P] * 9 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
         lib.lar_status_string.restype = ctypes.c_char_p
         lib.lar_status_string.argtypes = [ctypes.c_int]
         _lib = lib
@@ -222,12 +226,32 @@ def la_decode_varlen(q, k, v, decay, pool, cu_seqlens, read_idx, write_idx=None,
                    scale, None, dev_err, out_dtype, stream)
 
 
+def gdn_prefill(q, k, v, g, beta, pool, cu_seqlens, read_idx, write_idx=None, *, out=None, A_log=None,
+                dt_bias=None, scale=1.0, qk_l2norm=False, gate_raw=False, beta_raw=False, dev_err=None,
+                out_dtype=None, stream=None):
+    """Chunked GDN prefill over variable-length spans (K = V = 128): the
+    arguments and results of gdn_decode_varlen, without a state cache."""
+    return _varlen("gdn_prefill", q, k, v, (g, beta, A_log, dt_bias), pool, cu_seqlens, read_idx, write_idx, out,
+                   _NO_CACHE, scale, _flags(qk_l2norm, gate_raw, beta_raw), dev_err, out_dtype, stream)
+
+
+def la_prefill(q, k, v, decay, pool, cu_seqlens, read_idx, write_idx=None, *, out=None, scale=1.0,
+               dev_err=None, out_dtype=None, stream=None):
+    """Chunked Lightning-Attention prefill over variable-length spans (K = V = 128)."""
+    return _varlen("la_prefill", q, k, v, (decay,), pool, cu_seqlens, read_idx, write_idx, out, _NO_CACHE,
+                   scale, None, dev_err, out_dtype, stream)
+
+
+_NO_CACHE = object()   # the prefill calls take no state-cache argument
+
+
 def _varlen(name, q, k, v, gates, pool, cu_seqlens, read_idx, write_idx, out, inter, scale, flags, dev_err,
             out_dtype, stream):
     lib = load()
     if out is None:
         out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
-    ds = [describe(t) for t in (q, k, v) + tuple(gates) + (pool, cu_seqlens, read_idx, write_idx, out, inter)]
+    tail_t = () if inter is _NO_CACHE else (inter,)
+    ds = [describe(t) for t in (q, k, v) + tuple(gates) + (pool, cu_seqlens, read_idx, write_idx, out) + tail_t]
     err = dev_err.data_ptr() if dev_err is not None else None
     tail = [float(scale)] + ([] if flags is None else [flags]) + [err, _stream(stream)]
     st = getattr(lib, name)(*[_ref(d) for d in ds], *tail)
@@ -240,26 +264,32 @@ class PreparedCall:
     The tensors it was built from must stay alive and keep their storage.
     Passing ``state_idx`` (and ``num_accepted`` or ``read_idx``) selects the
     per-token-slot call (gdn_decode_tokens / kda_decode_tokens); passing
-    ``cu_seqlens`` selects the variable-length call (*_decode_varlen)."""
+    ``cu_seqlens`` selects the variable-length call (*_decode_varlen), and with
+    ``prefill=True`` the chunked prefill call (gdn_prefill / la_prefill)."""
 
     def __init__(self, form, *, scale=1.0, qk_l2norm=False, gate_raw=False, beta_raw=False,
-                 state_kv=False, dev_err=None, stream=None, **tensors):
+                 state_kv=False, dev_err=None, stream=None, prefill=False, **tensors):
         lib = load()
         tokens = tensors.get("state_idx") is not None
         varlen = tensors.get("cu_seqlens") is not None
-        self._name = f"{form}_decode_varlen" if varlen else (f"{form}_decode_tokens" if tokens else f"{form}_decode")
+        if prefill and (not varlen or tensors.get("inter") is not None):
+            raise ValueError("the prefill call takes cu_seqlens and no state cache")
+        if prefill:
+            self._name = f"{form}_prefill"
+        else:
+            self._name = f"{form}_decode_varlen" if varlen else (f"{form}_decode_tokens" if tokens else f"{form}_decode")
         self._fn = getattr(lib, self._name)
         self._keep = (tensors, dev_err)
         err = dev_err.data_ptr() if dev_err is not None else None
         st = _stream(stream)
         if form == "la":
             names = ("q", "k", "v", "decay", "pool") + (("cu_seqlens",) if varlen else ()) + \
-                ("read_idx", "write_idx", "out", "inter")
+                ("read_idx", "write_idx", "out") + (() if prefill else ("inter",))
             self._descs = [describe(tensors.get(n)) for n in names]
             self._args = [_ref(d) for d in self._descs] + [float(scale), err, st]
         elif varlen:
             names = ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "pool", "cu_seqlens", "read_idx",
-                     "write_idx", "out", "inter")
+                     "write_idx", "out") + (() if prefill else ("inter",))
             self._descs = [describe(tensors.get(n)) for n in names]
             # a state_kv flag is passed on, for the library to reject
             self._args = [_ref(d) for d in self._descs] + [

@@ -350,7 +350,7 @@ lar_status varlen(int form, const lar_tensor* q, const lar_tensor* k, const lar_
                   const lar_tensor* dt_bias, const lar_tensor* decay, const lar_tensor* pool,
                   const lar_tensor* cu_seqlens, const lar_tensor* read_idx, const lar_tensor* write_idx,
                   const lar_tensor* out, const lar_tensor* inter, float scale, uint32_t flags,
-                  int32_t* dev_err, void* stream) {
+                  int32_t* dev_err, void* stream, bool prefill = false) {
     DecodeParams p{};
     const bool delta = form != lar::FORM_LA;
     if (flags & ~static_cast<uint32_t>(LAR_QK_L2NORM | LAR_GATE_RAW | LAR_BETA_RAW)) return LAR_ERR_ARG;
@@ -374,6 +374,9 @@ lar_status varlen(int form, const lar_tensor* q, const lar_tensor* k, const lar_
     if (H < 1 || HV < 1 || V < 1 || HV > 65535 || V > (1 << 24) || NT > INT32_MAX) return LAR_ERR_SHAPE;
     if (HV % H != 0) return LAR_ERR_SHAPE;
     if (!delta && HV != H) return LAR_ERR_SHAPE;
+    // the chunked prefill kernel is built for K = V = 128 and keeps no per-token states
+    if (prefill && (K != 128 || V != 128)) return LAR_ERR_SHAPE;
+    if (prefill && inter) return LAR_ERR_ARG;
     if (cu_seqlens->ndim != 1) return LAR_ERR_RANK;
     if (!is_index(cu_seqlens)) return LAR_ERR_DTYPE;
     const int64_t N = cu_seqlens->shape[0] - 1;
@@ -459,6 +462,7 @@ lar_status varlen(int form, const lar_tensor* q, const lar_tensor* k, const lar_
     const lar_tensor* ins[] = {q, k, v, g, beta, A_log, dt_bias, decay, cu_seqlens, read_idx, write_idx};
     if ((st = check_aliasing(outs, 3, ins, 11)) != LAR_OK) return st;
     if (N == 0) return LAR_OK;
+    if (prefill) return lar::launch_prefill(p, stream);
     switch (form) {
         case lar::FORM_GDN: return lar::launch_gdn(p, stream);
         case lar::FORM_KDA: return lar::launch_kda(p, stream);
@@ -561,6 +565,23 @@ lar_status la_decode_varlen(const lar_tensor* q, const lar_tensor* k, const lar_
                             const lar_tensor* inter, float scale, int32_t* dev_err, void* stream) {
     return varlen(lar::FORM_LA, q, k, v, nullptr, nullptr, nullptr, nullptr, decay, pool, cu_seqlens, read_idx,
                   write_idx, out, inter, scale, 0, dev_err, stream);
+}
+
+lar_status gdn_prefill(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v, const lar_tensor* g,
+                       const lar_tensor* beta, const lar_tensor* A_log, const lar_tensor* dt_bias,
+                       const lar_tensor* pool, const lar_tensor* cu_seqlens, const lar_tensor* read_idx,
+                       const lar_tensor* write_idx, const lar_tensor* out, float scale, uint32_t flags,
+                       int32_t* dev_err, void* stream) {
+    return varlen(lar::FORM_GDN, q, k, v, g, beta, A_log, dt_bias, nullptr, pool, cu_seqlens, read_idx, write_idx,
+                  out, nullptr, scale, flags, dev_err, stream, true);
+}
+
+lar_status la_prefill(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v, const lar_tensor* decay,
+                      const lar_tensor* pool, const lar_tensor* cu_seqlens, const lar_tensor* read_idx,
+                      const lar_tensor* write_idx, const lar_tensor* out, float scale, int32_t* dev_err,
+                      void* stream) {
+    return varlen(lar::FORM_LA, q, k, v, nullptr, nullptr, nullptr, nullptr, decay, pool, cu_seqlens, read_idx,
+                  write_idx, out, nullptr, scale, 0, dev_err, stream, true);
 }
 
 const char* lar_status_string(lar_status status) {

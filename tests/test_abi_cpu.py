@@ -252,3 +252,28 @@ def test_varlen_kda_and_la_shapes(lib):
     cu0, ri0 = fake([1], I64), fake([0], I64)
     assert lib.la_decode_varlen(*[ctypes.byref(x) for x in (q, k, v, decay, pool, cu0, ri0)], None,
                                 ctypes.byref(out), None, 1.0, None, None) == OK
+
+
+PREFILL_ORDER = ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "pool", "cu_seqlens", "read_idx",
+                 "write_idx", "out")
+
+
+def prefill_call(lib, a, flags=0):
+    refs = [ctypes.byref(a[n]) if a[n] is not None else None for n in PREFILL_ORDER]
+    return lib.gdn_prefill(*refs, 1.0, flags, None, None)
+
+
+def test_prefill_rejects_on_host(lib):
+    assert prefill_call(lib, varlen_args(N=0, V=128)) == OK                # no sequences: nothing to do
+    assert prefill_call(lib, varlen_args(K=64, V=64)) == SHAPE             # built for K = V = 128
+    assert prefill_call(lib, varlen_args(K=128, V=64)) == SHAPE
+    assert prefill_call(lib, varlen_args(V=128), flags=8) == ARG           # no K x V layout
+    a = varlen_args(V=128)
+    a["cu_seqlens"] = None
+    assert prefill_call(lib, a) == NULL
+    q, k, v = fake([10, 4, 128], BF16), fake([10, 4, 128], BF16), fake([10, 4, 128], BF16)
+    pool, cu, ri, out = fake([5 * 4, 128, 128]), fake([3], I64), fake([2], I64), fake([10, 4, 128], BF16)
+    la = lambda decay: lib.la_prefill(*[ctypes.byref(x) for x in (q, k, v, decay, pool, cu, ri)], None,
+                                      ctypes.byref(out), 1.0, None, None)
+    assert la(fake([3])) == SHAPE
+    assert la(fake([4], BF16)) == DTYPE

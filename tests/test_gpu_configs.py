@@ -124,3 +124,33 @@ def test_full_size_varlen(cuda_device):
                                        torch.tensor([0, hi - lo]), torch.tensor([0]), torch.tensor([-1]))
         P.assert_out_close(out[lo:hi], ref["out"], f"sequence {n} out")
         P.assert_state_close(w.pool[int(w.write_idx[n])], ref["final_state"][0], f"sequence {n} state")
+
+
+def test_full_size_prefill(cuda_device):
+    """gdn_prefill_n16 at full size through the chunked call: every untouched
+    pool byte bit-identical; sampled sequences (first, last, the longest and
+    seeded others) against the oracle, outputs of their tokens and their
+    written states."""
+    import linear_attention_recurrent_gb300 as lar
+    import oracle
+    dev = cuda_device
+    w = W.make("gdn_prefill_n16", pool_device=dev)
+    before = w.pool.clone()
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = lar.gdn_prefill(w.q.to(dev), w.k.to(dev), w.v.to(dev), w.g.to(dev), w.beta.to(dev), w.pool,
+                          w.cu_seqlens.to(dev), w.read_idx.to(dev), w.write_idx.to(dev), dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    mask = P.written_mask(w).to(dev)
+    assert torch.equal(w.pool[~mask], before[~mask]), "untouched pool bytes changed"
+    cu = w.cu_seqlens.long()
+    lengths = cu[1:] - cu[:-1]
+    sample = sorted({0, w.B - 1, int(lengths.argmax()), 5, 9})
+    for n in sample:
+        lo, hi = int(cu[n]), int(cu[n + 1])
+        sub = before[int(w.read_idx[n])].cpu()[None].clone()
+        tok = lambda t: t[lo:hi]
+        ref = oracle.gdn_decode_varlen(tok(w.q), tok(w.k), tok(w.v), tok(w.g), tok(w.beta), sub,
+                                       torch.tensor([0, hi - lo]), torch.tensor([0]), torch.tensor([-1]))
+        P.assert_out_close(out[lo:hi], ref["out"], f"sequence {n} out")
+        P.assert_state_close(w.pool[int(w.write_idx[n])], ref["final_state"][0], f"sequence {n} state")

@@ -75,3 +75,11 @@ def test_make_varlen_layout():
     assert w.q.shape == (8, 2, 16) and w.g.shape == (8, 4, 16) and w.beta.shape == (8, 4)
     assert w.cu_seqlens.tolist() == [0, 3, 3, 8] and w.B == 3
     assert not set(w.read_idx.tolist()) & set(w.write_idx.tolist())
+
+
+def test_prefill_recipe():
+    w = W.make("gdn_prefill_n16")
+    cu = w.cu_seqlens.long()
+    lengths = (cu[1:] - cu[:-1]).tolist()
+    assert len(lengths) == 16 and all(256 <= x <= 1024 for x in lengths)
+    assert w.meta["prefill"] and w.pool.shape == (64, 32, 128, 128) and w.q.shape[0] == int(cu[-1])

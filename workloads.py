@@ -41,6 +41,9 @@ gdn_varlen_b64     N=64 variable-length spans (draw order: 48 lengths U{1..4}, 1
                    q/k/v [Ntok,..] drawn as gdn_b64 draws them, fp32 g/beta
                    [Ntok,HV], H=16 HV=32 K=V=128, pool [256,32,128,128];
                    read = write = randperm(256)[:64]; seed 7
+gdn_prefill_n16    N=16 spans, lengths U{256..1024} (drawn first), otherwise drawn as
+                   gdn_varlen_b64; pool [64,32,128,128], read = write =
+                   randperm(64)[:16]; run through the chunked prefill call; seed 8
 =================  ===========================================================
 
 Pool entries are N(0, 0.1^2) (standard deviation 0.1).  Full-size pools are
@@ -61,10 +64,11 @@ F32 = torch.float32
 
 CONFIGS = ("gdn_tiny", "gdn_b64", "gdn_mtp_strided", "kda_b256", "la_b512_packed",
            "gdn_b64_bf16", "gdn_spec_b64", "gdn_b64_kv", "gdn_b64_kv_bf16", "kda_b256_bf16",
-           "la_b512_bf16", "gdn_varlen_b64")
+           "la_b512_bf16", "gdn_varlen_b64", "gdn_prefill_n16")
 SEEDS = {"gdn_tiny": 0, "gdn_b64": 2, "gdn_mtp_strided": 3, "kda_b256": 4,
          "la_b512_packed": 5, "gdn_b64_bf16": 2, "gdn_spec_b64": 6, "gdn_b64_kv": 2,
-         "gdn_b64_kv_bf16": 2, "kda_b256_bf16": 4, "la_b512_bf16": 5, "gdn_varlen_b64": 7}
+         "gdn_b64_kv_bf16": 2, "kda_b256_bf16": 4, "la_b512_bf16": 5, "gdn_varlen_b64": 7,
+         "gdn_prefill_n16": 8}
 
 
 @dataclass
@@ -278,6 +282,22 @@ def make(name: str, *, seed: int | None = None, pool_device="cpu",
         pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
         return Workload(name, "gdn", N, 0, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
                         BF16, g=g, beta=beta, cu_seqlens=cu)
+    if name == "gdn_prefill_n16":
+        # long spans for the chunked prefill call: 16 sequences of 256-1024 tokens
+        N, H, HV, K, V, P = 16, 16, 32, 128, 128, 64
+        lengths = torch.randint(256, 1025, (N,), generator=gen)
+        cu = torch.zeros(N + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(lengths, 0).to(torch.int32)
+        NT = int(cu[-1])
+        q = _l2n(_normal(gen, (NT, H, K))).to(BF16)
+        k = _l2n(_normal(gen, (NT, H, K))).to(BF16)
+        v = _normal(gen, (NT, HV, V)).to(BF16)
+        g = -F.softplus(_normal(gen, (NT, HV)))
+        beta = torch.sigmoid(_normal(gen, (NT, HV)))
+        ri = torch.randperm(P, generator=gen)[:N].to(index_dtype)
+        pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
+        return Workload(name, "gdn", N, 0, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
+                        BF16, g=g, beta=beta, cu_seqlens=cu, meta={"prefill": True})
     raise KeyError(name)
 
 
