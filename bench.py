@@ -69,14 +69,21 @@ DESCRIPTIONS = {
 }
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources; ncu traffic figures are valid only for this hash."""
+# the sources each kernel is built from (the ABI layer included: it sets the launch parameters)
+_DECODE_SOURCES = ("decode_kernel.cuh", "decode_kv_kernel.cuh", "decode_gdn.cu", "decode_kda.cu", "decode_la.cu",
+                   "decode_params.h", "launch_cache.cpp", "lar_abi.cpp")
+_PREFILL_SOURCES = ("prefill.cu", "decode_kernel.cuh", "decode_params.h", "lar_abi.cpp")
+
+
+def kernel_source_hash(config: str = "gdn_b64") -> str:
+    """Hash of the sources of the kernel a workload runs (the chunked prefill
+    kernel or the decode kernels); ncu traffic figures are valid only for it."""
+    prefill = config in W.CONFIGS and W.make_meta(config).get("prefill", False)
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_recurrent_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in sorted(_PREFILL_SOURCES if prefill else _DECODE_SOURCES):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:12]
 
 
@@ -85,7 +92,7 @@ def measured_traffic(config: str):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(config)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 3 and not line.startswith("#") and parts[0] == config and parts[1] == want:
@@ -343,7 +350,7 @@ def roofline(w, config, mean_launch_ms, achieved_gbs, peak_gbs, peak_kind):
     (long variable-length spans), in which case the line reports against that."""
     kname = "prefill_kernel" if w.meta.get("prefill") else "decode_kernel"
     base = {"traffic": measured_traffic(config),
-            "kernel": f"{kname}<{w.form}> ({kernel_source_hash()})",
+            "kernel": f"{kname}<{w.form}> ({kernel_source_hash(config)})",
             "mean_launch_us": round(mean_launch_ms * 1e3, 3)}
     ops = w.alu_ops()
     t_hbm = w.algorithmic_bytes() / (peak_gbs * 1e9)

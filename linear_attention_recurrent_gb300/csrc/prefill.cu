@@ -19,12 +19,13 @@
 // from differences of log-decay prefix sums (which lose precision for large
 // decays and break down for a factor of 0).
 //
-// Work.  One CTA of 256 threads per (sequence, v-head) pair keeps S (K x V,
-// fp32) in shared memory for its whole span and walks the span a chunk at a
-// time: load the chunk (q, k l2-normalised when asked; v; decays; betas), the
-// products K S0 and Q S0 (4 x 4 outputs per thread), K K^T and Q K^T, the
-// triangular solve (one value column per thread), the outputs, and the state
-// update (8 x 8 state entries per thread).  Everything is fp32 on the CUDA
+// Work.  A CTA of 256 threads per (sequence, v-head, block of VB value
+// columns) keeps its columns of S (K x VB, fp32) in shared memory for the
+// whole span and walks the span a chunk at a time: load the chunk (q, k
+// l2-normalised when asked; v; decays; betas), the products K S0 and Q S0
+// (4 rows x VB/32 columns per thread), K K^T and Q K^T, the triangular solve
+// (one value column per thread), the outputs, and the state update (VB/16
+// rows x 8 columns per thread).  Everything is fp32 on the CUDA
 // cores with packed fp32x2 multiply-adds: the state must stay within 1e-4
 // relative of the fp64 recurrence, which the tensor cores' tf32 and bf16 input
 // formats do not give.  A tail chunk is padded with zero tokens (k = q = v = 0,
@@ -38,25 +39,36 @@ constexpr int PK = 128;        // key channels
 constexpr int PV = 128;        // value channels
 constexpr int PC = 32;         // tokens per chunk
 constexpr int PTH = 256;       // threads per CTA
-constexpr int SROW = PV + 4;   // padded state row: 16-byte aligned rows, columns spread over banks
 constexpr int KROW = PK + 4;   // padded q / k row
 constexpr int TROW = PC + 1;   // padded row of the chunk's C x C tables
+// value columns per CTA: each (sequence, head) pair is split over PV / VB CTAs,
+// one per column block (the triangular solve, the outputs and the state update
+// are independent per value column; K K^T and Q K^T are recomputed by each).
+// 64 columns halve the shared memory (86 KB) and the registers (126), so two
+// CTAs share an SM: 5-13 % faster than one 128-column CTA per pair.
+#ifndef LAR_PF_VB
+#define LAR_PF_VB 64
+#endif
 
-// shared-memory layout, in floats
-constexpr int OFF_S = 0;                       // S [K][SROW]
-constexpr int OFF_K = OFF_S + PK * SROW;       // k rows [C][KROW]
-constexpr int OFF_Q = OFF_K + PC * KROW;       // q rows [C][KROW]
-constexpr int OFF_D = OFF_Q + PC * KROW;       // v rows, then the right-hand sides, then d [C][V]
-constexpr int OFF_A = OFF_D + PC * PV;         // beta_t P[t][s] (k_t . k_s), s < t  [C][TROW]
-constexpr int OFF_M = OFF_A + PC * TROW;       // decay table, then P[t][s] (q_t . k_s), s <= t  [C][TROW]
-constexpr int OFF_AF = OFF_M + PC * TROW;      // a_t
-constexpr int OFF_E = OFF_AF + PC;             // E_t
-constexpr int OFF_W = OFF_E + PC;              // P[C-1][s]
-constexpr int OFF_B = OFF_W + PC;              // beta_t
-constexpr int SMEM_FLOATS = OFF_B + PC;
-constexpr size_t kPrefillSmem = static_cast<size_t>(SMEM_FLOATS) * sizeof(float);
-static_assert(OFF_K % 4 == 0 && OFF_Q % 4 == 0 && OFF_D % 4 == 0 && OFF_A % 4 == 0, "16-byte aligned blocks");
-static_assert(kPrefillSmem <= 227 * 1024, "fits one CTA's shared memory");
+// shared-memory layout for VB value columns per CTA, in floats
+template <int VB>
+struct PfLayout {
+    static constexpr int SROW = VB + 4;                  // padded state row
+    static constexpr int OFF_S = 0;                      // S [K][SROW]
+    static constexpr int OFF_K = OFF_S + PK * SROW;      // k rows [C][KROW]
+    static constexpr int OFF_Q = OFF_K + PC * KROW;      // q rows [C][KROW]
+    static constexpr int OFF_D = OFF_Q + PC * KROW;      // v rows, then right-hand sides, then d [C][VB]
+    static constexpr int OFF_A = OFF_D + PC * VB;        // beta_t P[t][s] (k_t . k_s), s < t  [C][TROW]
+    static constexpr int OFF_M = OFF_A + PC * TROW;      // decay table, then P[t][s] (q_t . k_s)  [C][TROW]
+    static constexpr int OFF_AF = OFF_M + PC * TROW;     // a_t
+    static constexpr int OFF_E = OFF_AF + PC;            // E_t
+    static constexpr int OFF_W = OFF_E + PC;             // P[C-1][s]
+    static constexpr int OFF_B = OFF_W + PC;             // beta_t
+    static constexpr int FLOATS = OFF_B + PC;
+    static constexpr size_t BYTES = static_cast<size_t>(FLOATS) * sizeof(float);
+    static_assert(OFF_K % 4 == 0 && OFF_Q % 4 == 0 && OFF_D % 4 == 0 && OFF_A % 4 == 0, "16-byte aligned blocks");
+    static_assert(BYTES <= 227 * 1024, "fits one CTA's shared memory");
+};
 
 __device__ __forceinline__ float comp(const float4& x, int i) {
     return i == 0 ? x.x : (i == 1 ? x.y : (i == 2 ? x.z : x.w));
@@ -64,24 +76,32 @@ __device__ __forceinline__ float comp(const float4& x, int i) {
 
 __device__ __forceinline__ float2 dup(float x) { return make_float2(x, x); }
 
-template <int FORM, int SB>
-__global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
+template <int FORM, int SB, int VB>
+__global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const DecodeParams p) {
+    using LY = PfLayout<VB>;
+    constexpr int SROW = LY::SROW;
     extern __shared__ __align__(16) float sm[];
-    float* S = sm + OFF_S;
-    float* Kc = sm + OFF_K;
-    float* Qc = sm + OFF_Q;
-    float* D = sm + OFF_D;
-    float* A = sm + OFF_A;
-    float* M = sm + OFF_M;
-    float* Af = sm + OFF_AF;
-    float* E = sm + OFF_E;
-    float* Wd = sm + OFF_W;
-    float* Bt = sm + OFF_B;
+    float* S = sm + LY::OFF_S;
+    float* Kc = sm + LY::OFF_K;
+    float* Qc = sm + LY::OFF_Q;
+    float* D = sm + LY::OFF_D;
+    float* A = sm + LY::OFF_A;
+    float* M = sm + LY::OFF_M;
+    float* Af = sm + LY::OFF_AF;
+    float* E = sm + LY::OFF_E;
+    float* Wd = sm + LY::OFF_W;
+    float* Bt = sm + LY::OFF_B;
 
+    constexpr int NSPLIT = PV / VB;        // CTAs per (sequence, head) pair, one per column block
+    constexpr int CP = VB / 32;            // columns per thread in the products and outputs (2 or 4)
+    constexpr int CP2 = CP / 2;            // ... as float pairs
+    constexpr int RK = VB / 16;            // state rows per thread in the update (8 columns each)
+    constexpr int VX = VB / 8;             // threads across the columns in the update
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const int hv = blockIdx.x;
+    const int hv = blockIdx.x / NSPLIT;
+    const int v0 = (blockIdx.x % NSPLIT) * VB;
     const int n = blockIdx.y;
     const int h = hv / p.group;
     constexpr int EPC = 16 / SB;     // pool elements per 16-byte chunk
@@ -91,8 +111,6 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 #endif
-    // ---- span and slots (a span that is reversed or runs past the token
-    // arrays is run as empty and flagged, as in the decode kernel)
     const int64_t lo = ld_idx(p.cu, n * p.cu_s, p.cu_dt);
     const int64_t hi = ld_idx(p.cu, (n + 1) * p.cu_s, p.cu_dt);
     const bool span_ok = lo >= 0 && hi >= lo && hi <= p.ntok;
@@ -102,33 +120,35 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
     const int64_t w = p.widx ? ld_idx(p.widx, n * p.wi_s, p.wi_dt) : r;
     const bool rd = r >= 0 && r < p.P;
     const bool wr = w >= 0 && w < p.P;
-    if (tid == 0 && hv == 0 && p.dev_err) {
+    if (tid == 0 && blockIdx.x == 0 && p.dev_err) {
         const int e = (r >= p.P ? LAR_DEVERR_READ_SLOT : 0) | (w >= p.P ? LAR_DEVERR_WRITE_SLOT : 0) |
                       (span_ok ? 0 : LAR_DEVERR_SEQLEN);
         if (e) atomicOr(p.dev_err, e);
     }
 
-    // ---- S[k][v] = pool[r][hv][v][k]; a warp reads 32 rows at one chunk offset
-    // and writes 32 consecutive columns of S
+    // ---- S[k][v] = pool[r][hv][v0 + v][k] for the CTA's VB columns
     {
         const unsigned char* base =
             static_cast<const unsigned char*>(p.pool) + ((rd ? r : 0) * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1]) * SB;
-        constexpr int NB = 8;   // chunks in flight per thread
-        static_assert((PV * NCHK) % (NB * PTH) == 0, "whole batches");
+        constexpr int TOT = VB * NCHK;
+        constexpr int NB = TOT / PTH < 8 ? TOT / PTH : 8;   // chunks in flight per thread
+        static_assert(TOT % (NB * PTH) == 0, "whole batches");
 #pragma unroll 1
-        for (int i0 = tid; i0 < PV * NCHK; i0 += NB * PTH) {
+        for (int i0 = tid; i0 < TOT; i0 += NB * PTH) {
             uint4 raw[NB];
 #pragma unroll
             for (int j = 0; j < NB; ++j) {
                 const int i = i0 + j * PTH;
                 raw[j] = make_uint4(0u, 0u, 0u, 0u);
-                if (rd) raw[j] = __ldg(reinterpret_cast<const uint4*>(base + static_cast<int64_t>(i % PV) * p.ps[2] * SB) + i / PV);
+                if (rd)
+                    raw[j] = __ldg(reinterpret_cast<const uint4*>(base + static_cast<int64_t>(v0 + i % VB) * p.ps[2] * SB) +
+                                   i / VB);
             }
 #pragma unroll
             for (int j = 0; j < NB; ++j) {
                 const int i = i0 + j * PTH;
-                const int v = i % PV;
-                const int c = i / PV;
+                const int v = i % VB;
+                const int c = i / VB;
                 const unsigned wd[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
                 if constexpr (SB == 4) {
 #pragma unroll
@@ -148,15 +168,10 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
     const bool l2 = FORM != FORM_LA && (p.flags & LAR_QK_L2NORM) != 0;
     const bool gate_raw = (p.flags & LAR_GATE_RAW) != 0;
     const bool beta_raw = (p.flags & LAR_BETA_RAW) != 0;
-    const int ty = tid >> 5, tx = tid & 31;   // products and outputs: rows 4ty.., columns 4tx..
+    const int ty = tid >> 5, tx = tid & 31;   // products and outputs: rows 4ty.., columns CP tx..
 
-    // A chunk's q, k, v, gate and beta values are loaded into registers, every
-    // load of a thread issued before any is used.  q, k: one warp per row
-    // (rows warp, warp + 8, ...), 4 channels per lane; v: 16 values per thread;
-    // gates and betas: lane t of warp 0.  (Loading the next chunk's values
-    // during the current chunk's arithmetic measured no faster.)
     constexpr int RPW = PC / (PTH / 32);   // q / k rows per warp
-    constexpr int VPT = PC * PV / PTH;     // v values per thread
+    constexpr int VPT = PC * VB / PTH;     // v values per thread
     float qx[RPW][4], kx[RPW][4], vx[VPT], gx = 0.f, bx = 0.f;
     auto fetch = [&](int64_t c0) {
         const int Lc = static_cast<int>(L - c0 < PC ? L - c0 : PC);
@@ -175,10 +190,10 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int i = tid + j * PTH;
-            const int t = i / PV;
-            const int v = i - t * PV;
-            vx[j] = t < Lc ? ld_in(p.v, (tb + c0 + t) * p.vs[1] + static_cast<int64_t>(hv) * p.vs[2] + v * p.vs[3],
-                                   p.v_dt)
+            const int t = i / VB;
+            const int v = i - t * VB;
+            vx[j] = t < Lc ? ld_in(p.v, (tb + c0 + t) * p.vs[1] + static_cast<int64_t>(hv) * p.vs[2] +
+                                           (v0 + v) * p.vs[3], p.v_dt)
                            : 0.f;
         }
         if constexpr (FORM != FORM_LA) {
@@ -194,8 +209,6 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
     for (int64_t c0 = 0; c0 < L; c0 += PC) {
         const int Lc = static_cast<int>(L - c0 < PC ? L - c0 : PC);
         fetch(c0);
-
-        // ---- the chunk's q, k (l2-normalised when asked) and v rows into shared memory
 #pragma unroll
         for (int j = 0; j < RPW; ++j) {
             const int t = warp + j * (PTH / 32);
@@ -222,10 +235,9 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
         }
 #pragma unroll
         for (int j = 0; j < VPT; ++j) D[tid + j * PTH] = vx[j];
-        // ---- per-token decay factors and betas (warp 0, lane t), then the decay table
         if (warp == 0) {
             const int t = lane;
-            float a = 1.f, bt = 0.f;   // padding tokens: no decay, no update
+            float a = 1.f, bt = 0.f;
             if (t < Lc) {
                 if constexpr (FORM == FORM_LA) {
                     a = p.decay[h * p.dec_s];
@@ -243,7 +255,6 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
             Af[t] = a;
             Bt[t] = bt;
             __syncwarp();
-            // row t of the decay table: P[t][s] = a_{s+1} ... a_t for s <= t, 0 above
             float f = 1.f;
 #pragma unroll 1
             for (int s = PC - 1; s >= 0; --s) {
@@ -254,7 +265,7 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
                     M[t * TROW + s] = 0.f;
                 }
             }
-            E[t] = f;   // a_0 ... a_t
+            E[t] = f;
             if (t == PC - 1) {
 #pragma unroll 1
                 for (int s = 0; s < PC; ++s) Wd[s] = M[t * TROW + s];
@@ -262,13 +273,14 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
         }
         __syncthreads();
 
-        // ---- K S0 and Q S0, 4 rows x 4 columns per thread; right-hand sides and
-        // the first output term
-        float2 oq[4][2];
+        // ---- K S0 and Q S0: rows 4ty..4ty+3, columns CP tx .. CP tx + CP - 1
+        float2 oq[4][CP2];
         {
-            float2 ak[4][2], aq[4][2];
+            float2 ak[4][CP2], aq[4][CP2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) ak[i][0] = ak[i][1] = aq[i][0] = aq[i][1] = make_float2(0.f, 0.f);
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int c = 0; c < CP2; ++c) ak[i][c] = aq[i][c] = make_float2(0.f, 0.f);
 #pragma unroll 2
             for (int k = 0; k < PK; k += 4) {
                 float4 kr[4], qr[4];
@@ -279,18 +291,24 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
                 }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const float4 s4 = *reinterpret_cast<const float4*>(S + (k + kk) * SROW + 4 * tx);
-                    const float2 s01 = make_float2(s4.x, s4.y), s23 = make_float2(s4.z, s4.w);
+                    float2 sv[CP2];
+                    if constexpr (CP == 4) {
+                        const float4 s4 = *reinterpret_cast<const float4*>(S + (k + kk) * SROW + 4 * tx);
+                        sv[0] = make_float2(s4.x, s4.y);
+                        sv[CP2 - 1] = make_float2(s4.z, s4.w);
+                    } else {
+                        sv[0] = *reinterpret_cast<const float2*>(S + (k + kk) * SROW + 2 * tx);
+                    }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         if constexpr (FORM != FORM_LA) {
                             const float2 kv = dup(comp(kr[i], kk));
-                            ak[i][0] = __ffma2_rn(kv, s01, ak[i][0]);
-                            ak[i][1] = __ffma2_rn(kv, s23, ak[i][1]);
+#pragma unroll
+                            for (int c = 0; c < CP2; ++c) ak[i][c] = __ffma2_rn(kv, sv[c], ak[i][c]);
                         }
                         const float2 qv = dup(comp(qr[i], kk));
-                        aq[i][0] = __ffma2_rn(qv, s01, aq[i][0]);
-                        aq[i][1] = __ffma2_rn(qv, s23, aq[i][1]);
+#pragma unroll
+                        for (int c = 0; c < CP2; ++c) aq[i][c] = __ffma2_rn(qv, sv[c], aq[i][c]);
                     }
                 }
             }
@@ -298,15 +316,16 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
             for (int i = 0; i < 4; ++i) {
                 const int t = 4 * ty + i;
                 const float2 et = dup(E[t]);
-                oq[i][0] = __fmul2_rn(et, aq[i][0]);
-                oq[i][1] = __fmul2_rn(et, aq[i][1]);
+#pragma unroll
+                for (int c = 0; c < CP2; ++c) oq[i][c] = __fmul2_rn(et, aq[i][c]);
                 if constexpr (FORM != FORM_LA) {
-                    // right-hand side beta_t (v_t - E_t (S0^T k_t)), in place of v_t
-                    float4* dp = reinterpret_cast<float4*>(D + t * PV + 4 * tx);
-                    const float4 d4 = *dp;
                     const float b = Bt[t], e = E[t];
-                    *dp = make_float4(b * fmaf(-e, ak[i][0].x, d4.x), b * fmaf(-e, ak[i][0].y, d4.y),
-                                      b * fmaf(-e, ak[i][1].x, d4.z), b * fmaf(-e, ak[i][1].y, d4.w));
+#pragma unroll
+                    for (int c = 0; c < CP2; ++c) {
+                        float2* dp = reinterpret_cast<float2*>(D + t * VB + CP * tx + 2 * c);
+                        const float2 d2 = *dp;
+                        *dp = make_float2(b * fmaf(-e, ak[i][c].x, d2.x), b * fmaf(-e, ak[i][c].y, d2.y));
+                    }
                 }
             }
         }
@@ -331,21 +350,20 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int s = sg + 8 * j;
-                const float pd = M[t * TROW + s];   // decay table entry (0 above the diagonal)
+                const float pd = M[t * TROW + s];
                 if constexpr (FORM != FORM_LA) A[t * TROW + s] = s < t ? bt * pd * kk[j] : 0.f;
                 M[t * TROW + s] = pd * qk[j];
             }
         }
         __syncthreads();
 
-        // ---- triangular solve for the corrections d, one value column per thread
+        // ---- triangular solve, one value column per thread
         if constexpr (FORM != FORM_LA) {
-            if (tid < PV) {
+            if (tid < VB) {
                 float d[PC];
 #pragma unroll
                 for (int t = 0; t < PC; ++t) {
-                    // two partial sums halve the dependent chain
-                    float acc0 = D[t * PV + tid], acc1 = 0.f;
+                    float acc0 = D[t * VB + tid], acc1 = 0.f;
 #pragma unroll
                     for (int s = 0; s + 1 < t; s += 2) {
                         acc0 = fmaf(-A[t * TROW + s], d[s], acc0);
@@ -355,22 +373,23 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
                     d[t] = acc0 + acc1;
                 }
 #pragma unroll
-                for (int t = 0; t < PC; ++t) D[t * PV + tid] = d[t];
+                for (int t = 0; t < PC; ++t) D[t * VB + tid] = d[t];
             }
             __syncthreads();
         }
 
-        // ---- outputs o_t = E_t S0^T q_t + sum_{s<=t} P[t][s] (q_t . k_s) d_s
+        // ---- outputs
         {
 #pragma unroll 4
             for (int s = 0; s < PC; ++s) {
-                const float4 d4 = *reinterpret_cast<const float4*>(D + s * PV + 4 * tx);
-                const float2 d01 = make_float2(d4.x, d4.y), d23 = make_float2(d4.z, d4.w);
+                float2 dv[CP2];
+#pragma unroll
+                for (int c = 0; c < CP2; ++c) dv[c] = *reinterpret_cast<const float2*>(D + s * VB + CP * tx + 2 * c);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float2 m = dup(M[(4 * ty + i) * TROW + s]);
-                    oq[i][0] = __ffma2_rn(m, d01, oq[i][0]);
-                    oq[i][1] = __ffma2_rn(m, d23, oq[i][1]);
+#pragma unroll
+                    for (int c = 0; c < CP2; ++c) oq[i][c] = __ffma2_rn(m, dv[c], oq[i][c]);
                 }
             }
             const bool obf = p.out_dt == LAR_BF16;
@@ -379,37 +398,46 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
                 const int t = 4 * ty + i;
                 if (t < Lc) {
                     const int64_t base = (tb + c0 + t) * p.os[1] + static_cast<int64_t>(hv) * p.os[2];
-                    const float o4[4] = {oq[i][0].x, oq[i][0].y, oq[i][1].x, oq[i][1].y};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int64_t off = base + (4 * tx + e) * p.os[3];
-                        if (obf) static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(o4[e] * p.scale);
-                        else static_cast<float*>(p.out)[off] = o4[e] * p.scale;
+                    for (int c = 0; c < CP2; ++c) {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float o = e == 0 ? oq[i][c].x : oq[i][c].y;
+                            const int64_t off = base + (v0 + CP * tx + 2 * c + e) * p.os[3];
+                            if (obf) static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(o * p.scale);
+                            else static_cast<float*>(p.out)[off] = o * p.scale;
+                        }
                     }
                 }
             }
         }
 
-        // ---- state update S = E_{C-1} S0 + sum_s P[C-1][s] k_s d_s^T, 8 x 8 entries per thread
+        // ---- state update: rows RK ky .., 8 columns 8vx .. per thread
         {
-            const int ky = tid >> 4, vx = tid & 15;   // rows k = 8ky.., columns v = 8vx..
-            float2 acc[8][4];
+            const int ky = tid / VX, vx8 = tid % VX;
+            float2 acc[RK][4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < RK; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
 #pragma unroll 2
             for (int s = 0; s < PC; ++s) {
                 const float2 ws = dup(Wd[s]);
-                const float4 k0 = *reinterpret_cast<const float4*>(Kc + s * KROW + 8 * ky);
-                const float4 k1 = *reinterpret_cast<const float4*>(Kc + s * KROW + 8 * ky + 4);
-                const float4 d0 = *reinterpret_cast<const float4*>(D + s * PV + 8 * vx);
-                const float4 d1 = *reinterpret_cast<const float4*>(D + s * PV + 8 * vx + 4);
+                float kv[RK];
+#pragma unroll
+                for (int i4 = 0; i4 < RK / 4; ++i4) {
+                    const float4 k4 = *reinterpret_cast<const float4*>(Kc + s * KROW + RK * ky + 4 * i4);
+                    kv[4 * i4] = k4.x;
+                    kv[4 * i4 + 1] = k4.y;
+                    kv[4 * i4 + 2] = k4.z;
+                    kv[4 * i4 + 3] = k4.w;
+                }
+                const float4 d0 = *reinterpret_cast<const float4*>(D + s * VB + 8 * vx8);
+                const float4 d1 = *reinterpret_cast<const float4*>(D + s * VB + 8 * vx8 + 4);
                 const float2 dd[4] = {__fmul2_rn(ws, make_float2(d0.x, d0.y)), __fmul2_rn(ws, make_float2(d0.z, d0.w)),
                                       __fmul2_rn(ws, make_float2(d1.x, d1.y)), __fmul2_rn(ws, make_float2(d1.z, d1.w))};
-                const float kv[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < RK; ++i) {
                     const float2 k2 = dup(kv[i]);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc[i][j] = __ffma2_rn(k2, dd[j], acc[i][j]);
@@ -417,8 +445,8 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
             }
             const float2 ec = dup(E[PC - 1]);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float4* sp = reinterpret_cast<float4*>(S + (8 * ky + i) * SROW + 8 * vx);
+            for (int i = 0; i < RK; ++i) {
+                float4* sp = reinterpret_cast<float4*>(S + (RK * ky + i) * SROW + 8 * vx8);
                 const float4 s0 = sp[0], s1 = sp[1];
                 const float2 n0 = __ffma2_rn(ec, make_float2(s0.x, s0.y), acc[i][0]);
                 const float2 n1 = __ffma2_rn(ec, make_float2(s0.z, s0.w), acc[i][1]);
@@ -431,14 +459,14 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
         __syncthreads();
     }
 
-    // ---- pool[w][hv][v][k] = S[k][v] (skipped for a negative or out-of-range slot)
+    // ---- pool[w][hv][v0 + v][k] = S[k][v]
     if (wr) {
         unsigned char* base =
             static_cast<unsigned char*>(p.pool) + (w * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1]) * SB;
-        for (int i = tid; i < PV * NCHK; i += PTH) {
-            const int v = i % PV;
-            const int c = i / PV;
-            uint4* dst = reinterpret_cast<uint4*>(base + static_cast<int64_t>(v) * p.ps[2] * SB) + c;
+        for (int i = tid; i < VB * NCHK; i += PTH) {
+            const int v = i % VB;
+            const int c = i / VB;
+            uint4* dst = reinterpret_cast<uint4*>(base + static_cast<int64_t>(v0 + v) * p.ps[2] * SB) + c;
             if constexpr (SB == 4) {
                 __stcs(dst, make_uint4(__float_as_uint(S[(c * 4) * SROW + v]), __float_as_uint(S[(c * 4 + 1) * SROW + v]),
                                        __float_as_uint(S[(c * 4 + 2) * SROW + v]),
@@ -459,17 +487,19 @@ __global__ void __launch_bounds__(PTH, 1) prefill_kernel(const DecodeParams p) {
 
 template <int FORM, int SB>
 lar_status launch_prefill_form(const DecodeParams& p, cudaStream_t stream) {
-    auto kern = prefill_kernel<FORM, SB>;
+    constexpr int VB = LAR_PF_VB;
+    auto kern = prefill_kernel<FORM, SB, VB>;
+    constexpr size_t smem = PfLayout<VB>::BYTES;
     // the shared-memory opt-in is a per-device function attribute; setting it on
     // every call keeps it right on whichever device is current (a host-side
     // call, small next to a prefill launch)
     if (cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kPrefillSmem)) != cudaSuccess)
+                             static_cast<int>(smem)) != cudaSuccess)
         return LAR_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.HV), static_cast<unsigned>(p.B));
+    cfg.gridDim = dim3(static_cast<unsigned>(p.HV) * (PV / VB), static_cast<unsigned>(p.B));
     cfg.blockDim = dim3(PTH);
-    cfg.dynamicSmemBytes = kPrefillSmem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
 #if LAR_PDL
     cudaLaunchAttribute attr[1];

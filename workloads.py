@@ -181,6 +181,13 @@ def _draw_pool(gen, shape, seed, device, dtype=F32):
     return pool.to(dtype)
 
 
+def make_meta(name: str) -> dict:
+    """Workload flags known without drawing it (which call runs it)."""
+    if name not in CONFIGS:
+        raise KeyError(name)
+    return {"prefill": name == "gdn_prefill_n16"}
+
+
 def make(name: str, *, seed: int | None = None, pool_device="cpu",
          index_dtype=torch.int32) -> Workload:
     """Draw the named workload (see the module docstring for the recipes)."""
