@@ -75,15 +75,41 @@ _DECODE_SOURCES = ("decode_kernel.cuh", "decode_kv_kernel.cuh", "decode_gdn.cu",
 _PREFILL_SOURCES = ("prefill.cu", "decode_kernel.cuh", "decode_params.h", "lar_abi.cpp")
 
 
+def _code_only(text: str) -> str:
+    """C / C++ / CUDA source with its comments removed and its whitespace runs
+    collapsed (string and character literals kept), so that a comment edit
+    does not count as a kernel change."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            i = text.find("\n", i)
+            i = n if i < 0 else i
+        elif text.startswith("/*", i):
+            i = text.find("*/", i + 2)
+            i = n if i < 0 else i + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(config: str = "gdn_b64") -> str:
-    """Hash of the sources of the kernel a workload runs (the chunked prefill
-    kernel or the decode kernels); ncu traffic figures are valid only for it."""
+    """Hash of the code (comments aside) of the kernel a workload runs (the
+    chunked prefill kernel or the decode kernels); ncu traffic figures are
+    valid only for it."""
     prefill = config in W.CONFIGS and W.make_meta(config).get("prefill", False)
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_recurrent_gb300", "csrc")
     for name in sorted(_PREFILL_SOURCES if prefill else _DECODE_SOURCES):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:12]
 
 

@@ -108,9 +108,14 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
     constexpr int NCHK = PK / EPC;   // chunks per state row
 
 #if LAR_PDL
+    // programmatic dependent launch: everything below may read what the
+    // previous kernel on the stream wrote
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 #endif
+    // ---- span and slots (a span that is reversed or runs past the token
+    // arrays is run as empty and flagged, as in the decode kernel; one CTA of
+    // the sequence reports)
     const int64_t lo = ld_idx(p.cu, n * p.cu_s, p.cu_dt);
     const int64_t hi = ld_idx(p.cu, (n + 1) * p.cu_s, p.cu_dt);
     const bool span_ok = lo >= 0 && hi >= lo && hi <= p.ntok;
@@ -170,6 +175,12 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
     const bool beta_raw = (p.flags & LAR_BETA_RAW) != 0;
     const int ty = tid >> 5, tx = tid & 31;   // products and outputs: rows 4ty.., columns CP tx..
 
+    // A chunk's q, k, v, gate and beta values are loaded into registers, every
+    // load of a thread issued before any is used.  q, k: one warp per row
+    // (rows warp, warp + 8, ...), 4 channels per lane; v: the CTA's columns,
+    // VB / 8 values per thread; gates and betas: lane t of warp 0.  (Loading
+    // the next chunk's values during the current chunk's arithmetic measured
+    // no faster.)
     constexpr int RPW = PC / (PTH / 32);   // q / k rows per warp
     constexpr int VPT = PC * VB / PTH;     // v values per thread
     float qx[RPW][4], kx[RPW][4], vx[VPT], gx = 0.f, bx = 0.f;
@@ -209,6 +220,7 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
     for (int64_t c0 = 0; c0 < L; c0 += PC) {
         const int Lc = static_cast<int>(L - c0 < PC ? L - c0 : PC);
         fetch(c0);
+        // ---- the chunk's q, k (l2-normalised when asked) and v rows into shared memory
 #pragma unroll
         for (int j = 0; j < RPW; ++j) {
             const int t = warp + j * (PTH / 32);
@@ -235,9 +247,10 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
         }
 #pragma unroll
         for (int j = 0; j < VPT; ++j) D[tid + j * PTH] = vx[j];
+        // ---- per-token decay factors and betas (warp 0, lane t), then the decay table
         if (warp == 0) {
             const int t = lane;
-            float a = 1.f, bt = 0.f;
+            float a = 1.f, bt = 0.f;   // padding tokens: no decay, no update
             if (t < Lc) {
                 if constexpr (FORM == FORM_LA) {
                     a = p.decay[h * p.dec_s];
@@ -255,6 +268,7 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
             Af[t] = a;
             Bt[t] = bt;
             __syncwarp();
+            // row t: P[t][s] = a_{s+1} ... a_t for s <= t, 0 above
             float f = 1.f;
 #pragma unroll 1
             for (int s = PC - 1; s >= 0; --s) {
@@ -265,7 +279,7 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
                     M[t * TROW + s] = 0.f;
                 }
             }
-            E[t] = f;
+            E[t] = f;   // a_0 ... a_t
             if (t == PC - 1) {
 #pragma unroll 1
                 for (int s = 0; s < PC; ++s) Wd[s] = M[t * TROW + s];
@@ -319,6 +333,7 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
 #pragma unroll
                 for (int c = 0; c < CP2; ++c) oq[i][c] = __fmul2_rn(et, aq[i][c]);
                 if constexpr (FORM != FORM_LA) {
+                    // right-hand side beta_t (v_t - E_t (S0^T k_t)), in place of v_t
                     const float b = Bt[t], e = E[t];
 #pragma unroll
                     for (int c = 0; c < CP2; ++c) {
@@ -350,7 +365,7 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int s = sg + 8 * j;
-                const float pd = M[t * TROW + s];
+                const float pd = M[t * TROW + s];   // decay table entry (0 above the diagonal)
                 if constexpr (FORM != FORM_LA) A[t * TROW + s] = s < t ? bt * pd * kk[j] : 0.f;
                 M[t * TROW + s] = pd * qk[j];
             }
@@ -363,6 +378,7 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
                 float d[PC];
 #pragma unroll
                 for (int t = 0; t < PC; ++t) {
+                    // two partial sums halve the dependent chain
                     float acc0 = D[t * VB + tid], acc1 = 0.f;
 #pragma unroll
                     for (int s = 0; s + 1 < t; s += 2) {
@@ -378,7 +394,7 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
             __syncthreads();
         }
 
-        // ---- outputs
+        // ---- outputs o_t = E_t S0^T q_t + sum_{s<=t} P[t][s] (q_t . k_s) d_s
         {
 #pragma unroll 4
             for (int s = 0; s < PC; ++s) {
@@ -412,7 +428,8 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
             }
         }
 
-        // ---- state update: rows RK ky .., 8 columns 8vx .. per thread
+        // ---- state update S = E_{C-1} S0 + sum_s P[C-1][s] k_s d_s^T: rows RK ky ..,
+        // 8 columns 8 vx8 .. per thread
         {
             const int ky = tid / VX, vx8 = tid % VX;
             float2 acc[RK][4];
@@ -459,7 +476,7 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
         __syncthreads();
     }
 
-    // ---- pool[w][hv][v0 + v][k] = S[k][v]
+    // ---- pool[w][hv][v0 + v][k] = S[k][v] (skipped for a negative or out-of-range slot)
     if (wr) {
         unsigned char* base =
             static_cast<unsigned char*>(p.pool) + (w * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1]) * SB;

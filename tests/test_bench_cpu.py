@@ -111,3 +111,18 @@ def test_oracle_step_on_variable_length_spans():
     oracle.gdn_decode_varlen(w.q, w.k, w.v, w.g, w.beta, ref_pool, w.cu_seqlens, w.read_idx, w.write_idx)
     bench._oracle_step(w, step_pool, torch.arange(w.B))
     assert torch.equal(ref_pool, step_pool)
+
+
+def test_kernel_hash_ignores_comments_and_separates_kernels():
+    """ncu traffic figures are keyed by a hash of the kernel's code: comments
+    and whitespace do not count, string literals do, and the decode and
+    prefill kernels are hashed from their own sources."""
+    sys.path.insert(0, ROOT)
+    import bench
+    a = 'int f() { return 1; } // one\n/* two */ const char* s = "// kept";\n'
+    b = 'int f()  {  return 1; }\nconst char* s = "// kept"; // other\n'
+    c = 'int f() { return 2; }\nconst char* s = "// kept";\n'
+    assert bench._code_only(a) == bench._code_only(b) != bench._code_only(c)
+    assert '"// kept"' in bench._code_only(a)
+    assert bench.kernel_source_hash("gdn_b64") == bench.kernel_source_hash("kda_b256")
+    assert bench.kernel_source_hash("gdn_b64") != bench.kernel_source_hash("gdn_prefill_n16")
