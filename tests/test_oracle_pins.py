@@ -608,3 +608,77 @@ def test_varlen_empty_and_bad_spans():
     one = oracle.gdn_decode(q[None, 2:5], k[None, 2:5], v[None, 2:5], g[None, 2:5], beta[None, 2:5],
                             before.clone(), torch.tensor([2]), torch.tensor([-1]))
     assert np.array_equal(res["out"][2:5], one["out"][0])
+
+
+# --------------------------------------------------------------------------- chunked (matrix) form
+
+def _chunked_delta_rule(S0, q, k, v, a, beta, C):
+    """The delta rule over T tokens in chunks of C, written as matrix products
+    (numpy, fp64): per chunk, with P[t][s] = a_{s+1}..a_t and E_t = a_0..a_t,
+    (I + tril_-1(beta_t P[t][s] k_t.k_s)) d = beta (v - E K S0),
+    O = E Q S0 + (P o tril(Q K^T)) d,  S = E_last S0 + K^T (P[last][:] d).
+    S0 is K x V; q, k [T, K]; v [T, V]; a (decay factors), beta [T]."""
+    S = S0.copy()
+    outs = []
+    for c0 in range(0, len(a), C):
+        qc, kc, vc, ac, bc = q[c0:c0 + C], k[c0:c0 + C], v[c0:c0 + C], a[c0:c0 + C], beta[c0:c0 + C]
+        n = len(ac)
+        P = np.zeros((n, n))
+        for t in range(n):
+            for s in range(t + 1):
+                P[t, s] = np.prod(ac[s + 1:t + 1])
+        E = np.cumprod(ac)
+        A = np.tril(bc[:, None] * P * (kc @ kc.T), -1)
+        R = bc[:, None] * (vc - E[:, None] * (kc @ S))
+        d = np.linalg.solve(np.eye(n) + A, R)
+        outs.append(E[:, None] * (qc @ S) + (P * (qc @ kc.T)) @ d)
+        S = E[-1] * S + kc.T @ (P[-1][:, None] * d)
+    return np.concatenate(outs), S
+
+
+@pytest.mark.parametrize("C", [1, 4, 5, 16])
+def test_delta_rule_matches_chunked_matrix_form(C):
+    """The oracle's token-by-token delta rule equals the chunked matrix form
+    (numpy solve and matmuls, any chunk size) on 11 tokens: outputs and final
+    state to fp64 rounding.  With C = 1 the form reduces to the recurrence; with
+    C > 1 it pins the decay / read-out / update order across a chunk."""
+    gen = torch.Generator().manual_seed(81)
+    T, K, V = 11, 6, 5
+    q = torch.randn(1, T, 1, K, generator=gen, dtype=torch.float64)
+    k = F.normalize(torch.randn(1, T, 1, K, generator=gen, dtype=torch.float64), dim=-1)
+    v = torch.randn(1, T, 1, V, generator=gen, dtype=torch.float64)
+    g = -torch.rand(1, T, 1, generator=gen, dtype=torch.float64)
+    beta = torch.rand(1, T, 1, generator=gen, dtype=torch.float64)
+    pool = torch.randn(2, 1, V, K, generator=gen, dtype=torch.float64).float()
+    res = oracle.gdn_decode(q, k, v, g, beta, pool.clone(), torch.tensor([1]), torch.tensor([-1]))
+    S0 = pool[1, 0].double().numpy().T                       # K x V
+    o, S = _chunked_delta_rule(S0, q[0, :, 0].numpy(), k[0, :, 0].numpy(), v[0, :, 0].numpy(),
+                               np.exp(g[0, :, 0].numpy()), beta[0, :, 0].numpy(), C)
+    np.testing.assert_allclose(res["out"][0, :, 0], o, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(res["final_state"][0, 0], S.T, rtol=1e-11, atol=1e-12)
+
+
+def test_la_matches_chunked_matrix_form():
+    """Lightning Attention is the chunked form with d = v (beta = 1 and no
+    read-out correction): P and E from the constant rate lambda."""
+    gen = torch.Generator().manual_seed(82)
+    T, K, V, H = 9, 4, 3, 1
+    q = torch.randn(1, T, H, K, generator=gen, dtype=torch.float64)
+    k = torch.randn(1, T, H, K, generator=gen, dtype=torch.float64)
+    v = torch.randn(1, T, H, V, generator=gen, dtype=torch.float64)
+    lam = torch.tensor([0.8])
+    pool = torch.randn(2 * H, V, K, generator=gen, dtype=torch.float64).float()
+    res = oracle.la_decode(q, k, v, lam, pool.clone(), torch.tensor([1]), torch.tensor([-1]))
+    S = pool[1].double().numpy().T
+    a = np.full(T, float(lam[0]))
+    outs = []
+    C = 4
+    for c0 in range(0, T, C):
+        qc, kc, vc, ac = q[0, c0:c0 + C, 0].numpy(), k[0, c0:c0 + C, 0].numpy(), v[0, c0:c0 + C, 0].numpy(), a[c0:c0 + C]
+        n = len(ac)
+        P = np.array([[np.prod(ac[s + 1:t + 1]) if s <= t else 0.0 for s in range(n)] for t in range(n)])
+        E = np.cumprod(ac)
+        outs.append(E[:, None] * (qc @ S) + (P * (qc @ kc.T)) @ vc)
+        S = E[-1] * S + kc.T @ (P[-1][:, None] * vc)
+    np.testing.assert_allclose(res["out"][0, :, 0], np.concatenate(outs), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(res["final_state"][0, 0], S.T, rtol=1e-11, atol=1e-12)
