@@ -8,6 +8,14 @@
  *   kda_decode  gated delta rule, decay per key channel
  *   la_decode   Lightning Attention: decay per head, no delta term
  *
+ * with variants for per-token pool slots (gdn_decode_tokens, kda_decode_tokens),
+ * token-major spans of any length per sequence (gdn_decode_varlen,
+ * kda_decode_varlen, la_decode_varlen) and the chunked form of the latter for
+ * long spans (gdn_prefill, la_prefill).  The chunked calls also set their
+ * kernel's shared-memory limit (a function attribute) on every call; capturing
+ * them into a CUDA graph has not been tested (the other calls' capture and
+ * replay are).
+ *
  * The delta-rule recurrence is the one the ROCm/aiter PR #4584 "Fused Gluon KDA
  * decode path" advisory review states: per token
  *     S <- exp(g_t) S;   S <- S + beta_t k_t (x) (v_t - S^T k_t);   o_t = S^T q_t
