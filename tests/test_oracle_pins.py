@@ -682,3 +682,45 @@ def test_la_matches_chunked_matrix_form():
         S = E[-1] * S + kc.T @ (P[-1][:, None] * vc)
     np.testing.assert_allclose(res["out"][0, :, 0], np.concatenate(outs), rtol=1e-11, atol=1e-12)
     np.testing.assert_allclose(res["final_state"][0, 0], S.T, rtol=1e-11, atol=1e-12)
+
+
+def test_kda_matches_per_channel_chunked_form():
+    """KDA (decay per key channel) equals its chunked form: with per-channel
+    decay products P[t][s][k] = a_{s+1}[k]..a_t[k] and E_t[k] = a_0[k]..a_t[k],
+    A[t][s] = beta_t sum_k k_t[k] P[t][s][k] k_s[k] (s < t),
+    (I + A) d = beta (v - (E o K) S0),  o_t = (E_t o q_t) S0 + sum_{s<=t} (q_t . (P[t][s] o k_s)) d_s,
+    S = diag(E_last) S0 + sum_s (P[last][s] o k_s) d_s^T  (numpy, fp64, chunk 4 over 10 tokens)."""
+    gen = torch.Generator().manual_seed(83)
+    T, K, V, C = 10, 5, 4, 4
+    q = torch.randn(1, T, 1, K, generator=gen, dtype=torch.float64)
+    k = F.normalize(torch.randn(1, T, 1, K, generator=gen, dtype=torch.float64), dim=-1)
+    v = torch.randn(1, T, 1, V, generator=gen, dtype=torch.float64)
+    g = -torch.rand(1, T, 1, K, generator=gen, dtype=torch.float64)
+    beta = torch.rand(1, T, 1, generator=gen, dtype=torch.float64)
+    pool = torch.randn(2, 1, V, K, generator=gen, dtype=torch.float64).float()
+    res = oracle.kda_decode(q, k, v, g, beta, pool.clone(), torch.tensor([1]), torch.tensor([-1]))
+    S = pool[1, 0].double().numpy().T                        # K x V
+    qn, kn, vn = q[0, :, 0].numpy(), k[0, :, 0].numpy(), v[0, :, 0].numpy()
+    an, bn = np.exp(g[0, :, 0].numpy()), beta[0, :, 0].numpy()
+    outs = []
+    for c0 in range(0, T, C):
+        qc, kc, vc, ac, bc = qn[c0:c0 + C], kn[c0:c0 + C], vn[c0:c0 + C], an[c0:c0 + C], bn[c0:c0 + C]
+        n = len(bc)
+        P = np.zeros((n, n, K))
+        for t in range(n):
+            for s in range(t + 1):
+                P[t, s] = np.prod(ac[s + 1:t + 1], axis=0) if t > s else np.ones(K)
+        E = np.cumprod(ac, axis=0)                            # [n, K]
+        A = np.zeros((n, n))
+        Mq = np.zeros((n, n))
+        for t in range(n):
+            for s in range(t + 1):
+                if s < t:
+                    A[t, s] = bc[t] * np.sum(kc[t] * P[t, s] * kc[s])
+                Mq[t, s] = np.sum(qc[t] * P[t, s] * kc[s])
+        R = bc[:, None] * (vc - (E * kc) @ S)
+        d = np.linalg.solve(np.eye(n) + A, R)
+        outs.append((E * qc) @ S + Mq @ d)
+        S = E[-1][:, None] * S + (P[-1] * kc).T @ d
+    np.testing.assert_allclose(res["out"][0, :, 0], np.concatenate(outs), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(res["final_state"][0, 0], S.T, rtol=1e-11, atol=1e-12)
