@@ -64,6 +64,8 @@ DESCRIPTIONS = {
                       "1159 tokens) H=16 HV=32 K=V=128, bf16 q/k/v/out, fp32 pool [256,32,128,128]",
     "gdn_prefill_n16": "GDN chunked prefill, N=16 spans of 256-1024 tokens (11094 tokens) H=16 HV=32 K=V=128, "
                        "bf16 q/k/v/out, fp32 pool [64,32,128,128]",
+    "kda_prefill_n16": "KDA chunked prefill, N=16 spans of 256-1024 tokens H=HV=24 K=V=128, raw bf16 q/k/a "
+                       "(gate chain, l2 norm, sigmoid in kernel), fp32 pool [64,24,128,128]",
     "la_b512_packed": "Lightning-Attention decode B=512 T=1 H=64 K=V=128, packed bf16 QKV, "
                       "flat pool [640*64,128,128]",
 }
@@ -241,7 +243,13 @@ def max_over_ranks(x: float, world: int, device) -> float:
 
 def device_inputs(w, dev):
     cu = lambda t: None if t is None else t.to(dev)
-    d = {"q": cu(w.q), "k": cu(w.k), "v": cu(w.v), "pool": w.pool if w.pool.is_cuda else w.pool.to(dev)}
+    q, k, v = w.qkv_to(dev)    # packed workloads: slices of one fused device buffer
+    if w.fused is not None:
+        es = q.element_size()
+        if not (q.stride() == k.stride() == w.q.stride() and k.data_ptr() == q.data_ptr() + w.K * es
+                and v.data_ptr() == q.data_ptr() + 2 * w.K * es):
+            raise RuntimeError("packed q/k/v did not reach the device as views of one buffer")
+    d = {"q": q, "k": k, "v": v, "pool": w.pool if w.pool.is_cuda else w.pool.to(dev)}
     if w.form == "la":
         d["decay"] = cu(w.decay)
     else:
@@ -357,7 +365,9 @@ def run_lar(args, world, rank, local):
                    "l2": (f"rotating {n_sets} disjoint slot sets "
                           f"({n_sets * w.B * w.HV * w.K * w.V * w.pool.element_size() / 2**20:.0f} MiB of state), "
                           "inputs larger than L2" if n_sets > 1 else "inputs larger than L2"),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   **({"qkv": f"head-dim slices of one fused device buffer, row stride {d['q'].stride()[-2]}"}
+                      if w.fused is not None else {})},
         "tokens_per_s": round(tokens, 1),
         "pct_of_8tbs": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_peak": round(100 * gbs / world / peak, 2),
@@ -398,50 +408,56 @@ def run_e2e(w, d, sets, dev, stream, args):
     one pinned-host -> device copy of all of the step's inputs (q, k, v, the
     gates and slot indices, packed back to back as a serving loop would stage
     them), one decode call through `PreparedCall`, a device -> host copy of
-    the output, and a stream synchronize.  The pool stays resident."""
+    the output, and a stream synchronize.  The pool stays resident; the steps
+    rotate over the same disjoint slot sets as the device-timed arm, so no step
+    finds its state in L2."""
     import linear_attention_recurrent_gb300 as lar
 
     names = ["q", "k", "v"] + (["decay"] if w.form == "la" else ["g", "beta"])
-    ri, wi = sets[0]
-    host_parts = {n: getattr(w, n).contiguous() for n in names if getattr(w, n) is not None}
-    if w.state_idx is not None:
-        host_parts["state_idx"] = w.state_idx.contiguous()
-        if w.num_accepted is not None:
-            host_parts["num_accepted"] = w.num_accepted.contiguous()
-        else:
-            host_parts["read_idx"] = ri.contiguous()
-    else:
-        host_parts["read_idx"] = ri.contiguous()
-        host_parts["write_idx"] = wi.contiguous()
-    if w.cu_seqlens is not None:
-        host_parts["cu_seqlens"] = w.cu_seqlens.contiguous()
-    offs, total = {}, 0
-    for n, t in host_parts.items():
-        offs[n] = total
-        total += (t.numel() * t.element_size() + 255) // 256 * 256
-    hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
-    dbuf = torch.empty(total, dtype=torch.uint8, device=dev)
-    views = {}
-    for n, t in host_parts.items():
-        nb = t.numel() * t.element_size()
-        hbuf[offs[n]:offs[n] + nb].copy_(t.view(-1).view(torch.uint8))
-        views[n] = dbuf[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
     out_dev = torch.empty(w.v.shape, dtype=w.out_dtype, device=dev)
     out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
     inter = (torch.empty(inter_shape(w), device=dev, dtype=w.inter_dtype)
              if w.cache_intermediate else None)
-    kw = dict(views, pool=d["pool"], out=out_dev, inter=inter)
-    if w.form != "la":
-        kw.update(A_log=d.get("A_log"), dt_bias=d.get("dt_bias"), qk_l2norm=w.qk_l2norm,
-                  gate_raw=w.gate_raw, beta_raw=w.beta_raw, state_kv=w.state_kv)
-    if w.meta.get("prefill"):
-        kw.update(prefill=True)
-    call = lar.PreparedCall(w.form, scale=w.scale, stream=stream, **kw)
+    staged = []    # per slot set: (pinned host buffer, device buffer, call)
+    for ri, wi in sets:
+        host_parts = {n: getattr(w, n).contiguous() for n in names if getattr(w, n) is not None}
+        if w.state_idx is not None:
+            host_parts["state_idx"] = w.state_idx.contiguous()
+            if w.num_accepted is not None:
+                host_parts["num_accepted"] = w.num_accepted.contiguous()
+            else:
+                host_parts["read_idx"] = ri.contiguous()
+        else:
+            host_parts["read_idx"] = ri.contiguous()
+            host_parts["write_idx"] = wi.contiguous()
+        if w.cu_seqlens is not None:
+            host_parts["cu_seqlens"] = w.cu_seqlens.contiguous()
+        offs, total = {}, 0
+        for n, t in host_parts.items():
+            offs[n] = total
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
+        dbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+        views = {}
+        for n, t in host_parts.items():
+            nb = t.numel() * t.element_size()
+            hbuf[offs[n]:offs[n] + nb].copy_(t.view(-1).view(torch.uint8))
+            views[n] = dbuf[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
+        kw = dict(views, pool=d["pool"], out=out_dev, inter=inter)
+        if w.form != "la":
+            kw.update(A_log=d.get("A_log"), dt_bias=d.get("dt_bias"), qk_l2norm=w.qk_l2norm,
+                      gate_raw=w.gate_raw, beta_raw=w.beta_raw, state_kv=w.state_kv)
+        if w.meta.get("prefill"):
+            kw.update(prefill=True)
+        staged.append((hbuf, dbuf, lar.PreparedCall(w.form, scale=w.scale, stream=stream, **kw)))
     h2d = sum(t.numel() * t.element_size() for t in host_parts.values())
     d2h = out_host.numel() * out_host.element_size()
     steps = max(10, min(args.steps, 2000))
+    it = [0]
 
     def step():
+        hbuf, dbuf, call = staged[it[0] % len(staged)]
+        it[0] += 1
         with torch.cuda.stream(stream):
             dbuf.copy_(hbuf, non_blocking=True)
             call()
@@ -458,7 +474,7 @@ def run_e2e(w, d, sets, dev, stream, args):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(dt * 1e3, 4), "steps": steps,
             "tokens_per_s": round(w.tokens() / dt, 1),
-            "note": "wall clock per step: one packed pinned H2D copy of the step's inputs, the "
+            "note": "wall clock per step, rotating the slot sets: one packed pinned H2D copy of the step's inputs, the "
                     "decode call, D2H of the output, stream sync; the pool stays resident"}
 
 

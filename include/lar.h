@@ -11,7 +11,7 @@
  * with variants for per-token pool slots (gdn_decode_tokens, kda_decode_tokens),
  * token-major spans of any length per sequence (gdn_decode_varlen,
  * kda_decode_varlen, la_decode_varlen) and the chunked form of the latter for
- * long spans (gdn_prefill, la_prefill).  The chunked calls also set their
+ * long spans (gdn_prefill, kda_prefill, la_prefill).  The chunked calls also set their
  * kernel's shared-memory limit (a function attribute) on every call; capturing
  * them into a CUDA graph has not been tested (the other calls' capture and
  * replay are).
@@ -55,8 +55,12 @@
  *   K must be 16, 32, 64 or 128; V from 1 to 2^24; T from 1 to 16;
  *   B and HV at most 65535.
  *
- * Ownership and execution: the caller owns every buffer (device memory).  The
- * library allocates nothing, keeps no state between calls and never
+ * Ownership and execution: the caller owns every buffer (device memory).
+ * Every pointer of a call (tensor data and dev_err) must be memory of the
+ * CUDA device that is current on the calling thread, and `stream` a stream of
+ * that device: the kernel is launched there and dereferences the pointers
+ * as given (memory of another device is not checked here, and a kernel that
+ * touches it without peer access faults).  The library allocates nothing, keeps no state between calls and never
  * synchronises: each call validates on the host and then enqueues one kernel
  * on `stream` (a cudaStream_t; NULL is the legacy default stream).  The kernel
  * is launched with programmatic dependent launch: it may be scheduled while
@@ -71,8 +75,9 @@
  * anything is launched (nothing is written).  Slot indices >= P are caught on
  * the device: that entry's state is not read (zero state) / not written, and
  * the bits LAR_DEVERR_* are OR-ed into *dev_err when dev_err is not NULL (a
- * caller-owned device int32, never cleared by the library).  No kernel traps
- * or asserts.
+ * caller-owned device int32, 4-byte aligned (else LAR_ERR_ALIGN) and clear of
+ * every tensor of the call (else LAR_ERR_ALIAS); never cleared by the
+ * library).  No kernel traps or asserts.
  *
  * Aliasing: pool, out and inter must not overlap one another or any input
  * (checked on the host by address range).  Entries must not read a slot that
@@ -112,9 +117,10 @@ typedef enum {
     LAR_ERR_RANK = 3,        /* wrong ndim */
     LAR_ERR_SHAPE = 4,       /* shapes disagree, or a size outside the supported range */
     LAR_ERR_STRIDE = 5,      /* k stride of pool/inter not 1, or negative strides */
-    LAR_ERR_ALIGN = 6,       /* pool/inter pointer or strides not multiples of 16 bytes */
+    LAR_ERR_ALIGN = 6,       /* pool/inter pointer or strides not multiples of 16 bytes, or dev_err
+                                not 4-byte aligned */
     LAR_ERR_ARG = 7,         /* inconsistent flags/arguments (e.g. A_log without LAR_GATE_RAW) */
-    LAR_ERR_ALIAS = 8,       /* an output overlaps another output or an input */
+    LAR_ERR_ALIAS = 8,       /* an output (dev_err included) overlaps another output or an input */
     LAR_ERR_LAUNCH = 9       /* the CUDA launch itself failed */
 } lar_status;
 
@@ -131,8 +137,10 @@ enum {
     LAR_DEVERR_READ_SLOT = 1,  /* some read_idx[b] >= P (that entry started from zero) */
     LAR_DEVERR_WRITE_SLOT = 2, /* some write slot >= P (that writeback was skipped) */
     LAR_DEVERR_ACCEPTED = 4,   /* some num_accepted[b] outside [1, T] (that entry started from zero) */
-    LAR_DEVERR_SEQLEN = 8      /* varlen: some span cu_seqlens[n]..[n+1] reversed or past the token
+    LAR_DEVERR_SEQLEN = 8,     /* varlen: some span cu_seqlens[n]..[n+1] reversed or past the token
                                   arrays (treated as empty: the read state goes to the write slot) */
+    LAR_DEVERR_TIMEOUT = 16    /* chunked prefill: a bounded wait for the tensor cores gave up; that
+                                  (sequence, head) skipped the rest of its span and its writeback */
 };
 
 /*
@@ -276,13 +284,30 @@ lar_status la_decode_varlen(const lar_tensor* q, const lar_tensor* k, const lar_
  * rounding).  Every output row of a token inside a span and every written state
  * is produced; there is no per-token state cache (the chunked form never forms
  * the intermediate states).
- *   K = V = 128 only (other shapes: LAR_ERR_SHAPE; use *_decode_varlen);
- *   GDN and LA only (KDA's per-channel decay has no entry point here).
- * One CTA per (sequence, v-head) pair holds the state in shared memory for the
- * whole span, so the work of a sequence is spread over its heads; short spans
- * are served better by the *_decode_varlen calls.
+ *   K = V = 128 only (other shapes: LAR_ERR_SHAPE; use *_decode_varlen).
+ * Two CTAs per (sequence, v-head) pair, one per half of the value columns,
+ * hold the state in shared memory for the whole span, so the work of a
+ * sequence is spread over its heads; short spans are served better by the
+ * *_decode_varlen calls.
+ *
+ * kda_prefill: KDA's per-key-channel decay moves into the chunk's dot
+ * products: with P[t][s][c] = exp(g_{s+1}[c]) ... exp(g_t[c]) (products of the
+ * per-token factors, never exponentials of differences),
+ *     A[t][s] = beta_t sum_c k_t[c] k_s[c] P[t][s][c]  (s < t),
+ *     o_t = sum_c q_t[c] E_t[c] (S0 column) + sum_{s<=t} (sum_c q_t[c] k_s[c] P[t][s][c]) d_s,
+ *     S   = diag(E_last) S0 + sum_s (P[last][s] o k_s) d_s^T,
+ * E_t[c] = exp(g_0[c]) ... exp(g_t[c]); arguments as kda_decode_varlen
+ * (g [Ntok, HV, K], dt_bias [HV * K]) without the state cache.
  */
 lar_status gdn_prefill(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
+                       const lar_tensor* g, const lar_tensor* beta,
+                       const lar_tensor* A_log, const lar_tensor* dt_bias,
+                       const lar_tensor* pool, const lar_tensor* cu_seqlens,
+                       const lar_tensor* read_idx, const lar_tensor* write_idx,
+                       const lar_tensor* out, float scale, uint32_t flags, int32_t* dev_err,
+                       void* stream);
+
+lar_status kda_prefill(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
                        const lar_tensor* g, const lar_tensor* beta,
                        const lar_tensor* A_log, const lar_tensor* dt_bias,
                        const lar_tensor* pool, const lar_tensor* cu_seqlens,

@@ -17,6 +17,7 @@ _LIB_PATH = _build.LIB
 LAR_F32, LAR_BF16, LAR_I32, LAR_I64 = 0, 1, 2, 3
 LAR_QK_L2NORM, LAR_GATE_RAW, LAR_BETA_RAW, LAR_STATE_KV = 1, 2, 4, 8
 LAR_DEVERR_READ_SLOT, LAR_DEVERR_WRITE_SLOT, LAR_DEVERR_ACCEPTED, LAR_DEVERR_SEQLEN = 1, 2, 4, 8
+LAR_DEVERR_TIMEOUT = 16
 
 STATUS = {0: "LAR_OK", 1: "LAR_ERR_NULL", 2: "LAR_ERR_DTYPE", 3: "LAR_ERR_RANK",
           4: "LAR_ERR_SHAPE", 5: "LAR_ERR_STRIDE", 6: "LAR_ERR_ALIGN", 7: "LAR_ERR_ARG",
@@ -71,8 +72,10 @@ def load() -> ctypes.CDLL:
             fn.argtypes = [P] * 13 + tail
         lib.la_decode_varlen.restype = ctypes.c_int
         lib.la_decode_varlen.argtypes = [P] * 10 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
-        lib.gdn_prefill.restype = ctypes.c_int
-        lib.gdn_prefill.argtypes = [P] * 12 + tail
+        for name in ("gdn_prefill", "kda_prefill"):
+            fn = getattr(lib, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = [P] * 12 + tail
         lib.la_prefill.restype = ctypes.c_int
         lib.la_prefill.argtypes = [P] * 9 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
         lib.lar_status_string.restype = ctypes.c_char_p
@@ -105,9 +108,29 @@ def _ref(d):
     return ctypes.byref(d) if d is not None else None
 
 
-def _stream(stream):
+def _device_of(tensors, dev_err=None, stream=None) -> torch.device:
+    """The one CUDA device every tensor of a call (and dev_err, and a torch
+    stream when given) lives on; mixed devices are rejected before anything is
+    launched (a kernel reading another GPU's memory without peer access would
+    fault)."""
+    ts = [t for t in tensors if t is not None] + ([dev_err] if dev_err is not None else [])
+    devs = {t.device for t in ts}
+    if len(devs) != 1:
+        raise ValueError(f"the tensors of one call must share one CUDA device, got {sorted(map(str, devs))}")
+    dev = devs.pop()
+    if dev.type != "cuda":
+        raise ValueError("liblar works on CUDA tensors only")
+    if dev_err is not None and (dev_err.dtype != torch.int32 or dev_err.numel() < 1):
+        raise ValueError("dev_err must be a CUDA int32 tensor of at least one element")
+    sdev = getattr(stream, "device", None)
+    if sdev is not None and torch.device(sdev) != dev:
+        raise ValueError(f"stream is on {sdev}, the tensors on {dev}")
+    return dev
+
+
+def _stream(stream, dev=None):
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        return torch.cuda.current_stream(dev).cuda_stream
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
@@ -145,10 +168,12 @@ def _delta(name, q, k, v, g, beta, pool, read_idx, write_idx, out, inter, A_log,
     lib = load()
     if out is None:
         out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
-    ds = [describe(t) for t in (q, k, v, g, beta, A_log, dt_bias, pool, read_idx, write_idx, out,
-                                inter)]
+    ts = (q, k, v, g, beta, A_log, dt_bias, pool, read_idx, write_idx, out, inter)
+    dev = _device_of(ts, dev_err, stream)
+    ds = [describe(t) for t in ts]
     err = dev_err.data_ptr() if dev_err is not None else None
-    st = getattr(lib, name)(*[_ref(d) for d in ds], float(scale), flags, err, _stream(stream))
+    with torch.cuda.device(dev):
+        st = getattr(lib, name)(*[_ref(d) for d in ds], float(scale), flags, err, _stream(stream, dev))
     _check(name, st)
     return out
 
@@ -178,10 +203,12 @@ def _tokens(name, q, k, v, g, beta, pool, state_idx, read_idx, num_accepted, out
     lib = load()
     if out is None:
         out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
-    ds = [describe(t) for t in (q, k, v, g, beta, A_log, dt_bias, pool, read_idx, num_accepted,
-                                state_idx, out)]
+    ts = (q, k, v, g, beta, A_log, dt_bias, pool, read_idx, num_accepted, state_idx, out)
+    dev = _device_of(ts, dev_err, stream)
+    ds = [describe(t) for t in ts]
     err = dev_err.data_ptr() if dev_err is not None else None
-    st = getattr(lib, name)(*[_ref(d) for d in ds], float(scale), flags, err, _stream(stream))
+    with torch.cuda.device(dev):
+        st = getattr(lib, name)(*[_ref(d) for d in ds], float(scale), flags, err, _stream(stream, dev))
     _check(name, st)
     return out
 
@@ -192,9 +219,12 @@ def la_decode(q, k, v, decay, pool, read_idx, write_idx=None, *, out=None, inter
     lib = load()
     if out is None:
         out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
-    ds = [describe(t) for t in (q, k, v, decay, pool, read_idx, write_idx, out, inter)]
+    ts = (q, k, v, decay, pool, read_idx, write_idx, out, inter)
+    dev = _device_of(ts, dev_err, stream)
+    ds = [describe(t) for t in ts]
     err = dev_err.data_ptr() if dev_err is not None else None
-    st = lib.la_decode(*[_ref(d) for d in ds], float(scale), err, _stream(stream))
+    with torch.cuda.device(dev):
+        st = lib.la_decode(*[_ref(d) for d in ds], float(scale), err, _stream(stream, dev))
     _check("la_decode", st)
     return out
 
@@ -235,6 +265,16 @@ def gdn_prefill(q, k, v, g, beta, pool, cu_seqlens, read_idx, write_idx=None, *,
                    _NO_CACHE, scale, _flags(qk_l2norm, gate_raw, beta_raw), dev_err, out_dtype, stream)
 
 
+def kda_prefill(q, k, v, g, beta, pool, cu_seqlens, read_idx, write_idx=None, *, out=None, A_log=None,
+                dt_bias=None, scale=1.0, qk_l2norm=False, gate_raw=False, beta_raw=False, dev_err=None,
+                out_dtype=None, stream=None):
+    """Chunked KDA prefill over variable-length spans (K = V = 128): the
+    arguments and results of kda_decode_varlen (g [Ntok, HV, K]), without a
+    state cache."""
+    return _varlen("kda_prefill", q, k, v, (g, beta, A_log, dt_bias), pool, cu_seqlens, read_idx, write_idx, out,
+                   _NO_CACHE, scale, _flags(qk_l2norm, gate_raw, beta_raw), dev_err, out_dtype, stream)
+
+
 def la_prefill(q, k, v, decay, pool, cu_seqlens, read_idx, write_idx=None, *, out=None, scale=1.0,
                dev_err=None, out_dtype=None, stream=None):
     """Chunked Lightning-Attention prefill over variable-length spans (K = V = 128)."""
@@ -251,10 +291,13 @@ def _varlen(name, q, k, v, gates, pool, cu_seqlens, read_idx, write_idx, out, in
     if out is None:
         out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
     tail_t = () if inter is _NO_CACHE else (inter,)
-    ds = [describe(t) for t in (q, k, v) + tuple(gates) + (pool, cu_seqlens, read_idx, write_idx, out) + tail_t]
+    ts = (q, k, v) + tuple(gates) + (pool, cu_seqlens, read_idx, write_idx, out) + tail_t
+    dev = _device_of(ts, dev_err, stream)
+    ds = [describe(t) for t in ts]
     err = dev_err.data_ptr() if dev_err is not None else None
-    tail = [float(scale)] + ([] if flags is None else [flags]) + [err, _stream(stream)]
-    st = getattr(lib, name)(*[_ref(d) for d in ds], *tail)
+    tail = [float(scale)] + ([] if flags is None else [flags]) + [err, _stream(stream, dev)]
+    with torch.cuda.device(dev):
+        st = getattr(lib, name)(*[_ref(d) for d in ds], *tail)
     _check(name, st)
     return out
 
@@ -280,8 +323,9 @@ class PreparedCall:
             self._name = f"{form}_decode_varlen" if varlen else (f"{form}_decode_tokens" if tokens else f"{form}_decode")
         self._fn = getattr(lib, self._name)
         self._keep = (tensors, dev_err)
+        self._dev = _device_of(tensors.values(), dev_err, stream)
         err = dev_err.data_ptr() if dev_err is not None else None
-        st = _stream(stream)
+        st = _stream(stream, self._dev)
         if form == "la":
             names = ("q", "k", "v", "decay", "pool") + (("cu_seqlens",) if varlen else ()) + \
                 ("read_idx", "write_idx", "out") + (() if prefill else ("inter",))
@@ -306,6 +350,10 @@ class PreparedCall:
                 float(scale), _flags(qk_l2norm, gate_raw, beta_raw, state_kv), err, st]
 
     def __call__(self):
-        st = self._fn(*self._args)
+        if torch.cuda.current_device() == self._dev.index:
+            st = self._fn(*self._args)
+        else:
+            with torch.cuda.device(self._dev):
+                st = self._fn(*self._args)
         if st != 0:
             _check(self._name, st)

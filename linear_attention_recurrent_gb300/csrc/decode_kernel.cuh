@@ -58,6 +58,11 @@
 #ifndef LAR_K128_BF16_MB
 #define LAR_K128_BF16_MB 1
 #endif
+// Resident CTAs per SM the fp32 single-token GDN / KDA instances are compiled
+// for.
+#ifndef LAR_K128_MB1
+#define LAR_K128_MB1 3
+#endif
 #ifndef LAR_K128_LPR
 #define LAR_K128_LPR 8
 #endif
@@ -829,7 +834,7 @@ lar_status launch_tile_mode(const DecodeParams& p, cudaStream_t stream) {
 // instance, single tokens take the general one).  The per-token-slot instance
 // stores every token's state, so it streams like a single-token call and
 // takes S1 stages too.
-template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB = 1, int S1 = 0>
+template <int FORM, int K, int LPR, int NR, int NW, int S, int SB, int MB = 1, int S1 = 0, int MB1 = MB>
 lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
     if (p.cu != nullptr)
         return launch_tile_mode<FORM, K, LPR, NR * (SB == 2 ? LAR_VL_BF16_NR_MUL : LAR_VL_NR_MUL),
@@ -840,7 +845,7 @@ lar_status launch_tile(const DecodeParams& p, cudaStream_t stream) {
     }
     if constexpr (S1 > 0) {
         if (p.T == 1 && p.inter == nullptr)
-            return launch_tile_mode<FORM, K, LPR, NR, NW, S1, SB, MB, false, 1>(p, stream);
+            return launch_tile_mode<FORM, K, LPR, NR, NW, S1, SB, MB1, false, 1>(p, stream);
     }
     return launch_tile_mode<FORM, K, LPR, NR, NW, S, SB, MB, false, 0>(p, stream);
 }
@@ -868,7 +873,8 @@ lar_status launch_form(const DecodeParams& p, void* stream) {
                                        LAR_K128_MIN_BLOCKS>(p, st);
                 else
                     return launch_tile<FORM, 128, LAR_K128_LPR, LAR_K128_NR, LAR_K128_NW, LAR_K128_S_MTP, 4,
-                                       FORM == FORM_GDN ? LAR_K128_GDN_MB : LAR_K128_MIN_BLOCKS, LAR_K128_S>(p, st);
+                                       FORM == FORM_GDN ? LAR_K128_GDN_MB : LAR_K128_MIN_BLOCKS, LAR_K128_S,
+                                       LAR_K128_MB1>(p, st);
             default: return LAR_ERR_SHAPE;
         }
     }

@@ -49,8 +49,10 @@ struct DecodeParams {
 lar_status launch_gdn(const DecodeParams& p, void* stream);
 lar_status launch_kda(const DecodeParams& p, void* stream);
 lar_status launch_la(const DecodeParams& p, void* stream);
-// chunked form over variable-length spans (GDN and LA, K = V = 128; prefill.cu)
+// chunked form over variable-length spans (GDN, KDA and LA, K = V = 128; prefill.cu)
 lar_status launch_prefill(const DecodeParams& p, void* stream);
+// the same for GDN and LA with the chunk products on the tensor cores (prefill_tc.cu)
+lar_status launch_prefill_tc(const DecodeParams& p, void* stream);
 
 // Largest T a call may use (per-pair token tables are sized for it).
 constexpr int kMaxTokens = 16;

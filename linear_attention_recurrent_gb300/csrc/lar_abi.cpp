@@ -237,7 +237,21 @@ lar_status check_common(const Common& c, int form, DecodeParams& p, bool kv = fa
     return LAR_OK;
 }
 
-lar_status check_aliasing(const lar_tensor* const* outs, int n_out, const lar_tensor* const* ins, int n_in) {
+// Outputs overlap neither each other nor any input.  The device error word
+// (written with atomicOr by the kernels) is a 4-byte output too: aligned to 4
+// bytes and clear of every tensor of the call.
+lar_status check_aliasing(const lar_tensor* const* outs, int n_out, const lar_tensor* const* ins, int n_in,
+                          const int32_t* dev_err) {
+    if (dev_err) {
+        if (reinterpret_cast<uintptr_t>(dev_err) % alignof(int32_t) != 0) return LAR_ERR_ALIGN;
+        Span e;
+        e.lo = reinterpret_cast<uintptr_t>(dev_err);
+        e.hi = e.lo + sizeof(int32_t);
+        for (int i = 0; i < n_out; ++i)
+            if (outs[i] && overlap(e, span_of(outs[i]))) return LAR_ERR_ALIAS;
+        for (int j = 0; j < n_in; ++j)
+            if (ins[j] && overlap(e, span_of(ins[j]))) return LAR_ERR_ALIAS;
+    }
     for (int i = 0; i < n_out; ++i) {
         if (!outs[i]) continue;
         const Span a = span_of(outs[i]);
@@ -334,7 +348,7 @@ lar_status delta_rule(int form, const lar_tensor* q, const lar_tensor* k, const 
 
     const lar_tensor* outs[] = {pool, out, inter};
     const lar_tensor* ins[] = {q, k, v, g, beta, A_log, dt_bias, read_idx, write_idx, num_accepted, state_idx};
-    st = check_aliasing(outs, 3, ins, 11);
+    st = check_aliasing(outs, 3, ins, 11, dev_err);
     if (st != LAR_OK) return st;
     if (p.B == 0) return LAR_OK;
     return kda ? lar::launch_kda(p, stream) : lar::launch_gdn(p, stream);
@@ -460,7 +474,7 @@ lar_status varlen(int form, const lar_tensor* q, const lar_tensor* k, const lar_
 
     const lar_tensor* outs[] = {pool, out, inter};
     const lar_tensor* ins[] = {q, k, v, g, beta, A_log, dt_bias, decay, cu_seqlens, read_idx, write_idx};
-    if ((st = check_aliasing(outs, 3, ins, 11)) != LAR_OK) return st;
+    if ((st = check_aliasing(outs, 3, ins, 11, dev_err)) != LAR_OK) return st;
     if (N == 0) return LAR_OK;
     if (prefill) return lar::launch_prefill(p, stream);
     switch (form) {
@@ -533,7 +547,7 @@ lar_status la_decode(const lar_tensor* q, const lar_tensor* k, const lar_tensor*
     p.dev_err = dev_err;
     const lar_tensor* outs[] = {pool, out, inter};
     const lar_tensor* ins[] = {q, k, v, decay, read_idx, write_idx};
-    st = check_aliasing(outs, 3, ins, 6);
+    st = check_aliasing(outs, 3, ins, 6, dev_err);
     if (st != LAR_OK) return st;
     if (p.B == 0) return LAR_OK;
     return lar::launch_la(p, stream);
@@ -576,6 +590,15 @@ lar_status gdn_prefill(const lar_tensor* q, const lar_tensor* k, const lar_tenso
                   out, nullptr, scale, flags, dev_err, stream, true);
 }
 
+lar_status kda_prefill(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v, const lar_tensor* g,
+                       const lar_tensor* beta, const lar_tensor* A_log, const lar_tensor* dt_bias,
+                       const lar_tensor* pool, const lar_tensor* cu_seqlens, const lar_tensor* read_idx,
+                       const lar_tensor* write_idx, const lar_tensor* out, float scale, uint32_t flags,
+                       int32_t* dev_err, void* stream) {
+    return varlen(lar::FORM_KDA, q, k, v, g, beta, A_log, dt_bias, nullptr, pool, cu_seqlens, read_idx, write_idx,
+                  out, nullptr, scale, flags, dev_err, stream, true);
+}
+
 lar_status la_prefill(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v, const lar_tensor* decay,
                       const lar_tensor* pool, const lar_tensor* cu_seqlens, const lar_tensor* read_idx,
                       const lar_tensor* write_idx, const lar_tensor* out, float scale, int32_t* dev_err,
@@ -592,9 +615,11 @@ const char* lar_status_string(lar_status status) {
         case LAR_ERR_RANK: return "wrong tensor rank";
         case LAR_ERR_SHAPE: return "shapes disagree or a size is outside the supported range";
         case LAR_ERR_STRIDE: return "unsupported strides (k stride of pool/inter must be 1; no negative strides)";
-        case LAR_ERR_ALIGN: return "pool/inter must be 16-byte aligned with strides that are multiples of 16 bytes";
+        case LAR_ERR_ALIGN:
+            return "pool/inter must be 16-byte aligned with strides that are multiples of 16 bytes; "
+                   "dev_err 4-byte aligned";
         case LAR_ERR_ARG: return "inconsistent arguments or flags";
-        case LAR_ERR_ALIAS: return "an output overlaps another output or an input";
+        case LAR_ERR_ALIAS: return "an output (dev_err included) overlaps another output or an input";
         case LAR_ERR_LAUNCH: return "kernel launch failed";
     }
     return "unknown status";

@@ -19,6 +19,17 @@
 // from differences of log-decay prefix sums (which lose precision for large
 // decays and break down for a factor of 0).
 //
+// KDA (a decay factor a_t[c] per key channel c) is the same unrolling with the
+// decay inside the dot products: P[t][s][c] = a_{s+1}[c] ... a_t[c],
+// E_t[c] = a_0[c] ... a_t[c], and
+//     A[t][s] = beta_t sum_c k_t[c] k_s[c] P[t][s][c]            (s < t)
+//     d + A d = beta (v - (E o K) S0),
+//     o_t = (E_t o q_t)^T S0 + sum_{s<=t} (sum_c q_t[c] k_s[c] P[t][s][c]) d_s,
+//     S = diag(E_{C-1}) S0 + sum_s (P[C-1][s] o k_s) d_s^T.
+// P[t][s][c] is a running product over t for each (s, c): every factor is at
+// most 1, so nothing overflows, and a product that underflows is negligible
+// next to the terms it is added to.
+//
 // Work.  A CTA of 256 threads per (sequence, v-head, block of VB value
 // columns) keeps its columns of S (K x VB, fp32) in shared memory for the
 // whole span and walks the span a chunk at a time: load the chunk (q, k
@@ -50,8 +61,9 @@ constexpr int TROW = PC + 1;   // padded row of the chunk's C x C tables
 #define LAR_PF_VB 64
 #endif
 
-// shared-memory layout for VB value columns per CTA, in floats
-template <int VB>
+// shared-memory layout for VB value columns per CTA, in floats (KDA adds the
+// per-channel decay rows)
+template <int VB, bool KDA = false>
 struct PfLayout {
     static constexpr int SROW = VB + 4;                  // padded state row
     static constexpr int OFF_S = 0;                      // S [K][SROW]
@@ -64,9 +76,14 @@ struct PfLayout {
     static constexpr int OFF_E = OFF_AF + PC;            // E_t
     static constexpr int OFF_W = OFF_E + PC;             // P[C-1][s]
     static constexpr int OFF_B = OFF_W + PC;             // beta_t
-    static constexpr int FLOATS = OFF_B + PC;
+    static constexpr int OFF_AD = OFF_B + PC;            // KDA: a_t[c] [C][K]
+    static constexpr int OFF_X = OFF_AD + (KDA ? PC * PK : 0);   // KDA: P[C-1][s][c] k_s[c] [C][K]
+    static constexpr int OFF_EC = OFF_X + (KDA ? PC * PK : 0);   // KDA: E_{C-1}[c] [K]
+    static constexpr int FLOATS = OFF_EC + (KDA ? PK : 0);
     static constexpr size_t BYTES = static_cast<size_t>(FLOATS) * sizeof(float);
-    static_assert(OFF_K % 4 == 0 && OFF_Q % 4 == 0 && OFF_D % 4 == 0 && OFF_A % 4 == 0, "16-byte aligned blocks");
+    static_assert(OFF_K % 4 == 0 && OFF_Q % 4 == 0 && OFF_D % 4 == 0 && OFF_A % 4 == 0 && OFF_AD % 4 == 0 &&
+                      OFF_X % 4 == 0,
+                  "16-byte aligned blocks");
     static_assert(BYTES <= 227 * 1024, "fits one CTA's shared memory");
 };
 
@@ -77,8 +94,9 @@ __device__ __forceinline__ float comp(const float4& x, int i) {
 __device__ __forceinline__ float2 dup(float x) { return make_float2(x, x); }
 
 template <int FORM, int SB, int VB>
-__global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const DecodeParams p) {
-    using LY = PfLayout<VB>;
+__global__ void __launch_bounds__(PTH, (VB == 128 || FORM == FORM_KDA) ? 1 : 2) prefill_kernel(const DecodeParams p) {
+    constexpr bool KDA = FORM == FORM_KDA;
+    using LY = PfLayout<VB, KDA>;
     constexpr int SROW = LY::SROW;
     extern __shared__ __align__(16) float sm[];
     float* S = sm + LY::OFF_S;
@@ -91,6 +109,9 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
     float* E = sm + LY::OFF_E;
     float* Wd = sm + LY::OFF_W;
     float* Bt = sm + LY::OFF_B;
+    float* Ad = sm + LY::OFF_AD;     // KDA only
+    float* X = sm + LY::OFF_X;       // KDA only
+    float* EC = sm + LY::OFF_EC;     // KDA only
 
     constexpr int NSPLIT = PV / VB;        // CTAs per (sequence, head) pair, one per column block
     constexpr int CP = VB / 32;            // columns per thread in the products and outputs (2 or 4)
@@ -184,6 +205,7 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
     constexpr int RPW = PC / (PTH / 32);   // q / k rows per warp
     constexpr int VPT = PC * VB / PTH;     // v values per thread
     float qx[RPW][4], kx[RPW][4], vx[VPT], gx = 0.f, bx = 0.f;
+    float gk[KDA ? RPW : 1][4];      // KDA: the gate inputs of a q / k row's channels
     auto fetch = [&](int64_t c0) {
         const int Lc = static_cast<int>(L - c0 < PC ? L - c0 : PC);
 #pragma unroll
@@ -196,6 +218,9 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
                 const int c = lane * 4 + e;
                 qx[j][e] = ok ? ld_in(p.q, gt * p.qs[1] + h * p.qs[2] + c * p.qs[3], p.q_dt) : 0.f;
                 kx[j][e] = ok ? ld_in(p.k, gt * p.ks[1] + h * p.ks[2] + c * p.ks[3], p.k_dt) : 0.f;
+                if constexpr (KDA)
+                    gk[j][e] = ok ? ld_in(p.g, gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2] + c * p.gs[3], p.g_dt)
+                                  : 0.f;
             }
         }
 #pragma unroll
@@ -210,7 +235,7 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
         if constexpr (FORM != FORM_LA) {
             if (warp == 0 && lane < Lc) {
                 const int64_t gt = tb + c0 + lane;
-                gx = ld_in(p.g, gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2], p.g_dt);
+                if constexpr (!KDA) gx = ld_in(p.g, gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2], p.g_dt);
                 bx = ld_in(p.beta, gt * p.bs[1] + static_cast<int64_t>(hv) * p.bs[2], p.beta_dt);
             }
         }
@@ -244,6 +269,21 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
                 make_float4(qx[j][0] * iq, qx[j][1] * iq, qx[j][2] * iq, qx[j][3] * iq);
             *reinterpret_cast<float4*>(Kc + t * KROW + lane * 4) =
                 make_float4(kx[j][0] * ik, kx[j][1] * ik, kx[j][2] * ik, kx[j][3] * ik);
+            if constexpr (KDA) {
+                // per-channel decay factors a_t[c] (gate chain included); padding tokens: 1
+                float a4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float x = gk[j][e];
+                    if (gate_raw) {
+                        const int c = lane * 4 + e;
+                        const float bias = p.dt_bias ? p.dt_bias[(static_cast<int64_t>(hv) * PK + c) * p.dtb_s] : 0.f;
+                        x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
+                    }
+                    a4[e] = t < Lc ? expf(x) : 1.f;
+                }
+                *reinterpret_cast<float4*>(Ad + t * PK + lane * 4) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+            }
         }
 #pragma unroll
         for (int j = 0; j < VPT; ++j) D[tid + j * PTH] = vx[j];
@@ -256,36 +296,110 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
                     a = p.decay[h * p.dec_s];
                     bt = 1.f;
                 } else {
-                    float x = gx;
-                    if (gate_raw) {
-                        const float bias = p.dt_bias ? p.dt_bias[hv * p.dtb_s] : 0.f;
-                        x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
+                    if constexpr (!KDA) {
+                        float x = gx;
+                        if (gate_raw) {
+                            const float bias = p.dt_bias ? p.dt_bias[hv * p.dtb_s] : 0.f;
+                            x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
+                        }
+                        a = expf(x);
                     }
-                    a = expf(x);
                     bt = beta_raw ? 1.f / (1.f + expf(-bx)) : bx;
                 }
             }
             Af[t] = a;
             Bt[t] = bt;
             __syncwarp();
-            // row t: P[t][s] = a_{s+1} ... a_t for s <= t, 0 above
-            float f = 1.f;
+            if constexpr (!KDA) {
+                // row t: P[t][s] = a_{s+1} ... a_t for s <= t, 0 above
+                float f = 1.f;
 #pragma unroll 1
-            for (int s = PC - 1; s >= 0; --s) {
-                if (s <= t) {
-                    M[t * TROW + s] = f;
-                    f *= Af[s];
-                } else {
-                    M[t * TROW + s] = 0.f;
+                for (int s = PC - 1; s >= 0; --s) {
+                    if (s <= t) {
+                        M[t * TROW + s] = f;
+                        f *= Af[s];
+                    } else {
+                        M[t * TROW + s] = 0.f;
+                    }
                 }
-            }
-            E[t] = f;   // a_0 ... a_t
-            if (t == PC - 1) {
+                E[t] = f;   // a_0 ... a_t
+                if (t == PC - 1) {
 #pragma unroll 1
-                for (int s = 0; s < PC; ++s) Wd[s] = M[t * TROW + s];
+                    for (int s = 0; s < PC; ++s) Wd[s] = M[t * TROW + s];
+                }
             }
         }
         __syncthreads();
+
+        if constexpr (KDA) {
+            // ---- A[t][s] = beta_t sum_c k_t[c] k_s[c] P[t][s][c] (s < t) and
+            // M[t][s] = sum_c q_t[c] k_s[c] P[t][s][c] (s <= t).  Warp w takes
+            // s = w, w + 8, ...; lane l channels 4l .. 4l + 3, with the products
+            // P[t][s][c] kept as a running product over t.  Each lane's 32
+            // partial sums (one per t) are reduced across the warp by recursive
+            // halving, which leaves lane l holding the sums for t = l.
+            static_assert(PC == 32, "one token per lane after the reduction");
+#pragma unroll 1
+            for (int s = warp; s < PC; s += PTH / 32) {
+                const float4 ks = *reinterpret_cast<const float4*>(Kc + s * KROW + 4 * lane);
+                float4 pr = make_float4(1.f, 1.f, 1.f, 1.f);
+                float va[PC], vm[PC];
+#pragma unroll
+                for (int t = 0; t < PC; ++t) {
+                    va[t] = 0.f;
+                    vm[t] = 0.f;
+                    if (t >= s) {
+                        if (t > s) {
+                            const float4 a4 = *reinterpret_cast<const float4*>(Ad + t * PK + 4 * lane);
+                            pr = make_float4(pr.x * a4.x, pr.y * a4.y, pr.z * a4.z, pr.w * a4.w);
+                        }
+                        const float4 kt = *reinterpret_cast<const float4*>(Kc + t * KROW + 4 * lane);
+                        const float4 qt = *reinterpret_cast<const float4*>(Qc + t * KROW + 4 * lane);
+                        const float wx = ks.x * pr.x, wy = ks.y * pr.y, wz = ks.z * pr.z, ww = ks.w * pr.w;
+                        va[t] = fmaf(kt.w, ww, fmaf(kt.z, wz, fmaf(kt.y, wy, kt.x * wx)));
+                        vm[t] = fmaf(qt.w, ww, fmaf(qt.z, wz, fmaf(qt.y, wy, qt.x * wx)));
+                    }
+                }
+#pragma unroll
+                for (int n = PC / 2; n >= 1; n >>= 1) {
+                    const bool up = (lane & n) != 0;
+#pragma unroll
+                    for (int i = 0; i < n; ++i) {
+                        const float sa = up ? va[i] : va[i + n];
+                        const float sq = up ? vm[i] : vm[i + n];
+                        const float ka = up ? va[i + n] : va[i];
+                        const float kq = up ? vm[i + n] : vm[i];
+                        va[i] = ka + __shfl_xor_sync(0xffffffffu, sa, n);
+                        vm[i] = kq + __shfl_xor_sync(0xffffffffu, sq, n);
+                    }
+                }
+                const int t = lane;
+                A[t * TROW + s] = t > s ? Bt[t] * va[0] : 0.f;
+                M[t * TROW + s] = t >= s ? vm[0] : 0.f;
+            }
+            __syncthreads();
+            // ---- per channel c: X[s][c] = P[C-1][s][c] k_s[c] (a running product
+            // from the chunk's end), then k_t and q_t scaled by E_t[c] in place, and
+            // E_{C-1}[c]
+            if (tid < PK) {
+                const int c = tid;
+                float w = 1.f;
+#pragma unroll 4
+                for (int s = PC - 1; s >= 0; --s) {
+                    X[s * PK + c] = Kc[s * KROW + c] * w;
+                    w *= Ad[s * PK + c];
+                }
+                float e = 1.f;
+#pragma unroll 4
+                for (int t = 0; t < PC; ++t) {
+                    e *= Ad[t * PK + c];
+                    Kc[t * KROW + c] *= e;
+                    Qc[t * KROW + c] *= e;
+                }
+                EC[c] = e;
+            }
+            __syncthreads();
+        }
 
         // ---- K S0 and Q S0: rows 4ty..4ty+3, columns CP tx .. CP tx + CP - 1
         float2 oq[4][CP2];
@@ -329,12 +443,13 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int t = 4 * ty + i;
-                const float2 et = dup(E[t]);
+                // KDA: the per-channel E_t is already inside the scaled q and k rows
+                const float2 et = dup(KDA ? 1.f : E[t]);
 #pragma unroll
                 for (int c = 0; c < CP2; ++c) oq[i][c] = __fmul2_rn(et, aq[i][c]);
                 if constexpr (FORM != FORM_LA) {
                     // right-hand side beta_t (v_t - E_t (S0^T k_t)), in place of v_t
-                    const float b = Bt[t], e = E[t];
+                    const float b = Bt[t], e = KDA ? 1.f : E[t];
 #pragma unroll
                     for (int c = 0; c < CP2; ++c) {
                         float2* dp = reinterpret_cast<float2*>(D + t * VB + CP * tx + 2 * c);
@@ -346,7 +461,8 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
         }
 
         // ---- K K^T and Q K^T: row t, columns s = sg, sg + 8, sg + 16, sg + 24
-        {
+        // (KDA built its decayed forms above)
+        if constexpr (!KDA) {
             const int t = tid >> 3, sg = tid & 7;
             float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
@@ -439,11 +555,13 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
                 for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
 #pragma unroll 2
             for (int s = 0; s < PC; ++s) {
-                const float2 ws = dup(Wd[s]);
+                // KDA: X holds P[C-1][s] o k_s, the scalar factor is 1
+                const float2 ws = dup(KDA ? 1.f : Wd[s]);
+                const float* krow = KDA ? X + s * PK : Kc + s * KROW;
                 float kv[RK];
 #pragma unroll
                 for (int i4 = 0; i4 < RK / 4; ++i4) {
-                    const float4 k4 = *reinterpret_cast<const float4*>(Kc + s * KROW + RK * ky + 4 * i4);
+                    const float4 k4 = *reinterpret_cast<const float4*>(krow + RK * ky + 4 * i4);
                     kv[4 * i4] = k4.x;
                     kv[4 * i4 + 1] = k4.y;
                     kv[4 * i4 + 2] = k4.z;
@@ -460,9 +578,9 @@ __global__ void __launch_bounds__(PTH, VB == 128 ? 1 : 2) prefill_kernel(const D
                     for (int j = 0; j < 4; ++j) acc[i][j] = __ffma2_rn(k2, dd[j], acc[i][j]);
                 }
             }
-            const float2 ec = dup(E[PC - 1]);
 #pragma unroll
             for (int i = 0; i < RK; ++i) {
+                const float2 ec = dup(KDA ? EC[RK * ky + i] : E[PC - 1]);
                 float4* sp = reinterpret_cast<float4*>(S + (RK * ky + i) * SROW + 8 * vx8);
                 const float4 s0 = sp[0], s1 = sp[1];
                 const float2 n0 = __ffma2_rn(ec, make_float2(s0.x, s0.y), acc[i][0]);
@@ -506,7 +624,7 @@ template <int FORM, int SB>
 lar_status launch_prefill_form(const DecodeParams& p, cudaStream_t stream) {
     constexpr int VB = LAR_PF_VB;
     auto kern = prefill_kernel<FORM, SB, VB>;
-    constexpr size_t smem = PfLayout<VB>::BYTES;
+    constexpr size_t smem = PfLayout<VB, FORM == FORM_KDA>::BYTES;
     // the shared-memory opt-in is a per-device function attribute; setting it on
     // every call keeps it right on whichever device is current (a host-side
     // call, small next to a prefill launch)
@@ -530,12 +648,20 @@ lar_status launch_prefill_form(const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
+// GDN and LA chunk products on the tensor cores (prefill_tc.cu); 0 keeps them
+// on the CUDA cores here
+#ifndef LAR_PF_TC
+#define LAR_PF_TC 0
+#endif
+
 lar_status launch_prefill(const DecodeParams& p, void* stream) {
     if (p.K != PK || p.V != PV) return LAR_ERR_SHAPE;
+    if (LAR_PF_TC && p.form != FORM_KDA) return launch_prefill_tc(p, stream);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool bf = p.pool_dt == LAR_BF16;
     if (p.form == FORM_LA) return bf ? launch_prefill_form<FORM_LA, 2>(p, st) : launch_prefill_form<FORM_LA, 4>(p, st);
     if (p.form == FORM_GDN) return bf ? launch_prefill_form<FORM_GDN, 2>(p, st) : launch_prefill_form<FORM_GDN, 4>(p, st);
+    if (p.form == FORM_KDA) return bf ? launch_prefill_form<FORM_KDA, 2>(p, st) : launch_prefill_form<FORM_KDA, 4>(p, st);
     return LAR_ERR_ARG;
 }
 

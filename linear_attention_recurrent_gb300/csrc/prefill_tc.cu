@@ -1,0 +1,550 @@
+// prefill_tc.cu -- the chunked prefill (gated delta rule with scalar decay, and
+// Lightning Attention) with its matrix products on the tensor cores.
+//
+// Same operation and chunk algebra as prefill.cu (32-token chunks; with S0 the
+// state entering a chunk, a_t the decay factors, P[t][s] = a_{s+1} ... a_t,
+// E_t = a_0 ... a_t):
+//     d_t + sum_{s<t} beta_t P[t][s] (k_t . k_s) d_s = beta_t (v_t - E_t S0^T k_t)
+//     o_t = E_t S0^T q_t + sum_{s<=t} P[t][s] (q_t . k_s) d_s
+//     S   = E_31 S0 + sum_s P[31][s] k_s d_s^T          (LA: d_t = v_t)
+// written for the tensor cores in the transposed form, value channels as the
+// 128 rows of every product:
+//     [U | P] = S0^T [K ; Q]^T        (128 x 64, reduction over the 128 keys)
+//     O       = D M^T                 (128 x 32, reduction over the chunk)
+//     S^T    += (D o W) K             (128 x 128, reduction over the chunk)
+// with D [v][s] = d_s[v], M[t][s] = P[t][s] (q_t . k_s) and W_s = P[31][s].
+//
+// Precision.  The products run as tcgen05.mma kind::tf32 in three passes
+// (A_hi B_hi + A_hi B_lo + A_lo B_hi, each operand split as x = hi + lo with hi
+// the nearest tf32 value): about 2^-21 relative per product term, so the fp32
+// state keeps the 1e-4 relative tolerance over thousands of tokens.  The
+// dropped A_lo B_lo term is below 2^-22 relative.
+//
+// Work.  One CTA of 256 threads per (sequence, v-head) keeps that pair's state
+// in tensor memory for the whole span: S^T (fp32, the accumulator of the state
+// update) and its tf32 halves (the A operand of the next chunk's first
+// product).  Thread (warp w, lane l) owns value row v = 32 (w % 4) + l; the two
+// warps of a row split its columns.  Per chunk: the chunk's k and q rows into
+// shared memory (l2-normalised when asked, fp32 copies and tf32 halves in the
+// K-major tile layout the tensor cores read), the per-token decays and betas;
+// one thread issues [U | P] while the others compute K K^T and Q K^T on the
+// CUDA cores (32 x 32, the decay table folded in) and scale the state by E_31;
+// the triangular solve runs per value row in registers; D and D o W go to
+// tensor memory; one thread issues O and the state update; the outputs
+// E_t P + O are stored and the new state's tf32 halves written back.  Tensor
+// memory holds 448 of 512 columns: S (0..127), S_hi / S_lo (128..383; reused
+// for D, D o W and O after [U | P] has read them), [U | P] (384..447).
+//
+// Every wait is bounded: a wait that gives up makes the whole CTA skip the
+// rest of its span and its writeback, and sets LAR_DEVERR_TIMEOUT.
+#include "decode_kernel.cuh"
+#include "tc_util.cuh"
+
+namespace lar {
+namespace {
+
+constexpr int TK = 128;       // key channels
+constexpr int TVV = 128;      // value channels (the M of every product)
+constexpr int TC = 32;        // tokens per chunk
+constexpr int TTH = 256;      // threads per CTA
+constexpr uint32_t LBO = 144;                         // between K-adjacent core matrices
+constexpr uint32_t KQ_SBO = (TK / 4) * LBO + 16;      // [K ; Q] tile: 64 rows x 128 keys
+constexpr uint32_t KQ_BYTES = 8 * KQ_SBO;
+constexpr uint32_t KT_SBO = (TC / 4) * LBO + 16;      // K^T tile: 128 keys x 32 tokens
+constexpr uint32_t KT_BYTES = (TK / 8) * KT_SBO;
+constexpr uint32_t MT_SBO = KT_SBO;                   // M tile: 32 tokens x 32 tokens
+constexpr uint32_t MT_BYTES = (TC / 8) * MT_SBO;
+constexpr int FROW = TK + 4;                          // fp32 k / q rows (padded)
+constexpr int TROW = TC + 1;                          // C x C tables (padded)
+
+// shared memory, bytes
+constexpr uint32_t OFF_KQH = 0;
+constexpr uint32_t OFF_KQL = OFF_KQH + KQ_BYTES;
+constexpr uint32_t OFF_KTH = OFF_KQL + KQ_BYTES;
+constexpr uint32_t OFF_KTL = OFF_KTH + KT_BYTES;
+constexpr uint32_t OFF_MTH = OFF_KTL + KT_BYTES;
+constexpr uint32_t OFF_MTL = OFF_MTH + MT_BYTES;
+constexpr uint32_t OFF_K32 = OFF_MTL + MT_BYTES;
+constexpr uint32_t OFF_Q32 = OFF_K32 + TC * FROW * 4;
+constexpr uint32_t OFF_A = OFF_Q32 + TC * FROW * 4;     // beta_t P[t][s] (k_t . k_s), s < t
+constexpr uint32_t OFF_P = OFF_A + TC * TROW * 4;       // P[t][s]
+constexpr uint32_t OFF_AF = OFF_P + TC * TROW * 4;      // a_t
+constexpr uint32_t OFF_E = OFF_AF + TC * 4;             // E_t
+constexpr uint32_t OFF_W = OFF_E + TC * 4;              // P[31][s]
+constexpr uint32_t OFF_B = OFF_W + TC * 4;              // beta_t
+constexpr uint32_t OFF_BAR = OFF_B + TC * 4;            // two mbarriers
+constexpr uint32_t OFF_TM = OFF_BAR + 16;               // TMEM base address
+constexpr uint32_t TC_SMEM = OFF_TM + 16;
+static_assert(OFF_KQL % 16 == 0 && OFF_KTH % 16 == 0 && OFF_KTL % 16 == 0 && OFF_MTH % 16 == 0 &&
+                  OFF_MTL % 16 == 0 && OFF_K32 % 16 == 0 && OFF_Q32 % 16 == 0 && OFF_BAR % 8 == 0,
+              "tile and barrier alignment");
+static_assert(tc::kmaj(63, TK - 1, LBO, KQ_SBO) + 4 <= KQ_BYTES && tc::kmaj(TK - 1, TC - 1, LBO, KT_SBO) + 4 <= KT_BYTES &&
+                  tc::kmaj(TC - 1, TC - 1, LBO, MT_SBO) + 4 <= MT_BYTES,
+              "tiles hold their elements");
+static_assert(TC_SMEM <= 227 * 1024, "fits one CTA's shared memory");
+
+// tensor-memory columns
+constexpr uint32_t COL_S = 0, COL_SHI = 128, COL_SLO = 256, COL_UP = 384;
+constexpr uint32_t COL_DHI = 128, COL_DLO = 160, COL_DWHI = 192, COL_DWLO = 224, COL_O = 256;
+constexpr uint32_t TMEM_COLS = 512;
+
+template <int N>
+__device__ __forceinline__ void split_store(uint32_t taddr_hi, uint32_t taddr_lo, const float* x) {
+    float hi[N], lo[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        hi[i] = tc::tf32_hi(x[i]);
+        lo[i] = x[i] - hi[i];
+    }
+#pragma unroll
+    for (int i = 0; i < N; i += 16) {
+        tc::tmem_st16(taddr_hi + i, hi + i);
+        tc::tmem_st16(taddr_lo + i, lo + i);
+    }
+}
+
+// all threads of the CTA: a barrier that also orders tensor-core work around it
+__device__ __forceinline__ void tc_sync() {
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+}
+
+template <int FORM, int SB>
+__global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p) {
+    constexpr bool LA = FORM == FORM_LA;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    float* K32 = reinterpret_cast<float*>(smem + OFF_K32);
+    float* Q32 = reinterpret_cast<float*>(smem + OFF_Q32);
+    float* At = reinterpret_cast<float*>(smem + OFF_A);
+    float* Pt = reinterpret_cast<float*>(smem + OFF_P);
+    float* Af = reinterpret_cast<float*>(smem + OFF_AF);
+    float* E = reinterpret_cast<float*>(smem + OFF_E);
+    float* Wd = reinterpret_cast<float*>(smem + OFF_W);
+    float* Bt = reinterpret_cast<float*>(smem + OFF_B);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint32_t* tm_slot = reinterpret_cast<uint32_t*>(smem + OFF_TM);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int vrow = quarter * 32 + lane;                      // this thread's value row (TMEM lane)
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int hv = blockIdx.x;
+    const int n = blockIdx.y;
+    const int h = hv / p.group;
+
+#if LAR_PDL
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+#endif
+    // ---- span and slots (reversed or overlong spans run as empty and are flagged)
+    const int64_t lo = ld_idx(p.cu, n * p.cu_s, p.cu_dt);
+    const int64_t hi = ld_idx(p.cu, (n + 1) * p.cu_s, p.cu_dt);
+    const bool span_ok = lo >= 0 && hi >= lo && hi <= p.ntok;
+    const int64_t tb = span_ok ? lo : 0;
+    const int64_t L = span_ok ? hi - lo : 0;
+    const int64_t r = ld_idx(p.ridx, n * p.ri_s, p.ri_dt);
+    const int64_t w = p.widx ? ld_idx(p.widx, n * p.wi_s, p.wi_dt) : r;
+    const bool rd = r >= 0 && r < p.P;
+    const bool wr = w >= 0 && w < p.P;
+    if (tid == 0 && blockIdx.x == 0 && p.dev_err) {
+        const int e = (r >= p.P ? LAR_DEVERR_READ_SLOT : 0) | (w >= p.P ? LAR_DEVERR_WRITE_SLOT : 0) |
+                      (span_ok ? 0 : LAR_DEVERR_SEQLEN);
+        if (e) atomicOr(p.dev_err, e);
+    }
+
+    if (tid == 0) {
+        tc::mbar_init(&bar[0], 1);
+        tc::mbar_init(&bar[1], 1);
+        tc::mbar_init_fence();
+    }
+    if (warp == 0) tc::tmem_alloc(tm_slot, TMEM_COLS);
+    tc_sync();
+    const uint32_t tm = *tm_slot;
+    const uint32_t my = tm + lane_off;                         // this thread's lane, column 0
+    const int col0 = 64 * half;                                // this thread's 64 state columns
+
+    // ---- S0 into tensor memory: S (fp32) and its tf32 halves
+    {
+        const unsigned char* src = static_cast<const unsigned char*>(p.pool) +
+                                   ((rd ? r : 0) * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1] +
+                                    static_cast<int64_t>(vrow) * p.ps[2] + col0) * SB;
+#pragma unroll 1
+        for (int c = 0; c < 64; c += 16) {
+            float x[16];
+            if (rd) {
+                if constexpr (SB == 4) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 f = __ldg(reinterpret_cast<const float4*>(src + c * 4) + i);
+                        x[4 * i] = f.x; x[4 * i + 1] = f.y; x[4 * i + 2] = f.z; x[4 * i + 3] = f.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const uint4 u = __ldg(reinterpret_cast<const uint4*>(src + c * 2) + i);
+                        const unsigned wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            x[8 * i + 2 * e] = __uint_as_float(wd[e] << 16);
+                            x[8 * i + 2 * e + 1] = __uint_as_float(wd[e] & 0xffff0000u);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x[i] = 0.f;
+            }
+            tc::tmem_st16(my + COL_S + col0 + c, x);
+            split_store<16>(my + COL_SHI + col0 + c, my + COL_SLO + col0 + c, x);
+        }
+        tc::tmem_st_wait();
+    }
+    tc_sync();
+
+    const bool l2 = !LA && (p.flags & LAR_QK_L2NORM) != 0;
+    const bool gate_raw = (p.flags & LAR_GATE_RAW) != 0;
+    const bool beta_raw = (p.flags & LAR_BETA_RAW) != 0;
+    const uint32_t kqh = tc::smem_addr(smem + OFF_KQH), kql = tc::smem_addr(smem + OFF_KQL);
+    const uint32_t kth = tc::smem_addr(smem + OFF_KTH), ktl = tc::smem_addr(smem + OFF_KTL);
+    const uint32_t mth = tc::smem_addr(smem + OFF_MTH), mtl = tc::smem_addr(smem + OFF_MTL);
+    bool ok = true;
+    int chunk = 0;
+
+#pragma unroll 1
+    for (int64_t c0 = 0; c0 < L; c0 += TC, ++chunk) {
+        const int Lc = static_cast<int>(L - c0 < TC ? L - c0 : TC);
+        const uint32_t par = static_cast<uint32_t>(chunk & 1);
+
+        // ---- (1) value inputs of this thread's row (the solve's right-hand side; LA: d itself)
+        float vv[TC];
+        if (half == 0) {
+#pragma unroll
+            for (int t = 0; t < TC; ++t)
+                vv[t] = t < Lc ? ld_in(p.v, (tb + c0 + t) * p.vs[1] + static_cast<int64_t>(hv) * p.vs[2] +
+                                                static_cast<int64_t>(vrow) * p.vs[3], p.v_dt)
+                               : 0.f;
+        }
+        // k and q rows: warp w takes tokens w, w + 8, ...; lane l channels 4l .. 4l + 3
+#pragma unroll 1
+        for (int t = warp; t < TC; t += TTH / 32) {
+            float qx[4], kx[4];
+            const bool tok = t < Lc;
+            const int64_t gt = tb + c0 + t;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c = lane * 4 + e;
+                qx[e] = tok ? ld_in(p.q, gt * p.qs[1] + h * p.qs[2] + c * p.qs[3], p.q_dt) : 0.f;
+                kx[e] = tok ? ld_in(p.k, gt * p.ks[1] + h * p.ks[2] + c * p.ks[3], p.k_dt) : 0.f;
+            }
+            if (l2) {
+                float sq = 0.f, sk = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    sq = fmaf(qx[e], qx[e], sq);
+                    sk = fmaf(kx[e], kx[e], sk);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                    sk += __shfl_xor_sync(0xffffffffu, sk, off);
+                }
+                const float iq = 1.f / sqrtf(sq + 1e-6f), ik = 1.f / sqrtf(sk + 1e-6f);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    qx[e] *= iq;
+                    kx[e] *= ik;
+                }
+            }
+            float kh[4], kl[4], qh[4], ql[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                kh[e] = tc::tf32_hi(kx[e]);
+                kl[e] = kx[e] - kh[e];
+                qh[e] = tc::tf32_hi(qx[e]);
+                ql[e] = qx[e] - qh[e];
+            }
+            *reinterpret_cast<float4*>(K32 + t * FROW + 4 * lane) = make_float4(kx[0], kx[1], kx[2], kx[3]);
+            *reinterpret_cast<float4*>(Q32 + t * FROW + 4 * lane) = make_float4(qx[0], qx[1], qx[2], qx[3]);
+            const uint32_t ok_ = tc::kmaj(t, 4 * lane, LBO, KQ_SBO), oq_ = tc::kmaj(TC + t, 4 * lane, LBO, KQ_SBO);
+            *reinterpret_cast<float4*>(smem + OFF_KQH + ok_) = make_float4(kh[0], kh[1], kh[2], kh[3]);
+            *reinterpret_cast<float4*>(smem + OFF_KQL + ok_) = make_float4(kl[0], kl[1], kl[2], kl[3]);
+            *reinterpret_cast<float4*>(smem + OFF_KQH + oq_) = make_float4(qh[0], qh[1], qh[2], qh[3]);
+            *reinterpret_cast<float4*>(smem + OFF_KQL + oq_) = make_float4(ql[0], ql[1], ql[2], ql[3]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t o = tc::kmaj(4 * lane + e, t, LBO, KT_SBO);
+                *reinterpret_cast<float*>(smem + OFF_KTH + o) = kh[e];
+                *reinterpret_cast<float*>(smem + OFF_KTL + o) = kl[e];
+            }
+        }
+        // decay factors and betas (warp 0, lane t), then the decay table
+        if (warp == 0) {
+            const int t = lane;
+            float a = 1.f, bt = 0.f;   // padding tokens: no decay, no update
+            if (t < Lc) {
+                const int64_t gt = tb + c0 + t;
+                if constexpr (LA) {
+                    a = p.decay[h * p.dec_s];
+                    bt = 1.f;
+                } else {
+                    float x = ld_in(p.g, gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2], p.g_dt);
+                    if (gate_raw) {
+                        const float bias = p.dt_bias ? p.dt_bias[hv * p.dtb_s] : 0.f;
+                        x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
+                    }
+                    a = expf(x);
+                    const float bx = ld_in(p.beta, gt * p.bs[1] + static_cast<int64_t>(hv) * p.bs[2], p.beta_dt);
+                    bt = beta_raw ? 1.f / (1.f + expf(-bx)) : bx;
+                }
+            }
+            Af[t] = a;
+            Bt[t] = bt;
+            __syncwarp();
+            // row t: P[t][s] = a_{s+1} ... a_t (products, as the recurrence applies them), 0 above
+            float f = 1.f;
+#pragma unroll 1
+            for (int s = TC - 1; s >= 0; --s) {
+                if (s <= t) {
+                    Pt[t * TROW + s] = f;
+                    f *= Af[s];
+                } else {
+                    Pt[t * TROW + s] = 0.f;
+                }
+            }
+            E[t] = f;
+            __syncwarp();
+            Wd[t] = Pt[(TC - 1) * TROW + t];
+        }
+        tc::fence_smem_to_async();
+        tc_sync();
+
+        // ---- (2) [U | P] = S0^T [K ; Q]^T (LA: P only), three tf32 passes
+        if (tid == 0) {
+            constexpr int NUP = LA ? TC : 2 * TC;
+            constexpr uint32_t idesc = tc::idesc_tf32(TVV, NUP);
+            const uint32_t boff = LA ? 4 * KQ_SBO : 0;       // LA: the q rows only
+            const uint32_t dcol = tm + COL_UP + (LA ? TC : 0);
+#pragma unroll 1
+            for (int ps = 0; ps < 3; ++ps) {
+                const uint32_t acol = tm + (ps == 2 ? COL_SLO : COL_SHI);
+                const uint32_t bb = (ps == 1 ? kql : kqh) + boff;
+#pragma unroll 1
+                for (int kb = 0; kb < TK / 8; ++kb)
+                    tc::mma_ts(dcol, acol + 8 * kb, tc::smem_desc(bb + kb * 2 * LBO, LBO, KQ_SBO), idesc,
+                               ps > 0 || kb > 0);
+            }
+            tc::mma_commit(&bar[0]);
+        }
+
+        // ---- (3) meanwhile on the CUDA cores: K K^T, Q K^T with the decay table
+        {
+            const int t = tid >> 3, sg = tid & 7;
+            float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int k = 0; k < TK; k += 4) {
+                const float4 kt = *reinterpret_cast<const float4*>(K32 + t * FROW + k);
+                const float4 qt = *reinterpret_cast<const float4*>(Q32 + t * FROW + k);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 ks = *reinterpret_cast<const float4*>(K32 + (sg + 8 * j) * FROW + k);
+                    if constexpr (!LA)
+                        kk[j] = fmaf(kt.w, ks.w, fmaf(kt.z, ks.z, fmaf(kt.y, ks.y, fmaf(kt.x, ks.x, kk[j]))));
+                    qk[j] = fmaf(qt.w, ks.w, fmaf(qt.z, ks.z, fmaf(qt.y, ks.y, fmaf(qt.x, ks.x, qk[j]))));
+                }
+            }
+            const float bt = Bt[t];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int s = sg + 8 * j;
+                const float pd = Pt[t * TROW + s];
+                if constexpr (!LA) At[t * TROW + s] = s < t ? bt * pd * kk[j] : 0.f;
+                const float m = pd * qk[j];
+                const float mh = tc::tf32_hi(m);
+                const uint32_t o = tc::kmaj(t, s, LBO, MT_SBO);
+                *reinterpret_cast<float*>(smem + OFF_MTH + o) = mh;
+                *reinterpret_cast<float*>(smem + OFF_MTL + o) = m - mh;
+            }
+        }
+        // the state accumulator scaled by E_31 (the products in flight read only its tf32 halves)
+        {
+            const float ec = E[TC - 1];
+#pragma unroll 1
+            for (int c = 0; c < 64; c += 16) {
+                float x[16];
+                tc::tmem_ld16(my + COL_S + col0 + c, x);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x[i] *= ec;
+                tc::tmem_st16(my + COL_S + col0 + c, x);
+            }
+            tc::tmem_st_wait();
+        }
+        tc::fence_smem_to_async();
+
+        // ---- (4) wait for [U | P]; the solve per value row, D and D o W into tensor memory
+        ok = tc::mbar_wait(&bar[0], par);
+        ok = !__syncthreads_or(!ok);
+        if (!ok) break;
+        tc::fence_after_sync();
+        float pv[TC];
+        if (half == 0) {
+            float d[TC];
+            if constexpr (LA) {
+#pragma unroll
+                for (int t = 0; t < TC; ++t) d[t] = vv[t];
+            } else {
+                float u[TC];
+#pragma unroll
+                for (int c = 0; c < TC; c += 16) tc::tmem_ld16(my + COL_UP + c, u + c);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int t = 0; t < TC; ++t) {
+                    // two partial sums halve the dependent chain
+                    float acc0 = Bt[t] * fmaf(-E[t], u[t], vv[t]), acc1 = 0.f;
+#pragma unroll
+                    for (int s = 0; s + 1 < t; s += 2) {
+                        acc0 = fmaf(-At[t * TROW + s], d[s], acc0);
+                        acc1 = fmaf(-At[t * TROW + s + 1], d[s + 1], acc1);
+                    }
+                    if (t & 1) acc0 = fmaf(-At[t * TROW + t - 1], d[t - 1], acc0);
+                    d[t] = acc0 + acc1;
+                }
+            }
+            split_store<TC>(my + COL_DHI, my + COL_DLO, d);
+#pragma unroll
+            for (int t = 0; t < TC; ++t) d[t] *= Wd[t];
+            split_store<TC>(my + COL_DWHI, my + COL_DWLO, d);
+            tc::tmem_st_wait();
+        } else {
+#pragma unroll
+            for (int c = 0; c < TC; c += 16) tc::tmem_ld16(my + COL_UP + TC + c, pv + c);
+            tc::tmem_ld_wait();
+        }
+        tc_sync();
+
+        // ---- (5) O = D M^T and S^T += (D o W) K, three tf32 passes each
+        if (tid == 0) {
+            constexpr uint32_t idesc_o = tc::idesc_tf32(TVV, TC);
+            constexpr uint32_t idesc_s = tc::idesc_tf32(TVV, TK);
+#pragma unroll 1
+            for (int ps = 0; ps < 3; ++ps) {
+                const uint32_t ad = tm + (ps == 2 ? COL_DLO : COL_DHI);
+                const uint32_t aw = tm + (ps == 2 ? COL_DWLO : COL_DWHI);
+                const uint32_t bm = ps == 1 ? mtl : mth;
+                const uint32_t bk = ps == 1 ? ktl : kth;
+#pragma unroll 1
+                for (int kb = 0; kb < TC / 8; ++kb) {
+                    tc::mma_ts(tm + COL_O, ad + 8 * kb, tc::smem_desc(bm + kb * 2 * LBO, LBO, MT_SBO), idesc_o,
+                               ps > 0 || kb > 0);
+                    tc::mma_ts(tm + COL_S, aw + 8 * kb, tc::smem_desc(bk + kb * 2 * LBO, LBO, KT_SBO), idesc_s,
+                               true);
+                }
+            }
+            tc::mma_commit(&bar[1]);
+        }
+        ok = tc::mbar_wait(&bar[1], par);
+        ok = !__syncthreads_or(!ok);
+        if (!ok) break;
+        tc::fence_after_sync();
+
+        // ---- (6) outputs o_t = E_t P[v][t] + O[v][t] (half 1), then the new state's tf32 halves
+        if (half == 1) {
+            float o[TC];
+#pragma unroll
+            for (int c = 0; c < TC; c += 16) tc::tmem_ld16(my + COL_O + c, o + c);
+            tc::tmem_ld_wait();
+            const bool obf = p.out_dt == LAR_BF16;
+#pragma unroll
+            for (int t = 0; t < TC; ++t) {
+                if (t < Lc) {
+                    const float y = fmaf(E[t], pv[t], o[t]) * p.scale;
+                    const int64_t off = (tb + c0 + t) * p.os[1] + static_cast<int64_t>(hv) * p.os[2] +
+                                        static_cast<int64_t>(vrow) * p.os[3];
+                    if (obf) static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(y);
+                    else static_cast<float*>(p.out)[off] = y;
+                }
+            }
+        }
+        tc_sync();
+        if (c0 + TC < L) {
+#pragma unroll 1
+            for (int c = 0; c < 64; c += 16) {
+                float x[16];
+                tc::tmem_ld16(my + COL_S + col0 + c, x);
+                tc::tmem_ld_wait();
+                split_store<16>(my + COL_SHI + col0 + c, my + COL_SLO + col0 + c, x);
+            }
+            tc::tmem_st_wait();
+            tc_sync();
+        }
+    }
+
+    if (!ok) {
+        if (tid == 0 && p.dev_err) atomicOr(p.dev_err, LAR_DEVERR_TIMEOUT);
+    } else if (wr) {
+        // ---- pool[w][hv][v][k] = S^T[v][k]
+        unsigned char* dst = static_cast<unsigned char*>(p.pool) +
+                             (w * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1] + static_cast<int64_t>(vrow) * p.ps[2] +
+                              col0) * SB;
+#pragma unroll 1
+        for (int c = 0; c < 64; c += 16) {
+            float x[16];
+            tc::tmem_ld16(my + COL_S + col0 + c, x);
+            tc::tmem_ld_wait();
+            if constexpr (SB == 4) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    __stcs(reinterpret_cast<float4*>(dst + c * 4) + i,
+                           make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    unsigned wd[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(x[8 * i + 2 * e], x[8 * i + 2 * e + 1]);
+                        wd[e] = *reinterpret_cast<const unsigned*>(&b2);
+                    }
+                    __stcs(reinterpret_cast<uint4*>(dst + c * 2) + i, make_uint4(wd[0], wd[1], wd[2], wd[3]));
+                }
+            }
+        }
+    }
+    tc_sync();
+    if (warp == 0) tc::tmem_dealloc(tm, TMEM_COLS);
+}
+
+template <int FORM, int SB>
+lar_status launch_tc_form(const DecodeParams& p, cudaStream_t stream) {
+    auto kern = prefill_tc_kernel<FORM, SB>;
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(TC_SMEM)) != cudaSuccess)
+        return LAR_ERR_LAUNCH;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.HV), static_cast<unsigned>(p.B));
+    cfg.blockDim = dim3(TTH);
+    cfg.dynamicSmemBytes = TC_SMEM;
+    cfg.stream = stream;
+#if LAR_PDL
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+#endif
+    return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? LAR_OK : LAR_ERR_LAUNCH;
+}
+
+}  // namespace
+
+lar_status launch_prefill_tc(const DecodeParams& p, void* stream) {
+    if (p.K != TK || p.V != TVV) return LAR_ERR_SHAPE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool bf = p.pool_dt == LAR_BF16;
+    if (p.form == FORM_LA) return bf ? launch_tc_form<FORM_LA, 2>(p, st) : launch_tc_form<FORM_LA, 4>(p, st);
+    if (p.form == FORM_GDN) return bf ? launch_tc_form<FORM_GDN, 2>(p, st) : launch_tc_form<FORM_GDN, 4>(p, st);
+    return LAR_ERR_ARG;
+}
+
+}  // namespace lar

@@ -87,6 +87,27 @@ def to_dev(t, dev):
     return None if t is None else t.to(dev)
 
 
+def qkv_dev(w, dev):
+    """w's q, k, v on the device.  Packed workloads stay packed there: the
+    fused buffer is copied once and q, k, v are its head-dim slices, which is
+    asserted on the device tensors themselves."""
+    q, k, v = w.qkv_to(dev)
+    if w.fused is not None:
+        assert_packed_views(w, q, k, v)
+    return q, k, v
+
+
+def assert_packed_views(w, q, k, v):
+    """q, k, v (device tensors) are head-dim slices of one fused buffer: the
+    host views' strides and their element offsets K and 2K inside each row."""
+    es = q.element_size()
+    assert q.is_cuda and not q.is_contiguous()
+    assert q.stride() == w.q.stride() == k.stride() and v.stride() == w.v.stride()
+    assert q.stride()[-2] == 2 * w.K + w.V, q.stride()
+    assert k.data_ptr() == q.data_ptr() + w.K * es
+    assert v.data_ptr() == q.data_ptr() + 2 * w.K * es
+
+
 def run_gpu(w, dev, *, pool=None, read_idx=None, write_idx="same", inter=True, dev_err=None,
             q=None, k=None, v=None):
     """Run w's decode on the GPU.  `pool` (a device view) is updated in place.
@@ -94,9 +115,8 @@ def run_gpu(w, dev, *, pool=None, read_idx=None, write_idx="same", inter=True, d
     pool = pool if pool is not None else w.pool.to(dev)
     ri = to_dev(read_idx if read_idx is not None else w.read_idx, dev)
     wi = to_dev(w.write_idx if write_idx == "same" else write_idx, dev)
-    q = q if q is not None else to_dev(w.q, dev)
-    k = k if k is not None else to_dev(w.k, dev)
-    v = v if v is not None else to_dev(w.v, dev)
+    if q is None and k is None and v is None:
+        q, k, v = qkv_dev(w, dev)
     it = None
     if inter and w.cache_intermediate:
         shape = (w.B, w.T, w.HV, w.K, w.V) if w.state_kv else (w.B, w.T, w.HV, w.V, w.K)
@@ -174,7 +194,7 @@ def run_gpu_varlen(w, dev, *, pool, cu_seqlens=None, dev_err=None, out_fill=floa
     it = None
     if w.cache_intermediate:
         it = torch.full((w.v.shape[0], w.HV, w.V, w.K), out_fill, device=dev, dtype=w.inter_dtype)
-    q, k, v = to_dev(w.q, dev), to_dev(w.k, dev), to_dev(w.v, dev)
+    q, k, v = qkv_dev(w, dev)
     if w.form == "la":
         lar.la_decode_varlen(q, k, v, to_dev(w.decay, dev), pool, cu, ri, wi, out=out, inter=it,
                              scale=w.scale, dev_err=dev_err)

@@ -263,6 +263,19 @@ def prefill_call(lib, a, flags=0):
     return lib.gdn_prefill(*refs, 1.0, flags, None, None)
 
 
+def test_kda_prefill_rejects_on_host(lib):
+    def kda(a, flags=0):
+        refs = [ctypes.byref(a[n]) if a[n] is not None else None for n in PREFILL_ORDER]
+        return lib.kda_prefill(*refs, 1.0, flags, None, None)
+    assert kda(varlen_args(N=0, V=128, kda=True)) == OK
+    assert kda(varlen_args(K=64, V=64, kda=True)) == SHAPE           # built for K = V = 128
+    assert kda(varlen_args(V=128)) == RANK                            # GDN-shaped gate [Ntok, HV]
+    a = varlen_args(V=128, kda=True)
+    a["A_log"], a["dt_bias"] = fake([4]), fake([4])                  # dt_bias must be [HV*K]
+    assert kda(a, flags=2) == SHAPE
+    assert kda(varlen_args(V=128, kda=True), flags=8) == ARG         # no K x V layout
+
+
 def test_prefill_rejects_on_host(lib):
     assert prefill_call(lib, varlen_args(N=0, V=128)) == OK                # no sequences: nothing to do
     assert prefill_call(lib, varlen_args(K=64, V=64)) == SHAPE             # built for K = V = 128
@@ -277,3 +290,63 @@ def test_prefill_rejects_on_host(lib):
                                       ctypes.byref(out), 1.0, None, None)
     assert la(fake([3])) == SHAPE
     assert la(fake([4], BF16)) == DTYPE
+
+
+def _err_word(addr):
+    return ctypes.cast(ctypes.c_void_p(addr), ctypes.POINTER(ctypes.c_int32))
+
+
+def test_dev_err_alignment_and_aliasing(lib):
+    """The device error word is a 4-byte output: misaligned -> ALIGN; inside
+    the pool, the output, the cache or an input -> ALIAS (decode, per-token
+    slots, varlen, prefill and LA calls alike)."""
+    def gdn(a, err):
+        refs = [ctypes.byref(a[n]) if a[n] is not None else None for n in ORDER]
+        return lib.gdn_decode(*refs, 1.0, 0, err, None)
+
+    a = gdn_args()
+    assert gdn(a, _err_word(0x7FF00002)) == ALIGN
+    assert gdn(a, _err_word(a["pool"].data + 4096)) == ALIAS
+    assert gdn(a, _err_word(a["out"].data)) == ALIAS
+    assert gdn(a, _err_word(a["read_idx"].data + 4)) == ALIAS          # an input: the kernel reads it
+    a["inter"] = fake([2, 1, 4, 64, 128])
+    assert gdn(a, _err_word(a["inter"].data + 64)) == ALIAS
+    # a word of its own passes these checks (the call then fails on an unrelated bad argument,
+    # so nothing is launched)
+    a = gdn_args()
+    a["read_idx"] = fake([3], I32)
+    assert gdn(a, _err_word(0x7FF00000)) == SHAPE
+
+    a = gdn_args(B=2, T=3)
+    refs = [ctypes.byref(x) if x is not None else None for x in
+            [a[n] for n in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "pool")] + [a["read_idx"], None,
+                                                                                       fake([2, 3], I32), a["out"]]]
+    assert lib.gdn_decode_tokens(*refs, 1.0, 0, _err_word(a["pool"].data), None) == ALIAS
+    assert lib.gdn_decode_tokens(*refs, 1.0, 0, _err_word(0x7FF00001), None) == ALIGN
+
+    v = varlen_args(V=128)
+    vrefs = [ctypes.byref(v[n]) if v[n] is not None else None for n in VARLEN_ORDER]
+    assert lib.gdn_decode_varlen(*vrefs, 1.0, 0, _err_word(v["cu_seqlens"].data), None) == ALIAS
+    assert lib.gdn_decode_varlen(*vrefs, 1.0, 0, _err_word(0x7FF00003), None) == ALIGN
+    prefs = [ctypes.byref(v[n]) if v[n] is not None else None for n in PREFILL_ORDER]
+    assert lib.gdn_prefill(*prefs, 1.0, 0, _err_word(v["out"].data + 8), None) == ALIAS
+
+    q, k, vv = fake([2, 4, 128], BF16), fake([2, 4, 128], BF16), fake([2, 4, 128], BF16)
+    pool, decay, ri, out = fake([5 * 4, 128, 128]), fake([4]), fake([2], I64), fake([2, 4, 128], BF16)
+    refs = [ctypes.byref(x) for x in (q, k, vv, decay, pool, ri)] + [None, ctypes.byref(out), None]
+    assert lib.la_decode(*refs, 1.0, _err_word(decay.data), None) == ALIAS
+    assert lib.la_decode(*refs, 1.0, _err_word(0x7FF00002), None) == ALIGN
+
+
+def test_binding_rejects_cpu_and_mixed_devices():
+    """The Python binding places a call on the one device all of its tensors
+    share; CPU tensors and mixed devices are refused before the C ABI is
+    reached (checked here with CPU and meta tensors, which need no GPU)."""
+    import torch
+    cpu = torch.zeros(4)
+    with pytest.raises(ValueError, match="CUDA tensors only"):
+        binding._device_of([cpu, cpu])
+    with pytest.raises(ValueError, match="one CUDA device"):
+        binding._device_of([cpu, torch.empty(4, device="meta")])
+    with pytest.raises(ValueError, match="one CUDA device"):
+        binding._device_of([cpu], dev_err=torch.empty(1, dtype=torch.int32, device="meta"))

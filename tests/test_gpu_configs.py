@@ -126,19 +126,25 @@ def test_full_size_varlen(cuda_device):
         P.assert_state_close(w.pool[int(w.write_idx[n])], ref["final_state"][0], f"sequence {n} state")
 
 
-def test_full_size_prefill(cuda_device):
-    """gdn_prefill_n16 at full size through the chunked call: every untouched
-    pool byte bit-identical; sampled sequences (first, last, the longest and
-    seeded others) against the oracle, outputs of their tokens and their
-    written states."""
+@pytest.mark.parametrize("name", ["gdn_prefill_n16", "kda_prefill_n16"])
+def test_full_size_prefill(name, cuda_device):
+    """The prefill workloads at full size through the chunked call: every
+    untouched pool byte bit-identical; sampled sequences (first, last, the
+    longest and seeded others) against the oracle, outputs of their tokens and
+    their written states."""
     import linear_attention_recurrent_gb300 as lar
     import oracle
     dev = cuda_device
-    w = W.make("gdn_prefill_n16", pool_device=dev)
+    w = W.make(name, pool_device=dev)
     before = w.pool.clone()
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    out = lar.gdn_prefill(w.q.to(dev), w.k.to(dev), w.v.to(dev), w.g.to(dev), w.beta.to(dev), w.pool,
-                          w.cu_seqlens.to(dev), w.read_idx.to(dev), w.write_idx.to(dev), dev_err=err)
+    fn = lar.gdn_prefill if w.form == "gdn" else lar.kda_prefill
+    ofn = oracle.gdn_decode_varlen if w.form == "gdn" else oracle.kda_decode_varlen
+    gates = dict(A_log=w.A_log, dt_bias=w.dt_bias, qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw,
+                 beta_raw=w.beta_raw)
+    dev_gates = {n: (x.to(dev) if isinstance(x, torch.Tensor) else x) for n, x in gates.items()}
+    out = fn(w.q.to(dev), w.k.to(dev), w.v.to(dev), w.g.to(dev), w.beta.to(dev), w.pool,
+             w.cu_seqlens.to(dev), w.read_idx.to(dev), w.write_idx.to(dev), dev_err=err, **dev_gates)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     mask = P.written_mask(w).to(dev)
@@ -150,7 +156,7 @@ def test_full_size_prefill(cuda_device):
         lo, hi = int(cu[n]), int(cu[n + 1])
         sub = before[int(w.read_idx[n])].cpu()[None].clone()
         tok = lambda t: t[lo:hi]
-        ref = oracle.gdn_decode_varlen(tok(w.q), tok(w.k), tok(w.v), tok(w.g), tok(w.beta), sub,
-                                       torch.tensor([0, hi - lo]), torch.tensor([0]), torch.tensor([-1]))
+        ref = ofn(tok(w.q), tok(w.k), tok(w.v), tok(w.g), tok(w.beta), sub,
+                  torch.tensor([0, hi - lo]), torch.tensor([0]), torch.tensor([-1]), **gates)
         P.assert_out_close(out[lo:hi], ref["out"], f"sequence {n} out")
         P.assert_state_close(w.pool[int(w.write_idx[n])], ref["final_state"][0], f"sequence {n} state")

@@ -71,12 +71,13 @@ def test_guards_and_parity(name, cuda_device):
         ishape = (w.B, w.T, w.HV, w.K, w.V) if w.state_kv else (w.B, w.T, w.HV, w.V, w.K)
         big_inter, inter = _guarded(ishape, w.inter_dtype, dev)
     cu = lambda t: None if t is None else t.to(dev)
+    q, k, v = P.qkv_dev(w, dev)
     if form == "la":
-        lar.la_decode(cu(w.q), cu(w.k), cu(w.v), cu(w.decay), pool, cu(w.read_idx), cu(w.write_idx),
+        lar.la_decode(q, k, v, cu(w.decay), pool, cu(w.read_idx), cu(w.write_idx),
                       out=out, inter=inter, scale=w.scale)
     else:
         fn = lar.gdn_decode if form == "gdn" else lar.kda_decode
-        fn(cu(w.q), cu(w.k), cu(w.v), cu(w.g), cu(w.beta), pool, cu(w.read_idx), cu(w.write_idx),
+        fn(q, k, v, cu(w.g), cu(w.beta), pool, cu(w.read_idx), cu(w.write_idx),
            out=out, inter=inter, A_log=cu(w.A_log), dt_bias=cu(w.dt_bias), scale=w.scale,
            qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw, state_kv=w.state_kv)
     torch.cuda.synchronize()

@@ -209,11 +209,12 @@ def test_mtp_fp32_state_pool_non_contiguous(B, T, mult, cuda_device):
 def test_packed_equals_contiguous(form, T, cuda_device):
     kw = dict(flat_pool=True) if form == "la" else dict(raw_gates=form == "kda")
     w = W.make_custom(form, B=5, T=T, H=3, HV=3, K=128, V=128, packed=True, seed=T, **kw)
-    assert not w.q.is_contiguous()
+    q, k, v = P.qkv_dev(w, cuda_device)    # slices of one fused device buffer (asserted)
+    qc, kc, vc = (x.contiguous() for x in (q, k, v))
+    assert qc.is_contiguous() and qc.data_ptr() != q.data_ptr()
     pa, pb = w.pool.to(cuda_device), w.pool.to(cuda_device)
-    oa = P.run_gpu(w, cuda_device, pool=pa)[0]
-    ob = P.run_gpu(w, cuda_device, pool=pb, q=w.q.contiguous().to(cuda_device),
-                   k=w.k.contiguous().to(cuda_device), v=w.v.contiguous().to(cuda_device))[0]
+    oa = P.run_gpu(w, cuda_device, pool=pa, q=q, k=k, v=v)[0]
+    ob = P.run_gpu(w, cuda_device, pool=pb, q=qc, k=kc, v=vc)[0]
     torch.cuda.synchronize()
     assert torch.equal(oa, ob)
     assert torch.equal(pa, pb)

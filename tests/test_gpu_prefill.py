@@ -33,18 +33,28 @@ CASES = {
     "la": dict(form="la", lengths=SPANS, H=3),
     "la_flat_bf16": dict(form="la", lengths=[33, 0, 64, 7], H=2, flat_pool=True, state_dtype=BF16),
     "la_packed": dict(form="la", lengths=[45, 90], H=2, packed=True),
+    # KDA: per-key-channel decay inside the chunk products (raw gates: in-kernel gate chain,
+    # l2 norm and sigmoid, decays down to exp(-16 softplus(.)) per token, whose products underflow)
+    "kda_raw_gates": dict(form="kda", lengths=SPANS, H=2, HV=2, raw_gates=True),
+    "kda_activated_gqa": dict(form="kda", lengths=SPANS, H=1, HV=3),
+    "kda_bf16_pool": dict(form="kda", lengths=SPANS, H=2, HV=2, raw_gates=True, state_dtype=BF16),
+    "kda_long": dict(form="kda", lengths=[1000], H=1, HV=2, raw_gates=True),
+    "kda_separate_skip_fp32_io": dict(form="kda", lengths=[40, 5, 96, 0, 70, 3], H=2, HV=2, separate_write=True,
+                                      skip_frac=0.34, in_dtype=F32, out_dtype=F32, raw_gates=True),
+    "kda_packed_strided": dict(form="kda", lengths=[50, 129], H=2, HV=2, packed=True, raw_gates=True, stride_mult=2),
 }
 
 
 def _run_prefill(w, dev, pool, cu_seqlens=None, dev_err=None):
     cu = P.to_dev(w.cu_seqlens if cu_seqlens is None else cu_seqlens, dev)
     out = torch.full(tuple(w.v.shape), float("nan"), dtype=w.out_dtype, device=dev)
-    q, k, v = P.to_dev(w.q, dev), P.to_dev(w.k, dev), P.to_dev(w.v, dev)
+    q, k, v = P.qkv_dev(w, dev)
     ri, wi = P.to_dev(w.read_idx, dev), P.to_dev(w.write_idx, dev)
     if w.form == "la":
         lar.la_prefill(q, k, v, P.to_dev(w.decay, dev), pool, cu, ri, wi, out=out, scale=w.scale, dev_err=dev_err)
     else:
-        lar.gdn_prefill(q, k, v, P.to_dev(w.g, dev), P.to_dev(w.beta, dev), pool, cu, ri, wi, out=out,
+        fn = lar.gdn_prefill if w.form == "gdn" else lar.kda_prefill
+        fn(q, k, v, P.to_dev(w.g, dev), P.to_dev(w.beta, dev), pool, cu, ri, wi, out=out,
                         A_log=P.to_dev(w.A_log, dev), dt_bias=P.to_dev(w.dt_bias, dev), scale=w.scale,
                         qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw, dev_err=dev_err)
     return out
@@ -86,10 +96,37 @@ def test_prefill_parity(name, cuda_device):
     prefill_check(w, cuda_device)
 
 
-def test_prefill_bad_spans(cuda_device):
-    w = W.make_varlen("gdn", [40, 6, 3, 5], H=1, HV=2, K=128, V=128, seed=72, separate_write=True)
+@pytest.mark.parametrize("form", ["gdn", "kda"])
+def test_prefill_bad_spans(form, cuda_device):
+    w = W.make_varlen(form, [40, 6, 3, 5], H=1, HV=2, K=128, V=128, seed=72, separate_write=True,
+                      raw_gates=form == "kda")
     cu = torch.tensor([0, 40, 46, 3, 80], dtype=torch.int32)       # [0,40) [40,46) [46,3) [3,80)
     prefill_check(w, cuda_device, cu_seqlens=cu, expect_err=lar.LAR_DEVERR_SEQLEN)
+
+
+def test_kda_prefill_then_decode_equals_one_recurrence(cuda_device):
+    """KDA: the chunked call over 300 tokens, then the multi-token decode of the
+    next 4 from the state it left, against the oracle on all 304 tokens."""
+    dev = cuda_device
+    w = W.make_varlen("kda", [304], H=2, HV=2, K=128, V=128, P=4, seed=76, raw_gates=True)
+    slot = torch.tensor([2], dtype=torch.int32, device=dev)
+    pool = w.pool.to(dev)
+    part = lambda x, a, b: P.to_dev(x[a:b], dev)
+    kw = dict(A_log=P.to_dev(w.A_log, dev), dt_bias=P.to_dev(w.dt_bias, dev), qk_l2norm=True, gate_raw=True,
+              beta_raw=True, scale=w.scale)
+    lar.kda_prefill(part(w.q, 0, 300), part(w.k, 0, 300), part(w.v, 0, 300), part(w.g, 0, 300),
+                    part(w.beta, 0, 300), pool, torch.tensor([0, 300], dtype=torch.int32, device=dev), slot, slot,
+                    **kw)
+    tail = lambda x: P.to_dev(x[300:304][None], dev)
+    out = lar.kda_decode(tail(w.q), tail(w.k), tail(w.v), tail(w.g), tail(w.beta), pool, slot, slot, **kw)
+    torch.cuda.synchronize()
+    import oracle
+    host = w.pool.clone()
+    ref = oracle.kda_decode_varlen(w.q, w.k, w.v, w.g, w.beta, host, torch.tensor([0, 304]), torch.tensor([2]),
+                                   torch.tensor([2]), A_log=w.A_log, dt_bias=w.dt_bias, qk_l2norm=True,
+                                   gate_raw=True, beta_raw=True, scale=w.scale)
+    P.assert_out_close(out[0], ref["out"][300:304])
+    P.assert_state_close(pool[2].cpu(), ref["final_state"][0], "slot 2")
 
 
 def test_prefill_then_decode_equals_one_recurrence(cuda_device):
@@ -123,8 +160,7 @@ def test_prefill_close_to_token_by_token(cuda_device):
     dev = cuda_device
     w = W.make_varlen("gdn", [1, 4, 40, 200, 0, 77], H=2, HV=4, K=128, V=128, seed=74, in_dtype=F32, out_dtype=F32)
     pa, pb = w.pool.to(dev), w.pool.to(dev)
-    args = lambda: (P.to_dev(w.q, dev), P.to_dev(w.k, dev), P.to_dev(w.v, dev), P.to_dev(w.g, dev),
-                    P.to_dev(w.beta, dev))
+    args = lambda: (*P.qkv_dev(w, dev), P.to_dev(w.g, dev), P.to_dev(w.beta, dev))
     cu, ri = P.to_dev(w.cu_seqlens, dev), P.to_dev(w.read_idx, dev)
     oa = lar.gdn_prefill(*args(), pa, cu, ri, scale=w.scale)
     ob = lar.gdn_decode_varlen(*args(), pb, cu, ri, scale=w.scale)

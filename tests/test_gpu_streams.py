@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _call(w, dev, pool, out, stream):
-    kw = dict(q=P.to_dev(w.q, dev), k=P.to_dev(w.k, dev), v=P.to_dev(w.v, dev), pool=pool,
+    kw = dict(zip("qkv", P.qkv_dev(w, dev)), pool=pool,
               read_idx=P.to_dev(w.read_idx, dev), write_idx=P.to_dev(w.write_idx, dev), out=out)
     if w.form == "la":
         kw["decay"] = P.to_dev(w.decay, dev)

@@ -125,8 +125,7 @@ def test_varlen_empty_batch_and_all_empty_spans(cuda_device):
     empty = torch.empty(0, dtype=torch.int32, device=dev)
     pool = w.pool.to(dev)
     before = pool.clone()
-    lar.gdn_decode_varlen(P.to_dev(w.q, dev), P.to_dev(w.k, dev), P.to_dev(w.v, dev), P.to_dev(w.g, dev),
-                          P.to_dev(w.beta, dev), pool, cu, empty, empty)
+    lar.gdn_decode_varlen(*P.qkv_dev(w, dev), P.to_dev(w.g, dev), P.to_dev(w.beta, dev), pool, cu, empty, empty)
     torch.cuda.synchronize()
     assert torch.equal(pool, before)
 
@@ -138,7 +137,7 @@ def test_varlen_graph_replay(cuda_device):
     pool_g, pool_e = w.pool.to(dev), w.pool.to(dev)
     out_g = torch.empty(tuple(w.v.shape), dtype=w.out_dtype, device=dev)
     out_e = torch.empty_like(out_g)
-    args = dict(q=P.to_dev(w.q, dev), k=P.to_dev(w.k, dev), v=P.to_dev(w.v, dev), g=P.to_dev(w.g, dev),
+    args = dict(zip("qkv", P.qkv_dev(w, dev)), g=P.to_dev(w.g, dev),
                 beta=P.to_dev(w.beta, dev), cu_seqlens=P.to_dev(w.cu_seqlens, dev),
                 read_idx=P.to_dev(w.read_idx, dev), write_idx=P.to_dev(w.write_idx, dev))
     side = torch.cuda.Stream(device=dev)

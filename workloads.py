@@ -44,6 +44,11 @@ gdn_varlen_b64     N=64 variable-length spans (draw order: 48 lengths U{1..4}, 1
 gdn_prefill_n16    N=16 spans, lengths U{256..1024} (drawn first), otherwise drawn as
                    gdn_varlen_b64; pool [64,32,128,128], read = write =
                    randperm(64)[:16]; run through the chunked prefill call; seed 8
+kda_prefill_n16    N=16 spans, lengths U{256..1024} (drawn first), H=HV=24
+                   K=V=128, token-major raw bf16 q/k/a drawn as kda_b256 draws
+                   them (l2 norm, gate chain and sigmoid in kernel); pool
+                   [64,24,128,128], read = write = randperm(64)[:16]; run
+                   through the chunked prefill call; seed 9
 =================  ===========================================================
 
 Pool entries are N(0, 0.1^2) (standard deviation 0.1).  Full-size pools are
@@ -64,11 +69,11 @@ F32 = torch.float32
 
 CONFIGS = ("gdn_tiny", "gdn_b64", "gdn_mtp_strided", "kda_b256", "la_b512_packed",
            "gdn_b64_bf16", "gdn_spec_b64", "gdn_b64_kv", "gdn_b64_kv_bf16", "kda_b256_bf16",
-           "la_b512_bf16", "gdn_varlen_b64", "gdn_prefill_n16")
+           "la_b512_bf16", "gdn_varlen_b64", "gdn_prefill_n16", "kda_prefill_n16")
 SEEDS = {"gdn_tiny": 0, "gdn_b64": 2, "gdn_mtp_strided": 3, "kda_b256": 4,
          "la_b512_packed": 5, "gdn_b64_bf16": 2, "gdn_spec_b64": 6, "gdn_b64_kv": 2,
          "gdn_b64_kv_bf16": 2, "kda_b256_bf16": 4, "la_b512_bf16": 5, "gdn_varlen_b64": 7,
-         "gdn_prefill_n16": 8}
+         "gdn_prefill_n16": 8, "kda_prefill_n16": 9}
 
 
 @dataclass
@@ -161,6 +166,24 @@ class Workload:
             return int((cu[1:] - cu[:-1]).clamp(min=0).sum())
         return self.B * self.T
 
+    def qkv_to(self, device):
+        """(q, k, v) on `device`.  When they are views of one fused buffer, that
+        buffer is copied once (same shape and strides) and q, k, v become the
+        same views of the copy (same shapes, strides and offsets), so a call on
+        the device sees the packed layout.  (`Tensor.to` of a non-dense view
+        would hand back a dense copy.)"""
+        if self.fused is None:
+            return self.q.to(device), self.k.to(device), self.v.to(device)
+        f = self.fused
+        fd = torch.empty_strided(f.shape, f.stride(), dtype=f.dtype, device=device)
+        fd.copy_(f)
+
+        def view(t):
+            assert t.untyped_storage().data_ptr() == f.untyped_storage().data_ptr()
+            return fd.as_strided(t.shape, t.stride(), fd.storage_offset() + t.storage_offset() - f.storage_offset())
+
+        return view(self.q), view(self.k), view(self.v)
+
 
 def _normal(gen, shape, std=1.0):
     return torch.randn(shape, generator=gen, dtype=F32) * std
@@ -185,7 +208,7 @@ def make_meta(name: str) -> dict:
     """Workload flags known without drawing it (which call runs it)."""
     if name not in CONFIGS:
         raise KeyError(name)
-    return {"prefill": name == "gdn_prefill_n16"}
+    return {"prefill": name in ("gdn_prefill_n16", "kda_prefill_n16")}
 
 
 def make(name: str, *, seed: int | None = None, pool_device="cpu",
@@ -305,6 +328,25 @@ def make(name: str, *, seed: int | None = None, pool_device="cpu",
         pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
         return Workload(name, "gdn", N, 0, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
                         BF16, g=g, beta=beta, cu_seqlens=cu, meta={"prefill": True})
+    if name == "kda_prefill_n16":
+        # long spans for the chunked KDA call: 16 sequences of 256-1024 tokens
+        N, H, HV, K, V, P = 16, 24, 24, 128, 128, 64
+        lengths = torch.randint(256, 1025, (N,), generator=gen)
+        cu = torch.zeros(N + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(lengths, 0).to(torch.int32)
+        NT = int(cu[-1])
+        q = _normal(gen, (NT, H, K)).to(BF16)
+        k = _normal(gen, (NT, H, K)).to(BF16)
+        v = _normal(gen, (NT, HV, V)).to(BF16)
+        a = _normal(gen, (NT, HV, K)).to(BF16)
+        b_raw = _normal(gen, (NT, HV))
+        A_log = torch.empty(HV).uniform_(math.log(1.0), math.log(16.0), generator=gen)
+        dt_bias = _normal(gen, (HV * K,), 0.1)
+        ri = torch.randperm(P, generator=gen)[:N].to(index_dtype)
+        pool = _draw_pool(gen, (P, HV, V, K), s, pool_device)
+        return Workload(name, "kda", N, 0, H, HV, K, V, P, q, k, v, pool, ri, ri.clone(),
+                        BF16, g=a, beta=b_raw, A_log=A_log, dt_bias=dt_bias, cu_seqlens=cu,
+                        qk_l2norm=True, gate_raw=True, beta_raw=True, meta={"prefill": True})
     raise KeyError(name)
 
 
