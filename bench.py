@@ -330,6 +330,7 @@ def run_lar(args, world, rank, local):
     with torch.cuda.stream(stream):
         first = torch.cuda.Event(enable_timing=True)
         last = torch.cuda.Event(enable_timing=True)
+        hold_stream(stream)
         first.record(stream)
         for i in range(args.steps):
             calls[i % n_sets]()
@@ -378,6 +379,16 @@ def run_lar(args, world, rank, local):
         "clocks": clocks,
     }
     return line
+
+
+def hold_stream(stream, cycles=400_000):
+    """Keep `stream` busy (a spin kernel of ~0.2 ms) while the host enqueues
+    the timed launches behind it, so the first timed launch does not wait for
+    the host: the events then bracket back-to-back device work only."""
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None:
+        with torch.cuda.stream(stream):
+            sleep(cycles)
 
 
 def roofline(w, config, mean_launch_ms, achieved_gbs, peak_gbs, peak_kind):

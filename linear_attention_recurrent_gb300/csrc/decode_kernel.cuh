@@ -69,6 +69,14 @@
 #ifndef LAR_PDL
 #define LAR_PDL 1
 #endif
+// 1: at a pair's first tile the ring refill is issued before the pair preamble
+#ifndef LAR_EARLY_ISSUE
+#define LAR_EARLY_ISSUE 0
+#endif
+// upper bound on the resident CTAs per SM the persistent grid is sized for
+#ifndef LAR_OCC_CAP
+#define LAR_OCC_CAP 64
+#endif
 #ifndef LAR_K128_BF16_S
 #define LAR_K128_BF16_S 3
 #endif
@@ -99,6 +107,36 @@ __device__ __forceinline__ float bf16_bits_to_float(unsigned short x) {
 __device__ __forceinline__ float ld_in(const void* base, int64_t off, int dt) {
     if (dt == LAR_F32) return __ldg(static_cast<const float*>(base) + off);
     return bf16_bits_to_float(__ldg(static_cast<const unsigned short*>(base) + off));
+}
+
+// x[e] = element off + e * st (e = 0..3), fp32 or bf16, with one vector load
+// when the four are contiguous and aligned for it
+__device__ __forceinline__ void ld_in4(const void* base, int64_t off, int64_t st, int dt, float* x) {
+    if (st == 1) {
+        if (dt == LAR_BF16) {
+            const unsigned short* q = static_cast<const unsigned short*>(base) + off;
+            if ((reinterpret_cast<uintptr_t>(q) & 7) == 0) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(q));
+                x[0] = __uint_as_float(u.x << 16);
+                x[1] = __uint_as_float(u.x & 0xffff0000u);
+                x[2] = __uint_as_float(u.y << 16);
+                x[3] = __uint_as_float(u.y & 0xffff0000u);
+                return;
+            }
+        } else {
+            const float* q = static_cast<const float*>(base) + off;
+            if ((reinterpret_cast<uintptr_t>(q) & 15) == 0) {
+                const float4 f = __ldg(reinterpret_cast<const float4*>(q));
+                x[0] = f.x;
+                x[1] = f.y;
+                x[2] = f.z;
+                x[3] = f.w;
+                return;
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = ld_in(base, off + e * st, dt);
 }
 
 __device__ __forceinline__ int64_t ld_idx(const void* base, int64_t off, int dt) {
@@ -573,9 +611,16 @@ decode_kernel(const DecodeParams p) {
 #pragma unroll 1
     for (int64_t n = t_end - t_begin; n > 0; --n) {
         const int b = c_b, hv = c_hv, vt = c_vt;
+        bool early = false;    // this iteration's refill went out before the pair preamble
         if (pair_start) {
             // ---- new (b, hv) pair: slots, bases and per-token vectors
             pair_start = false;
+#if LAR_EARLY_ISSUE
+            // the refill of the stage consumed last iteration goes out first, so
+            // that it is in flight while the preamble waits on its loads
+            issue(stage_next);
+            early = true;
+#endif
             const int h = hv / p.group;
             buf ^= 1;
             const int64_t r = seed_of(b);
@@ -626,7 +671,8 @@ decode_kernel(const DecodeParams p) {
         }
 
         // ---- this thread's copies of the tile have landed: pull its rows into registers
-        cp_async_wait<S - 2>();
+        if (early) cp_async_wait<S - 1>();
+        else cp_async_wait<S - 2>();
         float2 s[NR][KPL / 2];   // element 2e in .x, 2e+1 in .y
         {
             const unsigned char* src = ring + stage * STAGE + s_row0;
@@ -636,7 +682,7 @@ decode_kernel(const DecodeParams p) {
                 for (int c = 0; c < NCH; ++c) chunk_to_f2<SB>(src + i * S_RSTEP + c * CSTEP, &s[i][c * EPC / 2]);
         }
         // refill the stage consumed in the previous iteration (its rows were used long ago)
-        issue(stage_next);
+        if (!early) issue(stage_next);
         stage = stage + 1 == S ? 0 : stage + 1;
         stage_next = stage_next + 1 == S ? 0 : stage_next + 1;
 
@@ -805,8 +851,9 @@ lar_status launch_tile_mode(const DecodeParams& p, cudaStream_t stream) {
     // the largest footprint any call can ask for (T = 16 with staged v)
     constexpr size_t smem_max = decode_smem_bytes<FORM, K, LPR, NR, NW, S, SB>(16, kStageVMax / 16);
     int sms = 0;
-    const int occ = cached_occupancy(reinterpret_cast<const void*>(kern), NW * 32, smem, smem_max, &sms);
+    int occ = cached_occupancy(reinterpret_cast<const void*>(kern), NW * 32, smem, smem_max, &sms);
     if (occ < 1) return LAR_ERR_LAUNCH;
+    if (occ > LAR_OCC_CAP) occ = LAR_OCC_CAP;
     const int nvt = (p.V + G::TV - 1) / G::TV;
     const int64_t tiles = static_cast<int64_t>(p.B) * p.HV * nvt;
     const int64_t cap = static_cast<int64_t>(sms) * occ;

@@ -648,15 +648,15 @@ lar_status launch_prefill_form(const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-// GDN and LA chunk products on the tensor cores (prefill_tc.cu); 0 keeps them
-// on the CUDA cores here
+// chunk products on the tensor cores (prefill_tc.cu); 0 keeps them on the CUDA
+// cores here
 #ifndef LAR_PF_TC
 #define LAR_PF_TC 0
 #endif
 
 lar_status launch_prefill(const DecodeParams& p, void* stream) {
     if (p.K != PK || p.V != PV) return LAR_ERR_SHAPE;
-    if (LAR_PF_TC && p.form != FORM_KDA) return launch_prefill_tc(p, stream);
+    if (LAR_PF_TC) return launch_prefill_tc(p, stream);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool bf = p.pool_dt == LAR_BF16;
     if (p.form == FORM_LA) return bf ? launch_prefill_form<FORM_LA, 2>(p, st) : launch_prefill_form<FORM_LA, 4>(p, st);

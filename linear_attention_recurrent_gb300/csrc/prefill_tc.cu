@@ -1,5 +1,6 @@
-// prefill_tc.cu -- the chunked prefill (gated delta rule with scalar decay, and
-// Lightning Attention) with its matrix products on the tensor cores.
+// prefill_tc.cu -- the chunked prefill (gated delta rule with scalar decay GDN
+// or per-key-channel decay KDA, and Lightning Attention) with its matrix
+// products on the tensor cores.
 //
 // Same operation and chunk algebra as prefill.cu (32-token chunks; with S0 the
 // state entering a chunk, a_t the decay factors, P[t][s] = a_{s+1} ... a_t,
@@ -13,6 +14,11 @@
 //     O       = D M^T                 (128 x 32, reduction over the chunk)
 //     S^T    += (D o W) K             (128 x 128, reduction over the chunk)
 // with D [v][s] = d_s[v], M[t][s] = P[t][s] (q_t . k_s) and W_s = P[31][s].
+// KDA (a decay factor a_t[c] per key channel) takes the decays into the
+// operand rows: E_t[c] k_t[c] and E_t[c] q_t[c] in the first product,
+// P[31][s][c] k_s[c] in the update, diag(E_31) scaling the state's key
+// columns, and A, M from per-channel decay products (running products over
+// the chunk, no exponentials of differences), reduced across a warp.
 //
 // Precision.  The products run as tcgen05.mma kind::tf32 in three passes
 // (A_hi B_hi + A_hi B_lo + A_lo B_hi, each operand split as x = hi + lo with hi
@@ -21,19 +27,24 @@
 // dropped A_lo B_lo term is below 2^-22 relative.
 //
 // Work.  One CTA of 256 threads per (sequence, v-head) keeps that pair's state
-// in tensor memory for the whole span: S^T (fp32, the accumulator of the state
-// update) and its tf32 halves (the A operand of the next chunk's first
-// product).  Thread (warp w, lane l) owns value row v = 32 (w % 4) + l; the two
-// warps of a row split its columns.  Per chunk: the chunk's k and q rows into
+// on chip for the whole span: S^T in fp32 registers (thread (warp w, lane l)
+// owns value row v = 32 (w % 4) + l, the two warps of a row split its
+// columns) and its tf32 halves in tensor memory (the A operand of the next
+// chunk's first product).  The tensor cores produce each chunk's state
+// increment on its own, which the threads add to the decayed state with
+// round-to-nearest fp32 adds: accumulating into the state on the tensor cores,
+// whose adds do not round to nearest, left a drift that grew with the span
+// (4.7e-6 after 257 tokens at a decay of 0.996).  Per chunk: the chunk's k and q rows into
 // shared memory (l2-normalised when asked, fp32 copies and tf32 halves in the
 // K-major tile layout the tensor cores read), the per-token decays and betas;
 // one thread issues [U | P] while the others compute K K^T and Q K^T on the
-// CUDA cores (32 x 32, the decay table folded in) and scale the state by E_31;
-// the triangular solve runs per value row in registers; D and D o W go to
-// tensor memory; one thread issues O and the state update; the outputs
-// E_t P + O are stored and the new state's tf32 halves written back.  Tensor
-// memory holds 448 of 512 columns: S (0..127), S_hi / S_lo (128..383; reused
-// for D, D o W and O after [U | P] has read them), [U | P] (384..447).
+// CUDA cores (32 x 32, the decay table folded in); the triangular solve runs
+// per value row in registers; D and D o W go to tensor memory; one thread
+// issues O and the state increment (D o W) K; the outputs E_t P + O are
+// stored, the state becomes E_31 S + increment and its tf32 halves are written
+// back.  Tensor memory (512 columns): S_hi / S_lo (0..255; reused for D,
+// D o W and O once [U | P] has read them), [U | P] (256..319), the increment
+// (384..511).
 //
 // Every wait is bounded: a wait that gives up makes the whole CTA skip the
 // rest of its span and its writeback, and sets LAR_DEVERR_TIMEOUT.
@@ -72,7 +83,9 @@ constexpr uint32_t OFF_AF = OFF_P + TC * TROW * 4;      // a_t
 constexpr uint32_t OFF_E = OFF_AF + TC * 4;             // E_t
 constexpr uint32_t OFF_W = OFF_E + TC * 4;              // P[31][s]
 constexpr uint32_t OFF_B = OFF_W + TC * 4;              // beta_t
-constexpr uint32_t OFF_BAR = OFF_B + TC * 4;            // two mbarriers
+constexpr uint32_t OFF_AD = OFF_B + TC * 4;             // KDA: a_t[c] [C][K]
+constexpr uint32_t OFF_EC = OFF_AD + TC * TK * 4;       // KDA: E_31[c] [K]
+constexpr uint32_t OFF_BAR = OFF_EC + TK * 4;           // two mbarriers
 constexpr uint32_t OFF_TM = OFF_BAR + 16;               // TMEM base address
 constexpr uint32_t TC_SMEM = OFF_TM + 16;
 static_assert(OFF_KQL % 16 == 0 && OFF_KTH % 16 == 0 && OFF_KTL % 16 == 0 && OFF_MTH % 16 == 0 &&
@@ -84,22 +97,23 @@ static_assert(tc::kmaj(63, TK - 1, LBO, KQ_SBO) + 4 <= KQ_BYTES && tc::kmaj(TK -
 static_assert(TC_SMEM <= 227 * 1024, "fits one CTA's shared memory");
 
 // tensor-memory columns
-constexpr uint32_t COL_S = 0, COL_SHI = 128, COL_SLO = 256, COL_UP = 384;
-constexpr uint32_t COL_DHI = 128, COL_DLO = 160, COL_DWHI = 192, COL_DWLO = 224, COL_O = 256;
+constexpr uint32_t COL_SHI = 0, COL_SLO = 128, COL_UP = 256, COL_DS = 384;
+constexpr uint32_t COL_DHI = 0, COL_DLO = 32, COL_DWHI = 64, COL_DWLO = 96, COL_O = 128;
 constexpr uint32_t TMEM_COLS = 512;
 
+// x (N values, a multiple of 16) into tensor memory as its tf32 halves
 template <int N>
 __device__ __forceinline__ void split_store(uint32_t taddr_hi, uint32_t taddr_lo, const float* x) {
-    float hi[N], lo[N];
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        hi[i] = tc::tf32_hi(x[i]);
-        lo[i] = x[i] - hi[i];
-    }
+    for (int i0 = 0; i0 < N; i0 += 16) {
+        float hi[16], lo[16];
 #pragma unroll
-    for (int i = 0; i < N; i += 16) {
-        tc::tmem_st16(taddr_hi + i, hi + i);
-        tc::tmem_st16(taddr_lo + i, lo + i);
+        for (int i = 0; i < 16; ++i) {
+            hi[i] = tc::tf32_hi(x[i0 + i]);
+            lo[i] = x[i0 + i] - hi[i];
+        }
+        tc::tmem_st16(taddr_hi + i0, hi);
+        tc::tmem_st16(taddr_lo + i0, lo);
     }
 }
 
@@ -113,6 +127,7 @@ __device__ __forceinline__ void tc_sync() {
 template <int FORM, int SB>
 __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p) {
     constexpr bool LA = FORM == FORM_LA;
+    constexpr bool KDA = FORM == FORM_KDA;
     extern __shared__ __align__(1024) unsigned char smem[];
     float* K32 = reinterpret_cast<float*>(smem + OFF_K32);
     float* Q32 = reinterpret_cast<float*>(smem + OFF_Q32);
@@ -122,6 +137,8 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
     float* E = reinterpret_cast<float*>(smem + OFF_E);
     float* Wd = reinterpret_cast<float*>(smem + OFF_W);
     float* Bt = reinterpret_cast<float*>(smem + OFF_B);
+    float* Ad = reinterpret_cast<float*>(smem + OFF_AD);       // KDA only
+    float* EC = reinterpret_cast<float*>(smem + OFF_EC);       // KDA only
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint32_t* tm_slot = reinterpret_cast<uint32_t*>(smem + OFF_TM);
 
@@ -164,14 +181,16 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
     const uint32_t my = tm + lane_off;                         // this thread's lane, column 0
     const int col0 = 64 * half;                                // this thread's 64 state columns
 
-    // ---- S0 into tensor memory: S (fp32) and its tf32 halves
+    // ---- S0: this thread's 64 state values (row vrow, columns col0 ..) into
+    // registers, its tf32 halves into tensor memory
+    float S[64];
     {
         const unsigned char* src = static_cast<const unsigned char*>(p.pool) +
                                    ((rd ? r : 0) * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1] +
                                     static_cast<int64_t>(vrow) * p.ps[2] + col0) * SB;
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < 64; c += 16) {
-            float x[16];
+            float* x = S + c;
             if (rd) {
                 if constexpr (SB == 4) {
 #pragma unroll
@@ -195,9 +214,8 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
 #pragma unroll
                 for (int i = 0; i < 16; ++i) x[i] = 0.f;
             }
-            tc::tmem_st16(my + COL_S + col0 + c, x);
-            split_store<16>(my + COL_SHI + col0 + c, my + COL_SLO + col0 + c, x);
         }
+        split_store<64>(my + COL_SHI + col0, my + COL_SLO + col0, S);
         tc::tmem_st_wait();
     }
     tc_sync();
@@ -225,17 +243,50 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                                                 static_cast<int64_t>(vrow) * p.vs[3], p.v_dt)
                                : 0.f;
         }
-        // k and q rows: warp w takes tokens w, w + 8, ...; lane l channels 4l .. 4l + 3
-#pragma unroll 1
-        for (int t = warp; t < TC; t += TTH / 32) {
-            float qx[4], kx[4];
-            const bool tok = t < Lc;
-            const int64_t gt = tb + c0 + t;
+        // k and q rows: warp w takes tokens w, w + 8, ...; lane l channels 4l .. 4l + 3.
+        // All of a thread's loads are issued before any is used.
+        constexpr int RPW = TC / (TTH / 32);
+        float qa[RPW][4], ka[RPW][4], ga[KDA ? RPW : 1][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int c = lane * 4 + e;
-                qx[e] = tok ? ld_in(p.q, gt * p.qs[1] + h * p.qs[2] + c * p.qs[3], p.q_dt) : 0.f;
-                kx[e] = tok ? ld_in(p.k, gt * p.ks[1] + h * p.ks[2] + c * p.ks[3], p.k_dt) : 0.f;
+        for (int j = 0; j < RPW; ++j) {
+            const int t = warp + j * (TTH / 32);
+            const int64_t gt = tb + c0 + t;
+            const int64_t c = lane * 4;
+            if (t < Lc) {
+                ld_in4(p.q, gt * p.qs[1] + h * p.qs[2] + c * p.qs[3], p.qs[3], p.q_dt, qa[j]);
+                ld_in4(p.k, gt * p.ks[1] + h * p.ks[2] + c * p.ks[3], p.ks[3], p.k_dt, ka[j]);
+                if constexpr (KDA)
+                    ld_in4(p.g, gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2] + c * p.gs[3], p.gs[3], p.g_dt,
+                           ga[j]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    qa[j][e] = ka[j][e] = 0.f;
+                    if constexpr (KDA) ga[j][e] = 0.f;
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < RPW; ++j) {
+            const int t = warp + j * (TTH / 32);
+            const bool tok = t < Lc;
+            float* qx = qa[j];
+            float* kx = ka[j];
+            const float* gk = ga[KDA ? j : 0];
+            if constexpr (KDA) {
+                // per-channel decay factors a_t[c] (gate chain included); padding tokens: 1
+                float a4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float x = gk[e];
+                    if (gate_raw) {
+                        const int c = lane * 4 + e;
+                        const float bias = p.dt_bias ? p.dt_bias[(static_cast<int64_t>(hv) * TK + c) * p.dtb_s] : 0.f;
+                        x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
+                    }
+                    a4[e] = tok ? expf(x) : 1.f;
+                }
+                *reinterpret_cast<float4*>(Ad + t * TK + 4 * lane) = make_float4(a4[0], a4[1], a4[2], a4[3]);
             }
             if (l2) {
                 float sq = 0.f, sk = 0.f;
@@ -256,26 +307,28 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                     kx[e] *= ik;
                 }
             }
-            float kh[4], kl[4], qh[4], ql[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                kh[e] = tc::tf32_hi(kx[e]);
-                kl[e] = kx[e] - kh[e];
-                qh[e] = tc::tf32_hi(qx[e]);
-                ql[e] = qx[e] - qh[e];
-            }
             *reinterpret_cast<float4*>(K32 + t * FROW + 4 * lane) = make_float4(kx[0], kx[1], kx[2], kx[3]);
             *reinterpret_cast<float4*>(Q32 + t * FROW + 4 * lane) = make_float4(qx[0], qx[1], qx[2], qx[3]);
-            const uint32_t ok_ = tc::kmaj(t, 4 * lane, LBO, KQ_SBO), oq_ = tc::kmaj(TC + t, 4 * lane, LBO, KQ_SBO);
-            *reinterpret_cast<float4*>(smem + OFF_KQH + ok_) = make_float4(kh[0], kh[1], kh[2], kh[3]);
-            *reinterpret_cast<float4*>(smem + OFF_KQL + ok_) = make_float4(kl[0], kl[1], kl[2], kl[3]);
-            *reinterpret_cast<float4*>(smem + OFF_KQH + oq_) = make_float4(qh[0], qh[1], qh[2], qh[3]);
-            *reinterpret_cast<float4*>(smem + OFF_KQL + oq_) = make_float4(ql[0], ql[1], ql[2], ql[3]);
+            if constexpr (!KDA) {     // KDA's operand rows carry the decays: written below
+                float kh[4], kl[4], qh[4], ql[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t o = tc::kmaj(4 * lane + e, t, LBO, KT_SBO);
-                *reinterpret_cast<float*>(smem + OFF_KTH + o) = kh[e];
-                *reinterpret_cast<float*>(smem + OFF_KTL + o) = kl[e];
+                for (int e = 0; e < 4; ++e) {
+                    kh[e] = tc::tf32_hi(kx[e]);
+                    kl[e] = kx[e] - kh[e];
+                    qh[e] = tc::tf32_hi(qx[e]);
+                    ql[e] = qx[e] - qh[e];
+                }
+                const uint32_t ok_ = tc::kmaj(t, 4 * lane, LBO, KQ_SBO), oq_ = tc::kmaj(TC + t, 4 * lane, LBO, KQ_SBO);
+                *reinterpret_cast<float4*>(smem + OFF_KQH + ok_) = make_float4(kh[0], kh[1], kh[2], kh[3]);
+                *reinterpret_cast<float4*>(smem + OFF_KQL + ok_) = make_float4(kl[0], kl[1], kl[2], kl[3]);
+                *reinterpret_cast<float4*>(smem + OFF_KQH + oq_) = make_float4(qh[0], qh[1], qh[2], qh[3]);
+                *reinterpret_cast<float4*>(smem + OFF_KQL + oq_) = make_float4(ql[0], ql[1], ql[2], ql[3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t o = tc::kmaj(4 * lane + e, t, LBO, KT_SBO);
+                    *reinterpret_cast<float*>(smem + OFF_KTH + o) = kh[e];
+                    *reinterpret_cast<float*>(smem + OFF_KTL + o) = kl[e];
+                }
             }
         }
         // decay factors and betas (warp 0, lane t), then the decay table
@@ -288,12 +341,14 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                     a = p.decay[h * p.dec_s];
                     bt = 1.f;
                 } else {
-                    float x = ld_in(p.g, gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2], p.g_dt);
-                    if (gate_raw) {
-                        const float bias = p.dt_bias ? p.dt_bias[hv * p.dtb_s] : 0.f;
-                        x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
+                    if constexpr (!KDA) {   // KDA: the decay is per channel (Ad), the scalar factor 1
+                        float x = ld_in(p.g, gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2], p.g_dt);
+                        if (gate_raw) {
+                            const float bias = p.dt_bias ? p.dt_bias[hv * p.dtb_s] : 0.f;
+                            x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
+                        }
+                        a = expf(x);
                     }
-                    a = expf(x);
                     const float bx = ld_in(p.beta, gt * p.bs[1] + static_cast<int64_t>(hv) * p.bs[2], p.beta_dt);
                     bt = beta_raw ? 1.f / (1.f + expf(-bx)) : bx;
                 }
@@ -316,6 +371,86 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
             __syncwarp();
             Wd[t] = Pt[(TC - 1) * TROW + t];
         }
+        if constexpr (KDA) {
+            __syncthreads();
+            // ---- (1b) KDA: A[t][s] = beta_t sum_c k_t[c] k_s[c] P[t][s][c] (s < t) and
+            // M[t][s] = sum_c q_t[c] k_s[c] P[t][s][c] (s <= t), P[t][s][c] = a_{s+1}[c] ... a_t[c]
+            // kept as a running product over t (factors <= 1: nothing overflows).  Warp w
+            // takes s = w, w + 8, ...; lane l channels 4l .. 4l + 3; each lane's 32 partial sums
+            // (one per t) are reduced across the warp by recursive halving, which leaves lane
+            // l holding the sums for t = l.
+            static_assert(TC == 32, "one token per lane after the reduction");
+#pragma unroll 1
+            for (int s = warp; s < TC; s += TTH / 32) {
+                const float4 ks = *reinterpret_cast<const float4*>(K32 + s * FROW + 4 * lane);
+                float4 pr = make_float4(1.f, 1.f, 1.f, 1.f);
+                float va[TC], vm[TC];
+#pragma unroll
+                for (int t = 0; t < TC; ++t) {
+                    va[t] = 0.f;
+                    vm[t] = 0.f;
+                    if (t >= s) {
+                        if (t > s) {
+                            const float4 a4 = *reinterpret_cast<const float4*>(Ad + t * TK + 4 * lane);
+                            pr = make_float4(pr.x * a4.x, pr.y * a4.y, pr.z * a4.z, pr.w * a4.w);
+                        }
+                        const float4 kt = *reinterpret_cast<const float4*>(K32 + t * FROW + 4 * lane);
+                        const float4 qt = *reinterpret_cast<const float4*>(Q32 + t * FROW + 4 * lane);
+                        const float wx = ks.x * pr.x, wy = ks.y * pr.y, wz = ks.z * pr.z, ww = ks.w * pr.w;
+                        va[t] = fmaf(kt.w, ww, fmaf(kt.z, wz, fmaf(kt.y, wy, kt.x * wx)));
+                        vm[t] = fmaf(qt.w, ww, fmaf(qt.z, wz, fmaf(qt.y, wy, qt.x * wx)));
+                    }
+                }
+#pragma unroll
+                for (int nn = TC / 2; nn >= 1; nn >>= 1) {
+                    const bool up = (lane & nn) != 0;
+#pragma unroll
+                    for (int i = 0; i < nn; ++i) {
+                        const float sa = up ? va[i] : va[i + nn];
+                        const float sq = up ? vm[i] : vm[i + nn];
+                        const float ka = up ? va[i + nn] : va[i];
+                        const float kq = up ? vm[i + nn] : vm[i];
+                        va[i] = ka + __shfl_xor_sync(0xffffffffu, sa, nn);
+                        vm[i] = kq + __shfl_xor_sync(0xffffffffu, sq, nn);
+                    }
+                }
+                const int t = lane;
+                At[t * TROW + s] = t > s ? Bt[t] * va[0] : 0.f;
+                const float m = t >= s ? vm[0] : 0.f;
+                const float mh = tc::tf32_hi(m);
+                const uint32_t o = tc::kmaj(t, s, LBO, MT_SBO);
+                *reinterpret_cast<float*>(smem + OFF_MTH + o) = mh;
+                *reinterpret_cast<float*>(smem + OFF_MTL + o) = m - mh;
+            }
+            // per channel c: the update's rows P[31][s][c] k_s[c] (a running product from the
+            // chunk's end), the first product's rows E_t[c] k_t[c] and E_t[c] q_t[c], and E_31[c]
+            if (tid < TK) {
+                const int c = tid;
+                float wv = 1.f;
+#pragma unroll 4
+                for (int s2 = TC - 1; s2 >= 0; --s2) {
+                    const float x = K32[s2 * FROW + c] * wv;
+                    const float xh = tc::tf32_hi(x);
+                    const uint32_t o = tc::kmaj(c, s2, LBO, KT_SBO);
+                    *reinterpret_cast<float*>(smem + OFF_KTH + o) = xh;
+                    *reinterpret_cast<float*>(smem + OFF_KTL + o) = x - xh;
+                    wv *= Ad[s2 * TK + c];
+                }
+                float ev = 1.f;
+#pragma unroll 4
+                for (int t = 0; t < TC; ++t) {
+                    ev *= Ad[t * TK + c];
+                    const float xk = K32[t * FROW + c] * ev, xq = Q32[t * FROW + c] * ev;
+                    const float kh = tc::tf32_hi(xk), qh = tc::tf32_hi(xq);
+                    const uint32_t ok_ = tc::kmaj(t, c, LBO, KQ_SBO), oq_ = tc::kmaj(TC + t, c, LBO, KQ_SBO);
+                    *reinterpret_cast<float*>(smem + OFF_KQH + ok_) = kh;
+                    *reinterpret_cast<float*>(smem + OFF_KQL + ok_) = xk - kh;
+                    *reinterpret_cast<float*>(smem + OFF_KQH + oq_) = qh;
+                    *reinterpret_cast<float*>(smem + OFF_KQL + oq_) = xq - qh;
+                }
+                EC[c] = ev;
+            }
+        }
         tc::fence_smem_to_async();
         tc_sync();
 
@@ -337,8 +472,8 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
             tc::mma_commit(&bar[0]);
         }
 
-        // ---- (3) meanwhile on the CUDA cores: K K^T, Q K^T with the decay table
-        {
+        // ---- (3) meanwhile on the CUDA cores: K K^T, Q K^T with the decay table (KDA: done above)
+        if constexpr (!KDA) {
             const int t = tid >> 3, sg = tid & 7;
             float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
@@ -365,20 +500,6 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                 *reinterpret_cast<float*>(smem + OFF_MTH + o) = mh;
                 *reinterpret_cast<float*>(smem + OFF_MTL + o) = m - mh;
             }
-        }
-        // the state accumulator scaled by E_31 (the products in flight read only its tf32 halves)
-        {
-            const float ec = E[TC - 1];
-#pragma unroll 1
-            for (int c = 0; c < 64; c += 16) {
-                float x[16];
-                tc::tmem_ld16(my + COL_S + col0 + c, x);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) x[i] *= ec;
-                tc::tmem_st16(my + COL_S + col0 + c, x);
-            }
-            tc::tmem_st_wait();
         }
         tc::fence_smem_to_async();
 
@@ -423,7 +544,7 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
         }
         tc_sync();
 
-        // ---- (5) O = D M^T and S^T += (D o W) K, three tf32 passes each
+        // ---- (5) O = D M^T and the increment (D o W) K, three tf32 passes each
         if (tid == 0) {
             constexpr uint32_t idesc_o = tc::idesc_tf32(TVV, TC);
             constexpr uint32_t idesc_s = tc::idesc_tf32(TVV, TK);
@@ -437,8 +558,8 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                 for (int kb = 0; kb < TC / 8; ++kb) {
                     tc::mma_ts(tm + COL_O, ad + 8 * kb, tc::smem_desc(bm + kb * 2 * LBO, LBO, MT_SBO), idesc_o,
                                ps > 0 || kb > 0);
-                    tc::mma_ts(tm + COL_S, aw + 8 * kb, tc::smem_desc(bk + kb * 2 * LBO, LBO, KT_SBO), idesc_s,
-                               true);
+                    tc::mma_ts(tm + COL_DS, aw + 8 * kb, tc::smem_desc(bk + kb * 2 * LBO, LBO, KT_SBO), idesc_s,
+                               ps > 0 || kb > 0);
                 }
             }
             tc::mma_commit(&bar[1]);
@@ -466,15 +587,21 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                 }
             }
         }
-        tc_sync();
-        if (c0 + TC < L) {
-#pragma unroll 1
+        // the new state E_31 S + increment (KDA: E_31 per key column), rounded to nearest
+        {
+            const float ec = E[TC - 1];
+#pragma unroll
             for (int c = 0; c < 64; c += 16) {
                 float x[16];
-                tc::tmem_ld16(my + COL_S + col0 + c, x);
+                tc::tmem_ld16(my + COL_DS + col0 + c, x);
                 tc::tmem_ld_wait();
-                split_store<16>(my + COL_SHI + col0 + c, my + COL_SLO + col0 + c, x);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) S[c + i] = fmaf(KDA ? EC[col0 + c + i] : ec, S[c + i], x[i]);
             }
+        }
+        tc_sync();
+        if (c0 + TC < L) {
+            split_store<64>(my + COL_SHI + col0, my + COL_SLO + col0, S);
             tc::tmem_st_wait();
             tc_sync();
         }
@@ -487,11 +614,9 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
         unsigned char* dst = static_cast<unsigned char*>(p.pool) +
                              (w * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1] + static_cast<int64_t>(vrow) * p.ps[2] +
                               col0) * SB;
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < 64; c += 16) {
-            float x[16];
-            tc::tmem_ld16(my + COL_S + col0 + c, x);
-            tc::tmem_ld_wait();
+            const float* x = S + c;
             if constexpr (SB == 4) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
@@ -544,6 +669,7 @@ lar_status launch_prefill_tc(const DecodeParams& p, void* stream) {
     const bool bf = p.pool_dt == LAR_BF16;
     if (p.form == FORM_LA) return bf ? launch_tc_form<FORM_LA, 2>(p, st) : launch_tc_form<FORM_LA, 4>(p, st);
     if (p.form == FORM_GDN) return bf ? launch_tc_form<FORM_GDN, 2>(p, st) : launch_tc_form<FORM_GDN, 4>(p, st);
+    if (p.form == FORM_KDA) return bf ? launch_tc_form<FORM_KDA, 2>(p, st) : launch_tc_form<FORM_KDA, 4>(p, st);
     return LAR_ERR_ARG;
 }
 
