@@ -69,10 +69,6 @@
 #ifndef LAR_PDL
 #define LAR_PDL 1
 #endif
-// 1: at a pair's first tile the ring refill is issued before the pair preamble
-#ifndef LAR_EARLY_ISSUE
-#define LAR_EARLY_ISSUE 0
-#endif
 // upper bound on the resident CTAs per SM the persistent grid is sized for
 #ifndef LAR_OCC_CAP
 #define LAR_OCC_CAP 64
@@ -155,6 +151,12 @@ __device__ __forceinline__ float softplus_f(float x) { return x > 20.f ? x : log
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
     const unsigned dst = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(gmem_src) : "memory");
+}
+
+// 4-byte global -> shared copy (through L1; the 16-byte form above bypasses it)
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src) {
+    const unsigned dst = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(gmem_src) : "memory");
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
@@ -611,16 +613,9 @@ decode_kernel(const DecodeParams p) {
 #pragma unroll 1
     for (int64_t n = t_end - t_begin; n > 0; --n) {
         const int b = c_b, hv = c_hv, vt = c_vt;
-        bool early = false;    // this iteration's refill went out before the pair preamble
         if (pair_start) {
             // ---- new (b, hv) pair: slots, bases and per-token vectors
             pair_start = false;
-#if LAR_EARLY_ISSUE
-            // the refill of the stage consumed last iteration goes out first, so
-            // that it is in flight while the preamble waits on its loads
-            issue(stage_next);
-            early = true;
-#endif
             const int h = hv / p.group;
             buf ^= 1;
             const int64_t r = seed_of(b);
@@ -671,8 +666,7 @@ decode_kernel(const DecodeParams p) {
         }
 
         // ---- this thread's copies of the tile have landed: pull its rows into registers
-        if (early) cp_async_wait<S - 1>();
-        else cp_async_wait<S - 2>();
+        cp_async_wait<S - 2>();
         float2 s[NR][KPL / 2];   // element 2e in .x, 2e+1 in .y
         {
             const unsigned char* src = ring + stage * STAGE + s_row0;
@@ -682,7 +676,7 @@ decode_kernel(const DecodeParams p) {
                 for (int c = 0; c < NCH; ++c) chunk_to_f2<SB>(src + i * S_RSTEP + c * CSTEP, &s[i][c * EPC / 2]);
         }
         // refill the stage consumed in the previous iteration (its rows were used long ago)
-        if (!early) issue(stage_next);
+        issue(stage_next);
         stage = stage + 1 == S ? 0 : stage + 1;
         stage_next = stage_next + 1 == S ? 0 : stage_next + 1;
 

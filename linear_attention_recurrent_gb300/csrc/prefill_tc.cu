@@ -66,7 +66,7 @@ constexpr uint32_t KT_BYTES = (TK / 8) * KT_SBO;
 constexpr uint32_t MT_SBO = KT_SBO;                   // M tile: 32 tokens x 32 tokens
 constexpr uint32_t MT_BYTES = (TC / 8) * MT_SBO;
 constexpr int FROW = TK + 4;                          // fp32 k / q rows (padded)
-constexpr int TROW = TC + 1;                          // C x C tables (padded)
+constexpr int TROW = TC + 4;                          // C x C tables (rows 16-byte aligned)
 
 // shared memory, bytes
 constexpr uint32_t OFF_KQH = 0;
@@ -85,19 +85,28 @@ constexpr uint32_t OFF_W = OFF_E + TC * 4;              // P[31][s]
 constexpr uint32_t OFF_B = OFF_W + TC * 4;              // beta_t
 constexpr uint32_t OFF_AD = OFF_B + TC * 4;             // KDA: a_t[c] [C][K]
 constexpr uint32_t OFF_EC = OFF_AD + TC * TK * 4;       // KDA: E_31[c] [K]
-constexpr uint32_t OFF_BAR = OFF_EC + TK * 4;           // two mbarriers
+// staging of one chunk's raw inputs (bf16 rows with unit inner stride and
+// 16-byte aligned rows): q, k, v, the KDA gate rows, then the fp32 gate and beta
+// scalars; filled with cp.async one chunk ahead
+constexpr uint32_t STG_ROW = TK * 2;                    // one bf16 row (TK = TVV)
+constexpr uint32_t STG_Q = 0, STG_K = TC * STG_ROW, STG_V = 2 * TC * STG_ROW, STG_G = 3 * TC * STG_ROW;
+constexpr uint32_t STG_GS = 4 * TC * STG_ROW, STG_BS = STG_GS + TC * 4, STG_BYTES = STG_BS + TC * 4;
+constexpr uint32_t OFF_STG = OFF_EC + TK * 4;
+constexpr uint32_t OFF_BAR = OFF_STG + STG_BYTES;       // two mbarriers
 constexpr uint32_t OFF_TM = OFF_BAR + 16;               // TMEM base address
 constexpr uint32_t TC_SMEM = OFF_TM + 16;
 static_assert(OFF_KQL % 16 == 0 && OFF_KTH % 16 == 0 && OFF_KTL % 16 == 0 && OFF_MTH % 16 == 0 &&
-                  OFF_MTL % 16 == 0 && OFF_K32 % 16 == 0 && OFF_Q32 % 16 == 0 && OFF_BAR % 8 == 0,
+                  OFF_MTL % 16 == 0 && OFF_K32 % 16 == 0 && OFF_Q32 % 16 == 0 && OFF_A % 16 == 0 &&
+                  OFF_BAR % 8 == 0,
               "tile and barrier alignment");
 static_assert(tc::kmaj(63, TK - 1, LBO, KQ_SBO) + 4 <= KQ_BYTES && tc::kmaj(TK - 1, TC - 1, LBO, KT_SBO) + 4 <= KT_BYTES &&
                   tc::kmaj(TC - 1, TC - 1, LBO, MT_SBO) + 4 <= MT_BYTES,
               "tiles hold their elements");
 static_assert(TC_SMEM <= 227 * 1024, "fits one CTA's shared memory");
+static_assert(OFF_STG % 16 == 0 && TVV == TK, "staging rows are 16-byte aligned");
 
 // tensor-memory columns
-constexpr uint32_t COL_SHI = 0, COL_SLO = 128, COL_UP = 256, COL_DS = 384;
+constexpr uint32_t COL_SHI = 0, COL_SLO = 128, COL_UP = 256, COL_KK = 320, COL_DS = 384;
 constexpr uint32_t COL_DHI = 0, COL_DLO = 32, COL_DWHI = 64, COL_DWLO = 96, COL_O = 128;
 constexpr uint32_t TMEM_COLS = 512;
 
@@ -226,6 +235,48 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
     const uint32_t kqh = tc::smem_addr(smem + OFF_KQH), kql = tc::smem_addr(smem + OFF_KQL);
     const uint32_t kth = tc::smem_addr(smem + OFF_KTH), ktl = tc::smem_addr(smem + OFF_KTL);
     const uint32_t mth = tc::smem_addr(smem + OFF_MTH), mtl = tc::smem_addr(smem + OFF_MTL);
+    // Inputs staged through shared memory when every row is bf16 with unit inner
+    // stride and 16-byte aligned (each row a run of 16-byte chunks); other
+    // layouts are read element by element (same results).
+    auto rows16 = [](const void* base, int dt, const int64_t* st, int n) {
+        bool okr = dt == LAR_BF16 && st[3] == 1 && (reinterpret_cast<uintptr_t>(base) & 15) == 0;
+        for (int i = 1; i < n; ++i) okr = okr && (st[i] * 2) % 16 == 0;
+        return okr;
+    };
+    const bool staged = rows16(p.q, p.q_dt, p.qs, 3) && rows16(p.k, p.k_dt, p.ks, 3) && rows16(p.v, p.v_dt, p.vs, 3) &&
+                        (!KDA || rows16(p.g, p.g_dt, p.gs, 3));
+    const bool stage_scal = !LA && !KDA && p.g_dt == LAR_F32 && p.beta_dt == LAR_F32;
+    const bool stage_beta = KDA && p.beta_dt == LAR_F32;
+    unsigned char* stg = smem + OFF_STG;
+    // issue this thread's copies of the chunk that starts at token cs of the span
+    auto stage = [&](int64_t cs) {
+        const int Ln = static_cast<int>(L - cs < TC ? L - cs : TC);
+        constexpr int NR = KDA ? 4 : 3;
+#pragma unroll 1
+        for (int i = tid; i < NR * TC * 16; i += TTH) {
+            const int which = i / (TC * 16), rem = i - which * (TC * 16), t = rem >> 4, c = rem & 15;
+            if (t >= Ln) continue;
+            const int64_t gt = tb + cs + t;
+            const unsigned char* src;
+            if (which == 0) src = static_cast<const unsigned char*>(p.q) + (gt * p.qs[1] + h * p.qs[2]) * 2;
+            else if (which == 1) src = static_cast<const unsigned char*>(p.k) + (gt * p.ks[1] + h * p.ks[2]) * 2;
+            else if (which == 2)
+                src = static_cast<const unsigned char*>(p.v) + (gt * p.vs[1] + static_cast<int64_t>(hv) * p.vs[2]) * 2;
+            else
+                src = static_cast<const unsigned char*>(p.g) + (gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2]) * 2;
+            cp_async16(stg + which * (TC * STG_ROW) + t * STG_ROW + c * 16, src + c * 16);
+        }
+        if ((stage_scal || stage_beta) && tid < TC && tid < Ln) {
+            const int64_t gt = tb + cs + tid;
+            if (stage_scal)
+                cp_async4(stg + STG_GS + tid * 4, static_cast<const float*>(p.g) + gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2]);
+            cp_async4(stg + STG_BS + tid * 4,
+                      static_cast<const float*>(p.beta) + gt * p.bs[1] + static_cast<int64_t>(hv) * p.bs[2]);
+        }
+        cp_async_commit();
+    };
+    if (staged && L > 0) stage(0);
+
     bool ok = true;
     int chunk = 0;
 
@@ -234,14 +285,26 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
         const int Lc = static_cast<int>(L - c0 < TC ? L - c0 : TC);
         const uint32_t par = static_cast<uint32_t>(chunk & 1);
 
-        // ---- (1) value inputs of this thread's row (the solve's right-hand side; LA: d itself)
+        // ---- (1) the chunk's inputs: staged ones have landed (this thread's copies,
+        // then everyone's through the barrier)
+        if (staged) {
+            cp_async_wait<0>();
+            __syncthreads();
+        }
+        // value inputs of this thread's row (the solve's right-hand side; LA: d itself)
         float vv[TC];
         if (half == 0) {
+            if (staged) {
+                const unsigned short* sv = reinterpret_cast<const unsigned short*>(stg + STG_V) + vrow;
 #pragma unroll
-            for (int t = 0; t < TC; ++t)
-                vv[t] = t < Lc ? ld_in(p.v, (tb + c0 + t) * p.vs[1] + static_cast<int64_t>(hv) * p.vs[2] +
-                                                static_cast<int64_t>(vrow) * p.vs[3], p.v_dt)
-                               : 0.f;
+                for (int t = 0; t < TC; ++t) vv[t] = t < Lc ? bf16_bits_to_float(sv[t * TK]) : 0.f;
+            } else {
+#pragma unroll
+                for (int t = 0; t < TC; ++t)
+                    vv[t] = t < Lc ? ld_in(p.v, (tb + c0 + t) * p.vs[1] + static_cast<int64_t>(hv) * p.vs[2] +
+                                                    static_cast<int64_t>(vrow) * p.vs[3], p.v_dt)
+                                   : 0.f;
+            }
         }
         // k and q rows: warp w takes tokens w, w + 8, ...; lane l channels 4l .. 4l + 3.
         // All of a thread's loads are issued before any is used.
@@ -252,7 +315,18 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
             const int t = warp + j * (TTH / 32);
             const int64_t gt = tb + c0 + t;
             const int64_t c = lane * 4;
-            if (t < Lc) {
+            if (t < Lc && staged) {
+                auto widen = [&](uint32_t off, float* x) {
+                    const uint2 u = *reinterpret_cast<const uint2*>(stg + off + t * STG_ROW + lane * 8);
+                    x[0] = __uint_as_float(u.x << 16);
+                    x[1] = __uint_as_float(u.x & 0xffff0000u);
+                    x[2] = __uint_as_float(u.y << 16);
+                    x[3] = __uint_as_float(u.y & 0xffff0000u);
+                };
+                widen(STG_Q, qa[j]);
+                widen(STG_K, ka[j]);
+                if constexpr (KDA) widen(STG_G, ga[j]);
+            } else if (t < Lc) {
                 ld_in4(p.q, gt * p.qs[1] + h * p.qs[2] + c * p.qs[3], p.qs[3], p.q_dt, qa[j]);
                 ld_in4(p.k, gt * p.ks[1] + h * p.ks[2] + c * p.ks[3], p.ks[3], p.k_dt, ka[j]);
                 if constexpr (KDA)
@@ -342,14 +416,17 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                     bt = 1.f;
                 } else {
                     if constexpr (!KDA) {   // KDA: the decay is per channel (Ad), the scalar factor 1
-                        float x = ld_in(p.g, gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2], p.g_dt);
+                        float x = staged && stage_scal ? reinterpret_cast<const float*>(stg + STG_GS)[t]
+                                                       : ld_in(p.g, gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2], p.g_dt);
                         if (gate_raw) {
                             const float bias = p.dt_bias ? p.dt_bias[hv * p.dtb_s] : 0.f;
                             x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
                         }
                         a = expf(x);
                     }
-                    const float bx = ld_in(p.beta, gt * p.bs[1] + static_cast<int64_t>(hv) * p.bs[2], p.beta_dt);
+                    const float bx = staged && (stage_scal || stage_beta)
+                                         ? reinterpret_cast<const float*>(stg + STG_BS)[t]
+                                         : ld_in(p.beta, gt * p.bs[1] + static_cast<int64_t>(hv) * p.bs[2], p.beta_dt);
                     bt = beta_raw ? 1.f / (1.f + expf(-bx)) : bx;
                 }
             }
@@ -453,6 +530,8 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
         }
         tc::fence_smem_to_async();
         tc_sync();
+        // the staging buffer has been read: the next chunk's copies go out now
+        if (staged && c0 + TC < L) stage(c0 + TC);
 
         // ---- (2) [U | P] = S0^T [K ; Q]^T (LA: P only), three tf32 passes
         if (tid == 0) {
@@ -469,46 +548,71 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                     tc::mma_ts(dcol, acol + 8 * kb, tc::smem_desc(bb + kb * 2 * LBO, LBO, KQ_SBO), idesc,
                                ps > 0 || kb > 0);
             }
+            if constexpr (!KDA) {
+                // [K ; Q] K^T (64 x 32, M = 64): rows t of K K^T and of Q K^T
+                constexpr uint32_t idesc_kk = tc::idesc_tf32(64, TC);
+#pragma unroll 1
+                for (int ps = 0; ps < 3; ++ps) {
+                    const uint32_t ab = ps == 2 ? kql : kqh, bb = ps == 1 ? kql : kqh;
+#pragma unroll 1
+                    for (int kb = 0; kb < TK / 8; ++kb)
+                        tc::mma_ss(tm + COL_KK, tc::smem_desc(ab + kb * 2 * LBO, LBO, KQ_SBO),
+                                   tc::smem_desc(bb + kb * 2 * LBO, LBO, KQ_SBO), idesc_kk, ps > 0 || kb > 0);
+                }
+            }
             tc::mma_commit(&bar[0]);
         }
 
-        // ---- (3) meanwhile on the CUDA cores: K K^T, Q K^T with the decay table (KDA: done above)
-        if constexpr (!KDA) {
-            const int t = tid >> 3, sg = tid & 7;
-            float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-            for (int k = 0; k < TK; k += 4) {
-                const float4 kt = *reinterpret_cast<const float4*>(K32 + t * FROW + k);
-                const float4 qt = *reinterpret_cast<const float4*>(Q32 + t * FROW + k);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float4 ks = *reinterpret_cast<const float4*>(K32 + (sg + 8 * j) * FROW + k);
-                    if constexpr (!LA)
-                        kk[j] = fmaf(kt.w, ks.w, fmaf(kt.z, ks.z, fmaf(kt.y, ks.y, fmaf(kt.x, ks.x, kk[j]))));
-                    qk[j] = fmaf(qt.w, ks.w, fmaf(qt.z, ks.z, fmaf(qt.y, ks.y, fmaf(qt.x, ks.x, qk[j]))));
-                }
-            }
-            const float bt = Bt[t];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int s = sg + 8 * j;
-                const float pd = Pt[t * TROW + s];
-                if constexpr (!LA) At[t * TROW + s] = s < t ? bt * pd * kk[j] : 0.f;
-                const float m = pd * qk[j];
-                const float mh = tc::tf32_hi(m);
-                const uint32_t o = tc::kmaj(t, s, LBO, MT_SBO);
-                *reinterpret_cast<float*>(smem + OFF_MTH + o) = mh;
-                *reinterpret_cast<float*>(smem + OFF_MTL + o) = m - mh;
-            }
-        }
-        tc::fence_smem_to_async();
-
-        // ---- (4) wait for [U | P]; the solve per value row, D and D o W into tensor memory
+        // ---- (3) wait for [U | P] and [K ; Q] K^T
         ok = tc::mbar_wait(&bar[0], par);
         ok = !__syncthreads_or(!ok);
         if (!ok) break;
         tc::fence_after_sync();
         float pv[TC];
+        if (!KDA && half == 0) {
+            // rows of K K^T (quarters 0, 1) and Q K^T (quarters 2, 3) with the decay table:
+            // A[t][s] = beta_t P[t][s] (k_t . k_s) (s < t), M[t][s] = P[t][s] (q_t . k_s)
+            float x[TC];
+            tc::tmem_ld16(my + COL_KK, x);
+            tc::tmem_ld16(my + COL_KK + 16, x + 16);
+            tc::tmem_ld_wait();
+            if (lane < 16) {
+                const int t = 16 * (quarter & 1) + lane;
+                const float* pr = Pt + t * TROW;
+                if (quarter < 2) {
+                    const float bt = Bt[t];
+#pragma unroll
+                    for (int s4 = 0; s4 < TC; s4 += 4)
+                        *reinterpret_cast<float4*>(At + t * TROW + s4) =
+                            make_float4(s4 < t ? bt * pr[s4] * x[s4] : 0.f, s4 + 1 < t ? bt * pr[s4 + 1] * x[s4 + 1] : 0.f,
+                                        s4 + 2 < t ? bt * pr[s4 + 2] * x[s4 + 2] : 0.f,
+                                        s4 + 3 < t ? bt * pr[s4 + 3] * x[s4 + 3] : 0.f);
+                } else {
+#pragma unroll
+                    for (int s4 = 0; s4 < TC; s4 += 4) {
+                        float m[4], mh[4], ml[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            m[e] = pr[s4 + e] * x[s4 + e];
+                            mh[e] = tc::tf32_hi(m[e]);
+                            ml[e] = m[e] - mh[e];
+                        }
+                        const uint32_t o = tc::kmaj(t, s4, LBO, MT_SBO);
+                        *reinterpret_cast<float4*>(smem + OFF_MTH + o) = make_float4(mh[0], mh[1], mh[2], mh[3]);
+                        *reinterpret_cast<float4*>(smem + OFF_MTL + o) = make_float4(ml[0], ml[1], ml[2], ml[3]);
+                    }
+                }
+            }
+        }
+        if (half == 1) {
+#pragma unroll
+            for (int c = 0; c < TC; c += 16) tc::tmem_ld16(my + COL_UP + TC + c, pv + c);
+            tc::tmem_ld_wait();
+        }
+        tc::fence_smem_to_async();
+        tc_sync();
+
+        // ---- (4) the solve per value row, D and D o W into tensor memory
         if (half == 0) {
             float d[TC];
             if constexpr (LA) {
@@ -521,14 +625,18 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                 tc::tmem_ld_wait();
 #pragma unroll
                 for (int t = 0; t < TC; ++t) {
-                    // two partial sums halve the dependent chain
+                    // two partial sums halve the dependent chain; A rows read 4 at a time
                     float acc0 = Bt[t] * fmaf(-E[t], u[t], vv[t]), acc1 = 0.f;
 #pragma unroll
-                    for (int s = 0; s + 1 < t; s += 2) {
-                        acc0 = fmaf(-At[t * TROW + s], d[s], acc0);
-                        acc1 = fmaf(-At[t * TROW + s + 1], d[s + 1], acc1);
+                    for (int s = 0; s < (t & ~3); s += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(At + t * TROW + s);
+                        acc0 = fmaf(-a4.x, d[s], acc0);
+                        acc1 = fmaf(-a4.y, d[s + 1], acc1);
+                        acc0 = fmaf(-a4.z, d[s + 2], acc0);
+                        acc1 = fmaf(-a4.w, d[s + 3], acc1);
                     }
-                    if (t & 1) acc0 = fmaf(-At[t * TROW + t - 1], d[t - 1], acc0);
+#pragma unroll
+                    for (int s = t & ~3; s < t; ++s) acc0 = fmaf(-At[t * TROW + s], d[s], acc0);
                     d[t] = acc0 + acc1;
                 }
             }
@@ -537,10 +645,6 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
             for (int t = 0; t < TC; ++t) d[t] *= Wd[t];
             split_store<TC>(my + COL_DWHI, my + COL_DWLO, d);
             tc::tmem_st_wait();
-        } else {
-#pragma unroll
-            for (int c = 0; c < TC; c += 16) tc::tmem_ld16(my + COL_UP + TC + c, pv + c);
-            tc::tmem_ld_wait();
         }
         tc_sync();
 
@@ -607,6 +711,7 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
         }
     }
 
+    cp_async_wait<0>();   // nothing may be left in flight into shared memory at exit
     if (!ok) {
         if (tid == 0 && p.dev_err) atomicOr(p.dev_err, LAR_DEVERR_TIMEOUT);
     } else if (wr) {

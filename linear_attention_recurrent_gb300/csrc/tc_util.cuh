@@ -77,6 +77,21 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// ---- MMA: D[tmem] (+)= A[smem] B[smem]^T, issued by one thread
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       bool accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// Tensor-memory lane of row r of an M = 64 product (cta_group::1): rows
+// 16 j .. 16 j + 15 sit in lanes 32 j .. 32 j + 15 (lanes 16..31 of each warp's
+// quarter are not written).
+__host__ __device__ constexpr int m64_lane(int r) { return 32 * (r >> 4) + (r & 15); }
+
 // arrive on `mbar` once every MMA this thread issued so far has completed
 __device__ __forceinline__ void mma_commit(uint64_t* mbar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
