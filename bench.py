@@ -74,7 +74,8 @@ DESCRIPTIONS = {
 # the sources each kernel is built from (the ABI layer included: it sets the launch parameters)
 _DECODE_SOURCES = ("decode_kernel.cuh", "decode_kv_kernel.cuh", "decode_gdn.cu", "decode_kda.cu", "decode_la.cu",
                    "decode_params.h", "launch_cache.cpp", "lar_abi.cpp")
-_PREFILL_SOURCES = ("prefill.cu", "decode_kernel.cuh", "decode_params.h", "lar_abi.cpp")
+_PREFILL_SOURCES = ("prefill.cu", "prefill_tc.cu", "tc_util.cuh", "decode_kernel.cuh", "decode_params.h",
+                    "lar_abi.cpp")
 
 
 def _code_only(text: str) -> str:
@@ -391,15 +392,60 @@ def hold_stream(stream, cycles=400_000):
             sleep(cycles)
 
 
+# tensor-core rates: the measured dense bf16 GEMM rate x the nominal tf32 / bf16
+# ratio (1.1 / 2.25 PFLOP/s), the chunked prefill's products being tf32
+TF32_OVER_BF16 = 1.1 / 2.25
+PREFILL_CHUNK = 32
+
+
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def prefill_tensor_flops(w) -> int:
+    """FLOPs of the chunked prefill's tensor-core products per launch, one
+    pass (the kernel runs each product in three tf32 passes): per 32-token
+    chunk of a span and value head, [U | P] = S0^T [K ; Q]^T (GDN, KDA;
+    LA: P only), [K ; Q] K^T (GDN; LA: Q K^T; KDA builds it on the CUDA cores),
+    O = D M^T and the increment (D o W) K."""
+    C, K, V = PREFILL_CHUNK, w.K, w.V
+    up = 2 * V * (C if w.form == "la" else 2 * C) * K
+    kk = {"gdn": 2 * 2 * C * C * K, "la": 2 * C * C * K, "kda": 0}[w.form]
+    per_chunk = up + kk + 2 * V * C * C + 2 * V * K * C
+    cu = w.cu_seqlens.to("cpu").long()
+    lengths = (cu[1:] - cu[:-1]).clamp(min=0)
+    chunks = int(((lengths + C - 1) // C).sum())
+    return chunks * w.HV * per_chunk
+
+
 def roofline(w, config, mean_launch_ms, achieved_gbs, peak_gbs, peak_kind):
     """The bound of the launch: HBM (algorithmic bytes / copy bandwidth) unless
     the fp32 arithmetic of the state update takes longer at the FMA-pipe peak
-    (long variable-length spans), in which case the line reports against that."""
+    (long variable-length spans), in which case the line reports against that.
+    The chunked prefill runs its products on the tensor cores and reports
+    against the tf32 rate."""
     kname = "prefill_kernel" if w.meta.get("prefill") else "decode_kernel"
     base = {"traffic": measured_traffic(config),
             "kernel": f"{kname}<{w.form}> ({kernel_source_hash(config)})",
             "mean_launch_us": round(mean_launch_ms * 1e3, 3)}
     ops = w.alu_ops()
+    if w.meta.get("prefill"):
+        flops = prefill_tensor_flops(w)
+        bf16, kind = bf16_peak()
+        peak = bf16 * TF32_OVER_BF16
+        achieved = flops / (mean_launch_ms * 1e-3) / 1e12
+        return dict({"bound": "tensor", "achieved": round(achieved, 3), "peak": round(peak, 1),
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{kind} bf16 GEMM rate x nominal tf32/bf16 ratio 1.1/2.25",
+                     "flops_per_launch": flops, "passes": 3,
+                     "alu_equivalent": {"achieved": round(ops / (mean_launch_ms * 1e-3) / 1e12, 3),
+                                        "unit": "T lane-op/s", "frac": round(ops / (mean_launch_ms * 1e-3) / ALU_PEAK_OPS, 4)},
+                     "hbm_frac": round(achieved_gbs / peak_gbs, 4)}, **base)
     t_hbm = w.algorithmic_bytes() / (peak_gbs * 1e9)
     t_alu = ops / ALU_PEAK_OPS
     if t_alu > t_hbm:

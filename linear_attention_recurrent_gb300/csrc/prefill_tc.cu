@@ -625,19 +625,19 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                 tc::tmem_ld_wait();
 #pragma unroll
                 for (int t = 0; t < TC; ++t) {
-                    // two partial sums halve the dependent chain; A rows read 4 at a time
-                    float acc0 = Bt[t] * fmaf(-E[t], u[t], vv[t]), acc1 = 0.f;
+                    // four partial sums shorten the dependent chain; A rows read 4 at a time
+                    float acc0 = Bt[t] * fmaf(-E[t], u[t], vv[t]), acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
 #pragma unroll
                     for (int s = 0; s < (t & ~3); s += 4) {
                         const float4 a4 = *reinterpret_cast<const float4*>(At + t * TROW + s);
                         acc0 = fmaf(-a4.x, d[s], acc0);
                         acc1 = fmaf(-a4.y, d[s + 1], acc1);
-                        acc0 = fmaf(-a4.z, d[s + 2], acc0);
-                        acc1 = fmaf(-a4.w, d[s + 3], acc1);
+                        acc2 = fmaf(-a4.z, d[s + 2], acc2);
+                        acc3 = fmaf(-a4.w, d[s + 3], acc3);
                     }
 #pragma unroll
                     for (int s = t & ~3; s < t; ++s) acc0 = fmaf(-At[t * TROW + s], d[s], acc0);
-                    d[t] = acc0 + acc1;
+                    d[t] = (acc0 + acc1) + (acc2 + acc3);
                 }
             }
             split_store<TC>(my + COL_DHI, my + COL_DLO, d);
