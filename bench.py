@@ -116,9 +116,11 @@ def kernel_source_hash(config: str = "gdn_b64") -> str:
     return h.hexdigest()[:12]
 
 
-def measured_traffic(config: str):
-    """dram bytes per launch from profiles/dram_traffic.txt, if captured on the current kernel."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+def measured_traffic(config: str, steady: bool = False):
+    """dram bytes per launch from profiles/dram_traffic.txt (one cold launch) or
+    profiles/dram_traffic_steady.txt (back-to-back launches, the L2 left as the
+    previous launch left it), if captured on the current kernel."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_steady.txt" if steady else "dram_traffic.txt")
     if not os.path.exists(path):
         return None
     want = kernel_source_hash(config)
@@ -430,7 +432,7 @@ def roofline(w, config, mean_launch_ms, achieved_gbs, peak_gbs, peak_kind):
     The chunked prefill runs its products on the tensor cores and reports
     against the tf32 rate."""
     kname = "prefill_kernel" if w.meta.get("prefill") else "decode_kernel"
-    base = {"traffic": measured_traffic(config),
+    base = {"traffic": measured_traffic(config), "traffic_steady": measured_traffic(config, steady=True),
             "kernel": f"{kname}<{w.form}> ({kernel_source_hash(config)})",
             "mean_launch_us": round(mean_launch_ms * 1e3, 3)}
     ops = w.alu_ops()

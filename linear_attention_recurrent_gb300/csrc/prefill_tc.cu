@@ -92,8 +92,8 @@ constexpr uint32_t STG_ROW = TK * 2;                    // one bf16 row (TK = TV
 constexpr uint32_t STG_Q = 0, STG_K = TC * STG_ROW, STG_V = 2 * TC * STG_ROW, STG_G = 3 * TC * STG_ROW;
 constexpr uint32_t STG_GS = 4 * TC * STG_ROW, STG_BS = STG_GS + TC * 4, STG_BYTES = STG_BS + TC * 4;
 constexpr uint32_t OFF_STG = OFF_EC + TK * 4;
-constexpr uint32_t OFF_BAR = OFF_STG + STG_BYTES;       // two mbarriers
-constexpr uint32_t OFF_TM = OFF_BAR + 16;               // TMEM base address
+constexpr uint32_t OFF_BAR = OFF_STG + STG_BYTES;       // three mbarriers
+constexpr uint32_t OFF_TM = OFF_BAR + 24;               // TMEM base address
 constexpr uint32_t TC_SMEM = OFF_TM + 16;
 static_assert(OFF_KQL % 16 == 0 && OFF_KTH % 16 == 0 && OFF_KTL % 16 == 0 && OFF_MTH % 16 == 0 &&
                   OFF_MTL % 16 == 0 && OFF_K32 % 16 == 0 && OFF_Q32 % 16 == 0 && OFF_A % 16 == 0 &&
@@ -182,6 +182,7 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
     if (tid == 0) {
         tc::mbar_init(&bar[0], 1);
         tc::mbar_init(&bar[1], 1);
+        tc::mbar_init(&bar[2], 1);
         tc::mbar_init_fence();
     }
     if (warp == 0) tc::tmem_alloc(tm_slot, TMEM_COLS);
@@ -405,8 +406,9 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                 }
             }
         }
-        // decay factors and betas (warp 0, lane t), then the decay table
-        if (warp == 0) {
+        // decay factors and betas (warp 1, lane t); the decay table is built from them
+        // while the tensor cores run
+        if (warp == 1) {
             const int t = lane;
             float a = 1.f, bt = 0.f;   // padding tokens: no decay, no update
             if (t < Lc) {
@@ -432,21 +434,6 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
             }
             Af[t] = a;
             Bt[t] = bt;
-            __syncwarp();
-            // row t: P[t][s] = a_{s+1} ... a_t (products, as the recurrence applies them), 0 above
-            float f = 1.f;
-#pragma unroll 1
-            for (int s = TC - 1; s >= 0; --s) {
-                if (s <= t) {
-                    Pt[t * TROW + s] = f;
-                    f *= Af[s];
-                } else {
-                    Pt[t * TROW + s] = 0.f;
-                }
-            }
-            E[t] = f;
-            __syncwarp();
-            Wd[t] = Pt[(TC - 1) * TROW + t];
         }
         if constexpr (KDA) {
             __syncthreads();
@@ -533,8 +520,21 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
         // the staging buffer has been read: the next chunk's copies go out now
         if (staged && c0 + TC < L) stage(c0 + TC);
 
-        // ---- (2) [U | P] = S0^T [K ; Q]^T (LA: P only), three tf32 passes
+        // ---- (2) [K ; Q] K^T (GDN, LA; completes on bar[0]), then [U | P] = S0^T [K ; Q]^T
+        // (LA: P only; completes on bar[2]), three tf32 passes each
         if (tid == 0) {
+            if constexpr (!KDA) {
+                constexpr uint32_t idesc_kk = tc::idesc_tf32(64, TC);
+#pragma unroll 1
+                for (int ps = 0; ps < 3; ++ps) {
+                    const uint32_t ab = ps == 2 ? kql : kqh, bb = ps == 1 ? kql : kqh;
+#pragma unroll 1
+                    for (int kb = 0; kb < TK / 8; ++kb)
+                        tc::mma_ss(tm + COL_KK, tc::smem_desc(ab + kb * 2 * LBO, LBO, KQ_SBO),
+                                   tc::smem_desc(bb + kb * 2 * LBO, LBO, KQ_SBO), idesc_kk, ps > 0 || kb > 0);
+                }
+                tc::mma_commit(&bar[0]);
+            }
             constexpr int NUP = LA ? TC : 2 * TC;
             constexpr uint32_t idesc = tc::idesc_tf32(TVV, NUP);
             const uint32_t boff = LA ? 4 * KQ_SBO : 0;       // LA: the q rows only
@@ -548,27 +548,37 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                     tc::mma_ts(dcol, acol + 8 * kb, tc::smem_desc(bb + kb * 2 * LBO, LBO, KQ_SBO), idesc,
                                ps > 0 || kb > 0);
             }
-            if constexpr (!KDA) {
-                // [K ; Q] K^T (64 x 32, M = 64): rows t of K K^T and of Q K^T
-                constexpr uint32_t idesc_kk = tc::idesc_tf32(64, TC);
+            tc::mma_commit(&bar[2]);
+        }
+        if (warp == 1) {
+            // row t of the decay table: P[t][s] = a_{s+1} ... a_t (products, as the
+            // recurrence applies them), 0 above; E_t = a_0 ... a_t; W_s = P[31][s]
+            const int t = lane;
+            float f = 1.f;
 #pragma unroll 1
-                for (int ps = 0; ps < 3; ++ps) {
-                    const uint32_t ab = ps == 2 ? kql : kqh, bb = ps == 1 ? kql : kqh;
-#pragma unroll 1
-                    for (int kb = 0; kb < TK / 8; ++kb)
-                        tc::mma_ss(tm + COL_KK, tc::smem_desc(ab + kb * 2 * LBO, LBO, KQ_SBO),
-                                   tc::smem_desc(bb + kb * 2 * LBO, LBO, KQ_SBO), idesc_kk, ps > 0 || kb > 0);
+            for (int s2 = TC - 1; s2 >= 0; --s2) {
+                if (s2 <= t) {
+                    Pt[t * TROW + s2] = f;
+                    f *= Af[s2];
+                } else {
+                    Pt[t * TROW + s2] = 0.f;
                 }
             }
-            tc::mma_commit(&bar[0]);
+            E[t] = f;
+            __syncwarp();
+            Wd[t] = Pt[(TC - 1) * TROW + t];
         }
 
-        // ---- (3) wait for [U | P] and [K ; Q] K^T
-        ok = tc::mbar_wait(&bar[0], par);
-        ok = !__syncthreads_or(!ok);
-        if (!ok) break;
-        tc::fence_after_sync();
-        float pv[TC];
+        // ---- (3) wait for [K ; Q] K^T (GDN, LA), the A and M tables from it while
+        // [U | P] still runs, then wait for [U | P]
+        if constexpr (!KDA) {
+            ok = tc::mbar_wait(&bar[0], par);
+            ok = !__syncthreads_or(!ok);
+            if (!ok) break;
+            tc::fence_after_sync();
+        } else {
+            __syncthreads();   // the decay table (all ones for KDA: its decays sit in the operand rows)
+        }
         if (!KDA && half == 0) {
             // rows of K K^T (quarters 0, 1) and Q K^T (quarters 2, 3) with the decay table:
             // A[t][s] = beta_t P[t][s] (k_t . k_s) (s < t), M[t][s] = P[t][s] (q_t . k_s)
@@ -604,13 +614,17 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                 }
             }
         }
+        tc::fence_smem_to_async();
+        ok = tc::mbar_wait(&bar[2], par);
+        ok = !__syncthreads_or(!ok);
+        if (!ok) break;
+        tc::fence_after_sync();
+        float pv[TC];
         if (half == 1) {
 #pragma unroll
             for (int c = 0; c < TC; c += 16) tc::tmem_ld16(my + COL_UP + TC + c, pv + c);
             tc::tmem_ld_wait();
         }
-        tc::fence_smem_to_async();
-        tc_sync();
 
         // ---- (4) the solve per value row, D and D o W into tensor memory
         if (half == 0) {
