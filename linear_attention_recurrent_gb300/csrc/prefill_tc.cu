@@ -42,9 +42,9 @@
 // per value row in registers; D and D o W go to tensor memory; one thread
 // issues O and the state increment (D o W) K; the outputs E_t P + O are
 // stored, the state becomes E_31 S + increment and its tf32 halves are written
-// back.  Tensor memory (512 columns): S_hi / S_lo (0..255; reused for D,
-// D o W and O once [U | P] has read them), [U | P] (256..319), the increment
-// (384..511).
+// back.  Tensor memory (512 columns): S_hi / S_lo (0..255; reused for D and
+// D o W once [U | P] has read them), [U | P] (256..319; O takes U's half once the
+// solve has read U), [K ; Q] K^T (320..351), the increment (384..511).
 //
 // Every wait is bounded: a wait that gives up makes the whole CTA skip the
 // rest of its span and its writeback, and sets LAR_DEVERR_TIMEOUT.
@@ -107,7 +107,9 @@ static_assert(OFF_STG % 16 == 0 && TVV == TK, "staging rows are 16-byte aligned"
 
 // tensor-memory columns
 constexpr uint32_t COL_SHI = 0, COL_SLO = 128, COL_UP = 256, COL_KK = 320, COL_DS = 384;
-constexpr uint32_t COL_DHI = 0, COL_DLO = 32, COL_DWHI = 64, COL_DWLO = 96, COL_O = 128;
+// O takes U's columns (U is dead once the solve has read it), so the new state's
+// halves (0..255) can be written while O is still being read
+constexpr uint32_t COL_DHI = 0, COL_DLO = 32, COL_DWHI = 64, COL_DWLO = 96, COL_O = COL_UP;
 constexpr uint32_t TMEM_COLS = 512;
 
 // x (N values, a multiple of 16) into tensor memory as its tf32 halves
@@ -705,9 +707,11 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                 }
             }
         }
-        // the new state E_31 S + increment (KDA: E_31 per key column), rounded to nearest
+        // the new state E_31 S + increment (KDA: E_31 per key column), rounded to
+        // nearest, and its tf32 halves for the next chunk's first product
         {
             const float ec = E[TC - 1];
+            const bool more = c0 + TC < L;
 #pragma unroll
             for (int c = 0; c < 64; c += 16) {
                 float x[16];
@@ -715,14 +719,11 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                 tc::tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) S[c + i] = fmaf(KDA ? EC[col0 + c + i] : ec, S[c + i], x[i]);
+                if (more) split_store<16>(my + COL_SHI + col0 + c, my + COL_SLO + col0 + c, S + c);
             }
+            if (more) tc::tmem_st_wait();
         }
         tc_sync();
-        if (c0 + TC < L) {
-            split_store<64>(my + COL_SHI + col0, my + COL_SLO + col0, S);
-            tc::tmem_st_wait();
-            tc_sync();
-        }
     }
 
     cp_async_wait<0>();   // nothing may be left in flight into shared memory at exit
