@@ -93,7 +93,10 @@ constexpr uint32_t STG_Q = 0, STG_K = TC * STG_ROW, STG_V = 2 * TC * STG_ROW, ST
 constexpr uint32_t STG_GS = 4 * TC * STG_ROW, STG_BS = STG_GS + TC * 4, STG_BYTES = STG_BS + TC * 4;
 constexpr uint32_t OFF_STG = OFF_EC + TK * 4;
 constexpr uint32_t OFF_BAR = OFF_STG + STG_BYTES;       // three mbarriers
-constexpr uint32_t OFF_TM = OFF_BAR + 24;               // TMEM base address
+constexpr uint32_t OFF_TM = OFF_BAR + 24;               // TMEM base address (then the picked sequence)
+// sequences ranked by span length in every CTA (at most this many; the ranking
+// costs each thread one pass over the spans)
+constexpr int kLptMax = 256;
 constexpr uint32_t TC_SMEM = OFF_TM + 16;
 static_assert(OFF_KQL % 16 == 0 && OFF_KTH % 16 == 0 && OFF_KTL % 16 == 0 && OFF_MTH % 16 == 0 &&
                   OFF_MTL % 16 == 0 && OFF_K32 % 16 == 0 && OFF_Q32 % 16 == 0 && OFF_A % 16 == 0 &&
@@ -104,6 +107,7 @@ static_assert(tc::kmaj(63, TK - 1, LBO, KQ_SBO) + 4 <= KQ_BYTES && tc::kmaj(TK -
               "tiles hold their elements");
 static_assert(TC_SMEM <= 227 * 1024, "fits one CTA's shared memory");
 static_assert(OFF_STG % 16 == 0 && TVV == TK, "staging rows are 16-byte aligned");
+static_assert(kLptMax * 4 <= STG_BYTES, "the span lengths fit the staging buffer");
 
 // tensor-memory columns
 constexpr uint32_t COL_SHI = 0, COL_SLO = 128, COL_UP = 256, COL_KK = 320, COL_DS = 384;
@@ -158,13 +162,36 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
     const int vrow = quarter * 32 + lane;                      // this thread's value row (TMEM lane)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int hv = blockIdx.x;
-    const int n = blockIdx.y;
     const int h = hv / p.group;
 
 #if LAR_PDL
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 #endif
+    // ---- which sequence: CTAs start in blockIdx order, so with up to kLptMax
+    // sequences row y of the grid takes the sequence of the y-th longest span
+    // (ties by index), and the grid's tail holds the short spans (on 16 spans of
+    // 256-1024 tokens the simulated makespan drops from 1.21x to 1.12x the
+    // ideal); more sequences keep their own order
+    int n = blockIdx.y;
+    if (p.B <= kLptMax) {
+        int* lens = reinterpret_cast<int*>(smem + OFF_STG);   // the staging buffer is not in use yet
+        int* pick = reinterpret_cast<int*>(smem + OFF_TM) + 1;
+        for (int i = tid; i < p.B; i += TTH) {
+            const int64_t a = ld_idx(p.cu, i * p.cu_s, p.cu_dt), e = ld_idx(p.cu, (i + 1) * p.cu_s, p.cu_dt);
+            lens[i] = a >= 0 && e >= a && e <= p.ntok ? static_cast<int>(e - a) : 0;
+        }
+        __syncthreads();
+        for (int i = tid; i < p.B; i += TTH) {
+            const int li = lens[i];
+            int rank = 0;
+            for (int m = 0; m < p.B; ++m) rank += lens[m] > li || (lens[m] == li && m < i);
+            if (rank == static_cast<int>(blockIdx.y)) *pick = i;
+        }
+        __syncthreads();
+        n = *pick;
+        __syncthreads();   // the staging buffer's first copies may now go out
+    }
     // ---- span and slots (reversed or overlong spans run as empty and are flagged)
     const int64_t lo = ld_idx(p.cu, n * p.cu_s, p.cu_dt);
     const int64_t hi = ld_idx(p.cu, (n + 1) * p.cu_s, p.cu_dt);
