@@ -384,10 +384,10 @@ def run_lar(args, world, rank, local):
     return line
 
 
-def hold_stream(stream, cycles=400_000):
-    """Keep `stream` busy (a spin kernel of ~0.2 ms) while the host enqueues
-    the timed launches behind it, so the first timed launch does not wait for
-    the host: the events then bracket back-to-back device work only."""
+def hold_stream(stream, cycles=1_000_000):
+    """Keep `stream` busy (a spin kernel of about 0.5 ms) while the host
+    enqueues the timed launches behind it, so the first timed launch does not
+    wait for the host: the events then bracket back-to-back device work only."""
     sleep = getattr(torch.cuda, "_sleep", None)
     if sleep is not None:
         with torch.cuda.stream(stream):
