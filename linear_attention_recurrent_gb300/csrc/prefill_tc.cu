@@ -139,6 +139,194 @@ __device__ __forceinline__ void tc_sync() {
     tc::fence_after_sync();
 }
 
+// ---- the chunk's products, each issued by one thread in three tf32 passes
+// [K ; Q] K^T into COL_KK (M = 64: rows 0..31 K K^T, rows 32..63 Q K^T; N = 32)
+__device__ __forceinline__ void issue_kk(uint32_t tm, uint32_t kqh, uint32_t kql) {
+    constexpr uint32_t idesc_kk = tc::idesc_tf32(64, TC);
+#pragma unroll 1
+    for (int ps = 0; ps < 3; ++ps) {
+        const uint32_t ab = ps == 2 ? kql : kqh, bb = ps == 1 ? kql : kqh;
+#pragma unroll 1
+        for (int kb = 0; kb < TK / 8; ++kb)
+            tc::mma_ss(tm + COL_KK, tc::smem_desc(ab + kb * 2 * LBO, LBO, KQ_SBO),
+                       tc::smem_desc(bb + kb * 2 * LBO, LBO, KQ_SBO), idesc_kk, ps > 0 || kb > 0);
+    }
+}
+
+// [U | P] = S^T [K ; Q]^T into COL_UP from the state's tf32 halves (COL_SHI,
+// COL_SLO); LA needs P only (the q rows, into COL_UP + TC)
+template <bool LA>
+__device__ __forceinline__ void issue_up(uint32_t tm, uint32_t kqh, uint32_t kql) {
+    constexpr int NUP = LA ? TC : 2 * TC;
+    constexpr uint32_t idesc = tc::idesc_tf32(TVV, NUP);
+    const uint32_t boff = LA ? 4 * KQ_SBO : 0;
+    const uint32_t dcol = tm + COL_UP + (LA ? TC : 0);
+#pragma unroll 1
+    for (int ps = 0; ps < 3; ++ps) {
+        const uint32_t acol = tm + (ps == 2 ? COL_SLO : COL_SHI);
+        const uint32_t bb = (ps == 1 ? kql : kqh) + boff;
+#pragma unroll 1
+        for (int kb = 0; kb < TK / 8; ++kb)
+            tc::mma_ts(dcol, acol + 8 * kb, tc::smem_desc(bb + kb * 2 * LBO, LBO, KQ_SBO), idesc, ps > 0 || kb > 0);
+    }
+}
+
+// O = D M^T into COL_O and the increment (D o W) K into COL_DS, from D and
+// D o W in tensor memory and the M and K^T tiles
+__device__ __forceinline__ void issue_os(uint32_t tm, uint32_t mth, uint32_t mtl, uint32_t kth, uint32_t ktl) {
+    constexpr uint32_t idesc_o = tc::idesc_tf32(TVV, TC);
+    constexpr uint32_t idesc_s = tc::idesc_tf32(TVV, TK);
+#pragma unroll 1
+    for (int ps = 0; ps < 3; ++ps) {
+        const uint32_t ad = tm + (ps == 2 ? COL_DLO : COL_DHI);
+        const uint32_t aw = tm + (ps == 2 ? COL_DWLO : COL_DWHI);
+        const uint32_t bm = ps == 1 ? mtl : mth;
+        const uint32_t bk = ps == 1 ? ktl : kth;
+#pragma unroll 1
+        for (int kb = 0; kb < TC / 8; ++kb) {
+            tc::mma_ts(tm + COL_O, ad + 8 * kb, tc::smem_desc(bm + kb * 2 * LBO, LBO, MT_SBO), idesc_o, ps > 0 || kb > 0);
+            tc::mma_ts(tm + COL_DS, aw + 8 * kb, tc::smem_desc(bk + kb * 2 * LBO, LBO, KT_SBO), idesc_s,
+                       ps > 0 || kb > 0);
+        }
+    }
+}
+
+// token t's k and q values (this lane's 4 channels, c = 4 lane ..) into the
+// [K ; Q] tile and the K^T tile as tf32 halves
+__device__ __forceinline__ void put_kq(unsigned char* kqh, unsigned char* kql, unsigned char* kth,
+                                       unsigned char* ktl, int t, int lane, const float* kx, const float* qx) {
+    float kh[4], kl[4], qh[4], ql[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        kh[e] = tc::tf32_hi(kx[e]);
+        kl[e] = kx[e] - kh[e];
+        qh[e] = tc::tf32_hi(qx[e]);
+        ql[e] = qx[e] - qh[e];
+    }
+    const uint32_t ok_ = tc::kmaj(t, 4 * lane, LBO, KQ_SBO), oq_ = tc::kmaj(TC + t, 4 * lane, LBO, KQ_SBO);
+    *reinterpret_cast<float4*>(kqh + ok_) = make_float4(kh[0], kh[1], kh[2], kh[3]);
+    *reinterpret_cast<float4*>(kql + ok_) = make_float4(kl[0], kl[1], kl[2], kl[3]);
+    *reinterpret_cast<float4*>(kqh + oq_) = make_float4(qh[0], qh[1], qh[2], qh[3]);
+    *reinterpret_cast<float4*>(kql + oq_) = make_float4(ql[0], ql[1], ql[2], ql[3]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t o = tc::kmaj(4 * lane + e, t, LBO, KT_SBO);
+        *reinterpret_cast<float*>(kth + o) = kh[e];
+        *reinterpret_cast<float*>(ktl + o) = kl[e];
+    }
+}
+
+// l2-normalise a token's q and k rows held 4 channels per lane across a warp
+__device__ __forceinline__ void l2_rows(float* qx, float* kx) {
+    float sq = 0.f, sk = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        sq = fmaf(qx[e], qx[e], sq);
+        sk = fmaf(kx[e], kx[e], sk);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+    }
+    const float iq = 1.f / sqrtf(sq + 1e-6f), ik = 1.f / sqrtf(sk + 1e-6f);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        qx[e] *= iq;
+        kx[e] *= ik;
+    }
+}
+
+// Row t of the decay table for lane t of one warp: P[t][s] = a_{s+1} ... a_t
+// (products, as the recurrence applies them; 0 above the diagonal),
+// E_t = a_0 ... a_t and W_s = P[31][s].
+__device__ __forceinline__ void decay_table(int lane, const float* Af, float* Pt, float* E, float* Wd) {
+    const int t = lane;
+    float f = 1.f;
+#pragma unroll 1
+    for (int s2 = TC - 1; s2 >= 0; --s2) {
+        if (s2 <= t) {
+            Pt[t * TROW + s2] = f;
+            f *= Af[s2];
+        } else {
+            Pt[t * TROW + s2] = 0.f;
+        }
+    }
+    E[t] = f;
+    __syncwarp();
+    Wd[t] = Pt[(TC - 1) * TROW + t];
+}
+
+// The A and M tables from the [K ; Q] K^T rows a warp of quarter `quarter`
+// holds (x: its lane's 32 columns; lanes 0..15 hold rows): A[t][s] = beta_t
+// P[t][s] (k_t . k_s) (s < t) from quarters 0, 1; M[t][s] = P[t][s] (q_t . k_s)
+// as tf32 halves in the M tile from quarters 2, 3.
+template <bool WITH_A>
+__device__ __forceinline__ void kk_tables(int quarter, int lane, const float* x, const float* Pt, const float* Bt,
+                                          float* At, unsigned char* mth, unsigned char* mtl) {
+    if (lane >= 16) return;
+    const int t = 16 * (quarter & 1) + lane;
+    const float* pr = Pt + t * TROW;
+    if (quarter < 2) {
+        if constexpr (WITH_A) {
+            const float bt = Bt[t];
+#pragma unroll
+            for (int s4 = 0; s4 < TC; s4 += 4)
+                *reinterpret_cast<float4*>(At + t * TROW + s4) =
+                    make_float4(s4 < t ? bt * pr[s4] * x[s4] : 0.f, s4 + 1 < t ? bt * pr[s4 + 1] * x[s4 + 1] : 0.f,
+                                s4 + 2 < t ? bt * pr[s4 + 2] * x[s4 + 2] : 0.f,
+                                s4 + 3 < t ? bt * pr[s4 + 3] * x[s4 + 3] : 0.f);
+        }
+    } else {
+#pragma unroll
+        for (int s4 = 0; s4 < TC; s4 += 4) {
+            float m[4], mh[4], ml[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                m[e] = pr[s4 + e] * x[s4 + e];
+                mh[e] = tc::tf32_hi(m[e]);
+                ml[e] = m[e] - mh[e];
+            }
+            const uint32_t o = tc::kmaj(t, s4, LBO, MT_SBO);
+            *reinterpret_cast<float4*>(mth + o) = make_float4(mh[0], mh[1], mh[2], mh[3]);
+            *reinterpret_cast<float4*>(mtl + o) = make_float4(ml[0], ml[1], ml[2], ml[3]);
+        }
+    }
+}
+
+// The triangular solve of one value row: d_t = beta_t (v_t - E_t u_t) -
+// sum_{s<t} A[t][s] d_s, with u (= (S0^T k_t)[v]) read from tensor memory and
+// v_t from vin(t), 16 tokens at a time.  Four partial sums shorten the
+// dependent chain.
+template <typename VIn>
+__device__ __forceinline__ void solve_row(uint32_t u_taddr, VIn vin, const float* At, const float* Bt,
+                                          const float* E, float* d) {
+#pragma unroll
+    for (int t0 = 0; t0 < TC; t0 += 16) {
+        float u[16], vv[16];
+        tc::tmem_ld16(u_taddr + t0, u);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) vv[i] = vin(t0 + i);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int t = t0 + i;
+            float acc0 = Bt[t] * fmaf(-E[t], u[i], vv[i]), acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+            for (int s = 0; s < (t & ~3); s += 4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(At + t * TROW + s);
+                acc0 = fmaf(-a4.x, d[s], acc0);
+                acc1 = fmaf(-a4.y, d[s + 1], acc1);
+                acc2 = fmaf(-a4.z, d[s + 2], acc2);
+                acc3 = fmaf(-a4.w, d[s + 3], acc3);
+            }
+#pragma unroll
+            for (int s = t & ~3; s < t; ++s) acc0 = fmaf(-At[t * TROW + s], d[s], acc0);
+            d[t] = (acc0 + acc1) + (acc2 + acc3);
+        }
+    }
+}
+
 template <int FORM, int SB>
 __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p) {
     constexpr bool LA = FORM == FORM_LA;
@@ -392,48 +580,11 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                 }
                 *reinterpret_cast<float4*>(Ad + t * TK + 4 * lane) = make_float4(a4[0], a4[1], a4[2], a4[3]);
             }
-            if (l2) {
-                float sq = 0.f, sk = 0.f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    sq = fmaf(qx[e], qx[e], sq);
-                    sk = fmaf(kx[e], kx[e], sk);
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    sq += __shfl_xor_sync(0xffffffffu, sq, off);
-                    sk += __shfl_xor_sync(0xffffffffu, sk, off);
-                }
-                const float iq = 1.f / sqrtf(sq + 1e-6f), ik = 1.f / sqrtf(sk + 1e-6f);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    qx[e] *= iq;
-                    kx[e] *= ik;
-                }
-            }
+            if (l2) l2_rows(qx, kx);
             *reinterpret_cast<float4*>(K32 + t * FROW + 4 * lane) = make_float4(kx[0], kx[1], kx[2], kx[3]);
             *reinterpret_cast<float4*>(Q32 + t * FROW + 4 * lane) = make_float4(qx[0], qx[1], qx[2], qx[3]);
-            if constexpr (!KDA) {     // KDA's operand rows carry the decays: written below
-                float kh[4], kl[4], qh[4], ql[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    kh[e] = tc::tf32_hi(kx[e]);
-                    kl[e] = kx[e] - kh[e];
-                    qh[e] = tc::tf32_hi(qx[e]);
-                    ql[e] = qx[e] - qh[e];
-                }
-                const uint32_t ok_ = tc::kmaj(t, 4 * lane, LBO, KQ_SBO), oq_ = tc::kmaj(TC + t, 4 * lane, LBO, KQ_SBO);
-                *reinterpret_cast<float4*>(smem + OFF_KQH + ok_) = make_float4(kh[0], kh[1], kh[2], kh[3]);
-                *reinterpret_cast<float4*>(smem + OFF_KQL + ok_) = make_float4(kl[0], kl[1], kl[2], kl[3]);
-                *reinterpret_cast<float4*>(smem + OFF_KQH + oq_) = make_float4(qh[0], qh[1], qh[2], qh[3]);
-                *reinterpret_cast<float4*>(smem + OFF_KQL + oq_) = make_float4(ql[0], ql[1], ql[2], ql[3]);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint32_t o = tc::kmaj(4 * lane + e, t, LBO, KT_SBO);
-                    *reinterpret_cast<float*>(smem + OFF_KTH + o) = kh[e];
-                    *reinterpret_cast<float*>(smem + OFF_KTL + o) = kl[e];
-                }
-            }
+            if constexpr (!KDA)       // KDA's operand rows carry the decays: written below
+                put_kq(smem + OFF_KQH, smem + OFF_KQL, smem + OFF_KTH, smem + OFF_KTL, t, lane, kx, qx);
         }
         // decay factors and betas (warp 1, lane t); the decay table is built from them
         // while the tensor cores run
@@ -553,50 +704,13 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
         // (LA: P only; completes on bar[2]), three tf32 passes each
         if (tid == 0) {
             if constexpr (!KDA) {
-                constexpr uint32_t idesc_kk = tc::idesc_tf32(64, TC);
-#pragma unroll 1
-                for (int ps = 0; ps < 3; ++ps) {
-                    const uint32_t ab = ps == 2 ? kql : kqh, bb = ps == 1 ? kql : kqh;
-#pragma unroll 1
-                    for (int kb = 0; kb < TK / 8; ++kb)
-                        tc::mma_ss(tm + COL_KK, tc::smem_desc(ab + kb * 2 * LBO, LBO, KQ_SBO),
-                                   tc::smem_desc(bb + kb * 2 * LBO, LBO, KQ_SBO), idesc_kk, ps > 0 || kb > 0);
-                }
+                issue_kk(tm, kqh, kql);
                 tc::mma_commit(&bar[0]);
             }
-            constexpr int NUP = LA ? TC : 2 * TC;
-            constexpr uint32_t idesc = tc::idesc_tf32(TVV, NUP);
-            const uint32_t boff = LA ? 4 * KQ_SBO : 0;       // LA: the q rows only
-            const uint32_t dcol = tm + COL_UP + (LA ? TC : 0);
-#pragma unroll 1
-            for (int ps = 0; ps < 3; ++ps) {
-                const uint32_t acol = tm + (ps == 2 ? COL_SLO : COL_SHI);
-                const uint32_t bb = (ps == 1 ? kql : kqh) + boff;
-#pragma unroll 1
-                for (int kb = 0; kb < TK / 8; ++kb)
-                    tc::mma_ts(dcol, acol + 8 * kb, tc::smem_desc(bb + kb * 2 * LBO, LBO, KQ_SBO), idesc,
-                               ps > 0 || kb > 0);
-            }
+            issue_up<LA>(tm, kqh, kql);
             tc::mma_commit(&bar[2]);
         }
-        if (warp == 1) {
-            // row t of the decay table: P[t][s] = a_{s+1} ... a_t (products, as the
-            // recurrence applies them), 0 above; E_t = a_0 ... a_t; W_s = P[31][s]
-            const int t = lane;
-            float f = 1.f;
-#pragma unroll 1
-            for (int s2 = TC - 1; s2 >= 0; --s2) {
-                if (s2 <= t) {
-                    Pt[t * TROW + s2] = f;
-                    f *= Af[s2];
-                } else {
-                    Pt[t * TROW + s2] = 0.f;
-                }
-            }
-            E[t] = f;
-            __syncwarp();
-            Wd[t] = Pt[(TC - 1) * TROW + t];
-        }
+        if (warp == 1) decay_table(lane, Af, Pt, E, Wd);
 
         // ---- (3) wait for [K ; Q] K^T (GDN, LA), the A and M tables from it while
         // [U | P] still runs, then wait for [U | P]
@@ -609,39 +723,12 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
             __syncthreads();   // the decay table (all ones for KDA: its decays sit in the operand rows)
         }
         if (!KDA && half == 0) {
-            // rows of K K^T (quarters 0, 1) and Q K^T (quarters 2, 3) with the decay table:
-            // A[t][s] = beta_t P[t][s] (k_t . k_s) (s < t), M[t][s] = P[t][s] (q_t . k_s)
+            // rows of K K^T (quarters 0, 1) and Q K^T (quarters 2, 3) with the decay table
             float x[TC];
             tc::tmem_ld16(my + COL_KK, x);
             tc::tmem_ld16(my + COL_KK + 16, x + 16);
             tc::tmem_ld_wait();
-            if (lane < 16) {
-                const int t = 16 * (quarter & 1) + lane;
-                const float* pr = Pt + t * TROW;
-                if (quarter < 2) {
-                    const float bt = Bt[t];
-#pragma unroll
-                    for (int s4 = 0; s4 < TC; s4 += 4)
-                        *reinterpret_cast<float4*>(At + t * TROW + s4) =
-                            make_float4(s4 < t ? bt * pr[s4] * x[s4] : 0.f, s4 + 1 < t ? bt * pr[s4 + 1] * x[s4 + 1] : 0.f,
-                                        s4 + 2 < t ? bt * pr[s4 + 2] * x[s4 + 2] : 0.f,
-                                        s4 + 3 < t ? bt * pr[s4 + 3] * x[s4 + 3] : 0.f);
-                } else {
-#pragma unroll
-                    for (int s4 = 0; s4 < TC; s4 += 4) {
-                        float m[4], mh[4], ml[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            m[e] = pr[s4 + e] * x[s4 + e];
-                            mh[e] = tc::tf32_hi(m[e]);
-                            ml[e] = m[e] - mh[e];
-                        }
-                        const uint32_t o = tc::kmaj(t, s4, LBO, MT_SBO);
-                        *reinterpret_cast<float4*>(smem + OFF_MTH + o) = make_float4(mh[0], mh[1], mh[2], mh[3]);
-                        *reinterpret_cast<float4*>(smem + OFF_MTL + o) = make_float4(ml[0], ml[1], ml[2], ml[3]);
-                    }
-                }
-            }
+            kk_tables<!LA>(quarter, lane, x, Pt, Bt, At, smem + OFF_MTH, smem + OFF_MTL);
         }
         tc::fence_smem_to_async();
         ok = tc::mbar_wait(&bar[2], par);
@@ -662,26 +749,7 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
 #pragma unroll
                 for (int t = 0; t < TC; ++t) d[t] = vv[t];
             } else {
-                float u[TC];
-#pragma unroll
-                for (int c = 0; c < TC; c += 16) tc::tmem_ld16(my + COL_UP + c, u + c);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int t = 0; t < TC; ++t) {
-                    // four partial sums shorten the dependent chain; A rows read 4 at a time
-                    float acc0 = Bt[t] * fmaf(-E[t], u[t], vv[t]), acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-#pragma unroll
-                    for (int s = 0; s < (t & ~3); s += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(At + t * TROW + s);
-                        acc0 = fmaf(-a4.x, d[s], acc0);
-                        acc1 = fmaf(-a4.y, d[s + 1], acc1);
-                        acc2 = fmaf(-a4.z, d[s + 2], acc2);
-                        acc3 = fmaf(-a4.w, d[s + 3], acc3);
-                    }
-#pragma unroll
-                    for (int s = t & ~3; s < t; ++s) acc0 = fmaf(-At[t * TROW + s], d[s], acc0);
-                    d[t] = (acc0 + acc1) + (acc2 + acc3);
-                }
+                solve_row(my + COL_UP, [&](int t) { return vv[t]; }, At, Bt, E, d);
             }
             split_store<TC>(my + COL_DHI, my + COL_DLO, d);
 #pragma unroll
@@ -693,22 +761,7 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
 
         // ---- (5) O = D M^T and the increment (D o W) K, three tf32 passes each
         if (tid == 0) {
-            constexpr uint32_t idesc_o = tc::idesc_tf32(TVV, TC);
-            constexpr uint32_t idesc_s = tc::idesc_tf32(TVV, TK);
-#pragma unroll 1
-            for (int ps = 0; ps < 3; ++ps) {
-                const uint32_t ad = tm + (ps == 2 ? COL_DLO : COL_DHI);
-                const uint32_t aw = tm + (ps == 2 ? COL_DWLO : COL_DWHI);
-                const uint32_t bm = ps == 1 ? mtl : mth;
-                const uint32_t bk = ps == 1 ? ktl : kth;
-#pragma unroll 1
-                for (int kb = 0; kb < TC / 8; ++kb) {
-                    tc::mma_ts(tm + COL_O, ad + 8 * kb, tc::smem_desc(bm + kb * 2 * LBO, LBO, MT_SBO), idesc_o,
-                               ps > 0 || kb > 0);
-                    tc::mma_ts(tm + COL_DS, aw + 8 * kb, tc::smem_desc(bk + kb * 2 * LBO, LBO, KT_SBO), idesc_s,
-                               ps > 0 || kb > 0);
-                }
-            }
+            issue_os(tm, mth, mtl, kth, ktl);
             tc::mma_commit(&bar[1]);
         }
         ok = tc::mbar_wait(&bar[1], par);
@@ -787,16 +840,489 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
     if (warp == 0) tc::tmem_dealloc(tm, TMEM_COLS);
 }
 
+// ============================================================================
+// Warp-specialised form (GDN, LA).  Per (sequence, head) the chunks form one
+// dependent chain: [U | P] from the state, the solve, O and the increment, the
+// new state.  Everything that does not depend on the state -- the chunk's k / q
+// tiles, K K^T, the decay table, the A and M tables -- is prepared one chunk
+// ahead by four "side" warps while the eight "chain" warps run the previous
+// chunk.  The side warps own the input staging (q and k rows one chunk ahead, v
+// rows in a ring of three), the K^T, M and A tables and the per-token scalars
+// are double-buffered by chunk parity; hand-offs go through mbarriers:
+//   KQ_READY   side -> chain   chunk c's [K ; Q] and K^T tiles are written
+//   UP_DONE    tensor cores    [U | P] of chunk c has completed (and with it every
+//                              product issued before it by the chain's issuer)
+//   KK_DONE    tensor cores    K K^T of chunk c has completed (side)
+//   OS_DONE    tensor cores    O and the increment of chunk c have completed
+//   TAB_READY  side -> chain   chunk c's A and M tables, decays and betas (one
+//                              barrier per chunk parity)
+// The side warps write chunk c's tiles only once UP_DONE(c - 1) shows that the
+// chain has finished chunk c - 2 and that the tensor cores are done with
+// [K ; Q](c - 1).  A wait that gives up sets a shared abort flag; the waits of
+// the other group see it and give up too, both groups leave their loops, and
+// the CTA skips its writeback.
+namespace ws {
+constexpr int NCHAIN = 256;   // warps 0..7
+constexpr int NSIDE = 128;    // warps 8..11 (one per tensor-memory lane quarter)
+constexpr int NT = NCHAIN + NSIDE;
+constexpr int NVB = 3;        // v staging ring
+constexpr uint32_t OFF_KQH = 0;
+constexpr uint32_t OFF_KQL = OFF_KQH + KQ_BYTES;
+constexpr uint32_t OFF_KT = OFF_KQL + KQ_BYTES;           // [parity][hi, lo]
+constexpr uint32_t OFF_MT = OFF_KT + 4 * KT_BYTES;        // [parity][hi, lo]
+constexpr uint32_t OFF_A = OFF_MT + 4 * MT_BYTES;         // [parity][TC][TROW]
+constexpr uint32_t OFF_P = OFF_A + 2 * TC * TROW * 4;     // [TC][TROW]
+constexpr uint32_t OFF_AF = OFF_P + TC * TROW * 4;        // [TC]
+constexpr uint32_t OFF_B = OFF_AF + TC * 4;               // [parity][TC]
+constexpr uint32_t OFF_E = OFF_B + 2 * TC * 4;            // [parity][TC]
+constexpr uint32_t OFF_W = OFF_E + 2 * TC * 4;            // [parity][TC]
+// staging: q rows, k rows, fp32 gates, fp32 betas (one chunk), then the v ring
+constexpr uint32_t OFF_STG = OFF_W + 2 * TC * 4;
+[[maybe_unused]] constexpr uint32_t SQ = 0, SK = TC * STG_ROW;
+constexpr uint32_t SG = 2 * TC * STG_ROW, SBT = SG + TC * 4, S_BYTES = SBT + TC * 4;
+constexpr uint32_t OFF_V = OFF_STG + S_BYTES;             // [NVB][TC] bf16 rows
+constexpr uint32_t OFF_BAR = OFF_V + NVB * TC * STG_ROW;
+enum { KQ_READY = 0, UP_DONE = 1, KK_DONE = 2, OS_DONE = 3, TAB_READY = 4, NBAR = 6 };
+constexpr uint32_t OFF_TM = OFF_BAR + NBAR * 8;           // TMEM base, picked sequence, abort flag
+constexpr uint32_t SMEM = OFF_TM + 16;
+static_assert(OFF_KT % 16 == 0 && OFF_MT % 16 == 0 && OFF_A % 16 == 0 && OFF_STG % 16 == 0 && OFF_V % 16 == 0 &&
+                  OFF_BAR % 8 == 0 && KT_BYTES % 16 == 0 && MT_BYTES % 16 == 0,
+              "tile, staging and barrier alignment");
+static_assert(SMEM <= 227 * 1024, "fits one CTA's shared memory");
+static_assert(kLptMax * 4 <= NVB * TC * STG_ROW, "the span lengths fit the v ring");
+static_assert(NSIDE == 128 && TC == 32, "one side warp per lane quarter; 8 tokens per side warp");
+}  // namespace ws
+
 template <int FORM, int SB>
-lar_status launch_tc_form(const DecodeParams& p, cudaStream_t stream) {
-    auto kern = prefill_tc_kernel<FORM, SB>;
+__global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParams p) {
+    static_assert(FORM != FORM_KDA, "KDA runs in prefill_tc_kernel");
+    constexpr bool LA = FORM == FORM_LA;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + ws::OFF_BAR);
+    uint32_t* tm_slot = reinterpret_cast<uint32_t*>(smem + ws::OFF_TM);
+    volatile int* abort_f = reinterpret_cast<volatile int*>(smem + ws::OFF_TM + 8);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool chain = tid < ws::NCHAIN;
+    const int quarter = warp & 3, half = (warp >> 2) & 1;
+    const int vrow = quarter * 32 + lane;                      // chain: this thread's value row
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int hv = blockIdx.x;
+    const int h = hv / p.group;
+
+#if LAR_PDL
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+#endif
+    // ---- which sequence: row y of the grid takes the y-th longest span (as in
+    // prefill_tc_kernel)
+    int n = blockIdx.y;
+    if (p.B <= kLptMax) {
+        int* lens = reinterpret_cast<int*>(smem + ws::OFF_V);   // the v ring is not in use yet
+        int* pick = reinterpret_cast<int*>(smem + ws::OFF_TM) + 1;
+        for (int i = tid; i < p.B; i += ws::NT) {
+            const int64_t a = ld_idx(p.cu, i * p.cu_s, p.cu_dt), e = ld_idx(p.cu, (i + 1) * p.cu_s, p.cu_dt);
+            lens[i] = a >= 0 && e >= a && e <= p.ntok ? static_cast<int>(e - a) : 0;
+        }
+        __syncthreads();
+        for (int i = tid; i < p.B; i += ws::NT) {
+            const int li = lens[i];
+            int rank = 0;
+            for (int m = 0; m < p.B; ++m) rank += lens[m] > li || (lens[m] == li && m < i);
+            if (rank == static_cast<int>(blockIdx.y)) *pick = i;
+        }
+        __syncthreads();
+        n = *pick;
+        __syncthreads();   // the v ring's first copies may now go out
+    }
+    // ---- span and slots (reversed or overlong spans run as empty and are flagged)
+    const int64_t lo = ld_idx(p.cu, n * p.cu_s, p.cu_dt);
+    const int64_t hi = ld_idx(p.cu, (n + 1) * p.cu_s, p.cu_dt);
+    const bool span_ok = lo >= 0 && hi >= lo && hi <= p.ntok;
+    const int64_t tb = span_ok ? lo : 0;
+    const int64_t L = span_ok ? hi - lo : 0;
+    const int nch = static_cast<int>((L + TC - 1) / TC);
+    const int64_t r = ld_idx(p.ridx, n * p.ri_s, p.ri_dt);
+    const int64_t w = p.widx ? ld_idx(p.widx, n * p.wi_s, p.wi_dt) : r;
+    const bool rd = r >= 0 && r < p.P;
+    const bool wr = w >= 0 && w < p.P;
+    if (tid == 0 && blockIdx.x == 0 && p.dev_err) {
+        const int e = (r >= p.P ? LAR_DEVERR_READ_SLOT : 0) | (w >= p.P ? LAR_DEVERR_WRITE_SLOT : 0) |
+                      (span_ok ? 0 : LAR_DEVERR_SEQLEN);
+        if (e) atomicOr(p.dev_err, e);
+    }
+
+    if (tid == 0) {
+        for (int i = 0; i < ws::NBAR; ++i) tc::mbar_init(&bar[i], 1);
+        *abort_f = 0;
+        tc::mbar_init_fence();
+    }
+    if (warp == 0) tc::tmem_alloc(tm_slot, TMEM_COLS);
+    tc_sync();
+    const uint32_t tm = *tm_slot;
+
+    const bool l2 = !LA && (p.flags & LAR_QK_L2NORM) != 0;
+    const bool gate_raw = (p.flags & LAR_GATE_RAW) != 0;
+    const bool beta_raw = (p.flags & LAR_BETA_RAW) != 0;
+    const uint32_t kqh = tc::smem_addr(smem + ws::OFF_KQH), kql = tc::smem_addr(smem + ws::OFF_KQL);
+    // inputs staged through shared memory when every row is bf16 with unit inner
+    // stride and 16-byte aligned; other layouts are read element by element
+    auto rows16 = [](const void* base, int dt, const int64_t* st, int nn) {
+        bool okr = dt == LAR_BF16 && st[3] == 1 && (reinterpret_cast<uintptr_t>(base) & 15) == 0;
+        for (int i = 1; i < nn; ++i) okr = okr && (st[i] * 2) % 16 == 0;
+        return okr;
+    };
+    const bool staged = rows16(p.q, p.q_dt, p.qs, 3) && rows16(p.k, p.k_dt, p.ks, 3) && rows16(p.v, p.v_dt, p.vs, 3);
+    const bool stage_scal = !LA && p.g_dt == LAR_F32 && p.beta_dt == LAR_F32;
+
+    if (chain) {
+        // ================= chain warps =================
+        const uint32_t my = tm + lane_off;
+        const int col0 = 64 * half;                              // this thread's 64 state columns
+        float S[64];
+        {
+            const unsigned char* src = static_cast<const unsigned char*>(p.pool) +
+                                       ((rd ? r : 0) * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1] +
+                                        static_cast<int64_t>(vrow) * p.ps[2] + col0) * SB;
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+                float* x = S + c;
+                if (rd) {
+                    if constexpr (SB == 4) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float4 f = __ldg(reinterpret_cast<const float4*>(src + c * 4) + i);
+                            x[4 * i] = f.x; x[4 * i + 1] = f.y; x[4 * i + 2] = f.z; x[4 * i + 3] = f.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const uint4 u = __ldg(reinterpret_cast<const uint4*>(src + c * 2) + i);
+                            const unsigned wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                x[8 * i + 2 * e] = __uint_as_float(wd[e] << 16);
+                                x[8 * i + 2 * e + 1] = __uint_as_float(wd[e] & 0xffff0000u);
+                            }
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) x[i] = 0.f;
+                }
+            }
+            split_store<64>(my + COL_SHI + col0, my + COL_SLO + col0, S);
+            tc::tmem_st_wait();
+        }
+        tc::fence_before_sync();
+        tc::bar_sync(1, ws::NCHAIN);
+        tc::fence_after_sync();
+
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+            const int64_t c0 = static_cast<int64_t>(c) * TC;
+            const int Lc = static_cast<int>(L - c0 < TC ? L - c0 : TC);
+            const uint32_t par = static_cast<uint32_t>(c & 1);
+            const float* At = reinterpret_cast<const float*>(smem + ws::OFF_A) + (c & 1) * TC * TROW;
+            const float* Bt = reinterpret_cast<const float*>(smem + ws::OFF_B) + (c & 1) * TC;
+            const float* E = reinterpret_cast<const float*>(smem + ws::OFF_E) + (c & 1) * TC;
+            const float* Wd = reinterpret_cast<const float*>(smem + ws::OFF_W) + (c & 1) * TC;
+
+            // ---- [U | P] once the side warps have written the chunk's tiles
+            bool ok = true;
+            if (tid == 0) {
+                ok = tc::mbar_wait_or(&bar[ws::KQ_READY], par, abort_f);
+                if (ok) {
+                    tc::fence_after_sync();
+                    issue_up<LA>(tm, kqh, kql);
+                    tc::mma_commit(&bar[ws::UP_DONE]);
+                }
+            }
+            ok = ok && tc::mbar_wait_or(&bar[ws::UP_DONE], par, abort_f) &&
+                 tc::mbar_wait_or(&bar[ws::TAB_READY + (c & 1)], static_cast<uint32_t>((c >> 1) & 1), abort_f);
+            if (!ok) *abort_f = 1;
+            if (tc::bar_or(1, ws::NCHAIN, !ok)) break;
+            tc::fence_after_sync();
+
+            if (half == 0) {
+                // ---- the solve per value row (v_t: the staged row once the side warps
+                // report the chunk ready, else the input itself), D and D o W into
+                // tensor memory
+                const unsigned short* sv =
+                    reinterpret_cast<const unsigned short*>(smem + ws::OFF_V + (c % ws::NVB) * TC * STG_ROW) + vrow;
+                auto vin = [&](int t) -> float {
+                    if (t >= Lc) return 0.f;
+                    if (staged) return bf16_bits_to_float(sv[t * TVV]);
+                    return ld_in(p.v, (tb + c0 + t) * p.vs[1] + static_cast<int64_t>(hv) * p.vs[2] +
+                                          static_cast<int64_t>(vrow) * p.vs[3], p.v_dt);
+                };
+                float d[TC];
+                if constexpr (LA) {
+#pragma unroll
+                    for (int t = 0; t < TC; ++t) d[t] = vin(t);
+                } else {
+                    solve_row(my + COL_UP, vin, At, Bt, E, d);
+                }
+                split_store<TC>(my + COL_DHI, my + COL_DLO, d);
+#pragma unroll
+                for (int t = 0; t < TC; ++t) d[t] *= Wd[t];
+                split_store<TC>(my + COL_DWHI, my + COL_DWLO, d);
+                tc::tmem_st_wait();
+            }
+            tc::fence_before_sync();
+            tc::bar_sync(1, ws::NCHAIN);
+            tc::fence_after_sync();
+
+            // ---- O and the increment
+            if (tid == 0) {
+                const uint32_t mt = tc::smem_addr(smem + ws::OFF_MT + (c & 1) * 2 * MT_BYTES);
+                const uint32_t kt = tc::smem_addr(smem + ws::OFF_KT + (c & 1) * 2 * KT_BYTES);
+                issue_os(tm, mt, mt + MT_BYTES, kt, kt + KT_BYTES);
+                tc::mma_commit(&bar[ws::OS_DONE]);
+            }
+            ok = tc::mbar_wait_or(&bar[ws::OS_DONE], par, abort_f);
+            if (!ok) *abort_f = 1;
+            if (tc::bar_or(1, ws::NCHAIN, !ok)) break;
+            tc::fence_after_sync();
+
+            // ---- outputs o_t = E_t P[v][t] + O[v][t] (half 1; P's columns are not
+            // written again before the next chunk's [U | P])
+            if (half == 1) {
+                float o[TC], pv[TC];
+#pragma unroll
+                for (int cc = 0; cc < TC; cc += 16) {
+                    tc::tmem_ld16(my + COL_O + cc, o + cc);
+                    tc::tmem_ld16(my + COL_UP + TC + cc, pv + cc);
+                }
+                tc::tmem_ld_wait();
+                const bool obf = p.out_dt == LAR_BF16;
+#pragma unroll
+                for (int t = 0; t < TC; ++t) {
+                    if (t < Lc) {
+                        const float y = fmaf(E[t], pv[t], o[t]) * p.scale;
+                        const int64_t off = (tb + c0 + t) * p.os[1] + static_cast<int64_t>(hv) * p.os[2] +
+                                            static_cast<int64_t>(vrow) * p.os[3];
+                        if (obf) static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(y);
+                        else static_cast<float*>(p.out)[off] = y;
+                    }
+                }
+            }
+            // ---- the new state E_31 S + increment, rounded to nearest, and its
+            // tf32 halves for the next chunk's first product
+            {
+                const float ec = E[TC - 1];
+                const bool more = c + 1 < nch;
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 16) {
+                    float x[16];
+                    tc::tmem_ld16(my + COL_DS + col0 + cc, x);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) S[cc + i] = fmaf(ec, S[cc + i], x[i]);
+                    if (more) split_store<16>(my + COL_SHI + col0 + cc, my + COL_SLO + col0 + cc, S + cc);
+                }
+                if (more) tc::tmem_st_wait();
+            }
+            tc::fence_before_sync();
+            tc::bar_sync(1, ws::NCHAIN);
+            tc::fence_after_sync();
+        }
+
+        __syncthreads();
+        if (*abort_f == 0 && wr) {
+            // ---- pool[w][hv][v][k] = S^T[v][k]
+            unsigned char* dst = static_cast<unsigned char*>(p.pool) +
+                                 (w * p.ps[0] + static_cast<int64_t>(hv) * p.ps[1] +
+                                  static_cast<int64_t>(vrow) * p.ps[2] + col0) * SB;
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+                const float* x = S + c;
+                if constexpr (SB == 4) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        __stcs(reinterpret_cast<float4*>(dst + c * 4) + i,
+                               make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        unsigned wd[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(x[8 * i + 2 * e], x[8 * i + 2 * e + 1]);
+                            wd[e] = *reinterpret_cast<const unsigned*>(&b2);
+                        }
+                        __stcs(reinterpret_cast<uint4*>(dst + c * 2) + i, make_uint4(wd[0], wd[1], wd[2], wd[3]));
+                    }
+                }
+            }
+        }
+    } else {
+        // ================= side warps =================
+        const int sw = warp - ws::NCHAIN / 32;                   // 0..3: also the tensor-memory lane quarter
+        const int stid = tid - ws::NCHAIN;
+        unsigned char* stg = smem + ws::OFF_STG;
+        float* Pt = reinterpret_cast<float*>(smem + ws::OFF_P);
+        float* Af = reinterpret_cast<float*>(smem + ws::OFF_AF);
+        // this thread's copies of chunk `ci` (tokens from cs on): q and k rows into
+        // the staging, v rows into the ring, fp32 gates and betas
+        auto stage = [&](int64_t cs, int ci) {
+            const int Ln = static_cast<int>(L - cs < TC ? L - cs : TC);
+#pragma unroll 1
+            for (int i = stid; i < 3 * TC * 16; i += ws::NSIDE) {
+                const int which = i / (TC * 16), rem = i - which * (TC * 16), t = rem >> 4, cb = rem & 15;
+                if (t >= Ln) continue;
+                const int64_t gt = tb + cs + t;
+                const unsigned char* src;
+                unsigned char* dst;
+                if (which == 0) {
+                    src = static_cast<const unsigned char*>(p.q) + (gt * p.qs[1] + h * p.qs[2]) * 2;
+                    dst = stg + ws::SQ;
+                } else if (which == 1) {
+                    src = static_cast<const unsigned char*>(p.k) + (gt * p.ks[1] + h * p.ks[2]) * 2;
+                    dst = stg + ws::SK;
+                } else {
+                    src = static_cast<const unsigned char*>(p.v) + (gt * p.vs[1] + static_cast<int64_t>(hv) * p.vs[2]) * 2;
+                    dst = smem + ws::OFF_V + (ci % ws::NVB) * TC * STG_ROW;
+                }
+                cp_async16(dst + t * STG_ROW + cb * 16, src + cb * 16);
+            }
+            if (stage_scal && stid < TC && stid < Ln) {
+                const int64_t gt = tb + cs + stid;
+                cp_async4(stg + ws::SG + stid * 4,
+                          static_cast<const float*>(p.g) + gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2]);
+                cp_async4(stg + ws::SBT + stid * 4,
+                          static_cast<const float*>(p.beta) + gt * p.bs[1] + static_cast<int64_t>(hv) * p.bs[2]);
+            }
+            cp_async_commit();
+        };
+        if (staged && L > 0) stage(0, 0);
+
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+            const int64_t c0 = static_cast<int64_t>(c) * TC;
+            const int Lc = static_cast<int>(L - c0 < TC ? L - c0 : TC);
+            float* At = reinterpret_cast<float*>(smem + ws::OFF_A) + (c & 1) * TC * TROW;
+            float* Bt = reinterpret_cast<float*>(smem + ws::OFF_B) + (c & 1) * TC;
+            float* E = reinterpret_cast<float*>(smem + ws::OFF_E) + (c & 1) * TC;
+            float* Wd = reinterpret_cast<float*>(smem + ws::OFF_W) + (c & 1) * TC;
+            unsigned char* kt = smem + ws::OFF_KT + (c & 1) * 2 * KT_BYTES;
+            unsigned char* mt = smem + ws::OFF_MT + (c & 1) * 2 * MT_BYTES;
+
+            // ---- the chunk's inputs have landed, and the previous chunk's [U | P] is done
+            if (staged) cp_async_wait<0>();
+            bool ok = c == 0 || tc::mbar_wait_or(&bar[ws::UP_DONE], static_cast<uint32_t>((c - 1) & 1), abort_f);
+            if (!ok) *abort_f = 1;
+            if (tc::bar_or(2, ws::NSIDE, !ok)) break;
+            tc::fence_after_sync();
+
+            // ---- k and q rows: side warp sw takes tokens sw, sw + 4, ...; lane l
+            // channels 4l .. 4l + 3; all loads issued before any is used
+            constexpr int RPW = TC / 4;
+            float qa[RPW][4], ka[RPW][4];
+#pragma unroll
+            for (int j = 0; j < RPW; ++j) {
+                const int t = sw + 4 * j;
+                const int64_t gt = tb + c0 + t;
+                if (t < Lc && staged) {
+                    auto widen = [&](uint32_t off, float* x) {
+                        const uint2 u = *reinterpret_cast<const uint2*>(stg + off + t * STG_ROW + lane * 8);
+                        x[0] = __uint_as_float(u.x << 16);
+                        x[1] = __uint_as_float(u.x & 0xffff0000u);
+                        x[2] = __uint_as_float(u.y << 16);
+                        x[3] = __uint_as_float(u.y & 0xffff0000u);
+                    };
+                    widen(ws::SQ, qa[j]);
+                    widen(ws::SK, ka[j]);
+                } else if (t < Lc) {
+                    const int64_t ch = lane * 4;
+                    ld_in4(p.q, gt * p.qs[1] + h * p.qs[2] + ch * p.qs[3], p.qs[3], p.q_dt, qa[j]);
+                    ld_in4(p.k, gt * p.ks[1] + h * p.ks[2] + ch * p.ks[3], p.ks[3], p.k_dt, ka[j]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) qa[j][e] = ka[j][e] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < RPW; ++j) {
+                if (l2) l2_rows(qa[j], ka[j]);
+                put_kq(smem + ws::OFF_KQH, smem + ws::OFF_KQL, kt, kt + KT_BYTES, sw + 4 * j, lane, ka[j], qa[j]);
+            }
+            // decay factors and betas (side warp 1, lane t; padding tokens: no decay, no update)
+            if (sw == 1) {
+                const int t = lane;
+                float a = 1.f, bt = 0.f;
+                if (t < Lc) {
+                    const int64_t gt = tb + c0 + t;
+                    if constexpr (LA) {
+                        a = p.decay[h * p.dec_s];
+                        bt = 1.f;
+                    } else {
+                        float x = staged && stage_scal ? reinterpret_cast<const float*>(stg + ws::SG)[t]
+                                                       : ld_in(p.g, gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2], p.g_dt);
+                        if (gate_raw) {
+                            const float bias = p.dt_bias ? p.dt_bias[hv * p.dtb_s] : 0.f;
+                            x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
+                        }
+                        a = expf(x);
+                        const float bx = staged && stage_scal
+                                             ? reinterpret_cast<const float*>(stg + ws::SBT)[t]
+                                             : ld_in(p.beta, gt * p.bs[1] + static_cast<int64_t>(hv) * p.bs[2], p.beta_dt);
+                        bt = beta_raw ? 1.f / (1.f + expf(-bx)) : bx;
+                    }
+                }
+                Af[t] = a;
+                Bt[t] = bt;
+            }
+            tc::fence_smem_to_async();
+            tc::bar_sync(2, ws::NSIDE);
+            // the tiles are complete: the chain may issue [U | P]; K K^T goes out
+            // behind it, and the staging takes the next chunk's copies
+            if (stid == 0) {
+                tc::fence_after_sync();
+                tc::mbar_arrive(&bar[ws::KQ_READY]);
+                issue_kk(tm, kqh, kql);
+                tc::mma_commit(&bar[ws::KK_DONE]);
+            }
+            if (staged && c + 1 < nch) stage(c0 + TC, c + 1);
+            if (sw == 1) decay_table(lane, Af, Pt, E, Wd);
+            tc::bar_sync(2, ws::NSIDE);
+
+            // ---- the A and M tables from K K^T and Q K^T
+            ok = tc::mbar_wait_or(&bar[ws::KK_DONE], static_cast<uint32_t>(c & 1), abort_f);
+            if (!ok) *abort_f = 1;
+            if (tc::bar_or(2, ws::NSIDE, !ok)) break;
+            tc::fence_after_sync();
+            {
+                float x[TC];
+                const uint32_t q0 = tm + (static_cast<uint32_t>(sw * 32) << 16) + COL_KK;
+                tc::tmem_ld16(q0, x);
+                tc::tmem_ld16(q0 + 16, x + 16);
+                tc::tmem_ld_wait();
+                kk_tables<!LA>(sw, lane, x, Pt, Bt, At, mt, mt + MT_BYTES);
+            }
+            tc::fence_smem_to_async();
+            tc::fence_before_sync();
+            tc::bar_sync(2, ws::NSIDE);
+            if (stid == 0) tc::mbar_arrive(&bar[ws::TAB_READY + (c & 1)]);
+        }
+        cp_async_wait<0>();   // nothing may be left in flight into shared memory at exit
+        __syncthreads();
+    }
+
+    tc_sync();
+    if (tid == 0 && *abort_f != 0 && p.dev_err) atomicOr(p.dev_err, LAR_DEVERR_TIMEOUT);
+    if (warp == 0) tc::tmem_dealloc(tm, TMEM_COLS);
+}
+
+lar_status launch_kernel(void (*kern)(DecodeParams), int threads, uint32_t smem_bytes, const DecodeParams& p,
+                         cudaStream_t stream) {
     if (cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(TC_SMEM)) != cudaSuccess)
+                             static_cast<int>(smem_bytes)) != cudaSuccess)
         return LAR_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.HV), static_cast<unsigned>(p.B));
-    cfg.blockDim = dim3(TTH);
-    cfg.dynamicSmemBytes = TC_SMEM;
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = stream;
 #if LAR_PDL
     cudaLaunchAttribute attr[1];
@@ -806,6 +1332,20 @@ lar_status launch_tc_form(const DecodeParams& p, cudaStream_t stream) {
     cfg.numAttrs = 1;
 #endif
     return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? LAR_OK : LAR_ERR_LAUNCH;
+}
+
+// GDN and LA run warp-specialised; KDA (whose per-channel tables need the
+// shared memory the pipeline's second buffers take) in prefill_tc_kernel.  The
+// build flag LAR_PF_WS=0 runs GDN and LA there too.
+#ifndef LAR_PF_WS
+#define LAR_PF_WS 1
+#endif
+template <int FORM, int SB>
+lar_status launch_tc_form(const DecodeParams& p, cudaStream_t stream) {
+    if constexpr (FORM != FORM_KDA && LAR_PF_WS)
+        return launch_kernel(prefill_ws_kernel<FORM, SB>, ws::NT, ws::SMEM, p, stream);
+    else
+        return launch_kernel(prefill_tc_kernel<FORM, SB>, TTH, TC_SMEM, p, stream);
 }
 
 }  // namespace

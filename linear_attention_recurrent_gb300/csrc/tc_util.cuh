@@ -123,6 +123,47 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity) {
     return false;
 }
 
+// One arrival on `mbar` by this thread, releasing its prior writes (shared
+// memory included) to whoever waits for the phase.
+__device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(mbar)) : "memory");
+}
+
+// As mbar_wait, but it also gives up as soon as `*abort` is set (checked every
+// 256 polls), so that a group of threads whose partner group has stopped does
+// not spin out the whole limit.
+__device__ __forceinline__ bool mbar_wait_or(uint64_t* mbar, uint32_t parity, const volatile int* abort) {
+    const uint32_t a = smem_addr(mbar);
+#pragma unroll 1
+    for (int i = 0; i < (1 << 22); ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((i & 255) == 255 && *abort) return false;
+    }
+    return false;
+}
+
+// Named barrier `id` over the `n` threads (a multiple of 32) that use it,
+// returning the OR of `pred` over them.
+__device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+}
+
 // ---- TMEM <-> registers, 32 lanes x 16 columns (one lane per thread of the
 // warp; the warp reaches lanes 32 (warp % 4) .. + 31)
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
