@@ -26,6 +26,11 @@
 // state keeps the 1e-4 relative tolerance over thousands of tokens.  The
 // dropped A_lo B_lo term is below 2^-22 relative.
 //
+// Two kernels.  prefill_ws_kernel (GDN and LA with bf16 q and k, the usual
+// case) splits each CTA into warps that run the state chain and warps that
+// prepare the next chunk, on raw operands (fewer tensor-core passes); it is
+// described at its definition.  prefill_tc_kernel runs KDA and fp32 q / k:
+//
 // Work.  One CTA of 256 threads per (sequence, v-head) keeps that pair's state
 // on chip for the whole span: S^T in fp32 registers (thread (warp w, lane l)
 // owns value row v = 32 (w % 4) + l, the two warps of a row split its
@@ -840,57 +845,120 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
     if (warp == 0) tc::tmem_dealloc(tm, TMEM_COLS);
 }
 
+// The warp-specialised form below runs GDN and LA with bf16 q and k; the build
+// flag LAR_PF_WS=0 leaves it out (everything then runs in prefill_tc_kernel).
+#ifndef LAR_PF_WS
+#define LAR_PF_WS 1
+#endif
+#if LAR_PF_WS
 // ============================================================================
-// Warp-specialised form (GDN, LA).  Per (sequence, head) the chunks form one
-// dependent chain: [U | P] from the state, the solve, O and the increment, the
-// new state.  Everything that does not depend on the state -- the chunk's k / q
-// tiles, K K^T, the decay table, the A and M tables -- is prepared one chunk
-// ahead by four "side" warps while the eight "chain" warps run the previous
-// chunk.  The side warps own the input staging (q and k rows one chunk ahead, v
-// rows in a ring of three), the K^T, M and A tables and the per-token scalars
-// are double-buffered by chunk parity; hand-offs go through mbarriers:
-//   KQ_READY   side -> chain   chunk c's [K ; Q] and K^T tiles are written
-//   UP_DONE    tensor cores    [U | P] of chunk c has completed (and with it every
-//                              product issued before it by the chain's issuer)
-//   KK_DONE    tensor cores    K K^T of chunk c has completed (side)
-//   OS_DONE    tensor cores    O and the increment of chunk c have completed
-//   TAB_READY  side -> chain   chunk c's A and M tables, decays and betas (one
-//                              barrier per chunk parity)
-// The side warps write chunk c's tiles only once UP_DONE(c - 1) shows that the
-// chain has finished chunk c - 2 and that the tensor cores are done with
-// [K ; Q](c - 1).  A wait that gives up sets a shared abort flag; the waits of
-// the other group see it and give up too, both groups leave their loops, and
-// the CTA skips its writeback.
+// Warp-specialised form (GDN, LA; bf16 q and k).  Per (sequence, head) the
+// chunks form one dependent chain: [U | P] from the state, the solve, O and the
+// increment, the new state.  Everything that does not depend on the state --
+// the chunk's k / q tiles, K K^T, the decay table, the A and M tables -- is
+// prepared by four "side" warps while the eight "chain" warps run the previous
+// chunk.
+//
+// Raw operands.  bf16 q and k values are exact in tf32, so the tiles hold the
+// raw values and the l2 norms (when asked) enter as per-token factors
+// 1/|k_t|, 1/|q_t| applied to the products' rows and columns: K K^T and Q K^T
+// come out exact in one tensor-core pass, S^T [K ; Q]^T and (D o W) K in two
+// (the state's and D o W's tf32 halves against exact operands); only O = D M^T
+// keeps three (M is a computed fp32 table).  With no low halves to store, the
+// [K ; Q] and K^T tiles are double-buffered by chunk parity, as are the A, M
+// tables and the per-token factors.
+//
+// Hand-offs (mbarriers; [2]: one per chunk parity):
+//   KQ_READY[2]   side -> chain   chunk c's [K ; Q] and K^T tiles are written
+//   TAB_READY[2]  side -> chain   chunk c's A and M tables and factors are written
+//   CHAIN_DONE[2] chain -> side   the chain has finished chunk c: the side may
+//                                 refill chunk c's buffers with chunk c + 2
+//   UP_DONE, OS_DONE              the chain's products have completed
+//   KK_DONE                       the side's K K^T has completed
+// so the side works on chunk c + 1 while the chain runs chunk c.  O's
+// accumulator (columns 352..383) starts from E_t P[v][t] / |q_t|, written by the
+// chain's second half while the first half solves, and the finished outputs
+// are stored one chunk later, off the chain.  A wait that gives up sets a
+// shared abort flag; the waits of the other group see it and give up too, both
+// groups leave their loops, and the CTA skips its writeback.
 namespace ws {
 constexpr int NCHAIN = 256;   // warps 0..7
 constexpr int NSIDE = 128;    // warps 8..11 (one per tensor-memory lane quarter)
 constexpr int NT = NCHAIN + NSIDE;
 constexpr int NVB = 3;        // v staging ring
-constexpr uint32_t OFF_KQH = 0;
-constexpr uint32_t OFF_KQL = OFF_KQH + KQ_BYTES;
-constexpr uint32_t OFF_KT = OFF_KQL + KQ_BYTES;           // [parity][hi, lo]
-constexpr uint32_t OFF_MT = OFF_KT + 4 * KT_BYTES;        // [parity][hi, lo]
-constexpr uint32_t OFF_A = OFF_MT + 4 * MT_BYTES;         // [parity][TC][TROW]
-constexpr uint32_t OFF_P = OFF_A + 2 * TC * TROW * 4;     // [TC][TROW]
-constexpr uint32_t OFF_AF = OFF_P + TC * TROW * 4;        // [TC]
-constexpr uint32_t OFF_B = OFF_AF + TC * 4;               // [parity][TC]
-constexpr uint32_t OFF_E = OFF_B + 2 * TC * 4;            // [parity][TC]
-constexpr uint32_t OFF_W = OFF_E + 2 * TC * 4;            // [parity][TC]
+constexpr uint32_t OFF_KQ = 0;                                // [parity] raw [K ; Q] tile
+constexpr uint32_t OFF_KT = OFF_KQ + 2 * KQ_BYTES;            // [parity] raw K^T tile
+constexpr uint32_t OFF_MT = OFF_KT + 2 * KT_BYTES;            // [parity][hi, lo] M tile
+constexpr uint32_t OFF_AT = OFF_MT + 4 * MT_BYTES;            // [parity] A transposed: [s][t]
+constexpr uint32_t OFF_P = OFF_AT + 2 * TC * TROW * 4;        // decay table P[t][s] (side)
+constexpr uint32_t OFF_AF = OFF_P + TC * TROW * 4;            // a_t (side)
+constexpr uint32_t OFF_IQ = OFF_AF + TC * 4;                  // 1/|q_t| (side)
+constexpr uint32_t OFF_IK = OFF_IQ + TC * 4;                  // 1/|k_t| (side)
+constexpr uint32_t OFF_B = OFF_IK + TC * 4;                   // [parity] beta_t
+constexpr uint32_t OFF_EK = OFF_B + 2 * TC * 4;               // [parity] E_t / |k_t|
+constexpr uint32_t OFF_EQ = OFF_EK + 2 * TC * 4;              // [parity] E_t / |q_t|
+constexpr uint32_t OFF_WK = OFF_EQ + 2 * TC * 4;              // [parity] W_s / |k_s|
+constexpr uint32_t OFF_E31 = OFF_WK + 2 * TC * 4;             // [parity] E_31 (16 bytes each)
 // staging: q rows, k rows, fp32 gates, fp32 betas (one chunk), then the v ring
-constexpr uint32_t OFF_STG = OFF_W + 2 * TC * 4;
-[[maybe_unused]] constexpr uint32_t SQ = 0, SK = TC * STG_ROW;
-constexpr uint32_t SG = 2 * TC * STG_ROW, SBT = SG + TC * 4, S_BYTES = SBT + TC * 4;
-constexpr uint32_t OFF_V = OFF_STG + S_BYTES;             // [NVB][TC] bf16 rows
+constexpr uint32_t OFF_STG = OFF_E31 + 2 * 16;
+constexpr uint32_t SQ = 0, SK = TC * STG_ROW, SG = 2 * TC * STG_ROW, SBT = SG + TC * 4, S_BYTES = SBT + TC * 4;
+constexpr uint32_t OFF_V = OFF_STG + S_BYTES;                 // [NVB][TC] bf16 rows
 constexpr uint32_t OFF_BAR = OFF_V + NVB * TC * STG_ROW;
-enum { KQ_READY = 0, UP_DONE = 1, KK_DONE = 2, OS_DONE = 3, TAB_READY = 4, NBAR = 6 };
-constexpr uint32_t OFF_TM = OFF_BAR + NBAR * 8;           // TMEM base, picked sequence, abort flag
+enum { KQ_READY = 0, TAB_READY = 2, CHAIN_DONE = 4, UP_DONE = 6, OS_DONE = 7, KK_DONE = 8, NBAR = 9 };
+constexpr uint32_t OFF_TM = OFF_BAR + NBAR * 8;               // TMEM base, picked sequence, abort flag
 constexpr uint32_t SMEM = OFF_TM + 16;
-static_assert(OFF_KT % 16 == 0 && OFF_MT % 16 == 0 && OFF_A % 16 == 0 && OFF_STG % 16 == 0 && OFF_V % 16 == 0 &&
-                  OFF_BAR % 8 == 0 && KT_BYTES % 16 == 0 && MT_BYTES % 16 == 0,
+constexpr uint32_t COL_O2 = 352;                              // O's accumulator (32 columns)
+static_assert(OFF_KT % 16 == 0 && OFF_MT % 16 == 0 && OFF_AT % 16 == 0 && OFF_STG % 16 == 0 && OFF_V % 16 == 0 &&
+                  OFF_BAR % 8 == 0 && KQ_BYTES % 16 == 0 && KT_BYTES % 16 == 0 && MT_BYTES % 16 == 0,
               "tile, staging and barrier alignment");
 static_assert(SMEM <= 227 * 1024, "fits one CTA's shared memory");
 static_assert(kLptMax * 4 <= NVB * TC * STG_ROW, "the span lengths fit the v ring");
 static_assert(NSIDE == 128 && TC == 32, "one side warp per lane quarter; 8 tokens per side warp");
+static_assert(COL_O2 >= COL_KK + TC && COL_O2 + TC <= COL_DS, "O's accumulator in the free columns");
+
+// K K^T and Q K^T from the raw tile: one pass (exact products)
+__device__ __forceinline__ void issue_kk(uint32_t tm, uint32_t kq) {
+    constexpr uint32_t idesc_kk = tc::idesc_tf32(64, TC);
+#pragma unroll 1
+    for (int kb = 0; kb < TK / 8; ++kb)
+        tc::mma_ss(tm + COL_KK, tc::smem_desc(kq + kb * 2 * LBO, LBO, KQ_SBO),
+                   tc::smem_desc(kq + kb * 2 * LBO, LBO, KQ_SBO), idesc_kk, kb > 0);
+}
+
+// [U | P] = S^T [K ; Q]^T from the raw tile (LA: P only): the state's two tf32 halves
+template <bool LA>
+__device__ __forceinline__ void issue_up(uint32_t tm, uint32_t kq) {
+    constexpr int NUP = LA ? TC : 2 * TC;
+    constexpr uint32_t idesc = tc::idesc_tf32(TVV, NUP);
+    const uint32_t bb = kq + (LA ? 4 * KQ_SBO : 0);
+    const uint32_t dcol = tm + COL_UP + (LA ? TC : 0);
+#pragma unroll 1
+    for (int ps = 0; ps < 2; ++ps) {
+        const uint32_t acol = tm + (ps == 1 ? COL_SLO : COL_SHI);
+#pragma unroll 1
+        for (int kb = 0; kb < TK / 8; ++kb)
+            tc::mma_ts(dcol, acol + 8 * kb, tc::smem_desc(bb + kb * 2 * LBO, LBO, KQ_SBO), idesc, ps > 0 || kb > 0);
+    }
+}
+
+// O += D M^T (three passes, onto the accumulator's starting value) and the
+// increment (D o W / |k|) K from the raw K^T tile (two passes)
+__device__ __forceinline__ void issue_os(uint32_t tm, uint32_t mth, uint32_t mtl, uint32_t kt) {
+    constexpr uint32_t idesc_o = tc::idesc_tf32(TVV, TC);
+    constexpr uint32_t idesc_s = tc::idesc_tf32(TVV, TK);
+#pragma unroll 1
+    for (int ps = 0; ps < 3; ++ps) {
+        const uint32_t ad = tm + (ps == 2 ? COL_DLO : COL_DHI);
+        const uint32_t bm = ps == 1 ? mtl : mth;
+#pragma unroll 1
+        for (int kb = 0; kb < TC / 8; ++kb) {
+            tc::mma_ts(tm + COL_O2, ad + 8 * kb, tc::smem_desc(bm + kb * 2 * LBO, LBO, MT_SBO), idesc_o, true);
+            if (ps < 2)
+                tc::mma_ts(tm + COL_DS, tm + (ps == 1 ? COL_DWLO : COL_DWHI) + 8 * kb,
+                           tc::smem_desc(kt + kb * 2 * LBO, LBO, KT_SBO), idesc_s, ps > 0 || kb > 0);
+        }
+    }
+}
 }  // namespace ws
 
 template <int FORM, int SB>
@@ -964,7 +1032,6 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
     const bool l2 = !LA && (p.flags & LAR_QK_L2NORM) != 0;
     const bool gate_raw = (p.flags & LAR_GATE_RAW) != 0;
     const bool beta_raw = (p.flags & LAR_BETA_RAW) != 0;
-    const uint32_t kqh = tc::smem_addr(smem + ws::OFF_KQH), kql = tc::smem_addr(smem + ws::OFF_KQL);
     // inputs staged through shared memory when every row is bf16 with unit inner
     // stride and 16-byte aligned; other layouts are read element by element
     auto rows16 = [](const void* base, int dt, const int64_t* st, int nn) {
@@ -1018,36 +1085,64 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
         tc::bar_sync(1, ws::NCHAIN);
         tc::fence_after_sync();
 
+        // outputs of chunk cc (half 1): the finished accumulator E P / |q| + D M^T
+        auto store_outputs = [&](int cc) {
+            const int64_t o0 = static_cast<int64_t>(cc) * TC;
+            const int Lo = static_cast<int>(L - o0 < TC ? L - o0 : TC);
+            float o[TC];
+#pragma unroll
+            for (int i = 0; i < TC; i += 16) tc::tmem_ld16(my + ws::COL_O2 + i, o + i);
+            tc::tmem_ld_wait();
+            const bool obf = p.out_dt == LAR_BF16;
+            const int64_t off0 = (tb + o0) * p.os[1] + static_cast<int64_t>(hv) * p.os[2] +
+                                 static_cast<int64_t>(vrow) * p.os[3];
+#pragma unroll
+            for (int t = 0; t < TC; ++t) {
+                if (t < Lo) {
+                    const float y = o[t] * p.scale;
+                    const int64_t off = off0 + t * p.os[1];
+                    if (obf) static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(y);
+                    else static_cast<float*>(p.out)[off] = y;
+                }
+            }
+        };
+
+        bool done = true;
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
+            const int b = c & 1;
             const int64_t c0 = static_cast<int64_t>(c) * TC;
             const int Lc = static_cast<int>(L - c0 < TC ? L - c0 : TC);
-            const uint32_t par = static_cast<uint32_t>(c & 1);
-            const float* At = reinterpret_cast<const float*>(smem + ws::OFF_A) + (c & 1) * TC * TROW;
-            const float* Bt = reinterpret_cast<const float*>(smem + ws::OFF_B) + (c & 1) * TC;
-            const float* E = reinterpret_cast<const float*>(smem + ws::OFF_E) + (c & 1) * TC;
-            const float* Wd = reinterpret_cast<const float*>(smem + ws::OFF_W) + (c & 1) * TC;
+            const uint32_t par = static_cast<uint32_t>(c & 1), par2 = static_cast<uint32_t>((c >> 1) & 1);
+            const float* AT = reinterpret_cast<const float*>(smem + ws::OFF_AT) + b * TC * TROW;
+            const float* Bt = reinterpret_cast<const float*>(smem + ws::OFF_B) + b * TC;
+            const float* EK = reinterpret_cast<const float*>(smem + ws::OFF_EK) + b * TC;
+            const float* EQ = reinterpret_cast<const float*>(smem + ws::OFF_EQ) + b * TC;
+            const float* WK = reinterpret_cast<const float*>(smem + ws::OFF_WK) + b * TC;
 
             // ---- [U | P] once the side warps have written the chunk's tiles
             bool ok = true;
             if (tid == 0) {
-                ok = tc::mbar_wait_or(&bar[ws::KQ_READY], par, abort_f);
+                ok = tc::mbar_wait_or(&bar[ws::KQ_READY + b], par2, abort_f);
                 if (ok) {
                     tc::fence_after_sync();
-                    issue_up<LA>(tm, kqh, kql);
+                    ws::issue_up<LA>(tm, tc::smem_addr(smem + ws::OFF_KQ + b * KQ_BYTES));
                     tc::mma_commit(&bar[ws::UP_DONE]);
                 }
             }
             ok = ok && tc::mbar_wait_or(&bar[ws::UP_DONE], par, abort_f) &&
-                 tc::mbar_wait_or(&bar[ws::TAB_READY + (c & 1)], static_cast<uint32_t>((c >> 1) & 1), abort_f);
+                 tc::mbar_wait_or(&bar[ws::TAB_READY + b], par2, abort_f);
             if (!ok) *abort_f = 1;
-            if (tc::bar_or(1, ws::NCHAIN, !ok)) break;
+            if (tc::bar_or(1, ws::NCHAIN, !ok)) {
+                done = false;
+                break;
+            }
             tc::fence_after_sync();
 
             if (half == 0) {
-                // ---- the solve per value row (v_t: the staged row once the side warps
-                // report the chunk ready, else the input itself), D and D o W into
-                // tensor memory
+                // ---- the solve per value row, right-looking: once d_s is final it is
+                // taken out of every later row (one dependent FMA per step).  v_t: the
+                // staged row (the side warps reported the chunk ready) or the input.
                 const unsigned short* sv =
                     reinterpret_cast<const unsigned short*>(smem + ws::OFF_V + (c % ws::NVB) * TC * STG_ROW) + vrow;
                 auto vin = [&](int t) -> float {
@@ -1061,12 +1156,45 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
 #pragma unroll
                     for (int t = 0; t < TC; ++t) d[t] = vin(t);
                 } else {
-                    solve_row(my + COL_UP, vin, At, Bt, E, d);
+                    // d_t starts as beta_t (v_t - E_t u_t / |k_t|), u from [U | P]
+#pragma unroll
+                    for (int t0 = 0; t0 < TC; t0 += 16) {
+                        float u[16], vv[16];
+                        tc::tmem_ld16(my + COL_UP + t0, u);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) vv[i] = vin(t0 + i);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) d[t0 + i] = Bt[t0 + i] * fmaf(-EK[t0 + i], u[i], vv[i]);
+                    }
+#pragma unroll
+                    for (int s = 0; s < TC - 1; ++s) {
+#pragma unroll
+                        for (int t4 = (s + 1) & ~3; t4 < TC; t4 += 4) {
+                            const float4 a4 = *reinterpret_cast<const float4*>(AT + s * TROW + t4);
+                            if (t4 > s) d[t4] = fmaf(-a4.x, d[s], d[t4]);
+                            if (t4 + 1 > s) d[t4 + 1] = fmaf(-a4.y, d[s], d[t4 + 1]);
+                            if (t4 + 2 > s) d[t4 + 2] = fmaf(-a4.z, d[s], d[t4 + 2]);
+                            d[t4 + 3] = fmaf(-a4.w, d[s], d[t4 + 3]);
+                        }
+                    }
                 }
                 split_store<TC>(my + COL_DHI, my + COL_DLO, d);
 #pragma unroll
-                for (int t = 0; t < TC; ++t) d[t] *= Wd[t];
+                for (int t = 0; t < TC; ++t) d[t] *= WK[t];
                 split_store<TC>(my + COL_DWHI, my + COL_DWLO, d);
+                tc::tmem_st_wait();
+            } else {
+                // ---- the previous chunk's outputs, then O's accumulator starts as E_t P[v][t] / |q_t|
+                if (c > 0) store_outputs(c - 1);
+                float pv[TC];
+#pragma unroll
+                for (int i = 0; i < TC; i += 16) tc::tmem_ld16(my + COL_UP + TC + i, pv + i);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int t = 0; t < TC; ++t) pv[t] *= EQ[t];
+#pragma unroll
+                for (int i = 0; i < TC; i += 16) tc::tmem_st16(my + ws::COL_O2 + i, pv + i);
                 tc::tmem_st_wait();
             }
             tc::fence_before_sync();
@@ -1075,42 +1203,22 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
 
             // ---- O and the increment
             if (tid == 0) {
-                const uint32_t mt = tc::smem_addr(smem + ws::OFF_MT + (c & 1) * 2 * MT_BYTES);
-                const uint32_t kt = tc::smem_addr(smem + ws::OFF_KT + (c & 1) * 2 * KT_BYTES);
-                issue_os(tm, mt, mt + MT_BYTES, kt, kt + KT_BYTES);
+                const uint32_t mt = tc::smem_addr(smem + ws::OFF_MT + b * 2 * MT_BYTES);
+                ws::issue_os(tm, mt, mt + MT_BYTES, tc::smem_addr(smem + ws::OFF_KT + b * KT_BYTES));
                 tc::mma_commit(&bar[ws::OS_DONE]);
             }
             ok = tc::mbar_wait_or(&bar[ws::OS_DONE], par, abort_f);
             if (!ok) *abort_f = 1;
-            if (tc::bar_or(1, ws::NCHAIN, !ok)) break;
+            if (tc::bar_or(1, ws::NCHAIN, !ok)) {
+                done = false;
+                break;
+            }
             tc::fence_after_sync();
 
-            // ---- outputs o_t = E_t P[v][t] + O[v][t] (half 1; P's columns are not
-            // written again before the next chunk's [U | P])
-            if (half == 1) {
-                float o[TC], pv[TC];
-#pragma unroll
-                for (int cc = 0; cc < TC; cc += 16) {
-                    tc::tmem_ld16(my + COL_O + cc, o + cc);
-                    tc::tmem_ld16(my + COL_UP + TC + cc, pv + cc);
-                }
-                tc::tmem_ld_wait();
-                const bool obf = p.out_dt == LAR_BF16;
-#pragma unroll
-                for (int t = 0; t < TC; ++t) {
-                    if (t < Lc) {
-                        const float y = fmaf(E[t], pv[t], o[t]) * p.scale;
-                        const int64_t off = (tb + c0 + t) * p.os[1] + static_cast<int64_t>(hv) * p.os[2] +
-                                            static_cast<int64_t>(vrow) * p.os[3];
-                        if (obf) static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(y);
-                        else static_cast<float*>(p.out)[off] = y;
-                    }
-                }
-            }
             // ---- the new state E_31 S + increment, rounded to nearest, and its
             // tf32 halves for the next chunk's first product
             {
-                const float ec = E[TC - 1];
+                const float ec = reinterpret_cast<const float*>(smem + ws::OFF_E31)[4 * b];
                 const bool more = c + 1 < nch;
 #pragma unroll
                 for (int cc = 0; cc < 64; cc += 16) {
@@ -1126,7 +1234,9 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
             tc::fence_before_sync();
             tc::bar_sync(1, ws::NCHAIN);
             tc::fence_after_sync();
+            if (tid == 0) tc::mbar_arrive(&bar[ws::CHAIN_DONE + b]);
         }
+        if (done && nch > 0 && half == 1) store_outputs(nch - 1);
 
         __syncthreads();
         if (*abort_f == 0 && wr) {
@@ -1163,6 +1273,8 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
         unsigned char* stg = smem + ws::OFF_STG;
         float* Pt = reinterpret_cast<float*>(smem + ws::OFF_P);
         float* Af = reinterpret_cast<float*>(smem + ws::OFF_AF);
+        float* Iq = reinterpret_cast<float*>(smem + ws::OFF_IQ);
+        float* Ik = reinterpret_cast<float*>(smem + ws::OFF_IK);
         // this thread's copies of chunk `ci` (tokens from cs on): q and k rows into
         // the staging, v rows into the ring, fp32 gates and betas
         auto stage = [&](int64_t cs, int ci) {
@@ -1199,29 +1311,30 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
 
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
+            const int b = c & 1;
             const int64_t c0 = static_cast<int64_t>(c) * TC;
             const int Lc = static_cast<int>(L - c0 < TC ? L - c0 : TC);
-            float* At = reinterpret_cast<float*>(smem + ws::OFF_A) + (c & 1) * TC * TROW;
-            float* Bt = reinterpret_cast<float*>(smem + ws::OFF_B) + (c & 1) * TC;
-            float* E = reinterpret_cast<float*>(smem + ws::OFF_E) + (c & 1) * TC;
-            float* Wd = reinterpret_cast<float*>(smem + ws::OFF_W) + (c & 1) * TC;
-            unsigned char* kt = smem + ws::OFF_KT + (c & 1) * 2 * KT_BYTES;
-            unsigned char* mt = smem + ws::OFF_MT + (c & 1) * 2 * MT_BYTES;
+            float* AT = reinterpret_cast<float*>(smem + ws::OFF_AT) + b * TC * TROW;
+            float* Bt = reinterpret_cast<float*>(smem + ws::OFF_B) + b * TC;
+            unsigned char* kq = smem + ws::OFF_KQ + b * KQ_BYTES;
+            unsigned char* kt = smem + ws::OFF_KT + b * KT_BYTES;
+            unsigned char* mt = smem + ws::OFF_MT + b * 2 * MT_BYTES;
 
-            // ---- the chunk's inputs have landed, and the previous chunk's [U | P] is done
+            // ---- the chain has finished chunk c - 2 (this parity's buffers are free)
+            // and the chunk's inputs have landed
+            bool ok = c < 2 || tc::mbar_wait_or(&bar[ws::CHAIN_DONE + b], static_cast<uint32_t>(((c - 2) >> 1) & 1), abort_f);
             if (staged) cp_async_wait<0>();
-            bool ok = c == 0 || tc::mbar_wait_or(&bar[ws::UP_DONE], static_cast<uint32_t>((c - 1) & 1), abort_f);
             if (!ok) *abort_f = 1;
             if (tc::bar_or(2, ws::NSIDE, !ok)) break;
             tc::fence_after_sync();
 
-            // ---- k and q rows: side warp sw takes tokens sw, sw + 4, ...; lane l
+            // ---- raw k and q rows: side warp sw takes tokens 8 sw .. 8 sw + 7, lane l
             // channels 4l .. 4l + 3; all loads issued before any is used
             constexpr int RPW = TC / 4;
             float qa[RPW][4], ka[RPW][4];
 #pragma unroll
             for (int j = 0; j < RPW; ++j) {
-                const int t = sw + 4 * j;
+                const int t = RPW * sw + j;
                 const int64_t gt = tb + c0 + t;
                 if (t < Lc && staged) {
                     auto widen = [&](uint32_t off, float* x) {
@@ -1244,8 +1357,40 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
             }
 #pragma unroll
             for (int j = 0; j < RPW; ++j) {
-                if (l2) l2_rows(qa[j], ka[j]);
-                put_kq(smem + ws::OFF_KQH, smem + ws::OFF_KQL, kt, kt + KT_BYTES, sw + 4 * j, lane, ka[j], qa[j]);
+                const int t = RPW * sw + j;
+                float iq = 1.f, ik = 1.f;
+                if (l2) {
+                    float sq = 0.f, sk = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        sq = fmaf(qa[j][e], qa[j][e], sq);
+                        sk = fmaf(ka[j][e], ka[j][e], sk);
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+                    }
+                    iq = 1.f / sqrtf(sq + 1e-6f);
+                    ik = 1.f / sqrtf(sk + 1e-6f);
+                }
+                if (lane == 0) {
+                    Iq[t] = iq;
+                    Ik[t] = ik;
+                }
+                *reinterpret_cast<float4*>(kq + tc::kmaj(t, 4 * lane, LBO, KQ_SBO)) =
+                    make_float4(ka[j][0], ka[j][1], ka[j][2], ka[j][3]);
+                *reinterpret_cast<float4*>(kq + tc::kmaj(TC + t, 4 * lane, LBO, KQ_SBO)) =
+                    make_float4(qa[j][0], qa[j][1], qa[j][2], qa[j][3]);
+            }
+            // K^T: channel c = 4 lane + e, tokens 8 sw .. 8 sw + 7 as two 16-byte runs
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int ch = 4 * lane + e;
+#pragma unroll
+                for (int j4 = 0; j4 < RPW; j4 += 4)
+                    *reinterpret_cast<float4*>(kt + tc::kmaj(ch, RPW * sw + j4, LBO, KT_SBO)) =
+                        make_float4(ka[j4][e], ka[j4 + 1][e], ka[j4 + 2][e], ka[j4 + 3][e]);
             }
             // decay factors and betas (side warp 1, lane t; padding tokens: no decay, no update)
             if (sw == 1) {
@@ -1275,19 +1420,33 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
             }
             tc::fence_smem_to_async();
             tc::bar_sync(2, ws::NSIDE);
-            // the tiles are complete: the chain may issue [U | P]; K K^T goes out
-            // behind it, and the staging takes the next chunk's copies
+            // the tiles are complete: the chain may issue [U | P]; K K^T goes out,
+            // and the staging takes the next chunk's copies
             if (stid == 0) {
                 tc::fence_after_sync();
-                tc::mbar_arrive(&bar[ws::KQ_READY]);
-                issue_kk(tm, kqh, kql);
+                tc::mbar_arrive(&bar[ws::KQ_READY + b]);
+                ws::issue_kk(tm, tc::smem_addr(kq));
                 tc::mma_commit(&bar[ws::KK_DONE]);
             }
             if (staged && c + 1 < nch) stage(c0 + TC, c + 1);
-            if (sw == 1) decay_table(lane, Af, Pt, E, Wd);
+            if (sw == 1) {
+                // the decay table, then the factors the chain applies: E_t / |k_t|,
+                // E_t / |q_t|, W_s / |k_s|, E_31
+                float* E = reinterpret_cast<float*>(smem + ws::OFF_EK) + b * TC;   // E_t first, scaled below
+                float* Wd = reinterpret_cast<float*>(smem + ws::OFF_WK) + b * TC;
+                decay_table(lane, Af, Pt, E, Wd);
+                const int t = lane;
+                const float et = E[t];
+                if (t == TC - 1) reinterpret_cast<float*>(smem + ws::OFF_E31)[4 * b] = et;
+                reinterpret_cast<float*>(smem + ws::OFF_EQ)[b * TC + t] = et * Iq[t];
+                E[t] = et * Ik[t];
+                Wd[t] *= Ik[t];
+            }
             tc::bar_sync(2, ws::NSIDE);
 
-            // ---- the A and M tables from K K^T and Q K^T
+            // ---- the A (transposed) and M tables from K K^T and Q K^T:
+            // A[t][s] = beta_t P[t][s] (k_t . k_s) / (|k_t| |k_s|) for s < t, and
+            // M[t][s] = P[t][s] (q_t . k_s) / (|q_t| |k_s|)
             ok = tc::mbar_wait_or(&bar[ws::KK_DONE], static_cast<uint32_t>(c & 1), abort_f);
             if (!ok) *abort_f = 1;
             if (tc::bar_or(2, ws::NSIDE, !ok)) break;
@@ -1298,12 +1457,37 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
                 tc::tmem_ld16(q0, x);
                 tc::tmem_ld16(q0 + 16, x + 16);
                 tc::tmem_ld_wait();
-                kk_tables<!LA>(sw, lane, x, Pt, Bt, At, mt, mt + MT_BYTES);
+                if (lane < 16) {
+                    const int t = 16 * (sw & 1) + lane;
+                    const float* pr = Pt + t * TROW;
+                    if (sw < 2) {
+                        if constexpr (!LA) {
+                            const float bk = Bt[t] * Ik[t];
+#pragma unroll
+                            for (int s = 0; s < TC; ++s) AT[s * TROW + t] = s < t ? bk * pr[s] * Ik[s] * x[s] : 0.f;
+                        }
+                    } else {
+                        const float iqt = Iq[t];
+#pragma unroll
+                        for (int s4 = 0; s4 < TC; s4 += 4) {
+                            float m[4], mh[4], ml[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                m[e] = iqt * pr[s4 + e] * Ik[s4 + e] * x[s4 + e];
+                                mh[e] = tc::tf32_hi(m[e]);
+                                ml[e] = m[e] - mh[e];
+                            }
+                            const uint32_t o = tc::kmaj(t, s4, LBO, MT_SBO);
+                            *reinterpret_cast<float4*>(mt + o) = make_float4(mh[0], mh[1], mh[2], mh[3]);
+                            *reinterpret_cast<float4*>(mt + MT_BYTES + o) = make_float4(ml[0], ml[1], ml[2], ml[3]);
+                        }
+                    }
+                }
             }
             tc::fence_smem_to_async();
             tc::fence_before_sync();
             tc::bar_sync(2, ws::NSIDE);
-            if (stid == 0) tc::mbar_arrive(&bar[ws::TAB_READY + (c & 1)]);
+            if (stid == 0) tc::mbar_arrive(&bar[ws::TAB_READY + b]);
         }
         cp_async_wait<0>();   // nothing may be left in flight into shared memory at exit
         __syncthreads();
@@ -1313,6 +1497,8 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
     if (tid == 0 && *abort_f != 0 && p.dev_err) atomicOr(p.dev_err, LAR_DEVERR_TIMEOUT);
     if (warp == 0) tc::tmem_dealloc(tm, TMEM_COLS);
 }
+
+#endif  // LAR_PF_WS
 
 lar_status launch_kernel(void (*kern)(DecodeParams), int threads, uint32_t smem_bytes, const DecodeParams& p,
                          cudaStream_t stream) {
@@ -1334,18 +1520,18 @@ lar_status launch_kernel(void (*kern)(DecodeParams), int threads, uint32_t smem_
     return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? LAR_OK : LAR_ERR_LAUNCH;
 }
 
-// GDN and LA run warp-specialised; KDA (whose per-channel tables need the
-// shared memory the pipeline's second buffers take) in prefill_tc_kernel.  The
-// build flag LAR_PF_WS=0 runs GDN and LA there too.
-#ifndef LAR_PF_WS
-#define LAR_PF_WS 1
-#endif
+// GDN and LA with bf16 q and k run warp-specialised on the raw operands; KDA
+// (whose per-channel tables need the shared memory the pipeline's second
+// buffers take) and fp32 q or k (not exact in tf32) in prefill_tc_kernel.
 template <int FORM, int SB>
 lar_status launch_tc_form(const DecodeParams& p, cudaStream_t stream) {
-    if constexpr (FORM != FORM_KDA && LAR_PF_WS)
-        return launch_kernel(prefill_ws_kernel<FORM, SB>, ws::NT, ws::SMEM, p, stream);
-    else
-        return launch_kernel(prefill_tc_kernel<FORM, SB>, TTH, TC_SMEM, p, stream);
+#if LAR_PF_WS
+    if constexpr (FORM != FORM_KDA) {
+        if (p.q_dt == LAR_BF16 && p.k_dt == LAR_BF16)
+            return launch_kernel(prefill_ws_kernel<FORM, SB>, ws::NT, ws::SMEM, p, stream);
+    }
+#endif
+    return launch_kernel(prefill_tc_kernel<FORM, SB>, TTH, TC_SMEM, p, stream);
 }
 
 }  // namespace

@@ -7,7 +7,8 @@ same tolerances as the token-by-token calls: outputs of every token inside a
 span, written states, untouched pool bytes, rows of tokens outside every span
 left as allocated.  Span lengths straddle the chunk size (31, 32, 33, 64, 65)
 and run to several chunks; empty and bad spans, bf16 pools, in-kernel gates,
-separate and skipped write slots, packed and fp32 inputs are covered.
+separate and skipped write slots, packed, fp32 and unaligned inputs are
+covered.
 """
 import pytest
 import torch
@@ -167,6 +168,41 @@ def test_prefill_close_to_token_by_token(cuda_device):
     torch.cuda.synchronize()
     P.assert_out_close(oa, ob.double().cpu().numpy())
     P.assert_state_close(pa.cpu(), pb.double().cpu().numpy(), "pool")
+
+
+@pytest.mark.parametrize("form", ["gdn", "la"])
+def test_prefill_unaligned_rows_equal_aligned(form, cuda_device):
+    """bf16 q / k / v rows that do not start on a 16-byte boundary are read
+    element by element instead of through the shared-memory staging: the same
+    values enter the same arithmetic, so outputs and states are bit-identical
+    to the aligned call."""
+    dev = cuda_device
+    w = W.make_varlen(form, [31, 70, 0, 129, 5], H=2, HV=2 if form == "gdn" else None, K=128, V=128, seed=77,
+                      raw_gates=form == "gdn")
+    q, k, v = (x.to(dev) for x in (w.q, w.k, w.v))
+
+    def shifted(x):                      # the same values, rows starting 2 bytes past a 16-byte boundary
+        buf = torch.zeros(*x.shape[:-1], x.shape[-1] + 1, dtype=x.dtype, device=dev)
+        buf[..., 1:].copy_(x)
+        return buf[..., 1:]
+
+    def run(q_, k_, v_):
+        pool = w.pool.to(dev)
+        cu, ri = P.to_dev(w.cu_seqlens, dev), P.to_dev(w.read_idx, dev)
+        if form == "la":
+            out = lar.la_prefill(q_, k_, v_, P.to_dev(w.decay, dev), pool, cu, ri, scale=w.scale)
+        else:
+            out = lar.gdn_prefill(q_, k_, v_, P.to_dev(w.g, dev), P.to_dev(w.beta, dev), pool, cu, ri,
+                                  A_log=P.to_dev(w.A_log, dev), dt_bias=P.to_dev(w.dt_bias, dev), scale=w.scale,
+                                  qk_l2norm=w.qk_l2norm, gate_raw=w.gate_raw, beta_raw=w.beta_raw)
+        return out, pool
+
+    qs, ks, vs = shifted(q), shifted(k), shifted(v)
+    assert qs.data_ptr() % 16 != 0 and torch.equal(qs, q)
+    oa, pa = run(q, k, v)
+    ob, pb = run(qs, ks, vs)
+    torch.cuda.synchronize()
+    assert torch.equal(oa, ob) and torch.equal(pa, pb)
 
 
 def test_prefill_rejects_unsupported_shapes(cuda_device):
