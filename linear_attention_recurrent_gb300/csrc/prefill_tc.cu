@@ -845,14 +845,14 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
     if (warp == 0) tc::tmem_dealloc(tm, TMEM_COLS);
 }
 
-// The warp-specialised form below runs GDN and LA with bf16 q and k; the build
+// The warp-specialised form below runs GDN and LA with bf16 q, k and v; the build
 // flag LAR_PF_WS=0 leaves it out (everything then runs in prefill_tc_kernel).
 #ifndef LAR_PF_WS
 #define LAR_PF_WS 1
 #endif
 #if LAR_PF_WS
 // ============================================================================
-// Warp-specialised form (GDN, LA; bf16 q and k).  Per (sequence, head) the
+// Warp-specialised form (GDN, LA; bf16 q / k / v rows, 16-byte aligned).  Per (sequence, head) the
 // chunks form one dependent chain: [U | P] from the state, the solve, O and the
 // increment, the new state.  Everything that does not depend on the state --
 // the chunk's k / q tiles, K K^T, the decay table, the A and M tables -- is
@@ -959,6 +959,28 @@ __device__ __forceinline__ void issue_os(uint32_t tm, uint32_t mth, uint32_t mtl
         }
     }
 }
+// One value row's outputs of a chunk: the Lo finished accumulator columns at
+// taddr, times the scale, to p.out at element offset off0 + t * os[1] (kept out
+// of line: the output stores run once per chunk, and the kernel's code has to
+// share the instruction caches among three concurrent code paths).
+__device__ __noinline__ void store_outputs(uint32_t taddr, const DecodeParams& p, int64_t off0, int Lo) {
+    float o[TC];
+#pragma unroll
+    for (int i = 0; i < TC; i += 16) tc::tmem_ld16(taddr + i, o + i);
+    tc::tmem_ld_wait();
+    const int64_t st = p.os[1];
+    if (p.out_dt == LAR_BF16) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + off0;
+#pragma unroll
+        for (int t = 0; t < TC; ++t)
+            if (t < Lo) out[t * st] = __float2bfloat16_rn(o[t] * p.scale);
+    } else {
+        float* out = static_cast<float*>(p.out) + off0;
+#pragma unroll
+        for (int t = 0; t < TC; ++t)
+            if (t < Lo) out[t * st] = o[t] * p.scale;
+    }
+}
 }  // namespace ws
 
 template <int FORM, int SB>
@@ -1032,14 +1054,8 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
     const bool l2 = !LA && (p.flags & LAR_QK_L2NORM) != 0;
     const bool gate_raw = (p.flags & LAR_GATE_RAW) != 0;
     const bool beta_raw = (p.flags & LAR_BETA_RAW) != 0;
-    // inputs staged through shared memory when every row is bf16 with unit inner
-    // stride and 16-byte aligned; other layouts are read element by element
-    auto rows16 = [](const void* base, int dt, const int64_t* st, int nn) {
-        bool okr = dt == LAR_BF16 && st[3] == 1 && (reinterpret_cast<uintptr_t>(base) & 15) == 0;
-        for (int i = 1; i < nn; ++i) okr = okr && (st[i] * 2) % 16 == 0;
-        return okr;
-    };
-    const bool staged = rows16(p.q, p.q_dt, p.qs, 3) && rows16(p.k, p.k_dt, p.ks, 3) && rows16(p.v, p.v_dt, p.vs, 3);
+    // q, k and v rows are staged through shared memory (the launcher sends
+    // only bf16 rows with unit inner stride and 16-byte alignment here)
     const bool stage_scal = !LA && p.g_dt == LAR_F32 && p.beta_dt == LAR_F32;
 
     if (chain) {
@@ -1088,23 +1104,9 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
         // outputs of chunk cc (half 1): the finished accumulator E P / |q| + D M^T
         auto store_outputs = [&](int cc) {
             const int64_t o0 = static_cast<int64_t>(cc) * TC;
-            const int Lo = static_cast<int>(L - o0 < TC ? L - o0 : TC);
-            float o[TC];
-#pragma unroll
-            for (int i = 0; i < TC; i += 16) tc::tmem_ld16(my + ws::COL_O2 + i, o + i);
-            tc::tmem_ld_wait();
-            const bool obf = p.out_dt == LAR_BF16;
-            const int64_t off0 = (tb + o0) * p.os[1] + static_cast<int64_t>(hv) * p.os[2] +
-                                 static_cast<int64_t>(vrow) * p.os[3];
-#pragma unroll
-            for (int t = 0; t < TC; ++t) {
-                if (t < Lo) {
-                    const float y = o[t] * p.scale;
-                    const int64_t off = off0 + t * p.os[1];
-                    if (obf) static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(y);
-                    else static_cast<float*>(p.out)[off] = y;
-                }
-            }
+            ws::store_outputs(my + ws::COL_O2, p, (tb + o0) * p.os[1] + static_cast<int64_t>(hv) * p.os[2] +
+                                                       static_cast<int64_t>(vrow) * p.os[3],
+                              static_cast<int>(L - o0 < TC ? L - o0 : TC));
         };
 
         bool done = true;
@@ -1142,15 +1144,10 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
             if (half == 0) {
                 // ---- the solve per value row, right-looking: once d_s is final it is
                 // taken out of every later row (one dependent FMA per step).  v_t: the
-                // staged row (the side warps reported the chunk ready) or the input.
+                // staged row (the side warps reported the chunk ready).
                 const unsigned short* sv =
                     reinterpret_cast<const unsigned short*>(smem + ws::OFF_V + (c % ws::NVB) * TC * STG_ROW) + vrow;
-                auto vin = [&](int t) -> float {
-                    if (t >= Lc) return 0.f;
-                    if (staged) return bf16_bits_to_float(sv[t * TVV]);
-                    return ld_in(p.v, (tb + c0 + t) * p.vs[1] + static_cast<int64_t>(hv) * p.vs[2] +
-                                          static_cast<int64_t>(vrow) * p.vs[3], p.v_dt);
-                };
+                auto vin = [&](int t) -> float { return t < Lc ? bf16_bits_to_float(sv[t * TVV]) : 0.f; };
                 float d[TC];
                 if constexpr (LA) {
 #pragma unroll
@@ -1307,7 +1304,7 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
             }
             cp_async_commit();
         };
-        if (staged && L > 0) stage(0, 0);
+        if (L > 0) stage(0, 0);
 
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
@@ -1323,7 +1320,7 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
             // ---- the chain has finished chunk c - 2 (this parity's buffers are free)
             // and the chunk's inputs have landed
             bool ok = c < 2 || tc::mbar_wait_or(&bar[ws::CHAIN_DONE + b], static_cast<uint32_t>(((c - 2) >> 1) & 1), abort_f);
-            if (staged) cp_async_wait<0>();
+            cp_async_wait<0>();
             if (!ok) *abort_f = 1;
             if (tc::bar_or(2, ws::NSIDE, !ok)) break;
             tc::fence_after_sync();
@@ -1335,8 +1332,7 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
 #pragma unroll
             for (int j = 0; j < RPW; ++j) {
                 const int t = RPW * sw + j;
-                const int64_t gt = tb + c0 + t;
-                if (t < Lc && staged) {
+                if (t < Lc) {
                     auto widen = [&](uint32_t off, float* x) {
                         const uint2 u = *reinterpret_cast<const uint2*>(stg + off + t * STG_ROW + lane * 8);
                         x[0] = __uint_as_float(u.x << 16);
@@ -1346,10 +1342,6 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
                     };
                     widen(ws::SQ, qa[j]);
                     widen(ws::SK, ka[j]);
-                } else if (t < Lc) {
-                    const int64_t ch = lane * 4;
-                    ld_in4(p.q, gt * p.qs[1] + h * p.qs[2] + ch * p.qs[3], p.qs[3], p.q_dt, qa[j]);
-                    ld_in4(p.k, gt * p.ks[1] + h * p.ks[2] + ch * p.ks[3], p.ks[3], p.k_dt, ka[j]);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) qa[j][e] = ka[j][e] = 0.f;
@@ -1402,14 +1394,14 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
                         a = p.decay[h * p.dec_s];
                         bt = 1.f;
                     } else {
-                        float x = staged && stage_scal ? reinterpret_cast<const float*>(stg + ws::SG)[t]
-                                                       : ld_in(p.g, gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2], p.g_dt);
+                        float x = stage_scal ? reinterpret_cast<const float*>(stg + ws::SG)[t]
+                                             : ld_in(p.g, gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2], p.g_dt);
                         if (gate_raw) {
                             const float bias = p.dt_bias ? p.dt_bias[hv * p.dtb_s] : 0.f;
                             x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
                         }
                         a = expf(x);
-                        const float bx = staged && stage_scal
+                        const float bx = stage_scal
                                              ? reinterpret_cast<const float*>(stg + ws::SBT)[t]
                                              : ld_in(p.beta, gt * p.bs[1] + static_cast<int64_t>(hv) * p.bs[2], p.beta_dt);
                         bt = beta_raw ? 1.f / (1.f + expf(-bx)) : bx;
@@ -1428,7 +1420,7 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
                 ws::issue_kk(tm, tc::smem_addr(kq));
                 tc::mma_commit(&bar[ws::KK_DONE]);
             }
-            if (staged && c + 1 < nch) stage(c0 + TC, c + 1);
+            if (c + 1 < nch) stage(c0 + TC, c + 1);
             if (sw == 1) {
                 // the decay table, then the factors the chain applies: E_t / |k_t|,
                 // E_t / |q_t|, W_s / |k_s|, E_31
@@ -1520,14 +1512,20 @@ lar_status launch_kernel(void (*kern)(DecodeParams), int threads, uint32_t smem_
     return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? LAR_OK : LAR_ERR_LAUNCH;
 }
 
-// GDN and LA with bf16 q and k run warp-specialised on the raw operands; KDA
-// (whose per-channel tables need the shared memory the pipeline's second
-// buffers take) and fp32 q or k (not exact in tf32) in prefill_tc_kernel.
+// GDN and LA with bf16 q / k / v rows that can be staged run warp-specialised
+// on the raw operands; KDA (whose per-channel tables need the shared memory the
+// pipeline's second buffers take), fp32 q or k (not exact in tf32) and other
+// layouts in prefill_tc_kernel.
 template <int FORM, int SB>
 lar_status launch_tc_form(const DecodeParams& p, cudaStream_t stream) {
 #if LAR_PF_WS
     if constexpr (FORM != FORM_KDA) {
-        if (p.q_dt == LAR_BF16 && p.k_dt == LAR_BF16)
+        // every q / k / v row bf16 with unit inner stride, starting on a 16-byte boundary
+        auto rows16 = [](const void* base, int dt, const int64_t* st) {
+            return dt == LAR_BF16 && st[3] == 1 && (reinterpret_cast<uintptr_t>(base) & 15) == 0 &&
+                   (st[1] * 2) % 16 == 0 && (st[2] * 2) % 16 == 0;
+        };
+        if (rows16(p.q, p.q_dt, p.qs) && rows16(p.k, p.k_dt, p.ks) && rows16(p.v, p.v_dt, p.vs))
             return launch_kernel(prefill_ws_kernel<FORM, SB>, ws::NT, ws::SMEM, p, stream);
     }
 #endif

@@ -171,11 +171,11 @@ def test_prefill_close_to_token_by_token(cuda_device):
 
 
 @pytest.mark.parametrize("form", ["gdn", "la"])
-def test_prefill_unaligned_rows_equal_aligned(form, cuda_device):
-    """bf16 q / k / v rows that do not start on a 16-byte boundary are read
-    element by element instead of through the shared-memory staging: the same
-    values enter the same arithmetic, so outputs and states are bit-identical
-    to the aligned call."""
+def test_prefill_unaligned_rows(form, cuda_device):
+    """bf16 q / k / v rows that do not start on a 16-byte boundary cannot be
+    staged through shared memory; such a call runs the general kernel (rows read
+    element by element) and meets the same oracle tolerances as the aligned
+    call, which runs the warp-specialised one."""
     dev = cuda_device
     w = W.make_varlen(form, [31, 70, 0, 129, 5], H=2, HV=2 if form == "gdn" else None, K=128, V=128, seed=77,
                       raw_gates=form == "gdn")
@@ -199,10 +199,16 @@ def test_prefill_unaligned_rows_equal_aligned(form, cuda_device):
 
     qs, ks, vs = shifted(q), shifted(k), shifted(v)
     assert qs.data_ptr() % 16 != 0 and torch.equal(qs, q)
-    oa, pa = run(q, k, v)
-    ob, pb = run(qs, ks, vs)
+    runs = [run(q, k, v), run(qs, ks, vs)]
     torch.cuda.synchronize()
-    assert torch.equal(oa, ob) and torch.equal(pa, pb)
+    ref = P.run_oracle_varlen(w, w.pool.clone())
+    import numpy as np
+    covered = ~np.isnan(ref["out"]).all(axis=(1, 2))
+    cov = torch.from_numpy(covered).to(dev)
+    for out, pool in runs:
+        P.assert_out_close(out[cov], ref["out"][covered])
+        for n, slot in enumerate(w.read_idx.tolist()):
+            P.assert_state_close(P.slot_state(pool, w, slot), ref["final_state"][n], f"slot {slot}")
 
 
 def test_prefill_rejects_unsupported_shapes(cuda_device):
