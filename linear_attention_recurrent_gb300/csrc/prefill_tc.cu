@@ -53,6 +53,8 @@
 //
 // Every wait is bounded: a wait that gives up makes the whole CTA skip the
 // rest of its span and its writeback, and sets LAR_DEVERR_TIMEOUT.
+#include <cuda.h>   // CUtensorMap and its encoder's signature (called through the runtime's driver entry point)
+
 #include "decode_kernel.cuh"
 #include "tc_util.cuh"
 
@@ -875,6 +877,7 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
 //                                 refill chunk c's buffers with chunk c + 2
 //   UP_DONE, OS_DONE              the chain's products have completed
 //   KK_DONE                       the side's K K^T has completed
+//   STG_FULL                      a chunk's q, k and v boxes have landed
 // so the side works on chunk c + 1 while the chain runs chunk c.  O's
 // accumulator (columns 352..383) starts from E_t P[v][t] / |q_t|, written by the
 // chain's second half while the first half solves, and the finished outputs
@@ -899,16 +902,18 @@ constexpr uint32_t OFF_EK = OFF_B + 2 * TC * 4;               // [parity] E_t / 
 constexpr uint32_t OFF_EQ = OFF_EK + 2 * TC * 4;              // [parity] E_t / |q_t|
 constexpr uint32_t OFF_WK = OFF_EQ + 2 * TC * 4;              // [parity] W_s / |k_s|
 constexpr uint32_t OFF_E31 = OFF_WK + 2 * TC * 4;             // [parity] E_31 (16 bytes each)
-// staging: q rows, k rows, fp32 gates, fp32 betas (one chunk), then the v ring
-constexpr uint32_t OFF_STG = OFF_E31 + 2 * 16;
+// staging (tensor-copy destinations, 128-byte aligned): q rows, k rows, fp32
+// gates, fp32 betas (one chunk), then the v ring
+constexpr uint32_t OFF_STG = (OFF_E31 + 2 * 16 + 127) / 128 * 128;
 constexpr uint32_t SQ = 0, SK = TC * STG_ROW, SG = 2 * TC * STG_ROW, SBT = SG + TC * 4, S_BYTES = SBT + TC * 4;
 constexpr uint32_t OFF_V = OFF_STG + S_BYTES;                 // [NVB][TC] bf16 rows
 constexpr uint32_t OFF_BAR = OFF_V + NVB * TC * STG_ROW;
-enum { KQ_READY = 0, TAB_READY = 2, CHAIN_DONE = 4, UP_DONE = 6, OS_DONE = 7, KK_DONE = 8, NBAR = 9 };
+enum { KQ_READY = 0, TAB_READY = 2, CHAIN_DONE = 4, UP_DONE = 6, OS_DONE = 7, KK_DONE = 8, STG_FULL = 9, NBAR = 10 };
 constexpr uint32_t OFF_TM = OFF_BAR + NBAR * 8;               // TMEM base, picked sequence, abort flag
 constexpr uint32_t SMEM = OFF_TM + 16;
 constexpr uint32_t COL_O2 = 352;                              // O's accumulator (32 columns)
-static_assert(OFF_KT % 16 == 0 && OFF_MT % 16 == 0 && OFF_AT % 16 == 0 && OFF_STG % 16 == 0 && OFF_V % 16 == 0 &&
+static_assert(OFF_KT % 16 == 0 && OFF_MT % 16 == 0 && OFF_AT % 16 == 0 && OFF_STG % 128 == 0 && SK % 128 == 0 &&
+                  OFF_V % 128 == 0 && (TC * STG_ROW) % 128 == 0 &&
                   OFF_BAR % 8 == 0 && KQ_BYTES % 16 == 0 && KT_BYTES % 16 == 0 && MT_BYTES % 16 == 0,
               "tile, staging and barrier alignment");
 static_assert(SMEM <= 227 * 1024, "fits one CTA's shared memory");
@@ -983,9 +988,18 @@ __device__ __noinline__ void store_outputs(uint32_t taddr, const DecodeParams& p
 }
 }  // namespace ws
 
+// The call's arguments and tiled tensor maps over the token-major q, k and v
+// arrays ({channel, head, token}, 16-bit elements, box 128 x 1 x 32: one
+// chunk's rows of one head), which the side warps load one box per chunk.
+struct WsParams {
+    DecodeParams p;
+    CUtensorMap tq, tk, tv;
+};
+
 template <int FORM, int SB>
-__global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_constant__ WsParams wp) {
     static_assert(FORM != FORM_KDA, "KDA runs in prefill_tc_kernel");
+    const DecodeParams& p = wp.p;
     constexpr bool LA = FORM == FORM_LA;
     extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + ws::OFF_BAR);
@@ -1272,39 +1286,29 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
         float* Af = reinterpret_cast<float*>(smem + ws::OFF_AF);
         float* Iq = reinterpret_cast<float*>(smem + ws::OFF_IQ);
         float* Ik = reinterpret_cast<float*>(smem + ws::OFF_IK);
-        // this thread's copies of chunk `ci` (tokens from cs on): q and k rows into
-        // the staging, v rows into the ring, fp32 gates and betas
+        // chunk `ci`'s inputs (tokens from cs on; side warp 0): one box each of q, k
+        // (this head's rows) into the staging and of v into the ring, completing on
+        // STG_FULL; the fp32 gates and betas with cp.async
         auto stage = [&](int64_t cs, int ci) {
             const int Ln = static_cast<int>(L - cs < TC ? L - cs : TC);
-#pragma unroll 1
-            for (int i = stid; i < 3 * TC * 16; i += ws::NSIDE) {
-                const int which = i / (TC * 16), rem = i - which * (TC * 16), t = rem >> 4, cb = rem & 15;
-                if (t >= Ln) continue;
-                const int64_t gt = tb + cs + t;
-                const unsigned char* src;
-                unsigned char* dst;
-                if (which == 0) {
-                    src = static_cast<const unsigned char*>(p.q) + (gt * p.qs[1] + h * p.qs[2]) * 2;
-                    dst = stg + ws::SQ;
-                } else if (which == 1) {
-                    src = static_cast<const unsigned char*>(p.k) + (gt * p.ks[1] + h * p.ks[2]) * 2;
-                    dst = stg + ws::SK;
-                } else {
-                    src = static_cast<const unsigned char*>(p.v) + (gt * p.vs[1] + static_cast<int64_t>(hv) * p.vs[2]) * 2;
-                    dst = smem + ws::OFF_V + (ci % ws::NVB) * TC * STG_ROW;
-                }
-                cp_async16(dst + t * STG_ROW + cb * 16, src + cb * 16);
+            if (lane == 0) {
+                tc::fence_smem_to_async();   // earlier reads of these buffers come first
+                tc::mbar_arrive_expect_tx(&bar[ws::STG_FULL], 3 * TC * STG_ROW);
+                const int z = static_cast<int>(tb + cs);
+                tc::tma_load_3d(stg + ws::SQ, &wp.tq, 0, h, z, &bar[ws::STG_FULL]);
+                tc::tma_load_3d(stg + ws::SK, &wp.tk, 0, h, z, &bar[ws::STG_FULL]);
+                tc::tma_load_3d(smem + ws::OFF_V + (ci % ws::NVB) * TC * STG_ROW, &wp.tv, 0, hv, z, &bar[ws::STG_FULL]);
             }
-            if (stage_scal && stid < TC && stid < Ln) {
-                const int64_t gt = tb + cs + stid;
-                cp_async4(stg + ws::SG + stid * 4,
+            if (stage_scal && lane < Ln) {
+                const int64_t gt = tb + cs + lane;
+                cp_async4(stg + ws::SG + lane * 4,
                           static_cast<const float*>(p.g) + gt * p.gs[1] + static_cast<int64_t>(hv) * p.gs[2]);
-                cp_async4(stg + ws::SBT + stid * 4,
+                cp_async4(stg + ws::SBT + lane * 4,
                           static_cast<const float*>(p.beta) + gt * p.bs[1] + static_cast<int64_t>(hv) * p.bs[2]);
             }
             cp_async_commit();
         };
-        if (L > 0) stage(0, 0);
+        if (sw == 0 && L > 0) stage(0, 0);
 
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
@@ -1319,70 +1323,71 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
 
             // ---- the chain has finished chunk c - 2 (this parity's buffers are free)
             // and the chunk's inputs have landed
-            bool ok = c < 2 || tc::mbar_wait_or(&bar[ws::CHAIN_DONE + b], static_cast<uint32_t>(((c - 2) >> 1) & 1), abort_f);
+            bool ok = (c < 2 || tc::mbar_wait_or(&bar[ws::CHAIN_DONE + b], static_cast<uint32_t>(((c - 2) >> 1) & 1), abort_f)) &&
+                      tc::mbar_wait_or(&bar[ws::STG_FULL], static_cast<uint32_t>(c & 1), abort_f);
             cp_async_wait<0>();
             if (!ok) *abort_f = 1;
             if (tc::bar_or(2, ws::NSIDE, !ok)) break;
             tc::fence_after_sync();
 
-            // ---- raw k and q rows: side warp sw takes tokens 8 sw .. 8 sw + 7, lane l
-            // channels 4l .. 4l + 3; all loads issued before any is used
+            // ---- raw k and q rows: side warp sw takes tokens 8 sw .. 8 sw + 7 in two
+            // runs of 4 (a run's loads issued before any is used), lane l channels
+            // 4l .. 4l + 3
             constexpr int RPW = TC / 4;
-            float qa[RPW][4], ka[RPW][4];
+#pragma unroll 1
+            for (int j0 = 0; j0 < RPW; j0 += 4) {
+                float qa[4][4], ka[4][4];
 #pragma unroll
-            for (int j = 0; j < RPW; ++j) {
-                const int t = RPW * sw + j;
-                if (t < Lc) {
-                    auto widen = [&](uint32_t off, float* x) {
-                        const uint2 u = *reinterpret_cast<const uint2*>(stg + off + t * STG_ROW + lane * 8);
-                        x[0] = __uint_as_float(u.x << 16);
-                        x[1] = __uint_as_float(u.x & 0xffff0000u);
-                        x[2] = __uint_as_float(u.y << 16);
-                        x[3] = __uint_as_float(u.y & 0xffff0000u);
-                    };
-                    widen(ws::SQ, qa[j]);
-                    widen(ws::SK, ka[j]);
-                } else {
+                for (int j = 0; j < 4; ++j) {
+                    const int t = RPW * sw + j0 + j;
+                    if (t < Lc) {
+                        auto widen = [&](uint32_t off, float* x) {
+                            const uint2 u = *reinterpret_cast<const uint2*>(stg + off + t * STG_ROW + lane * 8);
+                            x[0] = __uint_as_float(u.x << 16);
+                            x[1] = __uint_as_float(u.x & 0xffff0000u);
+                            x[2] = __uint_as_float(u.y << 16);
+                            x[3] = __uint_as_float(u.y & 0xffff0000u);
+                        };
+                        widen(ws::SQ, qa[j]);
+                        widen(ws::SK, ka[j]);
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) qa[j][e] = ka[j][e] = 0.f;
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < RPW; ++j) {
-                const int t = RPW * sw + j;
-                float iq = 1.f, ik = 1.f;
-                if (l2) {
-                    float sq = 0.f, sk = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        sq = fmaf(qa[j][e], qa[j][e], sq);
-                        sk = fmaf(ka[j][e], ka[j][e], sk);
+                        for (int e = 0; e < 4; ++e) qa[j][e] = ka[j][e] = 0.f;
                     }
+                }
 #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        sq += __shfl_xor_sync(0xffffffffu, sq, off);
-                        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+                for (int j = 0; j < 4; ++j) {
+                    const int t = RPW * sw + j0 + j;
+                    float iq = 1.f, ik = 1.f;
+                    if (l2) {
+                        float sq = 0.f, sk = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            sq = fmaf(qa[j][e], qa[j][e], sq);
+                            sk = fmaf(ka[j][e], ka[j][e], sk);
+                        }
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1) {
+                            sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                            sk += __shfl_xor_sync(0xffffffffu, sk, off);
+                        }
+                        iq = 1.f / sqrtf(sq + 1e-6f);
+                        ik = 1.f / sqrtf(sk + 1e-6f);
                     }
-                    iq = 1.f / sqrtf(sq + 1e-6f);
-                    ik = 1.f / sqrtf(sk + 1e-6f);
+                    if (lane == 0) {
+                        Iq[t] = iq;
+                        Ik[t] = ik;
+                    }
+                    *reinterpret_cast<float4*>(kq + tc::kmaj(t, 4 * lane, LBO, KQ_SBO)) =
+                        make_float4(ka[j][0], ka[j][1], ka[j][2], ka[j][3]);
+                    *reinterpret_cast<float4*>(kq + tc::kmaj(TC + t, 4 * lane, LBO, KQ_SBO)) =
+                        make_float4(qa[j][0], qa[j][1], qa[j][2], qa[j][3]);
                 }
-                if (lane == 0) {
-                    Iq[t] = iq;
-                    Ik[t] = ik;
-                }
-                *reinterpret_cast<float4*>(kq + tc::kmaj(t, 4 * lane, LBO, KQ_SBO)) =
-                    make_float4(ka[j][0], ka[j][1], ka[j][2], ka[j][3]);
-                *reinterpret_cast<float4*>(kq + tc::kmaj(TC + t, 4 * lane, LBO, KQ_SBO)) =
-                    make_float4(qa[j][0], qa[j][1], qa[j][2], qa[j][3]);
-            }
-            // K^T: channel c = 4 lane + e, tokens 8 sw .. 8 sw + 7 as two 16-byte runs
+                // K^T: channel c = 4 lane + e, the run's 4 tokens as one 16-byte chunk
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int ch = 4 * lane + e;
-#pragma unroll
-                for (int j4 = 0; j4 < RPW; j4 += 4)
-                    *reinterpret_cast<float4*>(kt + tc::kmaj(ch, RPW * sw + j4, LBO, KT_SBO)) =
-                        make_float4(ka[j4][e], ka[j4 + 1][e], ka[j4 + 2][e], ka[j4 + 3][e]);
+                for (int e = 0; e < 4; ++e)
+                    *reinterpret_cast<float4*>(kt + tc::kmaj(4 * lane + e, RPW * sw + j0, LBO, KT_SBO)) =
+                        make_float4(ka[0][e], ka[1][e], ka[2][e], ka[3][e]);
             }
             // decay factors and betas (side warp 1, lane t; padding tokens: no decay, no update)
             if (sw == 1) {
@@ -1412,15 +1417,15 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
             }
             tc::fence_smem_to_async();
             tc::bar_sync(2, ws::NSIDE);
-            // the tiles are complete: the chain may issue [U | P]; K K^T goes out,
-            // and the staging takes the next chunk's copies
-            if (stid == 0) {
+            // the tiles are complete: the chain may issue [U | P]; K K^T goes out
+            // (side warp 3), and the staging takes the next chunk's copies (side warp 0)
+            if (stid == 96) {
                 tc::fence_after_sync();
                 tc::mbar_arrive(&bar[ws::KQ_READY + b]);
                 ws::issue_kk(tm, tc::smem_addr(kq));
                 tc::mma_commit(&bar[ws::KK_DONE]);
             }
-            if (c + 1 < nch) stage(c0 + TC, c + 1);
+            if (sw == 0 && c + 1 < nch) stage(c0 + TC, c + 1);
             if (sw == 1) {
                 // the decay table, then the factors the chain applies: E_t / |k_t|,
                 // E_t / |q_t|, W_s / |k_s|, E_31
@@ -1492,7 +1497,8 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const DecodeParam
 
 #endif  // LAR_PF_WS
 
-lar_status launch_kernel(void (*kern)(DecodeParams), int threads, uint32_t smem_bytes, const DecodeParams& p,
+template <typename Arg>
+lar_status launch_kernel(void (*kern)(Arg), int threads, uint32_t smem_bytes, const Arg& a, const DecodeParams& p,
                          cudaStream_t stream) {
     if (cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem_bytes)) != cudaSuccess)
@@ -1509,8 +1515,44 @@ lar_status launch_kernel(void (*kern)(DecodeParams), int threads, uint32_t smem_
     cfg.attrs = attr;
     cfg.numAttrs = 1;
 #endif
-    return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? LAR_OK : LAR_ERR_LAUNCH;
+    return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? LAR_OK : LAR_ERR_LAUNCH;
 }
+
+#if LAR_PF_WS
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once (null when unavailable).
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// Tensor map over a token-major bf16 array (element strides st: -, token,
+// head, channel with st[3] == 1): {channel 128, head `heads`, token ntok}, box
+// 128 x 1 x TC.  False when the encoder refuses it.
+bool token_map(CUtensorMap* m, const void* base, int64_t heads, int64_t ntok, const int64_t* st) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr || heads < 1 || ntok < 1) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(TK), static_cast<cuuint64_t>(heads),
+                                static_cast<cuuint64_t>(ntok)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(st[2]) * 2, static_cast<cuuint64_t>(st[1]) * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(TK), 1, static_cast<cuuint32_t>(TC)};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+#endif
 
 // GDN and LA with bf16 q / k / v rows that can be staged run warp-specialised
 // on the raw operands; KDA (whose per-channel tables need the shared memory the
@@ -1520,16 +1562,23 @@ template <int FORM, int SB>
 lar_status launch_tc_form(const DecodeParams& p, cudaStream_t stream) {
 #if LAR_PF_WS
     if constexpr (FORM != FORM_KDA) {
-        // every q / k / v row bf16 with unit inner stride, starting on a 16-byte boundary
+        // every q / k / v row bf16 with unit inner stride, starting on a 16-byte
+        // boundary, and token indices that fit the tensor copies' coordinates
         auto rows16 = [](const void* base, int dt, const int64_t* st) {
             return dt == LAR_BF16 && st[3] == 1 && (reinterpret_cast<uintptr_t>(base) & 15) == 0 &&
-                   (st[1] * 2) % 16 == 0 && (st[2] * 2) % 16 == 0;
+                   st[1] > 0 && st[2] > 0 && (st[1] * 2) % 16 == 0 && (st[2] * 2) % 16 == 0;
         };
-        if (rows16(p.q, p.q_dt, p.qs) && rows16(p.k, p.k_dt, p.ks) && rows16(p.v, p.v_dt, p.vs))
-            return launch_kernel(prefill_ws_kernel<FORM, SB>, ws::NT, ws::SMEM, p, stream);
+        if (rows16(p.q, p.q_dt, p.qs) && rows16(p.k, p.k_dt, p.ks) && rows16(p.v, p.v_dt, p.vs) && p.ntok >= 1 &&
+            p.ntok < (int64_t(1) << 31)) {
+            WsParams wp;
+            wp.p = p;
+            if (token_map(&wp.tq, p.q, p.H, p.ntok, p.qs) && token_map(&wp.tk, p.k, p.H, p.ntok, p.ks) &&
+                token_map(&wp.tv, p.v, p.HV, p.ntok, p.vs))
+                return launch_kernel(prefill_ws_kernel<FORM, SB>, ws::NT, ws::SMEM, wp, p, stream);
+        }
     }
 #endif
-    return launch_kernel(prefill_tc_kernel<FORM, SB>, TTH, TC_SMEM, p, stream);
+    return launch_kernel(prefill_tc_kernel<FORM, SB>, TTH, TC_SMEM, p, p, stream);
 }
 
 }  // namespace

@@ -129,6 +129,25 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(mbar)) : "memory");
 }
 
+// One arrival on `mbar` that also raises the phase's expected transaction
+// count by `bytes` (the bulk copies that complete on it count them down).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(mbar)), "r"(bytes)
+                 : "memory");
+}
+
+// One box of a 3-d tiled tensor map (in kernel parameter space) at coordinates
+// (x, y, z) into this CTA's shared memory (128-byte aligned), completing on
+// `mbar` as transactions of the box's full size (out-of-range elements are
+// written as zeros).  x times the element size must be a multiple of 16.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, int y, int z, uint64_t* mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];\n" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(mbar))
+        : "memory");
+}
+
 // As mbar_wait, but it also gives up as soon as `*abort` is set (checked every
 // 256 polls), so that a group of threads whose partner group has stopped does
 // not spin out the whole limit.
