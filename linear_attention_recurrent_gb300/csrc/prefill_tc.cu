@@ -1146,6 +1146,9 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
                     tc::mma_commit(&bar[ws::UP_DONE]);
                 }
             }
+            // the previous chunk's outputs (half 1) while [U | P] runs: its O is
+            // complete, and [U | P] does not touch O's columns
+            if (half == 1 && c > 0) store_outputs(c - 1);
             ok = ok && tc::mbar_wait_or(&bar[ws::UP_DONE], par, abort_f) &&
                  tc::mbar_wait_or(&bar[ws::TAB_READY + b], par2, abort_f);
             if (!ok) *abort_f = 1;
@@ -1196,8 +1199,7 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
                 split_store<TC>(my + COL_DWHI, my + COL_DWLO, d);
                 tc::tmem_st_wait();
             } else {
-                // ---- the previous chunk's outputs, then O's accumulator starts as E_t P[v][t] / |q_t|
-                if (c > 0) store_outputs(c - 1);
+                // ---- O's accumulator starts as E_t P[v][t] / |q_t|
                 float pv[TC];
 #pragma unroll
                 for (int i = 0; i < TC; i += 16) tc::tmem_ld16(my + COL_UP + TC + i, pv + i);
