@@ -854,44 +854,57 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
 #endif
 #if LAR_PF_WS
 // ============================================================================
-// Warp-specialised form (GDN, LA; bf16 q / k / v rows, 16-byte aligned).  Per (sequence, head) the
-// chunks form one dependent chain: [U | P] from the state, the solve, O and the
-// increment, the new state.  Everything that does not depend on the state --
-// the chunk's k / q tiles, K K^T, the decay table, the A and M tables -- is
-// prepared by four "side" warps while the eight "chain" warps run the previous
-// chunk.
+// Warp-specialised form (GDN, LA; bf16 q / k / v rows, 16-byte aligned).  Per
+// (sequence, head) the chunks form one dependent chain: [U | P] from the state,
+// the solve, the increment, the new state.  Everything that does not depend on
+// the state -- the chunk's k / q tiles, K K^T, the decay table, the A and M
+// tables -- and the output product O are handled by four "side" warps beside
+// the eight "chain" warps.
 //
-// Raw operands.  bf16 q and k values are exact in tf32, so the tiles hold the
-// raw values and the l2 norms (when asked) enter as per-token factors
-// 1/|k_t|, 1/|q_t| applied to the products' rows and columns: K K^T and Q K^T
-// come out exact in one tensor-core pass, S^T [K ; Q]^T and (D o W) K in two
-// (the state's and D o W's tf32 halves against exact operands); only O = D M^T
-// keeps three (M is a computed fp32 table).  With no low halves to store, the
-// [K ; Q] and K^T tiles are double-buffered by chunk parity, as are the A, M
-// tables and the per-token factors.
+// bf16 operands.  q and k arrive as bf16, so the [K ; Q] and K^T tiles hold the
+// raw bf16 values and the l2 norms (when asked) enter as per-token factors
+// 1/|k_t|, 1/|q_t| on the products' rows and columns.  The tensor-core operands
+// that are computed fp32 values -- the state and D o W -- are split into three
+// bf16 terms x = b1 + b2 + b3 (b1 the nearest bf16, each further term the
+// nearest bf16 to the exact remainder: 24 significant bits), so every product
+// is exact and accumulates in fp32: K K^T and Q K^T in one kind::f16 pass (8
+// instructions of K = 16), S^T [K ; Q]^T in three (24), (D o W / |k|) K in
+// three (6).  O = D M^T keeps the tf32 three-pass form (12 instructions).  A
+// tensor-core instruction takes about the same time whatever its N (up to 128)
+// and type, so instruction counts set the products' cost.
 //
-// Hand-offs (mbarriers; [2]: one per chunk parity):
+// Hand-offs (mbarriers; [2]: one per chunk parity, completing every other chunk):
 //   KQ_READY[2]   side -> chain   chunk c's [K ; Q] and K^T tiles are written
 //   TAB_READY[2]  side -> chain   chunk c's A and M tables and factors are written
-//   CHAIN_DONE[2] chain -> side   the chain has finished chunk c: the side may
-//                                 refill chunk c's buffers with chunk c + 2
-//   UP_DONE, OS_DONE              the chain's products have completed
-//   KK_DONE                       the side's K K^T has completed
-//   STG_FULL                      a chunk's q, k and v boxes have landed
-// so the side works on chunk c + 1 while the chain runs chunk c.  O's
-// accumulator (columns 352..383) starts from E_t P[v][t] / |q_t|, written by the
-// chain's second half while the first half solves, and the finished outputs
-// are stored one chunk later, off the chain.  A wait that gives up sets a
-// shared abort flag; the waits of the other group see it and give up too, both
-// groups leave their loops, and the CTA skips its writeback.
+//   D_READY[2]    chain -> side   chunk c's D is in tensor memory (and every read
+//                                 of chunk c's side buffers by the chain threads is
+//                                 done): the side issues O(c)
+//   DS_DONE[2]    tensor cores    [U | P](c) and the increment of chunk c have
+//                                 completed
+//   O_DONE[2]     tensor cores    O(c) has completed
+//   UP_DONE, KK_DONE, STG_FULL    [U | P], the side's K K^T, a chunk's input boxes
+// The side refills chunk c's buffers with chunk c + 2 once DS_DONE(c) and
+// O_DONE(c) are in, so it can run up to two chunks ahead.  O(c) enters the
+// tensor pipe right behind the increment and runs while the chain updates the
+// state; its accumulator (columns 352..383) starts from E_t P[v][t] / |q_t|,
+// written by the chain's second half while the first half solves, and its
+// outputs are stored early in the next chunk, while [U | P] runs.  A wait that
+// gives up sets a shared abort flag; the waits of the other group see it and
+// give up too, both groups leave their loops, and the CTA skips its writeback.
 namespace ws {
 constexpr int NCHAIN = 256;   // warps 0..7
 constexpr int NSIDE = 128;    // warps 8..11 (one per tensor-memory lane quarter)
 constexpr int NT = NCHAIN + NSIDE;
 constexpr int NVB = 3;        // v staging ring
-constexpr uint32_t OFF_KQ = 0;                                // [parity] raw [K ; Q] tile
-constexpr uint32_t OFF_KT = OFF_KQ + 2 * KQ_BYTES;            // [parity] raw K^T tile
-constexpr uint32_t OFF_MT = OFF_KT + 2 * KT_BYTES;            // [parity][hi, lo] M tile
+// bf16 tiles, K-major, no swizzle (16-byte core-matrix rows of 8 elements)
+constexpr uint32_t BLBO = 144;                                // K-adjacent core matrices
+constexpr uint32_t BKQ_SBO = (TK / 8) * BLBO + 16;            // [K ; Q]: 64 rows x 128 keys
+constexpr uint32_t BKQ_BYTES = 8 * BKQ_SBO;
+constexpr uint32_t BKT_SBO = (TC / 8) * BLBO + 16;            // K^T: 128 keys x 32 tokens
+constexpr uint32_t BKT_BYTES = (TK / 8) * BKT_SBO;
+constexpr uint32_t OFF_KQ = 0;                                // [parity] [K ; Q] tile
+constexpr uint32_t OFF_KT = OFF_KQ + 2 * BKQ_BYTES;           // [parity] K^T tile
+constexpr uint32_t OFF_MT = OFF_KT + 2 * BKT_BYTES;           // [parity][hi, lo] M tile (tf32)
 constexpr uint32_t OFF_AT = OFF_MT + 4 * MT_BYTES;            // [parity] A transposed: [s][t]
 constexpr uint32_t OFF_P = OFF_AT + 2 * TC * TROW * 4;        // decay table P[t][s] (side)
 constexpr uint32_t OFF_AF = OFF_P + TC * TROW * 4;            // a_t (side)
@@ -908,62 +921,110 @@ constexpr uint32_t OFF_STG = (OFF_E31 + 2 * 16 + 127) / 128 * 128;
 constexpr uint32_t SQ = 0, SK = TC * STG_ROW, SG = 2 * TC * STG_ROW, SBT = SG + TC * 4, S_BYTES = SBT + TC * 4;
 constexpr uint32_t OFF_V = OFF_STG + S_BYTES;                 // [NVB][TC] bf16 rows
 constexpr uint32_t OFF_BAR = OFF_V + NVB * TC * STG_ROW;
-enum { KQ_READY = 0, TAB_READY = 2, CHAIN_DONE = 4, UP_DONE = 6, OS_DONE = 7, KK_DONE = 8, STG_FULL = 9, NBAR = 10 };
+enum {
+    KQ_READY = 0, TAB_READY = 2, D_READY = 4, DS_DONE = 6, O_DONE = 8, UP_DONE = 10, KK_DONE = 11, STG_FULL = 12,
+    NBAR = 13
+};
 constexpr uint32_t OFF_TM = OFF_BAR + NBAR * 8;               // TMEM base, picked sequence, abort flag
 constexpr uint32_t SMEM = OFF_TM + 16;
-constexpr uint32_t COL_O2 = 352;                              // O's accumulator (32 columns)
+// tensor-memory columns: the state's three bf16 planes (64 columns each; D o W's
+// three planes of 16 reuse them once [U | P] has read the state), D's tf32
+// halves for O, [U | P], K K^T, O's accumulator, the increment
+constexpr uint32_t COL_SP = 0, SP_STRIDE = 64, COL_DWP = 0, DWP_STRIDE = 16;
+constexpr uint32_t COL_DH = 192, COL_DL = 224, COL_O2 = 352;
+static_assert(COL_SP + 3 * SP_STRIDE <= COL_DH && COL_DL + TC <= COL_UP && COL_O2 >= COL_KK + TC &&
+                  COL_O2 + TC <= COL_DS,
+              "tensor-memory map");
 static_assert(OFF_KT % 16 == 0 && OFF_MT % 16 == 0 && OFF_AT % 16 == 0 && OFF_STG % 128 == 0 && SK % 128 == 0 &&
-                  OFF_V % 128 == 0 && (TC * STG_ROW) % 128 == 0 &&
-                  OFF_BAR % 8 == 0 && KQ_BYTES % 16 == 0 && KT_BYTES % 16 == 0 && MT_BYTES % 16 == 0,
+                  OFF_V % 128 == 0 && (TC * STG_ROW) % 128 == 0 && OFF_BAR % 8 == 0 && BKQ_BYTES % 16 == 0 &&
+                  BKT_BYTES % 16 == 0 && MT_BYTES % 16 == 0,
               "tile, staging and barrier alignment");
+static_assert(tc::kmaj16(63, TK - 1, BLBO, BKQ_SBO) + 2 <= BKQ_BYTES &&
+                  tc::kmaj16(TK - 1, TC - 1, BLBO, BKT_SBO) + 2 <= BKT_BYTES,
+              "bf16 tiles hold their elements");
 static_assert(SMEM <= 227 * 1024, "fits one CTA's shared memory");
 static_assert(kLptMax * 4 <= NVB * TC * STG_ROW, "the span lengths fit the v ring");
 static_assert(NSIDE == 128 && TC == 32, "one side warp per lane quarter; 8 tokens per side warp");
-static_assert(COL_O2 >= COL_KK + TC && COL_O2 + TC <= COL_DS, "O's accumulator in the free columns");
 
-// K K^T and Q K^T from the raw tile: one pass (exact products)
+// K K^T and Q K^T from the [K ; Q] tile (M = 64, N = 32): one pass
 __device__ __forceinline__ void issue_kk(uint32_t tm, uint32_t kq) {
-    constexpr uint32_t idesc_kk = tc::idesc_tf32(64, TC);
+    constexpr uint32_t idesc = tc::idesc_bf16(64, TC);
 #pragma unroll 1
-    for (int kb = 0; kb < TK / 8; ++kb)
-        tc::mma_ss(tm + COL_KK, tc::smem_desc(kq + kb * 2 * LBO, LBO, KQ_SBO),
-                   tc::smem_desc(kq + kb * 2 * LBO, LBO, KQ_SBO), idesc_kk, kb > 0);
+    for (int kb = 0; kb < TK / 16; ++kb)
+        tc::mma_ss(tm + COL_KK, tc::smem_desc(kq + kb * 2 * BLBO, BLBO, BKQ_SBO),
+                   tc::smem_desc(kq + kb * 2 * BLBO, BLBO, BKQ_SBO), idesc, kb > 0);
 }
 
-// [U | P] = S^T [K ; Q]^T from the raw tile (LA: P only): the state's two tf32 halves
+// [U | P] = S^T [K ; Q]^T (LA: P only) from the state's three bf16 planes
 template <bool LA>
 __device__ __forceinline__ void issue_up(uint32_t tm, uint32_t kq) {
     constexpr int NUP = LA ? TC : 2 * TC;
-    constexpr uint32_t idesc = tc::idesc_tf32(TVV, NUP);
-    const uint32_t bb = kq + (LA ? 4 * KQ_SBO : 0);
+    constexpr uint32_t idesc = tc::idesc_bf16(TVV, NUP);
+    const uint32_t bb = kq + (LA ? 4 * BKQ_SBO : 0);
     const uint32_t dcol = tm + COL_UP + (LA ? TC : 0);
 #pragma unroll 1
-    for (int ps = 0; ps < 2; ++ps) {
-        const uint32_t acol = tm + (ps == 1 ? COL_SLO : COL_SHI);
+    for (int ps = 0; ps < 3; ++ps) {
 #pragma unroll 1
-        for (int kb = 0; kb < TK / 8; ++kb)
-            tc::mma_ts(dcol, acol + 8 * kb, tc::smem_desc(bb + kb * 2 * LBO, LBO, KQ_SBO), idesc, ps > 0 || kb > 0);
+        for (int kb = 0; kb < TK / 16; ++kb)
+            tc::mma_ts(dcol, tm + COL_SP + ps * SP_STRIDE + 8 * kb, tc::smem_desc(bb + kb * 2 * BLBO, BLBO, BKQ_SBO),
+                       idesc, ps > 0 || kb > 0);
     }
 }
 
-// O += D M^T (three passes, onto the accumulator's starting value) and the
-// increment (D o W / |k|) K from the raw K^T tile (two passes)
-__device__ __forceinline__ void issue_os(uint32_t tm, uint32_t mth, uint32_t mtl, uint32_t kt) {
-    constexpr uint32_t idesc_o = tc::idesc_tf32(TVV, TC);
-    constexpr uint32_t idesc_s = tc::idesc_tf32(TVV, TK);
+// the increment (D o W / |k|) K from D o W's three bf16 planes and the K^T tile
+__device__ __forceinline__ void issue_ds(uint32_t tm, uint32_t kt) {
+    constexpr uint32_t idesc = tc::idesc_bf16(TVV, TK);
 #pragma unroll 1
     for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t ad = tm + (ps == 2 ? COL_DLO : COL_DHI);
-        const uint32_t bm = ps == 1 ? mtl : mth;
 #pragma unroll 1
-        for (int kb = 0; kb < TC / 8; ++kb) {
-            tc::mma_ts(tm + COL_O2, ad + 8 * kb, tc::smem_desc(bm + kb * 2 * LBO, LBO, MT_SBO), idesc_o, true);
-            if (ps < 2)
-                tc::mma_ts(tm + COL_DS, tm + (ps == 1 ? COL_DWLO : COL_DWHI) + 8 * kb,
-                           tc::smem_desc(kt + kb * 2 * LBO, LBO, KT_SBO), idesc_s, ps > 0 || kb > 0);
-        }
+        for (int kb = 0; kb < TC / 16; ++kb)
+            tc::mma_ts(tm + COL_DS, tm + COL_DWP + ps * DWP_STRIDE + 8 * kb,
+                       tc::smem_desc(kt + kb * 2 * BLBO, BLBO, BKT_SBO), idesc, ps > 0 || kb > 0);
     }
 }
+
+// O += D M^T (tf32, three passes, onto the accumulator's starting value)
+__device__ __forceinline__ void issue_o(uint32_t tm, uint32_t mth, uint32_t mtl) {
+    constexpr uint32_t idesc = tc::idesc_tf32(TVV, TC);
+#pragma unroll 1
+    for (int ps = 0; ps < 3; ++ps) {
+        const uint32_t ad = tm + (ps == 2 ? COL_DL : COL_DH);
+        const uint32_t bm = ps == 1 ? mtl : mth;
+#pragma unroll 1
+        for (int kb = 0; kb < TC / 8; ++kb)
+            tc::mma_ts(tm + COL_O2, ad + 8 * kb, tc::smem_desc(bm + kb * 2 * LBO, LBO, MT_SBO), idesc, true);
+    }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// x (N values, a multiple of 32) into tensor memory as three bf16 planes
+// (plane i at taddr + i * stride, N / 2 columns of element pairs):
+// x = b1 + b2 + b3 with b1 the nearest bf16 to x and b2, b3 the nearest bf16 to
+// the remainders x - b1 and x - b1 - b2 (both exact in fp32)
+template <int N>
+__device__ __forceinline__ void split3_store(uint32_t taddr, uint32_t stride, const float* x) {
+#pragma unroll
+    for (int i0 = 0; i0 < N; i0 += 32) {
+        float w1[16], w2[16], w3[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float a = x[i0 + 2 * j], b = x[i0 + 2 * j + 1];
+            const uint32_t p1 = pack_bf16x2(a, b);
+            const float ra = a - bf16_lo(p1), rb = b - bf16_hi(p1);
+            const uint32_t p2 = pack_bf16x2(ra, rb);
+            const uint32_t p3 = pack_bf16x2(ra - bf16_lo(p2), rb - bf16_hi(p2));
+            w1[j] = __uint_as_float(p1);
+            w2[j] = __uint_as_float(p2);
+            w3[j] = __uint_as_float(p3);
+        }
+        tc::tmem_st16(taddr + i0 / 2, w1);
+        tc::tmem_st16(taddr + stride + i0 / 2, w2);
+        tc::tmem_st16(taddr + 2 * stride + i0 / 2, w3);
+    }
+}
+
 // One value row's outputs of a chunk: the Lo finished accumulator columns at
 // taddr, times the scale, to p.out at element offset off0 + t * os[1] (kept out
 // of line: the output stores run once per chunk, and the kernel's code has to
@@ -1108,7 +1169,7 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
                     for (int i = 0; i < 16; ++i) x[i] = 0.f;
                 }
             }
-            split_store<64>(my + COL_SHI + col0, my + COL_SLO + col0, S);
+            ws::split3_store<64>(my + ws::COL_SP + col0 / 2, ws::SP_STRIDE, S);
             tc::tmem_st_wait();
         }
         tc::fence_before_sync();
@@ -1142,13 +1203,21 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
                 ok = tc::mbar_wait_or(&bar[ws::KQ_READY + b], par2, abort_f);
                 if (ok) {
                     tc::fence_after_sync();
-                    ws::issue_up<LA>(tm, tc::smem_addr(smem + ws::OFF_KQ + b * KQ_BYTES));
+                    ws::issue_up<LA>(tm, tc::smem_addr(smem + ws::OFF_KQ + b * ws::BKQ_BYTES));
                     tc::mma_commit(&bar[ws::UP_DONE]);
                 }
             }
-            // the previous chunk's outputs (half 1) while [U | P] runs: its O is
-            // complete, and [U | P] does not touch O's columns
-            if (half == 1 && c > 0) store_outputs(c - 1);
+            // the previous chunk's outputs (half 1) while [U | P] runs, once its O has
+            // completed ([U | P] does not touch O's columns)
+            const int cp = c - 1;
+            if (half == 1 && c > 0) {
+                if (tc::mbar_wait_or(&bar[ws::O_DONE + (cp & 1)], static_cast<uint32_t>((cp >> 1) & 1), abort_f)) {
+                    tc::fence_after_sync();
+                    store_outputs(cp);
+                } else {
+                    ok = false;
+                }
+            }
             ok = ok && tc::mbar_wait_or(&bar[ws::UP_DONE], par, abort_f) &&
                  tc::mbar_wait_or(&bar[ws::TAB_READY + b], par2, abort_f);
             if (!ok) *abort_f = 1;
@@ -1157,6 +1226,9 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
                 break;
             }
             tc::fence_after_sync();
+            // every read of the side warps' chunk-c buffers happens before D_READY
+            // (E_31 is taken now)
+            const float ec = reinterpret_cast<const float*>(smem + ws::OFF_E31)[4 * b];
 
             if (half == 0) {
                 // ---- the solve per value row, right-looking: once d_s is final it is
@@ -1193,10 +1265,15 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
                         }
                     }
                 }
-                split_store<TC>(my + COL_DHI, my + COL_DLO, d);
+                // D's tf32 halves for O (once the previous chunk's O has read its D) and
+                // D o W / |k| as three bf16 planes for the increment
+                if (c > 0 && !tc::mbar_wait_or(&bar[ws::O_DONE + (cp & 1)], static_cast<uint32_t>((cp >> 1) & 1), abort_f))
+                    *abort_f = 1;
+                tc::fence_after_sync();
+                split_store<TC>(my + ws::COL_DH, my + ws::COL_DL, d);
 #pragma unroll
                 for (int t = 0; t < TC; ++t) d[t] *= WK[t];
-                split_store<TC>(my + COL_DWHI, my + COL_DWLO, d);
+                ws::split3_store<TC>(my + ws::COL_DWP, ws::DWP_STRIDE, d);
                 tc::tmem_st_wait();
             } else {
                 // ---- O's accumulator starts as E_t P[v][t] / |q_t|
@@ -1214,13 +1291,13 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
             tc::bar_sync(1, ws::NCHAIN);
             tc::fence_after_sync();
 
-            // ---- O and the increment
+            // ---- the increment; D is ready for the side warps' O
             if (tid == 0) {
-                const uint32_t mt = tc::smem_addr(smem + ws::OFF_MT + b * 2 * MT_BYTES);
-                ws::issue_os(tm, mt, mt + MT_BYTES, tc::smem_addr(smem + ws::OFF_KT + b * KT_BYTES));
-                tc::mma_commit(&bar[ws::OS_DONE]);
+                ws::issue_ds(tm, tc::smem_addr(smem + ws::OFF_KT + b * ws::BKT_BYTES));
+                tc::mma_commit(&bar[ws::DS_DONE + b]);
+                tc::mbar_arrive(&bar[ws::D_READY + b]);
             }
-            ok = tc::mbar_wait_or(&bar[ws::OS_DONE], par, abort_f);
+            ok = tc::mbar_wait_or(&bar[ws::DS_DONE + b], par2, abort_f);
             if (!ok) *abort_f = 1;
             if (tc::bar_or(1, ws::NCHAIN, !ok)) {
                 done = false;
@@ -1228,28 +1305,36 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
             }
             tc::fence_after_sync();
 
-            // ---- the new state E_31 S + increment, rounded to nearest, and its
-            // tf32 halves for the next chunk's first product
+            // ---- the new state E_31 S + increment, rounded to nearest, and its bf16
+            // planes for the next chunk's first product
             {
-                const float ec = reinterpret_cast<const float*>(smem + ws::OFF_E31)[4 * b];
                 const bool more = c + 1 < nch;
 #pragma unroll
-                for (int cc = 0; cc < 64; cc += 16) {
-                    float x[16];
+                for (int cc = 0; cc < 64; cc += 32) {
+                    float x[32];
                     tc::tmem_ld16(my + COL_DS + col0 + cc, x);
+                    tc::tmem_ld16(my + COL_DS + col0 + cc + 16, x + 16);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) S[cc + i] = fmaf(ec, S[cc + i], x[i]);
-                    if (more) split_store<16>(my + COL_SHI + col0 + cc, my + COL_SLO + col0 + cc, S + cc);
+                    for (int i = 0; i < 32; ++i) S[cc + i] = fmaf(ec, S[cc + i], x[i]);
+                    if (more) ws::split3_store<32>(my + ws::COL_SP + (col0 + cc) / 2, ws::SP_STRIDE, S + cc);
                 }
                 if (more) tc::tmem_st_wait();
             }
             tc::fence_before_sync();
             tc::bar_sync(1, ws::NCHAIN);
             tc::fence_after_sync();
-            if (tid == 0) tc::mbar_arrive(&bar[ws::CHAIN_DONE + b]);
         }
-        if (done && nch > 0 && half == 1) store_outputs(nch - 1);
+        // the last chunk's outputs, once its O has completed
+        if (done && nch > 0 && half == 1) {
+            const int cl = nch - 1;
+            if (tc::mbar_wait_or(&bar[ws::O_DONE + (cl & 1)], static_cast<uint32_t>((cl >> 1) & 1), abort_f)) {
+                tc::fence_after_sync();
+                store_outputs(cl);
+            } else {
+                *abort_f = 1;
+            }
+        }
 
         __syncthreads();
         if (*abort_f == 0 && wr) {
@@ -1319,14 +1404,27 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
             const int Lc = static_cast<int>(L - c0 < TC ? L - c0 : TC);
             float* AT = reinterpret_cast<float*>(smem + ws::OFF_AT) + b * TC * TROW;
             float* Bt = reinterpret_cast<float*>(smem + ws::OFF_B) + b * TC;
-            unsigned char* kq = smem + ws::OFF_KQ + b * KQ_BYTES;
-            unsigned char* kt = smem + ws::OFF_KT + b * KT_BYTES;
+            unsigned char* kq = smem + ws::OFF_KQ + b * ws::BKQ_BYTES;
+            unsigned char* kt = smem + ws::OFF_KT + b * ws::BKT_BYTES;
             unsigned char* mt = smem + ws::OFF_MT + b * 2 * MT_BYTES;
+            const uint32_t pm2 = static_cast<uint32_t>(((c - 2) >> 1) & 1);   // chunk c - 2's phase
 
-            // ---- the chain has finished chunk c - 2 (this parity's buffers are free)
-            // and the chunk's inputs have landed
-            bool ok = (c < 2 || tc::mbar_wait_or(&bar[ws::CHAIN_DONE + b], static_cast<uint32_t>(((c - 2) >> 1) & 1), abort_f)) &&
-                      tc::mbar_wait_or(&bar[ws::STG_FULL], static_cast<uint32_t>(c & 1), abort_f);
+            // ---- O of chunk c - 2 (side warp 3) once its D is ready: it enters the
+            // tensor pipe right behind that chunk's increment
+            bool ok = true;
+            if (c >= 2 && stid == 96) {
+                ok = tc::mbar_wait_or(&bar[ws::D_READY + b], pm2, abort_f);
+                if (ok) {
+                    tc::fence_after_sync();
+                    ws::issue_o(tm, tc::smem_addr(mt), tc::smem_addr(mt + MT_BYTES));
+                    tc::mma_commit(&bar[ws::O_DONE + b]);
+                }
+            }
+            // ---- chunk c - 2's [U | P] and increment have completed (this parity's
+            // [K ; Q] and K^T tiles, tables and factors are free), and the chunk's
+            // inputs have landed
+            ok = ok && (c < 2 || tc::mbar_wait_or(&bar[ws::DS_DONE + b], pm2, abort_f)) &&
+                 tc::mbar_wait_or(&bar[ws::STG_FULL], static_cast<uint32_t>(c & 1), abort_f);
             cp_async_wait<0>();
             if (!ok) *abort_f = 1;
             if (tc::bar_or(2, ws::NSIDE, !ok)) break;
@@ -1338,24 +1436,21 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
             constexpr int RPW = TC / 4;
 #pragma unroll 1
             for (int j0 = 0; j0 < RPW; j0 += 4) {
+                uint2 qr[4], kr[4];                    // raw bf16 bits (padding tokens: zero)
                 float qa[4][4], ka[4][4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int t = RPW * sw + j0 + j;
-                    if (t < Lc) {
-                        auto widen = [&](uint32_t off, float* x) {
-                            const uint2 u = *reinterpret_cast<const uint2*>(stg + off + t * STG_ROW + lane * 8);
-                            x[0] = __uint_as_float(u.x << 16);
-                            x[1] = __uint_as_float(u.x & 0xffff0000u);
-                            x[2] = __uint_as_float(u.y << 16);
-                            x[3] = __uint_as_float(u.y & 0xffff0000u);
-                        };
-                        widen(ws::SQ, qa[j]);
-                        widen(ws::SK, ka[j]);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) qa[j][e] = ka[j][e] = 0.f;
-                    }
+                    qr[j] = t < Lc ? *reinterpret_cast<const uint2*>(stg + ws::SQ + t * STG_ROW + lane * 8) : make_uint2(0, 0);
+                    kr[j] = t < Lc ? *reinterpret_cast<const uint2*>(stg + ws::SK + t * STG_ROW + lane * 8) : make_uint2(0, 0);
+                    auto widen = [](uint2 u, float* x) {
+                        x[0] = ws::bf16_lo(u.x);
+                        x[1] = ws::bf16_hi(u.x);
+                        x[2] = ws::bf16_lo(u.y);
+                        x[3] = ws::bf16_hi(u.y);
+                    };
+                    widen(qr[j], qa[j]);
+                    widen(kr[j], ka[j]);
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -1380,16 +1475,15 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
                         Iq[t] = iq;
                         Ik[t] = ik;
                     }
-                    *reinterpret_cast<float4*>(kq + tc::kmaj(t, 4 * lane, LBO, KQ_SBO)) =
-                        make_float4(ka[j][0], ka[j][1], ka[j][2], ka[j][3]);
-                    *reinterpret_cast<float4*>(kq + tc::kmaj(TC + t, 4 * lane, LBO, KQ_SBO)) =
-                        make_float4(qa[j][0], qa[j][1], qa[j][2], qa[j][3]);
+                    *reinterpret_cast<uint2*>(kq + tc::kmaj16(t, 4 * lane, ws::BLBO, ws::BKQ_SBO)) = kr[j];
+                    *reinterpret_cast<uint2*>(kq + tc::kmaj16(TC + t, 4 * lane, ws::BLBO, ws::BKQ_SBO)) = qr[j];
                 }
-                // K^T: channel c = 4 lane + e, the run's 4 tokens as one 16-byte chunk
+                // K^T: channel c = 4 lane + e, the run's 4 tokens as one 8-byte run
+                auto bits = [](float x) { return __float_as_uint(x) >> 16; };   // x holds a bf16 value
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    *reinterpret_cast<float4*>(kt + tc::kmaj(4 * lane + e, RPW * sw + j0, LBO, KT_SBO)) =
-                        make_float4(ka[0][e], ka[1][e], ka[2][e], ka[3][e]);
+                    *reinterpret_cast<uint2*>(kt + tc::kmaj16(4 * lane + e, RPW * sw + j0, ws::BLBO, ws::BKT_SBO)) =
+                        make_uint2(bits(ka[0][e]) | (bits(ka[1][e]) << 16), bits(ka[2][e]) | (bits(ka[3][e]) << 16));
             }
             // decay factors and betas (side warp 1, lane t; padding tokens: no decay, no update)
             if (sw == 1) {
@@ -1446,7 +1540,9 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
             // ---- the A (transposed) and M tables from K K^T and Q K^T:
             // A[t][s] = beta_t P[t][s] (k_t . k_s) / (|k_t| |k_s|) for s < t, and
             // M[t][s] = P[t][s] (q_t . k_s) / (|q_t| |k_s|)
-            ok = tc::mbar_wait_or(&bar[ws::KK_DONE], static_cast<uint32_t>(c & 1), abort_f);
+            // (the M tile's buffer also waits for chunk c - 2's O)
+            ok = tc::mbar_wait_or(&bar[ws::KK_DONE], static_cast<uint32_t>(c & 1), abort_f) &&
+                 (c < 2 || tc::mbar_wait_or(&bar[ws::O_DONE + b], pm2, abort_f));
             if (!ok) *abort_f = 1;
             if (tc::bar_or(2, ws::NSIDE, !ok)) break;
             tc::fence_after_sync();
@@ -1487,6 +1583,21 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
             tc::fence_before_sync();
             tc::bar_sync(2, ws::NSIDE);
             if (stid == 0) tc::mbar_arrive(&bar[ws::TAB_READY + b]);
+        }
+        // the last two chunks' O
+        if (stid == 96 && *abort_f == 0) {
+#pragma unroll 1
+            for (int cc = nch >= 2 ? nch - 2 : 0; cc < nch; ++cc) {
+                const int bb = cc & 1;
+                if (!tc::mbar_wait_or(&bar[ws::D_READY + bb], static_cast<uint32_t>((cc >> 1) & 1), abort_f)) {
+                    *abort_f = 1;
+                    break;
+                }
+                tc::fence_after_sync();
+                unsigned char* mt = smem + ws::OFF_MT + bb * 2 * MT_BYTES;
+                ws::issue_o(tm, tc::smem_addr(mt), tc::smem_addr(mt + MT_BYTES));
+                tc::mma_commit(&bar[ws::O_DONE + bb]);
+            }
         }
         cp_async_wait<0>();   // nothing may be left in flight into shared memory at exit
         __syncthreads();

@@ -1,7 +1,8 @@
 // tc_util.cuh -- sm_100-family tensor-core primitives for the chunked prefill:
-// tensor-memory (TMEM) allocation and access, tcgen05.mma (kind::tf32) with the
-// A operand in TMEM and the B operand in shared memory, completion through
-// mbarriers, and the 3-pass tf32 split that keeps fp32 accuracy.
+// tensor-memory (TMEM) allocation and access, tcgen05.mma (kind::tf32 and
+// kind::f16 with bf16 operands) with the A operand in TMEM or shared memory and
+// the B operand in shared memory, completion through mbarriers, tensor-map bulk
+// copies, and the tf32 split that keeps fp32 accuracy.
 //
 // Shared-memory operands use the K-major, no-swizzle layout: an operand tile
 // of R rows x KD elements (4-byte) is made of "core matrices" of 8 rows x 16
@@ -37,9 +38,23 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// 32-bit instruction descriptor of kind::f16 with bf16 A and B (both), D fp32,
+// both K-major, M x N (16 elements of K per instruction)
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // byte offset of element (r, k) of a K-major no-swizzle tile
 __host__ __device__ constexpr uint32_t kmaj(int r, int k, uint32_t lbo, uint32_t sbo) {
     return static_cast<uint32_t>((r & 7) * 16 + (r >> 3) * sbo + (k >> 2) * lbo + (k & 3) * 4);
+}
+
+// the same for 16-bit elements (8 per 16-byte core-matrix row).  In tensor
+// memory a 16-bit A operand packs elements 2j (low half) and 2j + 1 (high half)
+// of a row into 32-bit column j.
+__host__ __device__ constexpr uint32_t kmaj16(int r, int k, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint32_t>((r & 7) * 16 + (r >> 3) * sbo + (k >> 3) * lbo + (k & 7) * 2);
 }
 
 // ---- 3-pass tf32 split: x = hi + lo with hi = x rounded to tf32 (nearest,
