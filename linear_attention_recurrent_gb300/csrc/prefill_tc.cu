@@ -504,6 +504,16 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
 
     bool ok = true;
     int chunk = 0;
+    // KDA gate chain constants of this head and of this lane's four key channels
+    float negA = 0.f, bias4[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (KDA) {
+        if (gate_raw) {
+            negA = -expf(p.A_log[hv * p.A_s]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                bias4[e] = p.dt_bias ? p.dt_bias[(static_cast<int64_t>(hv) * TK + lane * 4 + e) * p.dtb_s] : 0.f;
+        }
+    }
 
 #pragma unroll 1
     for (int64_t c0 = 0; c0 < L; c0 += TC, ++chunk) {
@@ -578,11 +588,7 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float x = gk[e];
-                    if (gate_raw) {
-                        const int c = lane * 4 + e;
-                        const float bias = p.dt_bias ? p.dt_bias[(static_cast<int64_t>(hv) * TK + c) * p.dtb_s] : 0.f;
-                        x = -expf(p.A_log[hv * p.A_s]) * softplus_f(x + bias);
-                    }
+                    if (gate_raw) x = negA * softplus_f(x + bias4[e]);
                     a4[e] = tok ? expf(x) : 1.f;
                 }
                 *reinterpret_cast<float4*>(Ad + t * TK + 4 * lane) = make_float4(a4[0], a4[1], a4[2], a4[3]);
@@ -674,7 +680,9 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                 *reinterpret_cast<float*>(smem + OFF_MTL + o) = m - mh;
             }
             // per channel c: the update's rows P[31][s][c] k_s[c] (a running product from the
-            // chunk's end), the first product's rows E_t[c] k_t[c] and E_t[c] q_t[c], and E_31[c]
+            // chunk's end; threads 0..127), the first product's rows E_t[c] k_t[c] and
+            // E_t[c] q_t[c], and E_31[c] (threads 128..255)
+            static_assert(TTH == 2 * TK, "one thread per channel for each half of the tiles");
             if (tid < TK) {
                 const int c = tid;
                 float wv = 1.f;
@@ -687,6 +695,8 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
                     *reinterpret_cast<float*>(smem + OFF_KTL + o) = x - xh;
                     wv *= Ad[s2 * TK + c];
                 }
+            } else {
+                const int c = tid - TK;
                 float ev = 1.f;
 #pragma unroll 4
                 for (int t = 0; t < TC; ++t) {
