@@ -395,7 +395,8 @@ def hold_stream(stream, cycles=1_000_000):
 
 
 # tensor-core rates: the measured dense bf16 GEMM rate x the nominal tf32 / bf16
-# ratio (1.1 / 2.25 PFLOP/s), the chunked prefill's products being tf32
+# ratio (1.1 / 2.25 PFLOP/s): the chunked prefill's products are fp32-accurate,
+# reported against the rate of a single tf32 pass
 TF32_OVER_BF16 = 1.1 / 2.25
 PREFILL_CHUNK = 32
 
@@ -411,7 +412,8 @@ def bf16_peak():
 
 def prefill_tensor_flops(w) -> int:
     """FLOPs of the chunked prefill's tensor-core products per launch, one
-    pass (the kernel runs each product in three tf32 passes): per 32-token
+    pass (the kernels run each product as several exact-product passes: bf16
+    terms or tf32 halves): per 32-token
     chunk of a span and value head, [U | P] = S0^T [K ; Q]^T (GDN, KDA;
     LA: P only), [K ; Q] K^T (GDN; LA: Q K^T; KDA builds it on the CUDA cores),
     O = D M^T and the increment (D o W) K."""
@@ -431,7 +433,11 @@ def roofline(w, config, mean_launch_ms, achieved_gbs, peak_gbs, peak_kind):
     (long variable-length spans), in which case the line reports against that.
     The chunked prefill runs its products on the tensor cores and reports
     against the tf32 rate."""
-    kname = "prefill_kernel" if w.meta.get("prefill") else "decode_kernel"
+    if w.meta.get("prefill"):
+        # GDN / LA with staged bf16 rows run the warp-specialised kernel
+        kname = "prefill_tc_kernel" if w.form == "kda" else "prefill_ws_kernel"
+    else:
+        kname = "decode_kernel"
     base = {"traffic": measured_traffic(config), "traffic_steady": measured_traffic(config, steady=True),
             "kernel": f"{kname}<{w.form}> ({kernel_source_hash(config)})",
             "mean_launch_us": round(mean_launch_ms * 1e3, 3)}
@@ -444,7 +450,9 @@ def roofline(w, config, mean_launch_ms, achieved_gbs, peak_gbs, peak_kind):
         return dict({"bound": "tensor", "achieved": round(achieved, 3), "peak": round(peak, 1),
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{kind} bf16 GEMM rate x nominal tf32/bf16 ratio 1.1/2.25",
-                     "flops_per_launch": flops, "passes": 3,
+                     "flops_per_launch": flops,
+                     "passes": ("tf32 x3" if w.form == "kda" else
+                                "bf16 x3 ([U | P], increment), bf16 x1 (K K^T), tf32 x3 (O)"),
                      "alu_equivalent": {"achieved": round(ops / (mean_launch_ms * 1e-3) / 1e12, 3),
                                         "unit": "T lane-op/s", "frac": round(ops / (mean_launch_ms * 1e-3) / ALU_PEAK_OPS, 4)},
                      "hbm_frac": round(achieved_gbs / peak_gbs, 4)}, **base)
