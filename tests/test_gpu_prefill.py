@@ -98,6 +98,15 @@ def test_prefill_parity(name, cuda_device):
 
 
 @pytest.mark.parametrize("form", ["gdn", "kda"])
+def test_prefill_many_sequences(form, cuda_device):
+    """More sequences than the longest-first ranking takes (256): the grid
+    keeps the sequences' own order; short and chunk-straddling spans."""
+    lengths = [(7 * i) % 41 for i in range(300)]
+    w = W.make_varlen(form, lengths, H=1, HV=1, K=128, V=128, P=320, seed=78, raw_gates=form == "kda")
+    prefill_check(w, cuda_device)
+
+
+@pytest.mark.parametrize("form", ["gdn", "kda"])
 def test_prefill_bad_spans(form, cuda_device):
     w = W.make_varlen(form, [40, 6, 3, 5], H=1, HV=2, K=128, V=128, seed=72, separate_write=True,
                       raw_gates=form == "kda")
