@@ -74,8 +74,8 @@ DESCRIPTIONS = {
 # the sources each kernel is built from (the ABI layer included: it sets the launch parameters)
 _DECODE_SOURCES = ("decode_kernel.cuh", "decode_kv_kernel.cuh", "decode_gdn.cu", "decode_kda.cu", "decode_la.cu",
                    "decode_params.h", "launch_cache.cpp", "lar_abi.cpp")
-_PREFILL_SOURCES = ("prefill.cu", "prefill_tc.cu", "tc_util.cuh", "decode_kernel.cuh", "decode_params.h",
-                    "lar_abi.cpp")
+_PREFILL_SOURCES = ("prefill.cu", "prefill_tc.cu", "prefill_ws.cu", "prefill_common.cuh", "tc_util.cuh",
+                    "decode_kernel.cuh", "decode_params.h", "lar_abi.cpp")
 
 
 def _code_only(text: str) -> str:
