@@ -51,12 +51,8 @@ lar_status launch_kda(const DecodeParams& p, void* stream);
 lar_status launch_la(const DecodeParams& p, void* stream);
 // chunked form over variable-length spans (GDN, KDA and LA, K = V = 128; prefill.cu)
 lar_status launch_prefill(const DecodeParams& p, void* stream);
-// the same with the chunk products on the tensor cores (prefill_tc.cu)
+// the same for GDN and LA with the chunk products on the tensor cores (prefill_tc.cu)
 lar_status launch_prefill_tc(const DecodeParams& p, void* stream);
-// the warp-specialised tensor-core form for GDN and LA with bf16 q / k / v rows
-// that can be staged (prefill_ws.cu); *launched false: the call does not qualify
-// and nothing was launched
-lar_status launch_prefill_ws(const DecodeParams& p, void* stream, bool* launched);
 
 // Largest T a call may use (per-pair token tables are sized for it).
 constexpr int kMaxTokens = 16;

@@ -9,6 +9,12 @@
 #include "tc_util.cuh"
 
 namespace lar {
+
+// The warp-specialised tensor-core prefill for GDN and LA with bf16 q / k / v
+// rows that can be staged (prefill_ws.cu); *launched false: the call does not
+// qualify and nothing was launched.
+lar_status launch_prefill_ws(const DecodeParams& p, void* stream, bool* launched);
+
 namespace pf {
 
 inline constexpr int TK = 128;       // key channels
