@@ -357,3 +357,42 @@ class PreparedCall:
                 st = self._fn(*self._args)
         if st != 0:
             _check(self._name, st)
+
+
+class StepGraph:
+    """One serving step captured once as a CUDA graph and replayed with one
+    launch: the copies of the step's inputs to the device (``copies_in``, pairs
+    ``(device_dst, src)``), a ``PreparedCall`` built on ``stream``, and the
+    copies of its results back (``copies_out``, pairs ``(dst, device_src)``).
+    Replays reuse the captured storage: the caller refills the source buffers
+    (pinned host memory for asynchronous copies) between replays and keeps every
+    tensor alive.  ``stream`` must not be the default stream (a capture needs
+    its own).  ``warmup`` eager runs of the step come first, so that the call's
+    one-time setup (the library's attribute and occupancy caches) happens
+    outside the capture."""
+
+    def __init__(self, call: PreparedCall, *, copies_in=(), copies_out=(), stream: torch.cuda.Stream,
+                 warmup: int = 1):
+        if stream is None or stream == torch.cuda.default_stream(stream.device):
+            raise ValueError("StepGraph needs a non-default stream")
+        self._call, self._in, self._out, self._stream = call, list(copies_in), list(copies_out), stream
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                self._body()
+        stream.synchronize()
+        self._graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self._graph, stream=stream, capture_error_mode="thread_local"):
+            self._body()
+
+    def _body(self):
+        for dst, src in self._in:
+            dst.copy_(src, non_blocking=True)
+        self._call()
+        for dst, src in self._out:
+            dst.copy_(src, non_blocking=True)
+
+    def replay(self):
+        """Launch the step on its stream (asynchronous: synchronize the stream
+        before reading host-side results)."""
+        with torch.cuda.stream(self._stream):
+            self._graph.replay()
