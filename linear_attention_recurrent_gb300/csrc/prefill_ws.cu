@@ -291,6 +291,9 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
 
     if (chain) {
         // ================= chain warps =================
+        // registers: the chain's two warpgroups take 200 a thread, the side's
+        // warpgroup 104 (256 x 200 + 128 x 104 = 384 x 168, the launch's total)
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 200;\n" ::: "memory");
         const uint32_t my = tm + lane_off;
         const int col0 = 64 * half;                              // this thread's 64 state columns
         float S[64];
@@ -522,6 +525,7 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
         }
     } else {
         // ================= side warps =================
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 104;\n" ::: "memory");
         const int sw = warp - ws::NCHAIN / 32;                   // 0..3: also the tensor-memory lane quarter
         const int stid = tid - ws::NCHAIN;
         unsigned char* stg = smem + ws::OFF_STG;
