@@ -577,51 +577,57 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
             // ---- (1b) KDA: A[t][s] = beta_t sum_c k_t[c] k_s[c] P[t][s][c] (s < t) and
             // M[t][s] = sum_c q_t[c] k_s[c] P[t][s][c] (s <= t), P[t][s][c] = a_{s+1}[c] ... a_t[c]
             // kept as a running product over t (factors <= 1: nothing overflows).  Warp w
-            // takes s = w, w + 8, ...; lane l channels 4l .. 4l + 3; each lane's 32 partial sums
-            // (one per t) are reduced across the warp by recursive halving, which leaves lane
-            // l holding the sums for t = l.
-            static_assert(TC == 32, "one token per lane after the reduction");
-#pragma unroll 1
-            for (int s = warp; s < TC; s += TTH / 32) {
-                const float4 ks = *reinterpret_cast<const float4*>(K32 + s * FROW + 4 * lane);
-                float4 pr = make_float4(1.f, 1.f, 1.f, 1.f);
-                float va[TC], vm[TC];
+            // takes its four s = w, w + 8, w + 16, w + 24 together, so each token row is read
+            // once per warp; lane l channels 4l .. 4l + 3.  Over a block of 8 tokens each lane
+            // holds 64 partial sums, value j = 16 i + 2 tt + kind for s_i, t = 8 b + tt and
+            // kind 0 (A) / 1 (M); recursive halving across the warp leaves lane l holding
+            // j = 2l and 2l + 1: the pair (t = 8 b + l % 8, s = w + 8 (l / 8)).
+            static_assert(TC == 32 && TTH == 256, "8 warps x 4 s-values; 4 blocks of 8 tokens");
+            {
+                float4 ks[4], pr[4];
 #pragma unroll
-                for (int t = 0; t < TC; ++t) {
-                    va[t] = 0.f;
-                    vm[t] = 0.f;
-                    if (t >= s) {
-                        if (t > s) {
-                            const float4 a4 = *reinterpret_cast<const float4*>(Ad + t * TK + 4 * lane);
-                            pr = make_float4(pr.x * a4.x, pr.y * a4.y, pr.z * a4.z, pr.w * a4.w);
-                        }
+                for (int i = 0; i < 4; ++i) {
+                    ks[i] = *reinterpret_cast<const float4*>(K32 + (warp + 8 * i) * FROW + 4 * lane);
+                    pr[i] = make_float4(1.f, 1.f, 1.f, 1.f);
+                }
+#pragma unroll 1
+                for (int b8 = 0; b8 < TC / 8; ++b8) {
+                    float v[64];
+#pragma unroll
+                    for (int tt = 0; tt < 8; ++tt) {
+                        const int t = 8 * b8 + tt;
+                        const float4 a4 = *reinterpret_cast<const float4*>(Ad + t * TK + 4 * lane);
                         const float4 kt = *reinterpret_cast<const float4*>(K32 + t * FROW + 4 * lane);
                         const float4 qt = *reinterpret_cast<const float4*>(Q32 + t * FROW + 4 * lane);
-                        const float wx = ks.x * pr.x, wy = ks.y * pr.y, wz = ks.z * pr.z, ww = ks.w * pr.w;
-                        va[t] = fmaf(kt.w, ww, fmaf(kt.z, wz, fmaf(kt.y, wy, kt.x * wx)));
-                        vm[t] = fmaf(qt.w, ww, fmaf(qt.z, wz, fmaf(qt.y, wy, qt.x * wx)));
-                    }
-                }
 #pragma unroll
-                for (int nn = TC / 2; nn >= 1; nn >>= 1) {
-                    const bool up = (lane & nn) != 0;
-#pragma unroll
-                    for (int i = 0; i < nn; ++i) {
-                        const float sa = up ? va[i] : va[i + nn];
-                        const float sq = up ? vm[i] : vm[i + nn];
-                        const float ka = up ? va[i + nn] : va[i];
-                        const float kq = up ? vm[i + nn] : vm[i];
-                        va[i] = ka + __shfl_xor_sync(0xffffffffu, sa, nn);
-                        vm[i] = kq + __shfl_xor_sync(0xffffffffu, sq, nn);
+                        for (int i = 0; i < 4; ++i) {
+                            const int si = warp + 8 * i;
+                            if (t > si) pr[i] = make_float4(pr[i].x * a4.x, pr[i].y * a4.y, pr[i].z * a4.z, pr[i].w * a4.w);
+                            const float wx = ks[i].x * pr[i].x, wy = ks[i].y * pr[i].y, wz = ks[i].z * pr[i].z,
+                                        ww = ks[i].w * pr[i].w;
+                            const bool on = t >= si;
+                            v[16 * i + 2 * tt] = on ? fmaf(kt.w, ww, fmaf(kt.z, wz, fmaf(kt.y, wy, kt.x * wx))) : 0.f;
+                            v[16 * i + 2 * tt + 1] = on ? fmaf(qt.w, ww, fmaf(qt.z, wz, fmaf(qt.y, wy, qt.x * wx))) : 0.f;
+                        }
                     }
+#pragma unroll
+                    for (int half = 32, lb = 16; half >= 2; half >>= 1, lb >>= 1) {
+                        const bool up = (lane & lb) != 0;
+#pragma unroll
+                        for (int i = 0; i < half; ++i) {
+                            const float send = up ? v[i] : v[i + half];
+                            const float keep = up ? v[i + half] : v[i];
+                            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, lb);
+                        }
+                    }
+                    const int t = 8 * b8 + (lane & 7), s = warp + 8 * (lane >> 3);
+                    At[t * TROW + s] = t > s ? Bt[t] * v[0] : 0.f;
+                    const float m = t >= s ? v[1] : 0.f;
+                    const float mh = tc::tf32_hi(m);
+                    const uint32_t o = tc::kmaj(t, s, LBO, MT_SBO);
+                    *reinterpret_cast<float*>(smem + OFF_MTH + o) = mh;
+                    *reinterpret_cast<float*>(smem + OFF_MTL + o) = m - mh;
                 }
-                const int t = lane;
-                At[t * TROW + s] = t > s ? Bt[t] * va[0] : 0.f;
-                const float m = t >= s ? vm[0] : 0.f;
-                const float mh = tc::tf32_hi(m);
-                const uint32_t o = tc::kmaj(t, s, LBO, MT_SBO);
-                *reinterpret_cast<float*>(smem + OFF_MTH + o) = mh;
-                *reinterpret_cast<float*>(smem + OFF_MTL + o) = m - mh;
             }
             // per channel c: the update's rows P[31][s][c] k_s[c] (a running product from the
             // chunk's end; threads 0..127), the first product's rows E_t[c] k_t[c] and
