@@ -378,7 +378,7 @@ def run_lar(args, world, rank, local):
         "roofline": roofline(w, args.config, mean_launch_ms, achieved, peak, peak_kind),
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step(w),
         "clocks": clocks,
     }
     return line
@@ -399,6 +399,16 @@ def hold_stream(stream, cycles=1_000_000):
 # reported against the rate of a single tf32 pass
 TF32_OVER_BF16 = 1.1 / 2.25
 PREFILL_CHUNK = 32
+
+
+def launches_per_step(w) -> int:
+    """Kernels of this library launched per call: a variable-length call
+    without a state cache at K = V = 128 launches the chunked kernel for its
+    long spans and the token-by-token kernel for the rest."""
+    if w.cu_seqlens is not None and not w.meta.get("prefill") and not w.cache_intermediate and w.K == 128 \
+            and w.V == 128:
+        return 2
+    return 1
 
 
 def bf16_peak():

@@ -393,7 +393,9 @@ __device__ __forceinline__ void vl_partition(const DecodeParams& p, int64_t U, i
     auto weight = [&](int64_t b) -> long long {
         const int64_t a = ld_idx(p.cu, b * p.cu_s, p.cu_dt);
         const int64_t e = ld_idx(p.cu, (b + 1) * p.cu_s, p.cu_dt);
-        return (a >= 0 && e >= a && e <= p.ntok ? e - a : 0) + kVlTileCost;
+        const int64_t len = a >= 0 && e >= a && e <= p.ntok ? e - a : 0;
+        // spans the chunked kernel takes cost this kernel only their (empty) tiles
+        return (p.split_len > 0 && len >= p.split_len ? 0 : len) + kVlTileCost;
     };
     long long own = 0;
     for (int64_t b = lo; b < hi; ++b) own += weight(b);
@@ -511,6 +513,13 @@ decode_kernel(const DecodeParams p) {
     // slot and yields kBadCount (zero seed, flagged).
     constexpr int64_t kBadCount = INT64_MIN;
     auto seed_of = [&](int b) -> int64_t {
+        if constexpr (VL) {
+            // a span the chunked kernel takes: no state to load here
+            if (p.split_len > 0) {
+                const int64_t lo = ld_idx(p.cu, b * p.cu_s, p.cu_dt), hi = ld_idx(p.cu, (b + 1) * p.cu_s, p.cu_dt);
+                if (lo >= 0 && hi >= lo && hi <= p.ntok && hi - lo >= p.split_len) return -1;
+            }
+        }
         if (!TOK || p.nacc == nullptr) return ld_idx(p.ridx, b * p.ri_s, p.ri_dt);
         const int64_t a = ld_idx(p.nacc, b * p.na_s, p.na_dt);
         if (a < 1 || a > T) return kBadCount;
@@ -637,6 +646,11 @@ decode_kernel(const DecodeParams p) {
                 tb = span_ok ? lo : 0;
                 L = span_ok ? static_cast<int>(hi - lo) : 0;
                 fresh = true;
+                // a span the chunked kernel takes: nothing to compute or write here
+                if (p.split_len > 0 && L >= p.split_len) {
+                    L = 0;
+                    wr = false;
+                }
             }
             if (threadIdx.x == 0 && hv == 0 && p.dev_err) {
                 int e = (r >= p.P ? LAR_DEVERR_READ_SLOT : 0) | (w >= p.P ? LAR_DEVERR_WRITE_SLOT : 0) |

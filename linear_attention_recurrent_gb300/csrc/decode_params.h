@@ -37,6 +37,10 @@ struct DecodeParams {
 
     const void* cu;    int64_t cu_s; int cu_dt;    // varlen: token spans [N+1] or NULL (fixed T)
     int64_t ntok;                                   // varlen: tokens in the q/k/v arrays
+    // varlen: spans (valid ones) of at least this many tokens run in the chunked
+    // form -- the prefill kernels take only those, the token-by-token kernel skips
+    // them; 0: one kernel takes every span
+    int split_len;
 
     void* out;    int64_t os[4]; int out_dt;
     void* inter; int64_t is[4]; int inter_dt;     // fp32 or bf16; b, t, head, row (same layout as the pool); may be NULL
@@ -72,5 +76,12 @@ constexpr int kVarlenChunkBf16 = LAR_VL_CHUNK_BF16;
 static_assert(kVarlenChunk >= 1 && kVarlenChunk <= kMaxTokens && kVarlenChunkBf16 >= 1 &&
                   kVarlenChunkBf16 <= kMaxTokens,
               "chunks within the staging capacity");
+// A variable-length call without a state cache (K = V = 128) sends spans of at
+// least this many tokens to the chunked tensor-core kernels and the rest to the
+// token-by-token kernel; 0 keeps every span token by token.
+#ifndef LAR_VL_SPLIT
+#define LAR_VL_SPLIT 16
+#endif
+constexpr int kVarlenSplit = LAR_VL_SPLIT;
 
 }  // namespace lar

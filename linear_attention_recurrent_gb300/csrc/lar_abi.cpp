@@ -477,6 +477,14 @@ lar_status varlen(int form, const lar_tensor* q, const lar_tensor* k, const lar_
     if ((st = check_aliasing(outs, 3, ins, 11, dev_err)) != LAR_OK) return st;
     if (N == 0) return LAR_OK;
     if (prefill) return lar::launch_prefill(p, stream);
+    // Without a state cache, spans of kVarlenSplit tokens or more run in the
+    // chunked form (several times cheaper per token from about a dozen tokens on)
+    // and the token-by-token kernel skips them: two launches, each deciding per
+    // span on the device from cu_seqlens.
+    if (!inter && K == 128 && V == 128 && lar::kVarlenSplit > 0) {
+        p.split_len = lar::kVarlenSplit;
+        if ((st = lar::launch_prefill(p, stream)) != LAR_OK) return st;
+    }
     switch (form) {
         case lar::FORM_GDN: return lar::launch_gdn(p, stream);
         case lar::FORM_KDA: return lar::launch_kda(p, stream);
