@@ -104,13 +104,16 @@ def _code_only(text: str) -> str:
 
 
 def kernel_source_hash(config: str = "gdn_b64") -> str:
-    """Hash of the code (comments aside) of the kernel a workload runs (the
-    chunked prefill kernel or the decode kernels); ncu traffic figures are
-    valid only for it."""
-    prefill = config in W.CONFIGS and W.make_meta(config).get("prefill", False)
+    """Hash of the code (comments aside) of the kernels a workload runs (the
+    chunked prefill kernels, the decode kernels, or both for a split
+    variable-length call); ncu traffic figures are valid only for it."""
+    meta = W.make_meta(config) if config in W.CONFIGS else {}
+    names = set(_PREFILL_SOURCES if meta.get("prefill") else _DECODE_SOURCES)
+    if meta.get("split"):
+        names |= set(_PREFILL_SOURCES)
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_recurrent_gb300", "csrc")
-    for name in sorted(_PREFILL_SOURCES if prefill else _DECODE_SOURCES):
+    for name in sorted(names):
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:12]
@@ -344,8 +347,9 @@ def run_lar(args, world, rank, local):
     clocks = sampler.stop(t_wall0, t_wall1)
 
     total_ms = first.elapsed_time(last)
-    # the decode kernel is the only work on `stream` in the timed region, so its
-    # average launch duration (back to back, gaps included) is the region / K
+    # this library's kernels are the only work on `stream` in the timed region, so
+    # one call's average duration (back to back, gaps included) is the region / K;
+    # a call of one launch makes that the kernel's average launch duration
     mean_launch_ms = total_ms / args.steps
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
@@ -448,9 +452,16 @@ def roofline(w, config, mean_launch_ms, achieved_gbs, peak_gbs, peak_kind):
         kname = "prefill_tc_kernel" if w.form == "kda" else "prefill_ws_kernel"
     else:
         kname = "decode_kernel"
+    kernel = f"{kname}<{w.form}>"
+    if launches_per_step(w) == 2:
+        # long spans in the chunked kernel, the rest token by token: the figures
+        # below cover the call (both launches); traffic sums the two kernels
+        chunked = "prefill_tc_kernel" if w.form == "kda" else "prefill_ws_kernel"
+        kernel = f"{chunked}<{w.form}> + decode_kernel<{w.form}>"
     base = {"traffic": measured_traffic(config), "traffic_steady": measured_traffic(config, steady=True),
-            "kernel": f"{kname}<{w.form}> ({kernel_source_hash(config)})",
-            "mean_launch_us": round(mean_launch_ms * 1e3, 3)}
+            "kernel": f"{kernel} ({kernel_source_hash(config)})",
+            "launches_per_call": launches_per_step(w),
+            "mean_launch_us" if launches_per_step(w) == 1 else "mean_call_us": round(mean_launch_ms * 1e3, 3)}
     ops = w.alu_ops()
     if w.meta.get("prefill"):
         flops = prefill_tensor_flops(w)

@@ -252,6 +252,12 @@ lar_status kda_decode_tokens(const lar_tensor* q, const lar_tensor* k, const lar
  *   pool        as for gdn_decode, [v][k] layout only (LAR_STATE_KV is rejected)
  * Flags, A_log, dt_bias and decay as for the fixed-T calls.  N <= 65535,
  * Ntok < 2^31.
+ * Without a state cache (inter NULL) and at K = V = 128, spans of 16 tokens or
+ * more are computed in the chunked form of gdn_prefill / kda_prefill /
+ * la_prefill below (equal to the recurrence up to rounding, and several times
+ * cheaper per token on such spans) and the shorter ones token by token: two
+ * kernels on `stream`, each choosing its spans on the device from cu_seqlens.
+ * With a state cache every span runs token by token.
  */
 lar_status gdn_decode_varlen(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
                              const lar_tensor* g, const lar_tensor* beta,
@@ -285,10 +291,11 @@ lar_status la_decode_varlen(const lar_tensor* q, const lar_tensor* k, const lar_
  * is produced; there is no per-token state cache (the chunked form never forms
  * the intermediate states).
  *   K = V = 128 only (other shapes: LAR_ERR_SHAPE; use *_decode_varlen).
- * Two CTAs per (sequence, v-head) pair, one per half of the value columns,
- * hold the state in shared memory for the whole span, so the work of a
- * sequence is spread over its heads; short spans are served better by the
- * *_decode_varlen calls.
+ * One CTA per (sequence, v-head) pair keeps the state on chip (registers and
+ * tensor memory) for the whole span and runs the chunk's products on the
+ * tensor cores; the work of a sequence is spread over its heads, so a span
+ * shorter than a chunk costs a whole chunk (the *_decode_varlen calls send
+ * such spans token by token).
  *
  * kda_prefill: KDA's per-key-channel decay moves into the chunk's dot
  * products: with P[t][s][c] = exp(g_{s+1}[c]) ... exp(g_t[c]) (products of the

@@ -208,7 +208,9 @@ def make_meta(name: str) -> dict:
     """Workload flags known without drawing it (which call runs it)."""
     if name not in CONFIGS:
         raise KeyError(name)
-    return {"prefill": name in ("gdn_prefill_n16", "kda_prefill_n16")}
+    # split: a variable-length call without a state cache at K = V = 128 runs its
+    # long spans in the chunked kernel and the rest in the token-by-token kernel
+    return {"prefill": name in ("gdn_prefill_n16", "kda_prefill_n16"), "split": name == "gdn_varlen_b64"}
 
 
 def make(name: str, *, seed: int | None = None, pool_device="cpu",
