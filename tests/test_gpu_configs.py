@@ -115,7 +115,13 @@ def test_full_size_varlen(cuda_device):
     assert torch.equal(w.pool[~mask], before[~mask]), "untouched pool bytes changed"
     cu = w.cu_seqlens.long()
     lengths = cu[1:] - cu[:-1]
-    sample = sorted(set(_sample(w.B)) | {int(lengths.argmax())})
+    # the longest span, the shortest one the chunked kernel takes (16 tokens or
+    # more) and the longest one left to the token-by-token kernel, beside the
+    # seeded sample
+    long_ = (lengths >= 16).nonzero().flatten()
+    short = (lengths < 16).nonzero().flatten()
+    picks = {int(lengths.argmax()), int(long_[lengths[long_].argmin()]), int(short[lengths[short].argmax()])}
+    sample = sorted(set(_sample(w.B)) | picks)
     for n in sample:
         lo, hi = int(cu[n]), int(cu[n + 1])
         sub = before[int(w.read_idx[n])].cpu()[None].clone()

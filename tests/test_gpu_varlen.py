@@ -158,3 +158,47 @@ def test_varlen_graph_replay(cuda_device):
     torch.cuda.synchronize()
     assert torch.equal(out_g, out_e)
     assert torch.equal(pool_g, pool_e)
+
+
+# Without a state cache and at K = V = 128 the spans of 16 tokens or more run in
+# the chunked tensor-core kernels and the rest token by token, in one call: these
+# cases put long and short spans side by side in every pool form, around the
+# threshold, and with fp32 rows (the general chunked kernel instead of the
+# warp-specialised one).
+SPLIT_CASES = {
+    "gdn_bf16_pool": dict(form="gdn", lengths=MIXED, H=2, HV=4, state_dtype=BF16),
+    "kda_bf16_pool": dict(form="kda", lengths=MIXED, H=2, HV=2, raw_gates=True, state_dtype=BF16),
+    "la_flat_bf16": dict(form="la", lengths=[4, 0, 21, 1, 40], H=2, flat_pool=True, state_dtype=BF16),
+    "gdn_skip_write": dict(form="gdn", lengths=MIXED, H=2, HV=4, separate_write=True, skip_frac=0.25),
+    "gdn_fp32_rows": dict(form="gdn", lengths=MIXED, H=2, HV=4, in_dtype=F32, out_dtype=F32),
+    "gdn_threshold": dict(form="gdn", lengths=[15, 16, 17, 31, 32, 33, 1], H=1, HV=2),
+    "kda_threshold": dict(form="kda", lengths=[15, 16, 17, 2], H=1, HV=2, raw_gates=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SPLIT_CASES))
+def test_varlen_split_parity(name, cuda_device):
+    kw = dict(SPLIT_CASES[name])
+    form, lengths = kw.pop("form"), kw.pop("lengths")
+    w = W.make_varlen(form, lengths, K=128, V=128, seed=71, **kw)
+    P.varlen_check(w, cuda_device)
+
+
+def test_varlen_split_bad_spans(cuda_device):
+    """A reversed span and a long one past the token arrays: the chunked kernel
+    leaves both alone, the token-by-token kernel runs them as empty and flags
+    them; the valid long and short spans are unaffected."""
+    w = W.make_varlen("gdn", [4, 20, 3, 30], H=1, HV=2, K=128, V=128, seed=72, separate_write=True)
+    cu = torch.tensor([0, 4, 24, 3, 60], dtype=torch.int32)      # [0,4) [4,24) [24,3) [3,60) of 57 tokens
+    P.varlen_check(w, cuda_device, cu_seqlens=cu, expect_err=lar.LAR_DEVERR_SEQLEN)
+
+
+def test_varlen_split_absent_and_bad_slots(cuda_device):
+    """Long spans that start from an absent slot (-1: zero state) or an
+    out-of-range one (zero state, flagged), and one whose write slot is out of
+    range (writeback skipped, flagged), beside short spans."""
+    w = W.make_varlen("gdn", [20, 33, 5, 40, 2], H=1, HV=2, K=128, V=128, seed=73, separate_write=True)
+    w.read_idx[0] = -1
+    w.read_idx[1] = w.P + 3
+    w.write_idx[3] = w.P + 1
+    P.varlen_check(w, cuda_device, expect_err=lar.LAR_DEVERR_READ_SLOT | lar.LAR_DEVERR_WRITE_SLOT)
