@@ -257,7 +257,10 @@ lar_status kda_decode_tokens(const lar_tensor* q, const lar_tensor* k, const lar
  * la_prefill below (equal to the recurrence up to rounding, and several times
  * cheaper per token on such spans) and the shorter ones token by token: two
  * kernels on `stream`, each choosing its spans on the device from cu_seqlens.
- * With a state cache every span runs token by token.
+ * The chunked kernel's grid has a row per possible long span (at most
+ * Ntok / 16 when the valid spans are disjoint) and is not launched when Ntok <
+ * 16; if any span is reversed (then valid spans may overlap) every span runs
+ * token by token.  With a state cache every span runs token by token.
  */
 lar_status gdn_decode_varlen(const lar_tensor* q, const lar_tensor* k, const lar_tensor* v,
                              const lar_tensor* g, const lar_tensor* beta,

@@ -384,21 +384,38 @@ constexpr int kVlTileCost = LAR_VL_TILE_COST;
 
 template <int NTH>
 __device__ __forceinline__ void vl_partition(const DecodeParams& p, int64_t U, int64_t total, long long* red,
-                                             int64_t& t_begin, int64_t& t_end) {
+                                             int64_t& t_begin, int64_t& t_end, long long* split_out) {
     constexpr int NWARP = NTH / 32;
+    static_assert(NWARP + 2 < 2 * kMaxTokens, "the scratch leaves the slot tables' last entry (split_out) alone");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t N = p.B;
     const int64_t seg = (N + NTH - 1) / NTH;
     const int64_t lo = min(N, tid * seg), hi = min(N, lo + seg);
-    auto weight = [&](int64_t b) -> long long {
+    auto span = [&](int64_t b, bool& rev) -> int64_t {
         const int64_t a = ld_idx(p.cu, b * p.cu_s, p.cu_dt);
         const int64_t e = ld_idx(p.cu, (b + 1) * p.cu_s, p.cu_dt);
-        const int64_t len = a >= 0 && e >= a && e <= p.ntok ? e - a : 0;
-        // spans the chunked kernel takes cost this kernel only their (empty) tiles
-        return (p.split_len > 0 && len >= p.split_len ? 0 : len) + kVlTileCost;
+        rev = e < a;
+        return a >= 0 && e >= a && e <= p.ntok ? e - a : 0;
     };
-    long long own = 0;
-    for (int64_t b = lo; b < hi; ++b) own += weight(b);
+    // spans the chunked kernel takes cost this kernel only their (empty) tiles;
+    // a split call leaves it its long spans only when no span is reversed (then
+    // the valid spans are disjoint, which the chunked kernel's grid relies on)
+    long long own_split = 0, own_all = 0;
+    bool rev_any = false, rev;
+    for (int64_t b = lo; b < hi; ++b) {
+        const int64_t len = span(b, rev);
+        rev_any |= rev;
+        own_all += len + kVlTileCost;
+        own_split += (p.split_len > 0 && len >= p.split_len ? 0 : len) + kVlTileCost;
+    }
+    const int split = p.split_len > 0 && !__syncthreads_or(rev_any) ? p.split_len : 0;
+    if (tid == 0) *split_out = split;   // visible after the barrier below
+    auto weight = [&](int64_t b) -> long long {
+        bool r;
+        const int64_t len = span(b, r);
+        return (split > 0 && len >= split ? 0 : len) + kVlTileCost;
+    };
+    const long long own = split > 0 ? own_split : own_all;
     long long incl = own;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -475,13 +492,19 @@ decode_kernel(const DecodeParams p) {
     const int nvt = (V + TV - 1) / TV;
     const int64_t total = static_cast<int64_t>(p.B) * p.HV * nvt;
     int64_t t_begin, t_end;
+    // varlen: spans of this many tokens or more are the chunked kernel's (0: none);
+    // kept in the last entry of the per-token slot tables (which only the
+    // per-token-slot instances use, and the partition's scratch does not reach)
+    // and read once per pair, so that it holds no register
+    volatile long long* vl_split_slot = slot_tab + 2 * kMaxTokens - 1;
+    auto vl_split = [&]() -> int { return VL ? static_cast<int>(*vl_split_slot) : 0; };
     if constexpr (VL) {
 #if LAR_PDL
         // the span offsets may come from the previous kernel on the stream
         asm volatile("griddepcontrol.wait;\n" ::: "memory");
         asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 #endif
-        vl_partition<NW * 32>(p, static_cast<int64_t>(p.HV) * nvt, total, slot_tab, t_begin, t_end);
+        vl_partition<NW * 32>(p, static_cast<int64_t>(p.HV) * nvt, total, slot_tab, t_begin, t_end, const_cast<long long*>(vl_split_slot));
     } else {
         t_begin = blockIdx.x * total / gridDim.x;
         t_end = (blockIdx.x + 1) * total / gridDim.x;
@@ -516,8 +539,9 @@ decode_kernel(const DecodeParams p) {
         if constexpr (VL) {
             // a span the chunked kernel takes: no state to load here
             if (p.split_len > 0) {
+                const int sl = vl_split();
                 const int64_t lo = ld_idx(p.cu, b * p.cu_s, p.cu_dt), hi = ld_idx(p.cu, (b + 1) * p.cu_s, p.cu_dt);
-                if (lo >= 0 && hi >= lo && hi <= p.ntok && hi - lo >= p.split_len) return -1;
+                if (sl > 0 && lo >= 0 && hi >= lo && hi <= p.ntok && hi - lo >= sl) return -1;
             }
         }
         if (!TOK || p.nacc == nullptr) return ld_idx(p.ridx, b * p.ri_s, p.ri_dt);
@@ -647,7 +671,7 @@ decode_kernel(const DecodeParams p) {
                 L = span_ok ? static_cast<int>(hi - lo) : 0;
                 fresh = true;
                 // a span the chunked kernel takes: nothing to compute or write here
-                if (p.split_len > 0 && L >= p.split_len) {
+                if (p.split_len > 0 && vl_split() > 0 && L >= vl_split()) {
                     L = 0;
                     wr = false;
                 }

@@ -142,8 +142,16 @@ __global__ void __launch_bounds__(PTH, (VB == 128 || FORM == FORM_KDA) ? 1 : 2) 
     const bool span_ok = lo >= 0 && hi >= lo && hi <= p.ntok;
     const int64_t tb = span_ok ? lo : 0;
     const int64_t L = span_ok ? hi - lo : 0;
-    // a variable-length call sends only its long spans here (the rest run token by token)
-    if (p.split_len > 0 && L < p.split_len) return;
+    // a variable-length call sends only its long spans here (the rest run token
+    // by token), and none when some span is reversed (the token-by-token kernel
+    // then takes them all)
+    if (p.split_len > 0) {
+        if (L < p.split_len) return;
+        bool rev = false;
+        for (int i = tid; i < p.B; i += PTH)
+            rev |= ld_idx(p.cu, (i + 1) * p.cu_s, p.cu_dt) < ld_idx(p.cu, i * p.cu_s, p.cu_dt);
+        if (__syncthreads_or(rev)) return;
+    }
     const int64_t r = ld_idx(p.ridx, n * p.ri_s, p.ri_dt);
     const int64_t w = p.widx ? ld_idx(p.widx, n * p.wi_s, p.wi_dt) : r;
     const bool rd = r >= 0 && r < p.P;

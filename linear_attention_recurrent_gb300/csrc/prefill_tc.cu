@@ -307,30 +307,11 @@ __global__ void __launch_bounds__(TTH, 1) prefill_tc_kernel(const DecodeParams p
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 #endif
-    // ---- which sequence: CTAs start in blockIdx order, so with up to kLptMax
-    // sequences row y of the grid takes the sequence of the y-th longest span
-    // (ties by index), and the grid's tail holds the short spans (on 16 spans of
-    // 256-1024 tokens the simulated makespan drops from 1.21x to 1.12x the
-    // ideal); more sequences keep their own order
-    int n = blockIdx.y;
-    if (p.B <= kLptMax) {
-        int* lens = reinterpret_cast<int*>(smem + OFF_STG);   // the staging buffer is not in use yet
-        int* pick = reinterpret_cast<int*>(smem + OFF_TM) + 1;
-        for (int i = tid; i < p.B; i += TTH) {
-            const int64_t a = ld_idx(p.cu, i * p.cu_s, p.cu_dt), e = ld_idx(p.cu, (i + 1) * p.cu_s, p.cu_dt);
-            lens[i] = a >= 0 && e >= a && e <= p.ntok ? static_cast<int>(e - a) : 0;
-        }
-        __syncthreads();
-        for (int i = tid; i < p.B; i += TTH) {
-            const int li = lens[i];
-            int rank = 0;
-            for (int m = 0; m < p.B; ++m) rank += lens[m] > li || (lens[m] == li && m < i);
-            if (rank == static_cast<int>(blockIdx.y)) *pick = i;
-        }
-        __syncthreads();
-        n = *pick;
-        __syncthreads();   // the staging buffer's first copies may now go out
-    }
+    // ---- which sequence: longest spans first; in a split variable-length call
+    // only the long ones (pick_sequence); the staging buffer is not in use yet
+    const int n = pick_sequence<TTH>(p, reinterpret_cast<int*>(smem + OFF_STG),
+                                      reinterpret_cast<int*>(smem + OFF_TM) + 1);
+    if (n < 0) return;
     // ---- span and slots (reversed or overlong spans run as empty and are flagged)
     const int64_t lo = ld_idx(p.cu, n * p.cu_s, p.cu_dt);
     const int64_t hi = ld_idx(p.cu, (n + 1) * p.cu_s, p.cu_dt);

@@ -235,27 +235,11 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 #endif
-    // ---- which sequence: row y of the grid takes the y-th longest span (as in
-    // prefill_tc_kernel)
-    int n = blockIdx.y;
-    if (p.B <= kLptMax) {
-        int* lens = reinterpret_cast<int*>(smem + ws::OFF_V);   // the v ring is not in use yet
-        int* pick = reinterpret_cast<int*>(smem + ws::OFF_TM) + 1;
-        for (int i = tid; i < p.B; i += ws::NT) {
-            const int64_t a = ld_idx(p.cu, i * p.cu_s, p.cu_dt), e = ld_idx(p.cu, (i + 1) * p.cu_s, p.cu_dt);
-            lens[i] = a >= 0 && e >= a && e <= p.ntok ? static_cast<int>(e - a) : 0;
-        }
-        __syncthreads();
-        for (int i = tid; i < p.B; i += ws::NT) {
-            const int li = lens[i];
-            int rank = 0;
-            for (int m = 0; m < p.B; ++m) rank += lens[m] > li || (lens[m] == li && m < i);
-            if (rank == static_cast<int>(blockIdx.y)) *pick = i;
-        }
-        __syncthreads();
-        n = *pick;
-        __syncthreads();   // the v ring's first copies may now go out
-    }
+    // ---- which sequence: longest spans first; in a split variable-length call
+    // only the long ones (pick_sequence); the v ring is not in use yet
+    const int n = pick_sequence<ws::NT>(p, reinterpret_cast<int*>(smem + ws::OFF_V),
+                                      reinterpret_cast<int*>(smem + ws::OFF_TM) + 1);
+    if (n < 0) return;
     // ---- span and slots (reversed or overlong spans run as empty and are flagged)
     const int64_t lo = ld_idx(p.cu, n * p.cu_s, p.cu_dt);
     const int64_t hi = ld_idx(p.cu, (n + 1) * p.cu_s, p.cu_dt);

@@ -173,6 +173,14 @@ SPLIT_CASES = {
     "gdn_fp32_rows": dict(form="gdn", lengths=MIXED, H=2, HV=4, in_dtype=F32, out_dtype=F32),
     "gdn_threshold": dict(form="gdn", lengths=[15, 16, 17, 31, 32, 33, 1], H=1, HV=2),
     "kda_threshold": dict(form="kda", lengths=[15, 16, 17, 2], H=1, HV=2, raw_gates=True),
+    # fewer tokens than one long span: the chunked kernel is not launched
+    "gdn_no_long_span": dict(form="gdn", lengths=[3, 5, 2], H=1, HV=2),
+    # more sequences than the chunked kernels rank by length: the long spans are
+    # found in index order, and the grid has fewer rows than sequences
+    "gdn_many_sequences": dict(form="gdn", lengths=[1, 2, 0, 3] * 70 + [16, 1, 33, 2, 20, 70, 1, 17],
+                               H=1, HV=2, separate_write=True, skip_frac=0.1),
+    "kda_many_sequences": dict(form="kda", lengths=[2, 1] * 140 + [18, 40, 1, 16], H=1, HV=1,
+                               raw_gates=True),
 }
 
 
@@ -190,6 +198,25 @@ def test_varlen_split_bad_spans(cuda_device):
     them; the valid long and short spans are unaffected."""
     w = W.make_varlen("gdn", [4, 20, 3, 30], H=1, HV=2, K=128, V=128, seed=72, separate_write=True)
     cu = torch.tensor([0, 4, 24, 3, 60], dtype=torch.int32)      # [0,4) [4,24) [24,3) [3,60) of 57 tokens
+    P.varlen_check(w, cuda_device, cu_seqlens=cu, expect_err=lar.LAR_DEVERR_SEQLEN)
+
+
+def test_varlen_split_overlong_span(cuda_device):
+    """A long span past the token arrays (bad, flagged) with no span reversed:
+    the split stays on and the valid long span runs in the chunked kernel."""
+    w = W.make_varlen("gdn", [4, 20, 3, 30], H=1, HV=2, K=128, V=128, seed=74, separate_write=True)
+    cu = torch.tensor([0, 4, 24, 24, 60], dtype=torch.int32)     # [0,4) [4,24) [24,24) [24,60) of 57 tokens
+    P.varlen_check(w, cuda_device, cu_seqlens=cu, expect_err=lar.LAR_DEVERR_SEQLEN)
+
+
+def test_varlen_split_many_sequences_reversed(cuda_device):
+    """More sequences than the chunked kernels rank, one span reversed: every
+    span runs token by token (a reversed span lets valid spans overlap, so the
+    chunked kernel's grid bound would not hold)."""
+    lengths = [1, 2] * 150 + [20, 3, 17]
+    w = W.make_varlen("gdn", lengths, H=1, HV=2, K=128, V=128, seed=75, separate_write=True)
+    cu = w.cu_seqlens.clone()
+    cu[5] = int(cu[-1]) + 5                 # span 4 past the tokens, span 5 reversed; no two valid spans overlap
     P.varlen_check(w, cuda_device, cu_seqlens=cu, expect_err=lar.LAR_DEVERR_SEQLEN)
 
 
