@@ -2,6 +2,8 @@
 // unit inner stride, 16-byte aligned: the usual layouts) as a warp-specialised
 // tensor-core kernel.  Same operation and chunk algebra as prefill_tc.cu, whose
 // header states it; other forms and layouts run there.
+#include <type_traits>
+
 #include <cuda.h>   // CUtensorMap and its encoder's signature (called through the runtime's driver entry point)
 
 #include "prefill_common.cuh"
@@ -82,7 +84,11 @@ enum {
     NBAR = 13
 };
 constexpr uint32_t OFF_TM = OFF_BAR + NBAR * 8;               // TMEM base, picked sequence, abort flag
-constexpr uint32_t SMEM = OFF_TM + 16;
+// the solve's hand-over: d_0..15 of each value row (rows padded to 20 floats, so
+// a quarter-warp's 16-byte accesses fall in distinct banks)
+constexpr int XROW = 20;
+constexpr uint32_t OFF_X = (OFF_TM + 16 + 15) / 16 * 16;
+constexpr uint32_t SMEM = OFF_X + TVV * XROW * 4;
 // tensor-memory columns: the state's three bf16 planes (64 columns each; D o W's
 // three planes of 16 reuse them once [U | P] has read the state), D's tf32
 // halves for O, [U | P], K K^T, O's accumulator, the increment
@@ -179,6 +185,43 @@ __device__ __forceinline__ void split3_store(uint32_t taddr, uint32_t stride, co
         tc::tmem_st16(taddr + stride + i0 / 2, w2);
         tc::tmem_st16(taddr + 2 * stride + i0 / 2, w3);
     }
+}
+
+// The right-looking elimination of d_t for t in [TLO, THI) by every d_s, s < t
+// (s < THI - 1): once d_s is final it is taken out of each later row, one
+// dependent multiply-add per step.  AT[s][t] is the coefficient of d_s in row t.
+template <int TLO, int THI>
+__device__ __forceinline__ void eliminate(float* d, const float* AT) {
+#pragma unroll
+    for (int s = 0; s < THI - 1; ++s) {
+#pragma unroll
+        for (int t4 = ((s + 1) & ~3) > TLO ? ((s + 1) & ~3) : TLO; t4 < THI; t4 += 4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(AT + s * TROW + t4);
+            if (t4 > s) d[t4] = fmaf(-a4.x, d[s], d[t4]);
+            if (t4 + 1 > s) d[t4 + 1] = fmaf(-a4.y, d[s], d[t4 + 1]);
+            if (t4 + 2 > s) d[t4 + 2] = fmaf(-a4.z, d[s], d[t4 + 2]);
+            d[t4 + 3] = fmaf(-a4.w, d[s], d[t4 + 3]);
+        }
+    }
+}
+
+// 16 values into tensor memory as three bf16 planes of 8 columns (as split3_store)
+__device__ __forceinline__ void split3_store16(uint32_t taddr, uint32_t stride, const float* x) {
+    float w1[8], w2[8], w3[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float a = x[2 * j], b = x[2 * j + 1];
+        const uint32_t p1 = pack_bf16x2(a, b);
+        const float ra = a - bf16_lo(p1), rb = b - bf16_hi(p1);
+        const uint32_t p2 = pack_bf16x2(ra, rb);
+        const uint32_t p3 = pack_bf16x2(ra - bf16_lo(p2), rb - bf16_hi(p2));
+        w1[j] = __uint_as_float(p1);
+        w2[j] = __uint_as_float(p2);
+        w3[j] = __uint_as_float(p3);
+    }
+    tc::tmem_st8(taddr, w1);
+    tc::tmem_st8(taddr + stride, w2);
+    tc::tmem_st8(taddr + 2 * stride, w3);
 }
 
 // One value row's outputs of a chunk: the Lo finished accumulator columns at
@@ -375,62 +418,86 @@ __global__ void __launch_bounds__(ws::NT, 1) prefill_ws_kernel(const __grid_cons
             // (E_31 is taken now)
             const float ec = reinterpret_cast<const float*>(smem + ws::OFF_E31)[4 * b];
 
-            if (half == 0) {
-                // ---- the solve per value row, right-looking: once d_s is final it is
-                // taken out of every later row (one dependent FMA per step).  v_t: the
-                // staged row (the side warps reported the chunk ready).
+            {
+                // ---- the solve per value row, right-looking (once d_s is final it is
+                // taken out of every later row, one dependent FMA per step), split by
+                // tokens between the chain's halves: half 0 finishes d_0..15 and hands
+                // them over through shared memory, half 1 takes them out of d_16..31 and
+                // finishes those (the operations and their order those of one thread
+                // doing all 32).  Each half then stores its own tokens' D, and half 0
+                // starts O's accumulator.  v_t: the staged row (the side warps reported
+                // the chunk ready).
                 const unsigned short* sv =
                     reinterpret_cast<const unsigned short*>(smem + ws::OFF_V + (c % ws::NVB) * TC * STG_ROW) + vrow;
                 auto vin = [&](int t) -> float { return t < Lc ? bf16_bits_to_float(sv[t * TVV]) : 0.f; };
-                float d[TC];
-                if constexpr (LA) {
-#pragma unroll
-                    for (int t = 0; t < TC; ++t) d[t] = vin(t);
-                } else {
-                    // d_t starts as beta_t (v_t - E_t u_t / |k_t|), u from [U | P]
-#pragma unroll
-                    for (int t0 = 0; t0 < TC; t0 += 16) {
+                float* xr = reinterpret_cast<float*>(smem + ws::OFF_X) + vrow * ws::XROW;
+                auto solve = [&](auto half_c) {
+                    constexpr int T0 = decltype(half_c)::value * 16;
+                    float d[TC];
+                    {
+                        // d_t starts as beta_t (v_t - E_t u_t / |k_t|) (LA: v_t), u from [U | P]
                         float u[16], vv[16];
-                        tc::tmem_ld16(my + COL_UP + t0, u);
+                        if constexpr (!LA) tc::tmem_ld16(my + COL_UP + T0, u);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) vv[i] = vin(t0 + i);
-                        tc::tmem_ld_wait();
+                        for (int i = 0; i < 16; ++i) vv[i] = vin(T0 + i);
+                        if constexpr (LA) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) d[t0 + i] = Bt[t0 + i] * fmaf(-EK[t0 + i], u[i], vv[i]);
-                    }
+                            for (int i = 0; i < 16; ++i) d[T0 + i] = vv[i];
+                        } else {
+                            tc::tmem_ld_wait();
 #pragma unroll
-                    for (int s = 0; s < TC - 1; ++s) {
-#pragma unroll
-                        for (int t4 = (s + 1) & ~3; t4 < TC; t4 += 4) {
-                            const float4 a4 = *reinterpret_cast<const float4*>(AT + s * TROW + t4);
-                            if (t4 > s) d[t4] = fmaf(-a4.x, d[s], d[t4]);
-                            if (t4 + 1 > s) d[t4 + 1] = fmaf(-a4.y, d[s], d[t4 + 1]);
-                            if (t4 + 2 > s) d[t4 + 2] = fmaf(-a4.z, d[s], d[t4 + 2]);
-                            d[t4 + 3] = fmaf(-a4.w, d[s], d[t4 + 3]);
+                            for (int i = 0; i < 16; ++i) d[T0 + i] = Bt[T0 + i] * fmaf(-EK[T0 + i], u[i], vv[i]);
                         }
                     }
-                }
-                // D's tf32 halves for O (once the previous chunk's O has read its D) and
-                // D o W / |k| as three bf16 planes for the increment
-                if (c > 0 && !tc::mbar_wait_or(&bar[ws::O_DONE + (cp & 1)], static_cast<uint32_t>((cp >> 1) & 1), abort_f))
-                    *abort_f = 1;
-                tc::fence_after_sync();
-                split_store<TC>(my + ws::COL_DH, my + ws::COL_DL, d);
+                    if constexpr (!LA && T0 == 0) {
+                        ws::eliminate<0, 16>(d, AT);
 #pragma unroll
-                for (int t = 0; t < TC; ++t) d[t] *= WK[t];
-                ws::split3_store<TC>(my + ws::COL_DWP, ws::DWP_STRIDE, d);
-                tc::tmem_st_wait();
-            } else {
-                // ---- O's accumulator starts as E_t P[v][t] / |q_t|
-                float pv[TC];
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4*>(xr + i) = make_float4(d[i], d[i + 1], d[i + 2], d[i + 3]);
+                    }
+                    // the hand-over; also orders half 1's reads of O's accumulator (the
+                    // previous chunk's outputs) before half 0 restarts it
+                    tc::fence_before_sync();
+                    tc::bar_sync(1, ws::NCHAIN);
+                    tc::fence_after_sync();
+                    if constexpr (!LA && T0 == 16) {
 #pragma unroll
-                for (int i = 0; i < TC; i += 16) tc::tmem_ld16(my + COL_UP + TC + i, pv + i);
-                tc::tmem_ld_wait();
+                        for (int i = 0; i < 16; i += 4) {
+                            const float4 x = *reinterpret_cast<const float4*>(xr + i);
+                            d[i] = x.x;
+                            d[i + 1] = x.y;
+                            d[i + 2] = x.z;
+                            d[i + 3] = x.w;
+                        }
+                        ws::eliminate<16, 32>(d, AT);
+                    }
+                    // D's tf32 halves for O (once the previous chunk's O has read its D) and
+                    // D o W / |k| as three bf16 planes for the increment
+                    if (c > 0 &&
+                        !tc::mbar_wait_or(&bar[ws::O_DONE + (cp & 1)], static_cast<uint32_t>((cp >> 1) & 1), abort_f))
+                        *abort_f = 1;
+                    tc::fence_after_sync();
+                    split_store<16>(my + ws::COL_DH + T0, my + ws::COL_DL + T0, d + T0);
 #pragma unroll
-                for (int t = 0; t < TC; ++t) pv[t] *= EQ[t];
+                    for (int i = 0; i < 16; ++i) d[T0 + i] *= WK[T0 + i];
+                    ws::split3_store16(my + ws::COL_DWP + T0 / 2, ws::DWP_STRIDE, d + T0);
+                    if constexpr (T0 == 0) {
+                        // ---- O's accumulator starts as E_t P[v][t] / |q_t|
+                        float pv[TC];
 #pragma unroll
-                for (int i = 0; i < TC; i += 16) tc::tmem_st16(my + ws::COL_O2 + i, pv + i);
-                tc::tmem_st_wait();
+                        for (int i = 0; i < TC; i += 16) tc::tmem_ld16(my + COL_UP + TC + i, pv + i);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int t = 0; t < TC; ++t) pv[t] *= EQ[t];
+#pragma unroll
+                        for (int i = 0; i < TC; i += 16) tc::tmem_st16(my + ws::COL_O2 + i, pv + i);
+                    }
+                    tc::tmem_st_wait();
+                };
+                if (half == 0)
+                    solve(std::integral_constant<int, 0>{});
+                else
+                    solve(std::integral_constant<int, 1>{});
             }
             tc::fence_before_sync();
             tc::bar_sync(1, ws::NCHAIN);
