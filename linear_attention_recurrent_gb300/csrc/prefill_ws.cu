@@ -190,18 +190,37 @@ __device__ __forceinline__ void split3_store(uint32_t taddr, uint32_t stride, co
 // The right-looking elimination of d_t for t in [TLO, THI) by every d_s, s < t
 // (s < THI - 1): once d_s is final it is taken out of each later row, one
 // dependent multiply-add per step.  AT[s][t] is the coefficient of d_s in row t.
+// First group of four t's that step s updates.
+__host__ __device__ constexpr int elim_first(int s, int tlo) { return ((s + 1) & ~3) > tlo ? ((s + 1) & ~3) : tlo; }
+
 template <int TLO, int THI>
 __device__ __forceinline__ void eliminate(float* d, const float* AT) {
+    // each step's row of A is loaded while the step before it runs: the steps
+    // wait on one multiply-add of the previous step, not on shared memory
+    constexpr int NG = (THI - TLO) / 4;
+    float4 a[NG], an[NG];
+#pragma unroll
+    for (int g = 0; g < NG; ++g)
+        if (TLO + 4 * g >= elim_first(0, TLO)) a[g] = *reinterpret_cast<const float4*>(AT + TLO + 4 * g);
 #pragma unroll
     for (int s = 0; s < THI - 1; ++s) {
+        if (s + 1 < THI - 1) {
 #pragma unroll
-        for (int t4 = ((s + 1) & ~3) > TLO ? ((s + 1) & ~3) : TLO; t4 < THI; t4 += 4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(AT + s * TROW + t4);
-            if (t4 > s) d[t4] = fmaf(-a4.x, d[s], d[t4]);
-            if (t4 + 1 > s) d[t4 + 1] = fmaf(-a4.y, d[s], d[t4 + 1]);
-            if (t4 + 2 > s) d[t4 + 2] = fmaf(-a4.z, d[s], d[t4 + 2]);
-            d[t4 + 3] = fmaf(-a4.w, d[s], d[t4 + 3]);
+            for (int g = 0; g < NG; ++g)
+                if (TLO + 4 * g >= elim_first(s + 1, TLO))
+                    an[g] = *reinterpret_cast<const float4*>(AT + (s + 1) * TROW + TLO + 4 * g);
         }
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            const int t4 = TLO + 4 * g;
+            if (t4 < elim_first(s, TLO)) continue;
+            if (t4 > s) d[t4] = fmaf(-a[g].x, d[s], d[t4]);
+            if (t4 + 1 > s) d[t4 + 1] = fmaf(-a[g].y, d[s], d[t4 + 1]);
+            if (t4 + 2 > s) d[t4 + 2] = fmaf(-a[g].z, d[s], d[t4 + 2]);
+            d[t4 + 3] = fmaf(-a[g].w, d[s], d[t4 + 3]);
+        }
+#pragma unroll
+        for (int g = 0; g < NG; ++g) a[g] = an[g];
     }
 }
 
