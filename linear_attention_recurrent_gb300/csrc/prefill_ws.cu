@@ -45,8 +45,9 @@ using namespace pf;
 // O_DONE(c) are in, so it can run up to two chunks ahead.  O(c) enters the
 // tensor pipe right behind the increment and runs while the chain updates the
 // state; its accumulator (columns 352..383) starts from E_t P[v][t] / |q_t|,
-// written by the chain's second half while the first half solves, and its
-// outputs are stored early in the next chunk, while [U | P] runs.  A wait that
+// written by the chain's first half once it has handed its half of the solve
+// over (the second half finishes the solve meanwhile), and its outputs are
+// stored by the second half early in the next chunk, while [U | P] runs.  A wait that
 // gives up sets a shared abort flag; the waits of the other group see it and
 // give up too, both groups leave their loops, and the CTA skips its writeback.
 namespace ws {
