@@ -408,9 +408,10 @@ PREFILL_CHUNK = 32
 def launches_per_step(w) -> int:
     """Kernels of this library launched per call: a variable-length call
     without a state cache at K = V = 128 launches the chunked kernel for its
-    long spans and the token-by-token kernel for the rest."""
+    long spans (when its token arrays can hold a span of 16 tokens) and the
+    token-by-token kernel for the rest."""
     if w.cu_seqlens is not None and not w.meta.get("prefill") and not w.cache_intermediate and w.K == 128 \
-            and w.V == 128:
+            and w.V == 128 and min(w.B, w.q.shape[0] // 16) > 0:
         return 2
     return 1
 
