@@ -126,3 +126,21 @@ def test_kernel_hash_ignores_comments_and_separates_kernels():
     assert '"// kept"' in bench._code_only(a)
     assert bench.kernel_source_hash("gdn_b64") == bench.kernel_source_hash("kda_b256")
     assert bench.kernel_source_hash("gdn_b64") != bench.kernel_source_hash("gdn_prefill_n16")
+    # a split variable-length call runs both kernels: its hash covers both sets of sources
+    split = bench.kernel_source_hash("gdn_varlen_b64")
+    assert split not in (bench.kernel_source_hash("gdn_b64"), bench.kernel_source_hash("gdn_prefill_n16"))
+
+
+def test_launches_per_call():
+    """gpu_launches counts both kernels of a split variable-length call, and one
+    when no span can reach the chunked kernel's 16 tokens (it is not launched)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    assert bench.launches_per_step(W.make("gdn_b64")) == 1
+    assert bench.launches_per_step(W.make("gdn_prefill_n16")) == 1
+    assert bench.launches_per_step(W.make("gdn_varlen_b64")) == 2
+    assert bench.launches_per_step(W.make_varlen("gdn", [1] * 15, H=1, HV=2)) == 1
+    assert bench.launches_per_step(W.make_varlen("gdn", [1] * 16, H=1, HV=2)) == 2
+    assert bench.launches_per_step(W.make_varlen("gdn", [20], H=1, HV=2, K=64, V=64)) == 1
+    assert bench.launches_per_step(W.make_varlen("gdn", [20], H=1, HV=2, cache_intermediate=True)) == 1
